@@ -1,0 +1,285 @@
+/*
+ * w4a16.h — C ABI of the GB300 (sm_103a) W4A16 group-32 decode library.
+ *
+ * Format (page "Gemma 4 on a 4 GB GPU in Plain PyTorch", sections "Step 1 —
+ * Load Google's QAT Weights Without Unpacking Them" and "Step 3 — Multiply
+ * Straight From the Packed Weights"): a weight matrix W of N rows by K columns
+ * is stored as 4-bit codes in groups of 32 along K, with one 16-bit step per
+ * group, and W[n][k] = (code[n][k] - 8) * step[n][k / 32].  Activations and
+ * outputs are 16-bit.  Concretely, in this library:
+ *
+ *   qw  uint32 [N][K/8]  row-major; element k of row n is the 4-bit field at
+ *                        bits 4*(k%8) .. 4*(k%8)+3 of word k/8 (low nibble
+ *                        first);
+ *   st  bf16   [N][K/32] row-major steps;
+ *   x   bf16   [M][K]    row-major activations;
+ *   y   bf16   [M][N]    row-major results, y[m][n] = sum_k W[n][k] * x[m][k]
+ *                        accumulated in fp32 and rounded to nearest-even once.
+ *
+ * Conventions shared by every call:
+ *   - All array pointers are DEVICE pointers owned by the caller.  Calls only
+ *     enqueue work on `stream` (a cudaStream_t; 0 = legacy default stream) and
+ *     return; they never synchronise and never allocate device memory.
+ *   - Argument errors that the host can see (null pointers, sizes, alignment)
+ *     return a w4_status != W4_OK BEFORE any launch, and no output is touched.
+ *   - Errors that only the device can see (an id out of range, a wait that
+ *     timed out) are written into *status_dev, a caller-owned device int32
+ *     that the caller zeroes beforehand and reads after synchronising; the
+ *     first error recorded stays.  The output rows concerned are left
+ *     UNWRITTEN, so a caller that pre-fills its output can tell a failed row
+ *     from a result (page "Fixing Gemma 4's oversized KV cache", section "A
+ *     failed decode must not look uncertain": an untouched zero row passed
+ *     for a valid answer).  status_dev may be NULL; then such errors are
+ *     visible only through the unwritten rows.
+ *   - W4_FLAG_PDL launches the kernel as a programmatic dependent of the
+ *     previous kernel in the stream: its weight loads may start before that
+ *     kernel has finished, and it waits for it before reading activations or
+ *     ids and before writing any output.  Use it only when nothing still
+ *     running earlier in the stream writes qw / st.
+ *   - Results are deterministic: the same inputs give the same bits on every
+ *     call, and the arithmetic of an output row depends only on K, that row's
+ *     codes and steps and its activation row (not on N, M, the row index, the
+ *     number of ids or the addresses), so w4a16_gemv_id row i is bitwise
+ *     equal to w4a16_gemv on expert ids[i] with the same activation row.
+ */
+#ifndef W4A16_H
+#define W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* Identical to cudaStream_t. */
+typedef struct CUstream_st *w4_stream_t;
+
+typedef enum w4_status {
+    W4_OK = 0,
+    W4_ERR_ARG = 1,        /* null pointer, size < 1, unknown flag bit */
+    W4_ERR_ALIGN = 2,      /* pointer or stride breaks its alignment rule */
+    W4_ERR_SHAPE = 3,      /* K not a multiple of 32 or above the maximum, M or
+                              x_rows outside the supported range */
+    W4_ERR_WORKSPACE = 4,  /* workspace smaller than w4a16_gemv_workspace_bytes */
+    W4_ERR_LAUNCH = 5,     /* the CUDA launch failed */
+    W4_ERR_INDEX = 6,      /* device-side: an id outside [0, count) */
+    W4_ERR_VALUE = 7,      /* device-side: a code outside 0..15 (w4_pack) */
+    W4_ERR_TIMEOUT = 8,    /* device-side: a bounded wait in a kernel expired */
+    W4_ERR_DEVICE = 9,     /* no usable CUDA device / attribute query failed */
+    W4_ERR_STATE = 10      /* slot pool: request cannot be served, or a pool
+                              copy failed (the pool forgot the experts it was
+                              loading) */
+} w4_status;
+
+#define W4_FLAG_PDL 1u
+
+#define W4_GROUP 32        /* codes per group along K */
+#define W4_MAX_K 65536     /* largest supported K */
+#define W4_MAX_M 32        /* largest batch of activation rows per call */
+#define W4_ABI_VERSION 1
+
+/* Human-readable name of a status code (static string). */
+const char *w4_status_str(int status);
+
+/* W4_ABI_VERSION of the loaded library. */
+int w4_abi_version(void);
+
+/*
+ * w4a16_gemv — dense W4A16 matrix-vector (or small-batch matrix) product.
+ *
+ * Page "Gemma 4 on a 4 GB GPU in Plain PyTorch", section "Step 3 — Multiply
+ * Straight From the Packed Weights": decoding a token multiplies one vector by
+ * every weight matrix, straight from the packed 4-bit words.
+ *
+ *   y[m][n] = bf16( sum_{k<K} (code[n][k] - 8) * st[n][k/32] * x[m][k] )
+ *
+ * y          bf16 [M][N], written once per element (2-byte aligned).
+ * qw         uint32 [N][K/8], 16-byte aligned.
+ * st         bf16 [N][K/32], 16-byte aligned.
+ * x          bf16 [M][K], 16-byte aligned.
+ * M          1 .. W4_MAX_M activation rows.
+ * N          >= 1 output rows.
+ * K          multiple of 32, 32 .. W4_MAX_K.
+ * workspace  device scratch of at least w4a16_gemv_workspace_bytes(M, N, K)
+ *            bytes (16-byte aligned), or NULL when that is 0.  It must be
+ *            zero-filled before its first use; every call that completes
+ *            without a device-side error leaves it zero-filled again.  Calls
+ *            that may run concurrently need separate workspaces.
+ * status_dev device int32 for device-side errors (W4_ERR_TIMEOUT), or NULL.
+ * flags      0 or W4_FLAG_PDL.
+ * Returns W4_OK once the work is enqueued.
+ */
+w4_status w4a16_gemv(void *y, const void *qw, const void *st, const void *x,
+                     int M, int N, int K, void *workspace, size_t workspace_bytes,
+                     int32_t *status_dev, unsigned flags, w4_stream_t stream);
+
+/* Scratch bytes w4a16_gemv needs for this shape (0 when its plan needs none). */
+size_t w4a16_gemv_workspace_bytes(int M, int N, int K);
+
+/*
+ * w4a16_gemv_id — routed-expert GEMV through an expert (or slot) index.
+ *
+ * Page "Running a 26B MoE on an 8 GB Jetson by streaming experts from SSD",
+ * section "Streaming without touching a single GPU kernel": the expert matmul
+ * takes the expert weight tensor and a small tensor of selected ids and reads
+ * expert `id` at base + id * stride, so pointing base at a pool of slots and
+ * passing slot ids gives exactly the bytes, and the results, of the full
+ * expert tensor.
+ *
+ *   e = ids[i];  W_e at qw_base + e*qw_stride_bytes, st_base + e*st_stride_bytes
+ *   y[i][n] = bf16( sum_k W_e[n][k] * x[x_rows == 1 ? 0 : i][k] )
+ *
+ * y              bf16 [n_ids][N].
+ * qw_base        uint32 [num_experts] x [N][K/8] at a stride of qw_stride_bytes
+ *                (16-byte aligned base, stride a multiple of 16 and at least
+ *                N*K/2).
+ * st_base        bf16 steps, same rules with st_stride_bytes >= N*K/16.
+ * num_experts    number of experts (or slots) behind base; ids[i] must lie
+ *                in [0, num_experts).  An id outside it leaves y[i] unwritten
+ *                and records W4_ERR_INDEX in *status_dev.
+ * ids            device int32 [n_ids]; repeats are allowed.
+ * n_ids          >= 1.
+ * x              bf16 [x_rows][K], 16-byte aligned; x_rows is 1 (one row
+ *                shared by every id) or n_ids (row i goes with ids[i]).
+ * N, K           as for w4a16_gemv.
+ */
+w4_status w4a16_gemv_id(void *y, const void *qw_base, size_t qw_stride_bytes,
+                        const void *st_base, size_t st_stride_bytes, int num_experts,
+                        const int32_t *ids, int n_ids, const void *x, int x_rows,
+                        int N, int K, int32_t *status_dev, unsigned flags,
+                        w4_stream_t stream);
+
+/*
+ * w4_embed_gather — dequantised rows of a 4-bit vocabulary table.
+ *
+ * Page "Gemma 4 on a 4 GB GPU in Plain PyTorch", section "Step 2 — Keep the
+ * Vocabulary Tables in 4-Bit": embed_tokens (which is also the output layer)
+ * and the per-layer input table stay in 4-bit with a 16-bit step per group,
+ * and the lookup by token id runs on the GPU; one copy of the tied table
+ * serves the lookup and the output GEMV (pass the same qw/st to w4a16_gemv).
+ *
+ *   out[t][k] = bf16( (code[ids[t]][k] - 8) * st[ids[t]][k/32] )   (exact
+ *   product, one rounding)
+ *
+ * out        bf16 [T][K], 16-byte aligned.
+ * qw, st     the table, layout as for w4a16_gemv with N = V rows, 16-byte
+ *            aligned.
+ * ids        device int32 [T]; an id outside [0, V) leaves out[t] unwritten
+ *            and records W4_ERR_INDEX.
+ * T, V       >= 1.  K as for w4a16_gemv.
+ */
+w4_status w4_embed_gather(void *out, const void *qw, const void *st, const int32_t *ids,
+                          int T, int V, int K, int32_t *status_dev, unsigned flags,
+                          w4_stream_t stream);
+
+/*
+ * w4_pack — pack 4-bit codes into the qw layout.
+ *
+ * codes      device uint8 [N][K], values 0..15.  A larger value records
+ *            W4_ERR_VALUE and leaves that word of qw unwritten.
+ * qw         device uint32 [N][K/8], 16-byte aligned.
+ * K          multiple of 32.
+ */
+w4_status w4_pack(void *qw, const uint8_t *codes, int N, int K, int32_t *status_dev,
+                  w4_stream_t stream);
+
+/*
+ * w4_quantize — quantise fp32 weights into (qw, st).
+ *
+ * Page "Gemma 4 on a 4 GB GPU in Plain PyTorch", section "Step 2 — Keep the
+ * Vocabulary Tables in 4-Bit" says only that each group's step is recovered
+ * from its 4-bit grid.  This helper uses the plain signed-absmax rule, per
+ * group of 32 along K:
+ *   m    = element of largest |w| (the first in K order on ties)
+ *   step = bf16(m / -8)                     (nearest even)
+ *   code = 8 if step == 0, else clamp(rint(w / step) + 8, 0, 15)
+ *          with IEEE fp32 division and rint rounding half to even,
+ * so the element m becomes code 0 and dequantises back to m.
+ *
+ * w          device fp32 [N][K], finite values, 16-byte aligned.
+ * qw, st     outputs as for w4a16_gemv, 16-byte aligned.
+ */
+w4_status w4_quantize(void *qw, void *st, const float *w, int N, int K, w4_stream_t stream);
+
+/*
+ * Expert slot pool (host side of the routed-expert path).
+ *
+ * Page "Running a 26B MoE on an 8 GB Jetson by streaming experts from SSD",
+ * section "Streaming without touching a single GPU kernel": each MoE layer
+ * keeps a persistent pool of expert-sized slots and a small slot-id tensor;
+ * for every token an LFU cache finds which requested experts are resident,
+ * loads the misses into their assigned slots, and writes the slot indices for
+ * the expert matmul.  Policy (the page leaves the details open): every
+ * request counts as one use; misses take the lowest free slot, else evict the
+ * resident expert not requested now with the fewest uses, then the least
+ * recently used, then the lowest slot index; misses are placed in request
+ * order; a repeated id shares one slot.
+ *
+ * Only the expert matmul may see slot ids; anything else indexed by expert
+ * (per-expert scales, biases, adapters) must keep the real ids.
+ */
+typedef struct w4_slot_pool w4_slot_pool;
+
+/* Create a pool for num_experts experts and num_slots slots (host memory). */
+w4_status w4_slot_pool_create(w4_slot_pool **pool, int num_experts, int num_slots);
+void w4_slot_pool_destroy(w4_slot_pool *pool);
+
+/*
+ * Host-only remap of one request of k expert ids (host int32 [k]).
+ * Writes slot_ids (host int32 [k]) and the misses as parallel arrays
+ * miss_experts / miss_slots (host int32 [k] each, *n_miss entries).
+ * Returns W4_ERR_INDEX for an id outside [0, num_experts) and W4_ERR_STATE
+ * when k names more distinct experts than there are slots; the pool is then
+ * unchanged.
+ */
+w4_status w4_slot_pool_remap(w4_slot_pool *pool, const int32_t *expert_ids, int k,
+                             int32_t *slot_ids, int32_t *miss_experts, int32_t *miss_slots,
+                             int *n_miss);
+
+/*
+ * Remap one request and stage it on `stream`: one cudaMemcpyAsync per missed
+ * expert for its codes (qw_expert_bytes from full_qw + e*qw_stride to
+ * pool_qw + s*qw_stride) and one for its steps (likewise with st_*), then a
+ * tiny kernel that writes the k slot ids into slot_ids_dev (device int32
+ * [k], k <= 64).  If any copy fails to enqueue, the experts of this request
+ * that were being loaded are dropped from the pool (their slots become free)
+ * and W4_ERR_STATE is returned, so stale slot contents are never used.
+ * slot_ids / n_miss (host, optional, may be NULL) receive the remap.
+ */
+w4_status w4_slot_pool_stage(w4_slot_pool *pool, const int32_t *expert_ids, int k,
+                             void *pool_qw, const void *full_qw, size_t qw_stride_bytes,
+                             size_t qw_expert_bytes, void *pool_st, const void *full_st,
+                             size_t st_stride_bytes, size_t st_expert_bytes,
+                             int32_t *slot_ids_dev, int32_t *slot_ids, int *n_miss,
+                             w4_stream_t stream);
+
+/* Counters since creation: requests served (ids), hits, misses (copies). */
+void w4_slot_pool_stats(const w4_slot_pool *pool, long long *requests, long long *hits,
+                        long long *misses);
+
+/*
+ * Launch plan chosen for a w4a16_gemv shape (for tests and benchmarks).
+ * Returns W4_OK and fills *info, or an argument error for an invalid shape.
+ */
+typedef struct w4_plan_info {
+    int path;           /* 0 = CUDA-core packed-fp16 kernel */
+    int ctas;           /* CTAs launched */
+    int slices;         /* K slices (split-K); 1 = none */
+    int threads;        /* threads per CTA */
+    int team;           /* lanes that share one output row */
+    int tile_rows;      /* rows per pipeline stage */
+    int tile_groups;    /* 32-code groups per row per stage */
+    int stages;         /* pipeline depth */
+    int smem_bytes;     /* dynamic shared memory per CTA */
+    int rows_per_call;  /* activation rows handled per launch */
+} w4_plan_info;
+
+w4_status w4a16_gemv_plan(int M, int N, int K, w4_plan_info *info);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H */
