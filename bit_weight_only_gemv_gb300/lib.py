@@ -1,0 +1,263 @@
+"""ctypes binding of libw4a16.so (argument marshalling only).
+
+Every function takes torch tensors that already live on the GPU, checks
+dtypes/shapes, and passes raw pointers, sizes and the current CUDA stream to
+the C ABI declared in include/w4a16.h.  No arithmetic of the method happens
+here, and there is no fallback: if the library is missing, ``load()`` raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libw4a16.so")
+
+W4_FLAG_PDL = 1
+STATUS = {0: "W4_OK", 1: "W4_ERR_ARG", 2: "W4_ERR_ALIGN", 3: "W4_ERR_SHAPE",
+          4: "W4_ERR_WORKSPACE", 5: "W4_ERR_LAUNCH", 6: "W4_ERR_INDEX", 7: "W4_ERR_VALUE",
+          8: "W4_ERR_TIMEOUT", 9: "W4_ERR_DEVICE", 10: "W4_ERR_STATE"}
+STATUS_CODE = {v: k for k, v in STATUS.items()}
+
+EXPORTS = ("w4_status_str", "w4_abi_version", "w4_last_cuda_error", "w4a16_gemv", "w4a16_gemv_workspace_bytes",
+           "w4a16_gemv_id", "w4_embed_gather", "w4_pack", "w4_quantize",
+           "w4_slot_pool_create", "w4_slot_pool_destroy", "w4_slot_pool_remap",
+           "w4_slot_pool_stage", "w4_slot_pool_stats", "w4a16_gemv_plan")
+
+
+class W4Error(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        self.name = STATUS.get(code, str(code))
+        super().__init__(f"{what}: {self.name}")
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("path", "ctas", "slices", "threads", "team",
+                                            "tile_rows", "tile_groups", "stages", "smem_bytes",
+                                            "rows_per_call")]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the library once; raise if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: run __graft_entry__.build() first")
+    lib = ctypes.CDLL(path)
+    vp, i32, sz, u32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    lib.w4_status_str.restype = ctypes.c_char_p
+    lib.w4_status_str.argtypes = [i32]
+    lib.w4_abi_version.restype = i32
+    lib.w4_last_cuda_error.restype = ctypes.c_char_p
+    lib.w4_last_cuda_error.argtypes = []
+    lib.w4a16_gemv.restype = i32
+    lib.w4a16_gemv.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, sz, vp, u32, vp]
+    lib.w4a16_gemv_workspace_bytes.restype = sz
+    lib.w4a16_gemv_workspace_bytes.argtypes = [i32, i32, i32]
+    lib.w4a16_gemv_id.restype = i32
+    lib.w4a16_gemv_id.argtypes = [vp, vp, sz, vp, sz, i32, vp, i32, vp, i32, i32, i32, vp, u32, vp]
+    lib.w4_embed_gather.restype = i32
+    lib.w4_embed_gather.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, u32, vp]
+    lib.w4_pack.restype = i32
+    lib.w4_pack.argtypes = [vp, vp, i32, i32, vp, vp]
+    lib.w4_quantize.restype = i32
+    lib.w4_quantize.argtypes = [vp, vp, vp, i32, i32, vp]
+    lib.w4_slot_pool_create.restype = i32
+    lib.w4_slot_pool_create.argtypes = [ctypes.POINTER(vp), i32, i32]
+    lib.w4_slot_pool_destroy.restype = None
+    lib.w4_slot_pool_destroy.argtypes = [vp]
+    lib.w4_slot_pool_remap.restype = i32
+    lib.w4_slot_pool_remap.argtypes = [vp, i32p, i32, i32p, i32p, i32p, ctypes.POINTER(i32)]
+    lib.w4_slot_pool_stage.restype = i32
+    lib.w4_slot_pool_stage.argtypes = [vp, i32p, i32, vp, vp, sz, sz, vp, vp, sz, sz, vp, i32p,
+                                       ctypes.POINTER(i32), vp]
+    lib.w4_slot_pool_stats.restype = None
+    lib.w4_slot_pool_stats.argtypes = [vp] + [ctypes.POINTER(ctypes.c_longlong)] * 3
+    lib.w4a16_gemv_plan.restype = i32
+    lib.w4a16_gemv_plan.argtypes = [i32, i32, i32, ctypes.POINTER(PlanInfo)]
+    _lib = lib
+    return lib
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        if code in (5, 10):
+            what = f"{what} ({load().w4_last_cuda_error().decode()})"
+        raise W4Error(code, what)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _need(t: torch.Tensor, dtype, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _as_words(qw: torch.Tensor) -> torch.Tensor:
+    if qw.dtype not in (torch.int32, torch.uint32):
+        raise ValueError("qw must hold 32-bit words (int32 or uint32)")
+    return qw
+
+
+# ------------------------------------------------------------------ calls
+def workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load().w4a16_gemv_workspace_bytes(M, N, K))
+
+
+def plan(M: int, N: int, K: int) -> dict:
+    info = PlanInfo()
+    _check(load().w4a16_gemv_plan(M, N, K, ctypes.byref(info)), "w4a16_gemv_plan")
+    return {n: getattr(info, n) for n, _ in PlanInfo._fields_}
+
+
+def gemv(qw: torch.Tensor, st: torch.Tensor, x: torch.Tensor, y: torch.Tensor = None,
+         workspace: torch.Tensor = None, status: torch.Tensor = None, pdl: bool = False,
+         stream=None) -> torch.Tensor:
+    """y[M, N] = x[M, K] @ W^T with W from (qw [N, K/8], st [N, K/32])."""
+    qw = _as_words(qw)
+    _need(qw, qw.dtype, "qw")
+    _need(st, torch.bfloat16, "st")
+    _need(x, torch.bfloat16, "x")
+    x2 = x if x.dim() == 2 else x.view(1, -1)
+    M, K = x2.shape
+    N = qw.shape[0]
+    if qw.shape != (N, K // 8) or st.shape != (N, K // 32):
+        raise ValueError("qw/st shapes do not match x")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _need(y, torch.bfloat16, "y")
+    need = workspace_bytes(M, N, K)
+    if need and workspace is None:
+        raise ValueError(f"this shape needs a zero-filled workspace of {need} bytes")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().w4a16_gemv(_ptr(y), _ptr(qw), _ptr(st), _ptr(x2), M, N, K, _ptr(workspace),
+                             ws_bytes, _ptr(status), W4_FLAG_PDL if pdl else 0, _stream(stream)),
+           "w4a16_gemv")
+    return y
+
+
+def gemv_id(qw_base: torch.Tensor, st_base: torch.Tensor, ids: torch.Tensor, x: torch.Tensor,
+            N: int, K: int, num_experts: int, qw_stride_bytes: int, st_stride_bytes: int,
+            y: torch.Tensor = None, status: torch.Tensor = None, pdl: bool = False,
+            stream=None) -> torch.Tensor:
+    """y[i] = W_{ids[i]} @ x[i or 0]; experts at base + id * stride (bytes)."""
+    _need(ids, torch.int32, "ids")
+    _need(x, torch.bfloat16, "x")
+    if not (qw_base.is_cuda and st_base.is_cuda):
+        raise ValueError("bases must be CUDA tensors")
+    x2 = x if x.dim() == 2 else x.view(1, -1)
+    n_ids = ids.numel()
+    if y is None:
+        y = torch.empty((n_ids, N), dtype=torch.bfloat16, device=x.device)
+    _need(y, torch.bfloat16, "y")
+    _check(load().w4a16_gemv_id(_ptr(y), _ptr(qw_base), qw_stride_bytes, _ptr(st_base),
+                                st_stride_bytes, num_experts, _ptr(ids), n_ids, _ptr(x2),
+                                x2.shape[0], N, K, _ptr(status), W4_FLAG_PDL if pdl else 0,
+                                _stream(stream)), "w4a16_gemv_id")
+    return y
+
+
+def embed_gather(qw: torch.Tensor, st: torch.Tensor, ids: torch.Tensor, out: torch.Tensor = None,
+                 status: torch.Tensor = None, pdl: bool = False, stream=None) -> torch.Tensor:
+    qw = _as_words(qw)
+    _need(qw, qw.dtype, "qw")
+    _need(st, torch.bfloat16, "st")
+    _need(ids, torch.int32, "ids")
+    V, K = qw.shape[0], qw.shape[1] * 8
+    T = ids.numel()
+    if out is None:
+        out = torch.empty((T, K), dtype=torch.bfloat16, device=qw.device)
+    _need(out, torch.bfloat16, "out")
+    _check(load().w4_embed_gather(_ptr(out), _ptr(qw), _ptr(st), _ptr(ids), T, V, K, _ptr(status),
+                                  W4_FLAG_PDL if pdl else 0, _stream(stream)), "w4_embed_gather")
+    return out
+
+
+def pack(codes: torch.Tensor, qw: torch.Tensor = None, status: torch.Tensor = None,
+         stream=None) -> torch.Tensor:
+    _need(codes, torch.uint8, "codes")
+    N, K = codes.shape
+    if qw is None:
+        qw = torch.empty((N, K // 8), dtype=torch.int32, device=codes.device)
+    _check(load().w4_pack(_ptr(qw), _ptr(codes), N, K, _ptr(status), _stream(stream)), "w4_pack")
+    return qw
+
+
+def quantize(w: torch.Tensor, stream=None):
+    _need(w, torch.float32, "w")
+    N, K = w.shape
+    qw = torch.empty((N, K // 8), dtype=torch.int32, device=w.device)
+    st = torch.empty((N, K // 32), dtype=torch.bfloat16, device=w.device)
+    _check(load().w4_quantize(_ptr(qw), _ptr(st), _ptr(w), N, K, _stream(stream)), "w4_quantize")
+    return qw, st
+
+
+class SlotPool:
+    """Host LFU expert-slot pool (C++ in the library)."""
+
+    def __init__(self, num_experts: int, num_slots: int):
+        self._lib = load()
+        h = ctypes.c_void_p()
+        _check(self._lib.w4_slot_pool_create(ctypes.byref(h), num_experts, num_slots),
+               "w4_slot_pool_create")
+        self._h = h
+        self.num_experts, self.num_slots = num_experts, num_slots
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            self._lib.w4_slot_pool_destroy(h)
+            self._h = None
+
+    def remap(self, ids):
+        ids = [int(v) for v in ids]
+        k = len(ids)
+        arr = (ctypes.c_int32 * k)(*ids)
+        slots = (ctypes.c_int32 * k)()
+        me = (ctypes.c_int32 * k)()
+        ms = (ctypes.c_int32 * k)()
+        nm = ctypes.c_int()
+        _check(self._lib.w4_slot_pool_remap(self._h, arr, k, slots, me, ms, ctypes.byref(nm)),
+               "w4_slot_pool_remap")
+        return list(slots), [(me[i], ms[i]) for i in range(nm.value)]
+
+    def stage(self, ids, pool_qw, full_qw, qw_stride, qw_bytes, pool_st, full_st, st_stride,
+              st_bytes, slot_ids_dev: torch.Tensor, stream=None):
+        """Remap, copy missed experts into the pool and write slot ids, all on `stream`."""
+        ids = [int(v) for v in ids]
+        k = len(ids)
+        arr = (ctypes.c_int32 * k)(*ids)
+        slots = (ctypes.c_int32 * k)()
+        nm = ctypes.c_int()
+        _check(self._lib.w4_slot_pool_stage(self._h, arr, k, _ptr(pool_qw), _ptr(full_qw),
+                                            qw_stride, qw_bytes, _ptr(pool_st), _ptr(full_st),
+                                            st_stride, st_bytes, _ptr(slot_ids_dev), slots,
+                                            ctypes.byref(nm), _stream(stream)),
+               "w4_slot_pool_stage")
+        return list(slots), nm.value
+
+    def stats(self):
+        r, h, m = ctypes.c_longlong(), ctypes.c_longlong(), ctypes.c_longlong()
+        self._lib.w4_slot_pool_stats(self._h, ctypes.byref(r), ctypes.byref(h), ctypes.byref(m))
+        return {"requests": r.value, "hits": h.value, "misses": m.value}

@@ -86,6 +86,10 @@ const char *w4_status_str(int status);
 /* W4_ABI_VERSION of the loaded library. */
 int w4_abi_version(void);
 
+/* Text of the CUDA error behind the calling thread's last W4_ERR_LAUNCH or
+ * W4_ERR_STATE from a failed enqueue ("no error" if none; static string). */
+const char *w4_last_cuda_error(void);
+
 /*
  * w4a16_gemv — dense W4A16 matrix-vector (or small-batch matrix) product.
  *

@@ -1,0 +1,149 @@
+"""C-ABI checks that need no GPU: the library loads, exports every call the
+header declares, validates arguments on the host, plans launches, and runs the
+host-side slot pool exactly like the oracle's policy."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_weight_only_gemv_gb300 import lib, synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    return lib.load()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "w4a16.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(w4\w*)\s*\(", text)))
+
+
+def test_header_declares_the_calls():
+    names = header_functions()
+    for need in ("w4a16_gemv", "w4a16_gemv_id", "w4_embed_gather", "w4_pack", "w4_quantize"):
+        assert need in names
+
+
+def test_library_exports_every_declared_call(L):
+    for name in header_functions():
+        assert hasattr(L, name), name
+        assert isinstance(getattr(L, name), ctypes._CFuncPtr)
+    assert set(lib.EXPORTS) <= set(header_functions())
+
+
+def test_version_and_status_strings(L):
+    assert L.w4_abi_version() == 1
+    assert L.w4_status_str(0) == b"ok"
+    assert L.w4_status_str(6) == b"id out of range"
+    assert L.w4_status_str(999) == b"unknown status"
+
+
+def test_host_validation_rejects_before_any_launch(L):
+    vp = ctypes.c_void_p
+    good = vp(1 << 20)                      # never dereferenced: rejected earlier
+    # K not a multiple of 32
+    assert L.w4a16_gemv(good, good, good, good, 1, 16, 48, None, 0, None, 0, None) == 3
+    # null pointer
+    assert L.w4a16_gemv(None, good, good, good, 1, 16, 64, None, 0, None, 0, None) == 1
+    # M out of range
+    assert L.w4a16_gemv(good, good, good, good, 33, 16, 64, None, 0, None, 0, None) == 3
+    # misaligned weights
+    assert L.w4a16_gemv(good, vp((1 << 20) + 8), good, good, 1, 16, 64, None, 0, None, 0,
+                        None) == 2
+    # unknown flag bit
+    assert L.w4a16_gemv(good, good, good, good, 1, 16, 64, None, 0, None, 4, None) == 1
+    # gemv_id: x_rows must be 1 or n_ids, strides multiples of 16 and >= an expert
+    assert L.w4a16_gemv_id(good, good, 1024, good, 128, 4, good, 3, good, 2, 32, 64, None, 0,
+                           None) == 3
+    assert L.w4a16_gemv_id(good, good, 1032, good, 128, 4, good, 3, good, 1, 32, 64, None, 0,
+                           None) == 2
+    assert L.w4a16_gemv_id(good, good, 512, good, 128, 4, good, 3, good, 1, 32, 64, None, 0,
+                           None) == 1
+    assert L.w4_embed_gather(good, good, good, good, 0, 10, 64, None, 0, None) == 1
+    assert L.w4_pack(good, good, 4, 40, None, None) == 3
+    assert L.w4_quantize(good, good, vp((1 << 20) + 4), 4, 64, None) == 2
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 2048, 2048), (1, 512, 2048), (1, 2048, 8192),
+                                   (1, 5376, 21504), (1, 704, 2816), (1, 2816, 704),
+                                   (4, 8192, 2048), (1, 262144, 2048), (1, 7, 32),
+                                   (3, 100, 65536)])
+def test_plan_is_valid(M, N, K):
+    p = lib.plan(M, N, K)
+    assert p["threads"] == 512 and p["stages"] == 4
+    assert p["team"] in (8, 16, 32)
+    assert p["tile_rows"] * p["team"] == 512
+    assert 1 <= p["ctas"] <= 152
+    assert p["smem_bytes"] <= 232448
+    assert p["rows_per_call"] == min(M, 4)
+    ws = lib.workspace_bytes(M, N, K)
+    assert (ws > 0) == (p["slices"] > 1)
+
+
+def test_tiling_depends_on_k_only():
+    # the per-row arithmetic (team, chunk length) must not change with N or M
+    for K in (704, 2048, 2816, 5376, 8192, 21504):
+        ref = lib.plan(1, 4096, K)
+        for N in (16, 704, 2048, 100000):
+            p = lib.plan(1, N, K)
+            assert (p["team"], p["tile_groups"]) == (ref["team"], ref["tile_groups"])
+
+
+def test_slot_pool_matches_oracle_policy():
+    rng = np.random.default_rng(0)
+    for trial in range(20):
+        e = int(rng.integers(2, 200))
+        s = int(rng.integers(1, min(e, 48) + 1))
+        k = int(rng.integers(1, s + 1))
+        pool = lib.SlotPool(e, s)
+        ref = oracle.LFUSlotPoolRef(e, s)
+        if trial % 2:
+            trace = synth.moe_trace(e, k, 60, 1.1, 0.7, seed=trial) if k <= e else None
+        else:
+            trace = [list(rng.integers(0, e, size=k)) for _ in range(60)]
+        for req in trace:
+            assert pool.remap(req) == ref.step(req)
+
+
+def test_slot_pool_hand_traces_and_errors():
+    import test_oracle_pins as pins
+    for name, e, s, steps in pins._read_traces():
+        pool = lib.SlotPool(e, s)
+        for req, want_slots, want_miss in steps:
+            assert pool.remap(req) == (want_slots, want_miss), name
+    pool = lib.SlotPool(4, 2)
+    with pytest.raises(lib.W4Error) as ei:
+        pool.remap([0, 1, 2])
+    assert ei.value.name == "W4_ERR_STATE"
+    with pytest.raises(lib.W4Error) as ei:
+        pool.remap([4])
+    assert ei.value.name == "W4_ERR_INDEX"
+    # rejected requests leave the pool unchanged
+    assert pool.remap([1]) == ([0], [(1, 0)])
+    st = pool.stats()
+    assert st == {"requests": 1, "hits": 0, "misses": 1}
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="uses the failure of copies without a GPU")
+def test_slot_pool_failed_copy_forgets_the_slot():
+    # Without a device every enqueue fails: the pool must report it and must not
+    # keep the expert it could not load.
+    pool = lib.SlotPool(8, 2)
+    fake = torch.empty(1)
+    fake_ptr = type("P", (), {"data_ptr": lambda self: 1 << 20})()
+    with pytest.raises(lib.W4Error) as ei:
+        pool.stage([3], fake_ptr, fake_ptr, 4096, 4096, fake_ptr, fake_ptr, 512, 512, fake_ptr,
+                   stream=type("S", (), {"cuda_stream": 0})())
+    assert ei.value.name == "W4_ERR_STATE"
+    # the expert is not resident: the next request for it is a miss again
+    assert pool.remap([3]) == ([0], [(3, 0)])
+    del fake

@@ -1,0 +1,184 @@
+"""GPU parity of w4a16_gemv against the fp64 oracle (through the C ABI).
+
+Bar: every output within |y - y_ref| <= 2e-3 * sum_k |w x| + one bf16 ulp of
+y_ref; bit-exact where the result is a single rounding of an exact value.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_weight_only_gemv_gb300 import lib, synth
+from _helpers import (POISON, assert_gemv_parity, dev_bf16, dev_words, host_bits,
+                      poison_bf16)
+
+pytestmark = pytest.mark.gpu
+
+
+def make(rng, n, k, m=1, step_scale=0.02 / 8):
+    qw_h = synth.np_words(rng, (n, k // 8))
+    st_h = synth.np_steps(rng, (n, k // 32), scale=step_scale)
+    x_h = synth.np_x(rng, (m, k))
+    return qw_h, st_h, x_h
+
+
+def run(qw_h, st_h, x_h, pdl=False):
+    n, k = qw_h.shape[0], qw_h.shape[1] * 8
+    m = x_h.shape[0]
+    qw, st, x = dev_words(qw_h), dev_bf16(st_h), dev_bf16(x_h)
+    y = poison_bf16((m, n))
+    ws = None
+    need = lib.workspace_bytes(m, n, k)
+    if need:
+        ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lib.gemv(qw, st, x, y=y, workspace=ws, status=status, pdl=pdl)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return y, ws
+
+
+# Shapes spanning every tiling the plan picks (whole rows and K chunks, team
+# sizes 8/16/32), several tiles and CTAs, ragged row and chunk tails, and the
+# split-K path.
+SHAPES = [
+    (1, 32, 1), (7, 32, 1), (37, 96, 1), (16, 64, 1), (17, 2048, 1), (300, 2048, 1),
+    (2048, 2048, 1), (129, 704, 1), (1000, 704, 1), (333, 2816, 1), (250, 5376, 1),
+    (100, 8192, 1), (513, 8192, 1), (64, 21504, 1), (19, 65536, 1),
+    (300, 2048, 2), (300, 2048, 3), (130, 2048, 4), (77, 2816, 5), (50, 1024, 8),
+    (40, 5376, 32),
+]
+
+
+@pytest.mark.parametrize("n,k,m", SHAPES)
+def test_gemv_matches_oracle(cuda_lib, n, k, m):
+    rng = np.random.default_rng(n * 131 + k + m)
+    qw_h, st_h, x_h = make(rng, n, k, m)
+    y, _ = run(qw_h, st_h, x_h)
+    assert_gemv_parity(y, qw_h, st_h, x_h)
+
+
+def test_gemv_one_hot_is_bit_exact(cuda_lib):
+    rng = np.random.default_rng(1)
+    n, k = 333, 2816
+    qw_h, st_h, _ = make(rng, n, k)
+    w = oracle.dequant(qw_h, st_h)
+    for kk in (0, 5, 31, 32, 1000, k - 1):
+        x_h = np.zeros((1, k), np.uint16)
+        x_h[0, kk] = 0x3F80
+        y, _ = run(qw_h, st_h, x_h)
+        assert np.array_equal(host_bits(y)[0], oracle.bf16_rne(w[:, kk]))
+
+
+def test_gemv_code_eight_gives_zero_and_closed_form(cuda_lib):
+    rng = np.random.default_rng(2)
+    n, k = 200, 2048
+    x_h = synth.np_x(rng, (1, k))
+    st_h = synth.np_steps(rng, (n, k // 32))
+    qw_h = np.full((n, k // 8), 0x88888888, np.uint32)
+    y, _ = run(qw_h, st_h, x_h)
+    assert np.all(host_bits(y) & 0x7FFF == 0)
+    for c in (0, 3, 15):
+        qw_c = np.full((n, k // 8), int(format(c, "x") * 8, 16), np.uint32)
+        y, _ = run(qw_c, st_h, x_h)
+        assert_gemv_parity(y, qw_c, st_h, x_h)
+
+
+def test_gemv_is_deterministic_and_batch_rows_match(cuda_lib):
+    rng = np.random.default_rng(3)
+    n, k = 700, 5376
+    qw_h, st_h, x_h = make(rng, n, k, 4)
+    y4, _ = run(qw_h, st_h, x_h)
+    y4b, _ = run(qw_h, st_h, x_h)
+    assert torch.equal(y4.view(torch.int16), y4b.view(torch.int16))
+    for m in range(4):
+        y1, _ = run(qw_h, st_h, x_h[m:m + 1])
+        assert np.array_equal(host_bits(y1)[0], host_bits(y4)[m])
+
+
+def test_split_k_equals_unsplit_bitwise(cuda_lib):
+    # N = 256, K = 8192 is planned with K slices; gemv_id over the same rows is
+    # never split; the per-row arithmetic must not depend on the split.
+    rng = np.random.default_rng(4)
+    n, k = 256, 8192
+    assert lib.plan(1, n, k)["slices"] > 1
+    qw_h, st_h, x_h = make(rng, n, k)
+    y, ws = run(qw_h, st_h, x_h)
+    assert ws is not None and int(ws[:4].view(torch.int32).abs().sum()) == 0
+    qw, st, x = dev_words(qw_h), dev_bf16(st_h), dev_bf16(x_h)
+    ids = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y_id = lib.gemv_id(qw, st, ids, x, n, k, 1, n * k // 2, n * k // 16)
+    torch.cuda.synchronize()
+    assert np.array_equal(host_bits(y), host_bits(y_id))
+    assert_gemv_parity(y, qw_h, st_h, x_h)
+
+
+def test_split_k_workspace_is_rearmed(cuda_lib):
+    rng = np.random.default_rng(5)
+    n, k = 512, 8192
+    qw_h, st_h, x_h = make(rng, n, k)
+    qw, st, x = dev_words(qw_h), dev_bf16(st_h), dev_bf16(x_h)
+    need = lib.workspace_bytes(1, n, k)
+    assert need > 0
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    ys = [lib.gemv(qw, st, x, workspace=ws) for _ in range(3)]
+    torch.cuda.synchronize()
+    for y in ys[1:]:
+        assert torch.equal(y.view(torch.int16), ys[0].view(torch.int16))
+    assert_gemv_parity(ys[0], qw_h, st_h, x_h)
+    with pytest.raises(lib.W4Error) as ei:
+        lib.gemv(qw, st, x, workspace=ws[:16])
+    assert ei.value.name == "W4_ERR_WORKSPACE"
+
+
+def test_gemv_wide_dynamic_range_and_extreme_steps(cuda_lib):
+    rng = np.random.default_rng(6)
+    n, k = 300, 2048
+    qw_h = synth.np_words(rng, (n, k // 8))
+    mags = 10.0 ** rng.uniform(-6, 4, size=(2, k))
+    x_h = synth._to_bf16_bits(rng.choice([-1.0, 1.0], size=(2, k)) * mags)
+    x_h[1, :64] = 0                       # an all-zero group
+    st_h = synth._to_bf16_bits(10.0 ** rng.uniform(-30, 20, size=(n, k // 32)))
+    y, _ = run(qw_h, st_h, x_h)
+    assert_gemv_parity(y, qw_h, st_h, x_h)
+
+
+def test_gemv_non_finite_activation_propagates(cuda_lib):
+    rng = np.random.default_rng(7)
+    n, k = 64, 2048
+    qw_h, st_h, x_h = make(rng, n, k)
+    x_h[0, 100] = 0x7F80                  # +inf
+    y, _ = run(qw_h, st_h, x_h)
+    y_ref = oracle.gemv_ref(qw_h, st_h, x_h)
+    got = oracle.bf16_bits_to_f64(host_bits(y))
+    assert np.array_equal(np.isfinite(got), np.isfinite(y_ref))
+
+
+def test_gemv_pdl_flag_same_bits(cuda_lib):
+    rng = np.random.default_rng(8)
+    n, k = 1500, 2048
+    qw_h, st_h, x_h = make(rng, n, k)
+    qw, st, x = dev_words(qw_h), dev_bf16(st_h), dev_bf16(x_h)
+    y0 = lib.gemv(qw, st, x)
+    ys = []
+    for _ in range(5):                    # back-to-back programmatic dependents
+        ys.append(lib.gemv(qw, st, x, pdl=True))
+    torch.cuda.synchronize()
+    for y in ys:
+        assert torch.equal(y.view(torch.int16), y0.view(torch.int16))
+
+
+def test_gemv_unaligned_output_view_and_guard_band(cuda_lib):
+    rng = np.random.default_rng(9)
+    n, k = 100, 2048
+    qw_h, st_h, x_h = make(rng, n, k)
+    qw, st, x = dev_words(qw_h), dev_bf16(st_h), dev_bf16(x_h)
+    big = poison_bf16((1, n + 3))
+    y = big[:, 1:n + 1]                   # 2-byte aligned view inside a guard band
+    assert y.is_contiguous() and y.data_ptr() % 4 == 2
+    lib.gemv(qw, st, x, y=y)
+    torch.cuda.synchronize()
+    b = host_bits(big)[0]
+    assert b[0] == POISON and np.all(b[n + 1:] == POISON)
+    assert_gemv_parity(y, qw_h, st_h, x_h)

@@ -1,0 +1,112 @@
+"""GPU parity of w4a16_gemv_id: oracle bound, the slot-pool memcmp bar, and
+row-for-row identity with w4a16_gemv on the selected expert."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_weight_only_gemv_gb300 import lib, synth
+from _helpers import POISON, dev_bf16, dev_words, host_bits, poison_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+def experts(rng, e, n, k, pad_qw=0, pad_st=0):
+    """Expert tensors as one byte buffer each, expert stride = size + padding."""
+    qw_bytes, st_bytes = n * k // 2, n * k // 16
+    qs, ss = qw_bytes + pad_qw, st_bytes + pad_st
+    qw_buf = np.zeros(e * qs, np.uint8)
+    st_buf = np.zeros(e * ss, np.uint8)
+    qw_h = synth.np_words(rng, (e, n, k // 8))
+    st_h = synth.np_steps(rng, (e, n, k // 32))
+    for i in range(e):
+        qw_buf[i * qs:i * qs + qw_bytes] = qw_h[i].view(np.uint8).ravel()
+        st_buf[i * ss:i * ss + st_bytes] = st_h[i].view(np.uint8).ravel()
+    return qw_h, st_h, qw_buf, st_buf, qs, ss
+
+
+def dev_bytes(a):
+    return torch.from_numpy(a).to("cuda")
+
+
+@pytest.mark.parametrize("e,n,k,n_ids,x_rows,pad", [
+    (6, 96, 704, 4, 4, 0), (6, 96, 704, 4, 1, 32), (5, 704, 2816, 8, 1, 0),
+    (5, 2816, 704, 8, 8, 16), (3, 33, 2048, 5, 5, 48), (4, 100, 8192, 3, 1, 0),
+    (2, 40, 96, 1, 1, 0)])
+def test_gemv_id_matches_oracle(cuda_lib, e, n, k, n_ids, x_rows, pad):
+    rng = np.random.default_rng(e * 7 + n + k + n_ids + pad)
+    qw_h, st_h, qwb, stb, qs, ss = experts(rng, e, n, k, pad, pad)
+    ids_h = rng.integers(0, e, size=n_ids).astype(np.int32)
+    if n_ids > 1:
+        ids_h[1] = ids_h[0]                       # repeated id
+    x_h = synth.np_x(rng, (x_rows, k))
+    ids = torch.from_numpy(ids_h).to("cuda")
+    y = poison_bf16((n_ids, n))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lib.gemv_id(dev_bytes(qwb), dev_bytes(stb), ids, dev_bf16(x_h), n, k, e, qs, ss, y=y,
+                status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    yb = host_bits(y)
+    y_ref = oracle.gemv_id_ref(qw_h, st_h, ids_h, x_h)
+    a_ref = np.stack([oracle.gemv_abs_ref(qw_h[d], st_h[d], x_h[0 if x_rows == 1 else i])[0]
+                      for i, d in enumerate(ids_h)])
+    assert oracle.within_bound(yb, y_ref, a_ref)
+    # row i is bitwise the dense GEMV of expert ids[i] on its activation row
+    for i, d in enumerate(ids_h):
+        yd = lib.gemv(dev_words(qw_h[d]), dev_bf16(st_h[d]),
+                      dev_bf16(x_h[0 if x_rows == 1 else i][None]),
+                      workspace=torch.zeros(max(1, lib.workspace_bytes(1, n, k)),
+                                            dtype=torch.uint8, device="cuda"))
+        torch.cuda.synchronize()
+        assert np.array_equal(host_bits(yd)[0], yb[i])
+
+
+def test_gemv_id_bad_ids_leave_rows_unwritten(cuda_lib):
+    rng = np.random.default_rng(11)
+    e, n, k = 4, 64, 2048
+    qw_h, st_h, qwb, stb, qs, ss = experts(rng, e, n, k)
+    ids_h = np.array([1, 4, -1, 3], np.int32)
+    x_h = synth.np_x(rng, (1, k))
+    y = poison_bf16((4, n))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lib.gemv_id(dev_bytes(qwb), dev_bytes(stb), torch.from_numpy(ids_h).cuda(), dev_bf16(x_h),
+                n, k, e, qs, ss, y=y, status=status)
+    torch.cuda.synchronize()
+    assert lib.STATUS[int(status.item())] == "W4_ERR_INDEX"
+    yb = host_bits(y)
+    assert np.all(yb[1] == POISON) and np.all(yb[2] == POISON)
+    assert not np.any(yb[0] == POISON) and not np.any(yb[3] == POISON)
+    ref = oracle.gemv_id_ref(qw_h, st_h, ids_h[[0, 3]], x_h)
+    a = np.stack([oracle.gemv_abs_ref(qw_h[d], st_h[d], x_h)[0] for d in ids_h[[0, 3]]])
+    assert oracle.within_bound(yb[[0, 3]], ref, a)
+
+
+def test_slot_pool_is_bitwise_equal_to_full_tensor(cuda_lib):
+    """The page's memcmp bar: same kernel, same bytes, different addressing."""
+    rng = np.random.default_rng(12)
+    cfg = synth.moe_2816()
+    E, S, H, I = 32, 8, cfg.hidden, cfg.expert_inter
+    n_layers, steps = 2, 40
+    for proj, (n, k) in (("gate", (I, H)), ("down", (H, I))):
+        for layer in range(n_layers):
+            qs, ss = n * k // 2, n * k // 16
+            full_q = synth.torch_words((E, qs // 4), seed=synth.seed_of(3, layer, n), device="cuda")
+            full_s = synth.torch_steps((E, ss // 2), seed=synth.seed_of(4, layer, n), device="cuda")
+            pool_q = torch.zeros((S, qs // 4), dtype=torch.int32, device="cuda")
+            pool_s = torch.zeros((S, ss // 2), dtype=torch.bfloat16, device="cuda")
+            pool = lib.SlotPool(E, S)
+            slot_ids = torch.zeros(4, dtype=torch.int32, device="cuda")
+            trace = synth.moe_trace(E, 4, steps, 1.1, 0.7, seed=layer)
+            for t in range(steps):
+                x_rows = 1 if proj == "gate" else 4
+                x = synth.torch_x((x_rows, k), seed=synth.seed_of(5, layer, t), device="cuda")
+                pool.stage(trace[t], pool_q, full_q, qs, qs, pool_s, full_s, ss, ss, slot_ids)
+                ids_full = torch.from_numpy(trace[t].astype(np.int32)).cuda()
+                y_pool = lib.gemv_id(pool_q, pool_s, slot_ids, x, n, k, S, qs, ss)
+                y_full = lib.gemv_id(full_q, full_s, ids_full, x, n, k, E, qs, ss)
+                assert torch.equal(y_pool.view(torch.int16), y_full.view(torch.int16)), (proj, t)
+            st = pool.stats()
+            assert st["hits"] > 0 and st["misses"] >= S
+    torch.cuda.synchronize()
