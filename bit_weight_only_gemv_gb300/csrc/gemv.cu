@@ -8,36 +8,37 @@
 // SSD", section "Streaming without touching a single GPU kernel") reads expert
 // `id` at base + id * stride.
 //
-// Design (one persistent CTA per SM):
-//  * The weight matrix is split into row blocks of `tile_rows` rows; a row
-//    block is cut along K into chunks of G groups (G = K/32 when whole rows fit
-//    a stage).  A (row block, K slice) pair is a unit; every CTA owns a
-//    contiguous, balanced range of units.
-//  * Thread 0 streams each (row block, chunk) tile from HBM into a 4-deep ring
-//    of shared-memory stages with 1-D bulk copies (cp.async.bulk, TMA engine),
-//    completion tracked by one mbarrier per stage.  Codes of a whole-row tile
-//    are one contiguous copy.  With W4_FLAG_PDL the first copies are issued
-//    before waiting on the previous kernel in the stream.
-//  * The activation rows are staged once per CTA into shared memory as fp16
-//    pairs scaled by a power of two per group of 32 (exact), with the group's
-//    inverse scale kept beside them.
-//  * `TEAM` lanes share an output row.  Per 32-code group a lane turns each
-//    packed word into four fp16 pairs (c - 8) with the float-bit trick of the
-//    page (fp16 form: (0x6400 | c) - 1032 = c - 8, exact), multiplies them with
-//    the fp16 activation pairs in packed fp16 (products exact), sums each lane
-//    of a pair over the group's 4 words in fp16, converts and adds the 8
-//    partial sums into fp32, scales by step * group scale and accumulates in
-//    fp32.  Error: at most 3 fp16 roundings per 4-product partial, i.e.
-//    3 * 2^-11 of sum|w x|, plus fp32 accumulation.
-//  * After each chunk the team reduces its lanes with a fixed xor-shuffle
-//    tree; chunk sums are added in chunk order.  The arithmetic of a row thus
-//    depends on K only, never on N, the row index, the slice split or the
-//    addresses (bitwise-reproducible and gemv_id == gemv per row).
-//  * Split-K (slices > 1): every chunk sum goes to the workspace; the CTA that
-//    finishes a row block last (atomic counter, no waiting) adds the chunk
-//    sums in chunk order, writes the row block and re-arms the counter.
-//  * Every wait is bounded; on expiry the kernel records W4_ERR_TIMEOUT, waits
-//    (bounded) for its own copies in flight and leaves.
+// Design (one persistent CTA of 16 warps per SM):
+//  * The activation rows are staged once per CTA in shared memory as fp16
+//    pairs scaled by a power of two per group of 32 (exact), next to the
+//    group's inverse scale.
+//  * A team of `team` lanes shares a set of R output rows (team = the largest
+//    power of two <= 32 dividing K/32 that leaves each lane >= 8 groups of a
+//    row, so no lane idles); each lane walks the
+//    groups lane, lane + team, ... and handles the same group of its R rows
+//    together, so one shared-memory read of the activations serves R rows.
+//  * Packed codes and steps go straight from HBM to registers with coalesced
+//    128-bit (codes) loads that bypass L1; the weights never touch shared
+//    memory, which keeps shared-memory bandwidth for the activations.
+//  * Per group and row the lane turns each packed word into four fp16 pairs
+//    (c - 8) with the float-bit trick of the page in its fp16 form
+//    ((0x6400 | c) - 1032 = c - 8, exact), multiplies them with the fp16
+//    activation pairs in packed fp16 (products exact), sums each pair lane
+//    over the group's 4 words in fp16 (at most 3 roundings: 3 * 2^-11 of
+//    sum|w x|), adds the 8 partial sums in fp32, rescales by the group's 2^-e
+//    (exact), multiplies by the step and accumulates in fp32.
+//  * K is cut into chunks of 8 groups per lane; after each chunk the team
+//    reduces with a fixed xor-shuffle tree and chunk sums are added in chunk
+//    order.  A row's arithmetic therefore depends on K only, never on N, R,
+//    the row index, the split or the addresses: results are bitwise
+//    reproducible and a gemv_id row equals the gemv of that expert.
+//  * Work unit = (row block of 32/team * R rows, K slice).  Each CTA owns a
+//    balanced contiguous range of units; its warps take them round-robin.
+//    Split-K (slices > 1): chunk sums go to the workspace and the warp that
+//    finishes a row block last (atomic counter, no waiting) adds them in
+//    chunk order, writes the rows and re-arms the counter.
+//  * With W4_FLAG_PDL the launch may overlap the previous kernel in the
+//    stream; all global reads and writes happen after waiting for it.
 #include <algorithm>
 #include <mutex>
 
@@ -45,10 +46,10 @@
 
 namespace w4 {
 
-constexpr int kThreads = 512;      // 16 warps, all compute; thread 0 also issues copies
-constexpr int kStages = 4;         // shared-memory ring depth
-constexpr int kMaxMR = 4;          // activation rows per launch on this path
-constexpr long long kWaitCycles = 4000000000LL;   // ~2 s at GB300 clocks
+constexpr int kWarps = 16;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kMaxMR = 4;        // activation rows per launch
+constexpr int kChunkPerLane = 8; // groups per lane per chunk
 
 struct GemvParams {
   const uint8_t* qw;
@@ -63,143 +64,32 @@ struct GemvParams {
   int MR;                              // activation rows per item in this launch
   int N, K, Kg;
   int n_items;
-  int tile_rows, G, nch, whole;        // tiling (depends on K only)
-  int S, cps, bpi;                     // partition
-  long long B, U;
-  int xg_max;                          // groups of staged activations
-  int stage_codes, stage_steps, seg_stride, stage_bytes;
+  int team, sets, R, rows_per_unit;    // lanes per row, row sets per warp, rows per lane
+  int chunk, nch;                      // groups per chunk (team * 8), chunks per row
+  int S, cps, upi;                     // slices, chunks per slice, row blocks per item
+  int B, U;                            // row blocks, units (= S * B)
+  int x_slots;                         // activation rows staged per CTA (per MR row)
   int* ws_count;                       // [B] at the start of the workspace
-  float* ws_partial;                   // [B][nch][tile_rows][MR] after it
+  float* ws_partial;                   // [B][nch][rows_per_unit][MR] after it
   int32_t* status;
 };
 
-// ---------------------------------------------------------------- tile walk
-struct Walk {
-  long long u, u_end;
-  int c, c_end;
-  int slice, item, row0, rows;
-  long long rb;
-  const uint8_t* qw_item;
-  const uint8_t* st_item;
-
-  __device__ void load(const GemvParams& p) {
-    while (u < u_end) {
-      slice = (int)(u / p.B);
-      rb = u - (long long)slice * p.B;
-      item = (int)(rb / p.bpi);
-      const int rbi = (int)(rb - (long long)item * p.bpi);
-      row0 = rbi * p.tile_rows;
-      rows = min(p.tile_rows, p.N - row0);
-      c = slice * p.cps;
-      c_end = min(c + p.cps, p.nch);
-      long long blk = item;
-      if (p.ids != nullptr) {
-        const int e = __ldg(p.ids + item);
-        if (e < 0 || e >= p.num_experts) {   // id out of range: skip the unit
-          report(p.status, W4_ERR_INDEX);
-          ++u;
-          continue;
-        }
-        blk = e;
-      }
-      qw_item = p.qw + (unsigned long long)blk * p.qw_item_stride;
-      st_item = p.st + (unsigned long long)blk * p.st_item_stride;
-      return;
-    }
-  }
-  __device__ void init(const GemvParams& p, long long ub, long long ue) {
-    u = ub;
-    u_end = ue;
-    load(p);
-  }
-  __device__ bool done() const { return u >= u_end; }
-  __device__ void next(const GemvParams& p) {
-    if (++c >= c_end) {
-      ++u;
-      load(p);
-    }
-  }
-  __device__ int g0(const GemvParams& p) const { return c * p.G; }
-  __device__ int glen(const GemvParams& p) const { return min(p.G, p.Kg - c * p.G); }
-};
-
-// Copy bytes [b, e) of a step array of `total` bytes to shared memory at
-// `dst` (16-byte aligned), as the 16-byte-aligned superset [b & ~15, ...)
-// clipped to the array; bytes past the last full 16-byte line of the array
-// are loaded one by one.  Returns the number of bulk-copied bytes.
-__device__ __forceinline__ uint32_t copy_steps(uint8_t* dst, const uint8_t* src, long long b,
-                                               long long e, long long total, uint32_t bar,
-                                               uint64_t pol, bool issue) {
-  const long long lo = b & ~15LL;
-  const long long lim = total & ~15LL;
-  const long long hi = min((e + 15) & ~15LL, lim);
-  uint32_t bytes = 0;
-  if (hi > lo) {
-    bytes = (uint32_t)(hi - lo);
-    if (issue) bulk_g2s_evict_first(smem_addr(dst), src + lo, bytes, bar, pol);
-  }
-  if (!issue) {
-    for (long long i = max(lo, lim); i < e; ++i) dst[i - lo] = src[i];
-  }
-  return bytes;
-}
-
-// Thread 0: start loading tile `w` into stage `slot`.
-__device__ void issue_tile(const GemvParams& p, const Walk& w, uint8_t* stage, uint32_t bar,
-                           uint64_t pol) {
-  uint8_t* codes = stage;
-  uint8_t* steps = stage + p.stage_codes;
-  const long long row_bytes = (long long)p.K / 2;
-  const long long st_total = (long long)p.N * p.Kg * 2;
-  const int g0 = w.g0(p), gl = w.glen(p);
-  uint32_t tx = 0;
-  // scalar step tails first (generic stores), then one arrive with the byte
-  // count, then the bulk copies
-  for (int pass = 0; pass < 2; ++pass) {
-    const bool issue = pass == 1;
-    if (issue) {
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(bar, tx);
-      const uint8_t* src = w.qw_item + (long long)w.row0 * row_bytes + (long long)g0 * 16;
-      if (p.whole) {
-        bulk_g2s_evict_first(smem_addr(codes), src, (uint32_t)(w.rows * row_bytes), bar, pol);
-      } else {
-        for (int r = 0; r < w.rows; ++r)
-          bulk_g2s_evict_first(smem_addr(codes + r * p.G * 16), src + r * row_bytes,
-                               (uint32_t)gl * 16, bar, pol);
-      }
-    }
-    if (p.whole) {
-      const long long b = (long long)w.row0 * p.Kg * 2;
-      const uint32_t n = copy_steps(steps, w.st_item, b, b + (long long)w.rows * p.Kg * 2,
-                                    st_total, bar, pol, issue);
-      if (!issue) tx = (uint32_t)(w.rows * row_bytes) + n;
-    } else {
-      if (!issue) tx = 0;
-      for (int r = 0; r < w.rows; ++r) {
-        const long long b = ((long long)(w.row0 + r) * p.Kg + g0) * 2;
-        const uint32_t n = copy_steps(steps + r * p.seg_stride, w.st_item, b, b + gl * 2,
-                                      st_total, bar, pol, issue);
-        if (!issue) tx += (uint32_t)gl * 16 + n;
-      }
-    }
-  }
-}
-
 // ---------------------------------------------------------------- activations
-// Stage activation rows as fp16 pairs, scaled by 2^e per group of 32 so that
-// the group's largest magnitude lies in [2^9, 2^10).  Layout per row m:
-// 16-byte chunk (w, g) = pairs (x[8w+p], x[8w+p+4]) for p = 0..3 of group g,
-// stored at ((m * 4 + w) * xg_max + g) * 16; the inverse scale 2^-e of the
-// group at xscale[m * xg_max + g].
-__device__ void stage_x(const GemvParams& p, int xrow0, int gbeg, int gend, uint8_t* xs,
-                        float* xscale) {
-  const int ng = gend - gbeg;
-  for (int idx = threadIdx.x; idx < p.MR * ng; idx += blockDim.x) {
-    const int m = idx / ng;
-    const int gi = idx - m * ng;
-    const uint4* src = reinterpret_cast<const uint4*>(p.x + (long long)(xrow0 + m) * p.K +
-                                                      (long long)(gbeg + gi) * 32);
+// Stage the activation rows of `nslots` items (or one shared row) as fp16
+// pairs scaled by 2^e per group of 32 so that the group's largest magnitude
+// lies in [2^9, 2^10).  Layout for staged row j (= slot * MR + m): 16-byte
+// chunk (w, g) = pairs (x[8w+p], x[8w+p+4]) for p = 0..3 of group g, at
+// ((j * 4 + w) * Kg + g) * 16; the inverse scale 2^-e of the group at
+// xscale[j * Kg + g].
+__device__ void stage_x(const GemvParams& p, int item0, int nslots, uint8_t* xs, float* xscale) {
+  const int rows = nslots * p.MR;
+  for (int idx = threadIdx.x; idx < rows * p.Kg; idx += kThreads) {
+    const int j = idx / p.Kg;
+    const int g = idx - j * p.Kg;
+    const int slot = j / p.MR, m = j - slot * p.MR;
+    const int xrow = (p.x_per_item ? (item0 + slot) * p.MR : 0) + m;
+    const uint4* src =
+        reinterpret_cast<const uint4*>(p.x + (long long)xrow * p.K + (long long)g * 32);
     uint4 v[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) v[i] = __ldg(src + i);
@@ -227,11 +117,10 @@ __device__ void stage_x(const GemvParams& p, int xrow0, int gbeg, int gend, uint
     const uint32_t* wv = reinterpret_cast<const uint32_t*>(v);
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-      // elements 8w .. 8w+7 are bf16 halves of words wv[4w .. 4w+3]
       float f[8];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const uint32_t pair = wv[4 * w + i];
+        const uint32_t pair = wv[4 * w + i];       // elements 8w+2i, 8w+2i+1
         f[2 * i] = __uint_as_float(pair << 16) * fa * fb;
         f[2 * i + 1] = __uint_as_float(pair & 0xFFFF0000u) * fa * fb;
       }
@@ -245,9 +134,9 @@ __device__ void stage_x(const GemvParams& p, int xrow0, int gbeg, int gend, uint
       out.z = *reinterpret_cast<uint32_t*>(&h);
       h = __floats2half2_rn(f[3], f[7]);
       out.w = *reinterpret_cast<uint32_t*>(&h);
-      *reinterpret_cast<uint4*>(xs + ((long long)(m * 4 + w) * p.xg_max + gi) * 16) = out;
+      *reinterpret_cast<uint4*>(xs + ((long long)(j * 4 + w) * p.Kg + g) * 16) = out;
     }
-    xscale[m * p.xg_max + gi] = inv;
+    xscale[(long long)j * p.Kg + g] = inv;
   }
 }
 
@@ -280,195 +169,295 @@ __device__ __forceinline__ float add_pair_f32(float c, __half2 v) {
   return d;
 }
 
-template <int MR>
-__device__ __forceinline__ void group_dot(uint4 q, const uint8_t* xg, int wstride, int mstride,
-                                          float stf, const float* sc, int sc_mstride,
-                                          float acc[MR]) {
+// Dot of one group (4 packed words) with one staged activation row.
+__device__ __forceinline__ float group_sum(const uint4 q, const uint4 xv[4]) {
   __half2 h[4][4];
   unpack_word(q.x, h[0]);
   unpack_word(q.y, h[1]);
   unpack_word(q.z, h[2]);
   unpack_word(q.w, h[3]);
+  __half2 a0 = u2h(0u), a1 = u2h(0u), a2 = u2h(0u), a3 = u2h(0u);
 #pragma unroll
-  for (int m = 0; m < MR; ++m) {
-    __half2 a0 = u2h(0u), a1 = u2h(0u), a2 = u2h(0u), a3 = u2h(0u);
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const uint4 xv = *reinterpret_cast<const uint4*>(xg + m * mstride + w * wstride);
-      a0 = __hfma2(h[w][0], u2h(xv.x), a0);
-      a1 = __hfma2(h[w][1], u2h(xv.y), a1);
-      a2 = __hfma2(h[w][2], u2h(xv.z), a2);
-      a3 = __hfma2(h[w][3], u2h(xv.w), a3);
+  for (int w = 0; w < 4; ++w) {
+    a0 = __hfma2(h[w][0], u2h(xv[w].x), a0);
+    a1 = __hfma2(h[w][1], u2h(xv[w].y), a1);
+    a2 = __hfma2(h[w][2], u2h(xv[w].z), a2);
+    a3 = __hfma2(h[w][3], u2h(xv[w].w), a3);
+  }
+  float gs = add_pair_f32(0.0f, a0);
+  gs = add_pair_f32(gs, a1);
+  gs = add_pair_f32(gs, a2);
+  return add_pair_f32(gs, a3);
+}
+
+__device__ __forceinline__ uint4 ldg_stream16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ldg_stream2(const void* p) {
+  unsigned short v;
+  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+// Lanes of one warp: ask L2 for the codes and steps of unit `u` (rows of the
+// unit's row block, groups of its K slice).  Ranges are clipped to 16-byte
+// lines inside the item's arrays; bytes outside them are simply not
+// prefetched.
+__device__ __forceinline__ void prefetch_unit(const GemvParams& p, int u, int lane) {
+  if (u >= p.U) return;
+  const int slice = u / p.B;
+  const int rb = u - slice * p.B;
+  const int item = rb / p.upi;
+  const int row0 = (rb - item * p.upi) * p.rows_per_unit;
+  const int rows = min(p.rows_per_unit, p.N - row0);
+  long long blk = item;
+  if (p.ids != nullptr) {
+    const int e = __ldg(p.ids + item);
+    if (e < 0 || e >= p.num_experts) return;
+    blk = e;
+  }
+  const uint8_t* qw = p.qw + (unsigned long long)blk * p.qw_item_stride;
+  const uint8_t* st = p.st + (unsigned long long)blk * p.st_item_stride;
+  const long long row_bytes = (long long)p.K / 2, st_row = (long long)p.Kg * 2;
+  const long long st_lim = ((long long)p.N * st_row) & ~15LL;
+  const int g0 = slice * p.cps * p.chunk;
+  const int g1 = min((slice + 1) * p.cps * p.chunk, p.Kg);
+  if (p.S == 1) {   // whole rows: one contiguous range each for codes and steps
+    if (lane == 0) {
+      prefetch_l2_bulk(qw + row0 * row_bytes, (uint32_t)(rows * row_bytes));
+      const long long b = (row0 * st_row) & ~15LL;
+      const long long e = min((((long long)(row0 + rows) * st_row) + 15) & ~15LL, st_lim);
+      if (e > b) prefetch_l2_bulk(st + b, (uint32_t)(e - b));
     }
-    float gs = add_pair_f32(0.0f, a0);
-    gs = add_pair_f32(gs, a1);
-    gs = add_pair_f32(gs, a2);
-    gs = add_pair_f32(gs, a3);
-    // gs * 2^-e is exact (power-of-two rescale), so the step multiply is the
-    // only rounding before the fp32 accumulate
-    acc[m] = fmaf(gs * sc[m * sc_mstride], stf, acc[m]);
+  } else if (lane < rows) {
+    const long long r = row0 + lane;
+    prefetch_l2_bulk(qw + r * row_bytes + (long long)g0 * 16, (uint32_t)(g1 - g0) * 16);
+    const long long b = (r * st_row + (long long)g0 * 2) & ~15LL;
+    const long long e = min((r * st_row + (long long)g1 * 2 + 15) & ~15LL, st_lim);
+    if (e > b) prefetch_l2_bulk(st + b, (uint32_t)(e - b));
   }
 }
 
 // ---------------------------------------------------------------- kernel
-template <int TEAM, int MR>
-__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ GemvParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* xs = smem;
-  float* xscale = reinterpret_cast<float*>(xs + (long long)MR * 4 * p.xg_max * 16);
-  uint8_t* stages =
-      smem + (((long long)MR * 4 * p.xg_max * 16 + (long long)MR * p.xg_max * 4 + 127) & ~127LL);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(stages + (long long)kStages * p.stage_bytes);
-  __shared__ int s_last;
+// A warp's position in its walk over (unit, step) pairs.  A step is one group
+// of each of the lane's R rows: group g = slice start + lane_in_team + i*team.
+struct Cursor {
+  int u;                // current unit (>= end when the walk is over)
+  int i, n;             // step in the unit, steps per lane in the unit
+  int g;                // this lane's group at step i
+  int item, rb, slice;
+  int row0;             // this lane's first row
+  const uint8_t* qbase; // codes of row0
+  const uint8_t* sbase; // steps of row0
 
-  const int tid = threadIdx.x;
-  const long long ub = (long long)blockIdx.x * p.U / gridDim.x;
-  const long long ue = (long long)(blockIdx.x + 1) * p.U / gridDim.x;
-
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(smem_addr(&bars[s]), 1);
-    mbar_init_fence();
+  // First unit at or after uu (stride kWarps) with a valid expert id.
+  __device__ void seek(const GemvParams& p, int uu, int ue, int lt, int set, int R, bool rep) {
+    for (u = uu; u < ue; u += kWarps) {
+      slice = u / p.B;
+      rb = u - slice * p.B;
+      item = rb / p.upi;
+      row0 = (rb - item * p.upi) * p.rows_per_unit + set * R;
+      long long blk = item;
+      if (p.ids != nullptr) {
+        const int e = __ldg(p.ids + item);
+        if (e < 0 || e >= p.num_experts) {   // leave this unit's rows unwritten
+          if (rep) report(p.status, W4_ERR_INDEX);
+          continue;
+        }
+        blk = e;
+      }
+      const int g0 = slice * p.cps * p.chunk;
+      const int g1 = min((slice + 1) * p.cps * p.chunk, p.Kg);
+      n = (g1 - g0) / p.team;
+      i = 0;
+      g = g0 + lt;
+      qbase = p.qw + (unsigned long long)blk * p.qw_item_stride + (long long)row0 * (p.K / 2);
+      sbase = p.st + (unsigned long long)blk * p.st_item_stride + (long long)row0 * (p.Kg * 2);
+      return;
+    }
   }
+  __device__ void advance(const GemvParams& p, int ue, int lt, int set, int R, bool rep) {
+    if (++i < n) {
+      g += p.team;
+      return;
+    }
+    seek(p, u + kWarps, ue, lt, set, R, rep);
+  }
+};
+
+// Load the codes and steps of cursor c's step into one register slot.
+template <int R>
+__device__ __forceinline__ void load_step(const GemvParams& p, const Cursor& c, uint4 code[R],
+                                          uint32_t sb[R]) {
+  const long long row_bytes = (long long)p.K / 2;
+  const int st_row = p.Kg * 2;
+#pragma unroll
+  for (int q = 0; q < R; ++q) {
+    if (c.row0 + q < p.N) {
+      code[q] = ldg_stream16(c.qbase + q * row_bytes + (long long)c.g * 16);
+      sb[q] = ldg_stream2(c.sbase + q * st_row + c.g * 2);
+    } else {   // rows past N: code 8 and step 0 contribute nothing
+      code[q] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+      sb[q] = 0;
+    }
+  }
+}
+
+constexpr int kPrefetchUnits = 2;   // units per warp requested into L2 before the PDL wait
+
+template <int R, int MR>
+__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ GemvParams p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int team = p.team;
+  const int set = lane / team;   // row set of this lane within the warp
+  const int lt = lane - set * team;
+  const int ub = (int)((long long)blockIdx.x * p.U / gridDim.x);
+  const int ue = (int)((long long)(blockIdx.x + 1) * p.U / gridDim.x);
+
+  // items whose activation rows this CTA needs (units are slice-major)
+  int item0 = 0, nslots = 1;
+  if (p.x_per_item) {
+    const int rb_lo = ub % p.B, rb_hi = (ue - 1) % p.B;
+    if (ue - ub >= p.B || rb_lo > rb_hi) {
+      item0 = 0;
+      nslots = p.n_items;
+    } else {
+      item0 = rb_lo / p.upi;
+      nslots = rb_hi / p.upi - item0 + 1;
+    }
+  }
+  uint8_t* xs = smem;
+  float* xscale = reinterpret_cast<float*>(smem + (long long)p.x_slots * MR * 4 * p.Kg * 16);
+
+  // Dense weights do not depend on earlier kernels: start pulling this warp's
+  // first units into L2 before waiting for the previous kernel (W4_FLAG_PDL).
+  if (p.ids == nullptr)
+    for (int d = 0; d < kPrefetchUnits; ++d)
+      if (ub + warp + d * kWarps < ue) prefetch_unit(p, ub + warp + d * kWarps, lane);
+  pdl_wait();                // activations, ids and outputs follow earlier kernels
+  pdl_launch_dependents();
+  if (ub < ue) stage_x(p, item0, nslots, xs, xscale);
   __syncthreads();
 
-  // The ids (routed experts) may be written by the previous kernel: read them
-  // only after it has completed.  Dense weights do not depend on earlier
-  // kernels, so their first tiles are requested before the wait.
-  if (p.ids != nullptr) pdl_wait();
-  Walk it;
-  it.init(p, ub, ue);
-  Walk iss = it;          // thread 0's issue cursor, kStages tiles ahead
-  long long issued = 0;
-  uint64_t pol = 0;
-  if (tid == 0) {
-    pol = policy_evict_first();
-    for (; issued < kStages && !iss.done(); ++issued, iss.next(p))
-      issue_tile(p, iss, stages + issued * p.stage_bytes, smem_addr(&bars[issued]), pol);
+  // compute cursor `cp` and load cursor `ld`, two steps ahead; register ring
+  // of three slots
+  Cursor cp, ld;
+  cp.seek(p, ub + warp, ue, lt, set, R, true);
+  ld = cp;
+  uint4 code[3][R];
+  uint32_t sb[3][R];
+  if (ld.u < ue) {
+    load_step<R>(p, ld, code[0], sb[0]);
+    ld.advance(p, ue, lt, set, R, false);
   }
-  if (p.ids == nullptr) pdl_wait();
-  // Let the next kernel in the stream (if launched with PDL) get scheduled as
-  // SMs free up: it can only start once every CTA of this grid has reached
-  // this point, and it waits for this grid's completion before reading our
-  // outputs.
-  pdl_launch_dependents();
+  if (ld.u < ue) {
+    load_step<R>(p, ld, code[1], sb[1]);
+    ld.advance(p, ue, lt, set, R, false);
+  }
 
-  const int team = tid / TEAM;   // row of the tile this lane works on
-  const int lane_t = tid % TEAM;
-  const int wstride = p.xg_max * 16;
-  const int mstride = 4 * p.xg_max * 16;
-
-  int cur_xrow = -1, cur_slice = -1, xg_base = 0;
-  float row_acc[MR];
+  float acc[R][MR], rowsum[R][MR];
 #pragma unroll
-  for (int m = 0; m < MR; ++m) row_acc[m] = 0.0f;
-
-  long long t = 0;
-  bool timed_out = false;
-  while (!it.done()) {
-    const int xrow = p.x_per_item ? it.item * p.MR : 0;
-    if (xrow != cur_xrow || it.slice != cur_slice) {
-      xg_base = (p.S == 1) ? 0 : it.slice * p.cps * p.G;
-      const int xg_end = (p.S == 1) ? p.Kg : min(p.Kg, (it.slice + 1) * p.cps * p.G);
-      stage_x(p, xrow, xg_base, xg_end, xs, xscale);
-      __syncthreads();
-      cur_xrow = xrow;
-      cur_slice = it.slice;
-    }
-    const int slot = (int)(t % kStages);
-    const uint32_t parity = (uint32_t)((t / kStages) & 1);
-    const bool ok = mbar_wait_bounded(smem_addr(&bars[slot]), parity, kWaitCycles);
-
-    const uint8_t* stage = stages + (long long)slot * p.stage_bytes;
-    const int g0 = it.g0(p);
-    const int gl = it.glen(p);
-    const bool first_chunk = it.c == it.slice * p.cps;
-    const bool last_chunk = it.c + 1 == it.c_end;
-    if (first_chunk) {
+  for (int q = 0; q < R; ++q)
 #pragma unroll
-      for (int m = 0; m < MR; ++m) row_acc[m] = 0.0f;
-    }
-    float cs[MR];
+    for (int m = 0; m < MR; ++m) acc[q][m] = rowsum[q][m] = 0.0f;
+
+  while (cp.u < ue) {
 #pragma unroll
-    for (int m = 0; m < MR; ++m) cs[m] = 0.0f;
-    if (ok && team < it.rows) {
-      const uint8_t* codes = stage + (long long)team * p.G * 16;
-      long long st_first;
-      const uint8_t* steps;
-      if (p.whole) {
-        st_first = (long long)it.row0 * p.Kg * 2;
-        steps = stage + p.stage_codes + (st_first & 15) + (long long)team * p.Kg * 2;
-      } else {
-        st_first = ((long long)(it.row0 + team) * p.Kg + g0) * 2;
-        steps = stage + p.stage_codes + (long long)team * p.seg_stride + (st_first & 15);
+    for (int k = 0; k < 3; ++k) {
+      if (cp.u >= ue) break;
+      if (ld.u < ue) {   // refill the slot freed by the previous step
+        load_step<R>(p, ld, code[(k + 2) % 3], sb[(k + 2) % 3]);
+        ld.advance(p, ue, lt, set, R, false);
       }
-      const uint8_t* xg = xs + (long long)(g0 - xg_base) * 16;
-      const float* sc = xscale + (g0 - xg_base);
-#pragma unroll 2
-      for (int g = lane_t; g < gl; g += TEAM) {
-        const uint4 q = *reinterpret_cast<const uint4*>(codes + g * 16);
-        const uint32_t sb = *reinterpret_cast<const uint16_t*>(steps + g * 2);
-        group_dot<MR>(q, xg + g * 16, wstride, mstride, bf16_bits_to_float(sb), sc + g,
-                      p.xg_max, cs);
+      const int xslot = p.x_per_item ? cp.item - item0 : 0;
+      const uint8_t* xrow = xs + (long long)xslot * MR * 4 * p.Kg * 16;
+      const float* srow = xscale + (long long)xslot * MR * p.Kg;
+#pragma unroll
+      for (int m = 0; m < MR; ++m) {
+        uint4 xv[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+          xv[w] = *reinterpret_cast<const uint4*>(xrow + ((long long)(m * 4 + w) * p.Kg + cp.g) * 16);
+        const float sc = srow[(long long)m * p.Kg + cp.g];
+#pragma unroll
+        for (int q = 0; q < R; ++q)
+          acc[q][m] = fmaf(group_sum(code[k][q], xv) * sc, bf16_bits_to_float(sb[k][q]), acc[q][m]);
       }
-    }
-    // team reduction, fixed xor tree
+      const bool unit_end = cp.i + 1 == cp.n;
+      if (unit_end || (cp.i + 1) % kChunkPerLane == 0) {
+        // chunk sum: fixed xor tree over the team
 #pragma unroll
-    for (int m = 0; m < MR; ++m) {
+        for (int q = 0; q < R; ++q)
 #pragma unroll
-      for (int off = TEAM / 2; off > 0; off >>= 1) cs[m] += __shfl_xor_sync(0xffffffffu, cs[m], off);
-    }
-    const bool writer = ok && lane_t == 0 && team < it.rows;
-    if (p.S == 1) {
+          for (int m = 0; m < MR; ++m)
+            for (int off = team >> 1; off > 0; off >>= 1)
+              acc[q][m] += __shfl_xor_sync(0xffffffffu, acc[q][m], off);
+        if (p.S == 1) {
 #pragma unroll
-      for (int m = 0; m < MR; ++m) row_acc[m] += cs[m];
-      if (last_chunk && writer) {
+          for (int q = 0; q < R; ++q)
 #pragma unroll
-        for (int m = 0; m < MR; ++m)
-          p.y[((long long)it.item * p.MR + m) * p.N + it.row0 + team] =
-              __float2bfloat16_rn(row_acc[m]);
-      }
-    } else if (writer) {
-      float* dst = p.ws_partial + ((it.rb * p.nch + it.c) * p.tile_rows + team) * p.MR;
+            for (int m = 0; m < MR; ++m) rowsum[q][m] += acc[q][m];
+        } else if (lt == 0) {
+          const int c = cp.slice * p.cps + cp.i / kChunkPerLane;
+          float* dst = p.ws_partial +
+                       (((long long)cp.rb * p.nch + c) * p.rows_per_unit + set * R) * MR;
 #pragma unroll
-      for (int m = 0; m < MR; ++m) dst[m] = cs[m];
-      __threadfence();
-    }
-    timed_out = __syncthreads_or(!ok) != 0;
-    if (timed_out) break;
-
-    if (p.S > 1 && last_chunk) {
-      if (tid == 0) {
-        const int old = atomicAdd(p.ws_count + it.rb, 1);
-        s_last = (old == p.S - 1);
-      }
-      __syncthreads();
-      if (s_last) {
-        __threadfence();
-        const float* src = p.ws_partial + it.rb * p.nch * p.tile_rows * p.MR;
-        for (int i = tid; i < it.rows * p.MR; i += kThreads) {
-          const int r = i / p.MR, m = i - r * p.MR;
-          float v = 0.0f;
-          for (int c = 0; c < p.nch; ++c) v += __ldcg(src + ((long long)c * p.tile_rows + r) * p.MR + m);
-          p.y[((long long)it.item * p.MR + m) * p.N + it.row0 + r] = __float2bfloat16_rn(v);
+          for (int q = 0; q < R; ++q)
+#pragma unroll
+            for (int m = 0; m < MR; ++m) dst[q * MR + m] = acc[q][m];
         }
-        if (tid == 0) atomicExch(p.ws_count + it.rb, 0);
+#pragma unroll
+        for (int q = 0; q < R; ++q)
+#pragma unroll
+          for (int m = 0; m < MR; ++m) acc[q][m] = 0.0f;
       }
-    }
-
-    if (tid == 0 && !iss.done()) {
-      issue_tile(p, iss, stages + (long long)slot * p.stage_bytes, smem_addr(&bars[slot]), pol);
-      ++issued;
-      iss.next(p);
-    }
-    it.next(p);
-    ++t;
-  }
-  if (timed_out) {
-    report(p.status, W4_ERR_TIMEOUT);
-    if (tid == 0) {   // let this CTA's copies in flight land before leaving
-      for (long long k = t; k < issued; ++k)
-        mbar_wait_bounded(smem_addr(&bars[k % kStages]), (uint32_t)((k / kStages) & 1),
-                          kWaitCycles);
+      if (unit_end) {
+        if (p.S == 1) {
+          if (lt == 0) {
+#pragma unroll
+            for (int q = 0; q < R; ++q)
+              if (cp.row0 + q < p.N)
+#pragma unroll
+                for (int m = 0; m < MR; ++m)
+                  p.y[((long long)cp.item * MR + m) * p.N + cp.row0 + q] =
+                      __float2bfloat16_rn(rowsum[q][m]);
+          }
+#pragma unroll
+          for (int q = 0; q < R; ++q)
+#pragma unroll
+            for (int m = 0; m < MR; ++m) rowsum[q][m] = 0.0f;
+        } else {
+          // the last warp to finish this row block adds the chunk sums in
+          // chunk order, writes the rows and re-arms the counter
+          __threadfence();
+          __syncwarp();
+          int last = 0;
+          if (lane == 0) last = atomicAdd(p.ws_count + cp.rb, 1) == p.S - 1;
+          last = __shfl_sync(0xffffffffu, last, 0);
+          if (last) {
+            __threadfence();
+            const int rbase = (cp.rb - cp.item * p.upi) * p.rows_per_unit;
+            const float* src = p.ws_partial + (long long)cp.rb * p.nch * p.rows_per_unit * MR;
+            for (int e = lane; e < p.rows_per_unit * MR; e += 32) {
+              const int r = e / MR, m = e - r * MR;
+              if (rbase + r >= p.N) continue;
+              float v = 0.0f;
+              for (int c = 0; c < p.nch; ++c)
+                v += __ldcg(src + ((long long)c * p.rows_per_unit + r) * MR + m);
+              p.y[((long long)cp.item * MR + m) * p.N + rbase + r] = __float2bfloat16_rn(v);
+            }
+            if (lane == 0) atomicExch(p.ws_count + cp.rb, 0);
+          }
+        }
+      }
+      cp.advance(p, ue, lt, set, R, true);
     }
   }
 }
@@ -500,129 +489,85 @@ DeviceInfo device_info(int dev) {
   return cache[dev];
 }
 
-struct Tiling {
-  int team = 32;
-  int tile_rows = 16;
-  int G = 0;
-  int nch = 1;
-  int whole = 1;
-  int stage_codes = 0, stage_steps = 0, seg_stride = 0, stage_bytes = 0;
-};
-
-inline long long align16(long long v) { return (v + 15) & ~15LL; }
-
-Tiling make_tiling(int K) {
-  const int Kg = K / 32;
-  Tiling best;
-  double best_score = -1.0;
-  const int teams[3] = {32, 16, 8};
-  for (int ti = 0; ti < 3; ++ti) {
-    const int team = teams[ti];
-    const int rows = kThreads / team;
-    for (int u = 1; u <= 64; ++u) {
-      int G = team * u;
-      const bool whole = G >= Kg;
-      if (whole) G = Kg;
-      const int nch = whole ? 1 : (Kg + G - 1) / G;
-      const int glast = Kg - (nch - 1) * G;
-      const long long slots = (long long)team * ((long long)(nch - 1) * ((G + team - 1) / team) +
-                                                 (glast + team - 1) / team);
-      const double util = (double)Kg / (double)slots;
-      Tiling t;
-      t.team = team;
-      t.tile_rows = rows;
-      t.G = G;
-      t.nch = nch;
-      t.whole = whole ? 1 : 0;
-      t.stage_codes = rows * G * 16;
-      t.seg_stride = (int)(whole ? align16((long long)rows * Kg * 2 + 32) : align16(G * 2 + 32));
-      t.stage_steps = whole ? t.seg_stride : rows * t.seg_stride;
-      t.stage_bytes = t.stage_codes + t.stage_steps;
-      const double kb = t.stage_bytes / 1024.0;
-      const bool fits = kb <= 40.0;
-      if (fits) {
-        // utilisation first; then stages of 16-32 KB; then whole rows
-        double score = util * 100.0;
-        score -= (kb < 16.0) ? (16.0 - kb) * 0.15 : 0.0;
-        score -= (kb > 32.0) ? (kb - 32.0) * 0.15 : 0.0;
-        score += whole ? 0.5 : 0.0;
-        score -= (double)(whole ? 0 : rows) * 0.01;   // one bulk copy per row segment
-        if (score > best_score) {
-          best_score = score;
-          best = t;
-        }
-      }
-      if (whole) break;
-    }
-  }
-  if (best_score < 0) {   // no stage under the cap: smallest chunks of one warp per row
-    Tiling t;
-    t.team = 32;
-    t.tile_rows = kThreads / 32;
-    t.G = 32;
-    t.nch = (Kg + 31) / 32;
-    t.whole = (t.nch == 1) ? 1 : 0;
-    if (t.whole) t.G = Kg;
-    t.stage_codes = t.tile_rows * t.G * 16;
-    t.seg_stride = (int)(t.whole ? align16((long long)t.tile_rows * Kg * 2 + 32) : align16(t.G * 2 + 32));
-    t.stage_steps = t.whole ? t.seg_stride : t.tile_rows * t.seg_stride;
-    t.stage_bytes = t.stage_codes + t.stage_steps;
-    best = t;
-  }
-  return best;
-}
-
 struct Plan {
-  Tiling t;
   int MR = 1;
-  int S = 1, cps = 1, bpi = 1;
+  int team = 32, sets = 1, R = 1, rows_per_unit = 1;
+  int chunk = 0, nch = 1;
+  int S = 1, cps = 1, upi = 1;
   long long B = 0, U = 0;
-  int xg_max = 0;
+  int x_slots = 1;
   int ctas = 0;
   long long smem = 0;
   size_t ws_bytes = 0;
   size_t ws_part_off = 0;
 };
 
-long long smem_for(const Tiling& t, int MR, int xg_max) {
-  long long x = (long long)MR * 4 * xg_max * 16 + (long long)MR * xg_max * 4;
-  x = (x + 127) & ~127LL;
-  return x + (long long)kStages * t.stage_bytes + kStages * 8;
+// The per-row arithmetic (team, chunk) comes from K alone.
+void row_shape(int K, int* team, int* chunk, int* nch) {
+  // largest power of two <= 32 that divides K/32 and still leaves each lane
+  // at least kChunkPerLane groups of a row (fewer, longer lane loops amortise
+  // the per-row reduction)
+  const int Kg = K / 32;
+  int t = 1;
+  while (t < 32 && Kg % (2 * t) == 0 && Kg / (2 * t) >= kChunkPerLane) t *= 2;
+  *team = t;
+  *chunk = t * kChunkPerLane;
+  *nch = (Kg + *chunk - 1) / *chunk;
 }
 
-// Plan for `rows_items` items of N rows, MR activation rows per item.
-bool make_plan(int MR, int N, int K, int n_items, int allow_split, const DeviceInfo& di, Plan* out) {
+long long x_bytes(int slots, int MR, int Kg) {
+  return (long long)slots * MR * Kg * (64 + 4);
+}
+
+bool make_plan(int MR, int N, int K, int n_items, int allow_split, int x_per_item,
+               const DeviceInfo& di, Plan* out) {
   Plan pl;
-  pl.t = make_tiling(K);
   pl.MR = MR;
   const int Kg = K / 32;
-  pl.bpi = (N + pl.t.tile_rows - 1) / pl.t.tile_rows;
-  pl.B = (long long)n_items * pl.bpi;
+  row_shape(K, &pl.team, &pl.chunk, &pl.nch);
+  pl.sets = 32 / pl.team;
   const int sms = di.sms > 0 ? di.sms : 1;
-  int S = 1;
-  if (allow_split && pl.t.nch > 1 && pl.B < 8LL * sms)
-    S = (int)std::min<long long>(pl.t.nch, (8LL * sms + pl.B - 1) / pl.B);
-  while (true) {
-    const int cps = (pl.t.nch + S - 1) / S;
-    S = (pl.t.nch + cps - 1) / cps;
-    const int xg = (S == 1) ? Kg : std::min(Kg, cps * pl.t.G);
-    const long long sm = smem_for(pl.t, MR, xg);
-    if (sm <= di.smem_optin || di.smem_optin == 0) {
-      pl.S = S;
-      pl.cps = cps;
-      pl.xg_max = xg;
-      pl.smem = sm;
-      break;
-    }
-    if (!allow_split || S >= pl.t.nch) return false;
-    ++S;
+  const long long warps = (long long)sms * kWarps;
+  const long long want = 6 * warps;       // units for a balanced split over warps
+  // rows per lane: as many as keep enough units (activation reuse), fewer
+  // with several activation rows (registers)
+  int R = (MR == 1) ? 4 : (MR == 2 ? 2 : 1);
+  while (R > 1) {
+    const long long rpu = (long long)pl.sets * R;
+    if ((long long)n_items * ((N + rpu - 1) / rpu) >= want) break;
+    R >>= 1;
   }
+  pl.R = R;
+  pl.rows_per_unit = pl.sets * R;
+  pl.upi = (N + pl.rows_per_unit - 1) / pl.rows_per_unit;
+  pl.B = (long long)n_items * pl.upi;
+  if (pl.B > (1LL << 30)) return false;
+  int S = 1;
+  if (allow_split && pl.nch > 1 && pl.B < want)
+    S = (int)std::min<long long>(pl.nch, (want + pl.B - 1) / pl.B);
+  pl.cps = (pl.nch + S - 1) / S;
+  pl.S = (pl.nch + pl.cps - 1) / pl.cps;
   pl.U = (long long)pl.S * pl.B;
+  if (pl.U > (1LL << 30)) return false;
   pl.ctas = (int)std::min<long long>(pl.U, sms);
+  // activation rows a CTA stages: one, or the items its unit range touches
+  pl.x_slots = 1;
+  if (x_per_item) {
+    for (int c = 0; c < pl.ctas; ++c) {
+      const long long ub = (long long)c * pl.U / pl.ctas, ue = (long long)(c + 1) * pl.U / pl.ctas;
+      if (ue <= ub) continue;
+      const long long lo = ub % pl.B, hi = (ue - 1) % pl.B;
+      const long long n = (ue - ub >= pl.B || lo > hi) ? n_items : hi / pl.upi - lo / pl.upi + 1;
+      pl.x_slots = (int)std::max<long long>(pl.x_slots, n);
+    }
+  }
+  pl.smem = x_bytes(pl.x_slots, MR, Kg);
+  const long long smem_max = di.smem_optin > 0 ? di.smem_optin : 232448;
+  if (pl.smem > smem_max) return false;
   if (pl.S > 1) {
     // counters first, so every plan of the same shape (any MR) finds them at
     // the same place; chunk partials after them
-    const size_t part = (size_t)pl.B * pl.t.nch * pl.t.tile_rows * MR * sizeof(float);
+    const size_t part = (size_t)pl.B * pl.nch * pl.rows_per_unit * MR * sizeof(float);
     pl.ws_part_off = ((size_t)pl.B * sizeof(int) + 255) & ~size_t(255);
     pl.ws_bytes = pl.ws_part_off + part;
   }
@@ -630,11 +575,11 @@ bool make_plan(int MR, int N, int K, int n_items, int allow_split, const DeviceI
   return true;
 }
 
-template <int TEAM, int MR>
+template <int R, int MR>
 cudaError_t launch_one(const GemvParams& prm, const Plan& pl, bool pdl, cudaStream_t stream, int dev) {
   static std::mutex mu;
   static long long attr_bytes[64] = {};
-  auto kern = gemv_kernel<TEAM, MR>;
+  auto kern = gemv_kernel<R, MR>;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   {
     // raise the kernel's dynamic shared-memory limit to what this plan needs
@@ -659,21 +604,16 @@ cudaError_t launch_one(const GemvParams& prm, const Plan& pl, bool pdl, cudaStre
   return cudaLaunchKernelEx(&cfg, kern, prm);
 }
 
-template <int TEAM>
-cudaError_t launch_team(const GemvParams& prm, const Plan& pl, bool pdl, cudaStream_t s, int dev) {
-  switch (pl.MR) {
-    case 1: return launch_one<TEAM, 1>(prm, pl, pdl, s, dev);
-    case 2: return launch_one<TEAM, 2>(prm, pl, pdl, s, dev);
-    case 3: return launch_one<TEAM, 3>(prm, pl, pdl, s, dev);
-    default: return launch_one<TEAM, 4>(prm, pl, pdl, s, dev);
-  }
-}
-
 cudaError_t launch(const GemvParams& prm, const Plan& pl, bool pdl, cudaStream_t s, int dev) {
-  switch (pl.t.team) {
-    case 8: return launch_team<8>(prm, pl, pdl, s, dev);
-    case 16: return launch_team<16>(prm, pl, pdl, s, dev);
-    default: return launch_team<32>(prm, pl, pdl, s, dev);
+  switch (pl.MR * 8 + pl.R) {
+    case 8 + 4: return launch_one<4, 1>(prm, pl, pdl, s, dev);
+    case 8 + 2: return launch_one<2, 1>(prm, pl, pdl, s, dev);
+    case 8 + 1: return launch_one<1, 1>(prm, pl, pdl, s, dev);
+    case 16 + 2: return launch_one<2, 2>(prm, pl, pdl, s, dev);
+    case 16 + 1: return launch_one<1, 2>(prm, pl, pdl, s, dev);
+    case 24 + 1: return launch_one<1, 3>(prm, pl, pdl, s, dev);
+    case 32 + 1: return launch_one<1, 4>(prm, pl, pdl, s, dev);
+    default: return cudaErrorInvalidConfiguration;
   }
 }
 
@@ -683,20 +623,18 @@ GemvParams base_params(const Plan& pl, int N, int K) {
   p.K = K;
   p.Kg = K / 32;
   p.MR = pl.MR;
-  p.tile_rows = pl.t.tile_rows;
-  p.G = pl.t.G;
-  p.nch = pl.t.nch;
-  p.whole = pl.t.whole;
+  p.team = pl.team;
+  p.sets = pl.sets;
+  p.R = pl.R;
+  p.rows_per_unit = pl.rows_per_unit;
+  p.chunk = pl.chunk;
+  p.nch = pl.nch;
   p.S = pl.S;
   p.cps = pl.cps;
-  p.bpi = pl.bpi;
-  p.B = pl.B;
-  p.U = pl.U;
-  p.xg_max = pl.xg_max;
-  p.stage_codes = pl.t.stage_codes;
-  p.stage_steps = pl.t.stage_steps;
-  p.seg_stride = pl.t.seg_stride;
-  p.stage_bytes = pl.t.stage_bytes;
+  p.upi = pl.upi;
+  p.B = (int)pl.B;
+  p.U = (int)pl.U;
+  p.x_slots = pl.x_slots;
   return p;
 }
 
@@ -711,6 +649,56 @@ bool current_device(int* dev, DeviceInfo* di) {
   return di->sms > 0;
 }
 
+void planning_device(DeviceInfo* di) {
+  int dev = 0;
+  if (!current_device(&dev, di)) {
+    di->sms = 152;              // planning without a device: GB300 figures
+    di->smem_optin = 232448;
+  }
+}
+
+// Plans are cached per shape: planning is cheap but not free, and decode
+// loops call the same few shapes over and over.
+struct PlanKey {
+  int MR, N, K, n_items, split, xpi, sms;
+  bool operator==(const PlanKey& o) const {
+    return MR == o.MR && N == o.N && K == o.K && n_items == o.n_items && split == o.split &&
+           xpi == o.xpi && sms == o.sms;
+  }
+};
+
+bool cached_plan(int MR, int N, int K, int n_items, int split, int xpi, const DeviceInfo& di,
+                 Plan* out) {
+  static std::mutex mu;
+  static PlanKey keys[256];
+  static Plan plans[256];
+  static int used = 0, next = 0;
+  const PlanKey k{MR, N, K, n_items, split, xpi, di.sms};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+      if (keys[i] == k) {
+        *out = plans[i];
+        return true;
+      }
+  }
+  if (!make_plan(MR, N, K, n_items, split, xpi, di, out)) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  keys[next] = k;
+  plans[next] = *out;
+  next = (next + 1) % 256;
+  used = std::min(used + 1, 256);
+  return true;
+}
+
+// Activation rows per launch: up to kMaxMR, as many as fit shared memory.
+int max_rows_per_launch(int K, const DeviceInfo& di) {
+  const long long smem_max = di.smem_optin > 0 ? di.smem_optin : 232448;
+  int mr = kMaxMR;
+  while (mr > 0 && x_bytes(1, mr, K / 32) > smem_max) --mr;
+  return mr;
+}
+
 }  // namespace
 }  // namespace w4
 
@@ -720,22 +708,19 @@ using namespace w4;
 extern "C" w4_status w4a16_gemv_plan(int M, int N, int K, w4_plan_info* info) {
   if (info == nullptr || M < 1 || N < 1) return W4_ERR_ARG;
   if (M > W4_MAX_M || K < 32 || K % 32 != 0 || K > W4_MAX_K) return W4_ERR_SHAPE;
-  int dev = 0;
   DeviceInfo di;
-  if (!current_device(&dev, &di)) {
-    di.sms = 152;              // planning without a device: GB300 figures
-    di.smem_optin = 232448;
-  }
+  planning_device(&di);
   Plan pl;
-  if (!make_plan(std::min(M, kMaxMR), N, K, 1, 1, di, &pl)) return W4_ERR_SHAPE;
+  const int mr_cap = max_rows_per_launch(K, di);
+  if (mr_cap < 1 || !cached_plan(std::min(M, mr_cap), N, K, 1, 1, 0, di, &pl)) return W4_ERR_SHAPE;
   info->path = 0;
   info->ctas = pl.ctas;
   info->slices = pl.S;
   info->threads = kThreads;
-  info->team = pl.t.team;
-  info->tile_rows = pl.t.tile_rows;
-  info->tile_groups = pl.t.G;
-  info->stages = kStages;
+  info->team = pl.team;
+  info->unit_rows = pl.rows_per_unit;
+  info->chunk_groups = pl.chunk;
+  info->rows_per_lane = pl.R;
   info->smem_bytes = (int)pl.smem;
   info->rows_per_call = pl.MR;
   return W4_OK;
@@ -743,15 +728,17 @@ extern "C" w4_status w4a16_gemv_plan(int M, int N, int K, w4_plan_info* info) {
 
 extern "C" size_t w4a16_gemv_workspace_bytes(int M, int N, int K) {
   if (M < 1 || N < 1 || M > W4_MAX_M || K < 32 || K % 32 != 0 || K > W4_MAX_K) return 0;
-  int dev = 0;
   DeviceInfo di;
-  if (!current_device(&dev, &di)) {
-    di.sms = 152;
-    di.smem_optin = 232448;
-  }
+  planning_device(&di);
   Plan pl;
-  if (!make_plan(std::min(M, kMaxMR), N, K, 1, 1, di, &pl)) return 0;
-  return pl.ws_bytes;
+  const int mr_cap = max_rows_per_launch(K, di);
+  if (mr_cap < 1 || !cached_plan(std::min(M, mr_cap), N, K, 1, 1, 0, di, &pl)) return 0;
+  size_t ws = pl.ws_bytes;
+  for (int mr = 1; mr < std::min(M, mr_cap); ++mr) {   // smaller tail launches
+    Plan pm;
+    if (cached_plan(mr, N, K, 1, 1, 0, di, &pm)) ws = std::max(ws, pm.ws_bytes);
+  }
+  return ws;
 }
 
 extern "C" w4_status w4a16_gemv(void* y, const void* qw, const void* st, const void* x, int M,
@@ -765,16 +752,16 @@ extern "C" w4_status w4a16_gemv(void* y, const void* qw, const void* st, const v
   int dev = 0;
   DeviceInfo di;
   if (!current_device(&dev, &di)) return W4_ERR_DEVICE;
-  Plan pl;
-  if (!make_plan(std::min(M, kMaxMR), N, K, 1, 1, di, &pl)) return W4_ERR_SHAPE;
-  if (pl.ws_bytes > 0 && (workspace == nullptr || workspace_bytes < pl.ws_bytes))
-    return W4_ERR_WORKSPACE;
-  if (pl.ws_bytes > 0 && !aligned(workspace, 16)) return W4_ERR_ALIGN;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  for (int m0 = 0; m0 < M; m0 += kMaxMR) {
-    const int mr = std::min(kMaxMR, M - m0);
-    Plan pm = pl;
-    if (mr != pl.MR && !make_plan(mr, N, K, 1, 1, di, &pm)) return W4_ERR_SHAPE;
+  const int mr_cap = max_rows_per_launch(K, di);
+  if (mr_cap < 1) return W4_ERR_SHAPE;
+  for (int m0 = 0; m0 < M; m0 += mr_cap) {
+    const int mr = std::min(mr_cap, M - m0);
+    Plan pm;
+    if (!cached_plan(mr, N, K, 1, 1, 0, di, &pm)) return W4_ERR_SHAPE;
+    if (pm.ws_bytes > 0 && (workspace == nullptr || workspace_bytes < pm.ws_bytes))
+      return W4_ERR_WORKSPACE;
+    if (pm.ws_bytes > 0 && !aligned(workspace, 16)) return W4_ERR_ALIGN;
     GemvParams p = base_params(pm, N, K);
     p.qw = static_cast<const uint8_t*>(qw);
     p.st = static_cast<const uint8_t*>(st);
@@ -815,8 +802,9 @@ extern "C" w4_status w4a16_gemv_id(void* y, const void* qw_base, size_t qw_strid
   int dev = 0;
   DeviceInfo di;
   if (!current_device(&dev, &di)) return W4_ERR_DEVICE;
+  const int xpi = (x_rows == n_ids && n_ids > 1) ? 1 : 0;
   Plan pl;
-  if (!make_plan(1, N, K, n_ids, 0, di, &pl)) return W4_ERR_SHAPE;
+  if (!cached_plan(1, N, K, n_ids, 0, xpi, di, &pl)) return W4_ERR_SHAPE;
   GemvParams p = base_params(pl, N, K);
   p.qw = static_cast<const uint8_t*>(qw_base);
   p.st = static_cast<const uint8_t*>(st_base);
@@ -825,7 +813,7 @@ extern "C" w4_status w4a16_gemv_id(void* y, const void* qw_base, size_t qw_strid
   p.ids = ids;
   p.num_experts = num_experts;
   p.x = static_cast<const __nv_bfloat16*>(x);
-  p.x_per_item = (x_rows == n_ids && n_ids > 1) ? 1 : 0;
+  p.x_per_item = xpi;
   p.y = static_cast<__nv_bfloat16*>(y);
   p.n_items = n_ids;
   p.status = status_dev;

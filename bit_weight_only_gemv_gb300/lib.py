@@ -37,8 +37,8 @@ class W4Error(RuntimeError):
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("path", "ctas", "slices", "threads", "team",
-                                            "tile_rows", "tile_groups", "stages", "smem_bytes",
-                                            "rows_per_call")]
+                                            "unit_rows", "chunk_groups", "rows_per_lane",
+                                            "smem_bytes", "rows_per_call")]
 
 
 _lib = None

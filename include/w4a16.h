@@ -269,13 +269,13 @@ void w4_slot_pool_stats(const w4_slot_pool *pool, long long *requests, long long
  */
 typedef struct w4_plan_info {
     int path;           /* 0 = CUDA-core packed-fp16 kernel */
-    int ctas;           /* CTAs launched */
+    int ctas;           /* CTAs launched (at most one per SM) */
     int slices;         /* K slices (split-K); 1 = none */
     int threads;        /* threads per CTA */
     int team;           /* lanes that share one output row */
-    int tile_rows;      /* rows per pipeline stage */
-    int tile_groups;    /* 32-code groups per row per stage */
-    int stages;         /* pipeline depth */
+    int unit_rows;      /* output rows of one warp work unit */
+    int chunk_groups;   /* 32-code groups per K chunk of the row reduction */
+    int rows_per_lane;  /* rows a lane works on together (activation reuse) */
     int smem_bytes;     /* dynamic shared memory per CTA */
     int rows_per_call;  /* activation rows handled per launch */
 } w4_plan_info;

@@ -79,12 +79,14 @@ def test_host_validation_rejects_before_any_launch(L):
                                    (3, 100, 65536)])
 def test_plan_is_valid(M, N, K):
     p = lib.plan(M, N, K)
-    assert p["threads"] == 512 and p["stages"] == 4
-    assert p["team"] in (8, 16, 32)
-    assert p["tile_rows"] * p["team"] == 512
+    assert p["threads"] == 512
+    assert p["team"] in (1, 2, 4, 8, 16, 32) and (K // 32) % p["team"] == 0
+    assert p["rows_per_lane"] in (1, 2, 4)
+    assert p["unit_rows"] == (32 // p["team"]) * p["rows_per_lane"]
+    assert p["chunk_groups"] == 8 * p["team"]
     assert 1 <= p["ctas"] <= 152
     assert p["smem_bytes"] <= 232448
-    assert p["rows_per_call"] == min(M, 4)
+    assert p["rows_per_call"] == min(M, 4 if K <= 16384 else 1)
     ws = lib.workspace_bytes(M, N, K)
     assert (ws > 0) == (p["slices"] > 1)
 
@@ -95,7 +97,7 @@ def test_tiling_depends_on_k_only():
         ref = lib.plan(1, 4096, K)
         for N in (16, 704, 2048, 100000):
             p = lib.plan(1, N, K)
-            assert (p["team"], p["tile_groups"]) == (ref["team"], ref["tile_groups"])
+            assert (p["team"], p["chunk_groups"]) == (ref["team"], ref["chunk_groups"])
 
 
 def test_slot_pool_matches_oracle_policy():
