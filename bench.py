@@ -1,0 +1,552 @@
+#!/usr/bin/env python3
+"""Benchmark: batch-1 decode pass of a 35-layer W4A16 decoder (hidden 2048).
+
+One step = one decode pass over the whole hot path, replayed as one CUDA
+graph: embed-row gather (tied 262144 x 2048 table), per-layer-table row gather
+(262144 x 35*256), for each of 35 layers the q/k/v (2048/512/512 x 2048), o
+(2048 x 2048), gate/up (8192 x 2048) and down (2048 x 8192) GEMVs, and the
+lm_head GEMV over the tied table (262144 x 2048); 248 kernels, chained with
+programmatic dependent launch.  All weights and activations are seeded
+synthetic data (uniform codes, |N(0,1)|*0.02/8 steps, N(0,1) activations);
+each layer's q/k/v share one activation row and gate/up share another.  A pass
+reads 1.50 GB of packed weights, more than the 129 MB L2, so every step streams
+from HBM.
+
+Prints one JSON line (see --help).  `--impl reference` times the fp64 CPU
+oracle instead, on a bounded sample of the same pass.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from bit_weight_only_gemv_gb300 import metrics, synth  # noqa: E402
+
+METRIC = "W4A16 GEMV HBM GB/s and % of GB300 peak; decode-equivalent tok/s at batch 1"
+UNIT = "tok/s"
+NOMINAL_HBM_GBPS = 8000.0
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+
+
+# ------------------------------------------------------------------ helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK["hbm_gbs"], "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, period_ms: int = 100):
+        self.index, self.period = index, period_ms
+        self.proc = None
+        self.path = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.period)],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, flags in rows for i, f in enumerate(flags)
+                          if f.lower() == "active"})
+        sm = sorted(r[0] for r in rows)
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ workload
+class DecodePass:
+    """Device-resident weights, inputs and outputs of one decode pass."""
+
+    def __init__(self, model: synth.DenseDecoder, device, seed: int = 0, merge: bool = True):
+        from bit_weight_only_gemv_gb300 import lib
+        self.lib = lib
+        self.model = model
+        self.dev = device
+        self.merge = merge
+        h, V = model.hidden, model.vocab
+        s = seed
+        # tied embed / lm_head table and the per-layer table
+        self.emb_qw = synth.torch_words((V, h // 8), synth.seed_of(s, 1), device)
+        self.emb_st = synth.torch_steps((V, h // 32), synth.seed_of(s, 2), device)
+        pw = model.per_layer_width
+        self.ple_qw = synth.torch_words((V, pw // 8), synth.seed_of(s, 3), device)
+        self.ple_st = synth.torch_steps((V, pw // 32), synth.seed_of(s, 4), device)
+        # weight matrices per layer; projections that read the same activation
+        # (q/k/v, gate/up) are stored as one row-concatenated matrix when merged
+        groups = []
+        for pr in model.projs:
+            if merge and groups and groups[-1][0] == pr.x_key and groups[-1][1][0].k == pr.k:
+                groups[-1][1].append(pr)
+            else:
+                groups.append((pr.x_key, [pr]))
+        self.mats = []   # (layer, name, n, k, x_key, qw, st)
+        for li in range(model.layers):
+            for gi, (xk, prs) in enumerate(groups):
+                n = sum(p.n for p in prs)
+                k = prs[0].k
+                name = "+".join(p.name for p in prs)
+                qw = synth.torch_words((n, k // 8), synth.seed_of(s, 10, li, gi), device)
+                st = synth.torch_steps((n, k // 32), synth.seed_of(s, 11, li, gi), device)
+                self.mats.append((li, name, n, k, xk, qw, st))
+        # activations: one row per distinct (layer, x_key), plus the final row
+        self.x_keys = []
+        self.k_of = {}
+        for li, name, n, k, xk, _, _ in self.mats:
+            if (li, xk) not in self.k_of:
+                self.x_keys.append((li, xk))
+                self.k_of[(li, xk)] = k
+        total_x = sum(self.k_of[k] for k in self.x_keys) + h
+        self.x_flat = synth.torch_x((total_x,), synth.seed_of(s, 20), device)
+        self.x_off = {}
+        off = 0
+        for k in self.x_keys:
+            self.x_off[k] = off
+            off += self.k_of[k]
+        self.x_off["final"] = off
+        self.ids = torch.tensor([int(synth.seed_of(s, 30) % V)], dtype=torch.int32, device=device)
+        # outputs, one region per launch
+        self.y_off = {}
+        off = 0
+        for li, name, n, k, xk, _, _ in self.mats:
+            self.y_off[(li, name)] = off
+            off += n
+        self.y_off["logits"] = off
+        off += V
+        self.y_flat = torch.empty(off, dtype=torch.bfloat16, device=device)
+        self.emb_row = torch.empty((1, h), dtype=torch.bfloat16, device=device)
+        self.ple_row = torch.empty((1, pw), dtype=torch.bfloat16, device=device)
+        ws = 0
+        for li, name, n, k, xk, _, _ in self.mats:
+            ws = max(ws, lib.workspace_bytes(1, n, k))
+        ws = max(ws, lib.workspace_bytes(1, V, h))
+        self.ws = torch.zeros(max(ws, 16), dtype=torch.uint8, device=device) if ws else None
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def x(self, key, k):
+        o = self.x_off[key]
+        return self.x_flat[o:o + k].view(1, k)
+
+    def launches(self):
+        """(kind, shape, callable) for every kernel of the pass, in stream order."""
+        lib, m = self.lib, self.model
+        out = []
+        out.append(("gather", (1, m.hidden), lambda pdl: lib.embed_gather(
+            self.emb_qw, self.emb_st, self.ids, out=self.emb_row, status=self.status, pdl=pdl)))
+        out.append(("gather", (1, m.per_layer_width), lambda pdl: lib.embed_gather(
+            self.ple_qw, self.ple_st, self.ids, out=self.ple_row, status=self.status, pdl=pdl)))
+        for li, name, n, k, xk, qw, st in self.mats:
+            x = self.x((li, xk), k)
+            o = self.y_off[(li, name)]
+            y = self.y_flat[o:o + n].view(1, n)
+            out.append(("gemv", (1, n, k), self._gemv(qw, st, x, y)))
+        o = self.y_off["logits"]
+        out.append(("gemv", (1, m.vocab, m.hidden), self._gemv(
+            self.emb_qw, self.emb_st, self.x("final", m.hidden),
+            self.y_flat[o:o + m.vocab].view(1, m.vocab))))
+        return out
+
+    def _gemv(self, qw, st, x, y):
+        lib = self.lib
+        return lambda pdl: lib.gemv(qw, st, x, y=y, workspace=self.ws, status=self.status, pdl=pdl)
+
+    def step_bytes(self):
+        return step_bytes_of(self.model)
+
+    def host_inputs(self):
+        """Pinned host copies of the per-step inputs (token id, activation rows)."""
+        return (self.ids.cpu().pin_memory(), self.x_flat.cpu().pin_memory())
+
+    def host_outputs(self):
+        o = self.y_off["logits"]
+        return torch.empty(self.model.vocab, dtype=torch.bfloat16).pin_memory(), o
+
+
+def kernel_key(kind, shape, lib):  # ncu names the instantiation
+    if kind == "gather":
+        return "gather_kernel"
+    M, N, K = shape
+    p = lib.plan(M, N, K)
+    return f"gemv_kernel<{p['rows_per_call']}>"
+
+
+def capture(fns, stream, pdl=True):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i, f in enumerate(fns):
+            f(pdl and i > 0)
+    return g
+
+
+def time_replays(g, stream, steps):
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def traffic_from_profile(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if still current."""
+    path = os.path.join(ROOT, "profiles", "gemv_kernel_traffic.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    src = hashlib.sha256()
+    for f in ("gemv.cu", "common.cuh"):
+        src.update(open(os.path.join(ROOT, "bit_weight_only_gemv_gb300", "csrc", f), "rb").read())
+    m = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
+    if not m or m.group(1) != src.hexdigest():
+        return None
+    for line in text.splitlines():
+        mm = re.match(r"\s*-\s*kernel:\s*(.+?)\s*\|\s*dram_bytes_per_launch:\s*([0-9.]+)\s*\|"
+                      r"\s*workload:\s*(.+)$", line)
+        if mm and mm.group(1) == kernel:
+            return {"bytes": float(mm.group(2)), "workload": mm.group(3)}
+    return None
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_sample(dp, proj_names, lm_rows, layer=0):
+    """Copy a sample of the pass to the host and return (seconds, sample_bytes).
+
+    The sample is the given projections of one layer (full matrices), lm_rows
+    rows of the lm_head GEMV and both row gathers, computed by the fp64 oracle.
+    """
+    import oracle
+    m = dp.model
+    host = []
+    for li, name, n, k, xk, qw, st in dp.mats:
+        if li != layer or not any(p in name.split("+") for p in proj_names):
+            continue
+        x = dp.x((layer, xk), k)
+        host.append((qw.cpu().numpy().view(np.uint32), st.view(torch.int16).cpu().numpy().view(np.uint16),
+                     x.view(torch.int16).cpu().numpy().view(np.uint16), metrics.gemv_bytes(1, n, k)))
+    rows = np.arange(lm_rows) * (m.vocab // lm_rows)
+    lm_qw = dp.emb_qw[torch.from_numpy(rows).to(dp.dev)].cpu().numpy().view(np.uint32)
+    lm_st = dp.emb_st[torch.from_numpy(rows).to(dp.dev)].view(torch.int16).cpu().numpy().view(np.uint16)
+    lm_x = dp.x("final", m.hidden).view(torch.int16).cpu().numpy().view(np.uint16)
+    tid = int(dp.ids.item())
+    e_qw = dp.emb_qw[tid:tid + 1].cpu().numpy().view(np.uint32)
+    e_st = dp.emb_st[tid:tid + 1].view(torch.int16).cpu().numpy().view(np.uint16)
+    p_qw = dp.ple_qw[tid:tid + 1].cpu().numpy().view(np.uint32)
+    p_st = dp.ple_st[tid:tid + 1].view(torch.int16).cpu().numpy().view(np.uint16)
+    t0 = time.perf_counter()
+    nbytes = 0
+    for qw, st, x, b in host:
+        oracle.gemv_ref(qw, st, x)
+        nbytes += b
+    oracle.gemv_ref(lm_qw, lm_st, lm_x)
+    nbytes += metrics.gemv_bytes(1, lm_rows, m.hidden)
+    oracle.gather_ref(e_qw, e_st, np.array([0]))
+    oracle.gather_ref(p_qw, p_st, np.array([0]))
+    nbytes += metrics.gather_bytes(1, m.hidden) + metrics.gather_bytes(1, m.per_layer_width)
+    return time.perf_counter() - t0, nbytes
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ arms
+def reference_sample(model, seed=0):
+    """Host arrays for one bounded oracle sample, drawn by the same recipe."""
+    rng = np.random.default_rng(seed)
+    pr = model.projs[0]
+    lm_rows = 256
+    return {
+        "proj": (synth.np_words(rng, (pr.n, pr.k // 8)), synth.np_steps(rng, (pr.n, pr.k // 32)),
+                 synth.np_x(rng, (1, pr.k)), metrics.gemv_bytes(1, pr.n, pr.k)),
+        "lm": (synth.np_words(rng, (lm_rows, model.hidden // 8)),
+               synth.np_steps(rng, (lm_rows, model.hidden // 32)), synth.np_x(rng, (1, model.hidden)),
+               metrics.gemv_bytes(1, lm_rows, model.hidden)),
+        "emb": (synth.np_words(rng, (1, model.hidden // 8)), synth.np_steps(rng, (1, model.hidden // 32)),
+                metrics.gather_bytes(1, model.hidden)),
+        "ple": (synth.np_words(rng, (1, model.per_layer_width // 8)),
+                synth.np_steps(rng, (1, model.per_layer_width // 32)),
+                metrics.gather_bytes(1, model.per_layer_width)),
+    }
+
+
+def step_bytes_of(model):
+    b = metrics.gather_bytes(1, model.hidden) + metrics.gather_bytes(1, model.per_layer_width)
+    for pr in model.projs:
+        b += model.layers * metrics.gemv_bytes(1, pr.n, pr.k)
+    return b + metrics.gemv_bytes(1, model.vocab, model.hidden)
+
+
+def run_reference(args, world, rank):
+    """The CPU oracle, as it stands, on the host cores: bounded samples per step."""
+    if rank != 0:
+        return 0
+    import oracle
+    model = synth.dense_2048()
+    sample = reference_sample(model)
+    step_bytes = step_bytes_of(model)
+
+    def one():
+        t0 = time.perf_counter()
+        nb = 0
+        for key in ("proj", "lm"):
+            qw, st, x, b = sample[key]
+            oracle.gemv_ref(qw, st, x)
+            nb += b
+        for key in ("emb", "ple"):
+            qw, st, b = sample[key]
+            oracle.gather_ref(qw, st, np.array([0]))
+            nb += b
+        return time.perf_counter() - t0, nb
+
+    for _ in range(args.warmup):
+        one()
+    secs, nb = 0.0, 0
+    for _ in range(args.steps):
+        t, b = one()
+        secs += t
+        nb += b
+    per_token = secs * step_bytes / nb
+    value = 1.0 / per_token
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_token * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": model.name + " decode pass, batch 1 (gathers + 245 projection "
+                               "GEMVs + 262144x2048 lm_head)", "global_batch": 1,
+                   "parallelism": "single (rank 0 only)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "sample": "per step: one 2048x2048 projection + 256 lm_head rows + both "
+                                   "row gathers, fp64 NumPy oracle; scaled to the whole pass by "
+                                   "algorithmic bytes"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "hbm_gbs": metrics.gbps(step_bytes, per_token),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gb300(args, world, rank, local):
+    from bit_weight_only_gemv_gb300 import lib
+    lib.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    model = synth.dense_2048()
+    dp = DecodePass(model, dev, seed=0, merge=not args.separate)
+    launches = dp.launches()
+    stream = torch.cuda.Stream(device=dev)
+    # eager warm-up (plans, attributes), then capture the pass as one graph
+    with torch.cuda.stream(stream):
+        for i, (_, _, f) in enumerate(launches):
+            f(i > 0)
+    torch.cuda.synchronize()
+    g = capture([f for _, _, f in launches], stream)
+    step_bytes = dp.step_bytes()
+    n_launch = len(launches)
+
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local).start()
+    # settle under load so the clock samples of the timed region are steady
+    t_end = time.time() + 0.5
+    while time.time() < t_end:
+        g.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ms = time_replays(g, stream, args.steps)
+    torch.cuda.synchronize()
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    clocks = sampler.stop()
+    if int(dp.status.item()) != 0:
+        raise RuntimeError(f"device status {int(dp.status.item())}")
+
+    tok_s = world * 1000.0 / ms
+
+    # dominant kernel: time its launches of the pass on their own (same stream,
+    # same arguments), CUDA events around whole-graph replays
+    keys = [kernel_key(k, s, lib) for k, s, _ in launches]
+    by_key = {}
+    for (kind, shape, f), key in zip(launches, keys):
+        b = metrics.gemv_bytes(*shape) if kind == "gemv" else metrics.gather_bytes(*shape)
+        by_key.setdefault(key, []).append((f, b))
+    key_time = {}
+    for key, items in by_key.items():
+        gk = capture([f for f, _ in items], stream)
+        for _ in range(3):
+            gk.replay()
+        reps = max(3, min(args.steps, 50))
+        key_time[key] = (time_replays(gk, stream, reps), len(items), sum(b for _, b in items))
+        del gk
+    dom = max(key_time, key=lambda k: key_time[k][0])
+    dom_ms, dom_n, dom_bytes = key_time[dom]
+    peak, peak_kind = load_peaks()
+    achieved = metrics.gbps(dom_bytes / dom_n, dom_ms * 1e-3 / dom_n)
+    traffic = traffic_from_profile(dom)
+
+    # end to end: inputs from pinned host memory, logits back to the host
+    h_ids, h_x = dp.host_inputs()
+    h_logits, lo = dp.host_outputs()
+    e2e_steps = max(3, min(args.steps, 50))
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            dp.ids.copy_(h_ids, non_blocking=True)
+            dp.x_flat.copy_(h_x, non_blocking=True)
+            g.replay()
+            h_logits.copy_(dp.y_flat[lo:lo + model.vocab], non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    h2d = h_ids.numel() * 4 + h_x.numel() * 2
+    d2h = h_logits.numel() * 2
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        t, nb = oracle_sample(dp, [p.name for p in model.projs], 4096)
+        per_token = t * step_bytes / nb
+        cpu = {"value": 1.0 / per_token, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+               "sample": "layer 0 (all 7 projections, full) + 4096 of 262144 lm_head rows + both "
+                         "row gathers, fp64 NumPy oracle; scaled to the whole pass by algorithmic "
+                         "bytes; NumPy may use BLAS threads on the listed cores"}
+
+    line = {
+        "metric": METRIC, "value": tok_s, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "w4a16: f16 products, f32 accumulate",
+        "data": "synthetic",
+        "config": {"workload": model.name + " decode pass, batch 1 (gathers, 35 layers of "
+                               "q/k/v/o/gate/up/down GEMVs, 262144x2048 lm_head)",
+                   "projections": "separate (245 GEMVs)" if args.separate else
+                   "merged: q/k/v and gate/up row-concatenated (140 GEMVs)",
+                   "global_batch": world, "parallelism": f"replicas x{world}",
+                   "bytes_per_step": step_bytes,
+                   "l2": "inputs larger than L2 (1.50 GB of weights per step, 129 MB L2)"},
+        "hbm_gbs": metrics.gbps(step_bytes, ms * 1e-3),
+        "frac_of_nominal_8tbps": metrics.gbps(step_bytes, ms * 1e-3) / NOMINAL_HBM_GBPS,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None if traffic is None else traffic["bytes"],
+                     "traffic_note": None if traffic is None else
+                     "ncu dram read+write per launch, " + traffic["workload"],
+                     "launches_per_step": dom_n, "ms_per_step": dom_ms},
+        "kernels": {k: {"launches_per_step": v[1], "ms": v[0],
+                        "gbps": metrics.gbps(v[2], v[0] * 1e-3)} for k, v in key_time.items()},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * 1000.0 / e2e_ms, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": n_launch * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--separate", action="store_true",
+                    help="one GEMV per projection instead of merged q/k/v and gate/up")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_env()
+    if world > 1:
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        torch.distributed.init_process_group(backend)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, world, rank)
+        return run_gb300(args, world, rank, local)
+    finally:
+        if world > 1 and torch.distributed.is_initialized():
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

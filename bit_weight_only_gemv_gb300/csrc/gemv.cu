@@ -8,15 +8,13 @@
 // SSD", section "Streaming without touching a single GPU kernel") reads expert
 // `id` at base + id * stride.
 //
-// Design (one persistent CTA of 16 warps per SM):
+// Design (persistent CTAs of 8 warps, one or two per SM):
 //  * The activation rows are staged once per CTA in shared memory as fp16
 //    pairs scaled by a power of two per group of 32 (exact), next to the
 //    group's inverse scale.
-//  * A team of `team` lanes shares a set of R output rows (team = the largest
-//    power of two <= 32 dividing K/32 that leaves each lane >= 8 groups of a
-//    row, so no lane idles); each lane walks the
-//    groups lane, lane + team, ... and handles the same group of its R rows
-//    together, so one shared-memory read of the activations serves R rows.
+//  * A team of `team` lanes shares an output row (team = the largest power
+//    of two <= 32 dividing K/32 that leaves each lane >= 8 groups of a row,
+//    so no lane idles); each lane walks the groups lane, lane + team, ...
 //  * Packed codes and steps go straight from HBM to registers with coalesced
 //    128-bit (codes) loads that bypass L1; the weights never touch shared
 //    memory, which keeps shared-memory bandwidth for the activations.
@@ -27,12 +25,15 @@
 //    over the group's 4 words in fp16 (at most 3 roundings: 3 * 2^-11 of
 //    sum|w x|), adds the 8 partial sums in fp32, rescales by the group's 2^-e
 //    (exact), multiplies by the step and accumulates in fp32.
-//  * K is cut into chunks of 8 groups per lane; after each chunk the team
-//    reduces with a fixed xor-shuffle tree and chunk sums are added in chunk
-//    order.  A row's arithmetic therefore depends on K only, never on N, R,
-//    the row index, the split or the addresses: results are bitwise
-//    reproducible and a gemv_id row equals the gemv of that expert.
-//  * Work unit = (row block of 32/team * R rows, K slice).  Each CTA owns a
+//  * K is cut into chunks of 8 groups per lane; the loads of the next chunk
+//    are in flight (second register buffer) while a chunk is computed, and
+//    the first chunk is requested before waiting on the previous kernel.
+//    After each chunk the team reduces with a fixed xor-shuffle tree and
+//    chunk sums are added in chunk order.  A row's arithmetic therefore
+//    depends on K only, never on N, the row index, the split or the
+//    addresses: results are bitwise reproducible and a gemv_id row equals
+//    the gemv of that expert.
+//  * Work unit = (row block of 32/team rows, K slice).  Each CTA owns a
 //    balanced contiguous range of units; its warps take them round-robin.
 //    Split-K (slices > 1): chunk sums go to the workspace and the warp that
 //    finishes a row block last (atomic counter, no waiting) adds them in
@@ -46,8 +47,9 @@
 
 namespace w4 {
 
-constexpr int kWarps = 16;
+constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
+constexpr int kCtasPerSm = 2;    // two resident CTAs per SM: this launch and the next
 constexpr int kMaxMR = 4;        // activation rows per launch
 constexpr int kChunkPerLane = 8; // groups per lane per chunk
 
@@ -244,24 +246,30 @@ __device__ __forceinline__ void prefetch_unit(const GemvParams& p, int u, int la
 }
 
 // ---------------------------------------------------------------- kernel
-// A warp's position in its walk over (unit, step) pairs.  A step is one group
-// of each of the lane's R rows: group g = slice start + lane_in_team + i*team.
+// A warp's position in its walk over (unit, chunk) pairs.  Chunk c of a unit
+// holds, for this lane, the groups g = c*chunk + lane_in_team + s*team for
+// s < steps (steps <= kChunkPerLane; fewer only in the last chunk of K).
 struct Cursor {
   int u;                // current unit (>= end when the walk is over)
-  int i, n;             // step in the unit, steps per lane in the unit
-  int g;                // this lane's group at step i
+  int c, c_end;         // chunk and end chunk of the unit's slice
+  int steps;            // groups of this chunk per lane
+  int g;                // this lane's first group of the chunk
   int item, rb, slice;
-  int row0;             // this lane's first row
-  const uint8_t* qbase; // codes of row0
-  const uint8_t* sbase; // steps of row0
+  int row;              // this lane's row
+  const uint8_t* qrow;  // codes of the row
+  const uint8_t* srow;  // steps of the row
 
+  __device__ void set_chunk(const GemvParams& p, int lt) {
+    g = c * p.chunk + lt;
+    steps = (min((c + 1) * p.chunk, p.Kg) - c * p.chunk) / p.team;
+  }
   // First unit at or after uu (stride kWarps) with a valid expert id.
-  __device__ void seek(const GemvParams& p, int uu, int ue, int lt, int set, int R, bool rep) {
+  __device__ void seek(const GemvParams& p, int uu, int ue, int lt, int set, bool rep) {
     for (u = uu; u < ue; u += kWarps) {
       slice = u / p.B;
       rb = u - slice * p.B;
       item = rb / p.upi;
-      row0 = (rb - item * p.upi) * p.rows_per_unit + set * R;
+      row = (rb - item * p.upi) * p.rows_per_unit + set;
       long long blk = item;
       if (p.ids != nullptr) {
         const int e = __ldg(p.ids + item);
@@ -271,52 +279,49 @@ struct Cursor {
         }
         blk = e;
       }
-      const int g0 = slice * p.cps * p.chunk;
-      const int g1 = min((slice + 1) * p.cps * p.chunk, p.Kg);
-      n = (g1 - g0) / p.team;
-      i = 0;
-      g = g0 + lt;
-      qbase = p.qw + (unsigned long long)blk * p.qw_item_stride + (long long)row0 * (p.K / 2);
-      sbase = p.st + (unsigned long long)blk * p.st_item_stride + (long long)row0 * (p.Kg * 2);
+      c = slice * p.cps;
+      c_end = min(c + p.cps, p.nch);
+      set_chunk(p, lt);
+      qrow = p.qw + (unsigned long long)blk * p.qw_item_stride + (long long)row * (p.K / 2);
+      srow = p.st + (unsigned long long)blk * p.st_item_stride + (long long)row * (p.Kg * 2);
       return;
     }
   }
-  __device__ void advance(const GemvParams& p, int ue, int lt, int set, int R, bool rep) {
-    if (++i < n) {
-      g += p.team;
+  __device__ void next_chunk(const GemvParams& p, int ue, int lt, int set, bool rep) {
+    if (++c < c_end) {
+      set_chunk(p, lt);
       return;
     }
-    seek(p, u + kWarps, ue, lt, set, R, rep);
+    seek(p, u + kWarps, ue, lt, set, rep);
   }
 };
 
-// Load the codes and steps of cursor c's step into one register slot.
-template <int R>
-__device__ __forceinline__ void load_step(const GemvParams& p, const Cursor& c, uint4 code[R],
-                                          uint32_t sb[R]) {
-  const long long row_bytes = (long long)p.K / 2;
-  const int st_row = p.Kg * 2;
+// Load the codes and steps of cursor c's chunk into a register buffer.
+__device__ __forceinline__ void load_chunk(const GemvParams& p, const Cursor& c,
+                                           uint4 code[kChunkPerLane], uint32_t sb[kChunkPerLane]) {
+  const bool live = c.row < p.N;
 #pragma unroll
-  for (int q = 0; q < R; ++q) {
-    if (c.row0 + q < p.N) {
-      code[q] = ldg_stream16(c.qbase + q * row_bytes + (long long)c.g * 16);
-      sb[q] = ldg_stream2(c.sbase + q * st_row + c.g * 2);
-    } else {   // rows past N: code 8 and step 0 contribute nothing
-      code[q] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
-      sb[q] = 0;
+  for (int s = 0; s < kChunkPerLane; ++s) {
+    if (live && s < c.steps) {
+      const int g = c.g + s * p.team;
+      code[s] = ldg_stream16(c.qrow + g * 16);
+      sb[s] = ldg_stream2(c.srow + g * 2);
+    } else {   // rows past N and steps past the chunk: code 8, step 0
+      code[s] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+      sb[s] = 0;
     }
   }
 }
 
 constexpr int kPrefetchUnits = 2;   // units per warp requested into L2 before the PDL wait
 
-template <int R, int MR>
-__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ GemvParams p) {
+template <int MR>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid_constant__ GemvParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int team = p.team;
-  const int set = lane / team;   // row set of this lane within the warp
+  const int set = lane / team;   // row set (= row of the unit) of this lane
   const int lt = lane - set * team;
   const int ub = (int)((long long)blockIdx.x * p.U / gridDim.x);
   const int ue = (int)((long long)(blockIdx.x + 1) * p.U / gridDim.x);
@@ -336,128 +341,113 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   uint8_t* xs = smem;
   float* xscale = reinterpret_cast<float*>(smem + (long long)p.x_slots * MR * 4 * p.Kg * 16);
 
-  // Dense weights do not depend on earlier kernels: start pulling this warp's
-  // first units into L2 before waiting for the previous kernel (W4_FLAG_PDL).
-  if (p.ids == nullptr)
-    for (int d = 0; d < kPrefetchUnits; ++d)
-      if (ub + warp + d * kWarps < ue) prefetch_unit(p, ub + warp + d * kWarps, lane);
-  pdl_wait();                // activations, ids and outputs follow earlier kernels
+  // Compute cursor `cp` and load cursor `ld` one chunk ahead; two register
+  // buffers.  Dense weights do not depend on earlier kernels: this warp's
+  // first units are requested into L2 and its first chunk into registers
+  // before waiting for the previous kernel (W4_FLAG_PDL), so a launch that is
+  // resident early has its weights in flight already.  Routed ids may come
+  // from the previous kernel and are read after the wait.
+  Cursor cp, ld;
+  uint4 cur[kChunkPerLane], nxt[kChunkPerLane];
+  uint32_t cur_s[kChunkPerLane], nxt_s[kChunkPerLane];
+  const bool dense = p.ids == nullptr;
+  if (!dense) pdl_wait();
+  for (int d = 0; d < kPrefetchUnits; ++d)
+    if (ub + warp + d * kWarps < ue) prefetch_unit(p, ub + warp + d * kWarps, lane);
+  cp.seek(p, ub + warp, ue, lt, set, true);
+  ld = cp;
+  if (ld.u < ue) {
+    load_chunk(p, ld, cur, cur_s);
+    ld.next_chunk(p, ue, lt, set, false);
+  }
+  if (dense) pdl_wait();     // activations and outputs follow earlier kernels
   pdl_launch_dependents();
   if (ub < ue) stage_x(p, item0, nslots, xs, xscale);
   __syncthreads();
 
-  // compute cursor `cp` and load cursor `ld`, two steps ahead; register ring
-  // of three slots
-  Cursor cp, ld;
-  cp.seek(p, ub + warp, ue, lt, set, R, true);
-  ld = cp;
-  uint4 code[3][R];
-  uint32_t sb[3][R];
-  if (ld.u < ue) {
-    load_step<R>(p, ld, code[0], sb[0]);
-    ld.advance(p, ue, lt, set, R, false);
-  }
-  if (ld.u < ue) {
-    load_step<R>(p, ld, code[1], sb[1]);
-    ld.advance(p, ue, lt, set, R, false);
-  }
-
-  float acc[R][MR], rowsum[R][MR];
+  float rowsum[MR];
 #pragma unroll
-  for (int q = 0; q < R; ++q)
-#pragma unroll
-    for (int m = 0; m < MR; ++m) acc[q][m] = rowsum[q][m] = 0.0f;
+  for (int m = 0; m < MR; ++m) rowsum[m] = 0.0f;
 
   while (cp.u < ue) {
+    if (ld.u < ue) {   // next chunk's loads fly while this one is computed
+      load_chunk(p, ld, nxt, nxt_s);
+      ld.next_chunk(p, ue, lt, set, false);
+    }
+    const int xslot = p.x_per_item ? cp.item - item0 : 0;
+    const uint8_t* xrow = xs + (long long)xslot * MR * 4 * p.Kg * 16;
+    const float* srow = xscale + (long long)xslot * MR * p.Kg;
+    float acc[MR];
 #pragma unroll
-    for (int k = 0; k < 3; ++k) {
-      if (cp.u >= ue) break;
-      if (ld.u < ue) {   // refill the slot freed by the previous step
-        load_step<R>(p, ld, code[(k + 2) % 3], sb[(k + 2) % 3]);
-        ld.advance(p, ue, lt, set, R, false);
+    for (int m = 0; m < MR; ++m) acc[m] = 0.0f;
+#pragma unroll
+    for (int s = 0; s < kChunkPerLane; ++s) {
+      if (s < cp.steps) {
+        const int g = cp.g + s * team;
+#pragma unroll
+        for (int m = 0; m < MR; ++m) {
+          uint4 xv[4];
+#pragma unroll
+          for (int w = 0; w < 4; ++w)
+            xv[w] = *reinterpret_cast<const uint4*>(xrow + ((long long)(m * 4 + w) * p.Kg + g) * 16);
+          const float sc = srow[(long long)m * p.Kg + g];
+          acc[m] = fmaf(group_sum(cur[s], xv) * sc, bf16_bits_to_float(cur_s[s]), acc[m]);
+        }
       }
-      const int xslot = p.x_per_item ? cp.item - item0 : 0;
-      const uint8_t* xrow = xs + (long long)xslot * MR * 4 * p.Kg * 16;
-      const float* srow = xscale + (long long)xslot * MR * p.Kg;
+    }
+    // chunk sum: fixed xor tree over the team
 #pragma unroll
-      for (int m = 0; m < MR; ++m) {
-        uint4 xv[4];
+    for (int m = 0; m < MR; ++m)
+      for (int off = team >> 1; off > 0; off >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], off);
+    const bool unit_end = cp.c + 1 == cp.c_end;
+    if (p.S == 1) {
 #pragma unroll
-        for (int w = 0; w < 4; ++w)
-          xv[w] = *reinterpret_cast<const uint4*>(xrow + ((long long)(m * 4 + w) * p.Kg + cp.g) * 16);
-        const float sc = srow[(long long)m * p.Kg + cp.g];
-#pragma unroll
-        for (int q = 0; q < R; ++q)
-          acc[q][m] = fmaf(group_sum(code[k][q], xv) * sc, bf16_bits_to_float(sb[k][q]), acc[q][m]);
-      }
-      const bool unit_end = cp.i + 1 == cp.n;
-      if (unit_end || (cp.i + 1) % kChunkPerLane == 0) {
-        // chunk sum: fixed xor tree over the team
-#pragma unroll
-        for (int q = 0; q < R; ++q)
+      for (int m = 0; m < MR; ++m) rowsum[m] += acc[m];
+      if (unit_end) {
+        if (lt == 0 && cp.row < p.N) {
 #pragma unroll
           for (int m = 0; m < MR; ++m)
-            for (int off = team >> 1; off > 0; off >>= 1)
-              acc[q][m] += __shfl_xor_sync(0xffffffffu, acc[q][m], off);
-        if (p.S == 1) {
-#pragma unroll
-          for (int q = 0; q < R; ++q)
-#pragma unroll
-            for (int m = 0; m < MR; ++m) rowsum[q][m] += acc[q][m];
-        } else if (lt == 0) {
-          const int c = cp.slice * p.cps + cp.i / kChunkPerLane;
-          float* dst = p.ws_partial +
-                       (((long long)cp.rb * p.nch + c) * p.rows_per_unit + set * R) * MR;
-#pragma unroll
-          for (int q = 0; q < R; ++q)
-#pragma unroll
-            for (int m = 0; m < MR; ++m) dst[q * MR + m] = acc[q][m];
+            p.y[((long long)cp.item * MR + m) * p.N + cp.row] = __float2bfloat16_rn(rowsum[m]);
         }
 #pragma unroll
-        for (int q = 0; q < R; ++q)
+        for (int m = 0; m < MR; ++m) rowsum[m] = 0.0f;
+      }
+    } else {
+      if (lt == 0) {
+        float* dst = p.ws_partial +
+                     (((long long)cp.rb * p.nch + cp.c) * p.rows_per_unit + set) * MR;
 #pragma unroll
-          for (int m = 0; m < MR; ++m) acc[q][m] = 0.0f;
+        for (int m = 0; m < MR; ++m) dst[m] = acc[m];
       }
       if (unit_end) {
-        if (p.S == 1) {
-          if (lt == 0) {
-#pragma unroll
-            for (int q = 0; q < R; ++q)
-              if (cp.row0 + q < p.N)
-#pragma unroll
-                for (int m = 0; m < MR; ++m)
-                  p.y[((long long)cp.item * MR + m) * p.N + cp.row0 + q] =
-                      __float2bfloat16_rn(rowsum[q][m]);
-          }
-#pragma unroll
-          for (int q = 0; q < R; ++q)
-#pragma unroll
-            for (int m = 0; m < MR; ++m) rowsum[q][m] = 0.0f;
-        } else {
-          // the last warp to finish this row block adds the chunk sums in
-          // chunk order, writes the rows and re-arms the counter
+        // the last warp to finish this row block adds the chunk sums in
+        // chunk order, writes the rows and re-arms the counter
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomicAdd(p.ws_count + cp.rb, 1) == p.S - 1;
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
           __threadfence();
-          __syncwarp();
-          int last = 0;
-          if (lane == 0) last = atomicAdd(p.ws_count + cp.rb, 1) == p.S - 1;
-          last = __shfl_sync(0xffffffffu, last, 0);
-          if (last) {
-            __threadfence();
-            const int rbase = (cp.rb - cp.item * p.upi) * p.rows_per_unit;
-            const float* src = p.ws_partial + (long long)cp.rb * p.nch * p.rows_per_unit * MR;
-            for (int e = lane; e < p.rows_per_unit * MR; e += 32) {
-              const int r = e / MR, m = e - r * MR;
-              if (rbase + r >= p.N) continue;
-              float v = 0.0f;
-              for (int c = 0; c < p.nch; ++c)
-                v += __ldcg(src + ((long long)c * p.rows_per_unit + r) * MR + m);
-              p.y[((long long)cp.item * MR + m) * p.N + rbase + r] = __float2bfloat16_rn(v);
-            }
-            if (lane == 0) atomicExch(p.ws_count + cp.rb, 0);
+          const int rbase = (cp.rb - cp.item * p.upi) * p.rows_per_unit;
+          const float* src = p.ws_partial + (long long)cp.rb * p.nch * p.rows_per_unit * MR;
+          for (int e = lane; e < p.rows_per_unit * MR; e += 32) {
+            const int r = e / MR, m = e - r * MR;
+            if (rbase + r >= p.N) continue;
+            float v = 0.0f;
+            for (int c = 0; c < p.nch; ++c)
+              v += __ldcg(src + ((long long)c * p.rows_per_unit + r) * MR + m);
+            p.y[((long long)cp.item * MR + m) * p.N + rbase + r] = __float2bfloat16_rn(v);
           }
+          if (lane == 0) atomicExch(p.ws_count + cp.rb, 0);
         }
       }
-      cp.advance(p, ue, lt, set, R, true);
+    }
+    cp.next_chunk(p, ue, lt, set, true);
+#pragma unroll
+    for (int s = 0; s < kChunkPerLane; ++s) {
+      cur[s] = nxt[s];
+      cur_s[s] = nxt_s[s];
     }
   }
 }
@@ -527,18 +517,10 @@ bool make_plan(int MR, int N, int K, int n_items, int allow_split, int x_per_ite
   row_shape(K, &pl.team, &pl.chunk, &pl.nch);
   pl.sets = 32 / pl.team;
   const int sms = di.sms > 0 ? di.sms : 1;
-  const long long warps = (long long)sms * kWarps;
+  const long long warps = (long long)sms * kWarps * kCtasPerSm;
   const long long want = 6 * warps;       // units for a balanced split over warps
-  // rows per lane: as many as keep enough units (activation reuse), fewer
-  // with several activation rows (registers)
-  int R = (MR == 1) ? 4 : (MR == 2 ? 2 : 1);
-  while (R > 1) {
-    const long long rpu = (long long)pl.sets * R;
-    if ((long long)n_items * ((N + rpu - 1) / rpu) >= want) break;
-    R >>= 1;
-  }
-  pl.R = R;
-  pl.rows_per_unit = pl.sets * R;
+  pl.R = 1;   // one row per lane
+  pl.rows_per_unit = pl.sets;
   pl.upi = (N + pl.rows_per_unit - 1) / pl.rows_per_unit;
   pl.B = (long long)n_items * pl.upi;
   if (pl.B > (1LL << 30)) return false;
@@ -549,7 +531,10 @@ bool make_plan(int MR, int N, int K, int n_items, int allow_split, int x_per_ite
   pl.S = (pl.nch + pl.cps - 1) / pl.cps;
   pl.U = (long long)pl.S * pl.B;
   if (pl.U > (1LL << 30)) return false;
-  pl.ctas = (int)std::min<long long>(pl.U, sms);
+  // One CTA per SM leaves room for the next launch's CTA (PDL); problems
+  // with many units per warp fill two CTAs per SM instead.
+  const long long per_sm = (pl.U >= 4LL * kCtasPerSm * sms * kWarps) ? kCtasPerSm : 1;
+  pl.ctas = (int)std::min<long long>(pl.U, per_sm * sms);
   // activation rows a CTA stages: one, or the items its unit range touches
   pl.x_slots = 1;
   if (x_per_item) {
@@ -575,11 +560,11 @@ bool make_plan(int MR, int N, int K, int n_items, int allow_split, int x_per_ite
   return true;
 }
 
-template <int R, int MR>
+template <int MR>
 cudaError_t launch_one(const GemvParams& prm, const Plan& pl, bool pdl, cudaStream_t stream, int dev) {
   static std::mutex mu;
   static long long attr_bytes[64] = {};
-  auto kern = gemv_kernel<R, MR>;
+  auto kern = gemv_kernel<MR>;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   {
     // raise the kernel's dynamic shared-memory limit to what this plan needs
@@ -605,14 +590,11 @@ cudaError_t launch_one(const GemvParams& prm, const Plan& pl, bool pdl, cudaStre
 }
 
 cudaError_t launch(const GemvParams& prm, const Plan& pl, bool pdl, cudaStream_t s, int dev) {
-  switch (pl.MR * 8 + pl.R) {
-    case 8 + 4: return launch_one<4, 1>(prm, pl, pdl, s, dev);
-    case 8 + 2: return launch_one<2, 1>(prm, pl, pdl, s, dev);
-    case 8 + 1: return launch_one<1, 1>(prm, pl, pdl, s, dev);
-    case 16 + 2: return launch_one<2, 2>(prm, pl, pdl, s, dev);
-    case 16 + 1: return launch_one<1, 2>(prm, pl, pdl, s, dev);
-    case 24 + 1: return launch_one<1, 3>(prm, pl, pdl, s, dev);
-    case 32 + 1: return launch_one<1, 4>(prm, pl, pdl, s, dev);
+  switch (pl.MR) {
+    case 1: return launch_one<1>(prm, pl, pdl, s, dev);
+    case 2: return launch_one<2>(prm, pl, pdl, s, dev);
+    case 3: return launch_one<3>(prm, pl, pdl, s, dev);
+    case 4: return launch_one<4>(prm, pl, pdl, s, dev);
     default: return cudaErrorInvalidConfiguration;
   }
 }
@@ -723,6 +705,7 @@ extern "C" w4_status w4a16_gemv_plan(int M, int N, int K, w4_plan_info* info) {
   info->rows_per_lane = pl.R;
   info->smem_bytes = (int)pl.smem;
   info->rows_per_call = pl.MR;
+  info->ring_slots = 2;   // current and next chunk
   return W4_OK;
 }
 

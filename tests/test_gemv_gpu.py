@@ -182,3 +182,16 @@ def test_gemv_unaligned_output_view_and_guard_band(cuda_lib):
     b = host_bits(big)[0]
     assert b[0] == POISON and np.all(b[n + 1:] == POISON)
     assert_gemv_parity(y, qw_h, st_h, x_h)
+
+
+def test_merged_projection_rows_equal_separate_gemvs(cuda_lib):
+    # q/k/v (and gate/up) read the same activation; stored row-concatenated
+    # they run as one GEMV whose rows are bitwise those of the separate GEMVs
+    rng = np.random.default_rng(10)
+    k = 2048
+    parts = [synth.np_words(rng, (n, k // 8)) for n in (2048, 512, 512)]
+    steps = [synth.np_steps(rng, (n, k // 32)) for n in (2048, 512, 512)]
+    x_h = synth.np_x(rng, (1, k))
+    merged, _ = run(np.concatenate(parts), np.concatenate(steps), x_h)
+    sep = [run(q, s_, x_h)[0] for q, s_ in zip(parts, steps)]
+    assert np.array_equal(host_bits(merged), np.concatenate([host_bits(y) for y in sep], axis=1))

@@ -429,3 +429,41 @@ def test_moe_trace_recipe():
     assert tr.min() >= 0 and tr.max() < 128
     kept = np.mean([len(set(tr[t]) & set(tr[t - 1])) for t in range(1, 200)])
     assert 5.0 < kept < 7.5          # about 0.7 * 8 kept plus Zipf re-draws
+
+
+# ---------------------------------------------------------------- metric form
+def test_bandwidth_formula_reproduces_the_pages_example():
+    from bit_weight_only_gemv_gb300 import metrics
+    vals = {}
+    for line in open(os.path.join(GOLDEN, "bandwidth_example.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        parts = line.split()
+        if parts[0] == "bytes_per_token_MiB":
+            vals["mib"] = float(parts[1])
+        elif parts[0] == "kernel":
+            vals[parts[1]] = (float(parts[3]), float(parts[5]))
+        elif parts[0] == "plain_read_GBps":
+            vals["plain"] = float(parts[1])
+        elif parts[0] == "kernel_fraction_percent":
+            vals["pct"] = float(parts[1])
+    nbytes = vals["mib"] * metrics.MIB
+    for ver in ("v5", "v4"):
+        ms, printed = vals[ver]
+        digits = len(str(ms).split(".")[1])
+        half = 0.5 * 10.0 ** -digits
+        lo = metrics.gbps(nbytes, (ms + half) * 1e-3)
+        hi = metrics.gbps(nbytes, (ms - half) * 1e-3)
+        assert lo - 0.05 <= printed <= hi + 0.05, (ver, lo, hi, printed)
+    v5 = metrics.gbps(nbytes, vals["v5"][0] * 1e-3)
+    assert round(100 * v5 / vals["plain"]) == vals["pct"]
+
+
+def test_gemv_byte_accounting():
+    from bit_weight_only_gemv_gb300 import metrics
+    # one 2048 x 2048 GEMV at batch 1: 2 MiB codes + 256 KiB steps + x + y
+    assert metrics.gemv_bytes(1, 2048, 2048) == 2 * 1024 * 1024 + 256 * 1024 + 4096 + 4096
+    assert metrics.gemv_bytes(1, 2048, 2048) == 2367488
+    # per-layer table row: 35 x 256 values
+    assert metrics.gather_bytes(1, 35 * 256) == 4480 + 560 + 17920 + 4
+    assert metrics.gemv_id_bytes(8, 1, 704, 2816) == 8 * (991232 + 123904) + 5632 + 11264
