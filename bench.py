@@ -229,7 +229,7 @@ def kernel_key(kind, shape, lib):  # ncu names the instantiation
         return "gather_kernel"
     M, N, K = shape
     p = lib.plan(M, N, K)
-    return f"gemv_kernel<{p['rows_per_call']}>"
+    return f"gemv_kernel<{p['rows_per_call']}, {p['chunk_steps']}>"
 
 
 def capture(fns, stream, pdl=True):

@@ -248,7 +248,7 @@ __device__ __forceinline__ void prefetch_unit(const GemvParams& p, int u, int la
 // ---------------------------------------------------------------- kernel
 // A warp's position in its walk over (unit, chunk) pairs.  Chunk c of a unit
 // holds, for this lane, the groups g = c*chunk + lane_in_team + s*team for
-// s < steps (steps <= kChunkPerLane; fewer only in the last chunk of K).
+// s < steps (steps = chunk / team, smaller only in a ragged last chunk).
 struct Cursor {
   int u;                // current unit (>= end when the walk is over)
   int c, c_end;         // chunk and end chunk of the unit's slice
@@ -296,27 +296,75 @@ struct Cursor {
   }
 };
 
-// Load the codes and steps of cursor c's chunk into a register buffer.
-__device__ __forceinline__ void load_chunk(const GemvParams& p, const Cursor& c,
-                                           uint4 code[kChunkPerLane], uint32_t sb[kChunkPerLane]) {
-  const bool live = c.row < p.N;
+// Chunk register buffer: CS groups of one row for this lane.  CS > 0: every
+// chunk has exactly CS steps; CS == 0: up to kChunkPerLane, guarded.
+template <int CS>
+struct Buf {
+  static constexpr int kN = CS > 0 ? CS : kChunkPerLane;
+  uint4 code[kN];
+  uint32_t sb[kN];
+};
+
+// Load the codes and steps of cursor c's chunk (rows past N and steps past a
+// ragged chunk get code 8 and step 0, which contribute nothing).
+template <int CS>
+__device__ __forceinline__ void load_chunk(const GemvParams& p, const Cursor& c, Buf<CS>& b) {
+  const uint8_t* q = c.qrow + c.g * 16;
+  const uint8_t* st = c.srow + c.g * 2;
+  const int qstep = p.team * 16, sstep = p.team * 2;
+  if (c.row < p.N) {
 #pragma unroll
-  for (int s = 0; s < kChunkPerLane; ++s) {
-    if (live && s < c.steps) {
-      const int g = c.g + s * p.team;
-      code[s] = ldg_stream16(c.qrow + g * 16);
-      sb[s] = ldg_stream2(c.srow + g * 2);
-    } else {   // rows past N and steps past the chunk: code 8, step 0
-      code[s] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
-      sb[s] = 0;
+    for (int s = 0; s < Buf<CS>::kN; ++s) {
+      if (CS > 0 || s < c.steps) {
+        b.code[s] = ldg_stream16(q + s * qstep);
+        b.sb[s] = ldg_stream2(st + s * sstep);
+      } else {
+        b.code[s] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+        b.sb[s] = 0;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int s = 0; s < Buf<CS>::kN; ++s) {
+      b.code[s] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+      b.sb[s] = 0;
+    }
+  }
+}
+
+// Sum over the chunk's steps, in step order, for every activation row.
+template <int CS, int MR>
+__device__ __forceinline__ void chunk_dot(const GemvParams& p, const Cursor& c, const Buf<CS>& b,
+                                          const uint8_t* xrow, const float* srow, float acc[MR]) {
+  const int kgs = p.Kg * 16;                 // bytes between the 4 word planes
+  const uint8_t* x0 = xrow + c.g * 16;
+  const float* s0 = srow + c.g;
+  const int xstep = p.team * 16;
+#pragma unroll
+  for (int m = 0; m < MR; ++m) acc[m] = 0.0f;
+#pragma unroll
+  for (int s = 0; s < Buf<CS>::kN; ++s) {
+    if (CS == 0 && s >= c.steps) break;
+#pragma unroll
+    for (int m = 0; m < MR; ++m) {
+      const uint8_t* xp = x0 + m * 4 * kgs + s * xstep;
+      uint4 xv[4];
+#pragma unroll
+      for (int w = 0; w < 4; ++w) xv[w] = *reinterpret_cast<const uint4*>(xp + w * kgs);
+      const float sc = s0[m * p.Kg + s * p.team];
+      acc[m] = fmaf(group_sum(b.code[s], xv) * sc, bf16_bits_to_float(b.sb[s]), acc[m]);
     }
   }
 }
 
 constexpr int kPrefetchUnits = 2;   // units per warp requested into L2 before the PDL wait
 
-template <int MR>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid_constant__ GemvParams p) {
+// Chunks longer than 8 steps, or several activation rows, need more
+// registers: one CTA per SM.
+constexpr int ctas_per_sm(int cs, int mr) { return (cs > 8 || mr > 1) ? 1 : kCtasPerSm; }
+
+template <int MR, int CS>
+__global__ void __launch_bounds__(kThreads, ctas_per_sm(CS, MR)) gemv_kernel(const __grid_constant__ GemvParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -342,14 +390,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid
   float* xscale = reinterpret_cast<float*>(smem + (long long)p.x_slots * MR * 4 * p.Kg * 16);
 
   // Compute cursor `cp` and load cursor `ld` one chunk ahead; two register
-  // buffers.  Dense weights do not depend on earlier kernels: this warp's
-  // first units are requested into L2 and its first chunk into registers
-  // before waiting for the previous kernel (W4_FLAG_PDL), so a launch that is
-  // resident early has its weights in flight already.  Routed ids may come
-  // from the previous kernel and are read after the wait.
+  // buffers used in turn.  Dense weights do not depend on earlier kernels:
+  // this warp's first units are requested into L2 and its first chunk into
+  // registers before waiting for the previous kernel (W4_FLAG_PDL), so a
+  // launch that is resident early has its weights in flight already.  Routed
+  // ids may come from the previous kernel and are read after the wait.
   Cursor cp, ld;
-  uint4 cur[kChunkPerLane], nxt[kChunkPerLane];
-  uint32_t cur_s[kChunkPerLane], nxt_s[kChunkPerLane];
+  Buf<CS> ba, bb;
   const bool dense = p.ids == nullptr;
   if (!dense) pdl_wait();
   for (int d = 0; d < kPrefetchUnits; ++d)
@@ -357,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid
   cp.seek(p, ub + warp, ue, lt, set, true);
   ld = cp;
   if (ld.u < ue) {
-    load_chunk(p, ld, cur, cur_s);
+    load_chunk<CS>(p, ld, ba);
     ld.next_chunk(p, ue, lt, set, false);
   }
   if (dense) pdl_wait();     // activations and outputs follow earlier kernels
@@ -369,33 +416,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid
 #pragma unroll
   for (int m = 0; m < MR; ++m) rowsum[m] = 0.0f;
 
-  while (cp.u < ue) {
-    if (ld.u < ue) {   // next chunk's loads fly while this one is computed
-      load_chunk(p, ld, nxt, nxt_s);
-      ld.next_chunk(p, ue, lt, set, false);
-    }
-    const int xslot = p.x_per_item ? cp.item - item0 : 0;
-    const uint8_t* xrow = xs + (long long)xslot * MR * 4 * p.Kg * 16;
-    const float* srow = xscale + (long long)xslot * MR * p.Kg;
-    float acc[MR];
-#pragma unroll
-    for (int m = 0; m < MR; ++m) acc[m] = 0.0f;
-#pragma unroll
-    for (int s = 0; s < kChunkPerLane; ++s) {
-      if (s < cp.steps) {
-        const int g = cp.g + s * team;
-#pragma unroll
-        for (int m = 0; m < MR; ++m) {
-          uint4 xv[4];
-#pragma unroll
-          for (int w = 0; w < 4; ++w)
-            xv[w] = *reinterpret_cast<const uint4*>(xrow + ((long long)(m * 4 + w) * p.Kg + g) * 16);
-          const float sc = srow[(long long)m * p.Kg + g];
-          acc[m] = fmaf(group_sum(cur[s], xv) * sc, bf16_bits_to_float(cur_s[s]), acc[m]);
-        }
-      }
-    }
-    // chunk sum: fixed xor tree over the team
+  // End of a chunk: team reduction (fixed xor tree), then the chunk sum goes
+  // to the row sum, or to the workspace under split-K.
+  auto finish_chunk = [&](float acc[MR]) {
 #pragma unroll
     for (int m = 0; m < MR; ++m)
       for (int off = team >> 1; off > 0; off >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], off);
@@ -412,42 +435,53 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid
 #pragma unroll
         for (int m = 0; m < MR; ++m) rowsum[m] = 0.0f;
       }
-    } else {
-      if (lt == 0) {
-        float* dst = p.ws_partial +
-                     (((long long)cp.rb * p.nch + cp.c) * p.rows_per_unit + set) * MR;
+      return;
+    }
+    if (lt == 0) {
+      float* dst = p.ws_partial + (((long long)cp.rb * p.nch + cp.c) * p.rows_per_unit + set) * MR;
 #pragma unroll
-        for (int m = 0; m < MR; ++m) dst[m] = acc[m];
-      }
-      if (unit_end) {
-        // the last warp to finish this row block adds the chunk sums in
-        // chunk order, writes the rows and re-arms the counter
+      for (int m = 0; m < MR; ++m) dst[m] = acc[m];
+    }
+    if (unit_end) {
+      // the last warp to finish this row block adds the chunk sums in chunk
+      // order, writes the rows and re-arms the counter
+      __threadfence();
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) last = atomicAdd(p.ws_count + cp.rb, 1) == p.S - 1;
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
         __threadfence();
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) last = atomicAdd(p.ws_count + cp.rb, 1) == p.S - 1;
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
-          __threadfence();
-          const int rbase = (cp.rb - cp.item * p.upi) * p.rows_per_unit;
-          const float* src = p.ws_partial + (long long)cp.rb * p.nch * p.rows_per_unit * MR;
-          for (int e = lane; e < p.rows_per_unit * MR; e += 32) {
-            const int r = e / MR, m = e - r * MR;
-            if (rbase + r >= p.N) continue;
-            float v = 0.0f;
-            for (int c = 0; c < p.nch; ++c)
-              v += __ldcg(src + ((long long)c * p.rows_per_unit + r) * MR + m);
-            p.y[((long long)cp.item * MR + m) * p.N + rbase + r] = __float2bfloat16_rn(v);
-          }
-          if (lane == 0) atomicExch(p.ws_count + cp.rb, 0);
+        const int rbase = (cp.rb - cp.item * p.upi) * p.rows_per_unit;
+        const float* src = p.ws_partial + (long long)cp.rb * p.nch * p.rows_per_unit * MR;
+        for (int e = lane; e < p.rows_per_unit * MR; e += 32) {
+          const int r = e / MR, m = e - r * MR;
+          if (rbase + r >= p.N) continue;
+          float v = 0.0f;
+          for (int c = 0; c < p.nch; ++c) v += __ldcg(src + ((long long)c * p.rows_per_unit + r) * MR + m);
+          p.y[((long long)cp.item * MR + m) * p.N + rbase + r] = __float2bfloat16_rn(v);
         }
+        if (lane == 0) atomicExch(p.ws_count + cp.rb, 0);
       }
     }
-    cp.next_chunk(p, ue, lt, set, true);
+  };
+
+  while (cp.u < ue) {
 #pragma unroll
-    for (int s = 0; s < kChunkPerLane; ++s) {
-      cur[s] = nxt[s];
-      cur_s[s] = nxt_s[s];
+    for (int phase = 0; phase < 2; ++phase) {   // buffers ba, bb in turn
+      Buf<CS>& curb = phase == 0 ? ba : bb;
+      Buf<CS>& nxtb = phase == 0 ? bb : ba;
+      if (cp.u >= ue) break;
+      if (ld.u < ue) {   // next chunk's loads fly while this one is computed
+        load_chunk<CS>(p, ld, nxtb);
+        ld.next_chunk(p, ue, lt, set, false);
+      }
+      const int xslot = p.x_per_item ? cp.item - item0 : 0;
+      float acc[MR];
+      chunk_dot<CS, MR>(p, cp, curb, xs + (long long)xslot * MR * 4 * p.Kg * 16,
+                        xscale + (long long)xslot * MR * p.Kg, acc);
+      finish_chunk(acc);
+      cp.next_chunk(p, ue, lt, set, true);
     }
   }
 }
@@ -482,7 +516,7 @@ DeviceInfo device_info(int dev) {
 struct Plan {
   int MR = 1;
   int team = 32, sets = 1, R = 1, rows_per_unit = 1;
-  int chunk = 0, nch = 1;
+  int chunk = 0, nch = 1, cs = 0;
   int S = 1, cps = 1, upi = 1;
   long long B = 0, U = 0;
   int x_slots = 1;
@@ -492,16 +526,25 @@ struct Plan {
   size_t ws_part_off = 0;
 };
 
-// The per-row arithmetic (team, chunk) comes from K alone.
-void row_shape(int K, int* team, int* chunk, int* nch) {
-  // largest power of two <= 32 that divides K/32 and still leaves each lane
-  // at least kChunkPerLane groups of a row (fewer, longer lane loops amortise
-  // the per-row reduction)
+// The per-row arithmetic (team, chunk) comes from K alone.  team: the largest
+// power of two <= 32 dividing K/32 that leaves each lane >= kChunkPerLane
+// groups of a row.  Chunk steps per lane: the largest divisor of the lane's
+// groups per row in 5..12, so every chunk is full (0 = none: chunks of
+// kChunkPerLane steps, the last one ragged).
+void row_shape(int K, int* team, int* chunk, int* nch, int* cs) {
   const int Kg = K / 32;
   int t = 1;
   while (t < 32 && Kg % (2 * t) == 0 && Kg / (2 * t) >= kChunkPerLane) t *= 2;
   *team = t;
-  *chunk = t * kChunkPerLane;
+  const int q = Kg / t;
+  int c = 0;
+  for (int d = 12; d >= 5 && c == 0; --d)
+    if (q % d == 0) c = d;
+  if (q <= 12) c = q;             // a whole row per chunk
+  if (c != 0 && c != 7 && c != 8 && c != 11 && c != 12 && c != 5 && c != 6 && c != 9 && c != 10)
+    c = 0;
+  *cs = c;
+  *chunk = t * (c > 0 ? c : kChunkPerLane);
   *nch = (Kg + *chunk - 1) / *chunk;
 }
 
@@ -514,7 +557,7 @@ bool make_plan(int MR, int N, int K, int n_items, int allow_split, int x_per_ite
   Plan pl;
   pl.MR = MR;
   const int Kg = K / 32;
-  row_shape(K, &pl.team, &pl.chunk, &pl.nch);
+  row_shape(K, &pl.team, &pl.chunk, &pl.nch, &pl.cs);
   pl.sets = 32 / pl.team;
   const int sms = di.sms > 0 ? di.sms : 1;
   const long long warps = (long long)sms * kWarps * kCtasPerSm;
@@ -533,7 +576,8 @@ bool make_plan(int MR, int N, int K, int n_items, int allow_split, int x_per_ite
   if (pl.U > (1LL << 30)) return false;
   // One CTA per SM leaves room for the next launch's CTA (PDL); problems
   // with many units per warp fill two CTAs per SM instead.
-  const long long per_sm = (pl.U >= 4LL * kCtasPerSm * sms * kWarps) ? kCtasPerSm : 1;
+  const int cap = ctas_per_sm(pl.cs, MR);
+  const long long per_sm = (pl.U >= 4LL * cap * sms * kWarps) ? cap : 1;
   pl.ctas = (int)std::min<long long>(pl.U, per_sm * sms);
   // activation rows a CTA stages: one, or the items its unit range touches
   pl.x_slots = 1;
@@ -560,11 +604,11 @@ bool make_plan(int MR, int N, int K, int n_items, int allow_split, int x_per_ite
   return true;
 }
 
-template <int MR>
+template <int MR, int CS>
 cudaError_t launch_one(const GemvParams& prm, const Plan& pl, bool pdl, cudaStream_t stream, int dev) {
   static std::mutex mu;
   static long long attr_bytes[64] = {};
-  auto kern = gemv_kernel<MR>;
+  auto kern = gemv_kernel<MR, CS>;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   {
     // raise the kernel's dynamic shared-memory limit to what this plan needs
@@ -589,12 +633,27 @@ cudaError_t launch_one(const GemvParams& prm, const Plan& pl, bool pdl, cudaStre
   return cudaLaunchKernelEx(&cfg, kern, prm);
 }
 
+template <int MR>
+cudaError_t launch_cs(const GemvParams& prm, const Plan& pl, bool pdl, cudaStream_t s, int dev) {
+  switch (pl.cs) {
+    case 5: return launch_one<MR, 5>(prm, pl, pdl, s, dev);
+    case 6: return launch_one<MR, 6>(prm, pl, pdl, s, dev);
+    case 7: return launch_one<MR, 7>(prm, pl, pdl, s, dev);
+    case 8: return launch_one<MR, 8>(prm, pl, pdl, s, dev);
+    case 9: return launch_one<MR, 9>(prm, pl, pdl, s, dev);
+    case 10: return launch_one<MR, 10>(prm, pl, pdl, s, dev);
+    case 11: return launch_one<MR, 11>(prm, pl, pdl, s, dev);
+    case 12: return launch_one<MR, 12>(prm, pl, pdl, s, dev);
+    default: return launch_one<MR, 0>(prm, pl, pdl, s, dev);
+  }
+}
+
 cudaError_t launch(const GemvParams& prm, const Plan& pl, bool pdl, cudaStream_t s, int dev) {
   switch (pl.MR) {
-    case 1: return launch_one<1>(prm, pl, pdl, s, dev);
-    case 2: return launch_one<2>(prm, pl, pdl, s, dev);
-    case 3: return launch_one<3>(prm, pl, pdl, s, dev);
-    case 4: return launch_one<4>(prm, pl, pdl, s, dev);
+    case 1: return launch_cs<1>(prm, pl, pdl, s, dev);
+    case 2: return launch_cs<2>(prm, pl, pdl, s, dev);
+    case 3: return launch_cs<3>(prm, pl, pdl, s, dev);
+    case 4: return launch_cs<4>(prm, pl, pdl, s, dev);
     default: return cudaErrorInvalidConfiguration;
   }
 }
@@ -705,7 +764,7 @@ extern "C" w4_status w4a16_gemv_plan(int M, int N, int K, w4_plan_info* info) {
   info->rows_per_lane = pl.R;
   info->smem_bytes = (int)pl.smem;
   info->rows_per_call = pl.MR;
-  info->ring_slots = 2;   // current and next chunk
+  info->chunk_steps = pl.cs;
   return W4_OK;
 }
 

@@ -38,7 +38,7 @@ class W4Error(RuntimeError):
 class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("path", "ctas", "slices", "threads", "team",
                                             "unit_rows", "chunk_groups", "rows_per_lane",
-                                            "smem_bytes", "rows_per_call", "ring_slots")]
+                                            "smem_bytes", "rows_per_call", "chunk_steps")]
 
 
 _lib = None

@@ -278,7 +278,7 @@ typedef struct w4_plan_info {
     int rows_per_lane;  /* rows a lane works on together (activation reuse) */
     int smem_bytes;     /* dynamic shared memory per CTA */
     int rows_per_call;  /* activation rows handled per launch */
-    int ring_slots;     /* register-ring depth of the load pipeline (steps) */
+    int chunk_steps;    /* groups per lane per K chunk (0 = ragged chunks of 8) */
 } w4_plan_info;
 
 w4_status w4a16_gemv_plan(int M, int N, int K, w4_plan_info *info);

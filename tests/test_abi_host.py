@@ -83,7 +83,10 @@ def test_plan_is_valid(M, N, K):
     assert p["team"] in (1, 2, 4, 8, 16, 32) and (K // 32) % p["team"] == 0
     assert p["rows_per_lane"] == 1
     assert p["unit_rows"] == (32 // p["team"]) * p["rows_per_lane"]
-    assert p["chunk_groups"] == 8 * p["team"]
+    cs = p["chunk_steps"]           # chunk steps per lane, 0 = ragged chunks of 8
+    assert p["chunk_groups"] == p["team"] * (cs if cs else 8)
+    if cs:
+        assert (K // 32) % p["chunk_groups"] == 0
     assert 1 <= p["ctas"] <= 2 * 152
     assert p["smem_bytes"] <= 232448
     assert p["rows_per_call"] == min(M, 4 if K <= 16384 else 1)
