@@ -53,6 +53,15 @@ def load_peaks():
         return FALLBACK["hbm_gbs"], "fallback"
 
 
+def max_over_ranks(value: float, device) -> float:
+    """Largest value over all ranks (identity for one process)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -427,10 +436,7 @@ def run_gb300(args, world, rank, local):
     torch.cuda.synchronize()
     ms = time_replays(g, stream, args.steps)
     torch.cuda.synchronize()
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
     clocks = sampler.stop()
     if int(dp.status.item()) != 0:
         raise RuntimeError(f"device status {int(dp.status.item())}")
@@ -521,6 +527,39 @@ def run_gb300(args, world, rank, local):
     return 0
 
 
+def run_shape(args):
+    """One GEMV shape, timed alone: rotating weight copies (over 4x the L2
+    together, so every launch reads HBM), graph replay, CUDA events."""
+    from bit_weight_only_gemv_gb300 import lib
+    lib.load()
+    M, N, K = (int(v) for v in args.shape.split(","))
+    dev = torch.device("cuda", 0)
+    per = metrics.gemv_bytes(M, N, K)
+    copies = max(2, -(-600_000_000 // per))
+    qws = [synth.torch_words((N, K // 8), synth.seed_of(7, i), dev) for i in range(copies)]
+    sts = [synth.torch_steps((N, K // 32), synth.seed_of(8, i), dev) for i in range(copies)]
+    x = synth.torch_x((M, K), synth.seed_of(9), dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    need = lib.workspace_bytes(M, N, K)
+    ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev) if need else None
+    fns = [(lambda q, s_: (lambda pdl: lib.gemv(q, s_, x, y=y, workspace=ws, pdl=pdl)))(q, s_)
+           for q, s_ in zip(qws, sts)]
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for i, f in enumerate(fns):
+            f(i > 0)
+    torch.cuda.synchronize()
+    g = capture(fns, stream, pdl=not args.no_pdl)
+    for _ in range(args.warmup):
+        g.replay()
+    ms = time_replays(g, stream, args.steps) / copies
+    print(json.dumps({"mode": "shape", "M": M, "N": N, "K": K, "pdl": not args.no_pdl,
+                      "us_per_launch": ms * 1e3, "gbps": metrics.gbps(per, ms * 1e-3),
+                      "bytes_per_launch": per, "copies": copies, "plan": lib.plan(M, N, K)}),
+          flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -528,6 +567,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shape", default=None,
+                    help="M,N,K: time one GEMV shape alone instead of the decode pass")
+    ap.add_argument("--no-pdl", action="store_true", help="with --shape: plain launches")
     ap.add_argument("--separate", action="store_true",
                     help="one GEMV per projection instead of merged q/k/v and gate/up")
     args = ap.parse_args()
@@ -542,6 +584,8 @@ def main():
     try:
         if args.impl == "reference":
             return run_reference(args, world, rank)
+        if args.shape:
+            return run_shape(args)
         return run_gb300(args, world, rank, local)
     finally:
         if world > 1 and torch.distributed.is_initialized():
