@@ -868,3 +868,90 @@ extern "C" w4_status w4a16_gemv_id(void* y, const void* qw_base, size_t qw_strid
   }
   return W4_OK;
 }
+
+// ================================================================= no-allocation variant
+// Split-K GEMV whose scratch lives in a fixed device array compiled into the
+// library, for callers that cannot allocate device memory themselves (see
+// w4a16_gemv_static_scratch in w4a16.h).  Every GPU that loads the library
+// holds this array until the process exits.
+static __device__ __align__(256) unsigned char w4_static_scratch[W4_STATIC_SCRATCH_BYTES];
+
+namespace w4 {
+namespace {
+
+// Device address of w4_static_scratch on device `dev` (the host-side name is
+// only a stand-in).  Looked up once per device, with that device current.
+cudaError_t static_scratch_address(int dev, void** out) {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, w4_static_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace w4
+
+extern "C" w4_status w4a16_gemv_static_scratch(void* y, const void* qw, const void* st,
+                                               const void* x, int M, int N, int K,
+                                               int32_t* status_dev, unsigned flags,
+                                               w4_stream_t stream) {
+  if (y == nullptr || qw == nullptr || st == nullptr || x == nullptr) return W4_ERR_ARG;
+  if (M < 1 || N < 1 || (flags & ~W4_FLAG_PDL) != 0) return W4_ERR_ARG;
+  if (M > W4_MAX_M || K < 32 || K % 32 != 0 || K > W4_MAX_K) return W4_ERR_SHAPE;
+  if (!aligned(qw, 16) || !aligned(st, 16) || !aligned(x, 16) || !aligned(y, 2))
+    return W4_ERR_ALIGN;
+  int dev = 0;
+  DeviceInfo di;
+  if (!current_device(&dev, &di)) return W4_ERR_DEVICE;
+  const int mr_cap = max_rows_per_launch(K, di);
+  if (mr_cap < 1) return W4_ERR_SHAPE;
+  // every launch of this call must fit the fixed array: check before any work
+  for (int m0 = 0; m0 < M; m0 += mr_cap) {
+    Plan pm;
+    if (!cached_plan(std::min(mr_cap, M - m0), N, K, 1, 1, 0, di, &pm)) return W4_ERR_SHAPE;
+    if (pm.ws_bytes > (size_t)W4_STATIC_SCRATCH_BYTES) return W4_ERR_WORKSPACE;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  for (int m0 = 0; m0 < M; m0 += mr_cap) {
+    const int mr = std::min(mr_cap, M - m0);
+    Plan pm;
+    cached_plan(mr, N, K, 1, 1, 0, di, &pm);
+    GemvParams p = base_params(pm, N, K);
+    p.qw = static_cast<const uint8_t*>(qw);
+    p.st = static_cast<const uint8_t*>(st);
+    p.x = static_cast<const __nv_bfloat16*>(x) + (long long)m0 * K;
+    p.y = static_cast<__nv_bfloat16*>(y) + (long long)m0 * N;
+    p.n_items = 1;
+    p.num_experts = 1;
+    p.status = status_dev;
+    if (pm.ws_bytes > 0) {
+      void* base = nullptr;
+      cudaError_t e = static_scratch_address(dev, &base);
+      // the counters must start at zero; the array keeps the previous call's
+      // contents (and an aborted call may leave them armed)
+      if (e == cudaSuccess) e = cudaMemsetAsync(base, 0, (size_t)pm.B * sizeof(int), s);
+      if (e != cudaSuccess) {
+        note_cuda_error(e);
+        cudaGetLastError();
+        return W4_ERR_LAUNCH;
+      }
+      p.ws_count = static_cast<int*>(base);
+      p.ws_partial = reinterpret_cast<float*>(static_cast<uint8_t*>(base) + pm.ws_part_off);
+    }
+    const cudaError_t e = launch(p, pm, (flags & W4_FLAG_PDL) != 0, s, dev);
+    if (e != cudaSuccess) {
+      note_cuda_error(e);
+      cudaGetLastError();
+      return W4_ERR_LAUNCH;
+    }
+  }
+  return W4_OK;
+}

@@ -25,7 +25,8 @@ STATUS_CODE = {v: k for k, v in STATUS.items()}
 EXPORTS = ("w4_status_str", "w4_abi_version", "w4_last_cuda_error", "w4a16_gemv", "w4a16_gemv_workspace_bytes",
            "w4a16_gemv_id", "w4_embed_gather", "w4_pack", "w4_quantize",
            "w4_slot_pool_create", "w4_slot_pool_destroy", "w4_slot_pool_remap",
-           "w4_slot_pool_stage", "w4_slot_pool_stats", "w4a16_gemv_plan")
+           "w4_slot_pool_stage", "w4_slot_pool_stats", "w4a16_gemv_plan",
+           "w4a16_gemv_static_scratch")
 
 
 class W4Error(RuntimeError):
@@ -61,6 +62,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.w4_last_cuda_error.argtypes = []
     lib.w4a16_gemv.restype = i32
     lib.w4a16_gemv.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, sz, vp, u32, vp]
+    lib.w4a16_gemv_static_scratch.restype = i32
+    lib.w4a16_gemv_static_scratch.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, u32, vp]
     lib.w4a16_gemv_workspace_bytes.restype = sz
     lib.w4a16_gemv_workspace_bytes.argtypes = [i32, i32, i32]
     lib.w4a16_gemv_id.restype = i32

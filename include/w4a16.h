@@ -123,6 +123,41 @@ w4_status w4a16_gemv(void *y, const void *qw, const void *st, const void *x,
 size_t w4a16_gemv_workspace_bytes(int M, int N, int K);
 
 /*
+ * w4a16_gemv_static_scratch — w4a16_gemv without a caller-provided workspace.
+ *
+ * No passage of the source pages corresponds to this call; it exists for
+ * callers that cannot allocate device memory: code that runs inside a host
+ * framework owning every device allocation, code on a latency-critical path
+ * where an allocation (which may synchronise the device) is not allowed, and
+ * plain C callers with no way to keep a per-call workspace alive.  The
+ * split-K scratch that w4a16_gemv takes as `workspace` is instead a fixed
+ * array of W4_STATIC_SCRATCH_BYTES compiled into the library; every GPU that
+ * loads the library holds it until the process exits.
+ *
+ * Arguments, layouts, results and errors are those of w4a16_gemv (the same
+ * bits for the same inputs).  Inputs and outputs are still caller-owned
+ * device buffers; the call allocates nothing (no cudaMalloc / cudaFree and
+ * no allocating library routine).
+ *
+ *  - A shape whose split-K plan needs more than W4_STATIC_SCRATCH_BYTES of
+ *    scratch (w4a16_gemv_workspace_bytes(M, N, K)) returns W4_ERR_WORKSPACE
+ *    before any work is enqueued.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - All calls on a device share that device's one array, which keeps the
+ *    last call's contents: each call first clears, on its stream, the part
+ *    that must start at zero.  Calls on the same device that may overlap on
+ *    the GPU (for example issued to different streams) race on the array:
+ *    issue them one after another in one stream per device.
+ */
+#define W4_STATIC_SCRATCH_BYTES (4u << 20)
+
+w4_status w4a16_gemv_static_scratch(void *y, const void *qw, const void *st, const void *x,
+                                    int M, int N, int K, int32_t *status_dev,
+                                    unsigned flags, w4_stream_t stream);
+
+/*
  * w4a16_gemv_id — routed-expert GEMV through an expert (or slot) index.
  *
  * Page "Running a 26B MoE on an 8 GB Jetson by streaming experts from SSD",
