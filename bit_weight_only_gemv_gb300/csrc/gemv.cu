@@ -266,9 +266,14 @@ struct Cursor {
   // First unit at or after uu (stride kWarps) with a valid expert id.
   __device__ void seek(const GemvParams& p, int uu, int ue, int lt, int set, bool rep) {
     for (u = uu; u < ue; u += kWarps) {
-      slice = u / p.B;
-      rb = u - slice * p.B;
-      item = rb / p.upi;
+      if (p.S == 1) {          // common cases without divisions
+        slice = 0;
+        rb = u;
+      } else {
+        slice = u / p.B;
+        rb = u - slice * p.B;
+      }
+      item = (p.n_items == 1) ? 0 : rb / p.upi;
       row = (rb - item * p.upi) * p.rows_per_unit + set;
       long long blk = item;
       if (p.ids != nullptr) {
@@ -577,7 +582,7 @@ bool make_plan(int MR, int N, int K, int n_items, int allow_split, int x_per_ite
   // One CTA per SM leaves room for the next launch's CTA (PDL); problems
   // with many units per warp fill two CTAs per SM instead.
   const int cap = ctas_per_sm(pl.cs, MR);
-  const long long per_sm = (pl.U >= 4LL * cap * sms * kWarps) ? cap : 1;
+  const long long per_sm = (pl.U >= (long long)cap * sms * kWarps) ? cap : 1;
   pl.ctas = (int)std::min<long long>(pl.U, per_sm * sms);
   // activation rows a CTA stages: one, or the items its unit range touches
   pl.x_slots = 1;
