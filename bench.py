@@ -238,7 +238,8 @@ def kernel_key(kind, shape, lib):  # ncu names the instantiation
         return "gather_kernel"
     M, N, K = shape
     p = lib.plan(M, N, K)
-    return f"gemv_kernel<{p['rows_per_call']}, {p['chunk_steps']}>"
+    return (f"gemv_kernel<{p['rows_per_call']}, {p['rows_per_lane']}, "
+            f"{p['tmpl_team']}, {p['tmpl_chunk']}>")
 
 
 def capture(fns, stream, pdl=True):

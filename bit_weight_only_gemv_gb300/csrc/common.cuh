@@ -123,6 +123,15 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) {
   return __uint_as_float(b16 << 16);
 }
 
+// Atomic add with acquire-release semantics at GPU scope; returns the old
+// value.  Publishes the caller's earlier stores (and those ordered before it
+// by a barrier) and makes stores published by earlier releases visible.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // (a & b) | c in one LOP3.
 __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;

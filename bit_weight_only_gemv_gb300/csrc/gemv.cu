@@ -8,16 +8,22 @@
 // SSD", section "Streaming without touching a single GPU kernel") reads expert
 // `id` at base + id * stride.
 //
-// Design (persistent CTAs of 8 warps, one or two per SM):
+// Design (CTAs of 7 consumer warps + 1 producer warp, one or two per SM):
+//  * The producer warp streams weight tiles (a window of rows x one K chunk:
+//    packed codes and bf16 steps) from HBM into a ring of shared-memory
+//    stages with 1-D bulk copies on the TMA engine.  One mbarrier per stage
+//    counts the bytes in ("full"), another the consumer warps done with it
+//    ("empty").  The copies need no registers, so several tiles are in
+//    flight per CTA while the consumers compute, and with W4_FLAG_PDL the
+//    first tiles are requested before the previous kernel has finished.
 //  * The activation rows are staged once per CTA in shared memory as fp16
 //    pairs scaled by a power of two per group of 32 (exact), next to the
 //    group's inverse scale.
-//  * A team of `team` lanes shares an output row (team = the largest power
-//    of two <= 32 dividing K/32 that leaves each lane >= 8 groups of a row,
-//    so no lane idles); each lane walks the groups lane, lane + team, ...
-//  * Packed codes and steps go straight from HBM to registers with coalesced
-//    128-bit (codes) loads that bypass L1; the weights never touch shared
-//    memory, which keeps shared-memory bandwidth for the activations.
+//  * A team of T lanes shares an output row (T = a power of two dividing
+//    K/32, chosen from K alone); lane t of the team owns groups t, t + T, ...
+//    of the row.  A lane loads one group's activations once and applies them
+//    to RW rows of the tile (activation reuse), reading each row's codes and
+//    steps from shared memory.
 //  * Per group and row the lane turns each packed word into four fp16 pairs
 //    (c - 8) with the float-bit trick of the page in its fp16 form
 //    ((0x6400 | c) - 1032 = c - 8, exact), multiplies them with the fp16
@@ -25,21 +31,21 @@
 //    over the group's 4 words in fp16 (at most 3 roundings: 3 * 2^-11 of
 //    sum|w x|), adds the 8 partial sums in fp32, rescales by the group's 2^-e
 //    (exact), multiplies by the step and accumulates in fp32.
-//  * K is cut into chunks of 8 groups per lane; the loads of the next chunk
-//    are in flight (second register buffer) while a chunk is computed, and
-//    the first chunk is requested before waiting on the previous kernel.
-//    After each chunk the team reduces with a fixed xor-shuffle tree and
-//    chunk sums are added in chunk order.  A row's arithmetic therefore
-//    depends on K only, never on N, the row index, the split or the
-//    addresses: results are bitwise reproducible and a gemv_id row equals
-//    the gemv of that expert.
-//  * Work unit = (row block of 32/team rows, K slice).  Each CTA owns a
-//    balanced contiguous range of units; its warps take them round-robin.
-//    Split-K (slices > 1): chunk sums go to the workspace and the warp that
-//    finishes a row block last (atomic counter, no waiting) adds them in
-//    chunk order, writes the rows and re-arms the counter.
-//  * With W4_FLAG_PDL the launch may overlap the previous kernel in the
-//    stream; all global reads and writes happen after waiting for it.
+//  * K is cut into chunks of CL groups per lane (CL from K alone).  After
+//    each chunk the team reduces with a fixed xor-shuffle tree and the chunk
+//    sums of a row are added in chunk order.  A row's arithmetic therefore
+//    depends on K only, never on N, M, the row index, the tiling, the split
+//    or the addresses: results are bitwise reproducible, a gemv_id row
+//    equals the gemv of that expert, and merged projections equal separate
+//    ones.
+//  * Each CTA owns a balanced contiguous range of rows (split-K: of (row
+//    block, K slice) units).  Split-K writes chunk sums to the workspace; per
+//    row block and warp, the last of the slices to finish (atomic counter,
+//    no waiting) adds them in chunk order, writes the rows and re-arms the
+//    counter.
+//  * Every wait is bounded: on expiry the kernel records W4_ERR_TIMEOUT, the
+//    warps leave without further waiting, and the producer lets its copies
+//    in flight land (bounded) before the CTA exits.
 #include <algorithm>
 #include <mutex>
 
@@ -47,11 +53,13 @@
 
 namespace w4 {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = 32 * kWarps;
-constexpr int kCtasPerSm = 2;    // two resident CTAs per SM: this launch and the next
-constexpr int kMaxMR = 4;        // activation rows per launch
-constexpr int kChunkPerLane = 8; // groups per lane per chunk
+constexpr int kConsumerWarps = 7;
+constexpr int kConsumers = 32 * kConsumerWarps;
+constexpr int kThreads = kConsumers + 32;   // + the producer warp
+constexpr int kMaxMR = 4;                   // activation rows per launch
+constexpr int kMaxStages = 8;
+constexpr int kBarBytes = 256;              // full[8], empty[8], abort flag
+constexpr long long kWaitCycles = 1LL << 31;
 
 struct GemvParams {
   const uint8_t* qw;
@@ -66,13 +74,17 @@ struct GemvParams {
   int MR;                              // activation rows per item in this launch
   int N, K, Kg;
   int n_items;
-  int team, sets, R, rows_per_unit;    // lanes per row, row sets per warp, rows per lane
-  int chunk, nch;                      // groups per chunk (team * 8), chunks per row
+  int T, nsw;                          // lanes per row, row sets per warp (32 / T)
+  int NI, CL, nch;                     // groups per lane per row, per chunk; chunks
+  int RB;                              // rows of a tile window (7 warps * nsw * RW)
   int S, cps, upi;                     // slices, chunks per slice, row blocks per item
-  int B, U;                            // row blocks, units (= S * B)
+  int B;                               // row blocks (split-K only)
+  long long U;                         // work items: rows (S == 1) or units
   int x_slots;                         // activation rows staged per CTA (per MR row)
-  int* ws_count;                       // [B] at the start of the workspace
-  float* ws_partial;                   // [B][nch][rows_per_unit][MR] after it
+  int nst;                             // pipeline stages
+  int tile_bytes, code_pitch, step_pitch, step_off;
+  int* ws_count;                       // [B][7] at the start of the workspace
+  float* ws_partial;                   // [B][nch][RB][MR] after it
   int32_t* status;
 };
 
@@ -82,10 +94,10 @@ struct GemvParams {
 // lies in [2^9, 2^10).  Layout for staged row j (= slot * MR + m): 16-byte
 // chunk (w, g) = pairs (x[8w+p], x[8w+p+4]) for p = 0..3 of group g, at
 // ((j * 4 + w) * Kg + g) * 16; the inverse scale 2^-e of the group at
-// xscale[j * Kg + g].
+// xscale[j * Kg + g].  Run by the consumer threads.
 __device__ void stage_x(const GemvParams& p, int item0, int nslots, uint8_t* xs, float* xscale) {
   const int rows = nslots * p.MR;
-  for (int idx = threadIdx.x; idx < rows * p.Kg; idx += kThreads) {
+  for (int idx = threadIdx.x; idx < rows * p.Kg; idx += kConsumers) {
     const int j = idx / p.Kg;
     const int g = idx - j * p.Kg;
     const int slot = j / p.MR, m = j - slot * p.MR;
@@ -192,301 +204,424 @@ __device__ __forceinline__ float group_sum(const uint4 q, const uint4 xv[4]) {
   return add_pair_f32(gs, a3);
 }
 
-__device__ __forceinline__ uint4 ldg_stream16(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
+// ---------------------------------------------------------------- work walk
+// The producer and the consumers of a CTA walk the same sequence of windows
+// (item, rows [row0, row0 + nrows), chunks [c0, c1)); each (window, chunk)
+// is one tile of the stage ring.
+struct Walk {
+  long long pos, end;   // next work item, end of the CTA's range
+  int item, row0, nrows, c0, c1, rb;
 
-__device__ __forceinline__ uint32_t ldg_stream2(const void* p) {
-  unsigned short v;
-  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
-  return v;
-}
+  __device__ void init(const GemvParams& p) {
+    pos = (long long)blockIdx.x * p.U / gridDim.x;
+    end = (long long)(blockIdx.x + 1) * p.U / gridDim.x;
+  }
+  __device__ bool next(const GemvParams& p) {
+    if (pos >= end) return false;
+    if (p.S == 1) {   // rows of the flattened (item, row) space
+      const long long r = pos;
+      item = (p.n_items == 1) ? 0 : (int)(r / p.N);
+      row0 = (int)(r - (long long)item * p.N);
+      nrows = (int)min(min((long long)p.RB, end - r), (long long)(p.N - row0));
+      c0 = 0;
+      c1 = p.nch;
+      rb = 0;
+      pos += nrows;
+    } else {          // (slice, row block) units, slice-major
+      const int slice = (int)(pos / p.B);
+      rb = (int)(pos - (long long)slice * p.B);
+      item = rb / p.upi;
+      row0 = (rb - item * p.upi) * p.RB;
+      nrows = min(p.RB, p.N - row0);
+      c0 = slice * p.cps;
+      c1 = min(c0 + p.cps, p.nch);
+      pos += 1;
+    }
+    return true;
+  }
+};
 
-// Lanes of one warp: ask L2 for the codes and steps of unit `u` (rows of the
-// unit's row block, groups of its K slice).  Ranges are clipped to 16-byte
-// lines inside the item's arrays; bytes outside them are simply not
-// prefetched.
-__device__ __forceinline__ void prefetch_unit(const GemvParams& p, int u, int lane) {
-  if (u >= p.U) return;
-  const int slice = u / p.B;
-  const int rb = u - slice * p.B;
-  const int item = rb / p.upi;
-  const int row0 = (rb - item * p.upi) * p.rows_per_unit;
-  const int rows = min(p.rows_per_unit, p.N - row0);
+// Codes and steps of `item` (false: routed id out of range; its rows are left
+// unwritten).
+__device__ __forceinline__ bool item_arrays(const GemvParams& p, int item, const uint8_t** q,
+                                            const uint8_t** s) {
   long long blk = item;
   if (p.ids != nullptr) {
     const int e = __ldg(p.ids + item);
-    if (e < 0 || e >= p.num_experts) return;
+    if (e < 0 || e >= p.num_experts) return false;
     blk = e;
   }
-  const uint8_t* qw = p.qw + (unsigned long long)blk * p.qw_item_stride;
-  const uint8_t* st = p.st + (unsigned long long)blk * p.st_item_stride;
-  const long long row_bytes = (long long)p.K / 2, st_row = (long long)p.Kg * 2;
-  const long long st_lim = ((long long)p.N * st_row) & ~15LL;
-  const int g0 = slice * p.cps * p.chunk;
-  const int g1 = min((slice + 1) * p.cps * p.chunk, p.Kg);
-  if (p.S == 1) {   // whole rows: one contiguous range each for codes and steps
-    if (lane == 0) {
-      prefetch_l2_bulk(qw + row0 * row_bytes, (uint32_t)(rows * row_bytes));
-      const long long b = (row0 * st_row) & ~15LL;
-      const long long e = min((((long long)(row0 + rows) * st_row) + 15) & ~15LL, st_lim);
-      if (e > b) prefetch_l2_bulk(st + b, (uint32_t)(e - b));
-    }
-  } else if (lane < rows) {
-    const long long r = row0 + lane;
-    prefetch_l2_bulk(qw + r * row_bytes + (long long)g0 * 16, (uint32_t)(g1 - g0) * 16);
-    const long long b = (r * st_row + (long long)g0 * 2) & ~15LL;
-    const long long e = min((r * st_row + (long long)g1 * 2 + 15) & ~15LL, st_lim);
-    if (e > b) prefetch_l2_bulk(st + b, (uint32_t)(e - b));
+  *q = p.qw + (unsigned long long)blk * p.qw_item_stride;
+  *s = p.st + (unsigned long long)blk * p.st_item_stride;
+  return true;
+}
+
+// Bounded wait on a stage barrier that also gives up once another warp of
+// the CTA has aborted.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag != 0) return false;
+    if (clock64() - t0 > kWaitCycles) return false;
   }
 }
 
-// ---------------------------------------------------------------- kernel
-// A warp's position in its walk over (unit, chunk) pairs.  Chunk c of a unit
-// holds, for this lane, the groups g = c*chunk + lane_in_team + s*team for
-// s < steps (steps = chunk / team, smaller only in a ragged last chunk).
-struct Cursor {
-  int u;                // current unit (>= end when the walk is over)
-  int c, c_end;         // chunk and end chunk of the unit's slice
-  int steps;            // groups of this chunk per lane
-  int g;                // this lane's first group of the chunk
-  int item, rb, slice;
-  int row;              // this lane's row
-  const uint8_t* qrow;  // codes of the row
-  const uint8_t* srow;  // steps of the row
-
-  __device__ void set_chunk(const GemvParams& p, int lt) {
-    g = c * p.chunk + lt;
-    steps = (min((c + 1) * p.chunk, p.Kg) - c * p.chunk) / p.team;
+// ---------------------------------------------------------------- producer
+// All 32 lanes of the producer warp: request tile (window wk, chunk c) into
+// the stage at shared address `stage` (generic pointer `stage_ptr`).
+//  * codes: whole-row windows (one chunk per row) are one contiguous copy;
+//    otherwise one copy per row of the chunk's bytes.
+//  * steps: the 16-byte-aligned superset of the needed bytes, clipped to the
+//    item's last full 16-byte line; the bytes past that line (at most 14, at
+//    the very end of the item's step array) are stored by hand.  A row's
+//    steps start at (row * Kg * 2 + first group * 2) mod 16 in its slot.
+__device__ void issue_tile(const GemvParams& p, const Walk& wk, int c, const uint8_t* qwi,
+                           const uint8_t* sti, uint32_t stage, uint8_t* stage_ptr, uint32_t full,
+                           int lane, uint64_t pol) {
+  const int gpc = p.CL * p.T;
+  const int gs0 = c * gpc;
+  const int gs1 = min(gs0 + gpc, p.Kg);
+  const long long row_code = (long long)p.K / 2, row_st = (long long)p.Kg * 2;
+  const uintptr_t sbase = reinterpret_cast<uintptr_t>(sti);
+  const uintptr_t st_lim = (sbase + (uintptr_t)((long long)p.N * row_st)) & ~(uintptr_t)15;
+  const bool whole = p.nch == 1;
+  const int copies = whole ? 1 : wk.nrows;
+  const int rows = whole ? wk.nrows : 1;
+  uint32_t bytes = 0;
+  for (int r = lane; r < copies; r += 32) {
+    const long long row = wk.row0 + r;
+    bytes += (uint32_t)(rows * (gs1 - gs0) * 16);
+    const uintptr_t a0 = sbase + (uintptr_t)(row * row_st + gs0 * 2);
+    const uintptr_t e = whole ? sbase + (uintptr_t)((row + rows) * row_st) : a0 + (gs1 - gs0) * 2;
+    const uintptr_t a = a0 & ~(uintptr_t)15;
+    const uintptr_t b = min((e + 15) & ~(uintptr_t)15, st_lim);
+    if (b > a) bytes += (uint32_t)(b - a);
+    uint8_t* dst = stage_ptr + p.step_off + (whole ? 0 : r * p.step_pitch);
+    for (uintptr_t q = max(a, b); q < e; q += 2)
+      *reinterpret_cast<uint16_t*>(dst + (q - a)) = *reinterpret_cast<const uint16_t*>(q);
   }
-  // First unit at or after uu (stride kWarps) with a valid expert id.
-  __device__ void seek(const GemvParams& p, int uu, int ue, int lt, int set, bool rep) {
-    for (u = uu; u < ue; u += kWarps) {
-      if (p.S == 1) {          // common cases without divisions
-        slice = 0;
-        rb = u;
-      } else {
-        slice = u / p.B;
-        rb = u - slice * p.B;
-      }
-      item = (p.n_items == 1) ? 0 : rb / p.upi;
-      row = (rb - item * p.upi) * p.rows_per_unit + set;
-      long long blk = item;
-      if (p.ids != nullptr) {
-        const int e = __ldg(p.ids + item);
-        if (e < 0 || e >= p.num_experts) {   // leave this unit's rows unwritten
-          if (rep) report(p.status, W4_ERR_INDEX);
-          continue;
-        }
-        blk = e;
-      }
-      c = slice * p.cps;
-      c_end = min(c + p.cps, p.nch);
-      set_chunk(p, lt);
-      qrow = p.qw + (unsigned long long)blk * p.qw_item_stride + (long long)row * (p.K / 2);
-      srow = p.st + (unsigned long long)blk * p.st_item_stride + (long long)row * (p.Kg * 2);
-      return;
-    }
-  }
-  __device__ void next_chunk(const GemvParams& p, int ue, int lt, int set, bool rep) {
-    if (++c < c_end) {
-      set_chunk(p, lt);
-      return;
-    }
-    seek(p, u + kWarps, ue, lt, set, rep);
-  }
-};
-
-// Chunk register buffer: CS groups of one row for this lane.  CS > 0: every
-// chunk has exactly CS steps; CS == 0: up to kChunkPerLane, guarded.
-template <int CS>
-struct Buf {
-  static constexpr int kN = CS > 0 ? CS : kChunkPerLane;
-  uint4 code[kN];
-  uint32_t sb[kN];
-};
-
-// Load the codes and steps of cursor c's chunk (rows past N and steps past a
-// ragged chunk get code 8 and step 0, which contribute nothing).
-template <int CS>
-__device__ __forceinline__ void load_chunk(const GemvParams& p, const Cursor& c, Buf<CS>& b) {
-  const uint8_t* q = c.qrow + c.g * 16;
-  const uint8_t* st = c.srow + c.g * 2;
-  const int qstep = p.team * 16, sstep = p.team * 2;
-  if (c.row < p.N) {
-#pragma unroll
-    for (int s = 0; s < Buf<CS>::kN; ++s) {
-      if (CS > 0 || s < c.steps) {
-        b.code[s] = ldg_stream16(q + s * qstep);
-        b.sb[s] = ldg_stream2(st + s * sstep);
-      } else {
-        b.code[s] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
-        b.sb[s] = 0;
-      }
-    }
-  } else {
-#pragma unroll
-    for (int s = 0; s < Buf<CS>::kN; ++s) {
-      b.code[s] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
-      b.sb[s] = 0;
-    }
+  bytes = __reduce_add_sync(0xffffffffu, bytes);
+  __syncwarp();
+  if (lane == 0) mbar_arrive_expect_tx(full, bytes);   // also releases the hand-stored tails
+  __syncwarp();
+  for (int r = lane; r < copies; r += 32) {
+    const long long row = wk.row0 + r;
+    const uint8_t* src = qwi + row * row_code + (long long)gs0 * 16;
+    bulk_g2s_evict_first(stage + (whole ? 0 : r * p.code_pitch), src,
+                         (uint32_t)(rows * (gs1 - gs0) * 16), full, pol);
+    const uintptr_t a0 = sbase + (uintptr_t)(row * row_st + gs0 * 2);
+    const uintptr_t e = whole ? sbase + (uintptr_t)((row + rows) * row_st) : a0 + (gs1 - gs0) * 2;
+    const uintptr_t a = a0 & ~(uintptr_t)15;
+    const uintptr_t b = min((e + 15) & ~(uintptr_t)15, st_lim);
+    if (b > a)
+      bulk_g2s_evict_first(stage + p.step_off + (whole ? 0 : r * p.step_pitch),
+                           reinterpret_cast<const void*>(a), (uint32_t)(b - a), full, pol);
   }
 }
 
-// Sum over the chunk's steps, in step order, for every activation row.
-template <int CS, int MR>
-__device__ __forceinline__ void chunk_dot(const GemvParams& p, const Cursor& c, const Buf<CS>& b,
-                                          const uint8_t* xrow, const float* srow, float acc[MR]) {
-  const int kgs = p.Kg * 16;                 // bytes between the 4 word planes
-  const uint8_t* x0 = xrow + c.g * 16;
-  const float* s0 = srow + c.g;
-  const int xstep = p.team * 16;
+// ---------------------------------------------------------------- consumers
+constexpr int kMaxCL = 4;   // groups per lane per chunk, at most
+
+// One chunk of a tile: for each of its `ns` (<= kMaxCL) groups per lane, the
+// lane loads the group's staged activations (MR rows) once and applies them
+// to its RW rows.  acc[j][m] = sum over the chunk's groups, in group order.
+// TT, CLT > 0 fix the team size and the (always full) chunk length at compile
+// time, so every shared-memory offset is an immediate.
+template <int MR, int RW, int TT, int CLT>
+__device__ __forceinline__ void tile_dot(const uint8_t* sm, uint32_t xo, uint32_t xso, int xplane,
+                                         int xmrow, int xsmrow, const uint32_t co[RW],
+                                         const uint32_t so[RW], int ns, int T,
+                                         float acc[RW][MR]) {
 #pragma unroll
-  for (int m = 0; m < MR; ++m) acc[m] = 0.0f;
+  for (int j = 0; j < RW; ++j)
 #pragma unroll
-  for (int s = 0; s < Buf<CS>::kN; ++s) {
-    if (CS == 0 && s >= c.steps) break;
+    for (int m = 0; m < MR; ++m) acc[j][m] = 0.0f;
+  const int gstep = (TT > 0 ? TT : T) * 16;          // bytes between a lane's groups
+  const int sstep = gstep >> 3, xsstep = gstep >> 2;  // the same for steps, scales
+#pragma unroll
+  for (int s = 0; s < (CLT > 0 ? CLT : kMaxCL); ++s) {
+    if (CLT == 0 && s >= ns) break;
+    uint4 xv[MR][4];
+    float inv[MR];
 #pragma unroll
     for (int m = 0; m < MR; ++m) {
-      const uint8_t* xp = x0 + m * 4 * kgs + s * xstep;
-      uint4 xv[4];
 #pragma unroll
-      for (int w = 0; w < 4; ++w) xv[w] = *reinterpret_cast<const uint4*>(xp + w * kgs);
-      const float sc = s0[m * p.Kg + s * p.team];
-      acc[m] = fmaf(group_sum(b.code[s], xv) * sc, bf16_bits_to_float(b.sb[s]), acc[m]);
+      for (int w = 0; w < 4; ++w)
+        xv[m][w] = *reinterpret_cast<const uint4*>(sm + xo + m * xmrow + w * xplane + s * gstep);
+      inv[m] = *reinterpret_cast<const float*>(sm + xso + m * xsmrow + s * xsstep);
+    }
+#pragma unroll
+    for (int j = 0; j < RW; ++j) {
+      const uint4 q = *reinterpret_cast<const uint4*>(sm + co[j] + s * gstep);
+      const float stf = bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(sm + so[j] + s * sstep));
+#pragma unroll
+      for (int m = 0; m < MR; ++m) acc[j][m] = fmaf(group_sum(q, xv[m]) * inv[m], stf, acc[j][m]);
     }
   }
 }
 
-constexpr int kPrefetchUnits = 2;   // units per warp requested into L2 before the PDL wait
+// Sum over the T lanes of a team with a fixed xor tree (T a power of two;
+// TT > 0: T = TT known at compile time).
+template <int TT>
+__device__ __forceinline__ float team_sum(float v, int T) {
+  if (TT > 0) {
+#pragma unroll
+    for (int off = TT >> 1; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  } else {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+      if (off < T) v += __shfl_xor_sync(0xffffffffu, v, off);
+  }
+  return v;
+}
 
-// Chunks longer than 8 steps, or several activation rows, need more
-// registers: one CTA per SM.
-constexpr int ctas_per_sm(int cs, int mr) { return (cs > 8 || mr > 1) ? 1 : kCtasPerSm; }
+// Resident CTAs per SM the register budget allows: two (16 warps, 128
+// registers a thread) for up to four accumulated (row, activation row)
+// pairs, one otherwise.
+constexpr int min_ctas(int mr, int rw) { return (mr * rw <= 4) ? 2 : 1; }
 
-template <int MR, int CS>
-__global__ void __launch_bounds__(kThreads, ctas_per_sm(CS, MR)) gemv_kernel(const __grid_constant__ GemvParams p) {
-  extern __shared__ __align__(16) uint8_t smem[];
+// ---------------------------------------------------------------- kernel
+template <int MR, int RW, int TT, int CLT>
+__global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
+    gemv_kernel(const __grid_constant__ GemvParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int team = p.team;
-  const int set = lane / team;   // row set (= row of the unit) of this lane
-  const int lt = lane - set * team;
-  const int ub = (int)((long long)blockIdx.x * p.U / gridDim.x);
-  const int ue = (int)((long long)(blockIdx.x + 1) * p.U / gridDim.x);
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t full0 = sbase, empty0 = sbase + 8 * kMaxStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 16 * kMaxStages);
+  const bool dense = p.ids == nullptr;
+  const int nst = p.nst;
 
-  // items whose activation rows this CTA needs (units are slice-major)
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < nst; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kConsumerWarps);
+    }
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    // Dense weights do not depend on earlier kernels: their tiles are
+    // requested at once.  Routed ids may come from the previous kernel.
+    if (!dense) pdl_wait();
+    const uint64_t pol = policy_evict_first();
+    Walk wk;
+    wk.init(p);
+    long long issued = 0;
+    int slot = 0;
+    uint32_t phase = 0;   // use count of the slot, mod 2
+    bool ok = true;
+    while (ok && wk.next(p)) {
+      const uint8_t *qwi, *sti;
+      if (!item_arrays(p, wk.item, &qwi, &sti)) continue;
+      for (int c = wk.c0; c < wk.c1; ++c) {
+        // reuse of a slot waits for the consumers to release its last tile
+        if (issued >= nst && !wait_phase(empty0 + 8 * slot, phase ^ 1u, abort_flag)) {
+          if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        const uint32_t st_off = kBarBytes + slot * p.tile_bytes;
+        issue_tile(p, wk, c, qwi, sti, sbase + st_off, smem + st_off, full0 + 8 * slot, lane, pol);
+        ++issued;
+        if (++slot == nst) {
+          slot = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    // let the last copies land before the CTA may leave
+    const int last = issued < nst ? (int)issued : nst;
+    for (int i = 1; i <= last; ++i) {
+      const int sl = slot - i < 0 ? slot - i + nst : slot - i;
+      const uint32_t ph = slot - i < 0 ? phase ^ 1u : phase;
+      if (!mbar_wait_bounded(full0 + 8 * sl, ph, kWaitCycles)) {
+        report(p.status, W4_ERR_TIMEOUT);
+        break;
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int T = TT > 0 ? TT : p.T;
+  const int nsw = 32 / T;
+  const int set = lane / T;          // row set of this lane within the warp
+  const int t = lane - set * T;      // lane within the row's team
+
+  // items whose activation rows this CTA needs
   int item0 = 0, nslots = 1;
   if (p.x_per_item) {
-    const int rb_lo = ub % p.B, rb_hi = (ue - 1) % p.B;
-    if (ue - ub >= p.B || rb_lo > rb_hi) {
-      item0 = 0;
-      nslots = p.n_items;
-    } else {
-      item0 = rb_lo / p.upi;
-      nslots = rb_hi / p.upi - item0 + 1;
-    }
-  }
-  uint8_t* xs = smem;
-  float* xscale = reinterpret_cast<float*>(smem + (long long)p.x_slots * MR * 4 * p.Kg * 16);
-
-  // Compute cursor `cp` and load cursor `ld` one chunk ahead; two register
-  // buffers used in turn.  Dense weights do not depend on earlier kernels:
-  // this warp's first units are requested into L2 and its first chunk into
-  // registers before waiting for the previous kernel (W4_FLAG_PDL), so a
-  // launch that is resident early has its weights in flight already.  Routed
-  // ids may come from the previous kernel and are read after the wait.
-  Cursor cp, ld;
-  Buf<CS> ba, bb;
-  const bool dense = p.ids == nullptr;
-  if (!dense) pdl_wait();
-  for (int d = 0; d < kPrefetchUnits; ++d)
-    if (ub + warp + d * kWarps < ue) prefetch_unit(p, ub + warp + d * kWarps, lane);
-  cp.seek(p, ub + warp, ue, lt, set, true);
-  ld = cp;
-  if (ld.u < ue) {
-    load_chunk<CS>(p, ld, ba);
-    ld.next_chunk(p, ue, lt, set, false);
-  }
-  if (dense) pdl_wait();     // activations and outputs follow earlier kernels
-  pdl_launch_dependents();
-  if (ub < ue) stage_x(p, item0, nslots, xs, xscale);
-  __syncthreads();
-
-  float rowsum[MR];
-#pragma unroll
-  for (int m = 0; m < MR; ++m) rowsum[m] = 0.0f;
-
-  // End of a chunk: team reduction (fixed xor tree), then the chunk sum goes
-  // to the row sum, or to the workspace under split-K.
-  auto finish_chunk = [&](float acc[MR]) {
-#pragma unroll
-    for (int m = 0; m < MR; ++m)
-      for (int off = team >> 1; off > 0; off >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], off);
-    const bool unit_end = cp.c + 1 == cp.c_end;
+    Walk r;
+    r.init(p);
     if (p.S == 1) {
-#pragma unroll
-      for (int m = 0; m < MR; ++m) rowsum[m] += acc[m];
-      if (unit_end) {
-        if (lt == 0 && cp.row < p.N) {
-#pragma unroll
-          for (int m = 0; m < MR; ++m)
-            p.y[((long long)cp.item * MR + m) * p.N + cp.row] = __float2bfloat16_rn(rowsum[m]);
-        }
-#pragma unroll
-        for (int m = 0; m < MR; ++m) rowsum[m] = 0.0f;
-      }
-      return;
-    }
-    if (lt == 0) {
-      float* dst = p.ws_partial + (((long long)cp.rb * p.nch + cp.c) * p.rows_per_unit + set) * MR;
-#pragma unroll
-      for (int m = 0; m < MR; ++m) dst[m] = acc[m];
-    }
-    if (unit_end) {
-      // the last warp to finish this row block adds the chunk sums in chunk
-      // order, writes the rows and re-arms the counter
-      __threadfence();
-      __syncwarp();
-      int last = 0;
-      if (lane == 0) last = atomicAdd(p.ws_count + cp.rb, 1) == p.S - 1;
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {
-        __threadfence();
-        const int rbase = (cp.rb - cp.item * p.upi) * p.rows_per_unit;
-        const float* src = p.ws_partial + (long long)cp.rb * p.nch * p.rows_per_unit * MR;
-        for (int e = lane; e < p.rows_per_unit * MR; e += 32) {
-          const int r = e / MR, m = e - r * MR;
-          if (rbase + r >= p.N) continue;
-          float v = 0.0f;
-          for (int c = 0; c < p.nch; ++c) v += __ldcg(src + ((long long)c * p.rows_per_unit + r) * MR + m);
-          p.y[((long long)cp.item * MR + m) * p.N + rbase + r] = __float2bfloat16_rn(v);
-        }
-        if (lane == 0) atomicExch(p.ws_count + cp.rb, 0);
+      item0 = (int)(r.pos / p.N);
+      nslots = (r.end > r.pos) ? (int)((r.end - 1) / p.N) - item0 + 1 : 1;
+    } else {
+      const int rb_lo = (int)(r.pos % p.B), rb_hi = (int)((r.end - 1) % p.B);
+      if (r.end - r.pos >= p.B || rb_lo > rb_hi) {
+        nslots = p.n_items;
+      } else {
+        item0 = rb_lo / p.upi;
+        nslots = rb_hi / p.upi - item0 + 1;
       }
     }
-  };
+  }
+  const uint32_t xs_off = kBarBytes + nst * p.tile_bytes;
+  const uint32_t xsc_off = xs_off + (uint32_t)(p.x_slots * MR * 4 * p.Kg * 16);
+  pdl_wait();   // activations and outputs follow earlier kernels
+  stage_x(p, item0, nslots, smem + xs_off, reinterpret_cast<float*>(smem + xsc_off));
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
 
-  while (cp.u < ue) {
+  const int xplane = p.Kg * 16, xmrow = 4 * p.Kg * 16, xsmrow = p.Kg * 4;
+  const int gpc = p.CL * T;                  // groups per chunk
+  const bool whole = p.nch == 1;
+  const int kg2 = p.Kg * 2;
+  float rowsum[RW][MR];
 #pragma unroll
-    for (int phase = 0; phase < 2; ++phase) {   // buffers ba, bb in turn
-      Buf<CS>& curb = phase == 0 ? ba : bb;
-      Buf<CS>& nxtb = phase == 0 ? bb : ba;
-      if (cp.u >= ue) break;
-      if (ld.u < ue) {   // next chunk's loads fly while this one is computed
-        load_chunk<CS>(p, ld, nxtb);
-        ld.next_chunk(p, ue, lt, set, false);
+  for (int j = 0; j < RW; ++j)
+#pragma unroll
+    for (int m = 0; m < MR; ++m) rowsum[j][m] = 0.0f;
+
+  Walk wk;
+  wk.init(p);
+  int slot = 0;
+  uint32_t phase = 0;
+  uint32_t tile = kBarBytes;   // shared offset of the current slot
+  bool reported = false;
+  while (wk.next(p)) {
+    const uint8_t *qwi, *sti;
+    if (!item_arrays(p, wk.item, &qwi, &sti)) {
+      if (!reported && lane == 0) report(p.status, W4_ERR_INDEX);
+      reported = true;
+      continue;
+    }
+    // per-window, per-row offsets within a tile (32-bit)
+    const int xslot = p.x_per_item ? wk.item - item0 : 0;
+    uint32_t crow[RW], srow[RW], soff[RW];
+    bool rv[RW];
+#pragma unroll
+    for (int j = 0; j < RW; ++j) {
+      // rows past the window read the window's last row (results dropped)
+      const int rw = (j * kConsumerWarps + warp) * nsw + set;
+      rv[j] = rw < wk.nrows;
+      const int rl = rv[j] ? rw : wk.nrows - 1;
+      crow[j] = rl * p.code_pitch + t * 16;
+      // start of the row's steps within its copied 16-byte lines
+      const int r16 = ((wk.row0 + rl) & 7) * (kg2 & 15);
+      srow[j] = p.step_off + t * 2 +
+                (whole ? (((wk.row0 & 7) * (kg2 & 15)) & 15) + rl * kg2 : rl * p.step_pitch);
+      soff[j] = whole ? 0u : (uint32_t)r16;
+    }
+    __nv_bfloat16* yrow = p.y + (long long)wk.item * MR * p.N + wk.row0;
+    uint32_t xo = xs_off + (uint32_t)(((xslot * MR * 4) * p.Kg + wk.c0 * gpc + t) * 16);
+    uint32_t xso = xsc_off + (uint32_t)(((xslot * MR) * p.Kg + wk.c0 * gpc + t) * 4);
+    for (int c = wk.c0; c < wk.c1; ++c) {
+      if (!wait_phase(full0 + 8 * slot, phase, abort_flag)) {
+        if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
+        *abort_flag = 1;
+        return;
       }
-      const int xslot = p.x_per_item ? cp.item - item0 : 0;
-      float acc[MR];
-      chunk_dot<CS, MR>(p, cp, curb, xs + (long long)xslot * MR * 4 * p.Kg * 16,
-                        xscale + (long long)xslot * MR * p.Kg, acc);
-      finish_chunk(acc);
-      cp.next_chunk(p, ue, lt, set, true);
+      const int ns = min(p.CL, p.NI - c * p.CL);
+      const int g2 = c * gpc * 2;
+      uint32_t co[RW], so[RW];
+#pragma unroll
+      for (int j = 0; j < RW; ++j) {
+        co[j] = tile + crow[j];
+        so[j] = tile + srow[j] + (whole ? 0u : ((soff[j] + g2) & 15));
+      }
+      float acc[RW][MR];
+      tile_dot<MR, RW, TT, CLT>(smem, xo, xso, xplane, xmrow, xsmrow, co, so, ns, T, acc);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * slot);   // this warp is done with the stage
+      if (++slot == nst) {
+        slot = 0;
+        phase ^= 1u;
+        tile = kBarBytes;
+      } else {
+        tile += p.tile_bytes;
+      }
+      xo += gpc * 16;
+      xso += gpc * 4;
+
+#pragma unroll
+      for (int j = 0; j < RW; ++j)
+#pragma unroll
+        for (int m = 0; m < MR; ++m) acc[j][m] = team_sum<TT>(acc[j][m], T);
+
+      if (p.S == 1) {
+#pragma unroll
+        for (int j = 0; j < RW; ++j)
+#pragma unroll
+          for (int m = 0; m < MR; ++m) rowsum[j][m] += acc[j][m];
+        if (c == p.nch - 1) {
+          if (t == 0) {
+#pragma unroll
+            for (int j = 0; j < RW; ++j) {
+              if (!rv[j]) continue;
+              const int rl = (j * kConsumerWarps + warp) * nsw + set;
+#pragma unroll
+              for (int m = 0; m < MR; ++m)
+                yrow[(long long)m * p.N + rl] = __float2bfloat16_rn(rowsum[j][m]);
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < RW; ++j)
+#pragma unroll
+            for (int m = 0; m < MR; ++m) rowsum[j][m] = 0.0f;
+        }
+        continue;
+      }
+      // split-K: chunk sums to the workspace
+      if (t == 0) {
+#pragma unroll
+        for (int j = 0; j < RW; ++j) {
+          if (!rv[j]) continue;
+          const int rl = (j * kConsumerWarps + warp) * nsw + set;
+          float* dst = p.ws_partial + (((long long)wk.rb * p.nch + c) * p.RB + rl) * MR;
+#pragma unroll
+          for (int m = 0; m < MR; ++m) dst[m] = acc[j][m];
+        }
+      }
+      if (c == wk.c1 - 1) {
+        // The last of the slices to finish this row block (for this warp's
+        // rows) adds the chunk sums in chunk order, writes the rows and
+        // re-arms the counter.  The warp barrier orders every lane's partial
+        // stores before lane 0's counter update, whose release publishes them
+        // at GPU scope; its acquire side, then the second warp barrier, order
+        // the other slices' partials before this warp reads them.
+        __syncwarp();
+        int* counter = p.ws_count + (long long)wk.rb * kConsumerWarps + warp;
+        int last = 0;
+        if (lane == 0) last = atomic_add_acq_rel_gpu(counter, 1) == p.S - 1;
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          __syncwarp();
+          if (t == 0) {
+#pragma unroll
+            for (int j = 0; j < RW; ++j) {
+              if (!rv[j]) continue;
+              const int rl = (j * kConsumerWarps + warp) * nsw + set;
+              const float* src = p.ws_partial + ((long long)wk.rb * p.nch * p.RB + rl) * MR;
+#pragma unroll
+              for (int m = 0; m < MR; ++m) {
+                float v = 0.0f;
+                for (int cc = 0; cc < p.nch; ++cc) v += __ldcg(src + (long long)cc * p.RB * MR + m);
+                yrow[(long long)m * p.N + rl] = __float2bfloat16_rn(v);
+              }
+            }
+          }
+          if (lane == 0) atomicExch(counter, 0);
+        }
+      }
     }
   }
 }
@@ -495,8 +630,11 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(CS, MR)) gemv_kernel(con
 namespace {
 
 struct DeviceInfo {
+  int dev = -1;           // device ordinal, -1 when planning without one
   int sms = 0;
-  int smem_optin = 0;
+  int smem_optin = 0;     // largest dynamic shared memory per CTA
+  int smem_per_sm = 0;
+  int smem_reserved = 0;  // shared memory the system keeps per CTA
 };
 
 DeviceInfo device_info(int dev) {
@@ -505,126 +643,265 @@ DeviceInfo device_info(int dev) {
   std::lock_guard<std::mutex> lock(mu);
   if (dev < 0 || dev >= 64) return DeviceInfo{};
   if (cache[dev].sms == 0) {
-    int sms = 0, smem = 0;
+    int sms = 0, optin = 0, per_sm = 0, reserved = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) !=
             cudaSuccess) {
       cudaGetLastError();
       return DeviceInfo{};
     }
+    cache[dev].dev = dev;
     cache[dev].sms = sms;
-    cache[dev].smem_optin = smem;
+    cache[dev].smem_optin = optin;
+    cache[dev].smem_per_sm = per_sm;
+    cache[dev].smem_reserved = reserved;
   }
   return cache[dev];
 }
 
 struct Plan {
   int MR = 1;
-  int team = 32, sets = 1, R = 1, rows_per_unit = 1;
-  int chunk = 0, nch = 1, cs = 0;
+  int T = 32, nsw = 1, NI = 1, CL = 1, nch = 1;
+  int RW = 1, RB = 8;
   int S = 1, cps = 1, upi = 1;
   long long B = 0, U = 0;
   int x_slots = 1;
+  int nst = 2, per_sm = 1;
+  int tile_bytes = 0, code_pitch = 0, step_pitch = 0, step_off = 0;
   int ctas = 0;
   long long smem = 0;
   size_t ws_bytes = 0;
   size_t ws_part_off = 0;
 };
 
-// The per-row arithmetic (team, chunk) comes from K alone.  team: the largest
-// power of two <= 32 dividing K/32 that leaves each lane >= kChunkPerLane
-// groups of a row.  Chunk steps per lane: the largest divisor of the lane's
-// groups per row in 5..12, so every chunk is full (0 = none: chunks of
-// kChunkPerLane steps, the last one ragged).
-void row_shape(int K, int* team, int* chunk, int* nch, int* cs) {
+// The per-row arithmetic comes from K alone.  T: the largest power of two
+// <= 32 dividing K/32 that leaves each lane >= 4 groups of a row (else the
+// largest dividing one).  CL, groups per lane per chunk: all of the lane's
+// groups when they are <= 4, else 4 or 3 when that divides them, else 4
+// (the last chunk shorter).
+void row_shape(int K, int* T, int* NI, int* CL, int* nch) {
   const int Kg = K / 32;
   int t = 1;
-  while (t < 32 && Kg % (2 * t) == 0 && Kg / (2 * t) >= kChunkPerLane) t *= 2;
-  *team = t;
-  const int q = Kg / t;
-  int c = 0;
-  for (int d = 12; d >= 5 && c == 0; --d)
-    if (q % d == 0) c = d;
-  if (q <= 12) c = q;             // a whole row per chunk
-  if (c != 0 && c != 7 && c != 8 && c != 11 && c != 12 && c != 5 && c != 6 && c != 9 && c != 10)
-    c = 0;
-  *cs = c;
-  *chunk = t * (c > 0 ? c : kChunkPerLane);
-  *nch = (Kg + *chunk - 1) / *chunk;
+  while (t < 32 && Kg % (2 * t) == 0 && Kg / (2 * t) >= 4) t *= 2;
+  if (Kg / t < 4) {   // short rows: the largest power of two that divides
+    t = 1;
+    while (t < 32 && Kg % (2 * t) == 0) t *= 2;
+  }
+  *T = t;
+  const int ni = Kg / t;
+  int cl = 4;
+  if (ni <= 4) cl = ni;
+  else if (ni % 4 == 0) cl = 4;
+  else if (ni % 3 == 0) cl = 3;
+  *NI = ni;
+  *CL = cl;
+  *nch = (ni + cl - 1) / cl;
 }
 
-long long x_bytes(int slots, int MR, int Kg) {
-  return (long long)slots * MR * Kg * (64 + 4);
+long long x_bytes(int slots, int MR, int Kg) { return (long long)slots * MR * Kg * (64 + 4); }
+
+// Stage geometry for `rb` rows per window.
+void tile_geometry(int K, int T, int CL, int nch, int rb, int* code_pitch, int* step_pitch,
+                   int* step_off, int* tile_bytes) {
+  const int Kg = K / 32;
+  *code_pitch = CL * T * 16;
+  *step_pitch = nch == 1 ? Kg * 2 : ((CL * T * 2 + 30 + 15) & ~15);
+  *step_off = rb * *code_pitch;
+  const long long steps = nch == 1 ? (long long)rb * Kg * 2 + 32 : (long long)rb * *step_pitch;
+  *tile_bytes = (int)((*step_off + steps + 127) & ~127LL);
 }
+
+using KernelFn = void (*)(GemvParams);
+int occupancy(const struct Plan& pl, int dev);
 
 bool make_plan(int MR, int N, int K, int n_items, int allow_split, int x_per_item,
-               const DeviceInfo& di, Plan* out) {
+               const DeviceInfo& di, Plan* out, int force_per_sm = 0) {
   Plan pl;
   pl.MR = MR;
   const int Kg = K / 32;
-  row_shape(K, &pl.team, &pl.chunk, &pl.nch, &pl.cs);
-  pl.sets = 32 / pl.team;
+  row_shape(K, &pl.T, &pl.NI, &pl.CL, &pl.nch);
+  pl.nsw = 32 / pl.T;
   const int sms = di.sms > 0 ? di.sms : 1;
-  const long long warps = (long long)sms * kWarps * kCtasPerSm;
-  const long long want = 6 * warps;       // units for a balanced split over warps
-  pl.R = 1;   // one row per lane
-  pl.rows_per_unit = pl.sets;
-  pl.upi = (N + pl.rows_per_unit - 1) / pl.rows_per_unit;
-  pl.B = (long long)n_items * pl.upi;
-  if (pl.B > (1LL << 30)) return false;
-  int S = 1;
-  if (allow_split && pl.nch > 1 && pl.B < want)
-    S = (int)std::min<long long>(pl.nch, (want + pl.B - 1) / pl.B);
-  pl.cps = (pl.nch + S - 1) / S;
-  pl.S = (pl.nch + pl.cps - 1) / pl.cps;
-  pl.U = (long long)pl.S * pl.B;
-  if (pl.U > (1LL << 30)) return false;
-  // One CTA per SM leaves room for the next launch's CTA (PDL); problems
-  // with many units per warp fill two CTAs per SM instead.
-  const int cap = ctas_per_sm(pl.cs, MR);
-  const long long per_sm = (pl.U >= (long long)cap * sms * kWarps) ? cap : 1;
-  pl.ctas = (int)std::min<long long>(pl.U, per_sm * sms);
-  // activation rows a CTA stages: one, or the items its unit range touches
+  const long long optin = di.smem_optin > 0 ? di.smem_optin : 232448;
+  const long long per_sm_smem = di.smem_per_sm > 0 ? di.smem_per_sm : 233472;
+  const long long reserved = di.smem_reserved > 0 ? di.smem_reserved : 1024;
+  const long long rows_total = (long long)n_items * N;
+  if (rows_total > (1LL << 40)) return false;
+  const long long weight_bytes = rows_total * ((long long)K / 2 + Kg * 2);
+  // Two CTAs per SM for large problems; one otherwise, which leaves room for
+  // the next launch's CTA to start streaming its weights (W4_FLAG_PDL).
+  pl.per_sm = (weight_bytes >= (16LL << 20)) ? min_ctas(MR, 1) : 1;
+  if (force_per_sm > 0) pl.per_sm = force_per_sm;
+  // shared memory a CTA may take and still leave room for a second one
+  const long long half = per_sm_smem / 2 - reserved;
+  const long long min_rows = (long long)kConsumerWarps * pl.nsw;   // rows of one RW = 1 window
+  const long long target = (long long)pl.per_sm * sms;
+  const long long g1 = std::min(target, (rows_total + min_rows - 1) / min_rows);
+  int rw_cap = MR == 1 ? 4 : (MR == 2 ? 2 : 1);
+  if (allow_split && pl.nch > 1 && 2 * g1 < target) {
+    // few rows, long K: split K across CTAs
+    pl.RB = (int)min_rows;
+    pl.upi = (int)((N + pl.RB - 1) / pl.RB);
+    pl.B = (long long)n_items * pl.upi;
+    if (pl.B > (1LL << 30)) return false;
+    const int S = (int)std::min<long long>(pl.nch, (target + pl.B - 1) / pl.B);
+    pl.cps = (pl.nch + S - 1) / S;
+    pl.S = (pl.nch + pl.cps - 1) / pl.cps;
+    pl.U = (long long)pl.S * pl.B;
+    pl.ctas = (int)std::min<long long>(pl.U, target);
+    rw_cap = 1;
+  } else {
+    pl.S = 1;
+    pl.cps = pl.nch;
+    pl.U = rows_total;
+    pl.ctas = (int)std::max<long long>(1, g1);
+  }
+  // activation rows a CTA stages: one, or the items its range touches
   pl.x_slots = 1;
   if (x_per_item) {
     for (int c = 0; c < pl.ctas; ++c) {
       const long long ub = (long long)c * pl.U / pl.ctas, ue = (long long)(c + 1) * pl.U / pl.ctas;
       if (ue <= ub) continue;
-      const long long lo = ub % pl.B, hi = (ue - 1) % pl.B;
-      const long long n = (ue - ub >= pl.B || lo > hi) ? n_items : hi / pl.upi - lo / pl.upi + 1;
+      long long n;
+      if (pl.S == 1) {
+        n = (ue - 1) / N - ub / N + 1;
+      } else {
+        const long long lo = ub % pl.B, hi = (ue - 1) % pl.B;
+        n = (ue - ub >= pl.B || lo > hi) ? n_items : hi / pl.upi - lo / pl.upi + 1;
+      }
       pl.x_slots = (int)std::max<long long>(pl.x_slots, n);
     }
   }
-  pl.smem = x_bytes(pl.x_slots, MR, Kg);
-  const long long smem_max = di.smem_optin > 0 ? di.smem_optin : 232448;
-  if (pl.smem > smem_max) return false;
+  const long long xb = x_bytes(pl.x_slots, MR, Kg);
+  // rows per lane: the most that still gives >= 3 stages (>= 2 at RW = 1)
+  // and windows no taller than a CTA's share of the rows
+  const long long rows_per_cta = (pl.U + pl.ctas - 1) / pl.ctas;
+  bool found = false;
+  const long long budgets[2] = {half, std::min(optin, per_sm_smem - reserved)};
+  for (int bi = 0; bi < 2 && !found; ++bi) {
+    for (int rw = rw_cap; rw >= 1 && !found; rw /= 2) {
+      const int rb = (int)min_rows * rw;
+      if (pl.S == 1 && rw > 1 && rb > rows_per_cta) continue;
+      int cp, sp, so, tb;
+      tile_geometry(K, pl.T, pl.CL, pl.nch, rb, &cp, &sp, &so, &tb);
+      const long long room = budgets[bi] - kBarBytes - xb;
+      if (room < 2LL * tb) continue;
+      const int nst = (int)std::min<long long>(kMaxStages, room / tb);
+      if (nst < 3 && rw > 1) continue;
+      pl.RW = rw;
+      pl.RB = rb;
+      pl.nst = nst;
+      pl.code_pitch = cp;
+      pl.step_pitch = sp;
+      pl.step_off = so;
+      pl.tile_bytes = tb;
+      found = true;
+    }
+    if (found && bi == 1 && pl.per_sm > 1)   // only one CTA per SM fits
+      return make_plan(MR, N, K, n_items, allow_split, x_per_item, di, out, 1);
+  }
+  if (!found) return false;
+  pl.smem = kBarBytes + (long long)pl.nst * pl.tile_bytes + xb;
+  // resident CTAs the device really fits (registers, shared memory); fewer
+  // than planned: the same work over fewer CTAs
+  if (di.dev >= 0) {
+    const int occ = occupancy(pl, di.dev);
+    if (occ < 1) return false;
+    if (occ < pl.per_sm)
+      return make_plan(MR, N, K, n_items, allow_split, x_per_item, di, out, occ);
+  }
   if (pl.S > 1) {
-    // counters first, so every plan of the same shape (any MR) finds them at
-    // the same place; chunk partials after them
-    const size_t part = (size_t)pl.B * pl.nch * pl.rows_per_unit * MR * sizeof(float);
-    pl.ws_part_off = ((size_t)pl.B * sizeof(int) + 255) & ~size_t(255);
+    // counters first, partials after them
+    const size_t part = (size_t)pl.B * pl.nch * pl.RB * MR * sizeof(float);
+    pl.ws_part_off = ((size_t)pl.B * kConsumerWarps * sizeof(int) + 255) & ~size_t(255);
     pl.ws_bytes = pl.ws_part_off + part;
   }
   *out = pl;
   return true;
 }
 
-template <int MR, int CS>
-cudaError_t launch_one(const GemvParams& prm, const Plan& pl, bool pdl, cudaStream_t stream, int dev) {
-  static std::mutex mu;
-  static long long attr_bytes[64] = {};
-  auto kern = gemv_kernel<MR, CS>;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  {
-    // raise the kernel's dynamic shared-memory limit to what this plan needs
-    std::lock_guard<std::mutex> lock(mu);
-    if (pl.smem > attr_bytes[dev]) {
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)pl.smem);
-      if (e != cudaSuccess) return e;
-      attr_bytes[dev] = pl.smem;
-    }
+using KernelFn = void (*)(GemvParams);
+
+// The instantiation that runs a plan: batch-1 plans whose chunks are all full
+// get one compiled for their team size and chunk length (the common K);
+// everything else the generic one.  *tt, *clt (if given) receive the
+// compile-time team size and chunk length (0: generic).
+KernelFn kernel_for(const Plan& pl, int* tt = nullptr, int* clt = nullptr) {
+  if (tt != nullptr) *tt = 0;
+  if (clt != nullptr) *clt = 0;
+  const bool full = pl.NI % pl.CL == 0;
+  if (pl.MR == 1 && full && pl.RW <= 2) {
+    const int key = pl.T * 8 + pl.CL;
+#define W4_SPEC(t, cl)                                                          \
+  if (key == (t) * 8 + (cl)) {                                                  \
+    if (tt != nullptr) *tt = t;                                                 \
+    if (clt != nullptr) *clt = cl;                                              \
+    return pl.RW == 1 ? gemv_kernel<1, 1, t, cl> : gemv_kernel<1, 2, t, cl>;    \
   }
+    W4_SPEC(16, 4)   // K = 2048
+    W4_SPEC(8, 3)    // K = 5376
+    W4_SPEC(32, 3)   // K = 21504
+    W4_SPEC(32, 4)   // K = 4096 * n
+#undef W4_SPEC
+  }
+  switch (pl.MR * 8 + pl.RW) {
+    case 8 + 1: return gemv_kernel<1, 1, 0, 0>;
+    case 8 + 2: return gemv_kernel<1, 2, 0, 0>;
+    case 8 + 4: return gemv_kernel<1, 4, 0, 0>;
+    case 16 + 1: return gemv_kernel<2, 1, 0, 0>;
+    case 16 + 2: return gemv_kernel<2, 2, 0, 0>;
+    case 24 + 1: return gemv_kernel<3, 1, 0, 0>;
+    case 32 + 1: return gemv_kernel<4, 1, 0, 0>;
+    default: return nullptr;
+  }
+}
+
+// Raise `fn`'s dynamic shared-memory limit on `dev` (current) to at least
+// `smem` bytes.
+cudaError_t allow_smem(KernelFn fn, long long smem, int dev) {
+  struct Entry {
+    KernelFn fn;
+    int dev;
+    long long bytes;
+  };
+  static std::mutex mu;
+  static Entry seen[256];
+  static int used = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  Entry* e = nullptr;
+  for (int i = 0; i < used; ++i)
+    if (seen[i].fn == fn && seen[i].dev == dev) e = &seen[i];
+  if (e != nullptr && e->bytes >= smem) return cudaSuccess;
+  const cudaError_t r =
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (r != cudaSuccess) return r;
+  if (e == nullptr && used < 256) e = &seen[used++];
+  if (e != nullptr) *e = Entry{fn, dev, smem};
+  return cudaSuccess;
+}
+
+// Resident CTAs per SM of the plan's instantiation (0: not launchable).
+int occupancy(const Plan& pl, int dev) {
+  const KernelFn fn = kernel_for(pl);
+  int n = 0;
+  if (fn == nullptr || allow_smem(fn, pl.smem, dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, (size_t)pl.smem) !=
+          cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+cudaError_t launch(const GemvParams& prm, const Plan& pl, bool pdl, cudaStream_t stream, int dev) {
+  const KernelFn fn = kernel_for(pl);
+  if (fn == nullptr) return cudaErrorInvalidConfiguration;
+  const cudaError_t ea = allow_smem(fn, pl.smem, dev);
+  if (ea != cudaSuccess) return ea;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)pl.ctas);
   cfg.blockDim = dim3(kThreads);
@@ -635,32 +912,7 @@ cudaError_t launch_one(const GemvParams& prm, const Plan& pl, bool pdl, cudaStre
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, prm);
-}
-
-template <int MR>
-cudaError_t launch_cs(const GemvParams& prm, const Plan& pl, bool pdl, cudaStream_t s, int dev) {
-  switch (pl.cs) {
-    case 5: return launch_one<MR, 5>(prm, pl, pdl, s, dev);
-    case 6: return launch_one<MR, 6>(prm, pl, pdl, s, dev);
-    case 7: return launch_one<MR, 7>(prm, pl, pdl, s, dev);
-    case 8: return launch_one<MR, 8>(prm, pl, pdl, s, dev);
-    case 9: return launch_one<MR, 9>(prm, pl, pdl, s, dev);
-    case 10: return launch_one<MR, 10>(prm, pl, pdl, s, dev);
-    case 11: return launch_one<MR, 11>(prm, pl, pdl, s, dev);
-    case 12: return launch_one<MR, 12>(prm, pl, pdl, s, dev);
-    default: return launch_one<MR, 0>(prm, pl, pdl, s, dev);
-  }
-}
-
-cudaError_t launch(const GemvParams& prm, const Plan& pl, bool pdl, cudaStream_t s, int dev) {
-  switch (pl.MR) {
-    case 1: return launch_cs<1>(prm, pl, pdl, s, dev);
-    case 2: return launch_cs<2>(prm, pl, pdl, s, dev);
-    case 3: return launch_cs<3>(prm, pl, pdl, s, dev);
-    case 4: return launch_cs<4>(prm, pl, pdl, s, dev);
-    default: return cudaErrorInvalidConfiguration;
-  }
+  return cudaLaunchKernelEx(&cfg, fn, prm);
 }
 
 GemvParams base_params(const Plan& pl, int N, int K) {
@@ -669,18 +921,23 @@ GemvParams base_params(const Plan& pl, int N, int K) {
   p.K = K;
   p.Kg = K / 32;
   p.MR = pl.MR;
-  p.team = pl.team;
-  p.sets = pl.sets;
-  p.R = pl.R;
-  p.rows_per_unit = pl.rows_per_unit;
-  p.chunk = pl.chunk;
+  p.T = pl.T;
+  p.nsw = pl.nsw;
+  p.NI = pl.NI;
+  p.CL = pl.CL;
   p.nch = pl.nch;
+  p.RB = pl.RB;
   p.S = pl.S;
   p.cps = pl.cps;
   p.upi = pl.upi;
   p.B = (int)pl.B;
-  p.U = (int)pl.U;
+  p.U = pl.U;
   p.x_slots = pl.x_slots;
+  p.nst = pl.nst;
+  p.tile_bytes = pl.tile_bytes;
+  p.code_pitch = pl.code_pitch;
+  p.step_pitch = pl.step_pitch;
+  p.step_off = pl.step_off;
   return p;
 }
 
@@ -700,6 +957,8 @@ void planning_device(DeviceInfo* di) {
   if (!current_device(&dev, di)) {
     di->sms = 152;              // planning without a device: GB300 figures
     di->smem_optin = 232448;
+    di->smem_per_sm = 233472;
+    di->smem_reserved = 1024;
   }
 }
 
@@ -737,11 +996,15 @@ bool cached_plan(int MR, int N, int K, int n_items, int split, int xpi, const De
   return true;
 }
 
-// Activation rows per launch: up to kMaxMR, as many as fit shared memory.
+// Activation rows per launch: up to kMaxMR, as many as fit shared memory
+// next to two stages of one row per lane.
 int max_rows_per_launch(int K, const DeviceInfo& di) {
-  const long long smem_max = di.smem_optin > 0 ? di.smem_optin : 232448;
+  const long long optin = di.smem_optin > 0 ? di.smem_optin : 232448;
+  int T, NI, CL, nch, cp, sp, so, tb;
+  row_shape(K, &T, &NI, &CL, &nch);
+  tile_geometry(K, T, CL, nch, kConsumerWarps * (32 / T), &cp, &sp, &so, &tb);
   int mr = kMaxMR;
-  while (mr > 0 && x_bytes(1, mr, K / 32) > smem_max) --mr;
+  while (mr > 0 && kBarBytes + 2LL * tb + x_bytes(1, mr, K / 32) > optin) --mr;
   return mr;
 }
 
@@ -759,17 +1022,21 @@ extern "C" w4_status w4a16_gemv_plan(int M, int N, int K, w4_plan_info* info) {
   Plan pl;
   const int mr_cap = max_rows_per_launch(K, di);
   if (mr_cap < 1 || !cached_plan(std::min(M, mr_cap), N, K, 1, 1, 0, di, &pl)) return W4_ERR_SHAPE;
-  info->path = 0;
+  info->path = 1;
   info->ctas = pl.ctas;
   info->slices = pl.S;
   info->threads = kThreads;
-  info->team = pl.team;
-  info->unit_rows = pl.rows_per_unit;
-  info->chunk_groups = pl.chunk;
-  info->rows_per_lane = pl.R;
+  info->team = pl.T;
+  info->unit_rows = pl.RB;
+  info->chunk_groups = pl.CL * pl.T;
+  info->rows_per_lane = pl.RW;
   info->smem_bytes = (int)pl.smem;
   info->rows_per_call = pl.MR;
-  info->chunk_steps = pl.cs;
+  info->chunk_steps = pl.CL;
+  info->stages = pl.nst;
+  info->ctas_per_sm = pl.per_sm;
+  // compile-time team size / chunk length of the instantiation (0: generic)
+  kernel_for(pl, &info->tmpl_team, &info->tmpl_chunk);
   return W4_OK;
 }
 
@@ -942,7 +1209,8 @@ extern "C" w4_status w4a16_gemv_static_scratch(void* y, const void* qw, const vo
       cudaError_t e = static_scratch_address(dev, &base);
       // the counters must start at zero; the array keeps the previous call's
       // contents (and an aborted call may leave them armed)
-      if (e == cudaSuccess) e = cudaMemsetAsync(base, 0, (size_t)pm.B * sizeof(int), s);
+      if (e == cudaSuccess)
+        e = cudaMemsetAsync(base, 0, (size_t)pm.B * kConsumerWarps * sizeof(int), s);
       if (e != cudaSuccess) {
         note_cuda_error(e);
         cudaGetLastError();

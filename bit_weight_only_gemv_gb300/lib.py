@@ -39,7 +39,9 @@ class W4Error(RuntimeError):
 class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("path", "ctas", "slices", "threads", "team",
                                             "unit_rows", "chunk_groups", "rows_per_lane",
-                                            "smem_bytes", "rows_per_call", "chunk_steps")]
+                                            "smem_bytes", "rows_per_call", "chunk_steps",
+                                            "stages", "ctas_per_sm", "tmpl_team",
+                                            "tmpl_chunk")]
 
 
 _lib = None

@@ -78,7 +78,7 @@ typedef enum w4_status {
 #define W4_GROUP 32        /* codes per group along K */
 #define W4_MAX_K 65536     /* largest supported K */
 #define W4_MAX_M 32        /* largest batch of activation rows per call */
-#define W4_ABI_VERSION 1
+#define W4_ABI_VERSION 2
 
 /* Human-readable name of a status code (static string). */
 const char *w4_status_str(int status);
@@ -303,17 +303,21 @@ void w4_slot_pool_stats(const w4_slot_pool *pool, long long *requests, long long
  * Returns W4_OK and fills *info, or an argument error for an invalid shape.
  */
 typedef struct w4_plan_info {
-    int path;           /* 0 = CUDA-core packed-fp16 kernel */
-    int ctas;           /* CTAs launched (at most one per SM) */
+    int path;           /* 1 = tile-streamed CUDA-core packed-fp16 kernel */
+    int ctas;           /* CTAs launched */
     int slices;         /* K slices (split-K); 1 = none */
-    int threads;        /* threads per CTA */
+    int threads;        /* threads per CTA (7 consumer warps + 1 copy warp) */
     int team;           /* lanes that share one output row */
-    int unit_rows;      /* output rows of one warp work unit */
+    int unit_rows;      /* output rows of one streamed tile */
     int chunk_groups;   /* 32-code groups per K chunk of the row reduction */
     int rows_per_lane;  /* rows a lane works on together (activation reuse) */
     int smem_bytes;     /* dynamic shared memory per CTA */
     int rows_per_call;  /* activation rows handled per launch */
-    int chunk_steps;    /* groups per lane per K chunk (0 = ragged chunks of 8) */
+    int chunk_steps;    /* groups per lane per K chunk */
+    int stages;         /* shared-memory tiles in flight per CTA */
+    int ctas_per_sm;    /* resident CTAs per SM the plan is sized for */
+    int tmpl_team;      /* team size compiled into the kernel (0: generic) */
+    int tmpl_chunk;     /* chunk steps compiled into the kernel (0: generic) */
 } w4_plan_info;
 
 w4_status w4a16_gemv_plan(int M, int N, int K, w4_plan_info *info);

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_call(L):
 
 
 def test_version_and_status_strings(L):
-    assert L.w4_abi_version() == 1
+    assert L.w4_abi_version() == 2
     assert L.w4_status_str(0) == b"ok"
     assert L.w4_status_str(6) == b"id out of range"
     assert L.w4_status_str(999) == b"unknown status"
@@ -79,17 +79,22 @@ def test_host_validation_rejects_before_any_launch(L):
                                    (3, 100, 65536)])
 def test_plan_is_valid(M, N, K):
     p = lib.plan(M, N, K)
-    assert p["threads"] == 256
+    assert p["path"] == 1
+    assert p["threads"] == 256                   # 7 consumer warps + 1 copy warp
     assert p["team"] in (1, 2, 4, 8, 16, 32) and (K // 32) % p["team"] == 0
-    assert p["rows_per_lane"] == 1
-    assert p["unit_rows"] == (32 // p["team"]) * p["rows_per_lane"]
-    cs = p["chunk_steps"]           # chunk steps per lane, 0 = ragged chunks of 8
-    assert p["chunk_groups"] == p["team"] * (cs if cs else 8)
-    if cs:
-        assert (K // 32) % p["chunk_groups"] == 0
+    assert p["rows_per_lane"] in (1, 2, 4)
+    assert p["unit_rows"] == 7 * (32 // p["team"]) * p["rows_per_lane"]
+    assert 1 <= p["chunk_steps"] <= 4
+    assert p["chunk_groups"] == p["team"] * p["chunk_steps"]
     assert 1 <= p["ctas"] <= 2 * 152
+    assert p["ctas_per_sm"] in (1, 2)
+    assert 2 <= p["stages"] <= 8
     assert p["smem_bytes"] <= 232448
-    assert p["rows_per_call"] == min(M, 4 if K <= 16384 else 1)
+    if p["ctas_per_sm"] == 2:
+        assert p["smem_bytes"] <= 233472 // 2 - 1024
+    assert 1 <= p["rows_per_call"] <= min(M, 4)
+    if K <= 21504:
+        assert p["rows_per_call"] == min(M, 4)
     ws = lib.workspace_bytes(M, N, K)
     assert (ws > 0) == (p["slices"] > 1)
 
