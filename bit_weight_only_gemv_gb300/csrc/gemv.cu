@@ -9,9 +9,9 @@
 // `id` at base + id * stride.
 //
 // Design (CTAs of 7 consumer warps + 1 producer warp, one or two per SM):
-//  * The producer warp streams weight tiles (a window of rows x one K chunk:
-//    packed codes and bf16 steps) from HBM into a ring of shared-memory
-//    stages with 1-D bulk copies on the TMA engine.  One mbarrier per stage
+//  * The producer warp streams weight tiles (a window of whole rows: packed
+//    codes and bf16 steps, contiguous in memory) from HBM into a ring of
+//    shared-memory stages with 1-D bulk copies on the TMA engine.  One mbarrier per stage
 //    counts the bytes in ("full"), another the consumer warps done with it
 //    ("empty").  The copies need no registers, so several tiles are in
 //    flight per CTA while the consumers compute, and with W4_FLAG_PDL the
@@ -21,9 +21,10 @@
 //    group's inverse scale.
 //  * A team of T lanes shares an output row (T = a power of two dividing
 //    K/32, chosen from K alone); lane t of the team owns groups t, t + T, ...
-//    of the row.  A lane loads one group's activations once and applies them
-//    to RW rows of the tile (activation reuse), reading each row's codes and
-//    steps from shared memory.
+//    of the row.  The window's work items (a K chunk of a step of rows) are
+//    dealt round-robin to the consumer warps; a lane loads one group's
+//    activations once and applies them to RW rows (activation reuse),
+//    reading each row's codes and steps from shared memory.
 //  * Per group and row the lane turns each packed word into four fp16 pairs
 //    (c - 8) with the float-bit trick of the page in its fp16 form
 //    ((0x6400 | c) - 1032 = c - 8, exact), multiplies them with the fp16
@@ -32,17 +33,17 @@
 //    sum|w x|), adds the 8 partial sums in fp32, rescales by the group's 2^-e
 //    (exact), multiplies by the step and accumulates in fp32.
 //  * K is cut into chunks of CL groups per lane (CL from K alone).  After
-//    each chunk the team reduces with a fixed xor-shuffle tree and the chunk
-//    sums of a row are added in chunk order.  A row's arithmetic therefore
+//    each chunk the team reduces with a fixed xor-shuffle tree; the chunk
+//    sums of a row (kept in shared memory) are added in chunk order.  A row's arithmetic therefore
 //    depends on K only, never on N, M, the row index, the tiling, the split
 //    or the addresses: results are bitwise reproducible, a gemv_id row
 //    equals the gemv of that expert, and merged projections equal separate
 //    ones.
-//  * Each CTA owns a balanced contiguous range of rows (split-K: of (row
-//    block, K slice) units).  Split-K writes chunk sums to the workspace; per
-//    row block and warp, the last of the slices to finish (atomic counter,
-//    no waiting) adds them in chunk order, writes the rows and re-arms the
-//    counter.
+//  * Each CTA owns a balanced contiguous range of rows (split-K, for few
+//    rows and long K: of (row block, K slice) units).  Split-K writes chunk
+//    sums to the workspace; per row block, the last of the slices to finish
+//    (atomic counter, no waiting) adds them in chunk order, writes the rows
+//    and re-arms the counter.
 //  * Every wait is bounded: on expiry the kernel records W4_ERR_TIMEOUT, the
 //    warps leave without further waiting, and the producer lets its copies
 //    in flight land (bounded) before the CTA exits.
@@ -73,17 +74,18 @@ struct GemvParams {
   __nv_bfloat16* y;
   int MR;                              // activation rows per item in this launch
   int N, K, Kg;
+  int Kgp;                             // groups per row padded to a whole team (>= Kg)
   int n_items;
   int T, nsw;                          // lanes per row, row sets per warp (32 / T)
   int NI, CL, nch;                     // groups per lane per row, per chunk; chunks
-  int RB;                              // rows of a tile window (7 warps * nsw * RW)
+  int RB;                              // rows of a window (a multiple of nsw * RW)
   int S, cps, upi;                     // slices, chunks per slice, row blocks per item
   int B;                               // row blocks (split-K only)
   long long U;                         // work items: rows (S == 1) or units
   int x_slots;                         // activation rows staged per CTA (per MR row)
   int nst;                             // pipeline stages
   int tile_bytes, code_pitch, step_pitch, step_off;
-  int* ws_count;                       // [B][7] at the start of the workspace
+  int* ws_count;                       // [B] at the start of the workspace
   float* ws_partial;                   // [B][nch][RB][MR] after it
   int32_t* status;
 };
@@ -93,20 +95,24 @@ struct GemvParams {
 // pairs scaled by 2^e per group of 32 so that the group's largest magnitude
 // lies in [2^9, 2^10).  Layout for staged row j (= slot * MR + m): 16-byte
 // chunk (w, g) = pairs (x[8w+p], x[8w+p+4]) for p = 0..3 of group g, at
-// ((j * 4 + w) * Kg + g) * 16; the inverse scale 2^-e of the group at
-// xscale[j * Kg + g].  Run by the consumer threads.
+// ((j * 4 + w) * Kgp + g) * 16; the inverse scale 2^-e of the group at
+// xscale[j * Kgp + g].  Groups Kg .. Kgp-1 (padding of a team that does not
+// divide K/32) are zero with a zero inverse scale.  Run by the consumer
+// threads.
 __device__ void stage_x(const GemvParams& p, int item0, int nslots, uint8_t* xs, float* xscale) {
   const int rows = nslots * p.MR;
-  for (int idx = threadIdx.x; idx < rows * p.Kg; idx += kConsumers) {
-    const int j = idx / p.Kg;
-    const int g = idx - j * p.Kg;
+  for (int idx = threadIdx.x; idx < rows * p.Kgp; idx += kConsumers) {
+    const int j = idx / p.Kgp;
+    const int g = idx - j * p.Kgp;
     const int slot = j / p.MR, m = j - slot * p.MR;
     const int xrow = (p.x_per_item ? (item0 + slot) * p.MR : 0) + m;
-    const uint4* src =
-        reinterpret_cast<const uint4*>(p.x + (long long)xrow * p.K + (long long)g * 32);
-    uint4 v[4];
+    uint4 v[4] = {};
+    if (g < p.Kg) {
+      const uint4* src =
+          reinterpret_cast<const uint4*>(p.x + (long long)xrow * p.K + (long long)g * 32);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = __ldg(src + i);
+      for (int i = 0; i < 4; ++i) v[i] = __ldg(src + i);
+    }
     uint32_t mx = 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -148,9 +154,9 @@ __device__ void stage_x(const GemvParams& p, int item0, int nslots, uint8_t* xs,
       out.z = *reinterpret_cast<uint32_t*>(&h);
       h = __floats2half2_rn(f[3], f[7]);
       out.w = *reinterpret_cast<uint32_t*>(&h);
-      *reinterpret_cast<uint4*>(xs + ((long long)(j * 4 + w) * p.Kg + g) * 16) = out;
+      *reinterpret_cast<uint4*>(xs + ((long long)(j * 4 + w) * p.Kgp + g) * 16) = out;
     }
-    xscale[(long long)j * p.Kg + g] = inv;
+    xscale[(long long)j * p.Kgp + g] = g < p.Kg ? inv : 0.0f;
   }
 }
 
@@ -269,24 +275,26 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
 }
 
 // ---------------------------------------------------------------- producer
-// All 32 lanes of the producer warp: request tile (window wk, chunk c) into
-// the stage at shared address `stage` (generic pointer `stage_ptr`).
-//  * codes: whole-row windows (one chunk per row) are one contiguous copy;
-//    otherwise one copy per row of the chunk's bytes.
+// All 32 lanes of the producer warp: request the tile of window wk (its rows,
+// chunks [c0, c1)) into the stage at shared address `stage` (generic pointer
+// `stage_ptr`).
+//  * A window of whole rows (all chunks) is contiguous in memory: one copy
+//    for its codes, one for its steps.  A split-K window (a slice of the
+//    chunks) takes one copy of each per row.
 //  * steps: the 16-byte-aligned superset of the needed bytes, clipped to the
 //    item's last full 16-byte line; the bytes past that line (at most 14, at
 //    the very end of the item's step array) are stored by hand.  A row's
 //    steps start at (row * Kg * 2 + first group * 2) mod 16 in its slot.
-__device__ void issue_tile(const GemvParams& p, const Walk& wk, int c, const uint8_t* qwi,
+__device__ void issue_tile(const GemvParams& p, const Walk& wk, const uint8_t* qwi,
                            const uint8_t* sti, uint32_t stage, uint8_t* stage_ptr, uint32_t full,
                            int lane, uint64_t pol) {
   const int gpc = p.CL * p.T;
-  const int gs0 = c * gpc;
-  const int gs1 = min(gs0 + gpc, p.Kg);
+  const int gs0 = wk.c0 * gpc;
+  const int gs1 = min(wk.c1 * gpc, p.Kg);
   const long long row_code = (long long)p.K / 2, row_st = (long long)p.Kg * 2;
   const uintptr_t sbase = reinterpret_cast<uintptr_t>(sti);
   const uintptr_t st_lim = (sbase + (uintptr_t)((long long)p.N * row_st)) & ~(uintptr_t)15;
-  const bool whole = p.nch == 1;
+  const bool whole = wk.c0 == 0 && wk.c1 == p.nch;
   const int copies = whole ? 1 : wk.nrows;
   const int rows = whole ? wk.nrows : 1;
   uint32_t bytes = 0;
@@ -328,11 +336,13 @@ constexpr int kMaxCL = 4;   // groups per lane per chunk, at most
 // lane loads the group's staged activations (MR rows) once and applies them
 // to its RW rows.  acc[j][m] = sum over the chunk's groups, in group order.
 // TT, CLT > 0 fix the team size and the (always full) chunk length at compile
-// time, so every shared-memory offset is an immediate.
+// time, so every shared-memory offset is an immediate.  gleft: groups of the
+// row left from this lane's first one (fewer than the chunk only when the
+// team pads K/32; the generic kernel then drops the padding groups).
 template <int MR, int RW, int TT, int CLT>
 __device__ __forceinline__ void tile_dot(const uint8_t* sm, uint32_t xo, uint32_t xso, int xplane,
                                          int xmrow, int xsmrow, const uint32_t co[RW],
-                                         const uint32_t so[RW], int ns, int T,
+                                         const uint32_t so[RW], int ns, int T, int gleft,
                                          float acc[RW][MR]) {
 #pragma unroll
   for (int j = 0; j < RW; ++j)
@@ -355,7 +365,10 @@ __device__ __forceinline__ void tile_dot(const uint8_t* sm, uint32_t xo, uint32_
 #pragma unroll
     for (int j = 0; j < RW; ++j) {
       const uint4 q = *reinterpret_cast<const uint4*>(sm + co[j] + s * gstep);
-      const float stf = bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(sm + so[j] + s * sstep));
+      float stf = bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(sm + so[j] + s * sstep));
+      // padding groups (generic kernel only): their shared bytes belong to
+      // the next row, so the step is dropped (activations there are zero)
+      if (TT == 0 && s * T >= gleft) stf = 0.0f;
 #pragma unroll
       for (int m = 0; m < MR; ++m) acc[j][m] = fmaf(group_sum(q, xv[m]) * inv[m], stf, acc[j][m]);
     }
@@ -392,6 +405,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
   const uint32_t sbase = smem_addr(smem);
   const uint32_t full0 = sbase, empty0 = sbase + 8 * kMaxStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 16 * kMaxStages);
+  volatile int* last_flag = abort_flag + 1;
   const bool dense = p.ids == nullptr;
   const int nst = p.nst;
 
@@ -417,25 +431,21 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
     long long issued = 0;
     int slot = 0;
     uint32_t phase = 0;   // use count of the slot, mod 2
-    bool ok = true;
-    while (ok && wk.next(p)) {
+    while (wk.next(p)) {
       const uint8_t *qwi, *sti;
       if (!item_arrays(p, wk.item, &qwi, &sti)) continue;
-      for (int c = wk.c0; c < wk.c1; ++c) {
-        // reuse of a slot waits for the consumers to release its last tile
-        if (issued >= nst && !wait_phase(empty0 + 8 * slot, phase ^ 1u, abort_flag)) {
-          if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
-          *abort_flag = 1;
-          ok = false;
-          break;
-        }
-        const uint32_t st_off = kBarBytes + slot * p.tile_bytes;
-        issue_tile(p, wk, c, qwi, sti, sbase + st_off, smem + st_off, full0 + 8 * slot, lane, pol);
-        ++issued;
-        if (++slot == nst) {
-          slot = 0;
-          phase ^= 1u;
-        }
+      // reuse of a slot waits for the consumers to release its last tile
+      if (issued >= nst && !wait_phase(empty0 + 8 * slot, phase ^ 1u, abort_flag)) {
+        if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      const uint32_t st_off = kBarBytes + slot * p.tile_bytes;
+      issue_tile(p, wk, qwi, sti, sbase + st_off, smem + st_off, full0 + 8 * slot, lane, pol);
+      ++issued;
+      if (++slot == nst) {
+        slot = 0;
+        phase ^= 1u;
       }
     }
     // let the last copies land before the CTA may leave
@@ -476,152 +486,171 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
     }
   }
   const uint32_t xs_off = kBarBytes + nst * p.tile_bytes;
-  const uint32_t xsc_off = xs_off + (uint32_t)(p.x_slots * MR * 4 * p.Kg * 16);
+  const uint32_t xsc_off = xs_off + (uint32_t)(p.x_slots * MR * 4 * p.Kgp * 16);
+  float* red = reinterpret_cast<float*>(smem + xsc_off + p.x_slots * MR * p.Kgp * 4);
   pdl_wait();   // activations and outputs follow earlier kernels
   stage_x(p, item0, nslots, smem + xs_off, reinterpret_cast<float*>(smem + xsc_off));
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
 
-  const int xplane = p.Kg * 16, xmrow = 4 * p.Kg * 16, xsmrow = p.Kg * 4;
+  const int xplane = p.Kgp * 16, xmrow = 4 * p.Kgp * 16, xsmrow = p.Kgp * 4;
+  const int kg_valid = p.Kgp != p.Kg ? p.Kg : 0x7fffffff;   // groups past it are padding
   const int gpc = p.CL * T;                  // groups per chunk
-  const bool whole = p.nch == 1;
   const int kg2 = p.Kg * 2;
-  float rowsum[RW][MR];
+  const int rstep = nsw * RW;                // rows of one item
+  const int nrs_full = p.RB / rstep;         // row steps of a full window
+  const bool steps_aligned = (kg2 & 15) == 0;
+  uint32_t lane_c[RW], lane_s[RW];           // lane offsets within a whole-row tile
 #pragma unroll
-  for (int j = 0; j < RW; ++j)
-#pragma unroll
-    for (int m = 0; m < MR; ++m) rowsum[j][m] = 0.0f;
-
+  for (int j = 0; j < RW; ++j) {
+    lane_c[j] = (uint32_t)((j * nsw + set) * p.code_pitch + t * 16);
+    lane_s[j] = (uint32_t)(p.step_off + (j * nsw + set) * kg2 + t * 2);
+  }
   Walk wk;
   wk.init(p);
   int slot = 0;
   uint32_t phase = 0;
   uint32_t tile = kBarBytes;   // shared offset of the current slot
+  int rbuf = 0;                // chunk-sum buffer of this window
   bool reported = false;
   while (wk.next(p)) {
     const uint8_t *qwi, *sti;
-    if (!item_arrays(p, wk.item, &qwi, &sti)) {
+    if (!dense && !item_arrays(p, wk.item, &qwi, &sti)) {
       if (!reported && lane == 0) report(p.status, W4_ERR_INDEX);
       reported = true;
       continue;
     }
-    // per-window, per-row offsets within a tile (32-bit)
     const int xslot = p.x_per_item ? wk.item - item0 : 0;
-    uint32_t crow[RW], srow[RW], soff[RW];
-    bool rv[RW];
-#pragma unroll
-    for (int j = 0; j < RW; ++j) {
-      // rows past the window read the window's last row (results dropped)
-      const int rw = (j * kConsumerWarps + warp) * nsw + set;
-      rv[j] = rw < wk.nrows;
-      const int rl = rv[j] ? rw : wk.nrows - 1;
-      crow[j] = rl * p.code_pitch + t * 16;
-      // start of the row's steps within its copied 16-byte lines
-      const int r16 = ((wk.row0 + rl) & 7) * (kg2 & 15);
-      srow[j] = p.step_off + t * 2 +
-                (whole ? (((wk.row0 & 7) * (kg2 & 15)) & 15) + rl * kg2 : rl * p.step_pitch);
-      soff[j] = whole ? 0u : (uint32_t)r16;
-    }
+    const bool whole = p.S == 1;
+    const bool full = wk.nrows == p.RB;
+    // full windows of whole rows whose steps start on 16-byte lines: every
+    // offset below is a lane constant plus a per-item term
+    const bool fast = whole && full && steps_aligned;
+    const int ncw = wk.c1 - wk.c0;                       // chunks in the window
+    const int nrs = full ? nrs_full : (wk.nrows + rstep - 1) / rstep;   // row steps
+    const int items = ncw * nrs;
+    const int soff0 = whole ? (((wk.row0 & 7) * (kg2 & 15)) & 15) : 0;
+    float* redw = red + (long long)rbuf * p.RB * p.nch * MR;
     __nv_bfloat16* yrow = p.y + (long long)wk.item * MR * p.N + wk.row0;
-    uint32_t xo = xs_off + (uint32_t)(((xslot * MR * 4) * p.Kg + wk.c0 * gpc + t) * 16);
-    uint32_t xso = xsc_off + (uint32_t)(((xslot * MR) * p.Kg + wk.c0 * gpc + t) * 4);
-    for (int c = wk.c0; c < wk.c1; ++c) {
-      if (!wait_phase(full0 + 8 * slot, phase, abort_flag)) {
-        if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
-        *abort_flag = 1;
-        return;
-      }
-      const int ns = min(p.CL, p.NI - c * p.CL);
-      const int g2 = c * gpc * 2;
-      uint32_t co[RW], so[RW];
-#pragma unroll
-      for (int j = 0; j < RW; ++j) {
-        co[j] = tile + crow[j];
-        so[j] = tile + srow[j] + (whole ? 0u : ((soff[j] + g2) & 15));
-      }
-      float acc[RW][MR];
-      tile_dot<MR, RW, TT, CLT>(smem, xo, xso, xplane, xmrow, xsmrow, co, so, ns, T, acc);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * slot);   // this warp is done with the stage
-      if (++slot == nst) {
-        slot = 0;
-        phase ^= 1u;
-        tile = kBarBytes;
-      } else {
-        tile += p.tile_bytes;
-      }
-      xo += gpc * 16;
-      xso += gpc * 4;
 
+    if (!wait_phase(full0 + 8 * slot, phase, abort_flag)) {
+      if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
+      *abort_flag = 1;
+      return;
+    }
+    for (int it = warp; it < items; it += kConsumerWarps) {
+      // item = (chunk ci of the window, row step rs), it = ci * nrs + rs
+      int ci, rs;
+      if (nrs == 1) {
+        ci = it;
+        rs = 0;
+      } else if (ncw == 1) {
+        ci = 0;
+        rs = it;
+      } else {
+        ci = it / nrs;
+        rs = it - ci * nrs;
+      }
+      const int c = wk.c0 + ci;
+      uint32_t co[RW], so[RW];
+      int rl[RW];
+      bool rv[RW];
+      if (fast) {
+        const uint32_t ic = tile + (uint32_t)(rs * rstep * p.code_pitch + ci * gpc * 16);
+        const uint32_t is = tile + (uint32_t)(rs * rstep * kg2 + ci * gpc * 2);
+#pragma unroll
+        for (int j = 0; j < RW; ++j) {
+          rv[j] = true;
+          rl[j] = rs * rstep + j * nsw + set;
+          co[j] = ic + lane_c[j];
+          so[j] = is + lane_s[j];
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < RW; ++j) {
+          // rows past the window read the window's last row (results dropped)
+          const int r = rs * rstep + j * nsw + set;
+          rv[j] = r < wk.nrows;
+          rl[j] = rv[j] ? r : wk.nrows - 1;
+          co[j] = tile + rl[j] * p.code_pitch + (ci * gpc + t) * 16;
+          so[j] = tile + p.step_off + (ci * gpc + t) * 2 +
+                  (whole ? soff0 + rl[j] * kg2
+                         : rl[j] * p.step_pitch +
+                               ((((wk.row0 + rl[j]) & 7) * (kg2 & 15) + wk.c0 * gpc * 2) & 15));
+        }
+      }
+      const int g0 = c * gpc + t;
+      const uint32_t xo = xs_off + (uint32_t)(((xslot * MR * 4) * p.Kgp + g0) * 16);
+      const uint32_t xso = xsc_off + (uint32_t)(((xslot * MR) * p.Kgp + g0) * 4);
+      const int ns = min(p.CL, p.NI - c * p.CL);
+      float acc[RW][MR];
+      tile_dot<MR, RW, TT, CLT>(smem, xo, xso, xplane, xmrow, xsmrow, co, so, ns, T,
+                                kg_valid - g0, acc);
 #pragma unroll
       for (int j = 0; j < RW; ++j)
 #pragma unroll
         for (int m = 0; m < MR; ++m) acc[j][m] = team_sum<TT>(acc[j][m], T);
-
-      if (p.S == 1) {
-#pragma unroll
-        for (int j = 0; j < RW; ++j)
-#pragma unroll
-          for (int m = 0; m < MR; ++m) rowsum[j][m] += acc[j][m];
-        if (c == p.nch - 1) {
-          if (t == 0) {
-#pragma unroll
-            for (int j = 0; j < RW; ++j) {
-              if (!rv[j]) continue;
-              const int rl = (j * kConsumerWarps + warp) * nsw + set;
-#pragma unroll
-              for (int m = 0; m < MR; ++m)
-                yrow[(long long)m * p.N + rl] = __float2bfloat16_rn(rowsum[j][m]);
-            }
-          }
-#pragma unroll
-          for (int j = 0; j < RW; ++j)
-#pragma unroll
-            for (int m = 0; m < MR; ++m) rowsum[j][m] = 0.0f;
-        }
-        continue;
-      }
-      // split-K: chunk sums to the workspace
       if (t == 0) {
 #pragma unroll
         for (int j = 0; j < RW; ++j) {
           if (!rv[j]) continue;
-          const int rl = (j * kConsumerWarps + warp) * nsw + set;
-          float* dst = p.ws_partial + (((long long)wk.rb * p.nch + c) * p.RB + rl) * MR;
+          if (!whole) {          // split-K: chunk sums to the workspace
+            float* dst = p.ws_partial + (((long long)wk.rb * p.nch + c) * p.RB + rl[j]) * MR;
 #pragma unroll
-          for (int m = 0; m < MR; ++m) dst[m] = acc[j][m];
-        }
-      }
-      if (c == wk.c1 - 1) {
-        // The last of the slices to finish this row block (for this warp's
-        // rows) adds the chunk sums in chunk order, writes the rows and
-        // re-arms the counter.  The warp barrier orders every lane's partial
-        // stores before lane 0's counter update, whose release publishes them
-        // at GPU scope; its acquire side, then the second warp barrier, order
-        // the other slices' partials before this warp reads them.
-        __syncwarp();
-        int* counter = p.ws_count + (long long)wk.rb * kConsumerWarps + warp;
-        int last = 0;
-        if (lane == 0) last = atomic_add_acq_rel_gpu(counter, 1) == p.S - 1;
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
-          __syncwarp();
-          if (t == 0) {
+            for (int m = 0; m < MR; ++m) dst[m] = acc[j][m];
+          } else if (ncw == 1) { // one chunk: the row is done (0 + chunk sum)
 #pragma unroll
-            for (int j = 0; j < RW; ++j) {
-              if (!rv[j]) continue;
-              const int rl = (j * kConsumerWarps + warp) * nsw + set;
-              const float* src = p.ws_partial + ((long long)wk.rb * p.nch * p.RB + rl) * MR;
+            for (int m = 0; m < MR; ++m)
+              yrow[(long long)m * p.N + rl[j]] = __float2bfloat16_rn(0.0f + acc[j][m]);
+          } else {
 #pragma unroll
-              for (int m = 0; m < MR; ++m) {
-                float v = 0.0f;
-                for (int cc = 0; cc < p.nch; ++cc) v += __ldcg(src + (long long)cc * p.RB * MR + m);
-                yrow[(long long)m * p.N + rl] = __float2bfloat16_rn(v);
-              }
-            }
+            for (int m = 0; m < MR; ++m) redw[(rl[j] * p.nch + ci) * MR + m] = acc[j][m];
           }
-          if (lane == 0) atomicExch(counter, 0);
         }
       }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * slot);   // this warp is done with the stage
+    if (++slot == nst) {
+      slot = 0;
+      phase ^= 1u;
+      tile = kBarBytes;
+    } else {
+      tile += p.tile_bytes;
+    }
+
+    if (whole) {
+      if (ncw > 1) {
+        // chunk sums of each row, added in chunk order
+        asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+        for (int i = threadIdx.x; i < wk.nrows * MR; i += kConsumers) {
+          const int r = i / MR, m = i - r * MR;
+          float v = 0.0f;
+          for (int cc = 0; cc < ncw; ++cc) v += redw[(r * p.nch + cc) * MR + m];
+          yrow[(long long)m * p.N + r] = __float2bfloat16_rn(v);
+        }
+        rbuf ^= 1;
+      }
+      continue;
+    }
+    // Split-K: the last of the slices to finish this row block adds the chunk
+    // sums in chunk order, writes the rows and re-arms the counter.  The CTA
+    // barrier orders every thread's partial stores before thread 0's counter
+    // update, whose release publishes them at GPU scope; its acquire side,
+    // then the second barrier, order the other slices' partials before this
+    // CTA reads them.
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+    if (threadIdx.x == 0)
+      *last_flag = atomic_add_acq_rel_gpu(p.ws_count + wk.rb, 1) == p.S - 1;
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+    if (*last_flag) {
+      for (int i = threadIdx.x; i < wk.nrows * MR; i += kConsumers) {
+        const int r = i / MR, m = i - r * MR;
+        const float* src = p.ws_partial + ((long long)wk.rb * p.nch * p.RB + r) * MR + m;
+        float v = 0.0f;
+        for (int cc = 0; cc < p.nch; ++cc) v += __ldcg(src + (long long)cc * p.RB * MR);
+        yrow[(long long)m * p.N + r] = __float2bfloat16_rn(v);
+      }
+      if (threadIdx.x == 0) atomicExch(p.ws_count + wk.rb, 0);
     }
   }
 }
@@ -665,6 +694,7 @@ DeviceInfo device_info(int dev) {
 
 struct Plan {
   int MR = 1;
+  int Kg = 1;
   int T = 32, nsw = 1, NI = 1, CL = 1, nch = 1;
   int RW = 1, RB = 8;
   int S = 1, cps = 1, upi = 1;
@@ -677,6 +707,10 @@ struct Plan {
   size_t ws_bytes = 0;
   size_t ws_part_off = 0;
 };
+
+constexpr long long kTileMax = 48 << 10;   // largest stage the planner picks
+constexpr long long kTileGood = 24 << 10;  // stages this large amortise a window's overhead
+constexpr long long kRowStepMax = 40 << 10;  // largest step of whole rows
 
 // The per-row arithmetic comes from K alone.  T: the largest power of two
 // <= 32 dividing K/32 that leaves each lane >= 4 groups of a row (else the
@@ -691,8 +725,14 @@ void row_shape(int K, int* T, int* NI, int* CL, int* nch) {
     t = 1;
     while (t < 32 && Kg % (2 * t) == 0) t *= 2;
   }
+  // A step of 32 / t whole rows must fit a stage; otherwise a team of up to
+  // 32 lanes walks the row with the last groups padded.
+  if ((long long)(32 / t) * (K / 2 + Kg * 2) > kRowStepMax) {
+    t = 32;
+    while (t > 1 && (Kg + t - 1) / t < 4) t /= 2;
+  }
   *T = t;
-  const int ni = Kg / t;
+  const int ni = (Kg + t - 1) / t;
   int cl = 4;
   if (ni <= 4) cl = ni;
   else if (ni % 4 == 0) cl = 4;
@@ -702,18 +742,25 @@ void row_shape(int K, int* T, int* NI, int* CL, int* nch) {
   *nch = (ni + cl - 1) / cl;
 }
 
-long long x_bytes(int slots, int MR, int Kg) { return (long long)slots * MR * Kg * (64 + 4); }
+long long x_bytes(int slots, int MR, int Kgp) { return (long long)slots * MR * Kgp * (64 + 4); }
 
-// Stage geometry for `rb` rows per window.
-void tile_geometry(int K, int T, int CL, int nch, int rb, int* code_pitch, int* step_pitch,
-                   int* step_off, int* tile_bytes) {
+// Stage geometry of a window of `rb` rows: whole rows (contiguous codes, then
+// the steps' 16-byte superset), or `cps` chunks of each row (split-K: one
+// slot per row for codes and for steps).
+void tile_geometry(int K, int T, int CL, bool whole, int cps, int rb, int* code_pitch,
+                   int* step_pitch, int* step_off, int* tile_bytes) {
   const int Kg = K / 32;
-  *code_pitch = CL * T * 16;
-  *step_pitch = nch == 1 ? Kg * 2 : ((CL * T * 2 + 30 + 15) & ~15);
-  *step_off = rb * *code_pitch;
-  const long long steps = nch == 1 ? (long long)rb * Kg * 2 + 32 : (long long)rb * *step_pitch;
+  const int pad = T - 1;   // padding groups a lane may read past a row's end
+  *code_pitch = whole ? K / 2 : cps * CL * T * 16;
+  *step_pitch = whole ? Kg * 2 : ((cps * CL * T * 2 + 30 + 15) & ~15);
+  *step_off = rb * *code_pitch + pad * 16;
+  const long long steps =
+      whole ? (long long)rb * Kg * 2 + 32 + pad * 2 : (long long)rb * *step_pitch;
   *tile_bytes = (int)((*step_off + steps + 127) & ~127LL);
 }
+
+// Chunk sums of a window of whole rows, double-buffered (none for one chunk).
+long long red_bytes(int rb, int nch, int MR) { return nch > 1 ? 2LL * rb * nch * MR * 4 : 0; }
 
 using KernelFn = void (*)(GemvParams);
 int occupancy(const struct Plan& pl, int dev);
@@ -723,6 +770,7 @@ bool make_plan(int MR, int N, int K, int n_items, int allow_split, int x_per_ite
   Plan pl;
   pl.MR = MR;
   const int Kg = K / 32;
+  pl.Kg = Kg;
   row_shape(K, &pl.T, &pl.NI, &pl.CL, &pl.nch);
   pl.nsw = 32 / pl.T;
   const int sms = di.sms > 0 ? di.sms : 1;
@@ -738,18 +786,28 @@ bool make_plan(int MR, int N, int K, int n_items, int allow_split, int x_per_ite
   if (force_per_sm > 0) pl.per_sm = force_per_sm;
   // shared memory a CTA may take and still leave room for a second one
   const long long half = per_sm_smem / 2 - reserved;
-  const long long min_rows = (long long)kConsumerWarps * pl.nsw;   // rows of one RW = 1 window
+  // fewest rows a CTA should own: enough (row step, chunk) items for its warps
+  const long long min_rows =
+      std::max<long long>(pl.nsw, ((long long)kConsumerWarps * pl.nsw + pl.nch - 1) / pl.nch);
   const long long target = (long long)pl.per_sm * sms;
   const long long g1 = std::min(target, (rows_total + min_rows - 1) / min_rows);
   int rw_cap = MR == 1 ? 4 : (MR == 2 ? 2 : 1);
+  // few rows, long K: split K across CTAs (windows of one row step)
+  const long long blocks = (long long)n_items * ((N + pl.nsw - 1) / pl.nsw);
+  // chunks per slice: few enough that a window (one row step) fits a stage
+  const long long step_chunk = (long long)pl.nsw * pl.CL * pl.T * 18;
+  const int cps_max = (int)std::max<long long>(1, kTileMax / step_chunk);
+  int split = 1;
   if (allow_split && pl.nch > 1 && 2 * g1 < target) {
-    // few rows, long K: split K across CTAs
-    pl.RB = (int)min_rows;
+    split = (int)std::min<long long>(pl.nch, (target + blocks - 1) / blocks);
+    split = std::max(split, (pl.nch + cps_max - 1) / cps_max);
+  }
+  if (split > 1) {
+    pl.RB = pl.nsw;
     pl.upi = (int)((N + pl.RB - 1) / pl.RB);
-    pl.B = (long long)n_items * pl.upi;
+    pl.B = blocks;
     if (pl.B > (1LL << 30)) return false;
-    const int S = (int)std::min<long long>(pl.nch, (target + pl.B - 1) / pl.B);
-    pl.cps = (pl.nch + S - 1) / S;
+    pl.cps = (pl.nch + split - 1) / split;
     pl.S = (pl.nch + pl.cps - 1) / pl.cps;
     pl.U = (long long)pl.S * pl.B;
     pl.ctas = (int)std::min<long long>(pl.U, target);
@@ -776,36 +834,54 @@ bool make_plan(int MR, int N, int K, int n_items, int allow_split, int x_per_ite
       pl.x_slots = (int)std::max<long long>(pl.x_slots, n);
     }
   }
-  const long long xb = x_bytes(pl.x_slots, MR, Kg);
-  // rows per lane: the most that still gives >= 3 stages (>= 2 at RW = 1)
-  // and windows no taller than a CTA's share of the rows
+  const long long xb = x_bytes(pl.x_slots, MR, pl.NI * pl.T);
+  // Window shape: RW rows per lane and `rs` row steps per window (whole rows;
+  // a split-K window is one row step).  Score: the share of warp slots the
+  // window's (row step, chunk) items fill, stages of at least kTileGood
+  // bytes, three or more stages, then activation reuse (RW).
   const long long rows_per_cta = (pl.U + pl.ctas - 1) / pl.ctas;
   bool found = false;
   const long long budgets[2] = {half, std::min(optin, per_sm_smem - reserved)};
   for (int bi = 0; bi < 2 && !found; ++bi) {
-    for (int rw = rw_cap; rw >= 1 && !found; rw /= 2) {
-      const int rb = (int)min_rows * rw;
-      if (pl.S == 1 && rw > 1 && rb > rows_per_cta) continue;
-      int cp, sp, so, tb;
-      tile_geometry(K, pl.T, pl.CL, pl.nch, rb, &cp, &sp, &so, &tb);
-      const long long room = budgets[bi] - kBarBytes - xb;
-      if (room < 2LL * tb) continue;
-      const int nst = (int)std::min<long long>(kMaxStages, room / tb);
-      if (nst < 3 && rw > 1) continue;
-      pl.RW = rw;
-      pl.RB = rb;
-      pl.nst = nst;
-      pl.code_pitch = cp;
-      pl.step_pitch = sp;
-      pl.step_off = so;
-      pl.tile_bytes = tb;
-      found = true;
+    double best = 0.0;
+    for (int rw = rw_cap; rw >= 1; rw /= 2) {
+      for (int rs = 1; rs <= 64; ++rs) {
+        const int rb = rs * pl.nsw * rw;
+        if (pl.S > 1 && (rs > 1 || rw > 1)) break;
+        if (rs > 1 && rb > rows_per_cta) break;
+        int cp, sp, so, tb;
+        tile_geometry(K, pl.T, pl.CL, pl.S == 1, pl.cps, rb, &cp, &sp, &so, &tb);
+        if (rs > 1 && tb > kTileMax) break;
+        const long long rd = pl.S == 1 ? red_bytes(rb, pl.nch, MR) : 0;
+        const long long room = budgets[bi] - kBarBytes - xb - rd;
+        if (room < 2LL * tb) break;
+        const int nst = (int)std::min<long long>(kMaxStages, room / tb);
+        const long long items = (long long)(pl.S == 1 ? pl.nch : pl.cps) * rs;
+        const double util =
+            (double)items / (double)(kConsumerWarps * ((items + kConsumerWarps - 1) / kConsumerWarps));
+        const double per_warp = (double)items / kConsumerWarps;   // items a warp takes
+        const double score = util * std::min(1.0, (double)tb / kTileGood) *
+                             (nst >= 3 ? 1.0 : 0.95) * (1.0 - 0.15 / std::max(1.0, per_warp)) *
+                             (1.0 + 0.2 * (rw > 1) + 0.1 * (rw > 2));
+        if (score > best + 1e-9) {
+          best = score;
+          pl.RW = rw;
+          pl.RB = rb;
+          pl.nst = nst;
+          pl.code_pitch = cp;
+          pl.step_pitch = sp;
+          pl.step_off = so;
+          pl.tile_bytes = tb;
+          found = true;
+        }
+      }
     }
     if (found && bi == 1 && pl.per_sm > 1)   // only one CTA per SM fits
       return make_plan(MR, N, K, n_items, allow_split, x_per_item, di, out, 1);
   }
   if (!found) return false;
-  pl.smem = kBarBytes + (long long)pl.nst * pl.tile_bytes + xb;
+  pl.smem = kBarBytes + (long long)pl.nst * pl.tile_bytes + xb +
+            (pl.S == 1 ? red_bytes(pl.RB, pl.nch, MR) : 0);
   // resident CTAs the device really fits (registers, shared memory); fewer
   // than planned: the same work over fewer CTAs
   if (di.dev >= 0) {
@@ -817,7 +893,7 @@ bool make_plan(int MR, int N, int K, int n_items, int allow_split, int x_per_ite
   if (pl.S > 1) {
     // counters first, partials after them
     const size_t part = (size_t)pl.B * pl.nch * pl.RB * MR * sizeof(float);
-    pl.ws_part_off = ((size_t)pl.B * kConsumerWarps * sizeof(int) + 255) & ~size_t(255);
+    pl.ws_part_off = ((size_t)pl.B * sizeof(int) + 255) & ~size_t(255);
     pl.ws_bytes = pl.ws_part_off + part;
   }
   *out = pl;
@@ -833,7 +909,7 @@ using KernelFn = void (*)(GemvParams);
 KernelFn kernel_for(const Plan& pl, int* tt = nullptr, int* clt = nullptr) {
   if (tt != nullptr) *tt = 0;
   if (clt != nullptr) *clt = 0;
-  const bool full = pl.NI % pl.CL == 0;
+  const bool full = pl.NI % pl.CL == 0 && pl.NI * pl.T == pl.Kg;
   if (pl.MR == 1 && full && pl.RW <= 2) {
     const int key = pl.T * 8 + pl.CL;
 #define W4_SPEC(t, cl)                                                          \
@@ -920,6 +996,7 @@ GemvParams base_params(const Plan& pl, int N, int K) {
   p.N = N;
   p.K = K;
   p.Kg = K / 32;
+  p.Kgp = pl.NI * pl.T;
   p.MR = pl.MR;
   p.T = pl.T;
   p.nsw = pl.nsw;
@@ -1002,9 +1079,10 @@ int max_rows_per_launch(int K, const DeviceInfo& di) {
   const long long optin = di.smem_optin > 0 ? di.smem_optin : 232448;
   int T, NI, CL, nch, cp, sp, so, tb;
   row_shape(K, &T, &NI, &CL, &nch);
-  tile_geometry(K, T, CL, nch, kConsumerWarps * (32 / T), &cp, &sp, &so, &tb);
+  tile_geometry(K, T, CL, true, nch, 32 / T, &cp, &sp, &so, &tb);
   int mr = kMaxMR;
-  while (mr > 0 && kBarBytes + 2LL * tb + x_bytes(1, mr, K / 32) > optin) --mr;
+  while (mr > 0 && kBarBytes + 2LL * tb + x_bytes(1, mr, NI * T) + red_bytes(32 / T, nch, mr) > optin)
+    --mr;
   return mr;
 }
 
@@ -1210,7 +1288,7 @@ extern "C" w4_status w4a16_gemv_static_scratch(void* y, const void* qw, const vo
       // the counters must start at zero; the array keeps the previous call's
       // contents (and an aborted call may leave them armed)
       if (e == cudaSuccess)
-        e = cudaMemsetAsync(base, 0, (size_t)pm.B * kConsumerWarps * sizeof(int), s);
+        e = cudaMemsetAsync(base, 0, (size_t)pm.B * sizeof(int), s);
       if (e != cudaSuccess) {
         note_cuda_error(e);
         cudaGetLastError();

@@ -151,7 +151,7 @@ size_t w4a16_gemv_workspace_bytes(int M, int N, int K);
  *    the GPU (for example issued to different streams) race on the array:
  *    issue them one after another in one stream per device.
  */
-#define W4_STATIC_SCRATCH_BYTES (4u << 20)
+#define W4_STATIC_SCRATCH_BYTES (256u << 10)
 
 w4_status w4a16_gemv_static_scratch(void *y, const void *qw, const void *st, const void *x,
                                     int M, int N, int K, int32_t *status_dev,

@@ -83,7 +83,7 @@ def test_plan_is_valid(M, N, K):
     assert p["threads"] == 256                   # 7 consumer warps + 1 copy warp
     assert p["team"] in (1, 2, 4, 8, 16, 32) and (K // 32) % p["team"] == 0
     assert p["rows_per_lane"] in (1, 2, 4)
-    assert p["unit_rows"] == 7 * (32 // p["team"]) * p["rows_per_lane"]
+    assert p["unit_rows"] % ((32 // p["team"]) * p["rows_per_lane"]) == 0
     assert 1 <= p["chunk_steps"] <= 4
     assert p["chunk_groups"] == p["team"] * p["chunk_steps"]
     assert 1 <= p["ctas"] <= 2 * 152
