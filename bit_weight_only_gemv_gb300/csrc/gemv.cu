@@ -512,6 +512,92 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
   uint32_t tile = kBarBytes;   // shared offset of the current slot
   int rbuf = 0;                // chunk-sum buffer of this window
   bool reported = false;
+
+  // Steady state of a dense call: the CTA's full windows (the copy warp walks
+  // the same ones first), back to back, with every offset but the tile base
+  // and the window's first row fixed for the whole launch.
+  if (dense && p.S == 1) {
+    const long long nfull = (wk.end - wk.pos) / p.RB;
+    const int ncw = p.nch;
+    const int items = ncw * nrs_full;
+    int row0 = (int)wk.pos;
+    for (long long w = 0; w < nfull; ++w) {
+      const uint32_t soff0 = steps_aligned ? 0u : (uint32_t)(((row0 & 7) * (kg2 & 15)) & 15);
+      float* redw = red + rbuf * p.RB * p.nch * MR;
+      if (!wait_phase(full0 + 8 * slot, phase, abort_flag)) {
+        if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
+        *abort_flag = 1;
+        return;
+      }
+      for (int it = warp; it < items; it += kConsumerWarps) {
+        int ci, rs;
+        if (nrs_full == 1) {
+          ci = it;
+          rs = 0;
+        } else if (ncw == 1) {
+          ci = 0;
+          rs = it;
+        } else {
+          ci = it / nrs_full;
+          rs = it - ci * nrs_full;
+        }
+        const uint32_t ic = tile + (uint32_t)(rs * rstep * p.code_pitch + ci * gpc * 16);
+        const uint32_t is = tile + soff0 + (uint32_t)(rs * rstep * kg2 + ci * gpc * 2);
+        uint32_t co[RW], so[RW];
+#pragma unroll
+        for (int j = 0; j < RW; ++j) {
+          co[j] = ic + lane_c[j];
+          so[j] = is + lane_s[j];
+        }
+        const int g0 = ci * gpc + t;
+        const int ns = CLT > 0 ? CLT : min(p.CL, p.NI - ci * p.CL);
+        float acc[RW][MR];
+        tile_dot<MR, RW, TT, CLT>(smem, xs_off + (uint32_t)(g0 * 16), xsc_off + (uint32_t)(g0 * 4),
+                                  xplane, xmrow, xsmrow, co, so, ns, T, kg_valid - g0, acc);
+#pragma unroll
+        for (int j = 0; j < RW; ++j)
+#pragma unroll
+          for (int m = 0; m < MR; ++m) acc[j][m] = team_sum<TT>(acc[j][m], T);
+        if (t == 0) {
+#pragma unroll
+          for (int j = 0; j < RW; ++j) {
+            const int rl = rs * rstep + j * nsw + set;
+            if (ncw == 1) {   // one chunk: the row is done (0 + chunk sum)
+#pragma unroll
+              for (int m = 0; m < MR; ++m)
+                p.y[(long long)m * p.N + row0 + rl] = __float2bfloat16_rn(0.0f + acc[j][m]);
+            } else {
+#pragma unroll
+              for (int m = 0; m < MR; ++m) redw[(rl * p.nch + ci) * MR + m] = acc[j][m];
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * slot);   // this warp is done with the stage
+      if (++slot == nst) {
+        slot = 0;
+        phase ^= 1u;
+        tile = kBarBytes;
+      } else {
+        tile += p.tile_bytes;
+      }
+      if (ncw > 1) {
+        // chunk sums of each row, added in chunk order
+        asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+        for (int i = threadIdx.x; i < p.RB * MR; i += kConsumers) {
+          const int r = i / MR, m = i - r * MR;
+          float v = 0.0f;
+          for (int cc = 0; cc < ncw; ++cc) v += redw[(r * p.nch + cc) * MR + m];
+          p.y[(long long)m * p.N + row0 + r] = __float2bfloat16_rn(v);
+        }
+        rbuf ^= 1;
+      }
+      row0 += p.RB;
+    }
+    wk.pos += nfull * p.RB;   // the generic walk takes the partial window left
+  }
+
   while (wk.next(p)) {
     const uint8_t *qwi, *sti;
     if (!dense && !item_arrays(p, wk.item, &qwi, &sti)) {
