@@ -37,6 +37,7 @@ sys.path.insert(0, ROOT)
 from bit_weight_only_gemv_gb300 import metrics, synth  # noqa: E402
 
 METRIC = "W4A16 GEMV HBM GB/s and % of GB300 peak; decode-equivalent tok/s at batch 1"
+DENSE_WORKLOADS = {"dense-35L-h2048": synth.dense_2048, "dense-60L-h5376": synth.dense_5376}
 UNIT = "tok/s"
 NOMINAL_HBM_GBPS = 8000.0
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
@@ -141,8 +142,8 @@ class DecodePass:
         self.emb_qw = synth.torch_words((V, h // 8), synth.seed_of(s, 1), device)
         self.emb_st = synth.torch_steps((V, h // 32), synth.seed_of(s, 2), device)
         pw = model.per_layer_width
-        self.ple_qw = synth.torch_words((V, pw // 8), synth.seed_of(s, 3), device)
-        self.ple_st = synth.torch_steps((V, pw // 32), synth.seed_of(s, 4), device)
+        self.ple_qw = synth.torch_words((V, pw // 8), synth.seed_of(s, 3), device) if pw else None
+        self.ple_st = synth.torch_steps((V, pw // 32), synth.seed_of(s, 4), device) if pw else None
         # weight matrices per layer; projections that read the same activation
         # (q/k/v, gate/up) are stored as one row-concatenated matrix when merged
         groups = []
@@ -186,7 +187,7 @@ class DecodePass:
         off += V
         self.y_flat = torch.empty(off, dtype=torch.bfloat16, device=device)
         self.emb_row = torch.empty((1, h), dtype=torch.bfloat16, device=device)
-        self.ple_row = torch.empty((1, pw), dtype=torch.bfloat16, device=device)
+        self.ple_row = torch.empty((1, pw), dtype=torch.bfloat16, device=device) if pw else None
         ws = 0
         for li, name, n, k, xk, _, _ in self.mats:
             ws = max(ws, lib.workspace_bytes(1, n, k))
@@ -204,8 +205,9 @@ class DecodePass:
         out = []
         out.append(("gather", (1, m.hidden), lambda pdl: lib.embed_gather(
             self.emb_qw, self.emb_st, self.ids, out=self.emb_row, status=self.status, pdl=pdl)))
-        out.append(("gather", (1, m.per_layer_width), lambda pdl: lib.embed_gather(
-            self.ple_qw, self.ple_st, self.ids, out=self.ple_row, status=self.status, pdl=pdl)))
+        if m.per_layer_width:
+            out.append(("gather", (1, m.per_layer_width), lambda pdl: lib.embed_gather(
+                self.ple_qw, self.ple_st, self.ids, out=self.ple_row, status=self.status, pdl=pdl)))
         for li, name, n, k, xk, qw, st in self.mats:
             x = self.x((li, xk), k)
             o = self.y_off[(li, name)]
@@ -306,8 +308,10 @@ def oracle_sample(dp, proj_names, lm_rows, layer=0):
     tid = int(dp.ids.item())
     e_qw = dp.emb_qw[tid:tid + 1].cpu().numpy().view(np.uint32)
     e_st = dp.emb_st[tid:tid + 1].view(torch.int16).cpu().numpy().view(np.uint16)
-    p_qw = dp.ple_qw[tid:tid + 1].cpu().numpy().view(np.uint32)
-    p_st = dp.ple_st[tid:tid + 1].view(torch.int16).cpu().numpy().view(np.uint16)
+    pw = m.per_layer_width
+    if pw:
+        p_qw = dp.ple_qw[tid:tid + 1].cpu().numpy().view(np.uint32)
+        p_st = dp.ple_st[tid:tid + 1].view(torch.int16).cpu().numpy().view(np.uint16)
     t0 = time.perf_counter()
     nbytes = 0
     for qw, st, x, b in host:
@@ -316,8 +320,10 @@ def oracle_sample(dp, proj_names, lm_rows, layer=0):
     oracle.gemv_ref(lm_qw, lm_st, lm_x)
     nbytes += metrics.gemv_bytes(1, lm_rows, m.hidden)
     oracle.gather_ref(e_qw, e_st, np.array([0]))
-    oracle.gather_ref(p_qw, p_st, np.array([0]))
-    nbytes += metrics.gather_bytes(1, m.hidden) + metrics.gather_bytes(1, m.per_layer_width)
+    nbytes += metrics.gather_bytes(1, m.hidden)
+    if pw:
+        oracle.gather_ref(p_qw, p_st, np.array([0]))
+        nbytes += metrics.gather_bytes(1, pw)
     return time.perf_counter() - t0, nbytes
 
 
@@ -349,7 +355,9 @@ def reference_sample(model, seed=0):
 
 
 def step_bytes_of(model):
-    b = metrics.gather_bytes(1, model.hidden) + metrics.gather_bytes(1, model.per_layer_width)
+    b = metrics.gather_bytes(1, model.hidden)
+    if model.per_layer_width:
+        b += metrics.gather_bytes(1, model.per_layer_width)
     for pr in model.projs:
         b += model.layers * metrics.gemv_bytes(1, pr.n, pr.k)
     return b + metrics.gemv_bytes(1, model.vocab, model.hidden)
@@ -410,7 +418,7 @@ def run_gb300(args, world, rank, local):
     lib.load()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    model = synth.dense_2048()
+    model = DENSE_WORKLOADS[args.workload]()
     dp = DecodePass(model, dev, seed=0, merge=not args.separate)
     launches = dp.launches()
     stream = torch.cuda.Stream(device=dev)
@@ -487,12 +495,16 @@ def run_gb300(args, world, rank, local):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        t, nb = oracle_sample(dp, [p.name for p in model.projs], 4096)
+        # a bounded sample: every projection of layer 0 for the small model,
+        # the two smallest for the large one
+        small = sorted(model.projs, key=lambda pr: pr.n * pr.k)
+        names = [p.name for p in (model.projs if model.hidden <= 2048 else small[:2])]
+        t, nb = oracle_sample(dp, names, 4096)
         per_token = t * step_bytes / nb
         cpu = {"value": 1.0 / per_token, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-               "sample": "layer 0 (all 7 projections, full) + 4096 of 262144 lm_head rows + both "
-                         "row gathers, fp64 NumPy oracle; scaled to the whole pass by algorithmic "
-                         "bytes; NumPy may use BLAS threads on the listed cores"}
+               "sample": f"layer 0 ({', '.join(names)}, full) + 4096 of {model.vocab} lm_head "
+                         "rows + the row gathers, fp64 NumPy oracle; scaled to the whole pass by "
+                         "algorithmic bytes; NumPy may use BLAS threads on the listed cores"}
 
     line = {
         "metric": METRIC, "value": tok_s, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -500,13 +512,16 @@ def run_gb300(args, world, rank, local):
         "scaling": "weak", "vs_baseline": None,
         "dtype": "w4a16: f16 products, f32 accumulate",
         "data": "synthetic",
-        "config": {"workload": model.name + " decode pass, batch 1 (gathers, 35 layers of "
-                               "q/k/v/o/gate/up/down GEMVs, 262144x2048 lm_head)",
-                   "projections": "separate (245 GEMVs)" if args.separate else
-                   "merged: q/k/v and gate/up row-concatenated (140 GEMVs)",
+        "config": {"workload": f"{model.name} decode pass, batch 1 (gathers, {model.layers} "
+                               f"layers of q/k/v/o/gate/up/down GEMVs, {model.vocab}x"
+                               f"{model.hidden} lm_head)",
+                   "projections": f"separate ({len(model.projs) * model.layers} GEMVs)"
+                   if args.separate else
+                   f"merged: q/k/v and gate/up row-concatenated ({len(dp.mats)} GEMVs)",
                    "global_batch": world, "parallelism": f"replicas x{world}",
                    "bytes_per_step": step_bytes,
-                   "l2": "inputs larger than L2 (1.50 GB of weights per step, 129 MB L2)"},
+                   "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB of weights per step, "
+                         "129 MB L2)"},
         "hbm_gbs": metrics.gbps(step_bytes, ms * 1e-3),
         "frac_of_nominal_8tbps": metrics.gbps(step_bytes, ms * 1e-3) / NOMINAL_HBM_GBPS,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
@@ -522,6 +537,153 @@ def run_gb300(args, world, rank, local):
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": n_launch * args.steps,
         "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_moe(args, world, rank, local):
+    """Routed-expert decode (30 layers, 128 experts, top-8, 32-slot LFU pool per
+    layer): per step and layer, remap the step's experts to pool slots (host),
+    copy the missed experts into the pool and write the slot ids (device),
+    then w4a16_gemv_id for the merged gate/up (x broadcast) and for down (one
+    x row per expert), addressing the pool."""
+    from bit_weight_only_gemv_gb300 import lib
+    lib.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = synth.moe_2816()
+    E, S, H, I, k_top, L = (cfg.experts, cfg.slots, cfg.hidden, cfg.expert_inter, cfg.top_k,
+                            cfg.layers)
+    steps, warm = args.steps, args.warmup
+    total = warm + steps
+    shapes = {"gate_up": (2 * I, H), "down": (H, I)}
+    layers = []
+    for li in range(L):
+        lay = {"trace": synth.moe_trace(E, k_top, total, cfg.zipf_s, cfg.repeat_p,
+                                        seed=synth.seed_of(42, li)),
+               "x": {"gate_up": synth.torch_x((1, H), synth.seed_of(43, li), dev),
+                     "down": synth.torch_x((k_top, I), synth.seed_of(44, li), dev)},
+               "slot_ids": torch.zeros(k_top, dtype=torch.int32, device=dev)}
+        for name, (n, k) in shapes.items():
+            qs, ss = n * k // 2, n * k // 16          # bytes per expert
+            lay[name] = {
+                "n": n, "k": k, "qs": qs, "ss": ss,
+                "full_q": synth.torch_words((E, qs // 4), synth.seed_of(40, li, n), dev),
+                "full_s": synth.torch_steps((E, ss // 2), synth.seed_of(41, li, n), dev),
+                "pool_q": torch.zeros((S, qs // 4), dtype=torch.int32, device=dev),
+                "pool_s": torch.zeros((S, ss // 2), dtype=torch.bfloat16, device=dev),
+                "y": torch.empty((k_top, n), dtype=torch.bfloat16, device=dev),
+                "y_full": torch.empty((k_top, n), dtype=torch.bfloat16, device=dev)}
+        layers.append(lay)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def new_pools():
+        for lay in layers:
+            for name in shapes:
+                lay[name]["pool"] = lib.SlotPool(E, S)
+
+    def stage(lay, t):
+        copied = 0
+        for name in shapes:
+            d = lay[name]
+            _, nm = d["pool"].stage(lay["trace"][t], d["pool_q"], d["full_q"], d["qs"], d["qs"],
+                                    d["pool_s"], d["full_s"], d["ss"], d["ss"], lay["slot_ids"],
+                                    stream=stream)
+            copied += nm * (d["qs"] + d["ss"])
+        return copied
+
+    def gemvs(lay, ids=None, full=False):
+        for name in shapes:
+            d = lay[name]
+            lib.gemv_id(d["full_q"] if full else d["pool_q"], d["full_s"] if full else d["pool_s"],
+                        lay["slot_ids"] if ids is None else ids, lay["x"][name], d["n"], d["k"],
+                        E if full else S, d["qs"], d["ss"], y=d["y_full"] if full else d["y"],
+                        status=status, stream=stream)
+
+    kernel_bytes = L * sum(metrics.gemv_id_bytes(k_top, 1 if name == "gate_up" else k_top, n, k)
+                           for name, (n, k) in shapes.items())
+
+    # phase A (timed): the routed pass through the pools, eager
+    new_pools()
+    copied = 0
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for t in range(total):
+            if t == warm:
+                torch.cuda.synchronize()
+                e0.record(stream)
+                t_host = time.perf_counter()
+            c = 0
+            for lay in layers:
+                c += stage(lay, t)
+                gemvs(lay)
+            if t >= warm:
+                copied += c
+        e1.record(stream)
+    torch.cuda.synchronize()
+    host_s = time.perf_counter() - t_host
+    ms = e0.elapsed_time(e1) / steps
+    ms = max_over_ranks(ms, dev)
+    lfu = {"requests": 0, "hits": 0, "misses": 0}
+    for lay in layers:
+        st = lay["gate_up"]["pool"].stats()
+        for key in lfu:
+            lfu[key] += st[key]
+
+    # kernel only: the last step's 60 routed GEMVs (pool contents as left), as a graph
+    fns = [(lambda lay: (lambda pdl: gemvs(lay)))(lay) for lay in layers]
+    g = capture(fns, stream, pdl=False)
+    for _ in range(3):
+        g.replay()
+    kms = time_replays(g, stream, max(3, min(steps, 50)))
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+
+    # phase B (check): fresh pools, same traces; every step and layer the pool
+    # call must equal the call on the full 128-expert tensor bit for bit
+    new_pools()
+    bad = torch.zeros((), dtype=torch.int64, device=dev)
+    with torch.cuda.stream(stream):
+        for t in range(total):
+            for lay in layers:
+                stage(lay, t)
+                gemvs(lay)
+                ids_full = torch.from_numpy(lay["trace"][t].astype(np.int32)).to(dev,
+                                                                               non_blocking=True)
+                gemvs(lay, ids=ids_full, full=True)
+                for name in shapes:
+                    d = lay[name]
+                    bad += (d["y"].view(torch.int16) != d["y_full"].view(torch.int16)).sum()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+
+    peak, peak_kind = load_peaks()
+    gbps = metrics.gbps(kernel_bytes, kms * 1e-3)
+    line = {
+        "metric": METRIC, "value": world * 1000.0 / ms, "unit": UNIT, "n_gpus": world,
+        "steps": steps, "warmup": warm, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "w4a16: f16 products, f32 accumulate",
+        "data": "synthetic",
+        "config": {"workload": f"{cfg.name}: routed decode, batch 1, {L} layers, top-{k_top} of "
+                               f"{E} experts (Zipf {cfg.zipf_s}, repeat {cfg.repeat_p}), "
+                               f"{S}-slot LFU pool per layer; per layer merged gate/up "
+                               f"{2 * I}x{H} and down {H}x{I} through w4a16_gemv_id",
+                   "global_batch": world, "parallelism": f"replicas x{world}",
+                   "timed": "eager steps: host LFU remap + pool copies + slot ids + 2 gemv_id "
+                            "per layer (CUDA events)"},
+        "host_seconds_per_step": host_s / steps,
+        "kernel": {"ms_per_step": kms, "tok_s": 1000.0 / kms, "bytes_per_step": kernel_bytes,
+                   "gbps": gbps, "frac": gbps / peak, "peak": peak, "peak_kind": peak_kind,
+                   "note": "the 60 gemv_id launches of one step replayed as a graph"},
+        "pool": dict(lfu, hit_rate=lfu["hits"] / max(1, lfu["requests"]),
+                     copy_bytes_per_step=copied / steps),
+        "bitwise_pool_vs_full": {"steps": total, "layers": L, "mismatched_values": int(bad.item())},
+        "gpu_launches": steps * L * 6,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -564,7 +726,8 @@ def run_shape(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default 200; 128 for the routed-expert workload)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -573,7 +736,12 @@ def main():
     ap.add_argument("--no-pdl", action="store_true", help="with --shape: plain launches")
     ap.add_argument("--separate", action="store_true",
                     help="one GEMV per projection instead of merged q/k/v and gate/up")
+    ap.add_argument("--workload", default="dense-35L-h2048",
+                    choices=sorted(DENSE_WORKLOADS) + ["moe-30L-h2816"],
+                    help="decode pass to time (default: the 35-layer hidden-2048 decoder)")
     args = ap.parse_args()
+    if args.steps is None:
+        args.steps = 128 if args.workload.startswith("moe") else 200
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world, rank, local = dist_env()
@@ -587,6 +755,8 @@ def main():
             return run_reference(args, world, rank)
         if args.shape:
             return run_shape(args)
+        if args.workload.startswith("moe"):
+            return run_moe(args, world, rank, local)
         return run_gb300(args, world, rank, local)
     finally:
         if world > 1 and torch.distributed.is_initialized():
