@@ -703,9 +703,11 @@ def run_shape(args):
     sts = [synth.torch_steps((N, K // 32), synth.seed_of(8, i), dev) for i in range(copies)]
     x = synth.torch_x((M, K), synth.seed_of(9), dev)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    need = lib.workspace_bytes(M, N, K)
+    path = None if args.path == "auto" else args.path
+    need = lib.workspace_bytes(M, N, K, path)
     ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev) if need else None
-    fns = [(lambda q, s_: (lambda pdl: lib.gemv(q, s_, x, y=y, workspace=ws, pdl=pdl)))(q, s_)
+    fns = [(lambda q, s_: (lambda pdl: lib.gemv(q, s_, x, y=y, workspace=ws, pdl=pdl,
+                                                path=path)))(q, s_)
            for q, s_ in zip(qws, sts)]
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
@@ -717,6 +719,7 @@ def run_shape(args):
         g.replay()
     ms = time_replays(g, stream, args.steps) / copies
     print(json.dumps({"mode": "shape", "M": M, "N": N, "K": K, "pdl": not args.no_pdl,
+                      "path": args.path,
                       "us_per_launch": ms * 1e3, "gbps": metrics.gbps(per, ms * 1e-3),
                       "bytes_per_launch": per, "copies": copies, "plan": lib.plan(M, N, K)}),
           flush=True)
@@ -734,6 +737,8 @@ def main():
     ap.add_argument("--shape", default=None,
                     help="M,N,K: time one GEMV shape alone instead of the decode pass")
     ap.add_argument("--no-pdl", action="store_true", help="with --shape: plain launches")
+    ap.add_argument("--path", choices=("auto", "cuda", "tensor"), default="auto",
+                    help="with --shape: the library's choice, CUDA cores or tensor cores")
     ap.add_argument("--separate", action="store_true",
                     help="one GEMV per projection instead of merged q/k/v and gate/up")
     ap.add_argument("--workload", default="dense-35L-h2048",

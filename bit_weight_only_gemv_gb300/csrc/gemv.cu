@@ -51,6 +51,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "gemv_tc.h"
 
 namespace w4 {
 
@@ -1172,6 +1173,56 @@ int max_rows_per_launch(int K, const DeviceInfo& di) {
   return mr;
 }
 
+// Batches of at least this many activation rows use the tensor-core path
+// (when K is a multiple of 256): below it the CUDA-core kernel is faster.
+constexpr int kTcMinM = 8;
+constexpr unsigned kPathFlags = W4_FLAG_CUDA_CORES | W4_FLAG_TENSOR_CORES;
+
+bool tc_shape(int K) { return K >= 256 && K % 256 == 0; }
+
+// 1: tensor-core path, 0: CUDA-core path, -1: the flags ask for a path that
+// cannot run this shape (or for both paths).
+int path_of(int M, int K, unsigned flags) {
+  if ((flags & kPathFlags) == kPathFlags) return -1;
+  if (flags & W4_FLAG_CUDA_CORES) return 0;
+  if (flags & W4_FLAG_TENSOR_CORES) return tc_shape(K) ? 1 : -1;
+  return (M >= kTcMinM && tc_shape(K)) ? 1 : 0;
+}
+
+// Largest workspace of the tensor-core launches of an (M, N, K) call.
+size_t tc_workspace(int M, int N, int K, int sms) {
+  size_t ws = 0;
+  for (int m0 = 0; m0 < M; m0 += tc::kTcMaxM) {
+    tc::TcPlan tp;
+    if (tc::tc_plan(std::min(tc::kTcMaxM, M - m0), N, K, sms, &tp)) ws = std::max(ws, tp.ws_bytes);
+  }
+  return ws;
+}
+
+// Enqueue the tensor-core launches of a call (up to 32 activation rows each).
+w4_status tc_enqueue(void* y, const void* qw, const void* st, const void* x, int M, int N, int K,
+                     void* workspace, size_t workspace_bytes, int32_t* status_dev, bool pdl,
+                     cudaStream_t s, int dev, int sms) {
+  for (int m0 = 0; m0 < M; m0 += tc::kTcMaxM) {
+    const int mr = std::min(tc::kTcMaxM, M - m0);
+    tc::TcPlan tp;
+    if (!tc::tc_plan(mr, N, K, sms, &tp)) return W4_ERR_SHAPE;
+    if (tp.ws_bytes > 0 && (workspace == nullptr || workspace_bytes < tp.ws_bytes))
+      return W4_ERR_WORKSPACE;
+    if (tp.ws_bytes > 0 && !aligned(workspace, 16)) return W4_ERR_ALIGN;
+    const cudaError_t e =
+        tc::tc_launch(tp, static_cast<__nv_bfloat16*>(y) + (long long)m0 * N, qw, st,
+                      static_cast<const __nv_bfloat16*>(x) + (long long)m0 * K, mr, N, K, workspace,
+                      status_dev, pdl, s, dev);
+    if (e != cudaSuccess) {
+      note_cuda_error(e);
+      cudaGetLastError();
+      return W4_ERR_LAUNCH;
+    }
+  }
+  return W4_OK;
+}
+
 }  // namespace
 }  // namespace w4
 
@@ -1183,6 +1234,27 @@ extern "C" w4_status w4a16_gemv_plan(int M, int N, int K, w4_plan_info* info) {
   if (M > W4_MAX_M || K < 32 || K % 32 != 0 || K > W4_MAX_K) return W4_ERR_SHAPE;
   DeviceInfo di;
   planning_device(&di);
+  if (path_of(M, K, 0) == 1) {
+    tc::TcPlan tp;
+    if (!tc::tc_plan(std::min(M, tc::kTcMaxM), N, K, di.sms, &tp)) return W4_ERR_SHAPE;
+    *info = w4_plan_info{};
+    info->path = 2;
+    info->ctas = tp.ctas;
+    info->slices = tp.S;
+    info->threads = 160;
+    info->team = 1;
+    info->unit_rows = 128;
+    info->chunk_groups = 8;
+    info->rows_per_lane = 1;
+    info->smem_bytes = tp.smem;
+    info->rows_per_call = std::min(M, tc::kTcMaxM);
+    info->chunk_steps = 8;
+    info->stages = tp.nst;
+    info->ctas_per_sm = 2;
+    info->tmpl_team = tp.np;
+    info->tmpl_chunk = 0;
+    return W4_OK;
+  }
   Plan pl;
   const int mr_cap = max_rows_per_launch(K, di);
   if (mr_cap < 1 || !cached_plan(std::min(M, mr_cap), N, K, 1, 1, 0, di, &pl)) return W4_ERR_SHAPE;
@@ -1204,10 +1276,13 @@ extern "C" w4_status w4a16_gemv_plan(int M, int N, int K, w4_plan_info* info) {
   return W4_OK;
 }
 
-extern "C" size_t w4a16_gemv_workspace_bytes(int M, int N, int K) {
+extern "C" size_t w4a16_gemv_workspace_bytes_flags(int M, int N, int K, unsigned flags) {
   if (M < 1 || N < 1 || M > W4_MAX_M || K < 32 || K % 32 != 0 || K > W4_MAX_K) return 0;
+  const int path = path_of(M, K, flags);
+  if (path < 0) return 0;
   DeviceInfo di;
   planning_device(&di);
+  if (path == 1) return tc_workspace(M, N, K, di.sms);
   Plan pl;
   const int mr_cap = max_rows_per_launch(K, di);
   if (mr_cap < 1 || !cached_plan(std::min(M, mr_cap), N, K, 1, 1, 0, di, &pl)) return 0;
@@ -1219,18 +1294,28 @@ extern "C" size_t w4a16_gemv_workspace_bytes(int M, int N, int K) {
   return ws;
 }
 
+extern "C" size_t w4a16_gemv_workspace_bytes(int M, int N, int K) {
+  return w4a16_gemv_workspace_bytes_flags(M, N, K, 0);
+}
+
 extern "C" w4_status w4a16_gemv(void* y, const void* qw, const void* st, const void* x, int M,
                                 int N, int K, void* workspace, size_t workspace_bytes,
                                 int32_t* status_dev, unsigned flags, w4_stream_t stream) {
   if (y == nullptr || qw == nullptr || st == nullptr || x == nullptr) return W4_ERR_ARG;
-  if (M < 1 || N < 1 || (flags & ~W4_FLAG_PDL) != 0) return W4_ERR_ARG;
+  if (M < 1 || N < 1 || (flags & ~(W4_FLAG_PDL | kPathFlags)) != 0) return W4_ERR_ARG;
+  if ((flags & kPathFlags) == kPathFlags) return W4_ERR_ARG;
   if (M > W4_MAX_M || K < 32 || K % 32 != 0 || K > W4_MAX_K) return W4_ERR_SHAPE;
   if (!aligned(qw, 16) || !aligned(st, 16) || !aligned(x, 16) || !aligned(y, 2))
     return W4_ERR_ALIGN;
+  const int path = path_of(M, K, flags);
+  if (path < 0) return W4_ERR_SHAPE;
   int dev = 0;
   DeviceInfo di;
   if (!current_device(&dev, &di)) return W4_ERR_DEVICE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (path == 1)
+    return tc_enqueue(y, qw, st, x, M, N, K, workspace, workspace_bytes, status_dev,
+                      (flags & W4_FLAG_PDL) != 0, s, dev, di.sms);
   const int mr_cap = max_rows_per_launch(K, di);
   if (mr_cap < 1) return W4_ERR_SHAPE;
   for (int m0 = 0; m0 < M; m0 += mr_cap) {
@@ -1340,13 +1425,33 @@ extern "C" w4_status w4a16_gemv_static_scratch(void* y, const void* qw, const vo
                                                int32_t* status_dev, unsigned flags,
                                                w4_stream_t stream) {
   if (y == nullptr || qw == nullptr || st == nullptr || x == nullptr) return W4_ERR_ARG;
-  if (M < 1 || N < 1 || (flags & ~W4_FLAG_PDL) != 0) return W4_ERR_ARG;
+  if (M < 1 || N < 1 || (flags & ~(W4_FLAG_PDL | kPathFlags)) != 0) return W4_ERR_ARG;
+  if ((flags & kPathFlags) == kPathFlags) return W4_ERR_ARG;
   if (M > W4_MAX_M || K < 32 || K % 32 != 0 || K > W4_MAX_K) return W4_ERR_SHAPE;
   if (!aligned(qw, 16) || !aligned(st, 16) || !aligned(x, 16) || !aligned(y, 2))
     return W4_ERR_ALIGN;
+  const int path = path_of(M, K, flags);
+  if (path < 0) return W4_ERR_SHAPE;
   int dev = 0;
   DeviceInfo di;
   if (!current_device(&dev, &di)) return W4_ERR_DEVICE;
+  if (path == 1) {
+    // every launch of this call must fit the fixed array: check before any work
+    const size_t need = tc_workspace(M, N, K, di.sms);
+    if (need > (size_t)W4_STATIC_SCRATCH_BYTES) return W4_ERR_WORKSPACE;
+    void* base = nullptr;
+    if (need > 0) {
+      cudaError_t e = static_scratch_address(dev, &base);
+      if (e == cudaSuccess) e = cudaMemsetAsync(base, 0, need, reinterpret_cast<cudaStream_t>(stream));
+      if (e != cudaSuccess) {
+        note_cuda_error(e);
+        cudaGetLastError();
+        return W4_ERR_LAUNCH;
+      }
+    }
+    return tc_enqueue(y, qw, st, x, M, N, K, base, need, status_dev, (flags & W4_FLAG_PDL) != 0,
+                      reinterpret_cast<cudaStream_t>(stream), dev, di.sms);
+  }
   const int mr_cap = max_rows_per_launch(K, di);
   if (mr_cap < 1) return W4_ERR_SHAPE;
   // every launch of this call must fit the fixed array: check before any work

@@ -1,0 +1,729 @@
+// W4A16 group-32 GEMM for small batches on the 5th-generation tensor cores
+// (tcgen05, sm_103a).
+//
+// Page "Gemma 4 on a 4 GB GPU in Plain PyTorch", section "Step 3 — Multiply
+// Straight From the Packed Weights": the weights are multiplied straight from
+// the packed 4-bit words.  With several activation rows (M of 8 to 32) the
+// product is a real dense contraction, and the tensor cores take the dot
+// products while the CUDA cores only unpack codes:
+//
+//  * A CTA owns tiles of 128 weight rows (the MMA's M).  A copy warp streams
+//    each (tile, 256-code K slice) stage into a shared-memory ring: the codes
+//    as one 2-D TMA box with 128-byte swizzle (16 KB), the steps as one 2-D
+//    box (2 KB) and the M activation rows of the slice as 1-D bulk copies.
+//  * Four warps (thread = weight row) turn each packed word into four bf16
+//    pairs (c - 8) with the page's float-bit trick in bf16 form
+//    ((0x4300 | c) - 136 = c - 8, exact) and store them into tensor memory
+//    with tcgen05.st: tensor memory holds the A operand.  The pairs are
+//    codes (i, i + 4) of the word, so the activation slice is permuted the
+//    same way into the B operand (bf16, K-major, 8x8 core matrices) in shared
+//    memory.
+//  * Per group of 32 codes one thread issues two tcgen05.mma (K = 16 each,
+//    N = 16 or 32 activation columns, fp32 accumulate) into a fresh group
+//    accumulator in tensor memory; the four warps read it back (tcgen05.ld)
+//    and add step * dot to the row's running sum in fp32.  Products of bf16
+//    (c - 8) and bf16 activations are exact; only fp32 additions round.
+//  * Association: per row and activation row, groups are added in order
+//    within each 256-code slice and the slice sums in slice order, starting
+//    from 0.  Split-K (K slices over CTAs, for few row tiles) writes slice
+//    sums to the workspace and the last CTA of a tile adds them in the same
+//    order, so the result does not depend on N or on the split.
+//  * Every wait is bounded; on expiry W4_ERR_TIMEOUT is recorded, the warps
+//    leave their loops, in-flight copies and MMAs are waited for (bounded)
+//    and the tensor memory is released before exit.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "gemv_tc.h"
+
+namespace w4 {
+namespace tc {
+
+constexpr int kRows = 128;          // weight rows per tile = MMA M
+constexpr int kSliceK = 256;        // codes per row per stage
+constexpr int kSliceGroups = 8;     // 32-code groups per stage
+constexpr int kDequantWarps = 4;
+constexpr int kThreads = 32 * (kDequantWarps + 2);   // + copy warp + MMA warp
+constexpr int kMaxStages = 4;
+constexpr int kBarBytes = 128;      // full[4], empty[4], aready[2], dready[2], flags, tmem base
+constexpr int kCodesBytes = kRows * 128;   // 16 KB, 1024-byte aligned (128-byte swizzle)
+constexpr int kStepsBytes = kRows * 16;    // 2 KB
+constexpr long long kWaitCycles = 1LL << 31;
+
+struct TcParams {
+  CUtensorMap tm_codes;   // codes viewed as uint8 [N][K/2], box 128 x 128, 128-byte swizzle
+  CUtensorMap tm_steps;   // steps viewed as uint16 [N][K/32], box 8 x 128
+  const __nv_bfloat16* x; // [M][K]
+  __nv_bfloat16* y;       // [M][N]
+  int M, N, K, slices;    // slices = K / 256
+  int tiles, S, sps;      // row tiles, K splits, slices per split
+  int units;              // tiles * S
+  int nst, stage_bytes, off_x, off_b;
+  float* ws_partial;      // [slices][M][N] under split-K
+  int* ws_count;          // [tiles]
+  int32_t* status;
+};
+
+// Bounded wait on an mbarrier phase that also gives up once another warp of
+// the CTA has aborted.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag != 0) return false;
+    if (clock64() - t0 > kWaitCycles) return false;
+  }
+}
+
+// 2-D tiled TMA load of box (x, y) of `tmap` into shared memory at `dst`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tmap, int x, int y,
+                                            uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::"
+      "cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "l"(pol)
+      : "memory");
+}
+
+// bf16 pairs (c - 8) of one packed word, pair order (code 0, 4), (1, 5),
+// (2, 6), (3, 7): (0x4300 | c) is bf16 128 + c, minus 136 gives c - 8.
+__device__ __forceinline__ void unpack_bf16(uint32_t wd, uint32_t out[4]) {
+  const __nv_bfloat162 k136 = __halves2bfloat162(__ushort_as_bfloat16(0x4308), __ushort_as_bfloat16(0x4308));
+  uint32_t t[4];
+  t[0] = and_or(wd, 0x000F000Fu, 0x43004300u);
+  t[1] = and_or(wd >> 4, 0x000F000Fu, 0x43004300u);
+  t[2] = and_or(wd >> 8, 0x000F000Fu, 0x43004300u);
+  t[3] = and_or(wd >> 12, 0x000F000Fu, 0x43004300u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 v = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&t[i]), k136);
+    out[i] = *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t v[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+// tcgen05.ld of C consecutive 32-bit columns of this warp's 32 lanes.
+template <int C>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float* d);
+
+template <>
+__device__ __forceinline__ void tmem_ld<1>(uint32_t taddr, float* d) {
+  uint32_t r;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr) : "memory");
+  d[0] = __uint_as_float(r);
+}
+template <>
+__device__ __forceinline__ void tmem_ld<2>(uint32_t taddr, float* d) {
+  uint32_t r[2];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1]) : "r"(taddr) : "memory");
+  for (int i = 0; i < 2; ++i) d[i] = __uint_as_float(r[i]);
+}
+template <>
+__device__ __forceinline__ void tmem_ld<4>(uint32_t taddr, float* d) {
+  uint32_t r[4];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(taddr) : "memory");
+  for (int i = 0; i < 4; ++i) d[i] = __uint_as_float(r[i]);
+}
+template <>
+__device__ __forceinline__ void tmem_ld<8>(uint32_t taddr, float* d) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+  for (int i = 0; i < 8; ++i) d[i] = __uint_as_float(r[i]);
+}
+template <>
+__device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, float* d) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+  for (int i = 0; i < 16; ++i) d[i] = __uint_as_float(r[i]);
+}
+template <>
+__device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, float* d) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+  for (int i = 0; i < 32; ++i) d[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[128 x NP] (= or +=) A[128 x 16] (tensor memory) . B[16 x NP] (shared).
+__device__ __forceinline__ void mma_f16(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// MMA width (activation columns, 16 or 32) and groups per round for MC
+// columns of results.
+__host__ __device__ constexpr int np_of(int mc) { return mc <= 16 ? 16 : 32; }
+__host__ __device__ constexpr int g_of(int mc) { return np_of(mc) == 16 ? 4 : 2; }
+// Columns of tensor memory the kernel allocates (A and D, double-buffered).
+__host__ __device__ constexpr int tmem_cols(int np, int g) {
+  return 2 * g * (16 + np) <= 128 ? 128 : 256;
+}
+
+// MC: result columns read back (a power of two >= M, <= 32).
+// Warps 0-3 unpack rows and fold results, warp 4 copies, warp 5 issues MMAs.
+template <int MC>
+__global__ void __launch_bounds__(kThreads, 2) tc_kernel(const __grid_constant__ TcParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  constexpr int NP = np_of(MC), G = g_of(MC);
+  constexpr int kCols = tmem_cols(NP, G);
+  constexpr int kACol = 0;                 // A buffers: [2][G][16 columns]
+  constexpr int kDCol = 2 * G * 16;        // D buffers: [2][G][NP columns]
+  constexpr uint32_t kLBO = NP * 16;       // bytes between K-adjacent core matrices of B
+  constexpr int kRounds = kSliceGroups / G;
+  // instruction descriptor: D fp32, A and B bf16, both K-major, N = NP, M = 128
+  constexpr uint32_t kIdesc =
+      (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NP >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t base = smem_addr(smem_raw);
+  const uint32_t full0 = base, empty0 = base + 32, aready0 = base + 64, dready0 = base + 80;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + 96);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(smem_raw + 100);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + 104);
+  // stages start at the first 1024-byte boundary past the barriers
+  const uint32_t st0 = (base + kBarBytes + 1023) & ~1023u;
+  uint8_t* st0_ptr = smem_raw + (st0 - base);
+  const int nst = p.nst;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < nst; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kDequantWarps);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(aready0 + 8 * b, kDequantWarps);
+      mbar_init(dready0 + 8 * b, 1);
+    }
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tmem_slot)),
+                 "n"(kCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  // B operands: activation rows past M stay zero for the whole launch
+  for (int s = 0; s < nst; ++s) {
+    uint4* b = reinterpret_cast<uint4*>(st0_ptr + s * p.stage_bytes + p.off_b);
+    for (int i = threadIdx.x; i < NP * kSliceK * 2 / 16; i += kThreads) b[i] = make_uint4(0, 0, 0, 0);
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_launch_dependents();
+  pdl_wait();   // activations and outputs follow earlier kernels
+
+  const int u0 = (int)((long long)blockIdx.x * p.units / gridDim.x);
+  const int u1 = (int)((long long)(blockIdx.x + 1) * p.units / gridDim.x);
+
+  if (warp == kDequantWarps) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol = policy_evict_first();
+    int slot = 0, issued = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int u = u0; u < u1 && ok; ++u) {
+      const int s = u / p.tiles, t = u - s * p.tiles;
+      const int sl0 = s * p.sps, sl1 = min(sl0 + p.sps, p.slices);
+      for (int sl = sl0; sl < sl1; ++sl) {
+        if (issued >= nst && !wait_bar(empty0 + 8 * slot, phase ^ 1u, abort_flag)) {
+          if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        const uint32_t stg = st0 + slot * p.stage_bytes;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full0 + 8 * slot,
+                                (uint32_t)(kCodesBytes + kStepsBytes + p.M * kSliceK * 2));
+          tma_load_2d(stg, &p.tm_codes, sl * (kSliceK / 2), t * kRows, full0 + 8 * slot, pol);
+          tma_load_2d(stg + kCodesBytes, &p.tm_steps, sl * kSliceGroups, t * kRows,
+                      full0 + 8 * slot, pol);
+        }
+        __syncwarp();
+        if (lane < p.M)
+          bulk_g2s(stg + p.off_x + lane * kSliceK * 2,
+                   p.x + (long long)lane * p.K + (long long)sl * kSliceK, kSliceK * 2,
+                   full0 + 8 * slot);
+        ++issued;
+        if (++slot == nst) {
+          slot = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    // let the last copies land before the CTA may leave
+    const int last = issued < nst ? issued : nst;
+    for (int i = 1; i <= last; ++i) {
+      const int sl = slot - i < 0 ? slot - i + nst : slot - i;
+      const uint32_t ph = slot - i < 0 ? phase ^ 1u : phase;
+      if (!mbar_wait_bounded(full0 + 8 * sl, ph, kWaitCycles)) {
+        report(p.status, W4_ERR_TIMEOUT);
+        break;
+      }
+    }
+  } else if (warp == kDequantWarps + 1) {
+    // ---------------------------------------------------------- MMA issuer
+    // Walks the same rounds as the unpacking warps; a round's MMAs go out once
+    // all four warps have stored its A operands (which also means they have
+    // read back the results of the round that used the same buffers before).
+    int slot = 0, rbuf = 0;
+    uint32_t aphase = 0;                 // bit b: phase of aready[b]
+    int committed = 0;                   // rounds committed so far
+    bool ok = true;
+    for (int u = u0; u < u1 && ok; ++u) {
+      const int s = u / p.tiles;
+      const int sl0 = s * p.sps, sl1 = min(sl0 + p.sps, p.slices);
+      for (int sl = sl0; sl < sl1 && ok; ++sl) {
+        const uint32_t stg = st0 + slot * p.stage_bytes;
+        for (int r = 0; r < kRounds; ++r) {
+          if (!wait_bar(aready0 + 8 * rbuf, (aphase >> rbuf) & 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          aphase ^= 1u << rbuf;
+          tc_fence_after();
+          if (lane == 0) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              const int grp = r * G + g;
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const uint32_t baddr = stg + p.off_b + (uint32_t)(4 * grp + 2 * h) * kLBO;
+                const uint64_t bdesc = (uint64_t)((baddr >> 4) & 0x3FFF) |
+                                       ((uint64_t)((kLBO >> 4) & 0x3FFF) << 16) |
+                                       ((uint64_t)(128 >> 4) << 32) | (1ull << 46);
+                mma_f16(tmem + kDCol + (rbuf * G + g) * NP, tmem + kACol + (rbuf * G + g) * 16 + h * 8,
+                        bdesc, kIdesc, (uint32_t)h);
+              }
+            }
+            mma_commit(dready0 + 8 * rbuf);
+          }
+          __syncwarp();
+          ++committed;
+          rbuf ^= 1;
+        }
+        if (++slot == nst) slot = 0;
+      }
+    }
+    if (!ok) {
+      if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+    // the last commit must land before the tensor memory is released
+    if (committed > 0) {
+      const int lb = rbuf ^ 1;
+      // aready completions of buffer lb so far equal its dready completions
+      mbar_wait_bounded(dready0 + 8 * lb, ((aphase >> lb) & 1u) ^ 1u, kWaitCycles);
+    }
+  } else {
+    // ----------------------------------------------------------- consumers
+    const int tid = threadIdx.x;                       // weight row within the tile
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    int slot = 0;
+    uint32_t phase = 0;
+    uint32_t dphase = 0;                               // bit b: phase of dready[b]
+    int rbuf = 0;                                      // tensor-memory buffer of this round
+    // the previous round, whose dot products are read back in this round
+    bool prev = false, prev_last = false;
+    int prev_buf = 0, prev_slot = 0, prev_sl = 0, prev_row = 0;
+    float prev_st[G];
+    float acc[MC], rowsum[MC];
+    bool ok = true;
+
+    // Read back round `prev`'s group dot products and fold them into acc.
+    // When that round was its slice's last, the slice sum is complete: it
+    // goes to the row sum (or to the workspace under split-K) and the stage
+    // goes back to the copy warp.
+    auto epilogue = [&]() -> bool {
+      if (!wait_bar(dready0 + 8 * prev_buf, (dphase >> prev_buf) & 1u, abort_flag)) return false;
+      dphase ^= 1u << prev_buf;
+      tc_fence_after();
+      float d[G][MC];
+#pragma unroll
+      for (int g = 0; g < G; ++g) tmem_ld<MC>(tmem + lane_base + kDCol + (prev_buf * G + g) * NP, d[g]);
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int m = 0; m < MC; ++m) acc[m] = fmaf(prev_st[g], d[g][m], acc[m]);
+      if (prev_last) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * prev_slot);
+        if (p.S == 1) {
+#pragma unroll
+          for (int m = 0; m < MC; ++m) rowsum[m] += acc[m];
+        } else if (prev_row < p.N) {
+#pragma unroll
+          for (int m = 0; m < MC; ++m)
+            if (m < p.M) p.ws_partial[((long long)prev_sl * p.M + m) * p.N + prev_row] = acc[m];
+        }
+#pragma unroll
+        for (int m = 0; m < MC; ++m) acc[m] = 0.0f;
+      }
+      return true;
+    };
+
+    for (int u = u0; u < u1 && ok; ++u) {
+      const int s = u / p.tiles, t = u - s * p.tiles;
+      const int sl0 = s * p.sps, sl1 = min(sl0 + p.sps, p.slices);
+      const int row = t * kRows + tid;
+#pragma unroll
+      for (int m = 0; m < MC; ++m) {
+        rowsum[m] = 0.0f;
+        acc[m] = 0.0f;
+      }
+      for (int sl = sl0; sl < sl1 && ok; ++sl) {
+        if (!wait_bar(full0 + 8 * slot, phase, abort_flag)) {
+          ok = false;
+          break;
+        }
+        uint8_t* stg_ptr = st0_ptr + slot * p.stage_bytes;
+        // activations of the slice -> B operand, each 8-code block in the
+        // unpacked pair order (0, 4, 1, 5, 2, 6, 3, 7); blocks dealt over all
+        // four warps
+        for (int q = lane * kDequantWarps + warp; q < p.M * (kSliceK / 8); q += kRows) {
+          const int m = q / (kSliceK / 8), kb = q - m * (kSliceK / 8);
+          const uint4 v = *reinterpret_cast<const uint4*>(stg_ptr + p.off_x + m * kSliceK * 2 + kb * 16);
+          uint4 o;
+          o.x = prmt(v.x, v.z, 0x5410);
+          o.y = prmt(v.x, v.z, 0x7632);
+          o.z = prmt(v.y, v.w, 0x5410);
+          o.w = prmt(v.y, v.w, 0x7632);
+          *reinterpret_cast<uint4*>(stg_ptr + p.off_b + kb * kLBO + (m >> 3) * 128 + (m & 7) * 16) = o;
+        }
+        fence_proxy_async_smem();
+        for (int r0 = 0; r0 < kSliceGroups; r0 += G) {
+          // unpack this round's groups into tensor memory
+          float st[G];
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const int grp = r0 + g;
+            const uint4 q = *reinterpret_cast<const uint4*>(stg_ptr + tid * 128 + ((grp ^ (tid & 7)) << 4));
+            st[g] = bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(stg_ptr + kCodesBytes + tid * 16 + grp * 2));
+            uint32_t a[16];
+            unpack_bf16(q.x, a);
+            unpack_bf16(q.y, a + 4);
+            unpack_bf16(q.z, a + 8);
+            unpack_bf16(q.w, a + 12);
+            tmem_st16(tmem + lane_base + kACol + (rbuf * G + g) * 16, a);
+          }
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(aready0 + 8 * rbuf);   // this warp's rows are in
+          if (prev && !(ok = epilogue())) break;
+          prev = true;
+          prev_buf = rbuf;
+          prev_slot = slot;
+          prev_sl = sl;
+          prev_row = row;
+          prev_last = r0 + G >= kSliceGroups;
+#pragma unroll
+          for (int g = 0; g < G; ++g) prev_st[g] = st[g];
+          rbuf ^= 1;
+        }
+        if (!ok) break;
+        if (++slot == nst) {
+          slot = 0;
+          phase ^= 1u;
+        }
+      }
+      // the unit's last round is read back before its rows are finished
+      if (ok && prev) {
+        ok = epilogue();
+        prev = false;
+      }
+      if (!ok) break;
+      if (p.S == 1) {
+        if (row < p.N) {
+#pragma unroll
+          for (int m = 0; m < MC; ++m)
+            if (m < p.M) p.y[(long long)m * p.N + row] = __float2bfloat16_rn(rowsum[m]);
+        }
+        continue;
+      }
+      // Split-K: the last CTA to finish this tile adds the slice sums in
+      // slice order.  The barrier orders the partial stores of all rows
+      // before thread 0's release; its acquire, then the second barrier,
+      // order the other CTAs' partials before they are read.
+      asm volatile("bar.sync 1, %0;" ::"n"(kRows) : "memory");
+      if (tid == 0) *last_flag = atomic_add_acq_rel_gpu(p.ws_count + t, 1) == p.S - 1;
+      asm volatile("bar.sync 1, %0;" ::"n"(kRows) : "memory");
+      if (*last_flag) {
+        if (row < p.N) {
+          // slice by slice, all activation rows' partials in flight at once
+#pragma unroll
+          for (int m = 0; m < MC; ++m) rowsum[m] = 0.0f;
+          for (int sl = 0; sl < p.slices; ++sl) {
+            float v[MC];
+#pragma unroll
+            for (int m = 0; m < MC; ++m)
+              v[m] = m < p.M ? __ldcg(p.ws_partial + ((long long)sl * p.M + m) * p.N + row) : 0.0f;
+#pragma unroll
+            for (int m = 0; m < MC; ++m) rowsum[m] += v[m];
+          }
+#pragma unroll
+          for (int m = 0; m < MC; ++m)
+            if (m < p.M) p.y[(long long)m * p.N + row] = __float2bfloat16_rn(rowsum[m]);
+        }
+        if (tid == 0) atomicExch(p.ws_count + t, 0);
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(kRows) : "memory");
+    }
+    if (!ok) {
+      if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kCols)
+                 : "memory");
+}
+
+// ================================================================= host side
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static std::mutex mu;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!tried) {
+    tried = true;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    else
+      cudaGetLastError();
+  }
+  return fn;
+}
+
+int stage_bytes_of(int M, int np, int* off_x, int* off_b) {
+  *off_x = kCodesBytes + kStepsBytes;
+  *off_b = (*off_x + M * kSliceK * 2 + 127) & ~127;
+  return (*off_b + np * kSliceK * 2 + 1023) & ~1023;
+}
+
+struct DevInfo {
+  int sms = 0, smem_optin = 0;
+};
+
+DevInfo dev_info(int dev) {
+  static std::mutex mu;
+  static DevInfo cache[64];
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 0 || dev >= 64) return DevInfo{};
+  if (cache[dev].sms == 0) {
+    int sms = 0, optin = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess) {
+      cudaGetLastError();
+      return DevInfo{};
+    }
+    cache[dev].sms = sms;
+    cache[dev].smem_optin = optin;
+  }
+  return cache[dev];
+}
+
+using TcFn = void (*)(TcParams);
+
+int mc_of(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : M <= 16 ? 16 : 32; }
+
+TcFn kernel_of(int mc) {
+  switch (mc) {
+    case 1: return tc_kernel<1>;
+    case 2: return tc_kernel<2>;
+    case 4: return tc_kernel<4>;
+    case 8: return tc_kernel<8>;
+    case 16: return tc_kernel<16>;
+    default: return tc_kernel<32>;
+  }
+}
+
+cudaError_t allow_smem(TcFn fn, int smem, int dev) {
+  static std::mutex mu;
+  static int done[64][6] = {};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int k = 0;
+  while (k < 5 && fn != kernel_of(1 << k)) ++k;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev][k] >= smem) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess) done[dev][k] = smem;
+  return e;
+}
+
+}  // namespace
+
+bool tc_supported(int M, int K) {
+  return M >= 1 && M <= kTcMaxM && K >= kSliceK && K % kSliceK == 0 && encoder() != nullptr;
+}
+
+bool tc_plan(int M, int N, int K, int sms, TcPlan* out) {
+  if (M < 1 || M > kTcMaxM || K % kSliceK != 0 || N < 1) return false;
+  TcPlan pl;
+  pl.np = M <= 16 ? 16 : 32;
+  pl.slices = K / kSliceK;
+  pl.tiles = (N + kRows - 1) / kRows;
+  const int target = 2 * std::max(1, sms);
+  // K splits: as many as still give every CTA at most one unit
+  int S = 1;
+  if (pl.tiles < target) S = std::max(1, std::min(pl.slices, target / pl.tiles));
+  pl.sps = (pl.slices + S - 1) / S;
+  pl.S = (pl.slices + pl.sps - 1) / pl.sps;
+  pl.units = pl.tiles * pl.S;
+  pl.ctas = std::min(pl.units, target);
+  int off_x, off_b;
+  pl.stage_bytes = stage_bytes_of(M, pl.np, &off_x, &off_b);
+  pl.off_x = off_x;
+  pl.off_b = off_b;
+  // two CTAs per SM: each keeps under half of the 228 KB of shared memory
+  const int budget = 232448 / 2 - 1024;
+  pl.nst = std::min(kMaxStages, (budget - kBarBytes - 1024) / pl.stage_bytes);
+  if (pl.nst < 2) return false;
+  pl.smem = kBarBytes + 1024 + pl.nst * pl.stage_bytes;
+  if (pl.S > 1) {
+    pl.ws_part_off = ((size_t)pl.tiles * sizeof(int) + 255) & ~size_t(255);
+    pl.ws_bytes = pl.ws_part_off + (size_t)pl.slices * M * N * sizeof(float);
+  }
+  *out = pl;
+  return true;
+}
+
+cudaError_t tc_launch(const TcPlan& pl, void* y, const void* qw, const void* st, const void* x, int M,
+                      int N, int K, void* workspace, int32_t* status, bool pdl, cudaStream_t stream,
+                      int dev) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  TcParams p = {};
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)K / 2, (cuuint64_t)N};
+    const cuuint64_t strides[1] = {(cuuint64_t)K / 2};
+    const cuuint32_t box[2] = {128, kRows};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(&p.tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(qw), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)K / 32, (cuuint64_t)N};
+    const cuuint64_t strides[1] = {(cuuint64_t)K / 32 * 2};
+    const cuuint32_t box[2] = {kSliceGroups, kRows};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(&p.tm_steps, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(st), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  p.x = static_cast<const __nv_bfloat16*>(x);
+  p.y = static_cast<__nv_bfloat16*>(y);
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.slices = pl.slices;
+  p.tiles = pl.tiles;
+  p.S = pl.S;
+  p.sps = pl.sps;
+  p.units = pl.units;
+  p.nst = pl.nst;
+  p.stage_bytes = pl.stage_bytes;
+  p.off_x = pl.off_x;
+  p.off_b = pl.off_b;
+  p.status = status;
+  if (pl.S > 1) {
+    p.ws_count = static_cast<int*>(workspace);
+    p.ws_partial = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.ws_part_off);
+  }
+  const TcFn fn = kernel_of(mc_of(M));
+  const cudaError_t ea = allow_smem(fn, pl.smem, dev);
+  if (ea != cudaSuccess) return ea;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)pl.ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)pl.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, fn, p);
+}
+
+int tc_sms(int dev) { return dev_info(dev).sms; }
+
+}  // namespace tc
+}  // namespace w4

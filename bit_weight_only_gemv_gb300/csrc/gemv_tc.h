@@ -1,0 +1,35 @@
+// Host interface of the tensor-core (tcgen05) small-batch W4A16 path, used by
+// the w4a16_gemv entry in gemv.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace w4 {
+namespace tc {
+
+constexpr int kTcMaxM = 32;   // activation rows per launch
+
+struct TcPlan {
+  int np = 16;                // MMA N (activation columns, >= M)
+  int slices = 0, tiles = 0;  // 256-code K slices, 128-row tiles
+  int S = 1, sps = 1, units = 0, ctas = 0;
+  int nst = 2, stage_bytes = 0, off_x = 0, off_b = 0, smem = 0;
+  size_t ws_bytes = 0, ws_part_off = 0;
+};
+
+// True when the tensor-core path can run M activation rows with reduction K
+// (K a multiple of 256, M <= kTcMaxM, tensor-map encoder available).
+bool tc_supported(int M, int K);
+
+bool tc_plan(int M, int N, int K, int sms, TcPlan* out);
+
+cudaError_t tc_launch(const TcPlan& pl, void* y, const void* qw, const void* st, const void* x,
+                      int M, int N, int K, void* workspace, int32_t* status, bool pdl,
+                      cudaStream_t stream, int dev);
+
+int tc_sms(int dev);
+
+}  // namespace tc
+}  // namespace w4

@@ -17,12 +17,15 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libw4a16.so")
 
 W4_FLAG_PDL = 1
+W4_FLAG_CUDA_CORES = 2
+W4_FLAG_TENSOR_CORES = 4
+_PATH_FLAGS = {None: 0, "cuda": W4_FLAG_CUDA_CORES, "tensor": W4_FLAG_TENSOR_CORES}
 STATUS = {0: "W4_OK", 1: "W4_ERR_ARG", 2: "W4_ERR_ALIGN", 3: "W4_ERR_SHAPE",
           4: "W4_ERR_WORKSPACE", 5: "W4_ERR_LAUNCH", 6: "W4_ERR_INDEX", 7: "W4_ERR_VALUE",
           8: "W4_ERR_TIMEOUT", 9: "W4_ERR_DEVICE", 10: "W4_ERR_STATE"}
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 
-EXPORTS = ("w4_status_str", "w4_abi_version", "w4_last_cuda_error", "w4a16_gemv", "w4a16_gemv_workspace_bytes",
+EXPORTS = ("w4_status_str", "w4_abi_version", "w4_last_cuda_error", "w4a16_gemv", "w4a16_gemv_workspace_bytes", "w4a16_gemv_workspace_bytes_flags",
            "w4a16_gemv_id", "w4_embed_gather", "w4_pack", "w4_quantize",
            "w4_slot_pool_create", "w4_slot_pool_destroy", "w4_slot_pool_remap",
            "w4_slot_pool_stage", "w4_slot_pool_stats", "w4a16_gemv_plan",
@@ -68,6 +71,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.w4a16_gemv_static_scratch.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, u32, vp]
     lib.w4a16_gemv_workspace_bytes.restype = sz
     lib.w4a16_gemv_workspace_bytes.argtypes = [i32, i32, i32]
+    lib.w4a16_gemv_workspace_bytes_flags.restype = sz
+    lib.w4a16_gemv_workspace_bytes_flags.argtypes = [i32, i32, i32, ctypes.c_uint]
     lib.w4a16_gemv_id.restype = i32
     lib.w4a16_gemv_id.argtypes = [vp, vp, sz, vp, sz, i32, vp, i32, vp, i32, i32, i32, vp, u32, vp]
     lib.w4_embed_gather.restype = i32
@@ -126,8 +131,11 @@ def _as_words(qw: torch.Tensor) -> torch.Tensor:
 
 
 # ------------------------------------------------------------------ calls
-def workspace_bytes(M: int, N: int, K: int) -> int:
-    return int(load().w4a16_gemv_workspace_bytes(M, N, K))
+def workspace_bytes(M: int, N: int, K: int, path: str = None) -> int:
+    """Zero-filled scratch a gemv call of this shape (and path choice) needs."""
+    if path is None:
+        return int(load().w4a16_gemv_workspace_bytes(M, N, K))
+    return int(load().w4a16_gemv_workspace_bytes_flags(M, N, K, _PATH_FLAGS[path]))
 
 
 def plan(M: int, N: int, K: int) -> dict:
@@ -138,8 +146,11 @@ def plan(M: int, N: int, K: int) -> dict:
 
 def gemv(qw: torch.Tensor, st: torch.Tensor, x: torch.Tensor, y: torch.Tensor = None,
          workspace: torch.Tensor = None, status: torch.Tensor = None, pdl: bool = False,
-         stream=None) -> torch.Tensor:
-    """y[M, N] = x[M, K] @ W^T with W from (qw [N, K/8], st [N, K/32])."""
+         stream=None, path: str = None) -> torch.Tensor:
+    """y[M, N] = x[M, K] @ W^T with W from (qw [N, K/8], st [N, K/32]).
+
+    path: None (the library's choice), "cuda" (CUDA cores) or "tensor"
+    (tcgen05 tensor cores; K a multiple of 256)."""
     qw = _as_words(qw)
     _need(qw, qw.dtype, "qw")
     _need(st, torch.bfloat16, "st")
@@ -152,12 +163,13 @@ def gemv(qw: torch.Tensor, st: torch.Tensor, x: torch.Tensor, y: torch.Tensor = 
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     _need(y, torch.bfloat16, "y")
-    need = workspace_bytes(M, N, K)
+    need = workspace_bytes(M, N, K, path)
     if need and workspace is None:
         raise ValueError(f"this shape needs a zero-filled workspace of {need} bytes")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().w4a16_gemv(_ptr(y), _ptr(qw), _ptr(st), _ptr(x2), M, N, K, _ptr(workspace),
-                             ws_bytes, _ptr(status), W4_FLAG_PDL if pdl else 0, _stream(stream)),
+                             ws_bytes, _ptr(status), (W4_FLAG_PDL if pdl else 0) | _PATH_FLAGS[path],
+                             _stream(stream)),
            "w4a16_gemv")
     return y
 

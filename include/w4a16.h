@@ -37,10 +37,19 @@
  *     ids and before writing any output.  Use it only when nothing still
  *     running earlier in the stream writes qw / st.
  *   - Results are deterministic: the same inputs give the same bits on every
- *     call, and the arithmetic of an output row depends only on K, that row's
- *     codes and steps and its activation row (not on N, M, the row index, the
- *     number of ids or the addresses), so w4a16_gemv_id row i is bitwise
- *     equal to w4a16_gemv on expert ids[i] with the same activation row.
+ *     call, and the arithmetic of an output row depends only on K, on the
+ *     path that computes it, on that row's codes and steps and on its
+ *     activation row (not on N, the row index, the number of ids or the
+ *     addresses), so w4a16_gemv_id row i is bitwise equal to w4a16_gemv on
+ *     expert ids[i] with the same activation row.
+ *   - Two paths compute w4a16_gemv.  The CUDA-core path (every w4a16_gemv_id
+ *     call, and w4a16_gemv with fewer than 8 activation rows) dequantises in
+ *     packed fp16 with fp16 partial sums of 4 products; its rows do not
+ *     depend on M.  The tensor-core path (w4a16_gemv with 8 or more rows and
+ *     K a multiple of 256) lets tcgen05 MMAs take exact bf16 products with
+ *     fp32 sums; its rows do not depend on M either, but differ from the
+ *     CUDA-core path's in the last bits.  W4_FLAG_CUDA_CORES or
+ *     W4_FLAG_TENSOR_CORES pins the path.
  */
 #ifndef W4A16_H
 #define W4A16_H
@@ -74,6 +83,8 @@ typedef enum w4_status {
 } w4_status;
 
 #define W4_FLAG_PDL 1u
+#define W4_FLAG_CUDA_CORES 2u     /* w4a16_gemv: CUDA-core path at any M */
+#define W4_FLAG_TENSOR_CORES 4u   /* w4a16_gemv: tensor-core path at any M (K % 256 == 0) */
 
 #define W4_GROUP 32        /* codes per group along K */
 #define W4_MAX_K 65536     /* largest supported K */
@@ -112,15 +123,21 @@ const char *w4_last_cuda_error(void);
  *            without a device-side error leaves it zero-filled again.  Calls
  *            that may run concurrently need separate workspaces.
  * status_dev device int32 for device-side errors (W4_ERR_TIMEOUT), or NULL.
- * flags      0 or W4_FLAG_PDL.
+ * flags      W4_FLAG_PDL, and at most one of W4_FLAG_CUDA_CORES /
+ *            W4_FLAG_TENSOR_CORES (default: tensor cores from M = 8 when K is
+ *            a multiple of 256; W4_ERR_SHAPE if the pinned path cannot run K).
  * Returns W4_OK once the work is enqueued.
  */
 w4_status w4a16_gemv(void *y, const void *qw, const void *st, const void *x,
                      int M, int N, int K, void *workspace, size_t workspace_bytes,
                      int32_t *status_dev, unsigned flags, w4_stream_t stream);
 
-/* Scratch bytes w4a16_gemv needs for this shape (0 when its plan needs none). */
+/* Scratch bytes w4a16_gemv needs for this shape with flags 0 (0 when its
+ * plan needs none). */
 size_t w4a16_gemv_workspace_bytes(int M, int N, int K);
+
+/* The same for a call with the given flags (path flags change the plan). */
+size_t w4a16_gemv_workspace_bytes_flags(int M, int N, int K, unsigned flags);
 
 /*
  * w4a16_gemv_static_scratch — w4a16_gemv without a caller-provided workspace.

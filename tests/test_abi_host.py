@@ -60,7 +60,9 @@ def test_host_validation_rejects_before_any_launch(L):
     assert L.w4a16_gemv(good, vp((1 << 20) + 8), good, good, 1, 16, 64, None, 0, None, 0,
                         None) == 2
     # unknown flag bit
-    assert L.w4a16_gemv(good, good, good, good, 1, 16, 64, None, 0, None, 4, None) == 1
+    assert L.w4a16_gemv(good, good, good, good, 1, 16, 64, None, 0, None, 8, None) == 1
+    assert L.w4a16_gemv(good, good, good, good, 1, 16, 256, None, 0, None, 6, None) == 1
+    assert L.w4a16_gemv(good, good, good, good, 1, 16, 64, None, 0, None, 4, None) == 3
     # gemv_id: x_rows must be 1 or n_ids, strides multiples of 16 and >= an expert
     assert L.w4a16_gemv_id(good, good, 1024, good, 128, 4, good, 3, good, 2, 32, 64, None, 0,
                            None) == 3
@@ -97,6 +99,21 @@ def test_plan_is_valid(M, N, K):
         assert p["rows_per_call"] == min(M, 4)
     ws = lib.workspace_bytes(M, N, K)
     assert (ws > 0) == (p["slices"] > 1)
+
+
+@pytest.mark.parametrize("M,N,K", [(8, 2048, 2048), (16, 16384, 2048), (32, 2048, 8192),
+                                   (17, 300, 256), (9, 5376, 21504)])
+def test_tensor_core_plan_is_valid(M, N, K):
+    p = lib.plan(M, N, K)
+    assert p["path"] == 2 and p["threads"] == 160 and p["unit_rows"] == 128
+    assert p["tmpl_team"] == (16 if M <= 16 else 32)      # MMA N: activation columns
+    assert p["rows_per_call"] == min(M, 32)
+    assert 2 <= p["stages"] <= 4 and p["smem_bytes"] <= 233472 // 2 - 1024
+    assert 1 <= p["ctas"] <= 2 * 152
+    tiles, slices = -(-N // 128), K // 256
+    assert 1 <= p["slices"] <= slices
+    assert (lib.workspace_bytes(M, N, K) > 0) == (p["slices"] > 1)
+    assert lib.workspace_bytes(M, N, K, "tensor") == lib.workspace_bytes(M, N, K)
 
 
 def test_tiling_depends_on_k_only():
