@@ -60,7 +60,7 @@ constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kThreads = kConsumers + 32;   // + the producer warp
 constexpr int kMaxMR = 4;                   // activation rows per launch
 constexpr int kMaxStages = 8;
-constexpr int kBarBytes = 256;              // full[8], empty[8], abort flag
+constexpr int kBarBytes = 256;              // full[8], empty[8], abort and last flags
 constexpr long long kWaitCycles = 1LL << 31;
 
 struct GemvParams {
@@ -397,7 +397,28 @@ __device__ __forceinline__ float team_sum(float v, int T) {
 constexpr int min_ctas(int mr, int rw) { return (mr * rw <= 4) ? 2 : 1; }
 
 // ---------------------------------------------------------------- kernel
-template <int MR, int RW, int TT, int CLT>
+// End of a window of whole rows with several chunks, after the consumer
+// threads have released its stage: once every warp has stored its chunk sums
+// (CTA barrier), each row's are added in chunk order and the row is written.
+// The chunk sums have a buffer per stage, and a warp can only write a stage's
+// buffer again after every consumer thread has passed the barrier of a later
+// window, i.e. has finished reading this one.
+template <int MR>
+__device__ __forceinline__ void finish_window(const GemvParams& p, const float* redw, int nrows,
+                                              int ncw, __nv_bfloat16* yrow) {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+  for (int i = threadIdx.x; i < nrows * MR; i += kConsumers) {
+    const int r = i / MR, m = i - r * MR;
+    float v = 0.0f;
+    for (int cc = 0; cc < ncw; ++cc) v += redw[(r * p.nch + cc) * MR + m];
+    yrow[(long long)m * p.N + r] = __float2bfloat16_rn(v);
+  }
+}
+
+// DS: a dense call of whole rows (no routed ids, no split-K).  Its CTAs walk
+// their rows in windows of RB rows with every offset fixed for the launch;
+// the other calls take the general walk.
+template <int MR, int RW, int TT, int CLT, bool DS>
 __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
     gemv_kernel(const __grid_constant__ GemvParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -511,20 +532,20 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
   int slot = 0;
   uint32_t phase = 0;
   uint32_t tile = kBarBytes;   // shared offset of the current slot
-  int rbuf = 0;                // chunk-sum buffer of this window
-  bool reported = false;
+  const int red_slot = p.RB * p.nch * MR;   // chunk sums of one stage's window
 
-  // Steady state of a dense call: the CTA's full windows (the copy warp walks
-  // the same ones first), back to back, with every offset but the tile base
-  // and the window's first row fixed for the whole launch.
-  if (dense && p.S == 1) {
-    const long long nfull = (wk.end - wk.pos) / p.RB;
+  if constexpr (DS) {
+    // Windows of RB rows from the CTA's first row (the last one may be
+    // shorter; the copy warp walks the same ones).  Rows of a short window
+    // past its end read stale bytes of the stage (in bounds) and are dropped.
     const int ncw = p.nch;
-    const int items = ncw * nrs_full;
-    int row0 = (int)wk.pos;
-    for (long long w = 0; w < nfull; ++w) {
+    for (long long r0 = wk.pos; r0 < wk.end; r0 += p.RB) {
+      const int row0 = (int)r0;
+      const int nrows = (int)min((long long)p.RB, wk.end - r0);
+      const int nrs = nrows == p.RB ? nrs_full : (nrows + rstep - 1) / rstep;
+      const int items = ncw * nrs;
       const uint32_t soff0 = steps_aligned ? 0u : (uint32_t)(((row0 & 7) * (kg2 & 15)) & 15);
-      float* redw = red + rbuf * p.RB * p.nch * MR;
+      float* redw = red + slot * red_slot;
       if (!wait_phase(full0 + 8 * slot, phase, abort_flag)) {
         if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
         *abort_flag = 1;
@@ -532,15 +553,15 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
       }
       for (int it = warp; it < items; it += kConsumerWarps) {
         int ci, rs;
-        if (nrs_full == 1) {
+        if (nrs == 1) {
           ci = it;
           rs = 0;
         } else if (ncw == 1) {
           ci = 0;
           rs = it;
         } else {
-          ci = it / nrs_full;
-          rs = it - ci * nrs_full;
+          ci = it / nrs;
+          rs = it - ci * nrs;
         }
         const uint32_t ic = tile + (uint32_t)(rs * rstep * p.code_pitch + ci * gpc * 16);
         const uint32_t is = tile + soff0 + (uint32_t)(rs * rstep * kg2 + ci * gpc * 2);
@@ -563,6 +584,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
 #pragma unroll
           for (int j = 0; j < RW; ++j) {
             const int rl = rs * rstep + j * nsw + set;
+            if (rl >= nrows) continue;
             if (ncw == 1) {   // one chunk: the row is done (0 + chunk sum)
 #pragma unroll
               for (int m = 0; m < MR; ++m)
@@ -583,161 +605,149 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
       } else {
         tile += p.tile_bytes;
       }
-      if (ncw > 1) {
-        // chunk sums of each row, added in chunk order
-        asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
-        for (int i = threadIdx.x; i < p.RB * MR; i += kConsumers) {
-          const int r = i / MR, m = i - r * MR;
-          float v = 0.0f;
-          for (int cc = 0; cc < ncw; ++cc) v += redw[(r * p.nch + cc) * MR + m];
-          p.y[(long long)m * p.N + row0 + r] = __float2bfloat16_rn(v);
-        }
-        rbuf ^= 1;
-      }
-      row0 += p.RB;
+      if (ncw > 1) finish_window<MR>(p, redw, nrows, ncw, p.y + row0);
     }
-    wk.pos += nfull * p.RB;   // the generic walk takes the partial window left
-  }
+    return;
+  } else {
+    bool reported = false;
+    while (wk.next(p)) {
+      const uint8_t *qwi, *sti;
+      if (!dense && !item_arrays(p, wk.item, &qwi, &sti)) {
+        if (!reported && lane == 0) report(p.status, W4_ERR_INDEX);
+        reported = true;
+        continue;
+      }
+      const int xslot = p.x_per_item ? wk.item - item0 : 0;
+      const bool whole = p.S == 1;
+      const bool full = wk.nrows == p.RB;
+      // full windows of whole rows whose steps start on 16-byte lines: every
+      // offset below is a lane constant plus a per-item term
+      const bool fast = whole && full && steps_aligned;
+      const int ncw = wk.c1 - wk.c0;                       // chunks in the window
+      const int nrs = full ? nrs_full : (wk.nrows + rstep - 1) / rstep;   // row steps
+      const int items = ncw * nrs;
+      const int soff0 = whole ? (((wk.row0 & 7) * (kg2 & 15)) & 15) : 0;
+      float* redw = red + slot * red_slot;
+      __nv_bfloat16* yrow = p.y + (long long)wk.item * MR * p.N + wk.row0;
+      const uint32_t xo0 = xs_off + (uint32_t)(xslot * MR * 4 * p.Kgp * 16);
+      const uint32_t xso0 = xsc_off + (uint32_t)(xslot * MR * p.Kgp * 4);
 
-  while (wk.next(p)) {
-    const uint8_t *qwi, *sti;
-    if (!dense && !item_arrays(p, wk.item, &qwi, &sti)) {
-      if (!reported && lane == 0) report(p.status, W4_ERR_INDEX);
-      reported = true;
-      continue;
-    }
-    const int xslot = p.x_per_item ? wk.item - item0 : 0;
-    const bool whole = p.S == 1;
-    const bool full = wk.nrows == p.RB;
-    // full windows of whole rows whose steps start on 16-byte lines: every
-    // offset below is a lane constant plus a per-item term
-    const bool fast = whole && full && steps_aligned;
-    const int ncw = wk.c1 - wk.c0;                       // chunks in the window
-    const int nrs = full ? nrs_full : (wk.nrows + rstep - 1) / rstep;   // row steps
-    const int items = ncw * nrs;
-    const int soff0 = whole ? (((wk.row0 & 7) * (kg2 & 15)) & 15) : 0;
-    float* redw = red + (long long)rbuf * p.RB * p.nch * MR;
-    __nv_bfloat16* yrow = p.y + (long long)wk.item * MR * p.N + wk.row0;
-
-    if (!wait_phase(full0 + 8 * slot, phase, abort_flag)) {
-      if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
-      *abort_flag = 1;
-      return;
-    }
-    for (int it = warp; it < items; it += kConsumerWarps) {
-      // item = (chunk ci of the window, row step rs), it = ci * nrs + rs
-      int ci, rs;
-      if (nrs == 1) {
-        ci = it;
-        rs = 0;
-      } else if (ncw == 1) {
-        ci = 0;
-        rs = it;
-      } else {
-        ci = it / nrs;
-        rs = it - ci * nrs;
+      if (!wait_phase(full0 + 8 * slot, phase, abort_flag)) {
+        if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
+        *abort_flag = 1;
+        return;
       }
-      const int c = wk.c0 + ci;
-      uint32_t co[RW], so[RW];
-      int rl[RW];
-      bool rv[RW];
-      if (fast) {
-        const uint32_t ic = tile + (uint32_t)(rs * rstep * p.code_pitch + ci * gpc * 16);
-        const uint32_t is = tile + (uint32_t)(rs * rstep * kg2 + ci * gpc * 2);
-#pragma unroll
-        for (int j = 0; j < RW; ++j) {
-          rv[j] = true;
-          rl[j] = rs * rstep + j * nsw + set;
-          co[j] = ic + lane_c[j];
-          so[j] = is + lane_s[j];
+      for (int it = warp; it < items; it += kConsumerWarps) {
+        // item = (chunk ci of the window, row step rs), it = ci * nrs + rs
+        int ci, rs;
+        if (nrs == 1) {
+          ci = it;
+          rs = 0;
+        } else if (ncw == 1) {
+          ci = 0;
+          rs = it;
+        } else {
+          ci = it / nrs;
+          rs = it - ci * nrs;
         }
-      } else {
+        const int c = wk.c0 + ci;
+        uint32_t co[RW], so[RW];
+        int rl[RW];
+        bool rv[RW];
+        if (fast) {
+          const uint32_t ic = tile + (uint32_t)(rs * rstep * p.code_pitch + ci * gpc * 16);
+          const uint32_t is = tile + (uint32_t)(rs * rstep * kg2 + ci * gpc * 2);
 #pragma unroll
-        for (int j = 0; j < RW; ++j) {
-          // rows past the window read the window's last row (results dropped)
-          const int r = rs * rstep + j * nsw + set;
-          rv[j] = r < wk.nrows;
-          rl[j] = rv[j] ? r : wk.nrows - 1;
-          co[j] = tile + rl[j] * p.code_pitch + (ci * gpc + t) * 16;
-          so[j] = tile + p.step_off + (ci * gpc + t) * 2 +
-                  (whole ? soff0 + rl[j] * kg2
-                         : rl[j] * p.step_pitch +
-                               ((((wk.row0 + rl[j]) & 7) * (kg2 & 15) + wk.c0 * gpc * 2) & 15));
+          for (int j = 0; j < RW; ++j) {
+            rv[j] = true;
+            rl[j] = rs * rstep + j * nsw + set;
+            co[j] = ic + lane_c[j];
+            so[j] = is + lane_s[j];
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < RW; ++j) {
+            // rows past the window read the window's last row (results dropped)
+            const int r = rs * rstep + j * nsw + set;
+            rv[j] = r < wk.nrows;
+            rl[j] = rv[j] ? r : wk.nrows - 1;
+            co[j] = tile + rl[j] * p.code_pitch + (ci * gpc + t) * 16;
+            so[j] = tile + p.step_off + (ci * gpc + t) * 2 +
+                    (whole ? soff0 + rl[j] * kg2
+                           : rl[j] * p.step_pitch +
+                                 ((((wk.row0 + rl[j]) & 7) * (kg2 & 15) + wk.c0 * gpc * 2) & 15));
+          }
         }
-      }
-      const int g0 = c * gpc + t;
-      const uint32_t xo = xs_off + (uint32_t)(((xslot * MR * 4) * p.Kgp + g0) * 16);
-      const uint32_t xso = xsc_off + (uint32_t)(((xslot * MR) * p.Kgp + g0) * 4);
-      const int ns = min(p.CL, p.NI - c * p.CL);
-      float acc[RW][MR];
-      tile_dot<MR, RW, TT, CLT>(smem, xo, xso, xplane, xmrow, xsmrow, co, so, ns, T,
-                                kg_valid - g0, acc);
+        const int g0 = c * gpc + t;
+        const int ns = CLT > 0 ? CLT : min(p.CL, p.NI - c * p.CL);
+        float acc[RW][MR];
+        tile_dot<MR, RW, TT, CLT>(smem, xo0 + (uint32_t)(g0 * 16), xso0 + (uint32_t)(g0 * 4), xplane,
+                                  xmrow, xsmrow, co, so, ns, T, kg_valid - g0, acc);
 #pragma unroll
-      for (int j = 0; j < RW; ++j)
+        for (int j = 0; j < RW; ++j)
 #pragma unroll
-        for (int m = 0; m < MR; ++m) acc[j][m] = team_sum<TT>(acc[j][m], T);
-      if (t == 0) {
+          for (int m = 0; m < MR; ++m) acc[j][m] = team_sum<TT>(acc[j][m], T);
+        if (t == 0) {
 #pragma unroll
-        for (int j = 0; j < RW; ++j) {
-          if (!rv[j]) continue;
-          if (!whole) {          // split-K: chunk sums to the workspace
-            float* dst = p.ws_partial + (((long long)wk.rb * p.nch + c) * p.RB + rl[j]) * MR;
+          for (int j = 0; j < RW; ++j) {
+            if (!rv[j]) continue;
+            if (!whole) {          // split-K: chunk sums to the workspace
+              float* dst = p.ws_partial + (((long long)wk.rb * p.nch + c) * p.RB + rl[j]) * MR;
 #pragma unroll
-            for (int m = 0; m < MR; ++m) dst[m] = acc[j][m];
-          } else if (ncw == 1) { // one chunk: the row is done (0 + chunk sum)
+              for (int m = 0; m < MR; ++m) dst[m] = acc[j][m];
+            } else if (ncw == 1) { // one chunk: the row is done (0 + chunk sum)
 #pragma unroll
-            for (int m = 0; m < MR; ++m)
-              yrow[(long long)m * p.N + rl[j]] = __float2bfloat16_rn(0.0f + acc[j][m]);
-          } else {
+              for (int m = 0; m < MR; ++m)
+                yrow[(long long)m * p.N + rl[j]] = __float2bfloat16_rn(0.0f + acc[j][m]);
+            } else {
 #pragma unroll
-            for (int m = 0; m < MR; ++m) redw[(rl[j] * p.nch + ci) * MR + m] = acc[j][m];
+              for (int m = 0; m < MR; ++m) redw[(rl[j] * p.nch + ci) * MR + m] = acc[j][m];
+            }
           }
         }
       }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8 * slot);   // this warp is done with the stage
-    if (++slot == nst) {
-      slot = 0;
-      phase ^= 1u;
-      tile = kBarBytes;
-    } else {
-      tile += p.tile_bytes;
-    }
+      __syncwarp();
 
-    if (whole) {
-      if (ncw > 1) {
-        // chunk sums of each row, added in chunk order
-        asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+      if (whole) {
+        if (lane == 0) mbar_arrive(empty0 + 8 * slot);   // this warp is done with the stage
+        if (++slot == nst) {
+          slot = 0;
+          phase ^= 1u;
+          tile = kBarBytes;
+        } else {
+          tile += p.tile_bytes;
+        }
+        if (ncw > 1) finish_window<MR>(p, redw, wk.nrows, ncw, yrow);
+        continue;
+      }
+      if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+      if (++slot == nst) {
+        slot = 0;
+        phase ^= 1u;
+        tile = kBarBytes;
+      } else {
+        tile += p.tile_bytes;
+      }
+      // Split-K: the last of the slices to finish this row block adds the chunk
+      // sums in chunk order, writes the rows and re-arms the counter.  The CTA
+      // barrier orders every thread's partial stores before thread 0's counter
+      // update, whose release publishes them at GPU scope; its acquire side,
+      // then the second barrier, order the other slices' partials before this
+      // CTA reads them.
+      asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+      if (threadIdx.x == 0)
+        *last_flag = atomic_add_acq_rel_gpu(p.ws_count + wk.rb, 1) == p.S - 1;
+      asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+      if (*last_flag) {
         for (int i = threadIdx.x; i < wk.nrows * MR; i += kConsumers) {
           const int r = i / MR, m = i - r * MR;
+          const float* src = p.ws_partial + ((long long)wk.rb * p.nch * p.RB + r) * MR + m;
           float v = 0.0f;
-          for (int cc = 0; cc < ncw; ++cc) v += redw[(r * p.nch + cc) * MR + m];
+          for (int cc = 0; cc < p.nch; ++cc) v += __ldcg(src + (long long)cc * p.RB * MR);
           yrow[(long long)m * p.N + r] = __float2bfloat16_rn(v);
         }
-        rbuf ^= 1;
+        if (threadIdx.x == 0) atomicExch(p.ws_count + wk.rb, 0);
       }
-      continue;
-    }
-    // Split-K: the last of the slices to finish this row block adds the chunk
-    // sums in chunk order, writes the rows and re-arms the counter.  The CTA
-    // barrier orders every thread's partial stores before thread 0's counter
-    // update, whose release publishes them at GPU scope; its acquire side,
-    // then the second barrier, order the other slices' partials before this
-    // CTA reads them.
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
-    if (threadIdx.x == 0)
-      *last_flag = atomic_add_acq_rel_gpu(p.ws_count + wk.rb, 1) == p.S - 1;
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
-    if (*last_flag) {
-      for (int i = threadIdx.x; i < wk.nrows * MR; i += kConsumers) {
-        const int r = i / MR, m = i - r * MR;
-        const float* src = p.ws_partial + ((long long)wk.rb * p.nch * p.RB + r) * MR + m;
-        float v = 0.0f;
-        for (int cc = 0; cc < p.nch; ++cc) v += __ldcg(src + (long long)cc * p.RB * MR);
-        yrow[(long long)m * p.N + r] = __float2bfloat16_rn(v);
-      }
-      if (threadIdx.x == 0) atomicExch(p.ws_count + wk.rb, 0);
     }
   }
 }
@@ -780,6 +790,7 @@ DeviceInfo device_info(int dev) {
 }
 
 struct Plan {
+  bool routed = false;   // routed-expert call (ids), never split
   int MR = 1;
   int Kg = 1;
   int T = 32, nsw = 1, NI = 1, CL = 1, nch = 1;
@@ -846,15 +857,17 @@ void tile_geometry(int K, int T, int CL, bool whole, int cps, int rb, int* code_
   *tile_bytes = (int)((*step_off + steps + 127) & ~127LL);
 }
 
-// Chunk sums of a window of whole rows, double-buffered (none for one chunk).
-long long red_bytes(int rb, int nch, int MR) { return nch > 1 ? 2LL * rb * nch * MR * 4 : 0; }
+// Chunk sums of a window of whole rows, one buffer per stage (none for one
+// chunk).
+long long red_bytes(int rb, int nch, int MR) { return nch > 1 ? (long long)rb * nch * MR * 4 : 0; }
 
 using KernelFn = void (*)(GemvParams);
 int occupancy(const struct Plan& pl, int dev);
 
-bool make_plan(int MR, int N, int K, int n_items, int allow_split, int x_per_item,
+bool make_plan(int MR, int N, int K, int n_items, int allow_split, int x_per_item, bool routed,
                const DeviceInfo& di, Plan* out, int force_per_sm = 0) {
   Plan pl;
+  pl.routed = routed;
   pl.MR = MR;
   const int Kg = K / 32;
   pl.Kg = Kg;
@@ -940,9 +953,9 @@ bool make_plan(int MR, int N, int K, int n_items, int allow_split, int x_per_ite
         tile_geometry(K, pl.T, pl.CL, pl.S == 1, pl.cps, rb, &cp, &sp, &so, &tb);
         if (rs > 1 && tb > kTileMax) break;
         const long long rd = pl.S == 1 ? red_bytes(rb, pl.nch, MR) : 0;
-        const long long room = budgets[bi] - kBarBytes - xb - rd;
-        if (room < 2LL * tb) break;
-        const int nst = (int)std::min<long long>(kMaxStages, room / tb);
+        const long long room = budgets[bi] - kBarBytes - xb;
+        if (room < 2LL * (tb + rd)) break;
+        const int nst = (int)std::min<long long>(kMaxStages, room / (tb + rd));
         const long long items = (long long)(pl.S == 1 ? pl.nch : pl.cps) * rs;
         const double util =
             (double)items / (double)(kConsumerWarps * ((items + kConsumerWarps - 1) / kConsumerWarps));
@@ -964,18 +977,18 @@ bool make_plan(int MR, int N, int K, int n_items, int allow_split, int x_per_ite
       }
     }
     if (found && bi == 1 && pl.per_sm > 1)   // only one CTA per SM fits
-      return make_plan(MR, N, K, n_items, allow_split, x_per_item, di, out, 1);
+      return make_plan(MR, N, K, n_items, allow_split, x_per_item, routed, di, out, 1);
   }
   if (!found) return false;
   pl.smem = kBarBytes + (long long)pl.nst * pl.tile_bytes + xb +
-            (pl.S == 1 ? red_bytes(pl.RB, pl.nch, MR) : 0);
+            (pl.S == 1 ? pl.nst * red_bytes(pl.RB, pl.nch, MR) : 0);
   // resident CTAs the device really fits (registers, shared memory); fewer
   // than planned: the same work over fewer CTAs
   if (di.dev >= 0) {
     const int occ = occupancy(pl, di.dev);
     if (occ < 1) return false;
     if (occ < pl.per_sm)
-      return make_plan(MR, N, K, n_items, allow_split, x_per_item, di, out, occ);
+      return make_plan(MR, N, K, n_items, allow_split, x_per_item, routed, di, out, occ);
   }
   if (pl.S > 1) {
     // counters first, partials after them
@@ -996,14 +1009,16 @@ using KernelFn = void (*)(GemvParams);
 KernelFn kernel_for(const Plan& pl, int* tt = nullptr, int* clt = nullptr) {
   if (tt != nullptr) *tt = 0;
   if (clt != nullptr) *clt = 0;
+  const bool ds = !pl.routed && pl.S == 1;
   const bool full = pl.NI % pl.CL == 0 && pl.NI * pl.T == pl.Kg;
   if (pl.MR == 1 && full && pl.RW <= 2) {
     const int key = pl.T * 8 + pl.CL;
-#define W4_SPEC(t, cl)                                                          \
-  if (key == (t) * 8 + (cl)) {                                                  \
-    if (tt != nullptr) *tt = t;                                                 \
-    if (clt != nullptr) *clt = cl;                                              \
-    return pl.RW == 1 ? gemv_kernel<1, 1, t, cl> : gemv_kernel<1, 2, t, cl>;    \
+#define W4_SPEC(t, cl)                                                            \
+  if (key == (t) * 8 + (cl)) {                                                    \
+    if (tt != nullptr) *tt = t;                                                   \
+    if (clt != nullptr) *clt = cl;                                                \
+    if (ds) return pl.RW == 1 ? gemv_kernel<1, 1, t, cl, true> : gemv_kernel<1, 2, t, cl, true>; \
+    return pl.RW == 1 ? gemv_kernel<1, 1, t, cl, false> : gemv_kernel<1, 2, t, cl, false>;       \
   }
     W4_SPEC(16, 4)   // K = 2048
     W4_SPEC(8, 3)    // K = 5376
@@ -1011,16 +1026,18 @@ KernelFn kernel_for(const Plan& pl, int* tt = nullptr, int* clt = nullptr) {
     W4_SPEC(32, 4)   // K = 4096 * n
 #undef W4_SPEC
   }
+#define W4_GEN(mr, rw) (ds ? gemv_kernel<mr, rw, 0, 0, true> : gemv_kernel<mr, rw, 0, 0, false>)
   switch (pl.MR * 8 + pl.RW) {
-    case 8 + 1: return gemv_kernel<1, 1, 0, 0>;
-    case 8 + 2: return gemv_kernel<1, 2, 0, 0>;
-    case 8 + 4: return gemv_kernel<1, 4, 0, 0>;
-    case 16 + 1: return gemv_kernel<2, 1, 0, 0>;
-    case 16 + 2: return gemv_kernel<2, 2, 0, 0>;
-    case 24 + 1: return gemv_kernel<3, 1, 0, 0>;
-    case 32 + 1: return gemv_kernel<4, 1, 0, 0>;
+    case 8 + 1: return W4_GEN(1, 1);
+    case 8 + 2: return W4_GEN(1, 2);
+    case 8 + 4: return W4_GEN(1, 4);
+    case 16 + 1: return W4_GEN(2, 1);
+    case 16 + 2: return gemv_kernel<2, 2, 0, 0, true>;   // whole rows only (RW > 1)
+    case 24 + 1: return W4_GEN(3, 1);
+    case 32 + 1: return W4_GEN(4, 1);
     default: return nullptr;
   }
+#undef W4_GEN
 }
 
 // Raise `fn`'s dynamic shared-memory limit on `dev` (current) to at least
@@ -1130,19 +1147,20 @@ void planning_device(DeviceInfo* di) {
 // loops call the same few shapes over and over.
 struct PlanKey {
   int MR, N, K, n_items, split, xpi, sms;
+  bool routed;
   bool operator==(const PlanKey& o) const {
     return MR == o.MR && N == o.N && K == o.K && n_items == o.n_items && split == o.split &&
-           xpi == o.xpi && sms == o.sms;
+           xpi == o.xpi && sms == o.sms && routed == o.routed;
   }
 };
 
-bool cached_plan(int MR, int N, int K, int n_items, int split, int xpi, const DeviceInfo& di,
-                 Plan* out) {
+bool cached_plan(int MR, int N, int K, int n_items, int split, int xpi, bool routed,
+                 const DeviceInfo& di, Plan* out) {
   static std::mutex mu;
   static PlanKey keys[256];
   static Plan plans[256];
   static int used = 0, next = 0;
-  const PlanKey k{MR, N, K, n_items, split, xpi, di.sms};
+  const PlanKey k{MR, N, K, n_items, split, xpi, di.sms, routed};
   {
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < used; ++i)
@@ -1151,7 +1169,7 @@ bool cached_plan(int MR, int N, int K, int n_items, int split, int xpi, const De
         return true;
       }
   }
-  if (!make_plan(MR, N, K, n_items, split, xpi, di, out)) return false;
+  if (!make_plan(MR, N, K, n_items, split, xpi, routed, di, out)) return false;
   std::lock_guard<std::mutex> lock(mu);
   keys[next] = k;
   plans[next] = *out;
@@ -1168,7 +1186,8 @@ int max_rows_per_launch(int K, const DeviceInfo& di) {
   row_shape(K, &T, &NI, &CL, &nch);
   tile_geometry(K, T, CL, true, nch, 32 / T, &cp, &sp, &so, &tb);
   int mr = kMaxMR;
-  while (mr > 0 && kBarBytes + 2LL * tb + x_bytes(1, mr, NI * T) + red_bytes(32 / T, nch, mr) > optin)
+  while (mr > 0 &&
+         kBarBytes + 2LL * (tb + red_bytes(32 / T, nch, mr)) + x_bytes(1, mr, NI * T) > optin)
     --mr;
   return mr;
 }
@@ -1257,7 +1276,7 @@ extern "C" w4_status w4a16_gemv_plan(int M, int N, int K, w4_plan_info* info) {
   }
   Plan pl;
   const int mr_cap = max_rows_per_launch(K, di);
-  if (mr_cap < 1 || !cached_plan(std::min(M, mr_cap), N, K, 1, 1, 0, di, &pl)) return W4_ERR_SHAPE;
+  if (mr_cap < 1 || !cached_plan(std::min(M, mr_cap), N, K, 1, 1, 0, false, di, &pl)) return W4_ERR_SHAPE;
   info->path = 1;
   info->ctas = pl.ctas;
   info->slices = pl.S;
@@ -1285,11 +1304,11 @@ extern "C" size_t w4a16_gemv_workspace_bytes_flags(int M, int N, int K, unsigned
   if (path == 1) return tc_workspace(M, N, K, di.sms);
   Plan pl;
   const int mr_cap = max_rows_per_launch(K, di);
-  if (mr_cap < 1 || !cached_plan(std::min(M, mr_cap), N, K, 1, 1, 0, di, &pl)) return 0;
+  if (mr_cap < 1 || !cached_plan(std::min(M, mr_cap), N, K, 1, 1, 0, false, di, &pl)) return 0;
   size_t ws = pl.ws_bytes;
   for (int mr = 1; mr < std::min(M, mr_cap); ++mr) {   // smaller tail launches
     Plan pm;
-    if (cached_plan(mr, N, K, 1, 1, 0, di, &pm)) ws = std::max(ws, pm.ws_bytes);
+    if (cached_plan(mr, N, K, 1, 1, 0, false, di, &pm)) ws = std::max(ws, pm.ws_bytes);
   }
   return ws;
 }
@@ -1321,7 +1340,7 @@ extern "C" w4_status w4a16_gemv(void* y, const void* qw, const void* st, const v
   for (int m0 = 0; m0 < M; m0 += mr_cap) {
     const int mr = std::min(mr_cap, M - m0);
     Plan pm;
-    if (!cached_plan(mr, N, K, 1, 1, 0, di, &pm)) return W4_ERR_SHAPE;
+    if (!cached_plan(mr, N, K, 1, 1, 0, false, di, &pm)) return W4_ERR_SHAPE;
     if (pm.ws_bytes > 0 && (workspace == nullptr || workspace_bytes < pm.ws_bytes))
       return W4_ERR_WORKSPACE;
     if (pm.ws_bytes > 0 && !aligned(workspace, 16)) return W4_ERR_ALIGN;
@@ -1367,7 +1386,7 @@ extern "C" w4_status w4a16_gemv_id(void* y, const void* qw_base, size_t qw_strid
   if (!current_device(&dev, &di)) return W4_ERR_DEVICE;
   const int xpi = (x_rows == n_ids && n_ids > 1) ? 1 : 0;
   Plan pl;
-  if (!cached_plan(1, N, K, n_ids, 0, xpi, di, &pl)) return W4_ERR_SHAPE;
+  if (!cached_plan(1, N, K, n_ids, 0, xpi, true, di, &pl)) return W4_ERR_SHAPE;
   GemvParams p = base_params(pl, N, K);
   p.qw = static_cast<const uint8_t*>(qw_base);
   p.st = static_cast<const uint8_t*>(st_base);
@@ -1457,14 +1476,14 @@ extern "C" w4_status w4a16_gemv_static_scratch(void* y, const void* qw, const vo
   // every launch of this call must fit the fixed array: check before any work
   for (int m0 = 0; m0 < M; m0 += mr_cap) {
     Plan pm;
-    if (!cached_plan(std::min(mr_cap, M - m0), N, K, 1, 1, 0, di, &pm)) return W4_ERR_SHAPE;
+    if (!cached_plan(std::min(mr_cap, M - m0), N, K, 1, 1, 0, false, di, &pm)) return W4_ERR_SHAPE;
     if (pm.ws_bytes > (size_t)W4_STATIC_SCRATCH_BYTES) return W4_ERR_WORKSPACE;
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   for (int m0 = 0; m0 < M; m0 += mr_cap) {
     const int mr = std::min(mr_cap, M - m0);
     Plan pm;
-    cached_plan(mr, N, K, 1, 1, 0, di, &pm);
+    cached_plan(mr, N, K, 1, 1, 0, false, di, &pm);
     GemvParams p = base_params(pm, N, K);
     p.qw = static_cast<const uint8_t*>(qw);
     p.st = static_cast<const uint8_t*>(st);
