@@ -53,6 +53,14 @@
 #include "common.cuh"
 #include "gemv_tc.h"
 
+// Window counters of dense launches that hand out their windows at run time:
+// kWorkSlots slots of (windows taken, CTAs done), 64 bytes apart, used round
+// robin by successive launches on a device.  A launch's last CTA re-arms its
+// slot, so a slot is clean again long before it comes round (only a
+// launch still running kWorkSlots launches later could see it in use).
+constexpr int kWorkSlots = 1024;
+static __device__ __align__(64) int w4_window_counters[kWorkSlots * 16];
+
 namespace w4 {
 
 constexpr int kConsumerWarps = 7;
@@ -60,7 +68,8 @@ constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kThreads = kConsumers + 32;   // + the producer warp
 constexpr int kMaxMR = 4;                   // activation rows per launch
 constexpr int kMaxStages = 8;
-constexpr int kBarBytes = 256;              // full[8], empty[8], abort and last flags
+constexpr int kBarBytes = 256;              // full[8], empty[8], flags, windows[8]
+constexpr int kWinOff = 160;                // (row0, rows) of each stage's window (dense calls)
 constexpr long long kWaitCycles = 1LL << 31;
 
 struct GemvParams {
@@ -89,6 +98,8 @@ struct GemvParams {
   int* ws_count;                       // [B] at the start of the workspace
   float* ws_partial;                   // [B][nch][RB][MR] after it
   int32_t* status;
+  int dyn;                             // windows handed out at run time (dense, whole rows)
+  int* work;                           // [0] windows taken, [1] CTAs done (dyn only)
 };
 
 // ---------------------------------------------------------------- activations
@@ -428,6 +439,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
   const uint32_t full0 = sbase, empty0 = sbase + 8 * kMaxStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 16 * kMaxStages);
   volatile int* last_flag = abort_flag + 1;
+  volatile int* win = reinterpret_cast<volatile int*>(smem + kWinOff);
   const bool dense = p.ids == nullptr;
   const int nst = p.nst;
 
@@ -453,7 +465,65 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
     long long issued = 0;
     int slot = 0;
     uint32_t phase = 0;   // use count of the slot, mod 2
-    while (wk.next(p)) {
+    bool ended = false;   // the end of the windows went out in stage `slot`
+    if constexpr (DS) {
+      // Windows of RB rows: the CTA's range in order, or (dyn) window
+      // blockIdx.x first, then whichever the launch's counter hands out next.
+      // Each stage carries its window's (row0, rows) to the consumers; rows 0
+      // tells them there is no more work.
+      const long long nwin = (p.U + p.RB - 1) / p.RB;
+      long long r0 = wk.pos, w = blockIdx.x;
+      int grabbed = 0;      // lane 0: the counter's answer, in flight
+      bool pending = false;
+      while (true) {
+        if (issued >= nst && !wait_phase(empty0 + 8 * slot, phase ^ 1u, abort_flag)) {
+          if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        long long row0;
+        int nrows;
+        if (p.dyn) {
+          if (pending) w = (long long)__shfl_sync(0xffffffffu, grabbed, 0) + gridDim.x;
+          row0 = w * p.RB;
+          nrows = w < nwin ? (int)min((long long)p.RB, p.U - row0) : 0;
+        } else {
+          row0 = r0;
+          nrows = (int)max(0LL, min((long long)p.RB, wk.end - r0));
+          r0 += p.RB;
+        }
+        if (nrows == 0) {
+          if (lane == 0) {
+            win[2 * slot + 1] = 0;
+            mbar_arrive(full0 + 8 * slot);
+          }
+          ended = true;
+          break;
+        }
+        // the next window's number travels while this tile is requested
+        if (p.dyn && lane == 0) grabbed = atomicAdd(p.work, 1);
+        pending = p.dyn != 0;
+        if (lane == 0) {
+          win[2 * slot] = (int)row0;
+          win[2 * slot + 1] = nrows;
+        }
+        Walk cur = wk;
+        cur.item = 0;
+        cur.row0 = (int)row0;
+        cur.nrows = nrows;
+        cur.c0 = 0;
+        cur.c1 = p.nch;
+        cur.rb = 0;
+        const uint32_t st_off = kBarBytes + slot * p.tile_bytes;
+        issue_tile(p, cur, p.qw, p.st, sbase + st_off, smem + st_off, full0 + 8 * slot, lane, pol);
+        ++issued;
+        if (++slot == nst) {
+          slot = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    while (!DS && wk.next(p)) {
       const uint8_t *qwi, *sti;
       if (!item_arrays(p, wk.item, &qwi, &sti)) continue;
       // reuse of a slot waits for the consumers to release its last tile
@@ -470,14 +540,27 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
         phase ^= 1u;
       }
     }
-    // let the last copies land before the CTA may leave
-    const int last = issued < nst ? (int)issued : nst;
+    // Let the last copies land before the CTA may leave.  When the end went
+    // out in stage `slot`, that stage's previous tile had been released by
+    // the consumers (its barrier has moved on since): it is not waited for.
+    const int inflight = ended ? nst - 1 : nst;
+    const int last = issued < inflight ? (int)issued : inflight;
     for (int i = 1; i <= last; ++i) {
       const int sl = slot - i < 0 ? slot - i + nst : slot - i;
       const uint32_t ph = slot - i < 0 ? phase ^ 1u : phase;
       if (!mbar_wait_bounded(full0 + 8 * sl, ph, kWaitCycles)) {
         report(p.status, W4_ERR_TIMEOUT);
         break;
+      }
+    }
+    // dyn: the last CTA to finish re-arms the launch's counters (every CTA
+    // has taken its last window before it counts itself done)
+    if (DS && p.dyn && lane == 0) {
+      __threadfence();
+      if (atomicAdd(p.work + 1, 1) == (int)gridDim.x - 1) {
+        __threadfence();
+        atomicExch(p.work, 0);
+        atomicExch(p.work + 1, 0);
       }
     }
     return;
@@ -535,22 +618,23 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
   const int red_slot = p.RB * p.nch * MR;   // chunk sums of one stage's window
 
   if constexpr (DS) {
-    // Windows of RB rows from the CTA's first row (the last one may be
-    // shorter; the copy warp walks the same ones).  Rows of a short window
-    // past its end read stale bytes of the stage (in bounds) and are dropped.
+    // Each stage brings a window of whole rows (the copy warp's choice, up
+    // to RB rows; none: no more work).  Rows of a short window past its end
+    // read stale bytes of the stage (in bounds) and are dropped.
     const int ncw = p.nch;
-    for (long long r0 = wk.pos; r0 < wk.end; r0 += p.RB) {
-      const int row0 = (int)r0;
-      const int nrows = (int)min((long long)p.RB, wk.end - r0);
-      const int nrs = nrows == p.RB ? nrs_full : (nrows + rstep - 1) / rstep;
-      const int items = ncw * nrs;
-      const uint32_t soff0 = steps_aligned ? 0u : (uint32_t)(((row0 & 7) * (kg2 & 15)) & 15);
-      float* redw = red + slot * red_slot;
+    while (true) {
       if (!wait_phase(full0 + 8 * slot, phase, abort_flag)) {
         if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
         *abort_flag = 1;
         return;
       }
+      const int row0 = win[2 * slot];
+      const int nrows = win[2 * slot + 1];
+      if (nrows == 0) break;
+      const int nrs = nrows == p.RB ? nrs_full : (nrows + rstep - 1) / rstep;
+      const int items = ncw * nrs;
+      const uint32_t soff0 = steps_aligned ? 0u : (uint32_t)(((row0 & 7) * (kg2 & 15)) & 15);
+      float* redw = red + slot * red_slot;
       for (int it = warp; it < items; it += kConsumerWarps) {
         int ci, rs;
         if (nrs == 1) {
@@ -791,6 +875,7 @@ DeviceInfo device_info(int dev) {
 
 struct Plan {
   bool routed = false;   // routed-expert call (ids), never split
+  bool dyn = false;      // dense whole rows: windows handed out at run time
   int MR = 1;
   int Kg = 1;
   int T = 32, nsw = 1, NI = 1, CL = 1, nch = 1;
@@ -990,6 +1075,10 @@ bool make_plan(int MR, int N, int K, int n_items, int allow_split, int x_per_ite
     if (occ < pl.per_sm)
       return make_plan(MR, N, K, n_items, allow_split, x_per_item, routed, di, out, occ);
   }
+  // Dense whole-row launches with several windows per CTA take them from a
+  // counter at run time: SMs stream at different speeds, and a fixed share of
+  // rows per CTA would make the launch wait for the slowest.
+  if (!routed && pl.S == 1) pl.dyn = (pl.U + pl.RB - 1) / pl.RB >= 4LL * pl.ctas;
   if (pl.S > 1) {
     // counters first, partials after them
     const size_t part = (size_t)pl.B * pl.nch * pl.RB * MR * sizeof(float);
@@ -1077,11 +1166,34 @@ int occupancy(const Plan& pl, int dev) {
   return n;
 }
 
+// The next window-counter slot of device `dev` (current).
+cudaError_t work_slot(int dev, int** out) {
+  static std::mutex mu;
+  static int* base[64] = {};
+  static unsigned next[64] = {};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (base[dev] == nullptr) {
+    void* a = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&a, w4_window_counters);
+    if (e != cudaSuccess) return e;
+    base[dev] = static_cast<int*>(a);
+  }
+  *out = base[dev] + 16 * (next[dev]++ % kWorkSlots);
+  return cudaSuccess;
+}
+
 cudaError_t launch(const GemvParams& prm, const Plan& pl, bool pdl, cudaStream_t stream, int dev) {
   const KernelFn fn = kernel_for(pl);
   if (fn == nullptr) return cudaErrorInvalidConfiguration;
   const cudaError_t ea = allow_smem(fn, pl.smem, dev);
   if (ea != cudaSuccess) return ea;
+  GemvParams p = prm;
+  if (pl.dyn) {
+    const cudaError_t ew = work_slot(dev, &p.work);
+    if (ew != cudaSuccess) return ew;
+    p.dyn = 1;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)pl.ctas);
   cfg.blockDim = dim3(kThreads);
@@ -1092,7 +1204,7 @@ cudaError_t launch(const GemvParams& prm, const Plan& pl, bool pdl, cudaStream_t
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, fn, prm);
+  return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
 GemvParams base_params(const Plan& pl, int N, int K) {
@@ -1290,6 +1402,7 @@ extern "C" w4_status w4a16_gemv_plan(int M, int N, int K, w4_plan_info* info) {
   info->chunk_steps = pl.CL;
   info->stages = pl.nst;
   info->ctas_per_sm = pl.per_sm;
+  info->dynamic_windows = pl.dyn ? 1 : 0;
   // compile-time team size / chunk length of the instantiation (0: generic)
   kernel_for(pl, &info->tmpl_team, &info->tmpl_chunk);
   return W4_OK;

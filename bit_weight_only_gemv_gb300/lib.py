@@ -44,7 +44,7 @@ class PlanInfo(ctypes.Structure):
                                             "unit_rows", "chunk_groups", "rows_per_lane",
                                             "smem_bytes", "rows_per_call", "chunk_steps",
                                             "stages", "ctas_per_sm", "tmpl_team",
-                                            "tmpl_chunk")]
+                                            "tmpl_chunk", "dynamic_windows")]
 
 
 _lib = None

@@ -89,7 +89,7 @@ typedef enum w4_status {
 #define W4_GROUP 32        /* codes per group along K */
 #define W4_MAX_K 65536     /* largest supported K */
 #define W4_MAX_M 32        /* largest batch of activation rows per call */
-#define W4_ABI_VERSION 2
+#define W4_ABI_VERSION 3
 
 /* Human-readable name of a status code (static string). */
 const char *w4_status_str(int status);
@@ -127,6 +127,12 @@ const char *w4_last_cuda_error(void);
  *            W4_FLAG_TENSOR_CORES (default: tensor cores from M = 8 when K is
  *            a multiple of 256; W4_ERR_SHAPE if the pinned path cannot run K).
  * Returns W4_OK once the work is enqueued.
+ *
+ * Large CUDA-core launches (w4_plan_info.dynamic_windows) hand their row
+ * windows to the CTAs from a counter held by the library: one of 1024 slots
+ * per device, taken round robin per launch and re-armed by the launch's last
+ * CTA.  Only a launch still running 1024 launches after it was enqueued (on
+ * any stream of the device) could meet its slot in use.
  */
 w4_status w4a16_gemv(void *y, const void *qw, const void *st, const void *x,
                      int M, int N, int K, void *workspace, size_t workspace_bytes,
@@ -335,6 +341,8 @@ typedef struct w4_plan_info {
     int ctas_per_sm;    /* resident CTAs per SM the plan is sized for */
     int tmpl_team;      /* team size compiled into the kernel (0: generic) */
     int tmpl_chunk;     /* chunk steps compiled into the kernel (0: generic) */
+    int dynamic_windows; /* 1: CTAs take windows of unit_rows rows from a counter at
+                            run time (dense calls with many windows per CTA) */
 } w4_plan_info;
 
 w4_status w4a16_gemv_plan(int M, int N, int K, w4_plan_info *info);

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_call(L):
 
 
 def test_version_and_status_strings(L):
-    assert L.w4_abi_version() == 2
+    assert L.w4_abi_version() == 3
     assert L.w4_status_str(0) == b"ok"
     assert L.w4_status_str(6) == b"id out of range"
     assert L.w4_status_str(999) == b"unknown status"
