@@ -621,7 +621,13 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
     // Each stage brings a window of whole rows (the copy warp's choice, up
     // to RB rows; none: no more work).  Rows of a short window past its end
     // read stale bytes of the stage (in bounds) and are dropped.
+    // Every window is walked as a full one: item it = ci * nrs_full + rs
+    // (chunk ci, row step rs); a warp takes items warp, warp + 7, ..., its
+    // (chunk, row step) stepping by a fixed increment.
     const int ncw = p.nch;
+    const int items = ncw * nrs_full;
+    const int ci_first = warp / nrs_full, rs_first = warp - ci_first * nrs_full;
+    const int dci = kConsumerWarps / nrs_full, drs = kConsumerWarps - dci * nrs_full;
     while (true) {
       if (!wait_phase(full0 + 8 * slot, phase, abort_flag)) {
         if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
@@ -631,22 +637,10 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
       const int row0 = win[2 * slot];
       const int nrows = win[2 * slot + 1];
       if (nrows == 0) break;
-      const int nrs = nrows == p.RB ? nrs_full : (nrows + rstep - 1) / rstep;
-      const int items = ncw * nrs;
       const uint32_t soff0 = steps_aligned ? 0u : (uint32_t)(((row0 & 7) * (kg2 & 15)) & 15);
       float* redw = red + slot * red_slot;
+      int ci = ci_first, rs = rs_first;
       for (int it = warp; it < items; it += kConsumerWarps) {
-        int ci, rs;
-        if (nrs == 1) {
-          ci = it;
-          rs = 0;
-        } else if (ncw == 1) {
-          ci = 0;
-          rs = it;
-        } else {
-          ci = it / nrs;
-          rs = it - ci * nrs;
-        }
         const uint32_t ic = tile + (uint32_t)(rs * rstep * p.code_pitch + ci * gpc * 16);
         const uint32_t is = tile + soff0 + (uint32_t)(rs * rstep * kg2 + ci * gpc * 2);
         uint32_t co[RW], so[RW];
@@ -678,6 +672,12 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
               for (int m = 0; m < MR; ++m) redw[(rl * p.nch + ci) * MR + m] = acc[j][m];
             }
           }
+        }
+        ci += dci;
+        rs += drs;
+        if (rs >= nrs_full) {
+          rs -= nrs_full;
+          ++ci;
         }
       }
       __syncwarp();
@@ -1047,7 +1047,7 @@ bool make_plan(int MR, int N, int K, int n_items, int allow_split, int x_per_ite
         const double per_warp = (double)items / kConsumerWarps;   // items a warp takes
         const double score = util * std::min(1.0, (double)tb / kTileGood) *
                              (nst >= 3 ? 1.0 : 0.95) * (1.0 - 0.15 / std::max(1.0, per_warp)) *
-                             (1.0 + 0.2 * (rw > 1) + 0.1 * (rw > 2));
+                             (1.0 + 0.2 * (rw > 1) + 0.2 * (rw > 2));
         if (score > best + 1e-9) {
           best = score;
           pl.RW = rw;
@@ -1100,12 +1100,13 @@ KernelFn kernel_for(const Plan& pl, int* tt = nullptr, int* clt = nullptr) {
   if (clt != nullptr) *clt = 0;
   const bool ds = !pl.routed && pl.S == 1;
   const bool full = pl.NI % pl.CL == 0 && pl.NI * pl.T == pl.Kg;
-  if (pl.MR == 1 && full && pl.RW <= 2) {
+  if (pl.MR == 1 && full && (pl.RW <= 2 || (ds && pl.RW == 4))) {
     const int key = pl.T * 8 + pl.CL;
 #define W4_SPEC(t, cl)                                                            \
   if (key == (t) * 8 + (cl)) {                                                    \
     if (tt != nullptr) *tt = t;                                                   \
     if (clt != nullptr) *clt = cl;                                                \
+    if (ds && pl.RW == 4) return gemv_kernel<1, 4, t, cl, true>;                  \
     if (ds) return pl.RW == 1 ? gemv_kernel<1, 1, t, cl, true> : gemv_kernel<1, 2, t, cl, true>; \
     return pl.RW == 1 ? gemv_kernel<1, 1, t, cl, false> : gemv_kernel<1, 2, t, cl, false>;       \
   }
