@@ -240,8 +240,11 @@ def kernel_key(kind, shape, lib):  # ncu names the instantiation
         return "gather_kernel"
     M, N, K = shape
     p = lib.plan(M, N, K)
+    if p["path"] == 2:
+        return "tc_kernel"
+    dense = "1" if p["slices"] == 1 else "0"   # dense whole-row instantiation (as ncu prints it)
     return (f"gemv_kernel<{p['rows_per_call']}, {p['rows_per_lane']}, "
-            f"{p['tmpl_team']}, {p['tmpl_chunk']}>")
+            f"{p['tmpl_team']}, {p['tmpl_chunk']}, {dense}>")
 
 
 def capture(fns, stream, pdl=True):
@@ -595,13 +598,15 @@ def run_moe(args, world, rank, local):
             copied += nm * (d["qs"] + d["ss"])
         return copied
 
-    def gemvs(lay, ids=None, full=False):
-        for name in shapes:
+    def gemvs(lay, ids=None, full=False, pdl=False):
+        # programmatic dependent launch after the first kernel: the routed
+        # kernel reads its ids and activations only after the previous one
+        for i, name in enumerate(shapes):
             d = lay[name]
             lib.gemv_id(d["full_q"] if full else d["pool_q"], d["full_s"] if full else d["pool_s"],
                         lay["slot_ids"] if ids is None else ids, lay["x"][name], d["n"], d["k"],
                         E if full else S, d["qs"], d["ss"], y=d["y_full"] if full else d["y"],
-                        status=status, stream=stream)
+                        status=status, pdl=pdl or i > 0, stream=stream)
 
     kernel_bytes = L * sum(metrics.gemv_id_bytes(k_top, 1 if name == "gate_up" else k_top, n, k)
                            for name, (n, k) in shapes.items())
@@ -635,8 +640,8 @@ def run_moe(args, world, rank, local):
             lfu[key] += st[key]
 
     # kernel only: the last step's 60 routed GEMVs (pool contents as left), as a graph
-    fns = [(lambda lay: (lambda pdl: gemvs(lay)))(lay) for lay in layers]
-    g = capture(fns, stream, pdl=False)
+    fns = [(lambda lay: (lambda pdl: gemvs(lay, pdl=pdl)))(lay) for lay in layers]
+    g = capture(fns, stream)
     for _ in range(3):
         g.replay()
     kms = time_replays(g, stream, max(3, min(steps, 50)))
@@ -679,7 +684,8 @@ def run_moe(args, world, rank, local):
         "host_seconds_per_step": host_s / steps,
         "kernel": {"ms_per_step": kms, "tok_s": 1000.0 / kms, "bytes_per_step": kernel_bytes,
                    "gbps": gbps, "frac": gbps / peak, "peak": peak, "peak_kind": peak_kind,
-                   "note": "the 60 gemv_id launches of one step replayed as a graph"},
+                   "note": "the 60 gemv_id launches of one step replayed as a graph, "
+                           "PDL-chained"},
         "pool": dict(lfu, hit_rate=lfu["hits"] / max(1, lfu["requests"]),
                      copy_bytes_per_step=copied / steps),
         "bitwise_pool_vs_full": {"steps": total, "layers": L, "mismatched_values": int(bad.item())},

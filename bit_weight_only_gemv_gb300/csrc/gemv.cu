@@ -342,9 +342,7 @@ __device__ void issue_tile(const GemvParams& p, const Walk& wk, const uint8_t* q
 }
 
 // ---------------------------------------------------------------- consumers
-constexpr int kMaxCL = 4;   // groups per lane per chunk, at most
-
-// One chunk of a tile: for each of its `ns` (<= kMaxCL) groups per lane, the
+// One chunk of a tile: for each of its `ns` groups per lane, the
 // lane loads the group's staged activations (MR rows) once and applies them
 // to its RW rows.  acc[j][m] = sum over the chunk's groups, in group order.
 // TT, CLT > 0 fix the team size and the (always full) chunk length at compile
@@ -362,9 +360,7 @@ __device__ __forceinline__ void tile_dot(const uint8_t* sm, uint32_t xo, uint32_
     for (int m = 0; m < MR; ++m) acc[j][m] = 0.0f;
   const int gstep = (TT > 0 ? TT : T) * 16;          // bytes between a lane's groups
   const int sstep = gstep >> 3, xsstep = gstep >> 2;  // the same for steps, scales
-#pragma unroll
-  for (int s = 0; s < (CLT > 0 ? CLT : kMaxCL); ++s) {
-    if (CLT == 0 && s >= ns) break;
+  auto group = [&](int s) {
     uint4 xv[MR][4];
     float inv[MR];
 #pragma unroll
@@ -384,6 +380,13 @@ __device__ __forceinline__ void tile_dot(const uint8_t* sm, uint32_t xo, uint32_
 #pragma unroll
       for (int m = 0; m < MR; ++m) acc[j][m] = fmaf(group_sum(q, xv[m]) * inv[m], stf, acc[j][m]);
     }
+  };
+  if constexpr (CLT > 0) {
+#pragma unroll
+    for (int s = 0; s < CLT; ++s) group(s);
+  } else {
+#pragma unroll 4
+    for (int s = 0; s < ns; ++s) group(s);
   }
 }
 
@@ -898,8 +901,8 @@ constexpr long long kRowStepMax = 40 << 10;  // largest step of whole rows
 // The per-row arithmetic comes from K alone.  T: the largest power of two
 // <= 32 dividing K/32 that leaves each lane >= 4 groups of a row (else the
 // largest dividing one).  CL, groups per lane per chunk: all of the lane's
-// groups when they are <= 4, else 4 or 3 when that divides them, else 4
-// (the last chunk shorter).
+// groups when they are <= 4, else 4 or 3 when that divides them, else all of
+// them up to 12, else 4 (the last chunk shorter).
 void row_shape(int K, int* T, int* NI, int* CL, int* nch) {
   const int Kg = K / 32;
   int t = 1;
@@ -920,6 +923,7 @@ void row_shape(int K, int* T, int* NI, int* CL, int* nch) {
   if (ni <= 4) cl = ni;
   else if (ni % 4 == 0) cl = 4;
   else if (ni % 3 == 0) cl = 3;
+  else if (ni <= 12) cl = ni;   // 5, 7, 10, 11: one chunk
   *NI = ni;
   *CL = cl;
   *nch = (ni + cl - 1) / cl;
@@ -1101,9 +1105,9 @@ KernelFn kernel_for(const Plan& pl, int* tt = nullptr, int* clt = nullptr) {
   const bool ds = !pl.routed && pl.S == 1;
   const bool full = pl.NI % pl.CL == 0 && pl.NI * pl.T == pl.Kg;
   if (pl.MR == 1 && full && (pl.RW <= 2 || (ds && pl.RW == 4))) {
-    const int key = pl.T * 8 + pl.CL;
+    const int key = pl.T * 16 + pl.CL;
 #define W4_SPEC(t, cl)                                                            \
-  if (key == (t) * 8 + (cl)) {                                                    \
+  if (key == (t) * 16 + (cl)) {                                                   \
     if (tt != nullptr) *tt = t;                                                   \
     if (clt != nullptr) *clt = cl;                                                \
     if (ds && pl.RW == 4) return gemv_kernel<1, 4, t, cl, true>;                  \
@@ -1114,6 +1118,8 @@ KernelFn kernel_for(const Plan& pl, int* tt = nullptr, int* clt = nullptr) {
     W4_SPEC(8, 3)    // K = 5376
     W4_SPEC(32, 3)   // K = 21504
     W4_SPEC(32, 4)   // K = 4096 * n
+    W4_SPEC(8, 11)   // K = 2816
+    W4_SPEC(2, 11)   // K = 704
 #undef W4_SPEC
   }
 #define W4_GEN(mr, rw) (ds ? gemv_kernel<mr, rw, 0, 0, true> : gemv_kernel<mr, rw, 0, 0, false>)
