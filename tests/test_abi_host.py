@@ -86,7 +86,11 @@ def test_plan_is_valid(M, N, K):
     assert p["team"] in (1, 2, 4, 8, 16, 32) and (K // 32) % p["team"] == 0
     assert p["rows_per_lane"] in (1, 2, 4)
     assert p["unit_rows"] % ((32 // p["team"]) * p["rows_per_lane"]) == 0
-    assert 1 <= p["chunk_steps"] <= 4
+    # groups per lane per chunk: all of a lane's groups when <= 4, else 4 or 3
+    # when that divides them, else all of them up to 12, else 4
+    ni = -(-(K // 32) // p["team"])
+    want = (ni if ni <= 4 else 4 if ni % 4 == 0 else 3 if ni % 3 == 0 else ni if ni <= 12 else 4)
+    assert p["chunk_steps"] == want
     assert p["chunk_groups"] == p["team"] * p["chunk_steps"]
     assert 1 <= p["ctas"] <= 2 * 152
     assert p["ctas_per_sm"] in (1, 2)
