@@ -551,7 +551,9 @@ def run_moe(args, world, rank, local):
     layer): per step and layer, remap the step's experts to pool slots (host),
     copy the missed experts into the pool and write the slot ids (device),
     then w4a16_gemv_id for the merged gate/up (x broadcast) and for down (one
-    x row per expert), addressing the pool."""
+    x row per expert), addressing the pool.  An expert's gate/up and down
+    weights sit side by side in its slot (and in the full tensor), so one
+    remap and one copy of codes and one of steps per miss serve both."""
     from bit_weight_only_gemv_gb300 import lib
     lib.load()
     dev = torch.device("cuda", local)
@@ -562,51 +564,51 @@ def run_moe(args, world, rank, local):
     steps, warm = args.steps, args.warmup
     total = warm + steps
     shapes = {"gate_up": (2 * I, H), "down": (H, I)}
+    # bytes per expert: codes and steps of each projection, and where they sit
+    qoff, soff, qcomb, scomb = {}, {}, 0, 0
+    for name, (n, k) in shapes.items():
+        qoff[name], soff[name] = qcomb, scomb
+        qcomb += n * k // 2
+        scomb += n * k // 16
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
     layers = []
     for li in range(L):
         lay = {"trace": synth.moe_trace(E, k_top, total, cfg.zipf_s, cfg.repeat_p,
                                         seed=synth.seed_of(42, li)),
                "x": {"gate_up": synth.torch_x((1, H), synth.seed_of(43, li), dev),
                      "down": synth.torch_x((k_top, I), synth.seed_of(44, li), dev)},
-               "slot_ids": torch.zeros(k_top, dtype=torch.int32, device=dev)}
+               "slot_ids": torch.zeros(k_top, dtype=torch.int32, device=dev),
+               "ids_full": torch.zeros(k_top, dtype=torch.int32, device=dev),
+               "full_q": synth.torch_words((E, qcomb // 4), synth.seed_of(40, li), dev),
+               "full_s": synth.torch_steps((E, scomb // 2), synth.seed_of(41, li), dev),
+               "pool_q": torch.zeros((S, qcomb // 4), dtype=torch.int32, device=dev),
+               "pool_s": torch.zeros((S, scomb // 2), dtype=torch.bfloat16, device=dev),
+               "y": {}, "y_full": {}, "calls": [], "calls_full": []}
         for name, (n, k) in shapes.items():
-            qs, ss = n * k // 2, n * k // 16          # bytes per expert
-            lay[name] = {
-                "n": n, "k": k, "qs": qs, "ss": ss,
-                "full_q": synth.torch_words((E, qs // 4), synth.seed_of(40, li, n), dev),
-                "full_s": synth.torch_steps((E, ss // 2), synth.seed_of(41, li, n), dev),
-                "pool_q": torch.zeros((S, qs // 4), dtype=torch.int32, device=dev),
-                "pool_s": torch.zeros((S, ss // 2), dtype=torch.bfloat16, device=dev),
-                "y": torch.empty((k_top, n), dtype=torch.bfloat16, device=dev),
-                "y_full": torch.empty((k_top, n), dtype=torch.bfloat16, device=dev)}
+            lay["y"][name] = torch.empty((k_top, n), dtype=torch.bfloat16, device=dev)
+            lay["y_full"][name] = torch.empty((k_top, n), dtype=torch.bfloat16, device=dev)
+            for full, calls in ((False, lay["calls"]), (True, lay["calls_full"])):
+                q = lay["full_q" if full else "pool_q"][:, qoff[name] // 4:]
+                st = lay["full_s" if full else "pool_s"][:, soff[name] // 2:]
+                calls.append(lib.bind_gemv_id(q, st, lay["ids_full" if full else "slot_ids"],
+                                              lay["x"][name], n, k, E if full else S, qcomb,
+                                              scomb, lay["y_full" if full else "y"][name],
+                                              status))
         layers.append(lay)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    stream = torch.cuda.Stream(device=dev)
 
     def new_pools():
         for lay in layers:
-            for name in shapes:
-                lay[name]["pool"] = lib.SlotPool(E, S)
+            lay["pool"] = lib.SlotPool(E, S)
+            lay["stage"] = lay["pool"].bind_stage(k_top, lay["pool_q"], lay["full_q"], qcomb,
+                                                  qcomb, lay["pool_s"], lay["full_s"], scomb,
+                                                  scomb, lay["slot_ids"])
 
-    def stage(lay, t):
-        copied = 0
-        for name in shapes:
-            d = lay[name]
-            _, nm = d["pool"].stage(lay["trace"][t], d["pool_q"], d["full_q"], d["qs"], d["qs"],
-                                    d["pool_s"], d["full_s"], d["ss"], d["ss"], lay["slot_ids"],
-                                    stream=stream)
-            copied += nm * (d["qs"] + d["ss"])
-        return copied
-
-    def gemvs(lay, ids=None, full=False, pdl=False):
+    def gemvs(lay, full=False, pdl=False):
         # programmatic dependent launch after the first kernel: the routed
         # kernel reads its ids and activations only after the previous one
-        for i, name in enumerate(shapes):
-            d = lay[name]
-            lib.gemv_id(d["full_q"] if full else d["pool_q"], d["full_s"] if full else d["pool_s"],
-                        lay["slot_ids"] if ids is None else ids, lay["x"][name], d["n"], d["k"],
-                        E if full else S, d["qs"], d["ss"], y=d["y_full"] if full else d["y"],
-                        status=status, pdl=pdl or i > 0, stream=stream)
+        for i, call in enumerate(lay["calls_full" if full else "calls"]):
+            call(pdl=pdl or i > 0, stream=stream)
 
     kernel_bytes = L * sum(metrics.gemv_id_bytes(k_top, 1 if name == "gate_up" else k_top, n, k)
                            for name, (n, k) in shapes.items())
@@ -622,12 +624,12 @@ def run_moe(args, world, rank, local):
                 torch.cuda.synchronize()
                 e0.record(stream)
                 t_host = time.perf_counter()
-            c = 0
+            misses = 0
             for lay in layers:
-                c += stage(lay, t)
-                gemvs(lay)
+                misses += lay["stage"](lay["trace"][t], stream=stream)
+                gemvs(lay, pdl=True)
             if t >= warm:
-                copied += c
+                copied += misses * (qcomb + scomb)
         e1.record(stream)
     torch.cuda.synchronize()
     host_s = time.perf_counter() - t_host
@@ -635,7 +637,7 @@ def run_moe(args, world, rank, local):
     ms = max_over_ranks(ms, dev)
     lfu = {"requests": 0, "hits": 0, "misses": 0}
     for lay in layers:
-        st = lay["gate_up"]["pool"].stats()
+        st = lay["pool"].stats()
         for key in lfu:
             lfu[key] += st[key]
 
@@ -655,14 +657,13 @@ def run_moe(args, world, rank, local):
     with torch.cuda.stream(stream):
         for t in range(total):
             for lay in layers:
-                stage(lay, t)
+                lay["stage"](lay["trace"][t], stream=stream)
                 gemvs(lay)
-                ids_full = torch.from_numpy(lay["trace"][t].astype(np.int32)).to(dev,
-                                                                               non_blocking=True)
-                gemvs(lay, ids=ids_full, full=True)
+                lay["ids_full"].copy_(torch.from_numpy(lay["trace"][t].astype(np.int32)))
+                gemvs(lay, full=True)
                 for name in shapes:
-                    d = lay[name]
-                    bad += (d["y"].view(torch.int16) != d["y_full"].view(torch.int16)).sum()
+                    bad += (lay["y"][name].view(torch.int16) !=
+                            lay["y_full"][name].view(torch.int16)).sum()
     torch.cuda.synchronize()
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
@@ -680,7 +681,9 @@ def run_moe(args, world, rank, local):
                                f"{2 * I}x{H} and down {H}x{I} through w4a16_gemv_id",
                    "global_batch": world, "parallelism": f"replicas x{world}",
                    "timed": "eager steps: host LFU remap + pool copies + slot ids + 2 gemv_id "
-                            "per layer (CUDA events)"},
+                            "per layer (CUDA events)",
+                   "pool_layout": "one 32-slot pool per layer; a slot holds an expert's gate/up "
+                                  "and down codes (and, in a second pool array, steps)"},
         "host_seconds_per_step": host_s / steps,
         "kernel": {"ms_per_step": kms, "tok_s": 1000.0 / kms, "bytes_per_step": kernel_bytes,
                    "gbps": gbps, "frac": gbps / peak, "peak": peak, "peak_kind": peak_kind,
@@ -689,7 +692,7 @@ def run_moe(args, world, rank, local):
         "pool": dict(lfu, hit_rate=lfu["hits"] / max(1, lfu["requests"]),
                      copy_bytes_per_step=copied / steps),
         "bitwise_pool_vs_full": {"steps": total, "layers": L, "mismatched_values": int(bad.item())},
-        "gpu_launches": steps * L * 6,
+        "gpu_launches": steps * L * 3,   # per layer: slot-id write, 2 gemv_id
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -195,6 +195,32 @@ def gemv_id(qw_base: torch.Tensor, st_base: torch.Tensor, ids: torch.Tensor, x: 
     return y
 
 
+def bind_gemv_id(qw_base: torch.Tensor, st_base: torch.Tensor, ids: torch.Tensor,
+                 x: torch.Tensor, N: int, K: int, num_experts: int, qw_stride_bytes: int,
+                 st_stride_bytes: int, y: torch.Tensor, status: torch.Tensor = None):
+    """w4a16_gemv_id with its arguments marshalled once, for decode loops.
+
+    Returns call(pdl=False, stream=None), which enqueues the same routed
+    product again (reading whatever the tensors hold at that time; they must
+    stay allocated and in place).
+    """
+    _need(ids, torch.int32, "ids")
+    _need(x, torch.bfloat16, "x")
+    _need(y, torch.bfloat16, "y")
+    if not (qw_base.is_cuda and st_base.is_cuda):
+        raise ValueError("bases must be CUDA tensors")
+    x2 = x if x.dim() == 2 else x.view(1, -1)
+    fn = load().w4a16_gemv_id
+    args = (_ptr(y), _ptr(qw_base), qw_stride_bytes, _ptr(st_base), st_stride_bytes, num_experts,
+            _ptr(ids), ids.numel(), _ptr(x2), x2.shape[0], N, K, _ptr(status))
+
+    def call(pdl: bool = False, stream=None):
+        _check(fn(*args, W4_FLAG_PDL if pdl else 0, _stream(stream)), "w4a16_gemv_id")
+
+    call.tensors = (qw_base, st_base, ids, x2, y, status)   # keep them alive
+    return call
+
+
 def embed_gather(qw: torch.Tensor, st: torch.Tensor, ids: torch.Tensor, out: torch.Tensor = None,
                  status: torch.Tensor = None, pdl: bool = False, stream=None) -> torch.Tensor:
     qw = _as_words(qw)
@@ -273,6 +299,28 @@ class SlotPool:
                                             ctypes.byref(nm), _stream(stream)),
                "w4_slot_pool_stage")
         return list(slots), nm.value
+
+    def bind_stage(self, k: int, pool_qw, full_qw, qw_stride, qw_bytes, pool_st, full_st,
+                   st_stride, st_bytes, slot_ids_dev: torch.Tensor):
+        """stage() with the buffers marshalled once: returns call(ids, stream=None)
+        for requests of k ids (any int sequence), which returns the misses."""
+        arr = (ctypes.c_int32 * k)()
+        slots = (ctypes.c_int32 * k)()
+        nm = ctypes.c_int()
+        fixed = (_ptr(pool_qw), _ptr(full_qw), qw_stride, qw_bytes, _ptr(pool_st), _ptr(full_st),
+                 st_stride, st_bytes, _ptr(slot_ids_dev), slots, ctypes.byref(nm))
+        fn, h = self._lib.w4_slot_pool_stage, self._h
+
+        def call(ids, stream=None) -> int:
+            if len(ids) != k:
+                raise ValueError(f"expected {k} ids")
+            for i, v in enumerate(ids):
+                arr[i] = int(v)
+            _check(fn(h, arr, k, *fixed, _stream(stream)), "w4_slot_pool_stage")
+            return nm.value
+
+        call.tensors = (pool_qw, full_qw, pool_st, full_st, slot_ids_dev)
+        return call
 
     def stats(self):
         r, h, m = ctypes.c_longlong(), ctypes.c_longlong(), ctypes.c_longlong()

@@ -110,3 +110,49 @@ def test_slot_pool_is_bitwise_equal_to_full_tensor(cuda_lib):
             st = pool.stats()
             assert st["hits"] > 0 and st["misses"] >= S
     torch.cuda.synchronize()
+
+
+def test_bound_calls_and_side_by_side_slots(cuda_lib):
+    """Pre-marshalled calls (bind_stage, bind_gemv_id) over slots that hold two
+    projections side by side give the same slots and bits as the plain calls
+    on separate per-projection tensors."""
+    cfg = synth.moe_2816()
+    E, S, H, I, k_top = 16, 6, cfg.hidden, cfg.expert_inter, 4
+    shapes = {"gate_up": (2 * I, H), "down": (H, I)}
+    qoff, soff, qcomb, scomb = {}, {}, 0, 0
+    for name, (n, k) in shapes.items():
+        qoff[name], soff[name] = qcomb, scomb
+        qcomb += n * k // 2
+        scomb += n * k // 16
+    full_q = synth.torch_words((E, qcomb // 4), seed=synth.seed_of(6, 1), device="cuda")
+    full_s = synth.torch_steps((E, scomb // 2), seed=synth.seed_of(6, 2), device="cuda")
+    pool_q = torch.zeros((S, qcomb // 4), dtype=torch.int32, device="cuda")
+    pool_s = torch.zeros((S, scomb // 2), dtype=torch.bfloat16, device="cuda")
+    slot_ids = torch.zeros(k_top, dtype=torch.int32, device="cuda")
+    xs = {"gate_up": synth.torch_x((1, H), seed=7, device="cuda"),
+          "down": synth.torch_x((k_top, I), seed=8, device="cuda")}
+    ys = {name: torch.empty((k_top, n), dtype=torch.bfloat16, device="cuda")
+          for name, (n, k) in shapes.items()}
+    calls = {name: lib.bind_gemv_id(pool_q[:, qoff[name] // 4:], pool_s[:, soff[name] // 2:],
+                                    slot_ids, xs[name], n, k, S, qcomb, scomb, ys[name])
+             for name, (n, k) in shapes.items()}
+    pool, ref_pool = lib.SlotPool(E, S), lib.SlotPool(E, S)
+    stage = pool.bind_stage(k_top, pool_q, full_q, qcomb, qcomb, pool_s, full_s, scomb, scomb,
+                            slot_ids)
+    ref_slots = torch.zeros(k_top, dtype=torch.int32, device="cuda")
+    trace = synth.moe_trace(E, k_top, 30, 1.1, 0.7, seed=3)
+    for t in range(30):
+        nm = stage(trace[t])
+        _, nm_ref = ref_pool.stage(trace[t], pool_q, full_q, qcomb, qcomb, pool_s, full_s, scomb,
+                                   scomb, ref_slots)
+        assert nm == nm_ref
+        assert torch.equal(slot_ids, ref_slots)
+        for name, (n, k) in shapes.items():
+            calls[name](pdl=name == "down")
+            # the same product from this projection's weights of the named experts
+            q = full_q[:, qoff[name] // 4:(qoff[name] + n * k // 2) // 4].contiguous()
+            st = full_s[:, soff[name] // 2:(soff[name] + n * k // 16) // 2].contiguous()
+            ids = torch.from_numpy(trace[t].astype(np.int32)).cuda()
+            y_ref = lib.gemv_id(q, st, ids, xs[name], n, k, E, n * k // 2, n * k // 16)
+            assert torch.equal(ys[name].view(torch.int16), y_ref.view(torch.int16)), (name, t)
+    torch.cuda.synchronize()
