@@ -10,14 +10,13 @@
 //  * A CTA owns tiles of 128 weight rows (the MMA's M).  A copy warp streams
 //    each (tile, 256-code K slice) stage into a shared-memory ring: the codes
 //    as one 2-D TMA box with 128-byte swizzle (16 KB), the steps as one 2-D
-//    box (2 KB) and the M activation rows of the slice as 1-D bulk copies.
+//    box (2 KB), and the activation rows of the slice (M rounded up to 8)
+//    as one 3-D box that lands directly in the B-operand layout (bf16,
+//    K-major 8x8 core matrices).
 //  * Four warps (thread = weight row) turn each packed word into four bf16
-//    pairs (c - 8) with the page's float-bit trick in bf16 form
-//    ((0x4300 | c) - 136 = c - 8, exact) and store them into tensor memory
-//    with tcgen05.st: tensor memory holds the A operand.  The pairs are
-//    codes (i, i + 4) of the word, so the activation slice is permuted the
-//    same way into the B operand (bf16, K-major, 8x8 core matrices) in shared
-//    memory.
+//    pairs (c - 8) of consecutive codes with the page's float-bit trick in
+//    bf16 form ((0x4300 | c) - 136 = c - 8, exact) and store them into
+//    tensor memory with tcgen05.st: tensor memory holds the A operand.
 //  * Per group of 32 codes one thread issues two tcgen05.mma (K = 16 each,
 //    N = 16 or 32 activation columns, fp32 accumulate) into a fresh group
 //    accumulator in tensor memory; the four warps read it back (tcgen05.ld)
@@ -49,7 +48,8 @@ constexpr int kSliceGroups = 8;     // 32-code groups per stage
 constexpr int kDequantWarps = 4;
 constexpr int kThreads = 32 * (kDequantWarps + 2);   // + copy warp + MMA warp
 constexpr int kMaxStages = 4;
-constexpr int kBarBytes = 128;      // full[4], empty[4], aready[2], dready[2], flags, tmem base
+constexpr int kBufs = 2;            // rounds of A and D held in tensor memory
+constexpr int kBarBytes = 192;      // full[4], empty[4], aready[4], dready[4], flags, tmem base
 constexpr int kCodesBytes = kRows * 128;   // 16 KB, 1024-byte aligned (128-byte swizzle)
 constexpr int kStepsBytes = kRows * 16;    // 2 KB
 constexpr long long kWaitCycles = 1LL << 31;
@@ -57,12 +57,14 @@ constexpr long long kWaitCycles = 1LL << 31;
 struct TcParams {
   CUtensorMap tm_codes;   // codes viewed as uint8 [N][K/2], box 128 x 128, 128-byte swizzle
   CUtensorMap tm_steps;   // steps viewed as uint16 [N][K/32], box 8 x 128
+  CUtensorMap tm_x;       // activations viewed as uint16 [K/8][M][8], box 8 x NP x 32
   const __nv_bfloat16* x; // [M][K]
   __nv_bfloat16* y;       // [M][N]
   int M, N, K, slices;    // slices = K / 256
   int tiles, S, sps;      // row tiles, K splits, slices per split
   int units;              // tiles * S
-  int nst, stage_bytes, off_x, off_b;
+  int nst, stage_bytes, off_b;
+  int xrows;              // activation rows loaded per K block: M rounded up to 8
   float* ws_partial;      // [slices][M][N] under split-K
   int* ws_count;          // [tiles]
   int32_t* status;
@@ -90,18 +92,28 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tma
       : "memory");
 }
 
-// bf16 pairs (c - 8) of one packed word, pair order (code 0, 4), (1, 5),
-// (2, 6), (3, 7): (0x4300 | c) is bf16 128 + c, minus 136 gives c - 8.
+// 3-D tiled TMA load of box (x, y, z) of `tmap` into shared memory at `dst`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tmap, int x, int y, int z,
+                                            uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::"
+      "cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(pol)
+      : "memory");
+}
+
+// bf16 pairs (c - 8) of one packed word, codes (0, 1), (2, 3), (4, 5),
+// (6, 7): byte i of the word and byte i of the word shifted right by 4 go to
+// bytes 0 and 2, so codes 2i and 2i + 1 sit in bits 0-3 and 16-19; under
+// the bf16 pattern 0x4300 that is 128 + c, minus 136 gives c - 8 (exact).
 __device__ __forceinline__ void unpack_bf16(uint32_t wd, uint32_t out[4]) {
   const __nv_bfloat162 k136 = __halves2bfloat162(__ushort_as_bfloat16(0x4308), __ushort_as_bfloat16(0x4308));
-  uint32_t t[4];
-  t[0] = and_or(wd, 0x000F000Fu, 0x43004300u);
-  t[1] = and_or(wd >> 4, 0x000F000Fu, 0x43004300u);
-  t[2] = and_or(wd >> 8, 0x000F000Fu, 0x43004300u);
-  t[3] = and_or(wd >> 12, 0x000F000Fu, 0x43004300u);
+  const uint32_t hi = wd >> 4;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    __nv_bfloat162 v = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&t[i]), k136);
+    const uint32_t b = __byte_perm(wd, hi, (uint32_t)(i | (i << 4) | ((4 + i) << 8) | (i << 12)));
+    uint32_t t = and_or(b, 0x000F000Fu, 0x43004300u);
+    __nv_bfloat162 v = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&t), k136);
     out[i] = *reinterpret_cast<uint32_t*>(&v);
   }
 }
@@ -186,6 +198,15 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// Wait for this thread's tensor-memory loads; the empty asm statements make
+// the N loaded values depend on the wait, so no use moves above it.
+template <int N>
+__device__ __forceinline__ void tmem_wait_ld(float* d) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+f"(d[i]));
+}
+
 // D[128 x NP] (= or +=) A[128 x 16] (tensor memory) . B[16 x NP] (shared).
 __device__ __forceinline__ void mma_f16(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc,
                                         uint32_t accumulate) {
@@ -202,19 +223,13 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                : "memory");
 }
 
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t d;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-  return d;
-}
-
 // MMA width (activation columns, 16 or 32) and groups per round for MC
 // columns of results.
 __host__ __device__ constexpr int np_of(int mc) { return mc <= 16 ? 16 : 32; }
 __host__ __device__ constexpr int g_of(int mc) { return np_of(mc) == 16 ? 4 : 2; }
-// Columns of tensor memory the kernel allocates (A and D, double-buffered).
+// Columns of tensor memory the kernel allocates (A and D of kBufs rounds).
 __host__ __device__ constexpr int tmem_cols(int np, int g) {
-  return 2 * g * (16 + np) <= 128 ? 128 : 256;
+  return kBufs * g * (16 + np) <= 128 ? 128 : 256;
 }
 
 // MC: result columns read back (a power of two >= M, <= 32).
@@ -224,20 +239,25 @@ __global__ void __launch_bounds__(kThreads, 2) tc_kernel(const __grid_constant__
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   constexpr int NP = np_of(MC), G = g_of(MC);
   constexpr int kCols = tmem_cols(NP, G);
-  constexpr int kACol = 0;                 // A buffers: [2][G][16 columns]
-  constexpr int kDCol = 2 * G * 16;        // D buffers: [2][G][NP columns]
-  constexpr uint32_t kLBO = NP * 16;       // bytes between K-adjacent core matrices of B
+  constexpr int kACol = 0;                 // A buffers: [kBufs][G][16 columns]
+  constexpr int kDCol = kBufs * G * 16;    // D buffers: [kBufs][G][NP columns]
+  // bytes between K-adjacent core matrices of B: the loaded rows (M rounded
+  // up to 8).  Rows past them that the MMA's N reads belong to the next K
+  // block (or to the stage's spare bytes); they only reach result columns
+  // past M, which are never read.
+  const uint32_t lbo = (uint32_t)p.xrows * 16;
   constexpr int kRounds = kSliceGroups / G;
+  constexpr bool kEarly = G * MC <= 32;   // read-back loads issued before unpacking
   // instruction descriptor: D fp32, A and B bf16, both K-major, N = NP, M = 128
   constexpr uint32_t kIdesc =
       (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NP >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t base = smem_addr(smem_raw);
-  const uint32_t full0 = base, empty0 = base + 32, aready0 = base + 64, dready0 = base + 80;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + 96);
-  volatile int* last_flag = reinterpret_cast<volatile int*>(smem_raw + 100);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + 104);
+  const uint32_t full0 = base, empty0 = base + 32, aready0 = base + 64, dready0 = base + 96;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + 128);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(smem_raw + 132);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + 136);
   // stages start at the first 1024-byte boundary past the barriers
   const uint32_t st0 = (base + kBarBytes + 1023) & ~1023u;
   uint8_t* st0_ptr = smem_raw + (st0 - base);
@@ -248,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_kernel(const __grid_constant__
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, kDequantWarps);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kBufs; ++b) {
       mbar_init(aready0 + 8 * b, kDequantWarps);
       mbar_init(dready0 + 8 * b, 1);
     }
@@ -262,12 +282,6 @@ __global__ void __launch_bounds__(kThreads, 2) tc_kernel(const __grid_constant__
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  // B operands: activation rows past M stay zero for the whole launch
-  for (int s = 0; s < nst; ++s) {
-    uint4* b = reinterpret_cast<uint4*>(st0_ptr + s * p.stage_bytes + p.off_b);
-    for (int i = threadIdx.x; i < NP * kSliceK * 2 / 16; i += kThreads) b[i] = make_uint4(0, 0, 0, 0);
-  }
-  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -297,16 +311,13 @@ __global__ void __launch_bounds__(kThreads, 2) tc_kernel(const __grid_constant__
         const uint32_t stg = st0 + slot * p.stage_bytes;
         if (lane == 0) {
           mbar_arrive_expect_tx(full0 + 8 * slot,
-                                (uint32_t)(kCodesBytes + kStepsBytes + p.M * kSliceK * 2));
+                                (uint32_t)(kCodesBytes + kStepsBytes + p.xrows * kSliceK * 2));
           tma_load_2d(stg, &p.tm_codes, sl * (kSliceK / 2), t * kRows, full0 + 8 * slot, pol);
           tma_load_2d(stg + kCodesBytes, &p.tm_steps, sl * kSliceGroups, t * kRows,
                       full0 + 8 * slot, pol);
         }
+        if (lane == 0) tma_load_3d(stg + p.off_b, &p.tm_x, 0, 0, sl * (kSliceK / 8), full0 + 8 * slot, pol);
         __syncwarp();
-        if (lane < p.M)
-          bulk_g2s(stg + p.off_x + lane * kSliceK * 2,
-                   p.x + (long long)lane * p.K + (long long)sl * kSliceK, kSliceK * 2,
-                   full0 + 8 * slot);
         ++issued;
         if (++slot == nst) {
           slot = 0;
@@ -351,9 +362,9 @@ __global__ void __launch_bounds__(kThreads, 2) tc_kernel(const __grid_constant__
               const int grp = r * G + g;
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
-                const uint32_t baddr = stg + p.off_b + (uint32_t)(4 * grp + 2 * h) * kLBO;
+                const uint32_t baddr = stg + p.off_b + (uint32_t)(4 * grp + 2 * h) * lbo;
                 const uint64_t bdesc = (uint64_t)((baddr >> 4) & 0x3FFF) |
-                                       ((uint64_t)((kLBO >> 4) & 0x3FFF) << 16) |
+                                       ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
                                        ((uint64_t)(128 >> 4) << 32) | (1ull << 46);
                 mma_f16(tmem + kDCol + (rbuf * G + g) * NP, tmem + kACol + (rbuf * G + g) * 16 + h * 8,
                         bdesc, kIdesc, (uint32_t)h);
@@ -363,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_kernel(const __grid_constant__
           }
           __syncwarp();
           ++committed;
-          rbuf ^= 1;
+          if (++rbuf == kBufs) rbuf = 0;
         }
         if (++slot == nst) slot = 0;
       }
@@ -374,57 +385,22 @@ __global__ void __launch_bounds__(kThreads, 2) tc_kernel(const __grid_constant__
     }
     // the last commit must land before the tensor memory is released
     if (committed > 0) {
-      const int lb = rbuf ^ 1;
+      const int lb = rbuf == 0 ? kBufs - 1 : rbuf - 1;
       // aready completions of buffer lb so far equal its dready completions
       mbar_wait_bounded(dready0 + 8 * lb, ((aphase >> lb) & 1u) ^ 1u, kWaitCycles);
     }
   } else {
     // ----------------------------------------------------------- consumers
+    // Rounds are unpacked up to kBufs - 1 ahead of their read-back, so the
+    // MMAs of a round run while the warps unpack the next ones.
     const int tid = threadIdx.x;                       // weight row within the tile
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    int slot = 0;
+    int slot = 0;                                      // stage being unpacked
     uint32_t phase = 0;
     uint32_t dphase = 0;                               // bit b: phase of dready[b]
-    int rbuf = 0;                                      // tensor-memory buffer of this round
-    // the previous round, whose dot products are read back in this round
-    bool prev = false, prev_last = false;
-    int prev_buf = 0, prev_slot = 0, prev_sl = 0, prev_row = 0;
-    float prev_st[G];
+    int ubuf = 0, ebuf = 0;                            // buffers of the next round to unpack / read back
     float acc[MC], rowsum[MC];
     bool ok = true;
-
-    // Read back round `prev`'s group dot products and fold them into acc.
-    // When that round was its slice's last, the slice sum is complete: it
-    // goes to the row sum (or to the workspace under split-K) and the stage
-    // goes back to the copy warp.
-    auto epilogue = [&]() -> bool {
-      if (!wait_bar(dready0 + 8 * prev_buf, (dphase >> prev_buf) & 1u, abort_flag)) return false;
-      dphase ^= 1u << prev_buf;
-      tc_fence_after();
-      float d[G][MC];
-#pragma unroll
-      for (int g = 0; g < G; ++g) tmem_ld<MC>(tmem + lane_base + kDCol + (prev_buf * G + g) * NP, d[g]);
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-      for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int m = 0; m < MC; ++m) acc[m] = fmaf(prev_st[g], d[g][m], acc[m]);
-      if (prev_last) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty0 + 8 * prev_slot);
-        if (p.S == 1) {
-#pragma unroll
-          for (int m = 0; m < MC; ++m) rowsum[m] += acc[m];
-        } else if (prev_row < p.N) {
-#pragma unroll
-          for (int m = 0; m < MC; ++m)
-            if (m < p.M) p.ws_partial[((long long)prev_sl * p.M + m) * p.N + prev_row] = acc[m];
-        }
-#pragma unroll
-        for (int m = 0; m < MC; ++m) acc[m] = 0.0f;
-      }
-      return true;
-    };
 
     for (int u = u0; u < u1 && ok; ++u) {
       const int s = u / p.tiles, t = u - s * p.tiles;
@@ -435,55 +411,97 @@ __global__ void __launch_bounds__(kThreads, 2) tc_kernel(const __grid_constant__
         rowsum[m] = 0.0f;
         acc[m] = 0.0f;
       }
+      // read-back cursor: slice esl in stage eslot, its group er0; pend
+      // rounds unpacked and not yet read back
+      int esl = sl0, eslot = slot, er0 = 0, pend = 0;
+
+      // Read-back of the oldest pending round, in two parts: `fetch` waits
+      // for its MMAs and starts the tensor-memory loads of its group dot
+      // products; `fold` (after the loads land) adds step * dot to acc.  A
+      // slice's last round completes its sum (to the row sum, or to the
+      // workspace under split-K) and returns its stage to the copy warp.
+      float d[G][MC];
+      float stv[kSliceGroups];   // steps of this row in the slice being read back
+      auto fetch = [&]() -> bool {
+        if (!wait_bar(dready0 + 8 * ebuf, (dphase >> ebuf) & 1u, abort_flag)) return false;
+        dphase ^= 1u << ebuf;
+        tc_fence_after();
+#pragma unroll
+        for (int g = 0; g < G; ++g) tmem_ld<MC>(tmem + lane_base + kDCol + (ebuf * G + g) * NP, d[g]);
+        return true;
+      };
+      auto fold = [&]() {
+        if (er0 == 0) {   // the row's 8 steps of the slice, one 16-byte load
+          const uint4 sv =
+              *reinterpret_cast<const uint4*>(st0_ptr + eslot * p.stage_bytes + kCodesBytes + tid * 16);
+          const uint32_t w[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+          for (int j = 0; j < kSliceGroups; ++j) stv[j] = bf16_bits_to_float((w[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+        }
+        tmem_wait_ld<G * MC>(&d[0][0]);
+        const int q = er0 / G;   // round of the slice
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float sg = stv[g];
+#pragma unroll
+          for (int r = 1; r < kRounds; ++r) sg = q == r ? stv[r * G + g] : sg;
+#pragma unroll
+          for (int m = 0; m < MC; ++m) acc[m] = fmaf(sg, d[g][m], acc[m]);
+        }
+        if (++ebuf == kBufs) ebuf = 0;
+        --pend;
+        er0 += G;
+        if (er0 == kSliceGroups) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty0 + 8 * eslot);
+          if (p.S == 1) {
+#pragma unroll
+            for (int m = 0; m < MC; ++m) rowsum[m] += acc[m];
+          } else if (row < p.N) {
+#pragma unroll
+            for (int m = 0; m < MC; ++m)
+              if (m < p.M) p.ws_partial[((long long)esl * p.M + m) * p.N + row] = acc[m];
+          }
+#pragma unroll
+          for (int m = 0; m < MC; ++m) acc[m] = 0.0f;
+          er0 = 0;
+          ++esl;
+          if (++eslot == nst) eslot = 0;
+        }
+      };
+
       for (int sl = sl0; sl < sl1 && ok; ++sl) {
         if (!wait_bar(full0 + 8 * slot, phase, abort_flag)) {
           ok = false;
           break;
         }
         uint8_t* stg_ptr = st0_ptr + slot * p.stage_bytes;
-        // activations of the slice -> B operand, each 8-code block in the
-        // unpacked pair order (0, 4, 1, 5, 2, 6, 3, 7); blocks dealt over all
-        // four warps
-        for (int q = lane * kDequantWarps + warp; q < p.M * (kSliceK / 8); q += kRows) {
-          const int m = q / (kSliceK / 8), kb = q - m * (kSliceK / 8);
-          const uint4 v = *reinterpret_cast<const uint4*>(stg_ptr + p.off_x + m * kSliceK * 2 + kb * 16);
-          uint4 o;
-          o.x = prmt(v.x, v.z, 0x5410);
-          o.y = prmt(v.x, v.z, 0x7632);
-          o.z = prmt(v.y, v.w, 0x5410);
-          o.w = prmt(v.y, v.w, 0x7632);
-          *reinterpret_cast<uint4*>(stg_ptr + p.off_b + kb * kLBO + (m >> 3) * 128 + (m & 7) * 16) = o;
-        }
-        fence_proxy_async_smem();
         for (int r0 = 0; r0 < kSliceGroups; r0 += G) {
+          // with kBufs - 1 rounds pending, the oldest is read back around
+          // this round's unpacking: its loads are in flight meanwhile (when
+          // its dot products fit the registers beside the unpacking)
+          const bool back = pend == kBufs - 1;
+          if (kEarly && back && !(ok = fetch())) break;
           // unpack this round's groups into tensor memory
-          float st[G];
 #pragma unroll
           for (int g = 0; g < G; ++g) {
             const int grp = r0 + g;
             const uint4 q = *reinterpret_cast<const uint4*>(stg_ptr + tid * 128 + ((grp ^ (tid & 7)) << 4));
-            st[g] = bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(stg_ptr + kCodesBytes + tid * 16 + grp * 2));
             uint32_t a[16];
             unpack_bf16(q.x, a);
             unpack_bf16(q.y, a + 4);
             unpack_bf16(q.z, a + 8);
             unpack_bf16(q.w, a + 12);
-            tmem_st16(tmem + lane_base + kACol + (rbuf * G + g) * 16, a);
+            tmem_st16(tmem + lane_base + kACol + (ubuf * G + g) * 16, a);
           }
+          if (!kEarly && back && !(ok = fetch())) break;
+          if (back) fold();   // frees the oldest round's buffers for later rounds
           asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(aready0 + 8 * rbuf);   // this warp's rows are in
-          if (prev && !(ok = epilogue())) break;
-          prev = true;
-          prev_buf = rbuf;
-          prev_slot = slot;
-          prev_sl = sl;
-          prev_row = row;
-          prev_last = r0 + G >= kSliceGroups;
-#pragma unroll
-          for (int g = 0; g < G; ++g) prev_st[g] = st[g];
-          rbuf ^= 1;
+          if (lane == 0) mbar_arrive(aready0 + 8 * ubuf);   // this warp's rows are in
+          if (++ubuf == kBufs) ubuf = 0;
+          ++pend;
         }
         if (!ok) break;
         if (++slot == nst) {
@@ -491,10 +509,10 @@ __global__ void __launch_bounds__(kThreads, 2) tc_kernel(const __grid_constant__
           phase ^= 1u;
         }
       }
-      // the unit's last round is read back before its rows are finished
-      if (ok && prev) {
-        ok = epilogue();
-        prev = false;
+      // the unit's pending rounds are read back before its rows are finished
+      while (ok && pend > 0) {
+        if (!(ok = fetch())) break;
+        fold();
       }
       if (!ok) break;
       if (p.S == 1) {
@@ -568,9 +586,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return fn;
 }
 
-int stage_bytes_of(int M, int np, int* off_x, int* off_b) {
-  *off_x = kCodesBytes + kStepsBytes;
-  *off_b = (*off_x + M * kSliceK * 2 + 127) & ~127;
+// Stage: codes (16 KB, 1024-aligned for the swizzle), steps (2 KB), then the
+// B operand (np x 256 bf16).
+int stage_bytes_of(int np, int* off_b) {
+  *off_b = kCodesBytes + kStepsBytes;
   return (*off_b + np * kSliceK * 2 + 1023) & ~1023;
 }
 
@@ -645,9 +664,8 @@ bool tc_plan(int M, int N, int K, int sms, TcPlan* out) {
   pl.S = (pl.slices + pl.sps - 1) / pl.sps;
   pl.units = pl.tiles * pl.S;
   pl.ctas = std::min(pl.units, target);
-  int off_x, off_b;
-  pl.stage_bytes = stage_bytes_of(M, pl.np, &off_x, &off_b);
-  pl.off_x = off_x;
+  int off_b;
+  pl.stage_bytes = stage_bytes_of(pl.np, &off_b);
   pl.off_b = off_b;
   // two CTAs per SM: each keeps under half of the 228 KB of shared memory
   const int budget = 232448 / 2 - 1024;
@@ -688,6 +706,19 @@ cudaError_t tc_launch(const TcPlan& pl, void* y, const void* qw, const void* st,
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
+  {
+    // x [M][K] seen as (8 codes, M rows, K/8 blocks): a slice's box lands as
+    // [block][row][8] = the K-major core-matrix layout of the B operand
+    // (rows M .. xrows - 1 out of range, read as zeros)
+    const cuuint64_t dims[3] = {8, (cuuint64_t)M, (cuuint64_t)K / 8};
+    const cuuint64_t strides[2] = {(cuuint64_t)K * 2, 16};
+    const cuuint32_t box[3] = {8, (cuuint32_t)((M + 7) & ~7), kSliceK / 8};
+    const cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&p.tm_x, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(x), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.y = static_cast<__nv_bfloat16*>(y);
   p.M = M;
@@ -700,8 +731,8 @@ cudaError_t tc_launch(const TcPlan& pl, void* y, const void* qw, const void* st,
   p.units = pl.units;
   p.nst = pl.nst;
   p.stage_bytes = pl.stage_bytes;
-  p.off_x = pl.off_x;
   p.off_b = pl.off_b;
+  p.xrows = (M + 7) & ~7;
   p.status = status;
   if (pl.S > 1) {
     p.ws_count = static_cast<int*>(workspace);
