@@ -10,9 +10,9 @@
 //  * A CTA owns tiles of 128 weight rows (the MMA's M).  A copy warp streams
 //    each (tile, 256-code K slice) stage into a shared-memory ring: the codes
 //    as one 2-D TMA box with 128-byte swizzle (16 KB), the steps as one 2-D
-//    box (2 KB), and the activation rows of the slice (M rounded up to 8)
-//    as one 3-D box that lands directly in the B-operand layout (bf16,
-//    K-major 8x8 core matrices).
+//    box (2 KB), and the M activation rows of the slice as one 3-D box that
+//    lands directly in the B-operand layout (bf16, K-major 8x8 core
+//    matrices, 16-byte rows, K blocks M rows apart).
 //  * Four warps (thread = weight row) turn each packed word into four bf16
 //    pairs (c - 8) of consecutive codes with the page's float-bit trick in
 //    bf16 form ((0x4300 | c) - 136 = c - 8, exact) and store them into
@@ -64,7 +64,7 @@ struct TcParams {
   int tiles, S, sps;      // row tiles, K splits, slices per split
   int units;              // tiles * S
   int nst, stage_bytes, off_b;
-  int xrows;              // activation rows loaded per K block: M rounded up to 8
+  int xrows;              // activation rows loaded per K block (M)
   float* ws_partial;      // [slices][M][N] under split-K
   int* ws_count;          // [tiles]
   int32_t* status;
@@ -241,10 +241,10 @@ __global__ void __launch_bounds__(kThreads, 2) tc_kernel(const __grid_constant__
   constexpr int kCols = tmem_cols(NP, G);
   constexpr int kACol = 0;                 // A buffers: [kBufs][G][16 columns]
   constexpr int kDCol = kBufs * G * 16;    // D buffers: [kBufs][G][NP columns]
-  // bytes between K-adjacent core matrices of B: the loaded rows (M rounded
-  // up to 8).  Rows past them that the MMA's N reads belong to the next K
-  // block (or to the stage's spare bytes); they only reach result columns
-  // past M, which are never read.
+  // bytes between K-adjacent core matrices of B: the M loaded rows.  Rows
+  // past M that the MMA's N reads belong to the next K block (or to the
+  // stage's spare bytes); they only reach result columns past M, which are
+  // never read.
   const uint32_t lbo = (uint32_t)p.xrows * 16;
   constexpr int kRounds = kSliceGroups / G;
   constexpr bool kEarly = G * MC <= 32;   // read-back loads issued before unpacking
@@ -709,10 +709,9 @@ cudaError_t tc_launch(const TcPlan& pl, void* y, const void* qw, const void* st,
   {
     // x [M][K] seen as (8 codes, M rows, K/8 blocks): a slice's box lands as
     // [block][row][8] = the K-major core-matrix layout of the B operand
-    // (rows M .. xrows - 1 out of range, read as zeros)
     const cuuint64_t dims[3] = {8, (cuuint64_t)M, (cuuint64_t)K / 8};
     const cuuint64_t strides[2] = {(cuuint64_t)K * 2, 16};
-    const cuuint32_t box[3] = {8, (cuuint32_t)((M + 7) & ~7), kSliceK / 8};
+    const cuuint32_t box[3] = {8, (cuuint32_t)M, kSliceK / 8};
     const cuuint32_t es[3] = {1, 1, 1};
     if (enc(&p.tm_x, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(x), dims, strides, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -732,7 +731,7 @@ cudaError_t tc_launch(const TcPlan& pl, void* y, const void* qw, const void* st,
   p.nst = pl.nst;
   p.stage_bytes = pl.stage_bytes;
   p.off_b = pl.off_b;
-  p.xrows = (M + 7) & ~7;
+  p.xrows = M;
   p.status = status;
   if (pl.S > 1) {
     p.ws_count = static_cast<int*>(workspace);
