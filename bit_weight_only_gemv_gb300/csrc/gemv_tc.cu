@@ -532,16 +532,26 @@ __global__ void __launch_bounds__(kThreads, 2) tc_kernel(const __grid_constant__
       asm volatile("bar.sync 1, %0;" ::"n"(kRows) : "memory");
       if (*last_flag) {
         if (row < p.N) {
-          // slice by slice, all activation rows' partials in flight at once
+          // kBatch slices at a time, all their partials in flight at once,
+          // then added in slice order
+          constexpr int kBatch = MC <= 8 ? 8 : (MC <= 16 ? 4 : 2);
 #pragma unroll
           for (int m = 0; m < MC; ++m) rowsum[m] = 0.0f;
-          for (int sl = 0; sl < p.slices; ++sl) {
-            float v[MC];
+          for (int sl0 = 0; sl0 < p.slices; sl0 += kBatch) {
+            float v[kBatch][MC];
 #pragma unroll
-            for (int m = 0; m < MC; ++m)
-              v[m] = m < p.M ? __ldcg(p.ws_partial + ((long long)sl * p.M + m) * p.N + row) : 0.0f;
+            for (int b = 0; b < kBatch; ++b)
 #pragma unroll
-            for (int m = 0; m < MC; ++m) rowsum[m] += v[m];
+              for (int m = 0; m < MC; ++m)
+                v[b][m] = (sl0 + b < p.slices && m < p.M)
+                              ? __ldcg(p.ws_partial + ((long long)(sl0 + b) * p.M + m) * p.N + row)
+                              : 0.0f;
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b)
+              if (sl0 + b < p.slices) {
+#pragma unroll
+                for (int m = 0; m < MC; ++m) rowsum[m] += v[b][m];
+              }
           }
 #pragma unroll
           for (int m = 0; m < MC; ++m)
