@@ -48,6 +48,7 @@
 //    warps leave without further waiting, and the producer lets its copies
 //    in flight land (bounded) before the CTA exits.
 #include <algorithm>
+#include <cmath>
 #include <mutex>
 
 #include "common.cuh"
@@ -969,8 +970,28 @@ bool make_plan(int MR, int N, int K, int n_items, int allow_split, int x_per_ite
   const long long rows_total = (long long)n_items * N;
   if (rows_total > (1LL << 40)) return false;
   const long long weight_bytes = rows_total * ((long long)K / 2 + Kg * 2);
-  // Two CTAs per SM for large problems; one otherwise, which leaves room for
-  // the next launch's CTA to start streaming its weights (W4_FLAG_PDL).
+  // Two CTAs per SM for large problems.  For smaller ones, one CTA per SM
+  // leaves room for the next launch's CTA to start streaming its weights
+  // (W4_FLAG_PDL), two shorten each CTA's share: take two unless that pads
+  // the CTAs' last windows more (rows a CTA's windows could hold over the
+  // rows it has).
+  if (force_per_sm == 0 && weight_bytes < (16LL << 20) && min_ctas(MR, 1) == 2) {
+    Plan one, two;
+    const bool ok1 = make_plan(MR, N, K, n_items, allow_split, x_per_item, routed, di, &one, 1);
+    const bool ok2 = make_plan(MR, N, K, n_items, allow_split, x_per_item, routed, di, &two, 2);
+    if (!ok1 || !ok2) {
+      if (!ok1 && !ok2) return false;
+      *out = ok1 ? one : two;
+      return true;
+    }
+    auto padding = [](const Plan& q) {
+      const double rows = (double)q.U / q.ctas;   // rows (or units) per CTA
+      const double win = q.S == 1 ? q.RB : 1.0;
+      return std::ceil(rows / win) * win / rows;
+    };
+    *out = (two.per_sm == 2 && padding(two) <= 1.05 * padding(one)) ? two : one;
+    return true;
+  }
   pl.per_sm = (weight_bytes >= (16LL << 20)) ? min_ctas(MR, 1) : 1;
   if (force_per_sm > 0) pl.per_sm = force_per_sm;
   // shared memory a CTA may take and still leave room for a second one
