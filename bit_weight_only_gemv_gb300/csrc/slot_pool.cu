@@ -1,5 +1,5 @@
-// Per-layer expert slot pool (host C++), plus the tiny kernel that publishes
-// the slot ids to the device.
+// Per-layer expert slot pool (host C++), plus the kernels that load missed
+// experts into their slots and publish the slot ids to the device.
 //
 // Page "Running a 26B MoE on an 8 GB Jetson by streaming experts from SSD",
 // section "Streaming without touching a single GPU kernel": a persistent pool
@@ -40,6 +40,42 @@ struct IdList {
 __global__ void write_ids_kernel(int32_t* dst, IdList ids, int k) {
   const int i = threadIdx.x;
   if (i < k) dst[i] = ids.v[i];
+}
+
+// One launch that loads a request's missed experts into their slots (codes
+// and steps, 16 bytes per thread step) and writes the request's slot ids.
+struct FillParams {
+  uint8_t* pool_qw;
+  const uint8_t* full_qw;
+  uint8_t* pool_st;
+  const uint8_t* full_st;
+  unsigned long long qw_stride, st_stride;   // bytes between experts / slots
+  unsigned long long qw_units, st_units;     // 16-byte units per expert
+  int32_t* slot_ids_dev;
+  int n_miss, k;
+  int32_t miss_expert[64], miss_slot[64];
+  int32_t ids[64];
+};
+
+__global__ void __launch_bounds__(256) pool_fill_kernel(const __grid_constant__ FillParams p) {
+  if (blockIdx.x == 0 && threadIdx.x < p.k) p.slot_ids_dev[threadIdx.x] = p.ids[threadIdx.x];
+  const unsigned long long per = p.qw_units + p.st_units;
+  const unsigned long long total = per * (unsigned long long)p.n_miss;
+  for (unsigned long long u = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; u < total;
+       u += (unsigned long long)gridDim.x * blockDim.x) {
+    const int m = (int)(u / per);
+    const unsigned long long r = u - (unsigned long long)m * per;
+    const unsigned long long e = (unsigned long long)p.miss_expert[m];
+    const unsigned long long sl = (unsigned long long)p.miss_slot[m];
+    if (r < p.qw_units) {
+      reinterpret_cast<uint4*>(p.pool_qw + sl * p.qw_stride)[r] =
+          __ldcs(reinterpret_cast<const uint4*>(p.full_qw + e * p.qw_stride) + r);
+    } else {
+      const unsigned long long q = r - p.qw_units;
+      reinterpret_cast<uint4*>(p.pool_st + sl * p.st_stride)[q] =
+          __ldcs(reinterpret_cast<const uint4*>(p.full_st + e * p.st_stride) + q);
+    }
+  }
 }
 
 namespace {
@@ -155,6 +191,45 @@ extern "C" w4_status w4_slot_pool_stage(w4_slot_pool* pool, const int32_t* exper
   if (st != W4_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   bool failed = false;
+  // all 16-byte aligned: one kernel loads the misses and writes the slot ids
+  const auto a16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; };
+  if (a16(pool_qw) && a16(full_qw) && a16(pool_st) && a16(full_st) && qw_stride_bytes % 16 == 0 &&
+      st_stride_bytes % 16 == 0 && qw_expert_bytes % 16 == 0 && st_expert_bytes % 16 == 0) {
+    FillParams fp = {};
+    fp.pool_qw = static_cast<uint8_t*>(pool_qw);
+    fp.full_qw = static_cast<const uint8_t*>(full_qw);
+    fp.pool_st = static_cast<uint8_t*>(pool_st);
+    fp.full_st = static_cast<const uint8_t*>(full_st);
+    fp.qw_stride = qw_stride_bytes;
+    fp.st_stride = st_stride_bytes;
+    fp.qw_units = qw_expert_bytes / 16;
+    fp.st_units = st_expert_bytes / 16;
+    fp.slot_ids_dev = slot_ids_dev;
+    fp.n_miss = (int)misses.size();
+    fp.k = k;
+    for (int i = 0; i < fp.n_miss; ++i) {
+      fp.miss_expert[i] = misses[i].first;
+      fp.miss_slot[i] = misses[i].second;
+    }
+    std::copy(list.v, list.v + k, fp.ids);
+    const unsigned long long total = (fp.qw_units + fp.st_units) * (unsigned long long)fp.n_miss;
+    const int blocks = (int)std::max(1ULL, std::min(1024ULL, (total + 255) / 256));
+    pool_fill_kernel<<<blocks, 256, 0, s>>>(fp);
+    failed = cudaPeekAtLastError() != cudaSuccess;
+    if (failed) {
+      note_cuda_error(cudaGetLastError());
+      for (const auto& m : misses) {
+        if (pool->expert_in_slot[m.second] == m.first) {
+          pool->expert_in_slot[m.second] = -1;
+          pool->slot_of_expert[m.first] = -1;
+        }
+      }
+      return W4_ERR_STATE;
+    }
+    if (slot_ids) std::copy(list.v, list.v + k, slot_ids);
+    if (n_miss) *n_miss = (int)misses.size();
+    return W4_OK;
+  }
   for (const auto& m : misses) {
     const size_t e = (size_t)m.first, slot = (size_t)m.second;
     if (cudaMemcpyAsync(static_cast<uint8_t*>(pool_qw) + slot * qw_stride_bytes,

@@ -301,13 +301,15 @@ w4_status w4_slot_pool_remap(w4_slot_pool *pool, const int32_t *expert_ids, int 
                              int *n_miss);
 
 /*
- * Remap one request and stage it on `stream`: one cudaMemcpyAsync per missed
- * expert for its codes (qw_expert_bytes from full_qw + e*qw_stride to
- * pool_qw + s*qw_stride) and one for its steps (likewise with st_*), then a
- * tiny kernel that writes the k slot ids into slot_ids_dev (device int32
- * [k], k <= 64).  If any copy fails to enqueue, the experts of this request
- * that were being loaded are dropped from the pool (their slots become free)
- * and W4_ERR_STATE is returned, so stale slot contents are never used.
+ * Remap one request and stage it on `stream`: each missed expert's codes
+ * (qw_expert_bytes from full_qw + e*qw_stride to pool_qw + s*qw_stride) and
+ * steps (likewise with st_*) are copied into its slot and the k slot ids are
+ * written into slot_ids_dev (device int32 [k], k <= 64).  When every pointer,
+ * stride and size is a multiple of 16 bytes, one kernel launch does all of
+ * it; otherwise one cudaMemcpyAsync per copy, then a tiny kernel for the ids.
+ * If any of it fails to enqueue, the experts of this request that were being
+ * loaded are dropped from the pool (their slots become free) and
+ * W4_ERR_STATE is returned, so stale slot contents are never used.
  * slot_ids / n_miss (host, optional, may be NULL) receive the remap.
  */
 w4_status w4_slot_pool_stage(w4_slot_pool *pool, const int32_t *expert_ids, int k,
