@@ -1400,7 +1400,7 @@ extern "C" w4_status w4a16_gemv_plan(int M, int N, int K, w4_plan_info* info) {
     info->path = 2;
     info->ctas = tp.ctas;
     info->slices = tp.S;
-    info->threads = 160;
+    info->threads = 320;   // 4 unpacking, 4 folding, copy and MMA warps
     info->team = 1;
     info->unit_rows = 128;
     info->chunk_groups = 8;

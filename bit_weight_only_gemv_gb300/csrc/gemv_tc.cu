@@ -45,11 +45,14 @@ namespace tc {
 constexpr int kRows = 128;          // weight rows per tile = MMA M
 constexpr int kSliceK = 256;        // codes per row per stage
 constexpr int kSliceGroups = 8;     // 32-code groups per stage
-constexpr int kDequantWarps = 4;
-constexpr int kThreads = 32 * (kDequantWarps + 2);   // + copy warp + MMA warp
+constexpr int kUnpackWarps = 4;     // one weight row per thread
+constexpr int kFoldWarps = 4;       // one weight row per thread
+constexpr int kCopyWarp = kUnpackWarps + kFoldWarps;
+constexpr int kMmaWarp = kCopyWarp + 1;
+constexpr int kThreads = 32 * (kMmaWarp + 1);
 constexpr int kMaxStages = 4;
 constexpr int kBufs = 2;            // rounds of A and D held in tensor memory
-constexpr int kBarBytes = 192;      // full[4], empty[4], aready[4], dready[4], flags, tmem base
+constexpr int kBarBytes = 192;      // full[4], empty[4], aready/afree/dready/dfree[2], flags, tmem base
 constexpr int kCodesBytes = kRows * 128;   // 16 KB, 1024-byte aligned (128-byte swizzle)
 constexpr int kStepsBytes = kRows * 16;    // 2 KB
 constexpr long long kWaitCycles = 1LL << 31;
@@ -233,7 +236,10 @@ __host__ __device__ constexpr int tmem_cols(int np, int g) {
 }
 
 // MC: result columns read back (a power of two >= M, <= 32).
-// Warps 0-3 unpack rows and fold results, warp 4 copies, warp 5 issues MMAs.
+// Warps 0-3 unpack codes into A, warps 4-7 read results back and fold them,
+// warp 8 copies, warp 9 issues MMAs.  Per round (G groups) the four roles
+// hand off through mbarriers: aready (A stored), dready / afree (MMAs done:
+// D ready, A free again), dfree (D read back).
 template <int MC>
 __global__ void __launch_bounds__(kThreads, 2) tc_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -241,20 +247,27 @@ __global__ void __launch_bounds__(kThreads, 2) tc_kernel(const __grid_constant__
   constexpr int kCols = tmem_cols(NP, G);
   constexpr int kACol = 0;                 // A buffers: [kBufs][G][16 columns]
   constexpr int kDCol = kBufs * G * 16;    // D buffers: [kBufs][G][NP columns]
+  constexpr int kRounds = kSliceGroups / G;
+  constexpr int kLdBatch = MC >= 16 ? 1 : (16 / MC < G ? 16 / MC : G);   // groups per read-back
+  // 32 columns: the row's running sum over slices lives in tensor memory
+  // (columns past A and D), which keeps the folding threads' registers for
+  // two CTAs per SM
+  constexpr bool kTmemSum = MC >= 32;
+  constexpr int kSumCol = kDCol + kBufs * G * NP;
+  static_assert(!kTmemSum || kSumCol + MC <= kCols, "tensor memory");
   // bytes between K-adjacent core matrices of B: the M loaded rows.  Rows
   // past M that the MMA's N reads belong to the next K block (or to the
   // stage's spare bytes); they only reach result columns past M, which are
   // never read.
   const uint32_t lbo = (uint32_t)p.xrows * 16;
-  constexpr int kRounds = kSliceGroups / G;
-  constexpr bool kEarly = G * MC <= 32;   // read-back loads issued before unpacking
   // instruction descriptor: D fp32, A and B bf16, both K-major, N = NP, M = 128
   constexpr uint32_t kIdesc =
       (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NP >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t base = smem_addr(smem_raw);
-  const uint32_t full0 = base, empty0 = base + 32, aready0 = base + 64, dready0 = base + 96;
+  const uint32_t full0 = base, empty0 = base + 32;
+  const uint32_t aready0 = base + 64, afree0 = base + 80, dready0 = base + 96, dfree0 = base + 112;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + 128);
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem_raw + 132);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + 136);
@@ -266,11 +279,13 @@ __global__ void __launch_bounds__(kThreads, 2) tc_kernel(const __grid_constant__
   if (threadIdx.x == 0) {
     for (int s = 0; s < nst; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, kDequantWarps);
+      mbar_init(empty0 + 8 * s, kFoldWarps);
     }
     for (int b = 0; b < kBufs; ++b) {
-      mbar_init(aready0 + 8 * b, kDequantWarps);
+      mbar_init(aready0 + 8 * b, kUnpackWarps);
+      mbar_init(afree0 + 8 * b, 1);
       mbar_init(dready0 + 8 * b, 1);
+      mbar_init(dfree0 + 8 * b, kFoldWarps);
     }
     *abort_flag = 0;
     mbar_init_fence();
@@ -292,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_kernel(const __grid_constant__
   const int u0 = (int)((long long)blockIdx.x * p.units / gridDim.x);
   const int u1 = (int)((long long)(blockIdx.x + 1) * p.units / gridDim.x);
 
-  if (warp == kDequantWarps) {
+  if (warp == kCopyWarp) {
     // ------------------------------------------------------------ producer
     const uint64_t pol = policy_evict_first();
     int slot = 0, issued = 0;
@@ -315,8 +330,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_kernel(const __grid_constant__
           tma_load_2d(stg, &p.tm_codes, sl * (kSliceK / 2), t * kRows, full0 + 8 * slot, pol);
           tma_load_2d(stg + kCodesBytes, &p.tm_steps, sl * kSliceGroups, t * kRows,
                       full0 + 8 * slot, pol);
+          tma_load_3d(stg + p.off_b, &p.tm_x, 0, 0, sl * (kSliceK / 8), full0 + 8 * slot, pol);
         }
-        if (lane == 0) tma_load_3d(stg + p.off_b, &p.tm_x, 0, 0, sl * (kSliceK / 8), full0 + 8 * slot, pol);
         __syncwarp();
         ++issued;
         if (++slot == nst) {
@@ -335,46 +350,45 @@ __global__ void __launch_bounds__(kThreads, 2) tc_kernel(const __grid_constant__
         break;
       }
     }
-  } else if (warp == kDequantWarps + 1) {
+  } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
-    // Walks the same rounds as the unpacking warps; a round's MMAs go out once
-    // all four warps have stored its A operands (which also means they have
-    // read back the results of the round that used the same buffers before).
-    int slot = 0, rbuf = 0;
-    uint32_t aphase = 0;                 // bit b: phase of aready[b]
-    int committed = 0;                   // rounds committed so far
+    // Round r uses buffers b = r % kBufs for the (u = r / kBufs)-th time: its
+    // MMAs go out once its A is stored and the D of use u - 1 has been read.
+    int slot = 0;
+    long long r = 0;
     bool ok = true;
     for (int u = u0; u < u1 && ok; ++u) {
       const int s = u / p.tiles;
       const int sl0 = s * p.sps, sl1 = min(sl0 + p.sps, p.slices);
       for (int sl = sl0; sl < sl1 && ok; ++sl) {
         const uint32_t stg = st0 + slot * p.stage_bytes;
-        for (int r = 0; r < kRounds; ++r) {
-          if (!wait_bar(aready0 + 8 * rbuf, (aphase >> rbuf) & 1u, abort_flag)) {
+        for (int q = 0; q < kRounds; ++q, ++r) {
+          const int b = (int)(r % kBufs);
+          const uint32_t use = (uint32_t)(r / kBufs);
+          if (!wait_bar(aready0 + 8 * b, use & 1u, abort_flag) ||
+              (use > 0 && !wait_bar(dfree0 + 8 * b, (use - 1) & 1u, abort_flag))) {
             ok = false;
             break;
           }
-          aphase ^= 1u << rbuf;
           tc_fence_after();
           if (lane == 0) {
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-              const int grp = r * G + g;
+              const int grp = q * G + g;
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
                 const uint32_t baddr = stg + p.off_b + (uint32_t)(4 * grp + 2 * h) * lbo;
                 const uint64_t bdesc = (uint64_t)((baddr >> 4) & 0x3FFF) |
                                        ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
                                        ((uint64_t)(128 >> 4) << 32) | (1ull << 46);
-                mma_f16(tmem + kDCol + (rbuf * G + g) * NP, tmem + kACol + (rbuf * G + g) * 16 + h * 8,
+                mma_f16(tmem + kDCol + (b * G + g) * NP, tmem + kACol + (b * G + g) * 16 + h * 8,
                         bdesc, kIdesc, (uint32_t)h);
               }
             }
-            mma_commit(dready0 + 8 * rbuf);
+            mma_commit(dready0 + 8 * b);
+            mma_commit(afree0 + 8 * b);
           }
           __syncwarp();
-          ++committed;
-          if (++rbuf == kBufs) rbuf = 0;
         }
         if (++slot == nst) slot = 0;
       }
@@ -383,143 +397,171 @@ __global__ void __launch_bounds__(kThreads, 2) tc_kernel(const __grid_constant__
       if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
       *abort_flag = 1;
     }
-    // the last commit must land before the tensor memory is released
-    if (committed > 0) {
-      const int lb = rbuf == 0 ? kBufs - 1 : rbuf - 1;
-      // aready completions of buffer lb so far equal its dready completions
-      mbar_wait_bounded(dready0 + 8 * lb, ((aphase >> lb) & 1u) ^ 1u, kWaitCycles);
+    // the last commits must land before the tensor memory is released
+    for (int b = 0; b < kBufs && r > 0; ++b) {
+      const long long uses = (r - b + kBufs - 1) / kBufs;   // rounds r' < r with r' % kBufs == b
+      if (uses > 0) mbar_wait_bounded(afree0 + 8 * b, (uint32_t)((uses - 1) & 1), kWaitCycles);
     }
-  } else {
-    // ----------------------------------------------------------- consumers
-    // Rounds are unpacked up to kBufs - 1 ahead of their read-back, so the
-    // MMAs of a round run while the warps unpack the next ones.
+  } else if (warp < kUnpackWarps) {
+    // -------------------------------------------------------- unpacking warps
     const int tid = threadIdx.x;                       // weight row within the tile
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    int slot = 0;                                      // stage being unpacked
+    int slot = 0;
     uint32_t phase = 0;
-    uint32_t dphase = 0;                               // bit b: phase of dready[b]
-    int ubuf = 0, ebuf = 0;                            // buffers of the next round to unpack / read back
-    float acc[MC], rowsum[MC];
+    long long r = 0;
     bool ok = true;
-
     for (int u = u0; u < u1 && ok; ++u) {
-      const int s = u / p.tiles, t = u - s * p.tiles;
+      const int s = u / p.tiles;
       const int sl0 = s * p.sps, sl1 = min(sl0 + p.sps, p.slices);
-      const int row = t * kRows + tid;
-#pragma unroll
-      for (int m = 0; m < MC; ++m) {
-        rowsum[m] = 0.0f;
-        acc[m] = 0.0f;
-      }
-      // read-back cursor: slice esl in stage eslot, its group er0; pend
-      // rounds unpacked and not yet read back
-      int esl = sl0, eslot = slot, er0 = 0, pend = 0;
-
-      // Read-back of the oldest pending round, in two parts: `fetch` waits
-      // for its MMAs and starts the tensor-memory loads of its group dot
-      // products; `fold` (after the loads land) adds step * dot to acc.  A
-      // slice's last round completes its sum (to the row sum, or to the
-      // workspace under split-K) and returns its stage to the copy warp.
-      float d[G][MC];
-      float stv[kSliceGroups];   // steps of this row in the slice being read back
-      auto fetch = [&]() -> bool {
-        if (!wait_bar(dready0 + 8 * ebuf, (dphase >> ebuf) & 1u, abort_flag)) return false;
-        dphase ^= 1u << ebuf;
-        tc_fence_after();
-#pragma unroll
-        for (int g = 0; g < G; ++g) tmem_ld<MC>(tmem + lane_base + kDCol + (ebuf * G + g) * NP, d[g]);
-        return true;
-      };
-      auto fold = [&]() {
-        if (er0 == 0) {   // the row's 8 steps of the slice, one 16-byte load
-          const uint4 sv =
-              *reinterpret_cast<const uint4*>(st0_ptr + eslot * p.stage_bytes + kCodesBytes + tid * 16);
-          const uint32_t w[4] = {sv.x, sv.y, sv.z, sv.w};
-#pragma unroll
-          for (int j = 0; j < kSliceGroups; ++j) stv[j] = bf16_bits_to_float((w[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
-        }
-        tmem_wait_ld<G * MC>(&d[0][0]);
-        const int q = er0 / G;   // round of the slice
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float sg = stv[g];
-#pragma unroll
-          for (int r = 1; r < kRounds; ++r) sg = q == r ? stv[r * G + g] : sg;
-#pragma unroll
-          for (int m = 0; m < MC; ++m) acc[m] = fmaf(sg, d[g][m], acc[m]);
-        }
-        if (++ebuf == kBufs) ebuf = 0;
-        --pend;
-        er0 += G;
-        if (er0 == kSliceGroups) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(empty0 + 8 * eslot);
-          if (p.S == 1) {
-#pragma unroll
-            for (int m = 0; m < MC; ++m) rowsum[m] += acc[m];
-          } else if (row < p.N) {
-#pragma unroll
-            for (int m = 0; m < MC; ++m)
-              if (m < p.M) p.ws_partial[((long long)esl * p.M + m) * p.N + row] = acc[m];
-          }
-#pragma unroll
-          for (int m = 0; m < MC; ++m) acc[m] = 0.0f;
-          er0 = 0;
-          ++esl;
-          if (++eslot == nst) eslot = 0;
-        }
-      };
-
       for (int sl = sl0; sl < sl1 && ok; ++sl) {
         if (!wait_bar(full0 + 8 * slot, phase, abort_flag)) {
           ok = false;
           break;
         }
-        uint8_t* stg_ptr = st0_ptr + slot * p.stage_bytes;
-        for (int r0 = 0; r0 < kSliceGroups; r0 += G) {
-          // with kBufs - 1 rounds pending, the oldest is read back around
-          // this round's unpacking: its loads are in flight meanwhile (when
-          // its dot products fit the registers beside the unpacking)
-          const bool back = pend == kBufs - 1;
-          if (kEarly && back && !(ok = fetch())) break;
-          // unpack this round's groups into tensor memory
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const int grp = r0 + g;
-            const uint4 q = *reinterpret_cast<const uint4*>(stg_ptr + tid * 128 + ((grp ^ (tid & 7)) << 4));
-            uint32_t a[16];
-            unpack_bf16(q.x, a);
-            unpack_bf16(q.y, a + 4);
-            unpack_bf16(q.z, a + 8);
-            unpack_bf16(q.w, a + 12);
-            tmem_st16(tmem + lane_base + kACol + (ubuf * G + g) * 16, a);
+        const uint8_t* stg_ptr = st0_ptr + slot * p.stage_bytes;
+        for (int q = 0; q < kRounds; ++q, ++r) {
+          const int b = (int)(r % kBufs);
+          const uint32_t use = (uint32_t)(r / kBufs);
+          // A[b] is free once the MMAs of its previous use are done
+          if (use > 0 && !wait_bar(afree0 + 8 * b, (use - 1) & 1u, abort_flag)) {
+            ok = false;
+            break;
           }
-          if (!kEarly && back && !(ok = fetch())) break;
-          if (back) fold();   // frees the oldest round's buffers for later rounds
+          tc_fence_after();
+#pragma unroll 2
+          for (int g = 0; g < G; ++g) {
+            const int grp = q * G + g;
+            const uint4 w = *reinterpret_cast<const uint4*>(stg_ptr + tid * 128 + ((grp ^ (tid & 7)) << 4));
+            uint32_t a[16];
+            unpack_bf16(w.x, a);
+            unpack_bf16(w.y, a + 4);
+            unpack_bf16(w.z, a + 8);
+            unpack_bf16(w.w, a + 12);
+            tmem_st16(tmem + lane_base + kACol + (b * G + g) * 16, a);
+          }
           asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(aready0 + 8 * ubuf);   // this warp's rows are in
-          if (++ubuf == kBufs) ubuf = 0;
-          ++pend;
+          if (lane == 0) mbar_arrive(aready0 + 8 * b);   // this warp's rows are in
         }
-        if (!ok) break;
         if (++slot == nst) {
           slot = 0;
           phase ^= 1u;
         }
       }
-      // the unit's pending rounds are read back before its rows are finished
-      while (ok && pend > 0) {
-        if (!(ok = fetch())) break;
-        fold();
+    }
+    if (!ok) {
+      if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+  } else if (warp < kUnpackWarps + kFoldWarps) {
+    // ---------------------------------------------------------- folding warps
+    const int tid = threadIdx.x - 32 * kUnpackWarps;   // weight row within the tile
+    const uint32_t lane_base = (uint32_t)((warp - kUnpackWarps) * 32) << 16;
+    int slot = 0;
+    uint32_t phase = 0;
+    long long r = 0;
+    float acc[MC], rowsum[kTmemSum ? 1 : MC];
+    bool ok = true;
+    for (int u = u0; u < u1 && ok; ++u) {
+      const int s = u / p.tiles, t = u - s * p.tiles;
+      const int sl0 = s * p.sps, sl1 = min(sl0 + p.sps, p.slices);
+      const int row = t * kRows + tid;
+      if constexpr (!kTmemSum) {
+#pragma unroll
+        for (int m = 0; m < MC; ++m) rowsum[m] = 0.0f;
+      }
+      for (int sl = sl0; sl < sl1 && ok; ++sl) {
+        // the stage's data (steps) is visible once its copies have landed
+        if (!wait_bar(full0 + 8 * slot, phase, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* stg_ptr = st0_ptr + slot * p.stage_bytes;
+        float stv[kSliceGroups];   // the row's 8 steps of the slice, one 16-byte load
+        {
+          const uint4 sv = *reinterpret_cast<const uint4*>(stg_ptr + kCodesBytes + tid * 16);
+          const uint32_t wv[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+          for (int j = 0; j < kSliceGroups; ++j)
+            stv[j] = bf16_bits_to_float((wv[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+        }
+#pragma unroll
+        for (int m = 0; m < MC; ++m) acc[m] = 0.0f;
+#pragma unroll
+        for (int q = 0; q < kRounds; ++q) {
+          const int b = (int)(r % kBufs);
+          const uint32_t use = (uint32_t)(r / kBufs);
+          if (!wait_bar(dready0 + 8 * b, use & 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int g0 = 0; g0 < G; g0 += kLdBatch) {
+            float d[kLdBatch][MC];
+#pragma unroll
+            for (int g = 0; g < kLdBatch; ++g)
+              tmem_ld<MC>(tmem + lane_base + kDCol + (b * G + g0 + g) * NP, d[g]);
+            tmem_wait_ld<kLdBatch * MC>(&d[0][0]);
+#pragma unroll
+            for (int g = 0; g < kLdBatch; ++g)
+#pragma unroll
+              for (int m = 0; m < MC; ++m) acc[m] = fmaf(stv[q * G + g0 + g], d[g][m], acc[m]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(dfree0 + 8 * b);   // this warp has read D[b]
+          ++r;
+        }
+        if (!ok) break;
+        // the slice is done: its sum goes on, its stage back to the copy warp
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+        if (p.S == 1) {
+          if constexpr (kTmemSum) {
+            // sum (from 0) of the slices so far, kept in tensor memory
+            float sum[MC];
+            if (sl == sl0) {
+#pragma unroll
+              for (int m = 0; m < MC; ++m) sum[m] = 0.0f;
+            } else {
+              tmem_ld<MC>(tmem + lane_base + kSumCol, sum);
+              tmem_wait_ld<MC>(sum);
+            }
+            uint32_t v[MC];
+#pragma unroll
+            for (int m = 0; m < MC; ++m) v[m] = __float_as_uint(sum[m] + acc[m]);
+#pragma unroll
+            for (int c = 0; c < MC; c += 16) tmem_st16(tmem + lane_base + kSumCol + c, v + c);
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          } else {
+#pragma unroll
+            for (int m = 0; m < MC; ++m) rowsum[m] += acc[m];
+          }
+        } else if (row < p.N) {
+#pragma unroll
+          for (int m = 0; m < MC; ++m)
+            if (m < p.M) p.ws_partial[((long long)sl * p.M + m) * p.N + row] = acc[m];
+        }
+        if (++slot == nst) {
+          slot = 0;
+          phase ^= 1u;
+        }
       }
       if (!ok) break;
       if (p.S == 1) {
+        float* sum = rowsum;
+        float tsum[kTmemSum ? MC : 1];
+        if constexpr (kTmemSum) {
+          tmem_ld<MC>(tmem + lane_base + kSumCol, tsum);
+          tmem_wait_ld<MC>(tsum);
+          sum = tsum;
+        }
         if (row < p.N) {
 #pragma unroll
           for (int m = 0; m < MC; ++m)
-            if (m < p.M) p.y[(long long)m * p.N + row] = __float2bfloat16_rn(rowsum[m]);
+            if (m < p.M) p.y[(long long)m * p.N + row] = __float2bfloat16_rn(sum[m]);
         }
         continue;
       }
@@ -532,30 +574,35 @@ __global__ void __launch_bounds__(kThreads, 2) tc_kernel(const __grid_constant__
       asm volatile("bar.sync 1, %0;" ::"n"(kRows) : "memory");
       if (*last_flag) {
         if (row < p.N) {
-          // kBatch slices at a time, all their partials in flight at once,
-          // then added in slice order
-          constexpr int kBatch = MC <= 8 ? 8 : (MC <= 16 ? 4 : 2);
+          // CB activation columns at a time; for each, SB slices' partials
+          // in flight at once, then added in slice order
+          constexpr int CB = MC < 8 ? MC : 8, SB = 32 / CB;
+#pragma unroll 1
+          for (int m0 = 0; m0 < MC; m0 += CB) {
+            if (m0 >= p.M) break;
+            float fsum[CB];
 #pragma unroll
-          for (int m = 0; m < MC; ++m) rowsum[m] = 0.0f;
-          for (int sl0 = 0; sl0 < p.slices; sl0 += kBatch) {
-            float v[kBatch][MC];
+            for (int c = 0; c < CB; ++c) fsum[c] = 0.0f;
+            for (int sb = 0; sb < p.slices; sb += SB) {
+              float v[SB][CB];
 #pragma unroll
-            for (int b = 0; b < kBatch; ++b)
+              for (int k2 = 0; k2 < SB; ++k2)
 #pragma unroll
-              for (int m = 0; m < MC; ++m)
-                v[b][m] = (sl0 + b < p.slices && m < p.M)
-                              ? __ldcg(p.ws_partial + ((long long)(sl0 + b) * p.M + m) * p.N + row)
-                              : 0.0f;
+                for (int c = 0; c < CB; ++c)
+                  v[k2][c] = (sb + k2 < p.slices && m0 + c < p.M)
+                                 ? __ldcg(p.ws_partial + ((long long)(sb + k2) * p.M + m0 + c) * p.N + row)
+                                 : 0.0f;
 #pragma unroll
-            for (int b = 0; b < kBatch; ++b)
-              if (sl0 + b < p.slices) {
+              for (int k2 = 0; k2 < SB; ++k2)
+                if (sb + k2 < p.slices) {
 #pragma unroll
-                for (int m = 0; m < MC; ++m) rowsum[m] += v[b][m];
-              }
+                  for (int c = 0; c < CB; ++c) fsum[c] += v[k2][c];
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < CB; ++c)
+              if (m0 + c < p.M) p.y[(long long)(m0 + c) * p.N + row] = __float2bfloat16_rn(fsum[c]);
           }
-#pragma unroll
-          for (int m = 0; m < MC; ++m)
-            if (m < p.M) p.y[(long long)m * p.N + row] = __float2bfloat16_rn(rowsum[m]);
         }
         if (tid == 0) atomicExch(p.ws_count + t, 0);
       }
@@ -666,10 +713,13 @@ bool tc_plan(int M, int N, int K, int sms, TcPlan* out) {
   pl.np = M <= 16 ? 16 : 32;
   pl.slices = K / kSliceK;
   pl.tiles = (N + kRows - 1) / kRows;
-  const int target = 2 * std::max(1, sms);
-  // K splits: as many as still give every CTA at most one unit
+  const int per_sm = 2;   // CTAs per SM
+  const int target = per_sm * std::max(1, sms);
+  // K splits, only for few row tiles (the split-K fix-up costs more than
+  // leaving part of the grid idle): as many as still give every CTA at most
+  // one unit
   int S = 1;
-  if (pl.tiles < target) S = std::max(1, std::min(pl.slices, target / pl.tiles));
+  if (2 * pl.tiles <= std::max(1, sms)) S = std::max(1, std::min(pl.slices, target / pl.tiles));
   pl.sps = (pl.slices + S - 1) / S;
   pl.S = (pl.slices + pl.sps - 1) / pl.sps;
   pl.units = pl.tiles * pl.S;
@@ -677,8 +727,8 @@ bool tc_plan(int M, int N, int K, int sms, TcPlan* out) {
   int off_b;
   pl.stage_bytes = stage_bytes_of(pl.np, &off_b);
   pl.off_b = off_b;
-  // two CTAs per SM: each keeps under half of the 228 KB of shared memory
-  const int budget = 232448 / 2 - 1024;
+  // each of the SM's CTAs keeps its share of the 228 KB of shared memory
+  const int budget = per_sm == 2 ? 232448 / 2 - 1024 : 232448 - 1024;
   pl.nst = std::min(kMaxStages, (budget - kBarBytes - 1024) / pl.stage_bytes);
   if (pl.nst < 2) return false;
   pl.smem = kBarBytes + 1024 + pl.nst * pl.stage_bytes;

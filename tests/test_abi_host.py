@@ -109,11 +109,12 @@ def test_plan_is_valid(M, N, K):
                                    (17, 300, 256), (9, 5376, 21504)])
 def test_tensor_core_plan_is_valid(M, N, K):
     p = lib.plan(M, N, K)
-    assert p["path"] == 2 and p["threads"] == 160 and p["unit_rows"] == 128
+    assert p["path"] == 2 and p["threads"] == 320 and p["unit_rows"] == 128
     assert p["tmpl_team"] == (16 if M <= 16 else 32)      # MMA N: activation columns
     assert p["rows_per_call"] == min(M, 32)
+    assert p["ctas_per_sm"] == 2
     assert 2 <= p["stages"] <= 4 and p["smem_bytes"] <= 233472 // 2 - 1024
-    assert 1 <= p["ctas"] <= 2 * 152
+    assert 1 <= p["ctas"] <= p["ctas_per_sm"] * 152
     tiles, slices = -(-N // 128), K // 256
     assert 1 <= p["slices"] <= slices
     assert (lib.workspace_bytes(M, N, K) > 0) == (p["slices"] > 1)
