@@ -82,3 +82,24 @@ def test_window_counters_rearm_across_many_launches(cuda_lib):
     assert int(status.item()) == 0
     for y in ys:
         assert np.array_equal(host_bits(y), ref)
+
+
+@pytest.mark.parametrize("m,n,k", [(2, 131072, 2048), (3, 65536, 5376), (4, 65536, 2048)])
+def test_batched_rows_with_run_time_windows(cuda_lib, m, n, k):
+    """Several activation rows (CUDA-core path) with windows handed out at run
+    time: sampled rows against the oracle, and each activation row bitwise
+    equal to the single-row call (the row arithmetic depends on K alone)."""
+    assert lib.plan(m, n, k)["dynamic_windows"] == 1
+    qw, st, _ = weights(n, k, 7 * m + k)
+    x = synth.torch_x((m, k), synth.seed_of(m, k), "cuda")
+    y = poison_bf16((m, n))
+    lib.gemv(qw, st, x, y=y, pdl=True, path="cuda")
+    torch.cuda.synchronize()
+    yb = host_bits(y)
+    assert not np.any(yb == POISON)
+    rng = np.random.default_rng(m)
+    rows = np.unique(np.concatenate([rng.choice(n, 192, replace=False), [0, n - 1]]))
+    assert_gemv_parity(y[:, rows], host_words(qw[rows]), host_bits(st[rows]), host_bits(x))
+    for i in range(m):
+        yi = call(qw, st, x[i:i + 1].contiguous())
+        assert np.array_equal(host_bits(yi)[0], yb[i])
