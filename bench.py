@@ -572,6 +572,11 @@ def run_moe(args, world, rank, local):
         scomb += n * k // 16
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(device=dev)
+    host_home = args.expert_home == "host"
+    vectors = args.expert_vectors
+    # the router's real ids of every step, as it would leave them on the device
+    eids_dev = torch.zeros((L, k_top), dtype=torch.int32, device=dev)
+    eids_host = torch.zeros((total, L, k_top), dtype=torch.int32).pin_memory()
     layers = []
     for li in range(L):
         lay = {"trace": synth.moe_trace(E, k_top, total, cfg.zipf_s, cfg.repeat_p,
@@ -585,24 +590,49 @@ def run_moe(args, world, rank, local):
                "pool_q": torch.zeros((S, qcomb // 4), dtype=torch.int32, device=dev),
                "pool_s": torch.zeros((S, scomb // 2), dtype=torch.bfloat16, device=dev),
                "y": {}, "y_full": {}, "calls": [], "calls_full": []}
+        eids_host[:, li] = torch.from_numpy(np.asarray(lay["trace"], dtype=np.int32))
+        lay["src_q"], lay["src_s"] = lay["full_q"], lay["full_s"]
+        if host_home:   # the pool's source; the HBM copy only serves the bitwise check
+            lay["src_q"] = torch.empty(lay["full_q"].shape, dtype=torch.int32, pin_memory=True)
+            lay["src_s"] = torch.empty(lay["full_s"].shape, dtype=torch.bfloat16,
+                                       pin_memory=True)
+            lay["src_q"].copy_(lay["full_q"])
+            lay["src_s"].copy_(lay["full_s"])
+        if vectors:
+            lay["table"] = torch.full((S,), -1, dtype=torch.int32, device=dev)
+            lay["scale"] = {name: synth.torch_x((E, n), synth.seed_of(45, li, n), dev)
+                            for name, (n, k) in shapes.items()}
+            lay["bias"] = {"gate_up": None,
+                           "down": synth.torch_x((E, H), synth.seed_of(46, li), dev)}
         for name, (n, k) in shapes.items():
             lay["y"][name] = torch.empty((k_top, n), dtype=torch.bfloat16, device=dev)
             lay["y_full"][name] = torch.empty((k_top, n), dtype=torch.bfloat16, device=dev)
             for full, calls in ((False, lay["calls"]), (True, lay["calls_full"])):
                 q = lay["full_q" if full else "pool_q"][:, qoff[name] // 4:]
                 st = lay["full_s" if full else "pool_s"][:, soff[name] // 2:]
-                calls.append(lib.bind_gemv_id(q, st, lay["ids_full" if full else "slot_ids"],
-                                              lay["x"][name], n, k, E if full else S, qcomb,
-                                              scomb, lay["y_full" if full else "y"][name],
-                                              status))
+                ids = lay["ids_full" if full else "slot_ids"]
+                y = lay["y_full" if full else "y"][name]
+                if vectors:
+                    calls.append(lib.bind_gemv_id_scaled(
+                        q, st, ids, lay["x"][name], n, k, E if full else S, qcomb, scomb,
+                        ids if full else eids_dev[li], E, y,
+                        slot_expert=None if full else lay["table"], scale=lay["scale"][name],
+                        bias=lay["bias"][name], status=status))
+                else:
+                    calls.append(lib.bind_gemv_id(q, st, ids, lay["x"][name], n, k,
+                                                  E if full else S, qcomb, scomb, y, status))
         layers.append(lay)
 
     def new_pools():
         for lay in layers:
             lay["pool"] = lib.SlotPool(E, S)
-            lay["stage"] = lay["pool"].bind_stage(k_top, lay["pool_q"], lay["full_q"], qcomb,
-                                                  qcomb, lay["pool_s"], lay["full_s"], scomb,
-                                                  scomb, lay["slot_ids"])
+            lay["stage"] = lay["pool"].bind_stage(k_top, lay["pool_q"], lay["src_q"], qcomb,
+                                                  qcomb, lay["pool_s"], lay["src_s"], scomb,
+                                                  scomb, lay["slot_ids"],
+                                                  slot_expert=lay.get("table"))
+            if vectors:
+                lay["table"].fill_(-1)
+        torch.cuda.synchronize()
 
     def gemvs(lay, full=False, pdl=False):
         # programmatic dependent launch after the first kernel: the routed
@@ -625,6 +655,8 @@ def run_moe(args, world, rank, local):
                 e0.record(stream)
                 t_host = time.perf_counter()
             misses = 0
+            if vectors:
+                eids_dev.copy_(eids_host[t], non_blocking=True)
             for lay in layers:
                 misses += lay["stage"](lay["trace"][t], stream=stream)
                 gemvs(lay, pdl=True)
@@ -656,6 +688,8 @@ def run_moe(args, world, rank, local):
     bad = torch.zeros((), dtype=torch.int64, device=dev)
     with torch.cuda.stream(stream):
         for t in range(total):
+            if vectors:
+                eids_dev.copy_(eids_host[t], non_blocking=True)
             for lay in layers:
                 lay["stage"](lay["trace"][t], stream=stream)
                 gemvs(lay)
@@ -683,7 +717,13 @@ def run_moe(args, world, rank, local):
                    "timed": "eager steps: host LFU remap + pool copies + slot ids + 2 gemv_id "
                             "per layer (CUDA events)",
                    "pool_layout": "one 32-slot pool per layer; a slot holds an expert's gate/up "
-                                  "and down codes (and, in a second pool array, steps)"},
+                                  "and down codes (and, in a second pool array, steps)",
+                   "expert_home": ("page-locked host memory, pool fills over NVLink-C2C"
+                                   if host_home else "HBM"),
+                   "expert_vectors": ("per-expert output scales (gate/up, down) and down "
+                                      "biases by real id, slot table checked, "
+                                      "w4a16_gemv_id_scaled; real ids copied to the device "
+                                      "once per step" if vectors else None)},
         "host_seconds_per_step": host_s / steps,
         "kernel": {"ms_per_step": kms, "tok_s": 1000.0 / kms, "bytes_per_step": kernel_bytes,
                    "gbps": gbps, "frac": gbps / peak, "peak": peak, "peak_kind": peak_kind,
@@ -750,6 +790,12 @@ def main():
                     help="with --shape: the library's choice, CUDA cores or tensor cores")
     ap.add_argument("--separate", action="store_true",
                     help="one GEMV per projection instead of merged q/k/v and gate/up")
+    ap.add_argument("--expert-home", choices=("device", "host"), default="device",
+                    help="routed-expert workload: full expert tensors in HBM, or in page-locked "
+                         "host (Grace) memory that the pool fills read over NVLink-C2C")
+    ap.add_argument("--expert-vectors", action="store_true",
+                    help="routed-expert workload: per-expert output scales (and down biases) "
+                         "by real expert id, slot table checked (w4a16_gemv_id_scaled)")
     ap.add_argument("--workload", default="dense-35L-h2048",
                     choices=sorted(DENSE_WORKLOADS) + ["moe-30L-h2816"],
                     help="decode pass to time (default: the 35-layer hidden-2048 decoder)")

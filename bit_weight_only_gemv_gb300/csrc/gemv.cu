@@ -101,6 +101,12 @@ struct GemvParams {
   int32_t* status;
   int dyn;                             // windows handed out at run time (dense, whole rows)
   int* work;                           // [0] windows taken, [1] CTAs done (dyn only)
+  // routed calls with real expert ids (all nullptr otherwise)
+  const int32_t* eids;                 // [n_items] real expert of each item
+  int num_real;                        // experts behind eids
+  const int32_t* slot_expert;          // [num_experts] expert each slot holds, or nullptr
+  const __nv_bfloat16* escale;         // [num_real][N] output scale, or nullptr
+  const __nv_bfloat16* ebias;          // [num_real][N] output bias, or nullptr
 };
 
 // ---------------------------------------------------------------- activations
@@ -261,7 +267,8 @@ struct Walk {
 };
 
 // Codes and steps of `item` (false: routed id out of range; its rows are left
-// unwritten).
+// unwritten).  The copy warp and the consumers take the same decision for
+// every item.
 __device__ __forceinline__ bool item_arrays(const GemvParams& p, int item, const uint8_t** q,
                                             const uint8_t** s) {
   long long blk = item;
@@ -273,6 +280,20 @@ __device__ __forceinline__ bool item_arrays(const GemvParams& p, int item, const
   *q = p.qw + (unsigned long long)blk * p.qw_item_stride;
   *s = p.st + (unsigned long long)blk * p.st_item_stride;
   return true;
+}
+
+// Per-expert output vectors of a window (scale and bias from its first row),
+// nullptr when absent: an output is fma(sum, scale, bias) in fp32.
+struct OutVec {
+  const __nv_bfloat16* s;
+  const __nv_bfloat16* b;
+};
+
+__device__ __forceinline__ float out_value(const OutVec& o, int r, float v) {
+  if (o.s == nullptr && o.b == nullptr) return v;
+  const float sc = o.s != nullptr ? __bfloat162float(o.s[r]) : 1.0f;
+  const float bi = o.b != nullptr ? __bfloat162float(o.b[r]) : 0.0f;
+  return fmaf(v, sc, bi);
 }
 
 // Bounded wait on a stage barrier that also gives up once another warp of
@@ -420,22 +441,28 @@ constexpr int min_ctas(int mr, int rw) { return (mr * rw <= 4) ? 2 : 1; }
 // window, i.e. has finished reading this one.
 template <int MR>
 __device__ __forceinline__ void finish_window(const GemvParams& p, const float* redw, int nrows,
-                                              int ncw, __nv_bfloat16* yrow) {
+                                              int ncw, __nv_bfloat16* yrow, OutVec ov) {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
   for (int i = threadIdx.x; i < nrows * MR; i += kConsumers) {
     const int r = i / MR, m = i - r * MR;
     float v = 0.0f;
     for (int cc = 0; cc < ncw; ++cc) v += redw[(r * p.nch + cc) * MR + m];
-    yrow[(long long)m * p.N + r] = __float2bfloat16_rn(v);
+    yrow[(long long)m * p.N + r] = __float2bfloat16_rn(out_value(ov, r, v));
   }
 }
 
-// DS: a dense call of whole rows (no routed ids, no split-K).  Its CTAs walk
-// their rows in windows of RB rows with every offset fixed for the launch;
-// the other calls take the general walk.
-template <int MR, int RW, int TT, int CLT, bool DS>
+// WALK kWalkDense: a dense call of whole rows (no routed ids, no split-K).
+// Its CTAs walk their rows in windows of RB rows with every offset fixed for
+// the launch; the other calls take the general walk (kWalkGeneral), which
+// kWalkRealIds extends with the real-id checks and per-expert output vectors
+// of w4a16_gemv_id_scaled.
+constexpr int kWalkGeneral = 0, kWalkDense = 1, kWalkRealIds = 2;
+
+template <int MR, int RW, int TT, int CLT, int WALK>
 __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
     gemv_kernel(const __grid_constant__ GemvParams p) {
+  constexpr bool DS = WALK == kWalkDense;
+  constexpr bool RID = MR == 1 && WALK == kWalkRealIds;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -693,17 +720,35 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
       } else {
         tile += p.tile_bytes;
       }
-      if (ncw > 1) finish_window<MR>(p, redw, nrows, ncw, p.y + row0);
+      if (ncw > 1) finish_window<MR>(p, redw, nrows, ncw, p.y + row0, OutVec{nullptr, nullptr});
     }
     return;
   } else {
     bool reported = false;
     while (wk.next(p)) {
       const uint8_t *qwi, *sti;
+      int rid = 0;   // real expert id (RID), loaded together with the routed id
+      if constexpr (RID) rid = __ldg(p.eids + wk.item);
       if (!dense && !item_arrays(p, wk.item, &qwi, &sti)) {
         if (!reported && lane == 0) report(p.status, W4_ERR_INDEX);
         reported = true;
         continue;
+      }
+      // Real expert ids: a real id out of range (W4_ERR_INDEX) or a slot that
+      // does not hold that expert (W4_ERR_OWNER) keeps the window's rows
+      // unwritten; its tile is still read and released as usual.  The checks
+      // are taken at the stores, so their loads (and those of the output
+      // vectors, from a clamped row) overlap the dot product.
+      OutVec ov = {nullptr, nullptr};
+      int wcode = W4_OK;
+      if constexpr (RID) {
+        const bool in_range = rid >= 0 && rid < p.num_real;
+        const int holder = p.slot_expert != nullptr ? __ldg(p.slot_expert + __ldg(p.ids + wk.item))
+                                                    : rid;
+        const long long rr = in_range ? rid : 0;
+        if (p.escale != nullptr) ov.s = p.escale + rr * p.N + wk.row0;
+        if (p.ebias != nullptr) ov.b = p.ebias + rr * p.N + wk.row0;
+        wcode = !in_range ? W4_ERR_INDEX : (holder != rid ? W4_ERR_OWNER : W4_OK);
       }
       const int xslot = p.x_per_item ? wk.item - item0 : 0;
       const bool whole = p.S == 1;
@@ -768,6 +813,20 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
         }
         const int g0 = c * gpc + t;
         const int ns = CLT > 0 ? CLT : min(p.CL, p.NI - c * p.CL);
+        // Rows finished by this item (one chunk) of a call with per-expert
+        // vectors: their scale and bias are fetched now, so that the loads'
+        // latency hides behind the dot product.
+        const bool epi = RID && ncw == 1 && t == 0 && (ov.s != nullptr || ov.b != nullptr);
+        float osc[RW], obi[RW];
+#pragma unroll
+        for (int j = 0; j < RW; ++j) {
+          osc[j] = 1.0f;
+          obi[j] = 0.0f;
+          if (epi && rv[j]) {
+            if (ov.s != nullptr) osc[j] = __bfloat162float(__ldg(ov.s + rl[j]));
+            if (ov.b != nullptr) obi[j] = __bfloat162float(__ldg(ov.b + rl[j]));
+          }
+        }
         float acc[RW][MR];
         tile_dot<MR, RW, TT, CLT>(smem, xo0 + (uint32_t)(g0 * 16), xso0 + (uint32_t)(g0 * 4), xplane,
                                   xmrow, xsmrow, co, so, ns, T, kg_valid - g0, acc);
@@ -778,7 +837,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
         if (t == 0) {
 #pragma unroll
           for (int j = 0; j < RW; ++j) {
-            if (!rv[j]) continue;
+            if (!rv[j] || wcode != W4_OK) continue;
             if (!whole) {          // split-K: chunk sums to the workspace
               float* dst = p.ws_partial + (((long long)wk.rb * p.nch + c) * p.RB + rl[j]) * MR;
 #pragma unroll
@@ -786,7 +845,8 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
             } else if (ncw == 1) { // one chunk: the row is done (0 + chunk sum)
 #pragma unroll
               for (int m = 0; m < MR; ++m)
-                yrow[(long long)m * p.N + rl[j]] = __float2bfloat16_rn(0.0f + acc[j][m]);
+                yrow[(long long)m * p.N + rl[j]] = __float2bfloat16_rn(
+                    epi ? fmaf(0.0f + acc[j][m], osc[j], obi[j]) : 0.0f + acc[j][m]);
             } else {
 #pragma unroll
               for (int m = 0; m < MR; ++m) redw[(rl[j] * p.nch + ci) * MR + m] = acc[j][m];
@@ -805,7 +865,11 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
         } else {
           tile += p.tile_bytes;
         }
-        if (ncw > 1) finish_window<MR>(p, redw, wk.nrows, ncw, yrow);
+        if (RID && wcode != W4_OK) {
+          if (!reported && lane == 0) report(p.status, wcode);
+          reported = true;
+        }
+        if (ncw > 1) finish_window<MR>(p, redw, wcode == W4_OK ? wk.nrows : 0, ncw, yrow, ov);
         continue;
       }
       if (lane == 0) mbar_arrive(empty0 + 8 * slot);
@@ -1120,20 +1184,45 @@ using KernelFn = void (*)(GemvParams);
 // get one compiled for their team size and chunk length (the common K);
 // everything else the generic one.  *tt, *clt (if given) receive the
 // compile-time team size and chunk length (0: generic).
-KernelFn kernel_for(const Plan& pl, int* tt = nullptr, int* clt = nullptr) {
+// The instantiation that runs a plan.  Calls with real expert ids
+// (w4a16_gemv_id_scaled) take their own kernels: the checks and output
+// vectors stay out of every other launch.
+KernelFn kernel_for(const Plan& pl, bool real_ids = false, int* tt = nullptr, int* clt = nullptr) {
   if (tt != nullptr) *tt = 0;
   if (clt != nullptr) *clt = 0;
   const bool ds = !pl.routed && pl.S == 1;
   const bool full = pl.NI % pl.CL == 0 && pl.NI * pl.T == pl.Kg;
+  const int key = pl.T * 16 + pl.CL;
+  if (real_ids) {
+    if (pl.MR != 1) return nullptr;
+#define W4_RID(t, cl)                                                                   \
+  if (full && pl.RW <= 2 && key == (t) * 16 + (cl)) {                                   \
+    if (tt != nullptr) *tt = t;                                                         \
+    if (clt != nullptr) *clt = cl;                                                      \
+    return pl.RW == 1 ? gemv_kernel<1, 1, t, cl, kWalkRealIds>                          \
+                      : gemv_kernel<1, 2, t, cl, kWalkRealIds>;                         \
+  }
+    W4_RID(8, 11)   // K = 2816
+    W4_RID(2, 11)   // K = 704
+#undef W4_RID
+    switch (pl.RW) {
+      case 1: return gemv_kernel<1, 1, 0, 0, kWalkRealIds>;
+      case 2: return gemv_kernel<1, 2, 0, 0, kWalkRealIds>;
+      case 4: return gemv_kernel<1, 4, 0, 0, kWalkRealIds>;
+      default: return nullptr;
+    }
+  }
   if (pl.MR == 1 && full && (pl.RW <= 2 || (ds && pl.RW == 4))) {
-    const int key = pl.T * 16 + pl.CL;
-#define W4_SPEC(t, cl)                                                            \
-  if (key == (t) * 16 + (cl)) {                                                   \
-    if (tt != nullptr) *tt = t;                                                   \
-    if (clt != nullptr) *clt = cl;                                                \
-    if (ds && pl.RW == 4) return gemv_kernel<1, 4, t, cl, true>;                  \
-    if (ds) return pl.RW == 1 ? gemv_kernel<1, 1, t, cl, true> : gemv_kernel<1, 2, t, cl, true>; \
-    return pl.RW == 1 ? gemv_kernel<1, 1, t, cl, false> : gemv_kernel<1, 2, t, cl, false>;       \
+#define W4_SPEC(t, cl)                                                                  \
+  if (key == (t) * 16 + (cl)) {                                                         \
+    if (tt != nullptr) *tt = t;                                                         \
+    if (clt != nullptr) *clt = cl;                                                      \
+    if (ds && pl.RW == 4) return gemv_kernel<1, 4, t, cl, kWalkDense>;                  \
+    if (ds)                                                                             \
+      return pl.RW == 1 ? gemv_kernel<1, 1, t, cl, kWalkDense>                          \
+                        : gemv_kernel<1, 2, t, cl, kWalkDense>;                         \
+    return pl.RW == 1 ? gemv_kernel<1, 1, t, cl, kWalkGeneral>                          \
+                      : gemv_kernel<1, 2, t, cl, kWalkGeneral>;                         \
   }
     W4_SPEC(16, 4)   // K = 2048
     W4_SPEC(8, 3)    // K = 5376
@@ -1143,13 +1232,14 @@ KernelFn kernel_for(const Plan& pl, int* tt = nullptr, int* clt = nullptr) {
     W4_SPEC(2, 11)   // K = 704
 #undef W4_SPEC
   }
-#define W4_GEN(mr, rw) (ds ? gemv_kernel<mr, rw, 0, 0, true> : gemv_kernel<mr, rw, 0, 0, false>)
+#define W4_GEN(mr, rw) \
+  (ds ? gemv_kernel<mr, rw, 0, 0, kWalkDense> : gemv_kernel<mr, rw, 0, 0, kWalkGeneral>)
   switch (pl.MR * 8 + pl.RW) {
     case 8 + 1: return W4_GEN(1, 1);
     case 8 + 2: return W4_GEN(1, 2);
     case 8 + 4: return W4_GEN(1, 4);
     case 16 + 1: return W4_GEN(2, 1);
-    case 16 + 2: return gemv_kernel<2, 2, 0, 0, true>;   // whole rows only (RW > 1)
+    case 16 + 2: return gemv_kernel<2, 2, 0, 0, kWalkDense>;   // whole rows only (RW > 1)
     case 24 + 1: return W4_GEN(3, 1);
     case 32 + 1: return W4_GEN(4, 1);
     default: return nullptr;
@@ -1212,7 +1302,7 @@ cudaError_t work_slot(int dev, int** out) {
 }
 
 cudaError_t launch(const GemvParams& prm, const Plan& pl, bool pdl, cudaStream_t stream, int dev) {
-  const KernelFn fn = kernel_for(pl);
+  const KernelFn fn = kernel_for(pl, prm.eids != nullptr);
   if (fn == nullptr) return cudaErrorInvalidConfiguration;
   const cudaError_t ea = allow_smem(fn, pl.smem, dev);
   if (ea != cudaSuccess) return ea;
@@ -1432,7 +1522,7 @@ extern "C" w4_status w4a16_gemv_plan(int M, int N, int K, w4_plan_info* info) {
   info->ctas_per_sm = pl.per_sm;
   info->dynamic_windows = pl.dyn ? 1 : 0;
   // compile-time team size / chunk length of the instantiation (0: generic)
-  kernel_for(pl, &info->tmpl_team, &info->tmpl_chunk);
+  kernel_for(pl, false, &info->tmpl_team, &info->tmpl_chunk);
   return W4_OK;
 }
 
@@ -1507,11 +1597,23 @@ extern "C" w4_status w4a16_gemv(void* y, const void* qw, const void* st, const v
   return W4_OK;
 }
 
-extern "C" w4_status w4a16_gemv_id(void* y, const void* qw_base, size_t qw_stride_bytes,
-                                   const void* st_base, size_t st_stride_bytes, int num_experts,
-                                   const int32_t* ids, int n_ids, const void* x, int x_rows,
-                                   int N, int K, int32_t* status_dev, unsigned flags,
-                                   w4_stream_t stream) {
+namespace w4 {
+namespace {
+
+// Real expert ids and per-expert output vectors of a routed call (all null
+// for w4a16_gemv_id).
+struct RealIds {
+  const int32_t* eids = nullptr;
+  int num_real = 0;
+  const int32_t* slot_expert = nullptr;
+  const void* scale = nullptr;
+  const void* bias = nullptr;
+};
+
+w4_status routed(void* y, const void* qw_base, size_t qw_stride_bytes, const void* st_base,
+                 size_t st_stride_bytes, int num_experts, const int32_t* ids, int n_ids,
+                 const void* x, int x_rows, int N, int K, const RealIds& real,
+                 int32_t* status_dev, unsigned flags, w4_stream_t stream) {
   if (y == nullptr || qw_base == nullptr || st_base == nullptr || ids == nullptr || x == nullptr)
     return W4_ERR_ARG;
   if (n_ids < 1 || N < 1 || num_experts < 1 || (flags & ~W4_FLAG_PDL) != 0) return W4_ERR_ARG;
@@ -1521,6 +1623,9 @@ extern "C" w4_status w4a16_gemv_id(void* y, const void* qw_base, size_t qw_strid
     return W4_ERR_ARG;
   if (!aligned(qw_base, 16) || !aligned(st_base, 16) || !aligned(x, 16) || !aligned(y, 2) ||
       qw_stride_bytes % 16 != 0 || st_stride_bytes % 16 != 0)
+    return W4_ERR_ALIGN;
+  if (real.eids != nullptr &&
+      (!aligned(real.slot_expert, 4) || !aligned(real.scale, 2) || !aligned(real.bias, 2)))
     return W4_ERR_ALIGN;
   int dev = 0;
   DeviceInfo di;
@@ -1540,6 +1645,11 @@ extern "C" w4_status w4a16_gemv_id(void* y, const void* qw_base, size_t qw_strid
   p.y = static_cast<__nv_bfloat16*>(y);
   p.n_items = n_ids;
   p.status = status_dev;
+  p.eids = real.eids;
+  p.num_real = real.num_real;
+  p.slot_expert = real.slot_expert;
+  p.escale = static_cast<const __nv_bfloat16*>(real.scale);
+  p.ebias = static_cast<const __nv_bfloat16*>(real.bias);
   const cudaError_t e =
       launch(p, pl, (flags & W4_FLAG_PDL) != 0, reinterpret_cast<cudaStream_t>(stream), dev);
   if (e != cudaSuccess) {
@@ -1548,6 +1658,37 @@ extern "C" w4_status w4a16_gemv_id(void* y, const void* qw_base, size_t qw_strid
     return W4_ERR_LAUNCH;
   }
   return W4_OK;
+}
+
+}  // namespace
+}  // namespace w4
+
+extern "C" w4_status w4a16_gemv_id(void* y, const void* qw_base, size_t qw_stride_bytes,
+                                   const void* st_base, size_t st_stride_bytes, int num_experts,
+                                   const int32_t* ids, int n_ids, const void* x, int x_rows,
+                                   int N, int K, int32_t* status_dev, unsigned flags,
+                                   w4_stream_t stream) {
+  return routed(y, qw_base, qw_stride_bytes, st_base, st_stride_bytes, num_experts, ids, n_ids,
+                x, x_rows, N, K, RealIds{}, status_dev, flags, stream);
+}
+
+extern "C" w4_status w4a16_gemv_id_scaled(void* y, const void* qw_base, size_t qw_stride_bytes,
+                                          const void* st_base, size_t st_stride_bytes,
+                                          int num_slots, const int32_t* ids, int n_ids,
+                                          const void* x, int x_rows, int N, int K,
+                                          const int32_t* expert_ids, int num_experts,
+                                          const int32_t* slot_expert, const void* scale,
+                                          const void* bias, int32_t* status_dev, unsigned flags,
+                                          w4_stream_t stream) {
+  if (expert_ids == nullptr || num_experts < 1) return W4_ERR_ARG;
+  RealIds real;
+  real.eids = expert_ids;
+  real.num_real = num_experts;
+  real.slot_expert = slot_expert;
+  real.scale = scale;
+  real.bias = bias;
+  return routed(y, qw_base, qw_stride_bytes, st_base, st_stride_bytes, num_slots, ids, n_ids, x,
+                x_rows, N, K, real, status_dev, flags, stream);
 }
 
 // ================================================================= no-allocation variant

@@ -7,8 +7,11 @@
 // LFU cache keeps hits in place, loads misses into assigned slots and writes
 // the slot indices before the expert matmul, which then reads the pool through
 // slot ids and sees exactly the bytes of the full expert tensor.  Here the
-// misses are device-to-device copies from the full, HBM-resident expert
-// tensor (the page reads them from an SSD into host memory).
+// misses are copied from the full expert tensor, held in HBM or in page-locked
+// Grace memory that the GPU reads in place over NVLink-C2C (the page reads
+// them from an SSD into host memory the Jetson's GPU shares).  An optional
+// device slot table names the expert each slot holds, so that consumers of
+// the real expert ids can check what a slot id points at.
 //
 // Policy (the page leaves it open): every requested id counts one use; hits
 // stay; misses, in request order, take the lowest free slot, else the slot
@@ -37,13 +40,23 @@ struct IdList {
   int32_t v[64];
 };
 
-__global__ void write_ids_kernel(int32_t* dst, IdList ids, int k) {
+// Entries of the device slot table: table[slot[i]] = expert[i].
+struct SlotEntries {
+  int32_t slot[64], expert[64];
+  int n;
+};
+
+__global__ void write_ids_kernel(int32_t* dst, IdList ids, int k, int32_t* table,
+                                 SlotEntries t) {
   const int i = threadIdx.x;
-  if (i < k) dst[i] = ids.v[i];
+  if (dst != nullptr && i < k) dst[i] = ids.v[i];
+  if (table != nullptr && i < t.n) table[t.slot[i]] = t.expert[i];
 }
 
 // One launch that loads a request's missed experts into their slots (codes
-// and steps, 16 bytes per thread step) and writes the request's slot ids.
+// and steps, 16 bytes per thread step), writes the request's slot ids and
+// names the new experts in the slot table.  Kernels later in the stream see
+// all of it at once, so the table needs no ordering inside the launch.
 struct FillParams {
   uint8_t* pool_qw;
   const uint8_t* full_qw;
@@ -52,6 +65,7 @@ struct FillParams {
   unsigned long long qw_stride, st_stride;   // bytes between experts / slots
   unsigned long long qw_units, st_units;     // 16-byte units per expert
   int32_t* slot_ids_dev;
+  int32_t* slot_expert_dev;                  // slot table, or nullptr
   int n_miss, k;
   int32_t miss_expert[64], miss_slot[64];
   int32_t ids[64];
@@ -59,6 +73,8 @@ struct FillParams {
 
 __global__ void __launch_bounds__(256) pool_fill_kernel(const __grid_constant__ FillParams p) {
   if (blockIdx.x == 0 && threadIdx.x < p.k) p.slot_ids_dev[threadIdx.x] = p.ids[threadIdx.x];
+  if (blockIdx.x == 0 && p.slot_expert_dev != nullptr && threadIdx.x < p.n_miss)
+    p.slot_expert_dev[p.miss_slot[threadIdx.x]] = p.miss_expert[threadIdx.x];
   const unsigned long long per = p.qw_units + p.st_units;
   const unsigned long long total = per * (unsigned long long)p.n_miss;
   for (unsigned long long u = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; u < total;
@@ -79,6 +95,25 @@ __global__ void __launch_bounds__(256) pool_fill_kernel(const __grid_constant__ 
 }
 
 namespace {
+
+// The address through which kernels on the current device read `ptr`: the
+// pointer itself for memory of this device (or managed memory), the mapped
+// address of page-locked host memory, nullptr for anything else (pageable
+// host memory, another device's memory), which the copy engine serves.
+const void* device_view(const void* ptr) {
+  int dev = 0;
+  cudaPointerAttributes a = {};
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  switch (a.type) {
+    case cudaMemoryTypeDevice: return a.device == dev ? ptr : nullptr;
+    case cudaMemoryTypeManaged: return ptr;
+    case cudaMemoryTypeHost: return a.devicePointer;
+    default: return nullptr;
+  }
+}
 
 w4_status remap(w4_slot_pool* p, const int32_t* ids, int k, int32_t* slot_ids,
                 std::vector<std::pair<int, int>>* miss_list) {
@@ -178,8 +213,8 @@ extern "C" w4_status w4_slot_pool_stage(w4_slot_pool* pool, const int32_t* exper
                                         size_t qw_stride_bytes, size_t qw_expert_bytes,
                                         void* pool_st, const void* full_st,
                                         size_t st_stride_bytes, size_t st_expert_bytes,
-                                        int32_t* slot_ids_dev, int32_t* slot_ids, int* n_miss,
-                                        w4_stream_t stream) {
+                                        int32_t* slot_ids_dev, int32_t* slot_expert_dev,
+                                        int32_t* slot_ids, int* n_miss, w4_stream_t stream) {
   if (pool == nullptr || expert_ids == nullptr || pool_qw == nullptr || full_qw == nullptr ||
       pool_st == nullptr || full_st == nullptr || slot_ids_dev == nullptr || k < 1)
     return W4_ERR_ARG;
@@ -191,20 +226,25 @@ extern "C" w4_status w4_slot_pool_stage(w4_slot_pool* pool, const int32_t* exper
   if (st != W4_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   bool failed = false;
-  // all 16-byte aligned: one kernel loads the misses and writes the slot ids
+  // sources the kernels can read, everything 16-byte aligned: one kernel
+  // loads the misses and writes the slot ids
   const auto a16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; };
-  if (a16(pool_qw) && a16(full_qw) && a16(pool_st) && a16(full_st) && qw_stride_bytes % 16 == 0 &&
-      st_stride_bytes % 16 == 0 && qw_expert_bytes % 16 == 0 && st_expert_bytes % 16 == 0) {
+  const void* src_qw = misses.empty() ? full_qw : device_view(full_qw);
+  const void* src_st = misses.empty() ? full_st : device_view(full_st);
+  if (src_qw != nullptr && src_st != nullptr && a16(pool_qw) && a16(src_qw) && a16(pool_st) &&
+      a16(src_st) && qw_stride_bytes % 16 == 0 && st_stride_bytes % 16 == 0 &&
+      qw_expert_bytes % 16 == 0 && st_expert_bytes % 16 == 0) {
     FillParams fp = {};
     fp.pool_qw = static_cast<uint8_t*>(pool_qw);
-    fp.full_qw = static_cast<const uint8_t*>(full_qw);
+    fp.full_qw = static_cast<const uint8_t*>(src_qw);
     fp.pool_st = static_cast<uint8_t*>(pool_st);
-    fp.full_st = static_cast<const uint8_t*>(full_st);
+    fp.full_st = static_cast<const uint8_t*>(src_st);
     fp.qw_stride = qw_stride_bytes;
     fp.st_stride = st_stride_bytes;
     fp.qw_units = qw_expert_bytes / 16;
     fp.st_units = st_expert_bytes / 16;
     fp.slot_ids_dev = slot_ids_dev;
+    fp.slot_expert_dev = slot_expert_dev;
     fp.n_miss = (int)misses.size();
     fp.k = k;
     for (int i = 0; i < fp.n_miss; ++i) {
@@ -230,20 +270,31 @@ extern "C" w4_status w4_slot_pool_stage(w4_slot_pool* pool, const int32_t* exper
     if (n_miss) *n_miss = (int)misses.size();
     return W4_OK;
   }
-  for (const auto& m : misses) {
-    const size_t e = (size_t)m.first, slot = (size_t)m.second;
+  // Copies one by one: the refilled slots hold no expert until every copy is
+  // in (a copy that fails to enqueue leaves them so).
+  SlotEntries entries = {};
+  entries.n = (int)misses.size();
+  for (int i = 0; i < entries.n; ++i) {
+    entries.slot[i] = misses[i].second;
+    entries.expert[i] = -1;
+  }
+  if (slot_expert_dev != nullptr && entries.n > 0) {
+    write_ids_kernel<<<1, 64, 0, s>>>(nullptr, list, 0, slot_expert_dev, entries);
+    failed = cudaPeekAtLastError() != cudaSuccess;
+  }
+  for (size_t i = 0; i < misses.size() && !failed; ++i) {
+    const size_t e = (size_t)misses[i].first, slot = (size_t)misses[i].second;
     if (cudaMemcpyAsync(static_cast<uint8_t*>(pool_qw) + slot * qw_stride_bytes,
                         static_cast<const uint8_t*>(full_qw) + e * qw_stride_bytes,
-                        qw_expert_bytes, cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
+                        qw_expert_bytes, cudaMemcpyDefault, s) != cudaSuccess ||
         cudaMemcpyAsync(static_cast<uint8_t*>(pool_st) + slot * st_stride_bytes,
                         static_cast<const uint8_t*>(full_st) + e * st_stride_bytes,
-                        st_expert_bytes, cudaMemcpyDeviceToDevice, s) != cudaSuccess) {
+                        st_expert_bytes, cudaMemcpyDefault, s) != cudaSuccess)
       failed = true;
-      break;
-    }
   }
   if (!failed) {
-    write_ids_kernel<<<1, 64, 0, s>>>(slot_ids_dev, list, k);
+    for (int i = 0; i < entries.n; ++i) entries.expert[i] = misses[i].first;
+    write_ids_kernel<<<1, 64, 0, s>>>(slot_ids_dev, list, k, slot_expert_dev, entries);
     failed = cudaPeekAtLastError() != cudaSuccess;
   }
   if (failed) {
@@ -283,6 +334,7 @@ extern "C" const char* w4_status_str(int status) {
     case W4_ERR_TIMEOUT: return "device wait timed out";
     case W4_ERR_DEVICE: return "no usable CUDA device";
     case W4_ERR_STATE: return "slot pool request cannot be served";
+    case W4_ERR_OWNER: return "slot does not hold the named expert";
     default: return "unknown status";
   }
 }

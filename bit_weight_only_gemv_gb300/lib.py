@@ -22,11 +22,11 @@ W4_FLAG_TENSOR_CORES = 4
 _PATH_FLAGS = {None: 0, "cuda": W4_FLAG_CUDA_CORES, "tensor": W4_FLAG_TENSOR_CORES}
 STATUS = {0: "W4_OK", 1: "W4_ERR_ARG", 2: "W4_ERR_ALIGN", 3: "W4_ERR_SHAPE",
           4: "W4_ERR_WORKSPACE", 5: "W4_ERR_LAUNCH", 6: "W4_ERR_INDEX", 7: "W4_ERR_VALUE",
-          8: "W4_ERR_TIMEOUT", 9: "W4_ERR_DEVICE", 10: "W4_ERR_STATE"}
+          8: "W4_ERR_TIMEOUT", 9: "W4_ERR_DEVICE", 10: "W4_ERR_STATE", 11: "W4_ERR_OWNER"}
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 
 EXPORTS = ("w4_status_str", "w4_abi_version", "w4_last_cuda_error", "w4a16_gemv", "w4a16_gemv_workspace_bytes", "w4a16_gemv_workspace_bytes_flags",
-           "w4a16_gemv_id", "w4_embed_gather", "w4_pack", "w4_quantize",
+           "w4a16_gemv_id", "w4a16_gemv_id_scaled", "w4_embed_gather", "w4_pack", "w4_quantize",
            "w4_slot_pool_create", "w4_slot_pool_destroy", "w4_slot_pool_remap",
            "w4_slot_pool_stage", "w4_slot_pool_stats", "w4a16_gemv_plan",
            "w4a16_gemv_static_scratch")
@@ -75,6 +75,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.w4a16_gemv_workspace_bytes_flags.argtypes = [i32, i32, i32, ctypes.c_uint]
     lib.w4a16_gemv_id.restype = i32
     lib.w4a16_gemv_id.argtypes = [vp, vp, sz, vp, sz, i32, vp, i32, vp, i32, i32, i32, vp, u32, vp]
+    lib.w4a16_gemv_id_scaled.restype = i32
+    lib.w4a16_gemv_id_scaled.argtypes = [vp, vp, sz, vp, sz, i32, vp, i32, vp, i32, i32, i32,
+                                         vp, i32, vp, vp, vp, vp, u32, vp]
     lib.w4_embed_gather.restype = i32
     lib.w4_embed_gather.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, u32, vp]
     lib.w4_pack.restype = i32
@@ -88,8 +91,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.w4_slot_pool_remap.restype = i32
     lib.w4_slot_pool_remap.argtypes = [vp, i32p, i32, i32p, i32p, i32p, ctypes.POINTER(i32)]
     lib.w4_slot_pool_stage.restype = i32
-    lib.w4_slot_pool_stage.argtypes = [vp, i32p, i32, vp, vp, sz, sz, vp, vp, sz, sz, vp, i32p,
-                                       ctypes.POINTER(i32), vp]
+    lib.w4_slot_pool_stage.argtypes = [vp, i32p, i32, vp, vp, sz, sz, vp, vp, sz, sz, vp, vp,
+                                       i32p, ctypes.POINTER(i32), vp]
     lib.w4_slot_pool_stats.restype = None
     lib.w4_slot_pool_stats.argtypes = [vp] + [ctypes.POINTER(ctypes.c_longlong)] * 3
     lib.w4a16_gemv_plan.restype = i32
@@ -221,6 +224,63 @@ def bind_gemv_id(qw_base: torch.Tensor, st_base: torch.Tensor, ids: torch.Tensor
     return call
 
 
+def _scaled_args(y, qw_base, qw_stride_bytes, st_base, st_stride_bytes, num_slots, ids, x, N, K,
+                 expert_ids, num_experts, slot_expert, scale, bias, status):
+    _need(ids, torch.int32, "ids")
+    _need(expert_ids, torch.int32, "expert_ids")
+    _need(x, torch.bfloat16, "x")
+    _need(y, torch.bfloat16, "y")
+    if expert_ids.numel() != ids.numel():
+        raise ValueError("expert_ids must have one entry per id")
+    if slot_expert is not None:
+        _need(slot_expert, torch.int32, "slot_expert")
+    for name, t in (("scale", scale), ("bias", bias)):
+        if t is not None:
+            _need(t, torch.bfloat16, name)
+            if t.numel() != num_experts * N:
+                raise ValueError(f"{name} must be [num_experts][N]")
+    if not (qw_base.is_cuda and st_base.is_cuda):
+        raise ValueError("bases must be CUDA tensors")
+    x2 = x if x.dim() == 2 else x.view(1, -1)
+    return x2, (_ptr(y), _ptr(qw_base), qw_stride_bytes, _ptr(st_base), st_stride_bytes,
+                num_slots, _ptr(ids), ids.numel(), _ptr(x2), x2.shape[0], N, K, _ptr(expert_ids),
+                num_experts, _ptr(slot_expert), _ptr(scale), _ptr(bias), _ptr(status))
+
+
+def gemv_id_scaled(qw_base: torch.Tensor, st_base: torch.Tensor, ids: torch.Tensor,
+                   x: torch.Tensor, N: int, K: int, num_slots: int, qw_stride_bytes: int,
+                   st_stride_bytes: int, expert_ids: torch.Tensor, num_experts: int,
+                   slot_expert: torch.Tensor = None, scale: torch.Tensor = None,
+                   bias: torch.Tensor = None, y: torch.Tensor = None,
+                   status: torch.Tensor = None, pdl: bool = False, stream=None) -> torch.Tensor:
+    """y[i] = bf16(fma(W_{ids[i]} @ x[i or 0], scale[e], bias[e])), e = expert_ids[i]:
+    weights through slot (or expert) ids, per-expert vectors through real ids."""
+    if y is None:
+        y = torch.empty((ids.numel(), N), dtype=torch.bfloat16, device=x.device)
+    _, args = _scaled_args(y, qw_base, qw_stride_bytes, st_base, st_stride_bytes, num_slots, ids,
+                           x, N, K, expert_ids, num_experts, slot_expert, scale, bias, status)
+    _check(load().w4a16_gemv_id_scaled(*args, W4_FLAG_PDL if pdl else 0, _stream(stream)),
+           "w4a16_gemv_id_scaled")
+    return y
+
+
+def bind_gemv_id_scaled(qw_base, st_base, ids, x, N, K, num_slots, qw_stride_bytes,
+                        st_stride_bytes, expert_ids, num_experts, y, slot_expert=None,
+                        scale=None, bias=None, status=None):
+    """w4a16_gemv_id_scaled with its arguments marshalled once: returns
+    call(pdl=False, stream=None)."""
+    x2, args = _scaled_args(y, qw_base, qw_stride_bytes, st_base, st_stride_bytes, num_slots,
+                            ids, x, N, K, expert_ids, num_experts, slot_expert, scale, bias,
+                            status)
+    fn = load().w4a16_gemv_id_scaled
+
+    def call(pdl: bool = False, stream=None):
+        _check(fn(*args, W4_FLAG_PDL if pdl else 0, _stream(stream)), "w4a16_gemv_id_scaled")
+
+    call.tensors = (qw_base, st_base, ids, x2, y, expert_ids, slot_expert, scale, bias, status)
+    return call
+
+
 def embed_gather(qw: torch.Tensor, st: torch.Tensor, ids: torch.Tensor, out: torch.Tensor = None,
                  status: torch.Tensor = None, pdl: bool = False, stream=None) -> torch.Tensor:
     qw = _as_words(qw)
@@ -286,8 +346,10 @@ class SlotPool:
         return list(slots), [(me[i], ms[i]) for i in range(nm.value)]
 
     def stage(self, ids, pool_qw, full_qw, qw_stride, qw_bytes, pool_st, full_st, st_stride,
-              st_bytes, slot_ids_dev: torch.Tensor, stream=None):
-        """Remap, copy missed experts into the pool and write slot ids, all on `stream`."""
+              st_bytes, slot_ids_dev: torch.Tensor, stream=None, slot_expert=None):
+        """Remap, copy missed experts into the pool and write slot ids (and, when
+        given, the device slot table), all on `stream`.  full_qw / full_st may
+        be CUDA tensors or page-locked CPU tensors."""
         ids = [int(v) for v in ids]
         k = len(ids)
         arr = (ctypes.c_int32 * k)(*ids)
@@ -295,20 +357,22 @@ class SlotPool:
         nm = ctypes.c_int()
         _check(self._lib.w4_slot_pool_stage(self._h, arr, k, _ptr(pool_qw), _ptr(full_qw),
                                             qw_stride, qw_bytes, _ptr(pool_st), _ptr(full_st),
-                                            st_stride, st_bytes, _ptr(slot_ids_dev), slots,
-                                            ctypes.byref(nm), _stream(stream)),
+                                            st_stride, st_bytes, _ptr(slot_ids_dev),
+                                            _ptr(slot_expert), slots, ctypes.byref(nm),
+                                            _stream(stream)),
                "w4_slot_pool_stage")
         return list(slots), nm.value
 
     def bind_stage(self, k: int, pool_qw, full_qw, qw_stride, qw_bytes, pool_st, full_st,
-                   st_stride, st_bytes, slot_ids_dev: torch.Tensor):
+                   st_stride, st_bytes, slot_ids_dev: torch.Tensor, slot_expert=None):
         """stage() with the buffers marshalled once: returns call(ids, stream=None)
         for requests of k ids (any int sequence), which returns the misses."""
         arr = (ctypes.c_int32 * k)()
         slots = (ctypes.c_int32 * k)()
         nm = ctypes.c_int()
         fixed = (_ptr(pool_qw), _ptr(full_qw), qw_stride, qw_bytes, _ptr(pool_st), _ptr(full_st),
-                 st_stride, st_bytes, _ptr(slot_ids_dev), slots, ctypes.byref(nm))
+                 st_stride, st_bytes, _ptr(slot_ids_dev), _ptr(slot_expert), slots,
+                 ctypes.byref(nm))
         fn, h = self._lib.w4_slot_pool_stage, self._h
 
         def call(ids, stream=None) -> int:
@@ -319,7 +383,7 @@ class SlotPool:
             _check(fn(h, arr, k, *fixed, _stream(stream)), "w4_slot_pool_stage")
             return nm.value
 
-        call.tensors = (pool_qw, full_qw, pool_st, full_st, slot_ids_dev)
+        call.tensors = (pool_qw, full_qw, pool_st, full_st, slot_ids_dev, slot_expert)
         return call
 
     def stats(self):

@@ -77,9 +77,11 @@ typedef enum w4_status {
     W4_ERR_VALUE = 7,      /* device-side: a code outside 0..15 (w4_pack) */
     W4_ERR_TIMEOUT = 8,    /* device-side: a bounded wait in a kernel expired */
     W4_ERR_DEVICE = 9,     /* no usable CUDA device / attribute query failed */
-    W4_ERR_STATE = 10      /* slot pool: request cannot be served, or a pool
+    W4_ERR_STATE = 10,     /* slot pool: request cannot be served, or a pool
                               copy failed (the pool forgot the experts it was
                               loading) */
+    W4_ERR_OWNER = 11      /* device-side: a slot does not hold the expert
+                              named for it (w4a16_gemv_id_scaled) */
 } w4_status;
 
 #define W4_FLAG_PDL 1u
@@ -89,7 +91,7 @@ typedef enum w4_status {
 #define W4_GROUP 32        /* codes per group along K */
 #define W4_MAX_K 65536     /* largest supported K */
 #define W4_MAX_M 32        /* largest batch of activation rows per call */
-#define W4_ABI_VERSION 3
+#define W4_ABI_VERSION 4
 
 /* Human-readable name of a status code (static string). */
 const char *w4_status_str(int status);
@@ -214,6 +216,47 @@ w4_status w4a16_gemv_id(void *y, const void *qw_base, size_t qw_stride_bytes,
                         w4_stream_t stream);
 
 /*
+ * w4a16_gemv_id_scaled — routed-expert GEMV whose outputs also take
+ * per-expert vectors indexed by the REAL expert id.
+ *
+ * Page "Running a 26B MoE on an 8 GB Jetson by streaming experts from SSD",
+ * section "Streaming without touching a single GPU kernel": the selected
+ * expert ids feed several consumers; only the expert matmul may read slot
+ * ids, while the per-expert scale vectors and the expert biases stay fully
+ * resident and must be indexed by the actual expert number.  Feeding them
+ * slot ids crashes nothing and silently degrades the model; here the call
+ * takes both ids, and given the pool's slot table it checks on the device
+ * that every slot holds the expert named for it.
+ *
+ *   s = ids[i] (slot, or expert, whose weights are read),  e = expert_ids[i]
+ *   acc = the fp32 sum of w4a16_gemv_id for row i (same bits)
+ *   y[i][n] = bf16( fma(acc, scale[e][n], bias[e][n]) )   (one fp32 rounding,
+ *             then one bf16 rounding; scale 1 and bias 0 when NULL, which
+ *             gives exactly the bits of w4a16_gemv_id)
+ *
+ * y, qw_base, qw_stride_bytes, st_base, st_stride_bytes, num_slots, ids,
+ * n_ids, x, x_rows, N, K
+ *                as for w4a16_gemv_id (num_slots in the role of num_experts).
+ * expert_ids     device int32 [n_ids]: the real expert of row i, in
+ *                [0, num_experts); outside it y[i] is left unwritten and
+ *                W4_ERR_INDEX is recorded.
+ * num_experts    >= 1, rows of scale and bias.
+ * slot_expert    device int32 [num_slots] or NULL: the expert each slot
+ *                holds (-1: none), as kept by w4_slot_pool_stage.  When
+ *                given, a row with slot_expert[ids[i]] != expert_ids[i] is
+ *                left unwritten and W4_ERR_OWNER is recorded.
+ * scale, bias    bf16 [num_experts][N] (2-byte aligned), or NULL.
+ * flags          W4_FLAG_PDL or 0.
+ */
+w4_status w4a16_gemv_id_scaled(void *y, const void *qw_base, size_t qw_stride_bytes,
+                               const void *st_base, size_t st_stride_bytes, int num_slots,
+                               const int32_t *ids, int n_ids, const void *x, int x_rows,
+                               int N, int K, const int32_t *expert_ids, int num_experts,
+                               const int32_t *slot_expert, const void *scale,
+                               const void *bias, int32_t *status_dev, unsigned flags,
+                               w4_stream_t stream);
+
+/*
  * w4_embed_gather — dequantised rows of a 4-bit vocabulary table.
  *
  * Page "Gemma 4 on a 4 GB GPU in Plain PyTorch", section "Step 2 — Keep the
@@ -311,13 +354,22 @@ w4_status w4_slot_pool_remap(w4_slot_pool *pool, const int32_t *expert_ids, int 
  * loaded are dropped from the pool (their slots become free) and
  * W4_ERR_STATE is returned, so stale slot contents are never used.
  * slot_ids / n_miss (host, optional, may be NULL) receive the remap.
+ *
+ * full_qw / full_st may live in device memory or in page-locked host memory
+ * (on GB300 the Grace CPU's memory, read by the GPU over NVLink-C2C): the
+ * fill kernel reads them in place, the copy fallback uses cudaMemcpyDefault.
+ *
+ * slot_expert_dev (device int32 [num_slots], or NULL) is the pool's slot
+ * table for w4a16_gemv_id_scaled: the caller fills it with -1 once, then each
+ * stage marks the slots it refills as holding no expert before their copies
+ * and names the new expert once they are complete, in stream order.
  */
 w4_status w4_slot_pool_stage(w4_slot_pool *pool, const int32_t *expert_ids, int k,
                              void *pool_qw, const void *full_qw, size_t qw_stride_bytes,
                              size_t qw_expert_bytes, void *pool_st, const void *full_st,
                              size_t st_stride_bytes, size_t st_expert_bytes,
-                             int32_t *slot_ids_dev, int32_t *slot_ids, int *n_miss,
-                             w4_stream_t stream);
+                             int32_t *slot_ids_dev, int32_t *slot_expert_dev,
+                             int32_t *slot_ids, int *n_miss, w4_stream_t stream);
 
 /* Counters since creation: requests served (ids), hits, misses (copies). */
 void w4_slot_pool_stats(const w4_slot_pool *pool, long long *requests, long long *hits,

@@ -8,7 +8,8 @@ package imports nothing from the product.
 
 Modules
 -------
-ref         dequantisation, GEMV, routed-expert GEMV, row gather, quantiser,
+ref         dequantisation, GEMV, routed-expert GEMV (plain and with per-expert
+            output vectors by real id), row gather, quantiser,
             bf16 rounding and the acceptance bound (NumPy, fp64).
 lfu         the per-layer LFU expert-slot pool policy (pure Python).
 magic_check.c
@@ -28,6 +29,7 @@ from .ref import (  # noqa: F401
     gemv_ref,
     gemv_abs_ref,
     gemv_id_ref,
+    gemv_id_scaled_ref,
     gather_ref,
     quantize_ref,
     within_bound,

@@ -183,6 +183,37 @@ def gemv_id_ref(qw_experts: np.ndarray, st_experts: np.ndarray,
     return np.stack(rows) if rows else np.zeros((0, qw_experts.shape[1]))
 
 
+def gemv_id_scaled_ref(qw_experts: np.ndarray, st_experts: np.ndarray, expert_ids: np.ndarray,
+                       x_bits: np.ndarray, scale_bits=None, bias_bits=None):
+    """Routed-expert GEMV with per-expert output vectors, by REAL expert id.
+
+    [MoE] "Streaming without touching a single GPU kernel": the selected ids
+    feed several consumers; the per-expert scale vectors and expert biases
+    are fully resident and indexed by the actual expert number (only the
+    matmul may be pointed at a slot pool).  So, with e = expert_ids[i]:
+
+        y_ref[i, n] = scale[e, n] * (W_e x_i)[n] + bias[e, n]
+
+    from the FULL expert tensor (a pool is an addressing detail that must not
+    change the bits).  ``scale_bits`` / ``bias_bits`` are bf16 bit patterns
+    [E, N] or None (1 and 0).  Returns (y_ref, abs_ref) in fp64, where
+    abs_ref = |scale| * sum_k |w x| is the scale of the acceptance bound.
+    """
+    ids = np.asarray(expert_ids).reshape(-1)
+    y = gemv_id_ref(qw_experts, st_experts, ids, x_bits)
+    x = np.atleast_2d(x_bits)
+    a = np.stack([gemv_abs_ref(qw_experts[e], st_experts[e],
+                               x[0] if x.shape[0] == 1 else x[i])[0]
+                  for i, e in enumerate(ids)])
+    if scale_bits is not None:
+        s = bf16_bits_to_f64(np.asarray(scale_bits))[ids]
+        y = s * y
+        a = np.abs(s) * a
+    if bias_bits is not None:
+        y = y + bf16_bits_to_f64(np.asarray(bias_bits))[ids]
+    return y, a
+
+
 def gather_ref(qw: np.ndarray, st: np.ndarray, ids: np.ndarray) -> np.ndarray:
     """out[t, k] = bf16((code[ids[t], k] - 8) * step[ids[t], k // 32]).
 

@@ -29,7 +29,8 @@ def header_functions():
 
 def test_header_declares_the_calls():
     names = header_functions()
-    for need in ("w4a16_gemv", "w4a16_gemv_id", "w4_embed_gather", "w4_pack", "w4_quantize"):
+    for need in ("w4a16_gemv", "w4a16_gemv_id", "w4a16_gemv_id_scaled", "w4_embed_gather",
+                 "w4_pack", "w4_quantize"):
         assert need in names
 
 
@@ -41,9 +42,10 @@ def test_library_exports_every_declared_call(L):
 
 
 def test_version_and_status_strings(L):
-    assert L.w4_abi_version() == 3
+    assert L.w4_abi_version() == 4
     assert L.w4_status_str(0) == b"ok"
     assert L.w4_status_str(6) == b"id out of range"
+    assert L.w4_status_str(11) == b"slot does not hold the named expert"
     assert L.w4_status_str(999) == b"unknown status"
 
 
@@ -70,6 +72,16 @@ def test_host_validation_rejects_before_any_launch(L):
                            None) == 2
     assert L.w4a16_gemv_id(good, good, 512, good, 128, 4, good, 3, good, 1, 32, 64, None, 0,
                            None) == 1
+    # gemv_id_scaled: real ids required, vectors 2-byte aligned, table 4-byte aligned
+    def scaled(eids=good, n_real=8, table=None, scale=None, bias=None, x_rows=1):
+        return L.w4a16_gemv_id_scaled(good, good, 1024, good, 128, 4, good, 3, good, x_rows, 32,
+                                      64, eids, n_real, table, scale, bias, None, 0, None)
+    assert scaled(eids=None) == 1
+    assert scaled(n_real=0) == 1
+    assert scaled(x_rows=2) == 3
+    assert scaled(scale=vp((1 << 20) + 1)) == 2
+    assert scaled(bias=vp((1 << 20) + 3)) == 2
+    assert scaled(table=vp((1 << 20) + 2)) == 2
     assert L.w4_embed_gather(good, good, good, good, 0, 10, 64, None, 0, None) == 1
     assert L.w4_pack(good, good, 4, 40, None, None) == 3
     assert L.w4_quantize(good, good, vp((1 << 20) + 4), 4, 64, None) == 2
@@ -174,7 +186,7 @@ def test_slot_pool_failed_copy_forgets_the_slot():
     fake_ptr = type("P", (), {"data_ptr": lambda self: 1 << 20})()
     with pytest.raises(lib.W4Error) as ei:
         pool.stage([3], fake_ptr, fake_ptr, 4096, 4096, fake_ptr, fake_ptr, 512, 512, fake_ptr,
-                   stream=type("S", (), {"cuda_stream": 0})())
+                   stream=type("S", (), {"cuda_stream": 0})(), slot_expert=fake_ptr)
     assert ei.value.name == "W4_ERR_STATE"
     # the expert is not resident: the next request for it is a miss again
     assert pool.remap([3]) == ([0], [(3, 0)])

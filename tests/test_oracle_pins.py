@@ -215,6 +215,77 @@ def test_gemv_id_addresses_experts_and_broadcasts():
         ref.gemv_id_ref(qw, st, ids, synth.np_x(rng, (2, k)))
 
 
+def _bf16_bits(rng, shape, lo=-2.0, hi=2.0):
+    return f32_to_bf16_bits_torch(rng.uniform(lo, hi, size=shape))
+
+
+def test_gemv_id_scaled_exact_bruteforce_by_real_ids():
+    # y[i][n] = scale[e][n] * (W_e x_i)[n] + bias[e][n], e the REAL expert id,
+    # checked against rationals built from the raw bits
+    rng = np.random.default_rng(21)
+    e, n, k = 4, 3, 32
+    qw = synth.np_words(rng, (e, n, k // 8))
+    st = synth.np_steps(rng, (e, n, k // 32), scale=1.0)
+    sc = _bf16_bits(rng, (e, n))
+    bi = _bf16_bits(rng, (e, n))
+    eids = np.array([3, 1, 3], dtype=np.int32)
+    x = synth.np_x(rng, (3, k))
+    y, a = ref.gemv_id_scaled_ref(qw, st, eids, x, sc, bi)
+    for i, ex in enumerate(eids):
+        dot, dot_abs = exact_gemv(qw[ex], st[ex], x[i:i + 1])
+        for ni in range(n):
+            s_ = frac_bf16(int(sc[ex, ni]))
+            want = s_ * dot[0][ni] + frac_bf16(int(bi[ex, ni]))
+            assert abs(Fraction(y[i, ni]) - want) <= Fraction(2) ** -45 * (abs(want) + 1)
+            assert abs(Fraction(a[i, ni]) - abs(s_) * dot_abs[0][ni]) <= \
+                Fraction(2) ** -45 * (abs(s_) * dot_abs[0][ni] + 1)
+
+
+def test_gemv_id_scaled_special_cases():
+    rng = np.random.default_rng(22)
+    e, n, k = 6, 5, 64
+    qw = synth.np_words(rng, (e, n, k // 8))
+    st = synth.np_steps(rng, (e, n, k // 32), scale=1.0)
+    eids = np.array([5, 0, 2, 5], dtype=np.int32)
+    x = synth.np_x(rng, (1, k))
+    plain = ref.gemv_id_ref(qw, st, eids, x)
+    # no vectors: the plain routed product
+    y, a = ref.gemv_id_scaled_ref(qw, st, eids, x)
+    assert np.array_equal(y, plain)
+    # zero activations: exactly the bias row of the real expert
+    bi = _bf16_bits(rng, (e, n))
+    y0, a0 = ref.gemv_id_scaled_ref(qw, st, eids, np.zeros((1, k), np.uint16), None, bi)
+    for i, ex in enumerate(eids):
+        for ni in range(n):
+            assert Fraction(y0[i, ni]) == frac_bf16(int(bi[ex, ni]))
+    assert not np.any(a0)
+    # power-of-two scales: exact scaling of the plain product, row by row
+    pw = rng.integers(-3, 4, size=(e, n))
+    sc = f32_to_bf16_bits_torch(np.ldexp(1.0, pw).astype(np.float32))
+    ys, _ = ref.gemv_id_scaled_ref(qw, st, eids, x, sc, None)
+    assert np.array_equal(ys, plain * np.ldexp(1.0, pw[eids]))
+
+
+def test_gemv_id_scaled_slot_ids_fed_to_the_vectors_change_the_result():
+    # The page's hazard: a consumer of per-expert vectors given slot ids
+    # instead of real ids.  With distinct per-expert biases the planted
+    # mistake (vectors indexed by slot id) cannot pass for the real result.
+    rng = np.random.default_rng(23)
+    e, n, k = 8, 4, 32
+    qw = synth.np_words(rng, (e, n, k // 8))
+    st = synth.np_steps(rng, (e, n, k // 32), scale=1.0)
+    bi = _bf16_bits(rng, (e, n), 1.0, 2.0)
+    pool = oracle.LFUSlotPoolRef(e, 3)
+    x = synth.np_x(rng, (1, k))
+    for req in ([6, 2], [2, 7], [5, 6]):
+        slots, _ = pool.step(req)
+        good, _ = ref.gemv_id_scaled_ref(qw, st, np.array(req), x, None, bi)
+        # weights by real id, vectors by slot id
+        bad = ref.gemv_id_ref(qw, st, np.array(req), x) + \
+            ref.bf16_bits_to_f64(bi)[np.array(slots)]
+        assert not np.array_equal(good, bad)
+
+
 # ---------------------------------------------------------------- bf16
 def test_bf16_rne_hand_values():
     cases = [
