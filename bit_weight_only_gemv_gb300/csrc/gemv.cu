@@ -1452,13 +1452,18 @@ size_t tc_workspace(int M, int N, int K, int sms) {
 w4_status tc_enqueue(void* y, const void* qw, const void* st, const void* x, int M, int N, int K,
                      void* workspace, size_t workspace_bytes, int32_t* status_dev, bool pdl,
                      cudaStream_t s, int dev, int sms) {
+  // every launch of the call is checked before the first one is enqueued
   for (int m0 = 0; m0 < M; m0 += tc::kTcMaxM) {
-    const int mr = std::min(tc::kTcMaxM, M - m0);
     tc::TcPlan tp;
-    if (!tc::tc_plan(mr, N, K, sms, &tp)) return W4_ERR_SHAPE;
+    if (!tc::tc_plan(std::min(tc::kTcMaxM, M - m0), N, K, sms, &tp)) return W4_ERR_SHAPE;
     if (tp.ws_bytes > 0 && (workspace == nullptr || workspace_bytes < tp.ws_bytes))
       return W4_ERR_WORKSPACE;
     if (tp.ws_bytes > 0 && !aligned(workspace, 16)) return W4_ERR_ALIGN;
+  }
+  for (int m0 = 0; m0 < M; m0 += tc::kTcMaxM) {
+    const int mr = std::min(tc::kTcMaxM, M - m0);
+    tc::TcPlan tp;
+    tc::tc_plan(mr, N, K, sms, &tp);
     const cudaError_t e =
         tc::tc_launch(tp, static_cast<__nv_bfloat16*>(y) + (long long)m0 * N, qw, st,
                       static_cast<const __nv_bfloat16*>(x) + (long long)m0 * K, mr, N, K, workspace,
@@ -1568,13 +1573,19 @@ extern "C" w4_status w4a16_gemv(void* y, const void* qw, const void* st, const v
                       (flags & W4_FLAG_PDL) != 0, s, dev, di.sms);
   const int mr_cap = max_rows_per_launch(K, di);
   if (mr_cap < 1) return W4_ERR_SHAPE;
+  // every launch of the call is checked before the first one is enqueued
   for (int m0 = 0; m0 < M; m0 += mr_cap) {
-    const int mr = std::min(mr_cap, M - m0);
     Plan pm;
-    if (!cached_plan(mr, N, K, 1, 1, 0, false, di, &pm)) return W4_ERR_SHAPE;
+    if (!cached_plan(std::min(mr_cap, M - m0), N, K, 1, 1, 0, false, di, &pm))
+      return W4_ERR_SHAPE;
     if (pm.ws_bytes > 0 && (workspace == nullptr || workspace_bytes < pm.ws_bytes))
       return W4_ERR_WORKSPACE;
     if (pm.ws_bytes > 0 && !aligned(workspace, 16)) return W4_ERR_ALIGN;
+  }
+  for (int m0 = 0; m0 < M; m0 += mr_cap) {
+    const int mr = std::min(mr_cap, M - m0);
+    Plan pm;
+    cached_plan(mr, N, K, 1, 1, 0, false, di, &pm);
     GemvParams p = base_params(pm, N, K);
     p.qw = static_cast<const uint8_t*>(qw);
     p.st = static_cast<const uint8_t*>(st);

@@ -90,7 +90,10 @@ typedef enum w4_status {
 
 #define W4_GROUP 32        /* codes per group along K */
 #define W4_MAX_K 65536     /* largest supported K */
-#define W4_MAX_M 32        /* largest batch of activation rows per call */
+/* Largest batch of activation rows per call: a prompt chunk of 256 tokens
+ * (page "Gemma 4 on a 4 GB GPU in Plain PyTorch", section "Step 6 — Read
+ * Prompts in 32-Bit on a Card Without Tensor Cores"). */
+#define W4_MAX_M 256
 #define W4_ABI_VERSION 4
 
 /* Human-readable name of a status code (static string). */
@@ -116,7 +119,10 @@ const char *w4_last_cuda_error(void);
  * qw         uint32 [N][K/8], 16-byte aligned.
  * st         bf16 [N][K/32], 16-byte aligned.
  * x          bf16 [M][K], 16-byte aligned.
- * M          1 .. W4_MAX_M activation rows.
+ * M          1 .. W4_MAX_M activation rows.  The CUDA-core path takes up to 4
+ *            rows per launch and the tensor-core path up to 32; a call with
+ *            more rows enqueues several launches (each reading the weights),
+ *            all checked before the first is enqueued.
  * N          >= 1 output rows.
  * K          multiple of 32, 32 .. W4_MAX_K.
  * workspace  device scratch of at least w4a16_gemv_workspace_bytes(M, N, K)

@@ -57,7 +57,7 @@ def test_host_validation_rejects_before_any_launch(L):
     # null pointer
     assert L.w4a16_gemv(None, good, good, good, 1, 16, 64, None, 0, None, 0, None) == 1
     # M out of range
-    assert L.w4a16_gemv(good, good, good, good, 33, 16, 64, None, 0, None, 0, None) == 3
+    assert L.w4a16_gemv(good, good, good, good, 257, 16, 64, None, 0, None, 0, None) == 3
     # misaligned weights
     assert L.w4a16_gemv(good, vp((1 << 20) + 8), good, good, 1, 16, 64, None, 0, None, 0,
                         None) == 2

@@ -131,3 +131,21 @@ def test_tensor_core_pdl_chain(cuda_lib):
         assert not np.any(host_bits(y) == POISON)
         assert torch.equal(y.view(torch.int16), ys[0].view(torch.int16))
     assert_gemv_parity(ys[0], qw_h, st_h, x_h)
+
+
+@pytest.mark.parametrize("n,k,m", [(300, 2048, 64), (1000, 1024, 100), (256, 5376, 256)])
+def test_prompt_chunks_beyond_one_launch(cuda_lib, n, k, m):
+    """More activation rows than one launch takes (a prompt chunk of up to 256
+    tokens): oracle bound on every output, and each row bitwise equal to a
+    call with that row alone pinned to the same path."""
+    rng = np.random.default_rng(n + k + m)
+    qw_h, st_h, x_h = make(rng, n, k, m)
+    y = run(qw_h, st_h, x_h)
+    assert_gemv_parity(y, qw_h, st_h, x_h)
+    yb = host_bits(y)
+    for i in (0, 31, 32, m - 1):
+        yi = run(qw_h, st_h, x_h[i:i + 1], path="tensor")
+        assert np.array_equal(host_bits(yi)[0], yb[i])
+    # the CUDA-core path at the same M: 4 rows per launch
+    yc = run(qw_h, st_h, x_h[:40], path="cuda")
+    assert_gemv_parity(yc, qw_h, st_h, x_h[:40])
