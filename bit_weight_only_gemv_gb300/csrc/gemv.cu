@@ -1440,6 +1440,8 @@ int path_of(int M, int K, unsigned flags) {
 
 // Largest workspace of the tensor-core launches of an (M, N, K) call.
 size_t tc_workspace(int M, int N, int K, int sms) {
+  tc::TpPlan pp;
+  if (M > tc::kTcMaxM && tc::tp_plan(M, N, K, sms, &pp)) return 0;   // one prompt launch
   size_t ws = 0;
   for (int m0 = 0; m0 < M; m0 += tc::kTcMaxM) {
     tc::TcPlan tp;
@@ -1452,6 +1454,17 @@ size_t tc_workspace(int M, int N, int K, int sms) {
 w4_status tc_enqueue(void* y, const void* qw, const void* st, const void* x, int M, int N, int K,
                      void* workspace, size_t workspace_bytes, int32_t* status_dev, bool pdl,
                      cudaStream_t s, int dev, int sms) {
+  // more rows than a small-batch launch takes: one launch of the prompt GEMM
+  tc::TpPlan pp;
+  if (M > tc::kTcMaxM && tc::tp_plan(M, N, K, sms, &pp)) {
+    const cudaError_t e = tc::tp_launch(pp, y, qw, st, x, M, N, K, status_dev, pdl, s, dev);
+    if (e != cudaSuccess) {
+      note_cuda_error(e);
+      cudaGetLastError();
+      return W4_ERR_LAUNCH;
+    }
+    return W4_OK;
+  }
   // every launch of the call is checked before the first one is enqueued
   for (int m0 = 0; m0 < M; m0 += tc::kTcMaxM) {
     tc::TcPlan tp;
@@ -1488,6 +1501,26 @@ extern "C" w4_status w4a16_gemv_plan(int M, int N, int K, w4_plan_info* info) {
   if (M > W4_MAX_M || K < 32 || K % 32 != 0 || K > W4_MAX_K) return W4_ERR_SHAPE;
   DeviceInfo di;
   planning_device(&di);
+  tc::TpPlan pp;
+  if (path_of(M, K, 0) == 1 && M > tc::kTcMaxM && tc::tp_plan(M, N, K, di.sms, &pp)) {
+    *info = w4_plan_info{};
+    info->path = 3;
+    info->ctas = pp.ctas;
+    info->slices = 1;
+    info->threads = 320;   // 4 unpacking, 4 epilogue, copy and MMA warps
+    info->team = 1;
+    info->unit_rows = 128;
+    info->chunk_groups = 32;
+    info->rows_per_lane = 1;
+    info->smem_bytes = pp.smem;
+    info->rows_per_call = M;
+    info->chunk_steps = 8;
+    info->stages = pp.xs;
+    info->ctas_per_sm = 1;
+    info->tmpl_team = pp.nt;
+    info->tmpl_chunk = 0;
+    return W4_OK;
+  }
   if (path_of(M, K, 0) == 1) {
     tc::TcPlan tp;
     if (!tc::tc_plan(std::min(M, tc::kTcMaxM), N, K, di.sms, &tp)) return W4_ERR_SHAPE;

@@ -31,5 +31,21 @@ cudaError_t tc_launch(const TcPlan& pl, void* y, const void* qw, const void* st,
 
 int tc_sms(int dev);
 
+// Prompt chunks (more rows than one small-batch launch takes, up to
+// kTpMaxM): one launch of the exact hi/lo-split tcgen05 GEMM.
+constexpr int kTpMaxM = 256;
+
+struct TpPlan {
+  int xrows = 0, nt = 0;      // activation rows per unit tile, MMA N
+  int tiles = 0, units = 0, ctas = 0;
+  int xs = 0, x_stage_bytes = 0, smem = 0;
+};
+
+bool tp_plan(int M, int N, int K, int sms, TpPlan* out);
+
+cudaError_t tp_launch(const TpPlan& pl, void* y, const void* qw, const void* st, const void* x,
+                      int M, int N, int K, int32_t* status, bool pdl, cudaStream_t stream,
+                      int dev);
+
 }  // namespace tc
 }  // namespace w4

@@ -47,8 +47,11 @@
  *     packed fp16 with fp16 partial sums of 4 products; its rows do not
  *     depend on M.  The tensor-core path (w4a16_gemv with 8 or more rows and
  *     K a multiple of 256) lets tcgen05 MMAs take exact bf16 products with
- *     fp32 sums; its rows do not depend on M either, but differ from the
- *     CUDA-core path's in the last bits.  W4_FLAG_CUDA_CORES or
+ *     fp32 sums: up to 32 rows it folds each group's step into the sum after
+ *     the MMA, from 33 rows (prompt chunks) it splits each weight exactly
+ *     into two bf16 parts and accumulates over the whole of K.  Within
+ *     each of these kernels rows do not depend on M; the kernels differ from
+ *     each other in the last bits.  W4_FLAG_CUDA_CORES or
  *     W4_FLAG_TENSOR_CORES pins the path.
  */
 #ifndef W4A16_H
@@ -386,7 +389,10 @@ void w4_slot_pool_stats(const w4_slot_pool *pool, long long *requests, long long
  * Returns W4_OK and fills *info, or an argument error for an invalid shape.
  */
 typedef struct w4_plan_info {
-    int path;           /* 1 = tile-streamed CUDA-core packed-fp16 kernel */
+    int path;           /* 1 = tile-streamed CUDA-core packed-fp16 kernel,
+                           2 = tensor-core small-batch kernel (up to 32 rows
+                           per launch), 3 = tensor-core prompt GEMM (33 to
+                           256 rows in one launch) */
     int ctas;           /* CTAs launched */
     int slices;         /* K slices (split-K); 1 = none */
     int threads;        /* threads per CTA (7 consumer warps + 1 copy warp) */

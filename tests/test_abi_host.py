@@ -133,6 +133,23 @@ def test_tensor_core_plan_is_valid(M, N, K):
     assert lib.workspace_bytes(M, N, K, "tensor") == lib.workspace_bytes(M, N, K)
 
 
+@pytest.mark.parametrize("M,N,K", [(33, 2048, 2048), (64, 16384, 2048), (100, 300, 256),
+                                   (256, 43008, 5376), (256, 5376, 21504), (200, 7, 512)])
+def test_prompt_plan_is_valid(M, N, K):
+    p = lib.plan(M, N, K)
+    assert p["path"] == 3 and p["threads"] == 320 and p["unit_rows"] == 128
+    assert p["rows_per_call"] == M and p["ctas_per_sm"] == 1
+    nt = p["tmpl_team"]                                   # MMA N: all activation rows
+    assert nt % 16 == 0 and M <= nt < M + 16 and nt <= 256
+    assert 2 <= p["stages"] <= 8
+    # more than half the SM (one CTA holds all 512 tensor-memory columns), within the limit
+    assert 233472 // 2 < p["smem_bytes"] <= 232448
+    assert p["ctas"] == min(-(-N // 128), 152)
+    assert lib.workspace_bytes(M, N, K) == 0
+    # K not a multiple of 256 stays on the CUDA cores
+    assert lib.plan(M, N, K + 32)["path"] == 1
+
+
 def test_tiling_depends_on_k_only():
     # the per-row arithmetic (team, chunk length) must not change with N or M
     for K in (704, 2048, 2816, 5376, 8192, 21504):

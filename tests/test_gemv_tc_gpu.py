@@ -133,19 +133,53 @@ def test_tensor_core_pdl_chain(cuda_lib):
     assert_gemv_parity(ys[0], qw_h, st_h, x_h)
 
 
-@pytest.mark.parametrize("n,k,m", [(300, 2048, 64), (1000, 1024, 100), (256, 5376, 256)])
-def test_prompt_chunks_beyond_one_launch(cuda_lib, n, k, m):
-    """More activation rows than one launch takes (a prompt chunk of up to 256
-    tokens): oracle bound on every output, and each row bitwise equal to a
-    call with that row alone pinned to the same path."""
+PROMPT_SHAPES = [(300, 2048, 64), (1000, 1024, 100), (256, 5376, 256), (129, 256, 33),
+                 (200, 21504, 129), (4096, 2048, 256)]
+
+
+@pytest.mark.parametrize("n,k,m", PROMPT_SHAPES)
+def test_prompt_chunks_match_oracle(cuda_lib, n, k, m):
+    """Prompt chunks (33 to 256 activation rows, one launch of the hi/lo-split
+    GEMM): every output within the oracle bound, no output unwritten."""
+    assert lib.plan(m, n, k)["path"] == 3
     rng = np.random.default_rng(n + k + m)
     qw_h, st_h, x_h = make(rng, n, k, m)
     y = run(qw_h, st_h, x_h)
     assert_gemv_parity(y, qw_h, st_h, x_h)
-    yb = host_bits(y)
-    for i in (0, 31, 32, m - 1):
-        yi = run(qw_h, st_h, x_h[i:i + 1], path="tensor")
-        assert np.array_equal(host_bits(yi)[0], yb[i])
-    # the CUDA-core path at the same M: 4 rows per launch
-    yc = run(qw_h, st_h, x_h[:40], path="cuda")
-    assert_gemv_parity(yc, qw_h, st_h, x_h[:40])
+
+
+def test_prompt_rows_do_not_depend_on_m(cuda_lib):
+    # the same activation row gives the same bits in chunks of 33, 100 and
+    # 256 rows (different activation tiles and MMA widths)
+    rng = np.random.default_rng(77)
+    qw_h, st_h, x_h = make(rng, 384, 2048, 256)
+    ref = host_bits(run(qw_h, st_h, x_h))
+    for lo, hi in ((0, 33), (100, 200), (223, 256)):
+        part = host_bits(run(qw_h, st_h, x_h[lo:hi]))
+        assert np.array_equal(part, ref[lo:hi])
+
+
+def test_prompt_extreme_values(cuda_lib):
+    # steps over many decades and wide activations: the exact bf16 split
+    # keeps every output within the bound
+    rng = np.random.default_rng(78)
+    qw_h, st_h, x_h = make(rng, 256, 1024, 48)
+    st_h = oracle.bf16_rne(np.exp(rng.uniform(np.log(1e-20), np.log(1e20), size=st_h.shape)))
+    x_h = oracle.bf16_rne(rng.standard_normal(x_h.shape) *
+                          np.exp(rng.uniform(-23, 23, size=x_h.shape)))
+    y = run(qw_h, st_h, x_h)
+    assert_gemv_parity(y, qw_h, st_h, x_h)
+    # an infinite step poisons its row, and only it
+    st2 = st_h.copy()
+    st2[5, 3] = 0x7F80
+    ref = oracle.gemv_ref(qw_h, st2, x_h)
+    got = oracle.bf16_bits_to_f64(host_bits(run(qw_h, st2, x_h)))
+    assert np.array_equal(np.isfinite(got), np.isfinite(ref))
+
+
+def test_prompt_chunks_on_cuda_cores(cuda_lib):
+    # the CUDA-core path pinned at prompt size: 4 rows per launch
+    rng = np.random.default_rng(79)
+    qw_h, st_h, x_h = make(rng, 300, 2048, 40)
+    yc = run(qw_h, st_h, x_h, path="cuda")
+    assert_gemv_parity(yc, qw_h, st_h, x_h)
