@@ -26,10 +26,12 @@
 //  * Association: one fp32 accumulator per (weight row, activation row) over
 //    the whole of K, groups in order; four epilogue warps round it to bf16
 //    once.  Results depend on K only (not on N, M or the tiling).
-//  * Tensor memory: eight A buffers (one group each, 32 columns) and one
-//    accumulator of up to 256 columns.  Issuing a group's four MMAs and its
-//    commits costs the MMA warp several hundred cycles whatever N is, so the
-//    widest N (all activation rows at once) does the most work per issue.
+//  * Tensor memory: eight A buffers (one group each, 32 columns), handed from
+//    the unpacking warps to the MMA warp four groups at a time, and one
+//    accumulator of up to 256 columns.  Issuing MMAs and commits costs the
+//    MMA warp a fixed few hundred cycles per hand-off whatever N is, so the
+//    widest N (all activation rows at once) and the largest hand-off the
+//    ring allows do the most work per issue.
 //  * Every wait is bounded; on expiry W4_ERR_TIMEOUT is recorded, the warps
 //    leave their loops, in-flight copies and MMAs are waited for (bounded)
 //    and the tensor memory is released before exit.
@@ -56,12 +58,14 @@ constexpr int kThreads = 32 * (kMmaWarp + 1);
 constexpr int kCodeStages = 3;
 constexpr int kMaxXStages = 8;        // activation stages of two groups each
 constexpr int kABufs = 8;            // A operands in tensor memory (one group each)
-constexpr int kAPairs = kABufs / 2;  // handed over two groups at a time
+constexpr int kHand = 4;             // groups handed over at a time
+constexpr int kAPairs = kABufs / kHand;   // A hand-off units in the ring
 constexpr int kDBufs = 1;            // accumulators
 constexpr int kACol = 0;             // [kABufs][hi 16 | lo 16] columns
 constexpr int kDCol = kABufs * 32;   // [kDBufs][kMaxTok]
 constexpr int kCols = 512;
 static_assert(kDCol + kDBufs * kMaxTok <= kCols, "tensor memory");
+static_assert(kSliceGroups % kHand == 0 && kHand % 2 == 0, "hand-offs");
 static_assert((kAPairs & (kAPairs - 1)) == 0 && (kDBufs & (kDBufs - 1)) == 0, "ring sizes");
 static_assert(kTpMaxM <= kMaxTok, "one activation tile per unit");
 constexpr int kCodesBytes = kRows * 128;                  // 16 KB, 128-byte swizzle
@@ -238,22 +242,31 @@ __global__ void __launch_bounds__(kThreads, 1) tp_kernel(const __grid_constant__
     // instruction descriptor: D fp32, A and B bf16, both K-major, N = nt, M = 128
     const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(p.nt >> 3) << 17) |
                            ((uint32_t)(kRows >> 4) << 24);
-    // A buffers and activation stages go by pairs of groups: one wait, eight
-    // MMAs and two or three commits per pair
-    long long pi = 0, si = 0;   // pairs and units issued
-    int xsl = 0;                 // activation stage of the pair and its phase
+    // A buffers go by hand-offs of kHand groups (two activation stages): one
+    // wait per stage, 4 kHand MMAs and three or four commits per hand-off
+    long long pi = 0, si = 0;   // hand-offs and units issued
+    int xsl = 0;                 // next activation stage and its phase
     uint32_t xph = 0;
-    const int pairs = p.groups / 2;
+    const int hands = p.groups / kHand;
     for (int u = u0; u < u1 && ok; ++u, ++si) {
-      for (int q = 0; q < pairs; ++q, ++pi) {
+      for (int q = 0; q < hands; ++q, ++pi) {
         const int a = (int)(pi & (kAPairs - 1));
         const bool first = q == 0;
-        const bool last = q == pairs - 1;
+        const bool last = q == hands - 1;
         const int d = (int)(si & (kDBufs - 1));
-        if (!wait_bar(aready0 + 8 * a, (uint32_t)((pi / kAPairs) & 1), abort_flag) ||
-            !wait_bar(xfull0 + 8 * xsl, xph, abort_flag) ||
-            (first && si >= kDBufs &&
-             !wait_bar(dfree0 + 8 * d, (uint32_t)((si / kDBufs - 1) & 1), abort_flag))) {
+        int xsv[kHand / 2];
+        bool got = wait_bar(aready0 + 8 * a, (uint32_t)((pi / kAPairs) & 1), abort_flag);
+#pragma unroll
+        for (int k = 0; k < kHand / 2; ++k) {
+          xsv[k] = xsl;
+          got = got && wait_bar(xfull0 + 8 * xsl, xph, abort_flag);
+          if (++xsl == xs) {
+            xsl = 0;
+            xph ^= 1u;
+          }
+        }
+        if (!got || (first && si >= kDBufs &&
+                     !wait_bar(dfree0 + 8 * d, (uint32_t)((si / kDBufs - 1) & 1), abort_flag))) {
           ok = false;
           break;
         }
@@ -261,9 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1) tp_kernel(const __grid_constant__
         if (lane == 0) {
           const uint32_t dcol = tmem + kDCol + d * kMaxTok;
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {   // the pair's two groups
-            const uint32_t xst = xst0 + xsl * p.x_stage_bytes + (uint32_t)j * 64;
-            const uint32_t acol = tmem + kACol + (2 * a + j) * 32;
+          for (int j = 0; j < kHand; ++j) {   // the hand-off's groups, two per stage
+            const uint32_t xst = xst0 + xsv[j >> 1] * p.x_stage_bytes + (uint32_t)(j & 1) * 64;
+            const uint32_t acol = tmem + kACol + (kHand * a + j) * 32;
 #pragma unroll
             for (int h = 0; h < 2; ++h)   // hi: K = 16h .. 16h + 15
               mma_f16(dcol, acol + h * 8, b_desc_sw128(xst + 32 * h), idesc,
@@ -273,14 +286,11 @@ __global__ void __launch_bounds__(kThreads, 1) tp_kernel(const __grid_constant__
               mma_f16(dcol, acol + 16 + h * 8, b_desc_sw128(xst + 32 * h), idesc, 1u);
           }
           mma_commit(afree0 + 8 * a);
-          mma_commit(xempty0 + 8 * xsl);
+#pragma unroll
+          for (int k = 0; k < kHand / 2; ++k) mma_commit(xempty0 + 8 * xsv[k]);
           if (last) mma_commit(dready0 + 8 * d);
         }
         __syncwarp();
-        if (++xsl == xs) {
-          xsl = 0;
-          xph ^= 1u;
-        }
       }
     }
     // the last commits must land before the tensor memory is released
@@ -306,29 +316,29 @@ __global__ void __launch_bounds__(kThreads, 1) tp_kernel(const __grid_constant__
         // the row's 8 steps of the slice, one 16-byte load
         const uint4 sv = *reinterpret_cast<const uint4*>(cst + kCodesBytes + tid * 16);
 #pragma unroll 1
-        for (int q = 0; q < kSliceGroups / 2; ++q, ++pi) {
+        for (int q = 0; q < kSliceGroups / kHand; ++q, ++pi) {
           const int a = (int)(pi & (kAPairs - 1));
-          // A pair a is free once the MMAs of its previous use are done
+          // A buffers of hand-off a are free once the MMAs of their previous use are done
           if (pi >= kAPairs &&
               !wait_bar(afree0 + 8 * a, (uint32_t)((pi / kAPairs - 1) & 1), abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          // steps of groups 2q and 2q + 1: one 32-bit word of the row's eight
-          const uint32_t sw = (q & 2) ? ((q & 1) ? sv.w : sv.z) : ((q & 1) ? sv.y : sv.x);
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const int g = 2 * q + j;
+#pragma unroll 2
+          for (int j = 0; j < kHand; ++j) {
+            const int g = kHand * q + j;
             const uint4 w = *reinterpret_cast<const uint4*>(cst + tid * 128 + ((g ^ (tid & 7)) << 4));
-            const float step = bf16_bits_to_float((sw >> (16 * j)) & 0xFFFFu);
+            // steps of groups 2i and 2i + 1 share one 32-bit word of the row's eight
+            const uint32_t sw = (g & 4) ? ((g & 2) ? sv.w : sv.z) : ((g & 2) ? sv.y : sv.x);
+            const float step = bf16_bits_to_float((sw >> (16 * (g & 1))) & 0xFFFFu);
             uint32_t hi[16], lo[16];
             split_word(w.x, step, hi, lo);
             split_word(w.y, step, hi + 4, lo + 4);
             split_word(w.z, step, hi + 8, lo + 8);
             split_word(w.w, step, hi + 12, lo + 12);
-            tmem_st16(tmem + lane_base + kACol + (2 * a + j) * 32, hi);
-            tmem_st16(tmem + lane_base + kACol + (2 * a + j) * 32 + 16, lo);
+            tmem_st16(tmem + lane_base + kACol + (kHand * a + j) * 32, hi);
+            tmem_st16(tmem + lane_base + kACol + (kHand * a + j) * 32 + 16, lo);
           }
           asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
           tc_fence_before();
