@@ -422,10 +422,16 @@ cudaError_t allow_tp_smem(int smem, int dev) {
 bool tp_plan(int M, int N, int K, int sms, TpPlan* out) {
   if (M < 1 || M > kTpMaxM || N < 1 || K < kSliceK || K % kSliceK != 0) return false;
   TpPlan pl;
-  const int ttiles = (M + kMaxTok - 1) / kMaxTok;   // 1: kTpMaxM <= kMaxTok
+  pl.tiles = (N + kRows - 1) / kRows;
+  // All the activation rows in one unit, unless the weight tiles are too
+  // few for the SMs: then the rows are cut into equal tiles (of at least 16)
+  // while the units still fit one wave.  The tiling changes no result: each
+  // output is its own accumulator column.
+  int ttiles = (M + kMaxTok - 1) / kMaxTok;   // 1: kTpMaxM <= kMaxTok
+  while (2 * ttiles * pl.tiles <= std::max(1, sms) && (M + 2 * ttiles - 1) / (2 * ttiles) >= 16)
+    ttiles *= 2;
   pl.xrows = (M + ttiles - 1) / ttiles;
   pl.nt = (pl.xrows + 15) & ~15;
-  pl.tiles = (N + kRows - 1) / kRows;
   pl.units = pl.tiles * ttiles;
   pl.ctas = std::min(pl.units, std::max(1, sms));
   // an activation stage: 128-byte rows of the MMA's N (the rows past the

@@ -139,12 +139,23 @@ def test_prompt_plan_is_valid(M, N, K):
     p = lib.plan(M, N, K)
     assert p["path"] == 3 and p["threads"] == 320 and p["unit_rows"] == 128
     assert p["rows_per_call"] == M and p["ctas_per_sm"] == 1
-    nt = p["tmpl_team"]                                   # MMA N: all activation rows
-    assert nt % 16 == 0 and M <= nt < M + 16 and nt <= 256
+    nt = p["tmpl_team"]                  # MMA N: the activation rows of a unit
+    assert nt % 16 == 0 and 16 <= nt <= 256
+    tiles = -(-N // 128)
+    # activation rows stay in one unit unless the weight tiles are too few for
+    # the SMs: then they are halved (tiles of at least 16 rows) while the
+    # units fit one wave
+    ttiles = 1
+    while 2 * ttiles * tiles <= 152 and -(-M // (2 * ttiles)) >= 16:
+        ttiles *= 2
+    xrows = -(-M // ttiles)
+    assert nt == -(-xrows // 16) * 16
+    assert p["ctas"] == min(tiles * ttiles, 152)
+    if tiles >= 76:
+        assert ttiles == 1 and M <= nt < M + 16
     assert 2 <= p["stages"] <= 8
     # more than half the SM (one CTA holds all 512 tensor-memory columns), within the limit
     assert 233472 // 2 < p["smem_bytes"] <= 232448
-    assert p["ctas"] == min(-(-N // 128), 152)
     assert lib.workspace_bytes(M, N, K) == 0
     # K not a multiple of 256 stays on the CUDA cores
     assert lib.plan(M, N, K + 32)["path"] == 1

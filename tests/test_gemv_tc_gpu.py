@@ -133,8 +133,10 @@ def test_tensor_core_pdl_chain(cuda_lib):
     assert_gemv_parity(ys[0], qw_h, st_h, x_h)
 
 
+# one unit of all rows (4096 x 2048), and activation rows cut into tiles when
+# the weight tiles are few, the last tile ragged (201 rows in 8 tiles of 26)
 PROMPT_SHAPES = [(300, 2048, 64), (1000, 1024, 100), (256, 5376, 256), (129, 256, 33),
-                 (200, 21504, 129), (4096, 2048, 256)]
+                 (200, 21504, 129), (4096, 2048, 256), (300, 1024, 201)]
 
 
 @pytest.mark.parametrize("n,k,m", PROMPT_SHAPES)
