@@ -572,6 +572,8 @@ def run_moe(args, world, rank, local):
         scomb += n * k // 16
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(device=dev)
+    fill_stream = torch.cuda.Stream(device=dev)   # pool fills beside the dense FFN
+    shared = args.shared_ffn
     host_home = args.expert_home == "host"
     vectors = args.expert_vectors
     # the router's real ids of every step, as it would leave them on the device
@@ -591,6 +593,16 @@ def run_moe(args, world, rank, local):
                "pool_s": torch.zeros((S, scomb // 2), dtype=torch.bfloat16, device=dev),
                "y": {}, "y_full": {}, "calls": [], "calls_full": []}
         eids_host[:, li] = torch.from_numpy(np.asarray(lay["trace"], dtype=np.int32))
+        if shared != "none":
+            # a dense FFN per layer of one expert's shape, on the layer's input
+            lay["shared"] = [(synth.torch_words((n, k // 8), synth.seed_of(47, li, n), dev),
+                              synth.torch_steps((n, k // 32), synth.seed_of(48, li, n), dev),
+                              lay["x"]["gate_up"] if name == "gate_up" else
+                              synth.torch_x((1, k), synth.seed_of(49, li), dev),
+                              torch.empty((1, n), dtype=torch.bfloat16, device=dev))
+                             for name, (n, k) in shapes.items()]
+            lay["fill_done"] = torch.cuda.Event()
+            lay["pool_free"] = torch.cuda.Event()
         lay["src_q"], lay["src_s"] = lay["full_q"], lay["full_s"]
         if host_home:   # the pool's source; the HBM copy only serves the bitwise check
             lay["src_q"] = torch.empty(lay["full_q"].shape, dtype=torch.int32, pin_memory=True)
@@ -640,6 +652,29 @@ def run_moe(args, world, rank, local):
         for i, call in enumerate(lay["calls_full" if full else "calls"]):
             call(pdl=pdl or i > 0, stream=stream)
 
+    def layer_step(lay, t):
+        """One layer of one step: pool fill and slot ids, the dense FFN if any,
+        the routed GEMVs.  Returns the misses."""
+        if shared == "none":
+            misses = lay["stage"](lay["trace"][t], stream=stream)
+            gemvs(lay, pdl=True)
+            return misses
+        if shared == "overlap":
+            # the fill may start once the layer's previous routed GEMVs are done
+            fill_stream.wait_event(lay["pool_free"])
+            misses = lay["stage"](lay["trace"][t], stream=fill_stream)
+            lay["fill_done"].record(fill_stream)
+        else:
+            misses = lay["stage"](lay["trace"][t], stream=stream)
+        for qw, st, x, y in lay["shared"]:
+            lib.gemv(qw, st, x, y=y, status=status, pdl=True, stream=stream)
+        if shared == "overlap":
+            stream.wait_event(lay["fill_done"])
+        gemvs(lay)
+        if shared == "overlap":
+            lay["pool_free"].record(stream)
+        return misses
+
     kernel_bytes = L * sum(metrics.gemv_id_bytes(k_top, 1 if name == "gate_up" else k_top, n, k)
                            for name, (n, k) in shapes.items())
 
@@ -658,8 +693,7 @@ def run_moe(args, world, rank, local):
             if vectors:
                 eids_dev.copy_(eids_host[t], non_blocking=True)
             for lay in layers:
-                misses += lay["stage"](lay["trace"][t], stream=stream)
-                gemvs(lay, pdl=True)
+                misses += layer_step(lay, t)
             if t >= warm:
                 copied += misses * (qcomb + scomb)
         e1.record(stream)
@@ -691,8 +725,7 @@ def run_moe(args, world, rank, local):
             if vectors:
                 eids_dev.copy_(eids_host[t], non_blocking=True)
             for lay in layers:
-                lay["stage"](lay["trace"][t], stream=stream)
-                gemvs(lay)
+                layer_step(lay, t)
                 lay["ids_full"].copy_(torch.from_numpy(lay["trace"][t].astype(np.int32)))
                 gemvs(lay, full=True)
                 for name in shapes:
@@ -720,6 +753,12 @@ def run_moe(args, world, rank, local):
                                   "and down codes (and, in a second pool array, steps)",
                    "expert_home": ("page-locked host memory, pool fills over NVLink-C2C"
                                    if host_home else "HBM"),
+                   "shared_ffn": {"none": None,
+                                  "serial": "dense FFN of one expert's shape per layer, after "
+                                            "the pool fill on the same stream",
+                                  "overlap": "dense FFN of one expert's shape per layer, the "
+                                             "pool fill beside it on a second stream, joined "
+                                             "before the routed GEMVs"}[shared],
                    "expert_vectors": ("per-expert output scales (gate/up, down) and down "
                                       "biases by real id, slot table checked, "
                                       "w4a16_gemv_id_scaled; real ids copied to the device "
@@ -732,7 +771,8 @@ def run_moe(args, world, rank, local):
         "pool": dict(lfu, hit_rate=lfu["hits"] / max(1, lfu["requests"]),
                      copy_bytes_per_step=copied / steps),
         "bitwise_pool_vs_full": {"steps": total, "layers": L, "mismatched_values": int(bad.item())},
-        "gpu_launches": steps * L * 3,   # per layer: slot-id write, 2 gemv_id
+        # per layer: pool fill / slot ids, 2 gemv_id (+ 2 dense GEMVs)
+        "gpu_launches": steps * L * (3 if shared == "none" else 5),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -796,6 +836,11 @@ def main():
     ap.add_argument("--expert-vectors", action="store_true",
                     help="routed-expert workload: per-expert output scales (and down biases) "
                          "by real expert id, slot table checked (w4a16_gemv_id_scaled)")
+    ap.add_argument("--shared-ffn", choices=("none", "serial", "overlap"), default="none",
+                    help="routed-expert workload: add a dense FFN per layer of one expert's "
+                         "shape (merged gate/up, down; w4a16_gemv) and run the pool fill "
+                         "before it on the same stream (serial) or beside it on a second "
+                         "stream, joined before the routed GEMVs (overlap)")
     ap.add_argument("--workload", default="dense-35L-h2048",
                     choices=sorted(DENSE_WORKLOADS) + ["moe-30L-h2816"],
                     help="decode pass to time (default: the 35-layer hidden-2048 decoder)")
