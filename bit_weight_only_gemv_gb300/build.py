@@ -17,7 +17,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libw4a16.so")
-SOURCES = ["gemv.cu", "gemv_tc.cu", "gemm_tc.cu", "gather.cu", "quant.cu", "slot_pool.cu"]
+SOURCES = ["gemv.cu", "gemv_tc.cu", "gemm_tc.cu", "gather.cu", "quant.cu", "slot_pool.cu",
+           "dev_pool.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

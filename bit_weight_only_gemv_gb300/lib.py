@@ -29,7 +29,8 @@ EXPORTS = ("w4_status_str", "w4_abi_version", "w4_last_cuda_error", "w4a16_gemv"
            "w4a16_gemv_id", "w4a16_gemv_id_scaled", "w4_embed_gather", "w4_pack", "w4_quantize",
            "w4_slot_pool_create", "w4_slot_pool_destroy", "w4_slot_pool_remap",
            "w4_slot_pool_stage", "w4_slot_pool_stats", "w4a16_gemv_plan",
-           "w4a16_gemv_static_scratch")
+           "w4a16_gemv_static_scratch", "w4_dev_pool_state_bytes", "w4_dev_pool_init",
+           "w4_dev_pool_stage", "w4_dev_pool_stats")
 
 
 class W4Error(RuntimeError):
@@ -95,6 +96,15 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                        i32p, ctypes.POINTER(i32), vp]
     lib.w4_slot_pool_stats.restype = None
     lib.w4_slot_pool_stats.argtypes = [vp] + [ctypes.POINTER(ctypes.c_longlong)] * 3
+    lib.w4_dev_pool_state_bytes.restype = sz
+    lib.w4_dev_pool_state_bytes.argtypes = [i32, i32]
+    lib.w4_dev_pool_init.restype = i32
+    lib.w4_dev_pool_init.argtypes = [vp, i32, i32, vp]
+    lib.w4_dev_pool_stage.restype = i32
+    lib.w4_dev_pool_stage.argtypes = [vp, i32, i32, vp, i32, vp, vp, sz, sz, vp, vp, sz, sz, vp,
+                                      vp, vp, u32, vp]
+    lib.w4_dev_pool_stats.restype = i32
+    lib.w4_dev_pool_stats.argtypes = [vp, i32, i32] + [ctypes.POINTER(ctypes.c_longlong)] * 3
     lib.w4a16_gemv_plan.restype = i32
     lib.w4a16_gemv_plan.argtypes = [i32, i32, i32, ctypes.POINTER(PlanInfo)]
     _lib = lib
@@ -314,6 +324,47 @@ def quantize(w: torch.Tensor, stream=None):
     st = torch.empty((N, K // 32), dtype=torch.bfloat16, device=w.device)
     _check(load().w4_quantize(_ptr(qw), _ptr(st), _ptr(w), N, K, _stream(stream)), "w4_quantize")
     return qw, st
+
+
+class DevSlotPool:
+    """Device-side LFU expert-slot pool: state in a device buffer, remap and
+    fills enqueued on a stream (graph-capturable)."""
+
+    def __init__(self, num_experts: int, num_slots: int, device="cuda", stream=None):
+        self._lib = load()
+        n = self._lib.w4_dev_pool_state_bytes(num_experts, num_slots)
+        if n == 0:
+            raise W4Error(3, "w4_dev_pool_state_bytes")
+        self.state = torch.empty(n, dtype=torch.uint8, device=device)
+        self.num_experts, self.num_slots = num_experts, num_slots
+        _check(self._lib.w4_dev_pool_init(_ptr(self.state), num_experts, num_slots,
+                                          _stream(stream)), "w4_dev_pool_init")
+
+    def bind_stage(self, ids_dev: torch.Tensor, pool_qw, full_qw, qw_stride, qw_bytes, pool_st,
+                   full_st, st_stride, st_bytes, slot_ids_dev: torch.Tensor, slot_expert=None,
+                   status=None):
+        """Returns call(pdl=False, stream=None) that enqueues the remap of the
+        ids then held by ids_dev (device int32 [k]) and the fills."""
+        _need(ids_dev, torch.int32, "ids_dev")
+        _need(slot_ids_dev, torch.int32, "slot_ids_dev")
+        fn = self._lib.w4_dev_pool_stage
+        args = (_ptr(self.state), self.num_experts, self.num_slots, _ptr(ids_dev), ids_dev.numel(),
+                _ptr(pool_qw), _ptr(full_qw), qw_stride, qw_bytes, _ptr(pool_st), _ptr(full_st),
+                st_stride, st_bytes, _ptr(slot_ids_dev), _ptr(slot_expert), _ptr(status))
+
+        def call(pdl: bool = False, stream=None):
+            _check(fn(*args, W4_FLAG_PDL if pdl else 0, _stream(stream)), "w4_dev_pool_stage")
+
+        call.tensors = (self.state, ids_dev, pool_qw, full_qw, pool_st, full_st, slot_ids_dev,
+                        slot_expert, status)
+        return call
+
+    def stats(self):
+        r, h, m = ctypes.c_longlong(), ctypes.c_longlong(), ctypes.c_longlong()
+        _check(self._lib.w4_dev_pool_stats(_ptr(self.state), self.num_experts, self.num_slots,
+                                           ctypes.byref(r), ctypes.byref(h), ctypes.byref(m)),
+               "w4_dev_pool_stats")
+        return {"requests": r.value, "hits": h.value, "misses": m.value}
 
 
 class SlotPool:

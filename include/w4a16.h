@@ -380,6 +380,43 @@ w4_status w4_slot_pool_stage(w4_slot_pool *pool, const int32_t *expert_ids, int 
                              int32_t *slot_ids_dev, int32_t *slot_expert_dev,
                              int32_t *slot_ids, int *n_miss, w4_stream_t stream);
 
+/*
+ * Device-side slot pool: the same policy decided on the GPU, so a routed step
+ * (router ids on the device -> remap -> fills -> w4a16_gemv_id) needs no host
+ * round trip and can be captured in a CUDA graph.  The pool's whole state
+ * lives in a caller-owned device buffer of w4_dev_pool_state_bytes bytes
+ * (16-byte aligned), set up once with w4_dev_pool_init.  num_slots <= 64 and
+ * <= num_experts.
+ */
+size_t w4_dev_pool_state_bytes(int num_experts, int num_slots);
+
+/* Reset the state on `stream`: every slot free, every count 0. */
+w4_status w4_dev_pool_init(void *state, int num_experts, int num_slots, w4_stream_t stream);
+
+/*
+ * Enqueue the remap of the k (<= 64) device int32 expert ids at `ids` and the
+ * fills of the misses: one single-thread kernel decides, one kernel copies
+ * each missed expert's codes and steps (as w4_slot_pool_stage, every
+ * pointer, stride and size a multiple of 16 bytes; sources in device memory
+ * or page-locked host memory) and names the new experts in the slot table
+ * (slot_expert_dev, optional, the caller fills it with -1 once).  The slot
+ * ids go to slot_ids_dev.  A request with an id outside [0, num_experts) or
+ * more distinct ids than slots changes nothing, writes -1 slot ids (the
+ * routed GEMV then leaves those rows unwritten) and records W4_ERR_INDEX or
+ * W4_ERR_STATE in *status_dev.  W4_FLAG_PDL: the remap waits for earlier
+ * kernels (the router) only where it reads the ids.
+ */
+w4_status w4_dev_pool_stage(void *state, int num_experts, int num_slots, const int32_t *ids,
+                            int k, void *pool_qw, const void *full_qw, size_t qw_stride_bytes,
+                            size_t qw_expert_bytes, void *pool_st, const void *full_st,
+                            size_t st_stride_bytes, size_t st_expert_bytes,
+                            int32_t *slot_ids_dev, int32_t *slot_expert_dev,
+                            int32_t *status_dev, unsigned flags, w4_stream_t stream);
+
+/* Counters of a device-side pool (synchronous device-to-host read). */
+w4_status w4_dev_pool_stats(const void *state, int num_experts, int num_slots,
+                            long long *requests, long long *hits, long long *misses);
+
 /* Counters since creation: requests served (ids), hits, misses (copies). */
 void w4_slot_pool_stats(const w4_slot_pool *pool, long long *requests, long long *hits,
                         long long *misses);
