@@ -635,8 +635,28 @@ def run_moe(args, world, rank, local):
                                                   E if full else S, qcomb, scomb, y, status))
         layers.append(lay)
 
+    device_pool = args.pool == "device"
+    if device_pool and shared != "none":
+        raise SystemExit("--pool device runs without --shared-ffn")
+    # device pool: every step's router ids on the device; a device counter
+    # picks the current step's into eids_dev, which the remap reads
+    all_ids = eids_host.to(dev) if device_pool else None
+    step_idx = torch.zeros(1, dtype=torch.int64, device=dev)
+
     def new_pools():
-        for lay in layers:
+        for li, lay in enumerate(layers):
+            if device_pool:
+                if "dpool" not in lay:
+                    lay["dpool"] = lib.DevSlotPool(E, S, device=dev)
+                    lay["dstage"] = lay["dpool"].bind_stage(
+                        eids_dev[li], lay["pool_q"], lay["src_q"], qcomb, qcomb, lay["pool_s"],
+                        lay["src_s"], scomb, scomb, lay["slot_ids"], slot_expert=lay.get("table"),
+                        status=status)
+                else:
+                    lay["dpool"].reset()
+                if vectors:
+                    lay["table"].fill_(-1)
+                continue
             lay["pool"] = lib.SlotPool(E, S)
             lay["stage"] = lay["pool"].bind_stage(k_top, lay["pool_q"], lay["src_q"], qcomb,
                                                   qcomb, lay["pool_s"], lay["src_s"], scomb,
@@ -654,7 +674,11 @@ def run_moe(args, world, rank, local):
 
     def layer_step(lay, t):
         """One layer of one step: pool fill and slot ids, the dense FFN if any,
-        the routed GEMVs.  Returns the misses."""
+        the routed GEMVs.  Returns the misses (None for the device pool)."""
+        if device_pool:
+            lay["dstage"](pdl=True, stream=stream)
+            gemvs(lay, pdl=True)
+            return None
         if shared == "none":
             misses = lay["stage"](lay["trace"][t], stream=stream)
             gemvs(lay, pdl=True)
@@ -678,13 +702,48 @@ def run_moe(args, world, rank, local):
     kernel_bytes = L * sum(metrics.gemv_id_bytes(k_top, 1 if name == "gate_up" else k_top, n, k)
                            for name, (n, k) in shapes.items())
 
-    # phase A (timed): the routed pass through the pools, eager
+    def pool_stats():
+        lfu = {"requests": 0, "hits": 0, "misses": 0}
+        for lay in layers:
+            st = (lay["dpool"] if device_pool else lay["pool"]).stats()
+            for key in lfu:
+                lfu[key] += st[key]
+        return lfu
+
+    # phase A (timed): the routed pass through the pools, eager steps (host
+    # pool) or one graph replay per step (device pool)
     new_pools()
     copied = 0
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    if device_pool:
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            step_idx.zero_()
+        torch.cuda.synchronize()
+        gstep = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gstep, stream=stream):
+            eids_dev.copy_(torch.index_select(all_ids, 0, step_idx).view(L, k_top))
+            step_idx.add_(1)
+            for lay in layers:
+                layer_step(lay, 0)
+        with torch.cuda.stream(stream):   # the capture ran nothing: start again
+            step_idx.zero_()
+        new_pools()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for t in range(total):
+                if t == warm:
+                    torch.cuda.synchronize()
+                    miss0 = pool_stats()["misses"]
+                    e0.record(stream)
+                    t_host = time.perf_counter()
+                gstep.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        copied = (pool_stats()["misses"] - miss0) * (qcomb + scomb)
     with torch.cuda.stream(stream):
-        for t in range(total):
+        for t in range(0 if device_pool else total):
             if t == warm:
                 torch.cuda.synchronize()
                 e0.record(stream)
@@ -701,11 +760,7 @@ def run_moe(args, world, rank, local):
     host_s = time.perf_counter() - t_host
     ms = e0.elapsed_time(e1) / steps
     ms = max_over_ranks(ms, dev)
-    lfu = {"requests": 0, "hits": 0, "misses": 0}
-    for lay in layers:
-        st = lay["pool"].stats()
-        for key in lfu:
-            lfu[key] += st[key]
+    lfu = pool_stats()
 
     # kernel only: the last step's 60 routed GEMVs (pool contents as left), as a graph
     fns = [(lambda lay: (lambda pdl: gemvs(lay, pdl=pdl)))(lay) for lay in layers]
@@ -722,7 +777,7 @@ def run_moe(args, world, rank, local):
     bad = torch.zeros((), dtype=torch.int64, device=dev)
     with torch.cuda.stream(stream):
         for t in range(total):
-            if vectors:
+            if vectors or device_pool:
                 eids_dev.copy_(eids_host[t], non_blocking=True)
             for lay in layers:
                 layer_step(lay, t)
@@ -747,8 +802,11 @@ def run_moe(args, world, rank, local):
                                f"{S}-slot LFU pool per layer; per layer merged gate/up "
                                f"{2 * I}x{H} and down {H}x{I} through w4a16_gemv_id",
                    "global_batch": world, "parallelism": f"replicas x{world}",
-                   "timed": "eager steps: host LFU remap + pool copies + slot ids + 2 gemv_id "
-                            "per layer (CUDA events)",
+                   "timed": ("one CUDA graph replay per step: the step's router ids picked "
+                             "on the device, per layer the device LFU remap, pool copies and "
+                             "slot ids, 2 gemv_id (CUDA events)" if device_pool else
+                             "eager steps: host LFU remap + pool copies + slot ids + 2 gemv_id "
+                             "per layer (CUDA events)"),
                    "pool_layout": "one 32-slot pool per layer; a slot holds an expert's gate/up "
                                   "and down codes (and, in a second pool array, steps)",
                    "expert_home": ("page-locked host memory, pool fills over NVLink-C2C"
@@ -772,7 +830,7 @@ def run_moe(args, world, rank, local):
                      copy_bytes_per_step=copied / steps),
         "bitwise_pool_vs_full": {"steps": total, "layers": L, "mismatched_values": int(bad.item())},
         # per layer: pool fill / slot ids, 2 gemv_id (+ 2 dense GEMVs)
-        "gpu_launches": steps * L * (3 if shared == "none" else 5),
+        "gpu_launches": steps * L * (4 if device_pool else 3 if shared == "none" else 5),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -836,6 +894,9 @@ def main():
     ap.add_argument("--expert-vectors", action="store_true",
                     help="routed-expert workload: per-expert output scales (and down biases) "
                          "by real expert id, slot table checked (w4a16_gemv_id_scaled)")
+    ap.add_argument("--pool", choices=("host", "device"), default="host",
+                    help="routed-expert workload: LFU remap on the host per layer (eager steps), "
+                         "or on the device (w4_dev_pool_*), each step one CUDA graph replay")
     ap.add_argument("--shared-ffn", choices=("none", "serial", "overlap"), default="none",
                     help="routed-expert workload: add a dense FFN per layer of one expert's "
                          "shape (merged gate/up, down; w4a16_gemv) and run the pool fill "

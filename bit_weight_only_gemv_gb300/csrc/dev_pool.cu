@@ -25,6 +25,7 @@ namespace {
 
 constexpr int kMaxK = 64;       // ids per request
 constexpr int kMaxSlots = 64;   // slots per pool
+constexpr int kMaxExperts = 3980;   // experts per pool: the remap keeps a copy in 48 KB of shared memory
 
 // Device state, 8-byte aligned:
 //   int64 step, requests, hits, misses
@@ -82,100 +83,178 @@ __global__ void dev_pool_init_kernel(uint8_t* st, int E, int S) {
   }
 }
 
-// One thread: the remap of one request.  On an invalid request (an id out of
-// range, more distinct ids than slots) the state is left unchanged, the slot
-// ids become -1 (the routed GEMV then leaves those rows unwritten) and the
-// error goes to *status.  Slots about to be refilled are marked as holding no
-// expert in the slot table until the fill kernel has copied them.
-__global__ void dev_pool_remap_kernel(uint8_t* st, int E, int S, const int32_t* ids, int k,
-                                      int32_t* slot_ids, int32_t* slot_expert, int32_t* status) {
+// One block: the remap of one request.  The block loads the pool's state
+// into shared memory, one thread takes the decisions there (the policy is
+// sequential), the block writes the state back.  On an invalid request (an
+// id out of range, more distinct ids than slots) the state is left
+// unchanged, the slot ids become -1 (the routed GEMV then leaves those rows
+// unwritten) and the error goes to *status.  Slots about to be refilled are
+// marked as holding no expert in the slot table until the fill kernel has
+// copied them.
+__global__ void __launch_bounds__(256) dev_pool_remap_kernel(uint8_t* st, int E, int S,
+                                                             const int32_t* ids, int k,
+                                                             int32_t* slot_ids,
+                                                             int32_t* slot_expert,
+                                                             int32_t* status) {
+  extern __shared__ __align__(16) uint8_t sm[];
   pdl_wait();   // the ids come from earlier kernels
-  if (threadIdx.x != 0 || blockIdx.x != 0) return;
   const Layout l = layout(E, S);
   long long* hdr = reinterpret_cast<long long*>(st);
-  long long* count = reinterpret_cast<long long*>(st + l.count);
-  long long* last_use = reinterpret_cast<long long*>(st + l.last_use);
-  int* slot_of = reinterpret_cast<int*>(st + l.slot_of);
-  int* in_slot = reinterpret_cast<int*>(st + l.in_slot);
-  int* n_miss = reinterpret_cast<int*>(st + l.n_miss);
-  int* miss_e = reinterpret_cast<int*>(st + l.miss_e);
-  int* miss_s = reinterpret_cast<int*>(st + l.miss_s);
-  int* okp = reinterpret_cast<int*>(st + l.ok);
-  int id[kMaxK];
-  int distinct = 0, bad = 0;
-  for (int i = 0; i < k; ++i) {
-    id[i] = ids[i];
-    if (id[i] < 0 || id[i] >= E) bad = W4_ERR_INDEX;
+  long long* g_count = reinterpret_cast<long long*>(st + l.count);
+  long long* g_last = reinterpret_cast<long long*>(st + l.last_use);
+  int* g_slot_of = reinterpret_cast<int*>(st + l.slot_of);
+  int* g_in_slot = reinterpret_cast<int*>(st + l.in_slot);
+  // shared copy: count[E], last_use[S], slot_of[E], in_slot[S], ids, flags
+  long long* count = reinterpret_cast<long long*>(sm);
+  long long* last_use = count + E;
+  int* slot_of = reinterpret_cast<int*>(last_use + S);
+  int* in_slot = slot_of + E;
+  int* id = in_slot + S;
+  int* flag = id + kMaxK;   // [0] valid request; the slots of the ids follow at flag + 4
+  for (int i = threadIdx.x; i < E; i += blockDim.x) {
+    count[i] = g_count[i];
+    slot_of[i] = g_slot_of[i];
   }
-  if (!bad) {
-    for (int i = 0; i < k; ++i) {
-      bool seen = false;
-      for (int j = 0; j < i; ++j) seen = seen || id[j] == id[i];
-      distinct += seen ? 0 : 1;
-    }
-    if (distinct > S) bad = W4_ERR_STATE;
+  for (int i = threadIdx.x; i < S; i += blockDim.x) {
+    last_use[i] = g_last[i];
+    in_slot[i] = g_in_slot[i];
   }
-  *n_miss = 0;
-  *okp = bad ? 0 : 1;
-  if (bad) {
-    for (int i = 0; i < k; ++i) slot_ids[i] = -1;
-    report(status, bad);
-    return;
-  }
-  const long long t = hdr[0];
-  for (int i = 0; i < k; ++i) count[id[i]] += 1;
-  int out[kMaxK];
-  long long hits = 0;
-  for (int i = 0; i < k; ++i) {
-    const int s = slot_of[id[i]];
-    out[i] = s;
-    if (s >= 0) {
-      last_use[s] = t;
-      ++hits;
-    }
-  }
-  int nm = 0;
-  for (int i = 0; i < k; ++i) {
-    if (out[i] >= 0) continue;
-    const int e = id[i];
-    int s = slot_of[e];   // loaded earlier in this request
-    if (s < 0) {
-      for (int j = 0; j < S && s < 0; ++j)
-        if (in_slot[j] < 0) s = j;
-      if (s < 0) {
-        for (int j = 0; j < S; ++j) {
-          const int ej = in_slot[j];
-          bool needed = false;
-          for (int q = 0; q < k; ++q) needed = needed || id[q] == ej;
-          if (needed) continue;
-          if (s < 0) {
-            s = j;
-            continue;
-          }
-          const int es = in_slot[s];
-          if (count[ej] < count[es] || (count[ej] == count[es] && last_use[j] < last_use[s]))
-            s = j;   // ties on both keep the lower index
-        }
-        slot_of[in_slot[s]] = -1;
+  for (int i = threadIdx.x; i < k; i += blockDim.x) id[i] = ids[i];
+  __syncthreads();
+  // Warp 0 takes the decisions, its lanes side by side where the policy
+  // allows (checks, hits, the free-slot and victim searches over the slots);
+  // the misses themselves are placed one after another, in request order.
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int* n_miss = reinterpret_cast<int*>(st + l.n_miss);
+    int* miss_e = reinterpret_cast<int*>(st + l.miss_e);
+    int* miss_s = reinterpret_cast<int*>(st + l.miss_s);
+    int* out = flag + 4;   // [kMaxK] slot of each id
+    // validity: every id in range, at most S distinct ids
+    int bad_range = 0, distinct = 0;
+    for (int i0 = 0; i0 < k; i0 += 32) {
+      const int i = i0 + lane;
+      bool inr = true, first = false;
+      if (i < k) {
+        inr = id[i] >= 0 && id[i] < E;
+        first = true;
+        for (int j = 0; j < i; ++j) first = first && id[j] != id[i];
       }
-      in_slot[s] = e;
-      slot_of[e] = s;
-      miss_e[nm] = e;
-      miss_s[nm] = s;
-      ++nm;
-      if (slot_expert != nullptr) slot_expert[s] = -1;   // until its copy is in
-    } else {
-      ++hits;
+      bad_range |= __any_sync(0xffffffffu, !inr);
+      distinct += __popc(__ballot_sync(0xffffffffu, first));
     }
-    last_use[s] = t;
-    out[i] = s;
+    const int bad = bad_range ? W4_ERR_INDEX : (distinct > S ? W4_ERR_STATE : 0);
+    if (lane == 0) {
+      *n_miss = 0;
+      flag[0] = bad ? 0 : 1;
+    }
+    if (bad) {
+      for (int i = lane; i < k; i += 32) slot_ids[i] = -1;
+      if (lane == 0) report(status, bad);
+    } else {
+      const long long t = hdr[0];
+      if (lane == 0)
+        for (int i = 0; i < k; ++i) count[id[i]] += 1;   // repeats count each time
+      __syncwarp();
+      // hits: experts resident before this request
+      long long hits = 0;
+      for (int i0 = 0; i0 < k; i0 += 32) {
+        const int i = i0 + lane;
+        int s_ = -1;
+        if (i < k) {
+          s_ = slot_of[id[i]];
+          out[i] = s_;
+          if (s_ >= 0) last_use[s_] = t;
+        }
+        hits += __popc(__ballot_sync(0xffffffffu, s_ >= 0));
+      }
+      __syncwarp();
+      int nm = 0;
+      for (int i = 0; i < k; ++i) {
+        if (out[i] >= 0) continue;   // warp-uniform: shared memory
+        const int e = id[i];
+        int sl = slot_of[e];         // loaded earlier in this request
+        if (sl < 0) {
+          // lowest free slot
+          unsigned freem = 0;
+          for (int j0 = 0; j0 < S; j0 += 32) {
+            const int j = j0 + lane;
+            const unsigned b = __ballot_sync(0xffffffffu, j < S && in_slot[j] < 0);
+            if (sl < 0 && b != 0) sl = j0 + __ffs(b) - 1;
+            freem |= b;
+          }
+          if (sl < 0) {
+            // victim: the slot whose expert is not requested now with the
+            // fewest uses, then the least recently used, then the lowest index
+            long long bc = 0x7fffffffffffffffLL, bl = 0x7fffffffffffffffLL;
+            int bj = 0x7fffffff;
+            for (int j = lane; j < S; j += 32) {
+              const int ej = in_slot[j];
+              bool needed = false;
+              for (int q = 0; q < k; ++q) needed = needed || id[q] == ej;
+              if (needed) continue;
+              const long long c = count[ej], lu = last_use[j];
+              if (c < bc || (c == bc && (lu < bl || (lu == bl && j < bj)))) {
+                bc = c;
+                bl = lu;
+                bj = j;
+              }
+            }
+            for (int off = 16; off > 0; off >>= 1) {
+              const long long oc = __shfl_xor_sync(0xffffffffu, bc, off);
+              const long long ol = __shfl_xor_sync(0xffffffffu, bl, off);
+              const int oj = __shfl_xor_sync(0xffffffffu, bj, off);
+              if (oc < bc || (oc == bc && (ol < bl || (ol == bl && oj < bj)))) {
+                bc = oc;
+                bl = ol;
+                bj = oj;
+              }
+            }
+            sl = bj;
+            if (lane == 0) slot_of[in_slot[sl]] = -1;
+          }
+          if (lane == 0) {
+            in_slot[sl] = e;
+            slot_of[e] = sl;
+            miss_e[nm] = e;
+            miss_s[nm] = sl;
+            if (slot_expert != nullptr) slot_expert[sl] = -1;   // until its copy is in
+          }
+          ++nm;
+        } else {
+          ++hits;
+        }
+        if (lane == 0) {
+          last_use[sl] = t;
+          out[i] = sl;
+        }
+        __syncwarp();
+      }
+      if (lane == 0) {
+        *n_miss = nm;
+        hdr[0] = t + 1;
+        hdr[1] += k;
+        hdr[2] += hits;
+        hdr[3] += nm;
+      }
+      for (int i = lane; i < k; i += 32) slot_ids[i] = out[i];
+    }
   }
-  *n_miss = nm;
-  hdr[0] = t + 1;
-  hdr[1] += k;
-  hdr[2] += hits;
-  hdr[3] += nm;
-  for (int i = 0; i < k; ++i) slot_ids[i] = out[i];
+  __syncthreads();
+  if (flag[0]) {   // write the state back
+    for (int i = threadIdx.x; i < E; i += blockDim.x) {
+      g_count[i] = count[i];
+      g_slot_of[i] = slot_of[i];
+    }
+    for (int i = threadIdx.x; i < S; i += blockDim.x) {
+      g_last[i] = last_use[i];
+      g_in_slot[i] = in_slot[i];
+    }
+  }
+}
+
+size_t remap_smem(int E, int S) {
+  return (size_t)(E + S) * sizeof(long long) + (size_t)(E + S + 2 * kMaxK + 4) * sizeof(int);
 }
 
 // Copies of the remap's misses (16 bytes per thread step), then the slot
@@ -235,11 +314,12 @@ const void* kernel_view(const void* ptr) {
   }
 }
 
-cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, bool pdl, cudaStream_t s,
-                       void** args) {
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, bool pdl,
+                       cudaStream_t s, void** args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -255,14 +335,16 @@ cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, bool pdl, cudaStre
 using namespace w4;
 
 extern "C" size_t w4_dev_pool_state_bytes(int num_experts, int num_slots) {
-  if (num_experts < 1 || num_slots < 1 || num_slots > kMaxSlots) return 0;
+  if (num_experts < 1 || num_slots < 1 || num_slots > kMaxSlots || num_experts > kMaxExperts)
+    return 0;
   return layout(num_experts, num_slots).bytes;
 }
 
 extern "C" w4_status w4_dev_pool_init(void* state, int num_experts, int num_slots,
                                       w4_stream_t stream) {
   if (state == nullptr || num_experts < 1 || num_slots < 1) return W4_ERR_ARG;
-  if (num_slots > kMaxSlots || num_slots > num_experts) return W4_ERR_SHAPE;
+  if (num_slots > kMaxSlots || num_slots > num_experts || num_experts > kMaxExperts)
+    return W4_ERR_SHAPE;
   if ((reinterpret_cast<uintptr_t>(state) & 15) != 0) return W4_ERR_ALIGN;
   const int n = num_experts + num_slots + 4;
   dev_pool_init_kernel<<<std::min(1024, (n + 255) / 256), 256, 0,
@@ -288,7 +370,9 @@ extern "C" w4_status w4_dev_pool_stage(void* state, int num_experts, int num_slo
       pool_st == nullptr || full_st == nullptr || slot_ids_dev == nullptr || k < 1 ||
       num_experts < 1 || num_slots < 1 || (flags & ~W4_FLAG_PDL) != 0)
     return W4_ERR_ARG;
-  if (k > kMaxK || num_slots > kMaxSlots || num_slots > num_experts) return W4_ERR_SHAPE;
+  if (k > kMaxK || num_slots > kMaxSlots || num_slots > num_experts ||
+      num_experts > kMaxExperts)
+    return W4_ERR_SHAPE;
   if (qw_expert_bytes > qw_stride_bytes || st_expert_bytes > st_stride_bytes ||
       qw_expert_bytes == 0 || st_expert_bytes == 0)
     return W4_ERR_ARG;
@@ -307,7 +391,7 @@ extern "C" w4_status w4_dev_pool_stage(void* state, int num_experts, int num_slo
   void* rargs[] = {&st, &E, &S, const_cast<int32_t**>(&ids), &kk, &slot_ids_dev,
                    &slot_expert_dev, &status_dev};
   cudaError_t e = launch_pdl(reinterpret_cast<const void*>(dev_pool_remap_kernel), dim3(1),
-                             dim3(32), pdl, s, rargs);
+                             dim3(256), remap_smem(E, S), pdl, s, rargs);
   if (e == cudaSuccess) {
     DevFill fp = {};
     fp.st = st;
@@ -322,12 +406,15 @@ extern "C" w4_status w4_dev_pool_stage(void* state, int num_experts, int num_slo
     fp.qw_units = qw_expert_bytes / 16;
     fp.st_units = st_expert_bytes / 16;
     fp.slot_expert = slot_expert_dev;
-    // enough threads for k misses; blocks past the request's misses exit at once
-    const unsigned long long units = (fp.qw_units + fp.st_units) * (unsigned long long)k;
-    const int blocks = (int)std::max(1ULL, std::min(1024ULL, (units + 255) / 256));
+    // one block per SM, striding over the misses (their number is only
+    // known on the device)
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      sms = 152;
     void* fargs[] = {&fp};
-    e = launch_pdl(reinterpret_cast<const void*>(dev_pool_fill_kernel), dim3(blocks), dim3(256),
-                   true, s, fargs);
+    e = launch_pdl(reinterpret_cast<const void*>(dev_pool_fill_kernel), dim3(std::max(1, sms)),
+                   dim3(256), 0, true, s, fargs);
   }
   if (e != cudaSuccess) {
     note_cuda_error(e);

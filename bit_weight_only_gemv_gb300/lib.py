@@ -337,7 +337,11 @@ class DevSlotPool:
             raise W4Error(3, "w4_dev_pool_state_bytes")
         self.state = torch.empty(n, dtype=torch.uint8, device=device)
         self.num_experts, self.num_slots = num_experts, num_slots
-        _check(self._lib.w4_dev_pool_init(_ptr(self.state), num_experts, num_slots,
+        self.reset(stream)
+
+    def reset(self, stream=None):
+        """Every slot free, every count 0 (enqueued on `stream`)."""
+        _check(self._lib.w4_dev_pool_init(_ptr(self.state), self.num_experts, self.num_slots,
                                           _stream(stream)), "w4_dev_pool_init")
 
     def bind_stage(self, ids_dev: torch.Tensor, pool_qw, full_qw, qw_stride, qw_bytes, pool_st,

@@ -386,7 +386,7 @@ w4_status w4_slot_pool_stage(w4_slot_pool *pool, const int32_t *expert_ids, int 
  * round trip and can be captured in a CUDA graph.  The pool's whole state
  * lives in a caller-owned device buffer of w4_dev_pool_state_bytes bytes
  * (16-byte aligned), set up once with w4_dev_pool_init.  num_slots <= 64 and
- * <= num_experts.
+ * <= num_experts <= 3980.
  */
 size_t w4_dev_pool_state_bytes(int num_experts, int num_slots);
 
