@@ -87,6 +87,34 @@ def test_host_validation_rejects_before_any_launch(L):
     assert L.w4_quantize(good, good, vp((1 << 20) + 4), 4, 64, None) == 2
 
 
+def test_device_pool_host_checks(L):
+    vp = ctypes.c_void_p
+    good = vp(1 << 20)
+    # state size: slots and experts within their limits
+    assert L.w4_dev_pool_state_bytes(128, 32) > 0
+    assert L.w4_dev_pool_state_bytes(128, 32) % 16 == 0
+    assert L.w4_dev_pool_state_bytes(128, 65) == 0
+    assert L.w4_dev_pool_state_bytes(3981, 8) == 0
+    assert L.w4_dev_pool_state_bytes(0, 8) == 0
+    # init: arguments checked before any launch
+    assert L.w4_dev_pool_init(None, 128, 32, None) == 1
+    assert L.w4_dev_pool_init(good, 8, 9, None) == 3          # more slots than experts
+    assert L.w4_dev_pool_init(vp((1 << 20) + 8), 128, 32, None) == 2
+
+    def stage(state=good, E=128, S=32, ids=good, k=8, qw_stride=1024, qw_bytes=1024,
+              st_stride=128, st_bytes=128, slot_ids=good, flags=0):
+        return L.w4_dev_pool_stage(state, E, S, ids, k, good, good, qw_stride, qw_bytes, good,
+                                   good, st_stride, st_bytes, slot_ids, None, None, flags, None)
+    assert stage(state=None) == 1
+    assert stage(slot_ids=None) == 1
+    assert stage(k=0) == 1
+    assert stage(k=65) == 3
+    assert stage(S=65) == 3
+    assert stage(E=4000) == 3
+    assert stage(qw_bytes=2048) == 1                           # expert larger than its stride
+    assert stage(flags=2) == 1                                 # only W4_FLAG_PDL
+
+
 @pytest.mark.parametrize("M,N,K", [(1, 2048, 2048), (1, 512, 2048), (1, 2048, 8192),
                                    (1, 5376, 21504), (1, 704, 2816), (1, 2816, 704),
                                    (4, 8192, 2048), (1, 262144, 2048), (1, 7, 32),

@@ -36,7 +36,8 @@ def _static_call(L, y, qw, st, x, M, N, K, status):
 
 
 @pytest.mark.parametrize("m,n,k", [(1, 16, 21504), (1, 64, 21504), (5, 40, 21504),
-                                   (2, 300, 5376), (1, 2048, 2048)])
+                                   (2, 300, 5376), (1, 2048, 2048), (16, 300, 2048),
+                                   (100, 300, 2048)])
 def test_static_scratch_matches_workspace_call(cuda_lib, m, n, k):
     L = cuda_lib
     rng = np.random.default_rng(100 + m + n + k)
