@@ -9,7 +9,8 @@
 // fly, without rounding:
 //
 //  * w = (code - 8) * step has at most 11 significant bits, so it is exactly
-//    hi + lo with hi = bf16(w) and lo = w - hi (at most 3 significant bits).
+//    hi + lo with hi = bf16(w) and lo = w - hi (at most 3 significant bits):
+//    one bf16x2 multiply and one bf16x2 fused multiply-add per pair of codes.
 //    Four warps (thread = weight row) unpack each 32-code group into hi and
 //    lo and store both into tensor memory as the MMA's A operand; the MMA
 //    warp issues per group two K = 16 MMAs for hi and two for lo into one
@@ -94,20 +95,21 @@ struct TpParams {
   int32_t* status;
 };
 
-// Exact bf16 split of the eight weights of one packed word: w = (c - 8) *
-// step in fp32 (exact: the float-bit trick of the page gives c - 8, the
-// product has at most 11 significant bits), hi = bf16(w), lo = w - hi
-// (exact, at most 3 significant bits).  Pairs (2i, 2i + 1) of consecutive
-// codes, the lower code in the low half.
-__device__ __forceinline__ void split_word(uint32_t wd, float step, uint32_t hi[4],
+// Exact bf16 split of the eight weights of one packed word, in pairs of
+// consecutive codes (the lower code in the low half): (c - 8) from the
+// page's float-bit trick in bf16 form, then hi = (c - 8) * step by one bf16x2
+// multiply (the product of two bf16 values is exact before its one
+// rounding, so hi = bf16(w)) and lo = (c - 8) * step - hi by one fused
+// multiply-add (exact: w - hi has at most 3 significant bits).
+__device__ __forceinline__ void split_word(uint32_t wd, __nv_bfloat162 step2, uint32_t hi[4],
                                            uint32_t lo[4]) {
-  constexpr float kMagic = 8388616.0f;   // 2^23 + 8
+  uint32_t c8[4];
+  unpack_bf16(wd, c8);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float w0 = (__uint_as_float(0x4B000000u | ((wd >> (8 * i)) & 0xFu)) - kMagic) * step;
-    const float w1 = (__uint_as_float(0x4B000000u | ((wd >> (8 * i + 4)) & 0xFu)) - kMagic) * step;
-    const __nv_bfloat162 h = __floats2bfloat162_rn(w0, w1);
-    const __nv_bfloat162 l = __floats2bfloat162_rn(w0 - __low2float(h), w1 - __high2float(h));
+    const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&c8[i]);
+    const __nv_bfloat162 h = __hmul2(c, step2);
+    const __nv_bfloat162 l = __hfma2(c, step2, __hneg2(h));
     hi[i] = *reinterpret_cast<const uint32_t*>(&h);
     lo[i] = *reinterpret_cast<const uint32_t*>(&l);
   }
@@ -329,9 +331,12 @@ __global__ void __launch_bounds__(kThreads, 1) tp_kernel(const __grid_constant__
           for (int j = 0; j < kHand; ++j) {
             const int g = kHand * q + j;
             const uint4 w = *reinterpret_cast<const uint4*>(cst + tid * 128 + ((g ^ (tid & 7)) << 4));
-            // steps of groups 2i and 2i + 1 share one 32-bit word of the row's eight
+            // steps of groups 2i and 2i + 1 share one 32-bit word of the row's
+            // eight; the group's step goes to both halves
             const uint32_t sw = (g & 4) ? ((g & 2) ? sv.w : sv.z) : ((g & 2) ? sv.y : sv.x);
-            const float step = bf16_bits_to_float((sw >> (16 * (g & 1))) & 0xFFFFu);
+            const uint32_t sb = (sw >> (16 * (g & 1))) & 0xFFFFu;
+            const uint32_t s2 = sb | (sb << 16);
+            const __nv_bfloat162 step = *reinterpret_cast<const __nv_bfloat162*>(&s2);
             uint32_t hi[16], lo[16];
             split_word(w.x, step, hi, lo);
             split_word(w.y, step, hi + 4, lo + 4);

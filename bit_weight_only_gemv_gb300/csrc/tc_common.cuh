@@ -152,5 +152,21 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                : "memory");
 }
 
+// bf16 pairs (c - 8) of one packed word, codes (0, 1), (2, 3), (4, 5),
+// (6, 7): byte i of the word and byte i of the word shifted right by 4 go to
+// bytes 0 and 2, so codes 2i and 2i + 1 sit in bits 0-3 and 16-19; under
+// the bf16 pattern 0x4300 that is 128 + c, minus 136 gives c - 8 (exact).
+__device__ __forceinline__ void unpack_bf16(uint32_t wd, uint32_t out[4]) {
+  const __nv_bfloat162 k136 = __halves2bfloat162(__ushort_as_bfloat16(0x4308), __ushort_as_bfloat16(0x4308));
+  const uint32_t hi = wd >> 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t b = __byte_perm(wd, hi, (uint32_t)(i | (i << 4) | ((4 + i) << 8) | (i << 12)));
+    uint32_t t = and_or(b, 0x000F000Fu, 0x43004300u);
+    __nv_bfloat162 v = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&t), k136);
+    out[i] = *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
 }  // namespace tc
 }  // namespace w4
