@@ -47,7 +47,7 @@ def build(verbose_ptxas: bool = False, force: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
     srcs = [os.path.join(CSRC, s) for s in SOURCES]
     deps = srcs + [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "gemv_tc.h"),
-                   os.path.join(CSRC, "tc_common.cuh"),
+                   os.path.join(CSRC, "tc_common.cuh"), os.path.join(CSRC, "pointer_view.h"),
                    os.path.join(os.path.dirname(PKG), "include", "w4a16.h")]
     if not force and os.path.exists(LIB):
         newest = max(os.path.getmtime(d) for d in deps)

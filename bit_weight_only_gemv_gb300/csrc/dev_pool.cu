@@ -19,6 +19,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "pointer_view.h"
 
 namespace w4 {
 namespace {
@@ -297,23 +298,6 @@ __global__ void __launch_bounds__(256) dev_pool_fill_kernel(const __grid_constan
     p.slot_expert[miss_s[threadIdx.x]] = miss_e[threadIdx.x];
 }
 
-// Kernel-readable address of `ptr` (device memory of the current device,
-// managed memory, page-locked host memory), nullptr otherwise.
-const void* kernel_view(const void* ptr) {
-  int dev = 0;
-  cudaPointerAttributes a = {};
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
-    cudaGetLastError();
-    return nullptr;
-  }
-  switch (a.type) {
-    case cudaMemoryTypeDevice: return a.device == dev ? ptr : nullptr;
-    case cudaMemoryTypeManaged: return ptr;
-    case cudaMemoryTypeHost: return a.devicePointer;
-    default: return nullptr;
-  }
-}
-
 cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, bool pdl,
                        cudaStream_t s, void** args) {
   cudaLaunchConfig_t cfg = {};
@@ -376,8 +360,8 @@ extern "C" w4_status w4_dev_pool_stage(void* state, int num_experts, int num_slo
   if (qw_expert_bytes > qw_stride_bytes || st_expert_bytes > st_stride_bytes ||
       qw_expert_bytes == 0 || st_expert_bytes == 0)
     return W4_ERR_ARG;
-  const void* src_qw = kernel_view(full_qw);
-  const void* src_st = kernel_view(full_st);
+  const void* src_qw = device_view(full_qw);
+  const void* src_st = device_view(full_st);
   if (src_qw == nullptr || src_st == nullptr) return W4_ERR_ARG;
   const auto a16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; };
   if (!a16(state) || !a16(pool_qw) || !a16(src_qw) || !a16(pool_st) || !a16(src_st) ||

@@ -22,6 +22,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "pointer_view.h"
 
 struct w4_slot_pool {
   int num_experts = 0;
@@ -94,12 +95,6 @@ __global__ void __launch_bounds__(256) pool_fill_kernel(const __grid_constant__ 
   }
 }
 
-namespace {
-
-// The address through which kernels on the current device read `ptr`: the
-// pointer itself for memory of this device (or managed memory), the mapped
-// address of page-locked host memory, nullptr for anything else (pageable
-// host memory, another device's memory), which the copy engine serves.
 const void* device_view(const void* ptr) {
   int dev = 0;
   cudaPointerAttributes a = {};
@@ -114,6 +109,8 @@ const void* device_view(const void* ptr) {
     default: return nullptr;
   }
 }
+
+namespace {
 
 w4_status remap(w4_slot_pool* p, const int32_t* ids, int k, int32_t* slot_ids,
                 std::vector<std::pair<int, int>>* miss_list) {
