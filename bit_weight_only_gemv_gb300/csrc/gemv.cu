@@ -99,6 +99,7 @@ struct GemvParams {
   int* ws_count;                       // [B] at the start of the workspace
   float* ws_partial;                   // [B][nch][RB][MR] after it
   int32_t* status;
+  int gated;                           // x rows are [gate K | up K]: the product takes silu(gate) * up
   int dyn;                             // windows handed out at run time (dense, whole rows)
   int* work;                           // [0] windows taken, [1] CTAs done (dyn only)
   // routed calls with real expert ids (all nullptr otherwise)
@@ -118,7 +119,77 @@ struct GemvParams {
 // xscale[j * Kgp + g].  Groups Kg .. Kgp-1 (padding of a team that does not
 // divide K/32) are zero with a zero inverse scale.  Run by the consumer
 // threads.
+// Gated activations (W4_FLAG_SILU_MUL): row j of x holds gate[K] then
+// up[K], and the activation is h = silu(gate) * up = gate / (1 + e^-gate) *
+// up, computed in fp32 and staged as above (fp16 pairs scaled by 2^e per
+// group, rounded to nearest: a relative error of at most 2^-11 per element,
+// where bf16 inputs stage exactly).
+__device__ __noinline__ void stage_x_gated(const GemvParams& p, int nslots, uint8_t* xs,
+                                           float* xscale) {
+  const int rows = nslots * p.MR;
+  for (int idx = threadIdx.x; idx < rows * p.Kgp; idx += kConsumers) {
+    const int j = idx / p.Kgp;
+    const int g = idx - j * p.Kgp;
+    float h[32];
+    float mx = 0.0f;
+    if (g < p.Kg) {
+      const uint4* gs = reinterpret_cast<const uint4*>(p.x + (long long)j * 2 * p.K + (long long)g * 32);
+      const uint4* us = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(gs) + p.K);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 gv = __ldg(gs + i), uv = __ldg(us + i);
+        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {
+            const float gf = __uint_as_float(b ? (gw[q] & 0xFFFF0000u) : (gw[q] << 16));
+            const float uf = __uint_as_float(b ? (uw[q] & 0xFFFF0000u) : (uw[q] << 16));
+            const float v = gf / (1.0f + __expf(-gf)) * uf;
+            h[8 * i + 2 * q + b] = v;
+            mx = fmaxf(mx, fabsf(v));
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) h[i] = 0.0f;
+    }
+    int e = 0;
+    float inv = 1.0f;
+    if (mx != 0.0f) {
+      const int ef = (int)((__float_as_uint(mx) >> 23) & 0xFF);
+      const int E = (ef == 0) ? -127 : ef - 127;
+      e = 9 - E;                                     // max * 2^e in [2^9, 2^10)
+      const int ei = E - 9;
+      inv = (ei >= -126) ? __int_as_float((ei + 127) << 23) : __int_as_float(1 << (ei + 149));
+    }
+    const int ea = e >> 1, eb = e - ea;              // split so each factor is normal
+    const float fa = __int_as_float((ea + 127) << 23);
+    const float fb = __int_as_float((eb + 127) << 23);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      uint4 out;
+      __half2 hp;
+      hp = __floats2half2_rn(h[8 * w] * fa * fb, h[8 * w + 4] * fa * fb);
+      out.x = *reinterpret_cast<uint32_t*>(&hp);
+      hp = __floats2half2_rn(h[8 * w + 1] * fa * fb, h[8 * w + 5] * fa * fb);
+      out.y = *reinterpret_cast<uint32_t*>(&hp);
+      hp = __floats2half2_rn(h[8 * w + 2] * fa * fb, h[8 * w + 6] * fa * fb);
+      out.z = *reinterpret_cast<uint32_t*>(&hp);
+      hp = __floats2half2_rn(h[8 * w + 3] * fa * fb, h[8 * w + 7] * fa * fb);
+      out.w = *reinterpret_cast<uint32_t*>(&hp);
+      *reinterpret_cast<uint4*>(xs + ((long long)(j * 4 + w) * p.Kgp + g) * 16) = out;
+    }
+    xscale[(long long)j * p.Kgp + g] = g < p.Kg ? inv : 0.0f;
+  }
+}
+
 __device__ void stage_x(const GemvParams& p, int item0, int nslots, uint8_t* xs, float* xscale) {
+  if (p.gated) {   // dense calls only: one activation row set per launch
+    stage_x_gated(p, nslots, xs, xscale);
+    return;
+  }
   const int rows = nslots * p.MR;
   for (int idx = threadIdx.x; idx < rows * p.Kgp; idx += kConsumers) {
     const int j = idx / p.Kgp;
@@ -1433,6 +1504,7 @@ bool tc_shape(int K) { return K >= 256 && K % 256 == 0; }
 // cannot run this shape (or for both paths).
 int path_of(int M, int K, unsigned flags) {
   if ((flags & kPathFlags) == kPathFlags) return -1;
+  if (flags & W4_FLAG_SILU_MUL) return (flags & W4_FLAG_TENSOR_CORES) ? -1 : 0;   // CUDA cores
   if (flags & W4_FLAG_CUDA_CORES) return 0;
   if (flags & W4_FLAG_TENSOR_CORES) return tc_shape(K) ? 1 : -1;
   return (M >= kTcMinM && tc_shape(K)) ? 1 : 0;
@@ -1590,13 +1662,15 @@ extern "C" w4_status w4a16_gemv(void* y, const void* qw, const void* st, const v
                                 int N, int K, void* workspace, size_t workspace_bytes,
                                 int32_t* status_dev, unsigned flags, w4_stream_t stream) {
   if (y == nullptr || qw == nullptr || st == nullptr || x == nullptr) return W4_ERR_ARG;
-  if (M < 1 || N < 1 || (flags & ~(W4_FLAG_PDL | kPathFlags)) != 0) return W4_ERR_ARG;
+  if (M < 1 || N < 1 || (flags & ~(W4_FLAG_PDL | kPathFlags | W4_FLAG_SILU_MUL)) != 0)
+    return W4_ERR_ARG;
   if ((flags & kPathFlags) == kPathFlags) return W4_ERR_ARG;
   if (M > W4_MAX_M || K < 32 || K % 32 != 0 || K > W4_MAX_K) return W4_ERR_SHAPE;
   if (!aligned(qw, 16) || !aligned(st, 16) || !aligned(x, 16) || !aligned(y, 2))
     return W4_ERR_ALIGN;
   const int path = path_of(M, K, flags);
   if (path < 0) return W4_ERR_SHAPE;
+  const bool gated = (flags & W4_FLAG_SILU_MUL) != 0;   // x rows [gate K | up K]
   int dev = 0;
   DeviceInfo di;
   if (!current_device(&dev, &di)) return W4_ERR_DEVICE;
@@ -1622,7 +1696,8 @@ extern "C" w4_status w4a16_gemv(void* y, const void* qw, const void* st, const v
     GemvParams p = base_params(pm, N, K);
     p.qw = static_cast<const uint8_t*>(qw);
     p.st = static_cast<const uint8_t*>(st);
-    p.x = static_cast<const __nv_bfloat16*>(x) + (long long)m0 * K;
+    p.x = static_cast<const __nv_bfloat16*>(x) + (long long)m0 * K * (gated ? 2 : 1);
+    p.gated = gated ? 1 : 0;
     p.y = static_cast<__nv_bfloat16*>(y) + (long long)m0 * N;
     p.n_items = 1;
     p.num_experts = 1;

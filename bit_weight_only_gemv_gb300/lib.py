@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_PKG, "libw4a16.so")
 W4_FLAG_PDL = 1
 W4_FLAG_CUDA_CORES = 2
 W4_FLAG_TENSOR_CORES = 4
+W4_FLAG_SILU_MUL = 8
 _PATH_FLAGS = {None: 0, "cuda": W4_FLAG_CUDA_CORES, "tensor": W4_FLAG_TENSOR_CORES}
 STATUS = {0: "W4_OK", 1: "W4_ERR_ARG", 2: "W4_ERR_ALIGN", 3: "W4_ERR_SHAPE",
           4: "W4_ERR_WORKSPACE", 5: "W4_ERR_LAUNCH", 6: "W4_ERR_INDEX", 7: "W4_ERR_VALUE",
@@ -159,30 +160,36 @@ def plan(M: int, N: int, K: int) -> dict:
 
 def gemv(qw: torch.Tensor, st: torch.Tensor, x: torch.Tensor, y: torch.Tensor = None,
          workspace: torch.Tensor = None, status: torch.Tensor = None, pdl: bool = False,
-         stream=None, path: str = None) -> torch.Tensor:
+         stream=None, path: str = None, silu_mul: bool = False) -> torch.Tensor:
     """y[M, N] = x[M, K] @ W^T with W from (qw [N, K/8], st [N, K/32]).
 
     path: None (the library's choice), "cuda" (CUDA cores) or "tensor"
-    (tcgen05 tensor cores; K a multiple of 256)."""
+    (tcgen05 tensor cores; K a multiple of 256).
+    silu_mul: x is [M, 2K] (gate then up) and the product takes
+    silu(gate) * up, formed while the activations are staged."""
     qw = _as_words(qw)
     _need(qw, qw.dtype, "qw")
     _need(st, torch.bfloat16, "st")
     _need(x, torch.bfloat16, "x")
     x2 = x if x.dim() == 2 else x.view(1, -1)
     M, K = x2.shape
+    if silu_mul:
+        if K % 2:
+            raise ValueError("silu_mul needs x rows of [gate | up]")
+        K //= 2
     N = qw.shape[0]
     if qw.shape != (N, K // 8) or st.shape != (N, K // 32):
         raise ValueError("qw/st shapes do not match x")
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     _need(y, torch.bfloat16, "y")
-    need = workspace_bytes(M, N, K, path)
+    need = workspace_bytes(M, N, K, "cuda" if silu_mul else path)
     if need and workspace is None:
         raise ValueError(f"this shape needs a zero-filled workspace of {need} bytes")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    flags = (W4_FLAG_PDL if pdl else 0) | _PATH_FLAGS[path] | (W4_FLAG_SILU_MUL if silu_mul else 0)
     _check(load().w4a16_gemv(_ptr(y), _ptr(qw), _ptr(st), _ptr(x2), M, N, K, _ptr(workspace),
-                             ws_bytes, _ptr(status), (W4_FLAG_PDL if pdl else 0) | _PATH_FLAGS[path],
-                             _stream(stream)),
+                             ws_bytes, _ptr(status), flags, _stream(stream)),
            "w4a16_gemv")
     return y
 

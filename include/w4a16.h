@@ -90,6 +90,8 @@ typedef enum w4_status {
 #define W4_FLAG_PDL 1u
 #define W4_FLAG_CUDA_CORES 2u     /* w4a16_gemv: CUDA-core path at any M */
 #define W4_FLAG_TENSOR_CORES 4u   /* w4a16_gemv: tensor-core path at any M (K % 256 == 0) */
+#define W4_FLAG_SILU_MUL 8u       /* w4a16_gemv: x rows are [gate K | up K]; the product
+                                     takes h = silu(gate) * up (CUDA-core path) */
 
 #define W4_GROUP 32        /* codes per group along K */
 #define W4_MAX_K 65536     /* largest supported K */
@@ -137,6 +139,15 @@ const char *w4_last_cuda_error(void);
  * flags      W4_FLAG_PDL, and at most one of W4_FLAG_CUDA_CORES /
  *            W4_FLAG_TENSOR_CORES (default: tensor cores from M = 8 when K is
  *            a multiple of 256; W4_ERR_SHAPE if the pinned path cannot run K).
+ *            W4_FLAG_SILU_MUL: the gated MLP's down projection fused with its
+ *            activation (page "Gemma 4 on a 4 GB GPU in Plain PyTorch", tip
+ *            "Merge the Small Projections": gate and up are one merged GEMV,
+ *            whose output row [gate | up] feeds this call directly).  x is
+ *            then [M][2K] bf16 and the GEMV multiplies
+ *            h[m][k] = gate[m][k] / (1 + e^-gate[m][k]) * up[m][k], computed
+ *            in fp32 while the activations are staged (no bf16 rounding of h,
+ *            no separate kernel); CUDA-core path at any M (with
+ *            W4_FLAG_TENSOR_CORES: W4_ERR_SHAPE).
  * Returns W4_OK once the work is enqueued.
  *
  * Large CUDA-core launches (w4_plan_info.dynamic_windows) hand their row

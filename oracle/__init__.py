@@ -28,6 +28,8 @@ from .ref import (  # noqa: F401
     dequant,
     gemv_ref,
     gemv_abs_ref,
+    gemv_values_ref,
+    silu_mul_ref,
     gemv_id_ref,
     gemv_id_scaled_ref,
     gather_ref,

@@ -163,6 +163,30 @@ def gemv_abs_ref(qw: np.ndarray, st: np.ndarray, x_bits: np.ndarray) -> np.ndarr
     return x @ w.T
 
 
+def gemv_values_ref(qw: np.ndarray, st: np.ndarray, x: np.ndarray):
+    """(W x, sum_k |w x|) for real-valued activations x [M, K] (fp64): the
+    product gemv_ref takes, for activations that are not bf16 values."""
+    w = dequant(qw, st)
+    x = np.atleast_2d(np.asarray(x, dtype=np.float64))
+    return x @ w.T, np.abs(x) @ np.abs(w).T
+
+
+def silu_mul_ref(x_bits: np.ndarray) -> np.ndarray:
+    """Gated activation of rows [gate K | up K] (bf16 bit patterns): h =
+    silu(gate) * up = gate / (1 + e^-gate) * up, in fp64.
+
+    The down projection of a gated MLP reads this product of the merged
+    gate/up GEMV's two halves ([G4] tip "Merge the Small Projections" merges
+    gate and up into one GEMV; the pages name no activation, SiLU is the
+    reading taken here).
+    """
+    x = bf16_bits_to_f64(np.atleast_2d(x_bits))
+    k = x.shape[1] // 2
+    g, u = x[:, :k], x[:, k:]
+    with np.errstate(over="ignore"):
+        return g / (1.0 + np.exp(-g)) * u
+
+
 def gemv_id_ref(qw_experts: np.ndarray, st_experts: np.ndarray,
                 ids: np.ndarray, x_bits: np.ndarray) -> np.ndarray:
     """Routed-expert GEMV ([MoE] "Streaming without touching a single GPU kernel").

@@ -62,7 +62,9 @@ def test_host_validation_rejects_before_any_launch(L):
     assert L.w4a16_gemv(good, vp((1 << 20) + 8), good, good, 1, 16, 64, None, 0, None, 0,
                         None) == 2
     # unknown flag bit
-    assert L.w4a16_gemv(good, good, good, good, 1, 16, 64, None, 0, None, 8, None) == 1
+    assert L.w4a16_gemv(good, good, good, good, 1, 16, 64, None, 0, None, 16, None) == 1
+    # the fused SiLU-mul activation runs on the CUDA cores only
+    assert L.w4a16_gemv(good, good, good, good, 1, 16, 256, None, 0, None, 8 | 4, None) == 3
     assert L.w4a16_gemv(good, good, good, good, 1, 16, 256, None, 0, None, 6, None) == 1
     assert L.w4a16_gemv(good, good, good, good, 1, 16, 64, None, 0, None, 4, None) == 3
     # gemv_id: x_rows must be 1 or n_ids, strides multiples of 16 and >= an expert

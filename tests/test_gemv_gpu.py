@@ -195,3 +195,44 @@ def test_merged_projection_rows_equal_separate_gemvs(cuda_lib):
     merged, _ = run(np.concatenate(parts), np.concatenate(steps), x_h)
     sep = [run(q, s_, x_h)[0] for q, s_ in zip(parts, steps)]
     assert np.array_equal(host_bits(merged), np.concatenate([host_bits(y) for y in sep], axis=1))
+
+
+@pytest.mark.parametrize("m,n,k", [(1, 2048, 8192), (1, 300, 704), (2, 512, 2816),
+                                   (4, 1000, 2048), (3, 77, 96), (1, 5376, 21504),
+                                   (9, 300, 512)])
+def test_silu_mul_gated_activation_matches_oracle(cuda_lib, m, n, k):
+    """W4_FLAG_SILU_MUL: x rows are [gate K | up K]; the product takes
+    h = silu(gate) * up formed while staging (fp32, staged as fp16 pairs)."""
+    rng = np.random.default_rng(m * 13 + n + k)
+    qw_h = synth.np_words(rng, (n, k // 8))
+    st_h = synth.np_steps(rng, (n, k // 32))
+    x_h = synth.np_x(rng, (m, 2 * k))
+    y = poison_bf16((m, n))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    need = lib.workspace_bytes(m, n, k, "cuda")
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda") if need else None
+    lib.gemv(dev_words(qw_h), dev_bf16(st_h), dev_bf16(x_h), y=y, workspace=ws, status=status,
+             silu_mul=True)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    yb = host_bits(y)
+    assert not np.any(yb == POISON)
+    y_ref, a_ref = oracle.gemv_values_ref(qw_h, st_h, oracle.silu_mul_ref(x_h))
+    assert oracle.within_bound(yb, y_ref, a_ref)
+
+
+def test_merged_gate_up_feeds_the_gated_down_projection(cuda_lib):
+    # the gated MLP of one decode step: merged gate/up GEMV, then the down
+    # GEMV reading its [gate | up] output row directly
+    rng = np.random.default_rng(90)
+    hid, inter = 2048, 8192
+    gu_q = synth.np_words(rng, (2 * inter, hid // 8))
+    gu_s = synth.np_steps(rng, (2 * inter, hid // 32))
+    dn_q = synth.np_words(rng, (hid, inter // 8))
+    dn_s = synth.np_steps(rng, (hid, inter // 32))
+    x_h = synth.np_x(rng, (1, hid))
+    gu = lib.gemv(dev_words(gu_q), dev_bf16(gu_s), dev_bf16(x_h))
+    y = lib.gemv(dev_words(dn_q), dev_bf16(dn_s), gu, silu_mul=True, pdl=True)
+    torch.cuda.synchronize()
+    y_ref, a_ref = oracle.gemv_values_ref(dn_q, dn_s, oracle.silu_mul_ref(host_bits(gu)))
+    assert oracle.within_bound(host_bits(y), y_ref, a_ref)

@@ -286,6 +286,38 @@ def test_gemv_id_scaled_slot_ids_fed_to_the_vectors_change_the_result():
         assert not np.array_equal(good, bad)
 
 
+def test_gemv_values_ref_reduces_to_the_bf16_product():
+    rng = np.random.default_rng(31)
+    qw = synth.np_words(rng, (5, 12))
+    st = synth.np_steps(rng, (5, 3), scale=1.0)
+    xb = synth.np_x(rng, (2, 96))
+    y, a = ref.gemv_values_ref(qw, st, ref.bf16_bits_to_f64(xb))
+    assert np.array_equal(y, ref.gemv_ref(qw, st, xb))
+    assert np.array_equal(a, ref.gemv_abs_ref(qw, st, xb))
+
+
+def test_silu_mul_special_values_and_library_form():
+    from scipy.special import expit
+    g = np.array([0.0, 1.0, -1.0, 20.0, -20.0, 3.5, -100.0, 88.0], dtype=np.float32)
+    u = np.array([2.0, 1.0, 1.0, 0.5, 1.0, 0.0, 1.0, -1.0], dtype=np.float32)
+    x_bits = f32_to_bf16_bits_torch(np.concatenate([g, u]))[None, :]
+    gb = ref.bf16_bits_to_f64(x_bits[0, :8])
+    ub = ref.bf16_bits_to_f64(x_bits[0, 8:])
+    h = ref.silu_mul_ref(x_bits)[0]
+    assert h[0] == 0.0 and h[5] == 0.0                  # silu(0) = 0; up = 0
+    assert h[1] == pytest.approx(1.0 / (1.0 + np.exp(-1.0)), rel=1e-15)
+    assert h[2] == pytest.approx(-1.0 / (1.0 + np.exp(1.0)), rel=1e-15)
+    assert h[3] == pytest.approx(0.5 * 20.0, rel=3e-9)  # silu(g) -> g for large g
+    assert abs(h[6]) < 1e-40                             # -> 0 for very negative g
+    # the textbook form g * sigmoid(g) * u from the library's logistic function
+    assert np.allclose(h, gb * expit(gb) * ub, rtol=1e-14, atol=0)
+    rng = np.random.default_rng(32)
+    xb = synth.np_x(rng, (3, 64))
+    x = ref.bf16_bits_to_f64(xb)
+    assert np.allclose(ref.silu_mul_ref(xb), x[:, :32] * expit(x[:, :32]) * x[:, 32:],
+                       rtol=1e-14, atol=0)
+
+
 # ---------------------------------------------------------------- bf16
 def test_bf16_rne_hand_values():
     cases = [
