@@ -130,9 +130,13 @@ class ClockSampler:
 class DecodePass:
     """Device-resident weights, inputs and outputs of one decode pass."""
 
-    def __init__(self, model: synth.DenseDecoder, device, seed: int = 0, merge: bool = True):
+    def __init__(self, model: synth.DenseDecoder, device, seed: int = 0, merge: bool = True,
+                 gated: bool = False):
         from bit_weight_only_gemv_gb300 import lib
         self.lib = lib
+        # gated MLP: each layer's down projection reads the merged gate/up
+        # output through silu(gate) * up instead of its own activation row
+        self.gated = gated and merge
         self.model = model
         self.dev = device
         self.merge = merge
@@ -210,18 +214,23 @@ class DecodePass:
                 self.ple_qw, self.ple_st, self.ids, out=self.ple_row, status=self.status, pdl=pdl)))
         for li, name, n, k, xk, qw, st in self.mats:
             x = self.x((li, xk), k)
+            gated = self.gated and name == "down"
+            if gated:
+                og = self.y_off[(li, "gate+up")]
+                x = self.y_flat[og:og + 2 * k].view(1, 2 * k)
             o = self.y_off[(li, name)]
             y = self.y_flat[o:o + n].view(1, n)
-            out.append(("gemv", (1, n, k), self._gemv(qw, st, x, y)))
+            out.append(("gemv", (1, n, k), self._gemv(qw, st, x, y, gated)))
         o = self.y_off["logits"]
         out.append(("gemv", (1, m.vocab, m.hidden), self._gemv(
             self.emb_qw, self.emb_st, self.x("final", m.hidden),
             self.y_flat[o:o + m.vocab].view(1, m.vocab))))
         return out
 
-    def _gemv(self, qw, st, x, y):
+    def _gemv(self, qw, st, x, y, gated=False):
         lib = self.lib
-        return lambda pdl: lib.gemv(qw, st, x, y=y, workspace=self.ws, status=self.status, pdl=pdl)
+        return lambda pdl: lib.gemv(qw, st, x, y=y, workspace=self.ws, status=self.status, pdl=pdl,
+                                    silu_mul=gated)
 
     def step_bytes(self):
         return step_bytes_of(self.model)
@@ -422,7 +431,7 @@ def run_gb300(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     model = DENSE_WORKLOADS[args.workload]()
-    dp = DecodePass(model, dev, seed=0, merge=not args.separate)
+    dp = DecodePass(model, dev, seed=0, merge=not args.separate, gated=args.gated_mlp)
     launches = dp.launches()
     stream = torch.cuda.Stream(device=dev)
     # eager warm-up (plans, attributes), then capture the pass as one graph
@@ -521,6 +530,10 @@ def run_gb300(args, world, rank, local):
                    "projections": f"separate ({len(model.projs) * model.layers} GEMVs)"
                    if args.separate else
                    f"merged: q/k/v and gate/up row-concatenated ({len(dp.mats)} GEMVs)",
+                   "gated_mlp": ("each down projection reads its layer's gate/up output "
+                                 "through silu(gate) * up (fused into its activation staging; "
+                                 "bytes_per_step counts one activation row)"
+                                 if dp.gated else None),
                    "global_batch": world, "parallelism": f"replicas x{world}",
                    "bytes_per_step": step_bytes,
                    "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB of weights per step, "
@@ -894,6 +907,10 @@ def main():
     ap.add_argument("--expert-vectors", action="store_true",
                     help="routed-expert workload: per-expert output scales (and down biases) "
                          "by real expert id, slot table checked (w4a16_gemv_id_scaled)")
+    ap.add_argument("--gated-mlp", action="store_true",
+                    help="decode passes: each down projection reads its layer's merged gate/up "
+                         "output through silu(gate) * up (W4_FLAG_SILU_MUL) instead of its own "
+                         "activation row")
     ap.add_argument("--pool", choices=("host", "device"), default="host",
                     help="routed-expert workload: LFU remap on the host per layer (eager steps), "
                          "or on the device (w4_dev_pool_*), each step one CUDA graph replay")
