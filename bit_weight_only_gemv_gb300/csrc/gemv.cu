@@ -189,10 +189,6 @@ __device__ __noinline__ void stage_x_gated(const GemvParams& p, int nslots, uint
 }
 
 __device__ void stage_x(const GemvParams& p, int item0, int nslots, uint8_t* xs, float* xscale) {
-  if (p.gated) {   // dense calls only: one activation row set per launch
-    stage_x_gated(p, nslots, xs, xscale);
-    return;
-  }
   const int rows = nslots * p.MR;
   for (int idx = threadIdx.x; idx < rows * p.Kgp; idx += kConsumers) {
     const int j = idx / p.Kgp;
@@ -529,14 +525,16 @@ __device__ __forceinline__ void finish_window(const GemvParams& p, const float* 
 // Its CTAs walk their rows in windows of RB rows with every offset fixed for
 // the launch; the other calls take the general walk (kWalkGeneral), which
 // kWalkRealIds extends with the real-id checks and per-expert output vectors
-// of w4a16_gemv_id_scaled.
-constexpr int kWalkGeneral = 0, kWalkDense = 1, kWalkRealIds = 2;
+// of w4a16_gemv_id_scaled, and kWalkGated with the gated activation staging
+// (W4_FLAG_SILU_MUL).
+constexpr int kWalkGeneral = 0, kWalkDense = 1, kWalkRealIds = 2, kWalkGated = 3;
 
 template <int MR, int RW, int TT, int CLT, int WALK>
 __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
     gemv_kernel(const __grid_constant__ GemvParams p) {
   constexpr bool DS = WALK == kWalkDense;
   constexpr bool RID = MR == 1 && WALK == kWalkRealIds;
+  constexpr bool GATED = WALK == kWalkGated;   // general walk, gated activations
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -699,7 +697,10 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
   const uint32_t xsc_off = xs_off + (uint32_t)(p.x_slots * MR * 4 * p.Kgp * 16);
   float* red = reinterpret_cast<float*>(smem + xsc_off + p.x_slots * MR * p.Kgp * 4);
   pdl_wait();   // activations and outputs follow earlier kernels
-  stage_x(p, item0, nslots, smem + xs_off, reinterpret_cast<float*>(smem + xsc_off));
+  if constexpr (GATED)
+    stage_x_gated(p, nslots, smem + xs_off, reinterpret_cast<float*>(smem + xsc_off));
+  else
+    stage_x(p, item0, nslots, smem + xs_off, reinterpret_cast<float*>(smem + xsc_off));
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
 
   const int xplane = p.Kgp * 16, xmrow = 4 * p.Kgp * 16, xsmrow = p.Kgp * 4;
@@ -1261,9 +1262,22 @@ using KernelFn = void (*)(GemvParams);
 // The instantiation that runs a plan.  Calls with real expert ids
 // (w4a16_gemv_id_scaled) take their own kernels: the checks and output
 // vectors stay out of every other launch.
-KernelFn kernel_for(const Plan& pl, bool real_ids = false, int* tt = nullptr, int* clt = nullptr) {
+KernelFn kernel_for(const Plan& pl, bool real_ids = false, int* tt = nullptr, int* clt = nullptr,
+                    bool gated = false) {
   if (tt != nullptr) *tt = 0;
   if (clt != nullptr) *clt = 0;
+  if (gated) {   // dense calls with gated activations: generic instantiations
+    switch (pl.MR * 8 + pl.RW) {
+      case 8 + 1: return gemv_kernel<1, 1, 0, 0, kWalkGated>;
+      case 8 + 2: return gemv_kernel<1, 2, 0, 0, kWalkGated>;
+      case 8 + 4: return gemv_kernel<1, 4, 0, 0, kWalkGated>;
+      case 16 + 1: return gemv_kernel<2, 1, 0, 0, kWalkGated>;
+      case 16 + 2: return gemv_kernel<2, 2, 0, 0, kWalkGated>;
+      case 24 + 1: return gemv_kernel<3, 1, 0, 0, kWalkGated>;
+      case 32 + 1: return gemv_kernel<4, 1, 0, 0, kWalkGated>;
+      default: return nullptr;
+    }
+  }
   const bool ds = !pl.routed && pl.S == 1;
   const bool full = pl.NI % pl.CL == 0 && pl.NI * pl.T == pl.Kg;
   const int key = pl.T * 16 + pl.CL;
@@ -1376,12 +1390,12 @@ cudaError_t work_slot(int dev, int** out) {
 }
 
 cudaError_t launch(const GemvParams& prm, const Plan& pl, bool pdl, cudaStream_t stream, int dev) {
-  const KernelFn fn = kernel_for(pl, prm.eids != nullptr);
+  const KernelFn fn = kernel_for(pl, prm.eids != nullptr, nullptr, nullptr, prm.gated != 0);
   if (fn == nullptr) return cudaErrorInvalidConfiguration;
   const cudaError_t ea = allow_smem(fn, pl.smem, dev);
   if (ea != cudaSuccess) return ea;
   GemvParams p = prm;
-  if (pl.dyn) {
+  if (pl.dyn && !prm.gated) {   // run-time windows: the dense walk only
     const cudaError_t ew = work_slot(dev, &p.work);
     if (ew != cudaSuccess) return ew;
     p.dyn = 1;
