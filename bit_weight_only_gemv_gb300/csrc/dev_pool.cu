@@ -177,12 +177,10 @@ __global__ void __launch_bounds__(256) dev_pool_remap_kernel(uint8_t* st, int E,
         int sl = slot_of[e];         // loaded earlier in this request
         if (sl < 0) {
           // lowest free slot
-          unsigned freem = 0;
           for (int j0 = 0; j0 < S; j0 += 32) {
             const int j = j0 + lane;
             const unsigned b = __ballot_sync(0xffffffffu, j < S && in_slot[j] < 0);
             if (sl < 0 && b != 0) sl = j0 + __ffs(b) - 1;
-            freem |= b;
           }
           if (sl < 0) {
             // victim: the slot whose expert is not requested now with the
