@@ -17,22 +17,22 @@
 //    fp32 accumulator.  bf16 x bf16 products are exact; only the fp32 sums
 //    round.  The step is inside A, so no per-group rescaling follows.
 //  * A CTA owns units of 128 weight rows times all the activation rows (the
-//    MMA's N, up to 256).  The copy warp streams 256-code slices of codes (2-D TMA box,
-//    128-byte swizzle) and steps (2-D box), and per two groups the tile's
-//    activations as one 2-D box of 64 codes x the tile's rows with 128-byte
-//    swizzle: the canonical K-major B-operand layout, each 16-code K step an
-//    address offset inside the 128-byte rows.  (A first version staged the
-//    activations as 16-byte rows, one TMA request each; the requests, not the
-//    MMAs or the unpacking, set the pace.)
+//    MMA's N, up to 256; when the weight tiles are too few for the SMs, a
+//    tile of the activation rows).  The copy warp streams 256-code slices of
+//    codes (2-D TMA box, 128-byte swizzle) and steps (2-D box), and per two
+//    groups the unit's activations as one 2-D box of 64 codes x its rows
+//    with 128-byte swizzle: the canonical K-major B-operand layout, each
+//    16-code K step an address offset inside the 128-byte rows.
 //  * Association: one fp32 accumulator per (weight row, activation row) over
 //    the whole of K, groups in order; four epilogue warps round it to bf16
 //    once.  Results depend on K only (not on N, M or the tiling).
 //  * Tensor memory: eight A buffers (one group each, 32 columns), handed from
 //    the unpacking warps to the MMA warp four groups at a time, and one
-//    accumulator of up to 256 columns.  Issuing MMAs and commits costs the
-//    MMA warp a fixed few hundred cycles per hand-off whatever N is, so the
+//    accumulator of up to 256 columns.  Below N = 256 an MMA of 128 rows
+//    takes about as long whatever its N (measured: about 90 cycles), and
+//    each hand-off costs a few hundred cycles of commits and waits, so the
 //    widest N (all activation rows at once) and the largest hand-off the
-//    ring allows do the most work per issue.
+//    ring allows do the most work per MMA.
 //  * Every wait is bounded; on expiry W4_ERR_TIMEOUT is recorded, the warps
 //    leave their loops, in-flight copies and MMAs are waited for (bounded)
 //    and the tensor memory is released before exit.
