@@ -103,3 +103,30 @@ def test_batched_rows_with_run_time_windows(cuda_lib, m, n, k):
     for i in range(m):
         yi = call(qw, st, x[i:i + 1].contiguous())
         assert np.array_equal(host_bits(yi)[0], yb[i])
+
+
+# (M, N, K): the tensor-core small-batch kernel and the prompt GEMM on the
+# merged gate/up and lm_head of the hidden-2048 decoder and the merged gate/up
+# and down of the hidden-5376 decoder
+FULL_BATCHED = [(16, 16384, 2048), (32, 262144, 2048), (8, 43008, 5376),
+                (64, 5376, 21504), (256, 43008, 5376), (200, 16384, 2048)]
+
+
+@pytest.mark.parametrize("m,n,k", FULL_BATCHED)
+def test_full_size_tensor_core_paths(cuda_lib, m, n, k):
+    """Batches of 8-256 activation rows at full size, on the path the plan
+    picks (small-batch kernel up to 32 rows, prompt GEMM above): sampled rows
+    against the oracle, no output unwritten, and the first and last weight
+    rows bitwise equal to a launch over just those rows."""
+    assert lib.plan(m, n, k)["path"] == (2 if m <= 32 else 3)
+    qw, st, _ = weights(n, k, 3 * m + k)
+    x = synth.torch_x((m, k), synth.seed_of(m + 1, k), "cuda")
+    y = call(qw, st, x)
+    yb = host_bits(y)
+    assert not np.any(yb == POISON), "unwritten outputs"
+    rng = np.random.default_rng(m + k)
+    rows = np.unique(np.concatenate([rng.choice(n, 256, replace=False), [0, n - 1]]))
+    assert_gemv_parity(y[:, rows], host_words(qw[rows]), host_bits(st[rows]), host_bits(x))
+    for sl in (slice(0, 640), slice(n - 300, n)):
+        ys = call(qw[sl].contiguous(), st[sl].contiguous(), x)
+        assert np.array_equal(host_bits(ys), yb[:, sl])
