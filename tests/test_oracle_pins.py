@@ -296,6 +296,26 @@ def test_gemv_values_ref_reduces_to_the_bf16_product():
     assert np.array_equal(a, ref.gemv_abs_ref(qw, st, xb))
 
 
+def test_gemv_values_ref_exact_on_real_valued_activations():
+    # activations that are not bf16 values (the gated activation's fp64
+    # products): rational brute force, each fp64 input taken exactly
+    rng = np.random.default_rng(33)
+    n, k = 3, 64
+    qw = synth.np_words(rng, (n, k // 8))
+    st = synth.np_steps(rng, (n, k // 32), scale=1.0)
+    x = rng.standard_normal((2, k)) / 3.0
+    y, a = ref.gemv_values_ref(qw, st, x)
+    for m in range(2):
+        for ni in range(n):
+            codes = [c for j in range(k // 8) for c in hex_codes(qw[ni, j])]
+            terms = [(codes[kk] - 8) * frac_bf16(int(st[ni, kk // 32])) * Fraction(float(x[m, kk]))
+                     for kk in range(k)]
+            exact, exact_abs = sum(terms, Fraction(0)), sum((abs(t) for t in terms), Fraction(0))
+            tol = float(exact_abs) * k * 2.0 ** -52
+            assert abs(Fraction(float(y[m, ni])) - exact) <= Fraction(tol)
+            assert abs(Fraction(float(a[m, ni])) - exact_abs) <= Fraction(tol)
+
+
 def test_silu_mul_special_values_and_library_form():
     from scipy.special import expit
     g = np.array([0.0, 1.0, -1.0, 20.0, -20.0, 3.5, -100.0, 88.0], dtype=np.float32)
@@ -450,6 +470,17 @@ def test_quantize_step_is_bf16_of_signed_absmax_over_minus_eight():
     w2[0, 0] = 1.01                     # 1.01 / -8 is not a bf16: rounded once
     _, st2 = ref.quantize_ref(w2)
     assert int(st2[0, 0]) == int(f32_to_bf16_bits_torch(np.array([np.float32(1.01) / np.float32(-8)]))[0])
+    # steps that round up: 1.99 / -8 (bits past the 8th above one half) and
+    # 8.09375 / -8 = -(1 + 3 * 2^-8), a tie resolved to the even neighbour
+    # -(1 + 4 * 2^-8); truncation would give -(1 + 2^-7) and -(1 + 2 * 2^-8)
+    for v, want in ((1.99, None), (8.09375, -1.015625)):
+        w3 = np.zeros((1, 32), np.float32)
+        w3[0, 7] = v
+        _, st3 = ref.quantize_ref(w3)
+        lib_bits = int(f32_to_bf16_bits_torch(np.array([np.float32(v) / np.float32(-8)]))[0])
+        assert int(st3[0, 0]) == lib_bits
+        if want is not None:
+            assert ref.bf16_bits_to_f64(st3)[0, 0] == want
 
 
 def test_quantize_round_trip_on_grid():
