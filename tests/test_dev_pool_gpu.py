@@ -154,3 +154,42 @@ def test_bad_requests_change_nothing(cuda_lib):
     torch.cuda.synchronize()
     assert lib.STATUS[int(status.item())] == "W4_ERR_INDEX"
     assert np.all(host_bits(y) == POISON)
+
+
+def test_device_pool_hand_traces(cuda_lib):
+    """The hand-worked traces of the policy (tests/golden/lfu_traces.txt):
+    slot ids, the slot table and the miss count at every step."""
+    import test_oracle_pins as pins
+    n, K = 64, 256
+    for name, E, S, steps in pins._read_traces():
+        full_q, full_s, _, _, qs, ss = experts(E, n, K, 7 * E + S)
+        pool_q = torch.zeros((S, qs // 4), dtype=torch.int32, device="cuda")
+        pool_s = torch.zeros((S, ss // 2), dtype=torch.bfloat16, device="cuda")
+        table = torch.full((S,), -1, dtype=torch.int32, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        pool = lib.DevSlotPool(E, S)
+        stages = {}
+        resident = [-1] * S
+        for req, want_slots, want_miss in steps:
+            k = len(req)
+            if k not in stages:      # one bound stage per request length, one pool state
+                ids = torch.zeros(k, dtype=torch.int32, device="cuda")
+                sl = torch.zeros(k, dtype=torch.int32, device="cuda")
+                stages[k] = (ids, sl, pool.bind_stage(ids, pool_q, full_q, qs, qs, pool_s, full_s,
+                                                      ss, ss, sl, slot_expert=table,
+                                                      status=status))
+            ids, sl, stage = stages[k]
+            ids.copy_(torch.tensor(req, dtype=torch.int32))
+            stage()
+            torch.cuda.synchronize()
+            for ex, s_ in want_miss:
+                resident[s_] = ex
+            assert sl.cpu().tolist() == want_slots, name
+            assert table.cpu().tolist() == resident, name
+        assert int(status.item()) == 0, name
+        misses = sum(len(m) for _, _, m in steps)
+        requests = sum(len(r) for r, _, _ in steps)
+        assert pool.stats() == {"requests": requests, "hits": requests - misses, "misses": misses}
+        for s_, ex in enumerate(resident):
+            if ex >= 0:
+                assert torch.equal(pool_q[s_], full_q[ex]) and torch.equal(pool_s[s_], full_s[ex])
