@@ -124,10 +124,13 @@ const char *w4_last_cuda_error(void);
  * qw         uint32 [N][K/8], 16-byte aligned.
  * st         bf16 [N][K/32], 16-byte aligned.
  * x          bf16 [M][K], 16-byte aligned.
- * M          1 .. W4_MAX_M activation rows.  The CUDA-core path takes up to 4
- *            rows per launch and the tensor-core path up to 32; a call with
- *            more rows enqueues several launches (each reading the weights),
- *            all checked before the first is enqueued.
+ * M          1 .. W4_MAX_M activation rows.  By default: below 8 rows the
+ *            CUDA-core path, one launch per 4 rows; 8 to 32 rows one launch
+ *            of the tensor-core small-batch kernel; 33 to W4_MAX_M rows (a
+ *            prompt chunk) one launch of the tensor-core GEMM.  A call pinned
+ *            to the CUDA cores enqueues one launch per 4 rows at any M (each
+ *            reading the weights), all checked before the first is
+ *            enqueued.
  * N          >= 1 output rows.
  * K          multiple of 32, 32 .. W4_MAX_K.
  * workspace  device scratch of at least w4a16_gemv_workspace_bytes(M, N, K)
