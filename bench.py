@@ -277,17 +277,56 @@ def time_replays(g, stream, steps):
     return e0.elapsed_time(e1) / steps
 
 
+def code_tokens(text: str) -> str:
+    """C/C++/CUDA source with comments removed and each run of blank space
+    outside string and character literals made one line break (if it held
+    one: preprocessor lines keep their ends) or one space: the part of a
+    source file that can change what it compiles to."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif c.isspace():
+            j = i
+            while j < n and text[j].isspace():
+                j += 1
+            out.append("\n" if "\n" in text[i:j] else " ")
+            i = j
+        else:
+            out.append(c)
+            i += 1
+    return re.sub(r"\s*\n\s*", "\n", re.sub(r"[ ]+", " ", "".join(out))).strip()
+
+
+def kernel_source_digest() -> str:
+    """sha256 over the code tokens of csrc/gemv.cu then csrc/common.cuh."""
+    h = hashlib.sha256()
+    for f in ("gemv.cu", "common.cuh"):
+        path = os.path.join(ROOT, "bit_weight_only_gemv_gb300", "csrc", f)
+        h.update(code_tokens(open(path, encoding="utf-8").read()).encode())
+    return h.hexdigest()
+
+
 def traffic_from_profile(kernel):
     """DRAM bytes per launch from the committed ncu summary, if still current."""
     path = os.path.join(ROOT, "profiles", "gemv_kernel_traffic.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
-    src = hashlib.sha256()
-    for f in ("gemv.cu", "common.cuh"):
-        src.update(open(os.path.join(ROOT, "bit_weight_only_gemv_gb300", "csrc", f), "rb").read())
     m = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
-    if not m or m.group(1) != src.hexdigest():
+    if not m or m.group(1) != kernel_source_digest():
         return None
     for line in text.splitlines():
         mm = re.match(r"\s*-\s*kernel:\s*(.+?)\s*\|\s*dram_bytes_per_launch:\s*([0-9.]+)\s*\|"
