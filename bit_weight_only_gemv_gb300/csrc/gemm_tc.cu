@@ -2,9 +2,10 @@
 // 5th-generation tensor cores (tcgen05, sm_103a).
 //
 // Page "Gemma 4 on a 4 GB GPU in Plain PyTorch", section "Step 6 — Read
-// Prompts in 32-Bit on a Card Without Tensor Cores": a prompt is read in
-// chunks of 256 tokens, with the weights unpacked to full precision for each
-// multiply (that card has no tensor cores, so it unpacks to fp32 for cuBLAS).
+// Prompts in 32-Bit on a Card Without Tensor Cores": prompts go through the
+// model 256 tokens at a time, and for each product the weights are expanded
+// to full precision first (fp32 for cuBLAS there, on a card with no tensor
+// cores).
 // Here the tensor cores take the product and the weights are unpacked on the
 // fly, without rounding:
 //

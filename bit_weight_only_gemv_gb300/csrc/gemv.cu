@@ -1,9 +1,10 @@
 // W4A16 group-32 GEMV and routed-expert GEMV for GB300 (sm_103a).
 //
 // Page "Gemma 4 on a 4 GB GPU in Plain PyTorch", section "Step 3 — Multiply
-// Straight From the Packed Weights": a decode step multiplies one activation
-// vector by every weight matrix straight from the packed 4-bit words, so the
-// speed limit is how fast the weights stream from memory.  The routed-expert
+// Straight From the Packed Weights": every decoded token takes the product of
+// one activation vector with each weight matrix, computed from the 4-bit words
+// as stored; the time per token is then set by the rate at which those words
+// can be read from memory.  The routed-expert
 // variant (page "Running a 26B MoE on an 8 GB Jetson by streaming experts from
 // SSD", section "Streaming without touching a single GPU kernel") reads expert
 // `id` at base + id * stride.

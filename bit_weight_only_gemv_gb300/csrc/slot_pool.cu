@@ -2,11 +2,12 @@
 // experts into their slots and publish the slot ids to the device.
 //
 // Page "Running a 26B MoE on an 8 GB Jetson by streaming experts from SSD",
-// section "Streaming without touching a single GPU kernel": a persistent pool
-// of expert-sized slots and a small slot-id tensor per MoE layer; a per-layer
-// LFU cache keeps hits in place, loads misses into assigned slots and writes
-// the slot indices before the expert matmul, which then reads the pool through
-// slot ids and sees exactly the bytes of the full expert tensor.  Here the
+// section "Streaming without touching a single GPU kernel": every MoE layer
+// owns a long-lived set of slots, each the size of one expert, and a short
+// tensor of slot numbers.  An LFU policy leaves resident experts where they
+// are, copies missing ones into the slots it picks and fills in the slot
+// numbers before the expert matmul runs; addressed through those numbers, the
+// pool hands the matmul the same bytes as the full expert tensor would.  Here the
 // misses are copied from the full expert tensor, held in HBM or in page-locked
 // Grace memory that the GPU reads in place over NVLink-C2C (the page reads
 // them from an SSD into host memory the Jetson's GPU shares).  An optional

@@ -115,8 +115,9 @@ const char *w4_last_cuda_error(void);
  * w4a16_gemv — dense W4A16 matrix-vector (or small-batch matrix) product.
  *
  * Page "Gemma 4 on a 4 GB GPU in Plain PyTorch", section "Step 3 — Multiply
- * Straight From the Packed Weights": decoding a token multiplies one vector by
- * every weight matrix, straight from the packed 4-bit words.
+ * Straight From the Packed Weights": each decoded token needs the product of
+ * an activation vector with each weight matrix, taken from the packed 4-bit
+ * words as they are stored.
  *
  *   y[m][n] = bf16( sum_{k<K} (code[n][k] - 8) * st[n][k/32] * x[m][k] )
  *
@@ -243,13 +244,14 @@ w4_status w4a16_gemv_id(void *y, const void *qw_base, size_t qw_stride_bytes,
  * per-expert vectors indexed by the REAL expert id.
  *
  * Page "Running a 26B MoE on an 8 GB Jetson by streaming experts from SSD",
- * section "Streaming without touching a single GPU kernel": the selected
- * expert ids feed several consumers; only the expert matmul may read slot
- * ids, while the per-expert scale vectors and the expert biases stay fully
- * resident and must be indexed by the actual expert number.  Feeding them
- * slot ids crashes nothing and silently degrades the model; here the call
- * takes both ids, and given the pool's slot table it checks on the device
- * that every slot holds the expert named for it.
+ * section "Streaming without touching a single GPU kernel": the router's
+ * choice is read by more than the expert matmul.  Per-expert scale vectors
+ * and biases keep a row for every expert in memory at all times, so their
+ * row must be chosen by the true expert number; only the matmul may be sent
+ * to a slot pool.  Handing those tables slot numbers raises no error, it
+ * just picks the wrong rows.  This call therefore takes both kinds of id,
+ * and given the pool's slot table it checks on the device that every slot
+ * holds the expert named for it.
  *
  *   s = ids[i] (slot, or expert, whose weights are read),  e = expert_ids[i]
  *   acc = the fp32 sum of w4a16_gemv_id for row i (same bits)

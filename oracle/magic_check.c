@@ -3,8 +3,8 @@
  * INFRASTRUCTURE: built by __graft_entry__.build() and run by the CPU tests.
  *
  * Page "Gemma 4 on a 4 GB GPU in Plain PyTorch", section "Step 3 — Multiply
- * Straight From the Packed Weights": a 4-bit code c becomes a float by OR-ing
- * it into the bit pattern of 2^23 and subtracting 2^23 + 8, which gives c - 8
+ * Straight From the Packed Weights": placing a 4-bit code c in the low
+ * mantissa bits of the float 2^23 and then subtracting 2^23 + 8 yields c - 8
  * exactly.  The same idea works in 16-bit formats, where the magic constant
  * is 2^10 (fp16, mantissa 10 bits) or 2^7 (bf16, mantissa 7 bits).  The CUDA
  * kernels use the fp16 form on two codes at a time; this program checks every

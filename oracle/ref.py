@@ -12,13 +12,15 @@ Sources (cited by page title and section):
     - "Step 1 — Load Google's QAT Weights Without Unpacking Them": the format
       is compressed-tensors W4A16, 4-bit weight codes in groups of 32 with a
       16-bit step per group and 16-bit activations.
-    - "Step 2 — Keep the Vocabulary Tables in 4-Bit": embed_tokens (tied with
-      lm_head) and the per-layer table are 4-bit codes with one 16-bit step per
-      group; one device copy serves both the row lookup and the output GEMV.
-    - "Step 3 — Multiply Straight From the Packed Weights": a decode step
-      multiplies one vector by every weight matrix straight from the packed
-      words; a code becomes a float by OR-ing it into the bit pattern of 2^23
-      and subtracting 2^23 + 8, i.e. the dequantised value is (code - 8) * step.
+    - "Step 2 — Keep the Vocabulary Tables in 4-Bit": the token table (shared
+      with the output layer) and the per-layer table stay as 4-bit codes, a
+      16-bit step for each group; a single copy on the device serves both the
+      lookup by token id and the output GEMV.
+    - "Step 3 — Multiply Straight From the Packed Weights": each decoded token
+      needs the product of an activation vector with each weight matrix,
+      taken from the packed words as stored; a code is turned into a float by
+      placing it in the low mantissa bits of 2^23 and subtracting 2^23 + 8, so
+      the dequantised value is (code - 8) * step.
     - "Why Doesn't 16-bit Fit?": the per-layer table holds, for every one of
       262,144 vocabulary ids, a row of 35 x 256 values.
 * [MoE] "Running a 26B MoE on an 8 GB Jetson by streaming experts from SSD"
@@ -211,10 +213,11 @@ def gemv_id_scaled_ref(qw_experts: np.ndarray, st_experts: np.ndarray, expert_id
                        x_bits: np.ndarray, scale_bits=None, bias_bits=None):
     """Routed-expert GEMV with per-expert output vectors, by REAL expert id.
 
-    [MoE] "Streaming without touching a single GPU kernel": the selected ids
-    feed several consumers; the per-expert scale vectors and expert biases
-    are fully resident and indexed by the actual expert number (only the
-    matmul may be pointed at a slot pool).  So, with e = expert_ids[i]:
+    [MoE] "Streaming without touching a single GPU kernel": besides the
+    expert matmul, per-expert scale vectors and biases consume the router's
+    choice; those tables hold one row for every expert in memory at all
+    times, so their row is chosen by the true expert number, and only the
+    matmul is redirected to a slot pool.  So, with e = expert_ids[i]:
 
         y_ref[i, n] = scale[e, n] * (W_e x_i)[n] + bias[e, n]
 
