@@ -164,8 +164,10 @@ w4_status w4a16_gemv(void *y, const void *qw, const void *st, const void *x,
                      int M, int N, int K, void *workspace, size_t workspace_bytes,
                      int32_t *status_dev, unsigned flags, w4_stream_t stream);
 
-/* Scratch bytes w4a16_gemv needs for this shape with flags 0 (0 when its
- * plan needs none). */
+/* Scratch bytes to give w4a16_gemv for this shape with flags 0: enough for
+ * every launch a call of this shape makes (on the CUDA cores, the largest
+ * split-K scratch of the plans for up to 4 rows, so it may exceed what one
+ * launch uses); 0 when none of them splits K. */
 size_t w4a16_gemv_workspace_bytes(int M, int N, int K);
 
 /* The same for a call with the given flags (path flags change the plan). */

@@ -249,3 +249,61 @@ def test_slot_pool_failed_copy_forgets_the_slot():
     # the expert is not resident: the next request for it is a miss again
     assert pool.remap([3]) == ([0], [(3, 0)])
     del fake
+
+
+def test_planner_sweep_of_random_shapes():
+    """Every valid shape gets a plan on the path the rule names, within the
+    SM's limits (seeded sample: M 1..256, N 1..300000, K 32..65536)."""
+    rng = np.random.default_rng(2024)
+    for _ in range(3000):
+        M = int(rng.choice([1, 2, 3, 4, 5, 7, 8, 9, 16, 31, 32, 33, 64, 100, 255, 256])) \
+            if rng.random() < 0.5 else int(rng.integers(1, 257))
+        N = int(np.exp(rng.uniform(0, np.log(300000))))
+        K = 32 * int(np.exp(rng.uniform(0, np.log(2048))))
+        if rng.random() < 0.3:
+            K = 256 * max(1, K // 256)
+        p = lib.plan(M, N, K)
+        want = 1 if (M < 8 or K % 256) else (2 if M <= 32 else 3)
+        assert p["path"] == want, (M, N, K, p)
+        assert 1 <= p["ctas"] <= p["ctas_per_sm"] * 152, (M, N, K, p)
+        assert p["smem_bytes"] <= 232448, (M, N, K, p)
+        if p["ctas_per_sm"] == 2:
+            assert p["smem_bytes"] <= 233472 // 2 - 1024, (M, N, K, p)
+        if want == 1:
+            assert p["threads"] == 256 and 1 <= p["rows_per_call"] <= min(M, 4)
+            # a team of lanes shares a row: the largest power of two dividing
+            # the groups that leaves each lane 4 or more (else the largest
+            # dividing one); when a step of 32/team whole rows would pass
+            # 40 KB, up to 32 lanes walk the row and the last are padded
+            g = K // 32
+            t = 1
+            while t < 32 and g % (2 * t) == 0 and g // (2 * t) >= 4:
+                t *= 2
+            if g // t < 4:
+                t = 1
+                while t < 32 and g % (2 * t) == 0:
+                    t *= 2
+            if (32 // t) * (K // 2 + g * 2) > 40 << 10:
+                t = 32
+                while t > 1 and -(-g // t) < 4:
+                    t //= 2
+            assert p["team"] == t, (M, N, K, p)
+            assert 1 <= p["chunk_steps"] <= min(-(-g // t), 12)
+        elif want == 2:
+            assert p["threads"] == 320 and p["rows_per_call"] == min(M, 32)
+        else:
+            assert p["threads"] == 320 and p["rows_per_call"] == M
+            assert lib.workspace_bytes(M, N, K) == 0
+        ws = lib.workspace_bytes(M, N, K)
+        # CUDA cores: the size covers the largest plan a launch of up to 4
+        # rows of this shape may take (a bound); tensor cores: exactly the
+        # split-K scratch of the one launch
+        if want == 1:
+            assert ws > 0 or p["slices"] == 1, (M, N, K, p, ws)
+        else:
+            assert (ws > 0) == (p["slices"] > 1), (M, N, K, p, ws)
+        # a call pinned to either path is planned too (tensor cores: K % 256 == 0)
+        assert lib.workspace_bytes(M, N, K, "cuda") >= 0
+        if K % 256 == 0:
+            assert lib.workspace_bytes(M, N, K, "tensor") == (ws if want != 1 else
+                                                             lib.workspace_bytes(M, N, K, "tensor"))

@@ -236,3 +236,21 @@ def test_merged_gate_up_feeds_the_gated_down_projection(cuda_lib):
     torch.cuda.synchronize()
     y_ref, a_ref = oracle.gemv_values_ref(dn_q, dn_s, oracle.silu_mul_ref(host_bits(gu)))
     assert oracle.within_bound(host_bits(y), y_ref, a_ref)
+
+
+# K whose groups do not split evenly: a short last chunk (37 and 13 groups
+# with chunks of 4) and lane teams padded past the end of a row (101 and 443
+# groups walked by 32 lanes); the generic kernel instantiation
+RAGGED = [(300, 1184, 1), (129, 416, 3), (77, 3232, 1), (40, 14176, 2), (20, 65504, 1)]
+
+
+@pytest.mark.parametrize("n,k,m", RAGGED)
+def test_gemv_ragged_k_matches_oracle(cuda_lib, n, k, m):
+    p = lib.plan(m, n, k)
+    groups = k // 32
+    lanes = -(-groups // p["team"])
+    assert groups % p["team"] or lanes % p["chunk_steps"]     # the shape is ragged
+    rng = np.random.default_rng(n + 3 * k + m)
+    qw_h, st_h, x_h = make(rng, n, k, m)
+    y, _ = run(qw_h, st_h, x_h)
+    assert_gemv_parity(y, qw_h, st_h, x_h)
