@@ -143,6 +143,6 @@ def test_planted_mistake_fails_a_pin(monkeypatch, mid, module, name, old, new):
     for pin, fn, kw in _pin_cases():
         try:
             fn(**kw)
-        except (AssertionError, ValueError, IndexError, FloatingPointError):
-            return          # caught by this pin
+        except AssertionError:
+            return          # a value check of this pin caught it (a crash would not count)
     pytest.fail(f"no pin fails with the planted mistake {mid}")
