@@ -925,7 +925,7 @@ def run_shape(args):
     return 0
 
 
-def main():
+def build_parser() -> argparse.ArgumentParser:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None,
@@ -961,6 +961,11 @@ def main():
     ap.add_argument("--workload", default="dense-35L-h2048",
                     choices=sorted(DENSE_WORKLOADS) + ["moe-30L-h2816"],
                     help="decode pass to time (default: the 35-layer hidden-2048 decoder)")
+    return ap
+
+
+def main():
+    ap = build_parser()
     args = ap.parse_args()
     if args.steps is None:
         args.steps = 128 if args.workload.startswith("moe") else 200
