@@ -1,16 +1,18 @@
 #!/usr/bin/env python3
-"""Benchmark: batch-1 decode pass of a 35-layer W4A16 decoder (hidden 2048).
+"""Benchmark: batch-1 decode pass of a W4A16 decoder, by default the 60-layer
+hidden-5376 one.
 
 One step = one decode pass over the whole hot path, replayed as one CUDA
-graph: embed-row gather (tied 262144 x 2048 table), per-layer-table row gather
-(262144 x 35*256), for each of 35 layers the q/k/v (2048/512/512 x 2048), o
-(2048 x 2048), gate/up (8192 x 2048) and down (2048 x 8192) GEMVs, and the
-lm_head GEMV over the tied table (262144 x 2048); 248 kernels, chained with
-programmatic dependent launch.  All weights and activations are seeded
-synthetic data (uniform codes, |N(0,1)|*0.02/8 steps, N(0,1) activations);
-each layer's q/k/v share one activation row and gate/up share another.  A pass
-reads 1.50 GB of packed weights, more than the 129 MB L2, so every step streams
-from HBM.
+graph: the embed-row gather (tied 262144 x 5376 table), for each of 60 layers
+the merged q/k/v (9472 x 5376), o (5376 x 5376), merged gate/up (43008 x 5376)
+and down (5376 x 21504) GEMVs, and the lm_head GEMV over the tied table
+(262144 x 5376); 242 kernels, chained with programmatic dependent launch.
+All weights and activations are seeded synthetic data (uniform codes,
+|N(0,1)|*0.02/8 steps, N(0,1) activations); each layer's q/k/v share one
+activation row and gate/up share another.  A pass reads 15.2 GB of packed
+weights, far more than the 129 MB L2, so every step streams from HBM.
+`--workload dense-35L-h2048` runs the 35-layer hidden-2048 decoder (with its
+per-layer table), `--workload moe-30L-h2816` the routed-expert decoder.
 
 Prints one JSON line (see --help).  `--impl reference` times the fp64 CPU
 oracle instead, on a bounded sample of the same pass.
@@ -39,6 +41,10 @@ from bit_weight_only_gemv_gb300 import metrics, synth  # noqa: E402
 METRIC = "W4A16 GEMV HBM GB/s and % of GB300 peak; decode-equivalent tok/s at batch 1"
 DENSE_WORKLOADS = {"dense-35L-h2048": synth.dense_2048, "dense-60L-h5376": synth.dense_5376}
 UNIT = "tok/s"
+# the arithmetic of the CUDA-core path (batch 1): exact fp16 products of
+# (code - 8) and power-of-two-scaled activations, fp16 partial sums of 4
+# products, fp32 accumulation
+DTYPE = "w4a16: exact f16 products, f16 partial sums of 4 products, f32 accumulate"
 NOMINAL_HBM_GBPS = 8000.0
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 
@@ -337,45 +343,113 @@ def traffic_from_profile(kernel):
 
 
 # ------------------------------------------------------------------ CPU oracle
-def oracle_sample(dp, proj_names, lm_rows, layer=0):
-    """Copy a sample of the pass to the host and return (seconds, sample_bytes).
+# One sample definition serves the main line's cpu_baseline and the
+# --impl reference arm: a bounded slice of one decode pass of the same
+# workload, run by the fp64 oracle, its time scaled to the whole pass by
+# algorithmic bytes.
+SAMPLE_ROWS = 256          # rows of each sampled matrix
+CPU_BASELINE_SECONDS = 10.0
 
-    The sample is the given projections of one layer (full matrices), lm_rows
-    rows of the lm_head GEMV and both row gathers, computed by the fp64 oracle.
-    """
-    import oracle
+
+def merged_groups(model, merge=True):
+    """Projections that one GEMV serves, in launch order: q/k/v and gate/up
+    row-concatenated when merged (they read the same activation row)."""
+    groups = []
+    for pr in model.projs:
+        if merge and groups and groups[-1][0] == pr.x_key and groups[-1][1][0].k == pr.k:
+            groups[-1][1].append(pr)
+        else:
+            groups.append((pr.x_key, [pr]))
+    return [("+".join(p.name for p in prs), sum(p.n for p in prs), prs[0].k) for _, prs in groups]
+
+
+def sample_rows(n, rows=SAMPLE_ROWS):
+    """Evenly spaced row indices of an n-row matrix."""
+    r = min(rows, n)
+    return np.arange(r, dtype=np.int64) * (n // r)
+
+
+def dense_sample_from_recipe(model, merge=True, seed=0):
+    """The sample drawn on the host by the workload's recipe (same shapes and
+    distributions as the GPU arm's weights): layer 0's GEMVs as launched,
+    SAMPLE_ROWS rows each, SAMPLE_ROWS lm_head rows, the row gathers."""
+    rng = np.random.default_rng(seed)
+    items = []
+    for name, n, k in merged_groups(model, merge):
+        r = len(sample_rows(n))
+        items.append(("gemv", synth.np_words(rng, (r, k // 8)), synth.np_steps(rng, (r, k // 32)),
+                      synth.np_x(rng, (1, k))))
+    r = len(sample_rows(model.vocab))
+    h = model.hidden
+    items.append(("gemv", synth.np_words(rng, (r, h // 8)), synth.np_steps(rng, (r, h // 32)),
+                  synth.np_x(rng, (1, h))))
+    for w in (h, model.per_layer_width):
+        if w:
+            items.append(("gather", synth.np_words(rng, (1, w // 8)),
+                          synth.np_steps(rng, (1, w // 32)), None))
+    return items
+
+
+def dense_sample_from_device(dp):
+    """The same sample, read back from the bytes the GPU arm uses."""
     m = dp.model
-    host = []
+    items = []
+
+    def rows_of(qw, st, idx):
+        t = torch.from_numpy(idx).to(dp.dev)
+        return (qw[t].cpu().numpy().view(np.uint32),
+                st[t].view(torch.int16).cpu().numpy().view(np.uint16))
+
     for li, name, n, k, xk, qw, st in dp.mats:
-        if li != layer or not any(p in name.split("+") for p in proj_names):
+        if li != 0:
             continue
-        x = dp.x((layer, xk), k)
-        host.append((qw.cpu().numpy().view(np.uint32), st.view(torch.int16).cpu().numpy().view(np.uint16),
-                     x.view(torch.int16).cpu().numpy().view(np.uint16), metrics.gemv_bytes(1, n, k)))
-    rows = np.arange(lm_rows) * (m.vocab // lm_rows)
-    lm_qw = dp.emb_qw[torch.from_numpy(rows).to(dp.dev)].cpu().numpy().view(np.uint32)
-    lm_st = dp.emb_st[torch.from_numpy(rows).to(dp.dev)].view(torch.int16).cpu().numpy().view(np.uint16)
-    lm_x = dp.x("final", m.hidden).view(torch.int16).cpu().numpy().view(np.uint16)
-    tid = int(dp.ids.item())
-    e_qw = dp.emb_qw[tid:tid + 1].cpu().numpy().view(np.uint32)
-    e_st = dp.emb_st[tid:tid + 1].view(torch.int16).cpu().numpy().view(np.uint16)
-    pw = m.per_layer_width
-    if pw:
-        p_qw = dp.ple_qw[tid:tid + 1].cpu().numpy().view(np.uint32)
-        p_st = dp.ple_st[tid:tid + 1].view(torch.int16).cpu().numpy().view(np.uint16)
+        q, s_ = rows_of(qw, st, sample_rows(n))
+        items.append(("gemv", q, s_, dp.x((0, xk), k).view(torch.int16).cpu().numpy().view(np.uint16)))
+    q, s_ = rows_of(dp.emb_qw, dp.emb_st, sample_rows(m.vocab))
+    items.append(("gemv", q, s_, dp.x("final", m.hidden).view(torch.int16).cpu().numpy()
+                  .view(np.uint16)))
+    tid = np.array([int(dp.ids.item())])
+    items.append(("gather",) + rows_of(dp.emb_qw, dp.emb_st, tid) + (None,))
+    if m.per_layer_width:
+        items.append(("gather",) + rows_of(dp.ple_qw, dp.ple_st, tid) + (None,))
+    return items
+
+
+def moe_sample_from_recipe(cfg, seed=0):
+    """Routed workload: one layer's top-k experts, SAMPLE_ROWS // 2 rows of
+    each expert's merged gate/up (shared activation row) and of its down
+    projection (its own activation row)."""
+    rng = np.random.default_rng(seed)
+    items = []
+    r = SAMPLE_ROWS // 2
+    for n, k in ((2 * cfg.expert_inter, cfg.hidden), (cfg.hidden, cfg.expert_inter)):
+        x = synth.np_x(rng, (1, k))
+        for _ in range(cfg.top_k):
+            items.append(("gemv", synth.np_words(rng, (min(r, n), k // 8)),
+                          synth.np_steps(rng, (min(r, n), k // 32)), x))
+    return items
+
+
+def sample_bytes(items):
+    nb = 0
+    for kind, qw, st, x in items:
+        if kind == "gemv":
+            nb += metrics.gemv_bytes(1, qw.shape[0], qw.shape[1] * 8)
+        else:
+            nb += metrics.gather_bytes(1, qw.shape[1] * 8)
+    return nb
+
+
+def run_oracle_sample(items):
+    """Seconds the fp64 oracle takes over the sample."""
+    import oracle
     t0 = time.perf_counter()
-    nbytes = 0
-    for qw, st, x, b in host:
-        oracle.gemv_ref(qw, st, x)
-        nbytes += b
-    oracle.gemv_ref(lm_qw, lm_st, lm_x)
-    nbytes += metrics.gemv_bytes(1, lm_rows, m.hidden)
-    oracle.gather_ref(e_qw, e_st, np.array([0]))
-    nbytes += metrics.gather_bytes(1, m.hidden)
-    if pw:
-        oracle.gather_ref(p_qw, p_st, np.array([0]))
-        nbytes += metrics.gather_bytes(1, pw)
-    return time.perf_counter() - t0, nbytes
+    for kind, qw, st, x in items:
+        if kind == "gemv":
+            oracle.gemv_ref(qw, st, x)
+        else:
+            oracle.gather_ref(qw, st, np.array([0]))
+    return time.perf_counter() - t0
 
 
 def cpu_cores():
@@ -385,26 +459,27 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+def sample_note(items, pass_bytes):
+    return (f"{len(items)} pieces of one pass (layer 0's GEMVs as launched, {SAMPLE_ROWS} rows "
+            f"each, {SAMPLE_ROWS} lm_head rows, the row gathers; {sample_bytes(items):,} of "
+            f"{pass_bytes:,} algorithmic bytes), fp64 NumPy oracle; time scaled to the whole "
+            "pass by algorithmic bytes; NumPy may use BLAS threads on the listed cores")
+
+
+def cpu_baseline_of(items, pass_bytes, seconds=CPU_BASELINE_SECONDS):
+    """The oracle on the sample, repeated for about `seconds`; tok/s scaled
+    to whole passes."""
+    reps, spent = 0, 0.0
+    while reps == 0 or spent < seconds:
+        spent += run_oracle_sample(items)
+        reps += 1
+    per_token = spent / reps * pass_bytes / sample_bytes(items)
+    return {"value": 1.0 / per_token, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": sample_note(items, pass_bytes) + f"; {reps} repetitions, {spent:.1f} s",
+            "sample_ms": spent / reps * 1e3, "extrapolated_ms_per_token": per_token * 1e3}
+
+
 # ------------------------------------------------------------------ arms
-def reference_sample(model, seed=0):
-    """Host arrays for one bounded oracle sample, drawn by the same recipe."""
-    rng = np.random.default_rng(seed)
-    pr = model.projs[0]
-    lm_rows = 256
-    return {
-        "proj": (synth.np_words(rng, (pr.n, pr.k // 8)), synth.np_steps(rng, (pr.n, pr.k // 32)),
-                 synth.np_x(rng, (1, pr.k)), metrics.gemv_bytes(1, pr.n, pr.k)),
-        "lm": (synth.np_words(rng, (lm_rows, model.hidden // 8)),
-               synth.np_steps(rng, (lm_rows, model.hidden // 32)), synth.np_x(rng, (1, model.hidden)),
-               metrics.gemv_bytes(1, lm_rows, model.hidden)),
-        "emb": (synth.np_words(rng, (1, model.hidden // 8)), synth.np_steps(rng, (1, model.hidden // 32)),
-                metrics.gather_bytes(1, model.hidden)),
-        "ple": (synth.np_words(rng, (1, model.per_layer_width // 8)),
-                synth.np_steps(rng, (1, model.per_layer_width // 32)),
-                metrics.gather_bytes(1, model.per_layer_width)),
-    }
-
-
 def step_bytes_of(model):
     b = metrics.gather_bytes(1, model.hidden)
     if model.per_layer_width:
@@ -414,51 +489,98 @@ def step_bytes_of(model):
     return b + metrics.gemv_bytes(1, model.vocab, model.hidden)
 
 
+def moe_step_bytes(cfg):
+    I, H, k_top = cfg.expert_inter, cfg.hidden, cfg.top_k
+    return cfg.layers * (metrics.gemv_id_bytes(k_top, 1, 2 * I, H) +
+                         metrics.gemv_id_bytes(k_top, k_top, H, I))
+
+
+def dense_config(model, args, world, step_bytes):
+    """config object of a dense decode pass (shared by both arms)."""
+    n_mats = len(merged_groups(model, not args.separate)) * model.layers
+    return {"workload": f"{model.name} decode pass, batch 1 (gathers, {model.layers} "
+                        f"layers of q/k/v/o/gate/up/down GEMVs, {model.vocab}x"
+                        f"{model.hidden} lm_head)",
+            "projections": f"separate ({len(model.projs) * model.layers} GEMVs)"
+            if args.separate else
+            f"merged: q/k/v and gate/up row-concatenated ({n_mats} GEMVs)",
+            "gated_mlp": ("each down projection reads its layer's gate/up output "
+                          "through silu(gate) * up (fused into its activation staging; "
+                          "bytes_per_step counts one activation row)"
+                          if args.gated_mlp and not args.separate else None),
+            "global_batch": world, "parallelism": f"replicas x{world}",
+            "bytes_per_step": step_bytes,
+            "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB of weights per step, "
+                  "129 MB L2)"}
+
+
+def moe_config(cfg, args, world):
+    """config object of the routed-expert decode workload (shared by both arms)."""
+    E, S, H, I, k_top, L = (cfg.experts, cfg.slots, cfg.hidden, cfg.expert_inter, cfg.top_k,
+                            cfg.layers)
+    device_pool = args.pool == "device"
+    return {"workload": f"{cfg.name}: routed decode, batch 1, {L} layers, top-{k_top} of "
+                        f"{E} experts (Zipf {cfg.zipf_s}, repeat {cfg.repeat_p}), "
+                        f"{S}-slot LFU pool per layer; per layer merged gate/up "
+                        f"{2 * I}x{H} and down {H}x{I} through w4a16_gemv_id",
+            "global_batch": world, "parallelism": f"replicas x{world}",
+            "timed": ("one CUDA graph replay per step: the step's router ids picked "
+                      "on the device, per layer the device LFU remap, pool copies and "
+                      "slot ids, 2 gemv_id (CUDA events)" if device_pool else
+                      "eager steps: host LFU remap + pool copies + slot ids + 2 gemv_id "
+                      "per layer (CUDA events)"),
+            "pool_layout": "one 32-slot pool per layer; a slot holds an expert's gate/up "
+                           "and down codes (and, in a second pool array, steps)",
+            "expert_home": ("page-locked host memory, pool fills over NVLink-C2C"
+                            if args.expert_home == "host" else "HBM"),
+            "shared_ffn": {"none": None,
+                           "serial": "dense FFN of one expert's shape per layer, after "
+                                     "the pool fill on the same stream",
+                           "overlap": "dense FFN of one expert's shape per layer, the "
+                                      "pool fill beside it on a second stream, joined "
+                                      "before the routed GEMVs"}[args.shared_ffn],
+            "expert_vectors": ("per-expert output scales (gate/up, down) and down "
+                               "biases by real id, slot table checked, "
+                               "w4a16_gemv_id_scaled; real ids copied to the device "
+                               "once per step" if args.expert_vectors else None)}
+
+
 def run_reference(args, world, rank):
-    """The CPU oracle, as it stands, on the host cores: bounded samples per step."""
+    """The CPU oracle, as it stands, on the host cores: each step one run of
+    the bounded sample of the selected workload's pass."""
     if rank != 0:
         return 0
-    import oracle
-    model = synth.dense_2048()
-    sample = reference_sample(model)
-    step_bytes = step_bytes_of(model)
-
-    def one():
-        t0 = time.perf_counter()
-        nb = 0
-        for key in ("proj", "lm"):
-            qw, st, x, b = sample[key]
-            oracle.gemv_ref(qw, st, x)
-            nb += b
-        for key in ("emb", "ple"):
-            qw, st, b = sample[key]
-            oracle.gather_ref(qw, st, np.array([0]))
-            nb += b
-        return time.perf_counter() - t0, nb
-
+    if args.workload.startswith("moe"):
+        cfg = synth.moe_2816()
+        items = moe_sample_from_recipe(cfg)
+        pass_bytes = moe_step_bytes(cfg)
+        config = moe_config(cfg, args, world)
+    else:
+        model = DENSE_WORKLOADS[args.workload]()
+        items = dense_sample_from_recipe(model, merge=not args.separate)
+        pass_bytes = step_bytes_of(model)
+        config = dense_config(model, args, world, pass_bytes)
     for _ in range(args.warmup):
-        one()
-    secs, nb = 0.0, 0
+        run_oracle_sample(items)
+    t0 = time.perf_counter()
     for _ in range(args.steps):
-        t, b = one()
-        secs += t
-        nb += b
-    per_token = secs * step_bytes / nb
+        run_oracle_sample(items)
+    spent = time.perf_counter() - t0
+    sample_ms = spent / args.steps * 1e3
+    per_token = spent / args.steps * pass_bytes / sample_bytes(items)
     value = 1.0 / per_token
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_token * 1e3,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sample_ms,
+        "ms_per_step_note": "time actually spent per step: one oracle run of the sample",
+        "extrapolated_ms_per_token": per_token * 1e3,
+        "sample_fraction_of_pass": sample_bytes(items) / pass_bytes,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic",
-        "config": {"workload": model.name + " decode pass, batch 1 (gathers + 245 projection "
-                               "GEMVs + 262144x2048 lm_head)", "global_batch": 1,
-                   "parallelism": "single (rank 0 only)"},
+        "data": "synthetic", "config": config,
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-                         "sample": "per step: one 2048x2048 projection + 256 lm_head rows + both "
-                                   "row gathers, fp64 NumPy oracle; scaled to the whole pass by "
-                                   "algorithmic bytes"},
+                         "sample": sample_note(items, pass_bytes)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        "hbm_gbs": metrics.gbps(step_bytes, per_token),
+        "hbm_gbs": metrics.gbps(pass_bytes, per_token),
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -546,37 +668,15 @@ def run_gb300(args, world, rank, local):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        # a bounded sample: every projection of layer 0 for the small model,
-        # the two smallest for the large one
-        small = sorted(model.projs, key=lambda pr: pr.n * pr.k)
-        names = [p.name for p in (model.projs if model.hidden <= 2048 else small[:2])]
-        t, nb = oracle_sample(dp, names, 4096)
-        per_token = t * step_bytes / nb
-        cpu = {"value": 1.0 / per_token, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-               "sample": f"layer 0 ({', '.join(names)}, full) + 4096 of {model.vocab} lm_head "
-                         "rows + the row gathers, fp64 NumPy oracle; scaled to the whole pass by "
-                         "algorithmic bytes; NumPy may use BLAS threads on the listed cores"}
+        cpu = cpu_baseline_of(dense_sample_from_device(dp), step_bytes)
 
     line = {
         "metric": METRIC, "value": tok_s, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "w4a16: f16 products, f32 accumulate",
+        "dtype": DTYPE,
         "data": "synthetic",
-        "config": {"workload": f"{model.name} decode pass, batch 1 (gathers, {model.layers} "
-                               f"layers of q/k/v/o/gate/up/down GEMVs, {model.vocab}x"
-                               f"{model.hidden} lm_head)",
-                   "projections": f"separate ({len(model.projs) * model.layers} GEMVs)"
-                   if args.separate else
-                   f"merged: q/k/v and gate/up row-concatenated ({len(dp.mats)} GEMVs)",
-                   "gated_mlp": ("each down projection reads its layer's gate/up output "
-                                 "through silu(gate) * up (fused into its activation staging; "
-                                 "bytes_per_step counts one activation row)"
-                                 if dp.gated else None),
-                   "global_batch": world, "parallelism": f"replicas x{world}",
-                   "bytes_per_step": step_bytes,
-                   "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB of weights per step, "
-                         "129 MB L2)"},
+        "config": dense_config(model, args, world, step_bytes),
         "hbm_gbs": metrics.gbps(step_bytes, ms * 1e-3),
         "frac_of_nominal_8tbps": metrics.gbps(step_bytes, ms * 1e-3) / NOMINAL_HBM_GBPS,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
@@ -847,32 +947,9 @@ def run_moe(args, world, rank, local):
     line = {
         "metric": METRIC, "value": world * 1000.0 / ms, "unit": UNIT, "n_gpus": world,
         "steps": steps, "warmup": warm, "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "w4a16: f16 products, f32 accumulate",
+        "scaling": "weak", "vs_baseline": None, "dtype": DTYPE,
         "data": "synthetic",
-        "config": {"workload": f"{cfg.name}: routed decode, batch 1, {L} layers, top-{k_top} of "
-                               f"{E} experts (Zipf {cfg.zipf_s}, repeat {cfg.repeat_p}), "
-                               f"{S}-slot LFU pool per layer; per layer merged gate/up "
-                               f"{2 * I}x{H} and down {H}x{I} through w4a16_gemv_id",
-                   "global_batch": world, "parallelism": f"replicas x{world}",
-                   "timed": ("one CUDA graph replay per step: the step's router ids picked "
-                             "on the device, per layer the device LFU remap, pool copies and "
-                             "slot ids, 2 gemv_id (CUDA events)" if device_pool else
-                             "eager steps: host LFU remap + pool copies + slot ids + 2 gemv_id "
-                             "per layer (CUDA events)"),
-                   "pool_layout": "one 32-slot pool per layer; a slot holds an expert's gate/up "
-                                  "and down codes (and, in a second pool array, steps)",
-                   "expert_home": ("page-locked host memory, pool fills over NVLink-C2C"
-                                   if host_home else "HBM"),
-                   "shared_ffn": {"none": None,
-                                  "serial": "dense FFN of one expert's shape per layer, after "
-                                            "the pool fill on the same stream",
-                                  "overlap": "dense FFN of one expert's shape per layer, the "
-                                             "pool fill beside it on a second stream, joined "
-                                             "before the routed GEMVs"}[shared],
-                   "expert_vectors": ("per-expert output scales (gate/up, down) and down "
-                                      "biases by real id, slot table checked, "
-                                      "w4a16_gemv_id_scaled; real ids copied to the device "
-                                      "once per step" if vectors else None)},
+        "config": moe_config(cfg, args, world),
         "host_seconds_per_step": host_s / steps,
         "kernel": {"ms_per_step": kms, "tok_s": 1000.0 / kms, "bytes_per_step": kernel_bytes,
                    "gbps": gbps, "frac": gbps / peak, "peak": peak, "peak_kind": peak_kind,
@@ -958,9 +1035,10 @@ def build_parser() -> argparse.ArgumentParser:
                          "shape (merged gate/up, down; w4a16_gemv) and run the pool fill "
                          "before it on the same stream (serial) or beside it on a second "
                          "stream, joined before the routed GEMVs (overlap)")
-    ap.add_argument("--workload", default="dense-35L-h2048",
+    ap.add_argument("--workload", default="dense-60L-h5376",
                     choices=sorted(DENSE_WORKLOADS) + ["moe-30L-h2816"],
-                    help="decode pass to time (default: the 35-layer hidden-2048 decoder)")
+                    help="decode pass to time (default: the 60-layer hidden-5376 decoder "
+                         "with its 262144 x 5376 lm_head)")
     return ap
 
 

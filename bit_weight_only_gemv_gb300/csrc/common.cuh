@@ -106,12 +106,6 @@ __device__ __forceinline__ void bulk_g2s_evict_first(uint32_t dst, const void* s
       : "memory");
 }
 
-// Hint: bring [p, p + bytes) into L2 (bulk, no destination).  p 16-byte
-// aligned, bytes a positive multiple of 16, the range inside one allocation.
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

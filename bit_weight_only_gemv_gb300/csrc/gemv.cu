@@ -1863,13 +1863,15 @@ extern "C" w4_status w4a16_gemv_static_scratch(void* y, const void* qw, const vo
                                                int32_t* status_dev, unsigned flags,
                                                w4_stream_t stream) {
   if (y == nullptr || qw == nullptr || st == nullptr || x == nullptr) return W4_ERR_ARG;
-  if (M < 1 || N < 1 || (flags & ~(W4_FLAG_PDL | kPathFlags)) != 0) return W4_ERR_ARG;
+  if (M < 1 || N < 1 || (flags & ~(W4_FLAG_PDL | kPathFlags | W4_FLAG_SILU_MUL)) != 0)
+    return W4_ERR_ARG;
   if ((flags & kPathFlags) == kPathFlags) return W4_ERR_ARG;
   if (M > W4_MAX_M || K < 32 || K % 32 != 0 || K > W4_MAX_K) return W4_ERR_SHAPE;
   if (!aligned(qw, 16) || !aligned(st, 16) || !aligned(x, 16) || !aligned(y, 2))
     return W4_ERR_ALIGN;
   const int path = path_of(M, K, flags);
   if (path < 0) return W4_ERR_SHAPE;
+  const bool gated = (flags & W4_FLAG_SILU_MUL) != 0;   // x rows [gate K | up K]
   int dev = 0;
   DeviceInfo di;
   if (!current_device(&dev, &di)) return W4_ERR_DEVICE;
@@ -1906,7 +1908,8 @@ extern "C" w4_status w4a16_gemv_static_scratch(void* y, const void* qw, const vo
     GemvParams p = base_params(pm, N, K);
     p.qw = static_cast<const uint8_t*>(qw);
     p.st = static_cast<const uint8_t*>(st);
-    p.x = static_cast<const __nv_bfloat16*>(x) + (long long)m0 * K;
+    p.x = static_cast<const __nv_bfloat16*>(x) + (long long)m0 * K * (gated ? 2 : 1);
+    p.gated = gated ? 1 : 0;
     p.y = static_cast<__nv_bfloat16*>(y) + (long long)m0 * N;
     p.n_items = 1;
     p.num_experts = 1;

@@ -201,6 +201,10 @@ size_t w4a16_gemv_workspace_bytes_flags(int M, int N, int K, unsigned flags);
  *    that must start at zero.  Calls on the same device that may overlap on
  *    the GPU (for example issued to different streams) race on the array:
  *    issue them one after another in one stream per device.
+ *  - W4_FLAG_PDL is accepted, but a launch that uses the array follows the
+ *    clearing memset in its stream, so it does not overlap the kernel
+ *    before it; launches of shapes that need no scratch overlap as with
+ *    w4a16_gemv.
  */
 #define W4_STATIC_SCRATCH_BYTES (256u << 10)
 

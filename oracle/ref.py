@@ -29,7 +29,7 @@ Sources (cited by page title and section):
   pool plus a slot-id tensor must give bitwise the same logits as addressing
   the full expert tensor.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
 
 * nibble order inside a 32-bit word: low nibble first, so element ``k`` of a
   row lives in word ``k // 8`` at bits ``4*(k % 8) .. 4*(k % 8)+3``;
@@ -297,7 +297,8 @@ def bound_violations(y_bits: np.ndarray, y_ref: np.ndarray, abs_ref: np.ndarray,
 
     ``y_bits`` are the bf16 results, ``y_ref`` the unrounded fp64 sums and
     ``abs_ref`` the fp64 sums of |w x|.  +0 and -0 compare equal.  A
-    non-finite reference requires a non-finite result.
+    non-finite reference requires a result of the same class: +inf for +inf,
+    -inf for -inf, a NaN for a NaN.
     """
     y = bf16_bits_to_f64(y_bits)
     y_ref = np.asarray(y_ref, dtype=np.float64)
@@ -305,7 +306,8 @@ def bound_violations(y_bits: np.ndarray, y_ref: np.ndarray, abs_ref: np.ndarray,
     with np.errstate(invalid="ignore"):
         err = np.abs(y - y_ref)
         ok = err <= rel * np.asarray(abs_ref) + ulp_bf16(y_ref)
-    ok = np.where(ref_finite, ok & np.isfinite(y), ~np.isfinite(y))
+    same_class = (np.isnan(y) & np.isnan(y_ref)) | (np.isinf(y_ref) & (y == y_ref))
+    ok = np.where(ref_finite, ok & np.isfinite(y), same_class)
     return ~ok
 
 

@@ -84,6 +84,14 @@ def test_host_validation_rejects_before_any_launch(L):
     assert scaled(scale=vp((1 << 20) + 1)) == 2
     assert scaled(bias=vp((1 << 20) + 3)) == 2
     assert scaled(table=vp((1 << 20) + 2)) == 2
+    # the no-allocation GEMV takes w4a16_gemv's flags (the gated flag on the
+    # CUDA cores only) and refuses the rest before any launch
+    sgemv = L.w4a16_gemv_static_scratch
+    assert sgemv(good, good, good, good, 1, 16, 64, None, 16, None) == 1
+    assert sgemv(good, good, good, good, 1, 16, 256, None, 6, None) == 1
+    assert sgemv(good, good, good, good, 1, 16, 256, None, 8 | 4, None) == 3
+    assert sgemv(good, good, good, good, 1, 16, 48, None, 8, None) == 3
+    assert sgemv(None, good, good, good, 1, 16, 64, None, 8, None) == 1
     assert L.w4_embed_gather(good, good, good, good, 0, 10, 64, None, 0, None) == 1
     assert L.w4_pack(good, good, 4, 40, None, None) == 3
     assert L.w4_quantize(good, good, vp((1 << 20) + 4), 4, 64, None) == 2

@@ -50,3 +50,40 @@ def test_profile_commands_parse_with_the_current_flags():
             raise AssertionError(f"{name}: bench.py {' '.join(argv)} no longer parses")
         seen += 1
     assert seen >= 8
+
+
+def test_reference_arm_reports_time_it_spent(capsys):
+    """The oracle arm runs the selected workload's sample; steps x ms_per_step
+    is the time it spent, the extrapolation to a whole pass is apart."""
+    import json
+    import time
+    for workload in ("dense-60L-h5376", "dense-35L-h2048", "moe-30L-h2816"):
+        args = bench.build_parser().parse_args(
+            ["--impl", "reference", "--steps", "3", "--warmup", "3", "--workload", workload])
+        t0 = time.perf_counter()
+        assert bench.run_reference(args, 1, 0) == 0
+        wall = time.perf_counter() - t0
+        line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+        assert line["impl"] == "reference" and line["steps"] == 3
+        assert line["steps"] * line["ms_per_step"] <= wall * 1e3
+        assert workload.split("-")[0] in line["config"]["workload"]
+        frac = line["sample_fraction_of_pass"]
+        assert 0 < frac < 1
+        # value is the extrapolated whole-pass rate
+        assert abs(line["value"] * line["extrapolated_ms_per_token"] - 1e3) < 1e-6 * 1e3
+        assert abs(line["extrapolated_ms_per_token"] * frac - line["ms_per_step"]) < \
+            1e-6 * line["ms_per_step"]
+
+
+def test_dense_sample_covers_each_launched_matrix():
+    from bit_weight_only_gemv_gb300 import synth
+    model = synth.dense_5376()
+    groups = bench.merged_groups(model)
+    assert [g[0] for g in groups] == ["q+k+v", "o", "gate+up", "down"]
+    assert [g[1:] for g in groups] == [(9472, 5376), (5376, 5376), (43008, 5376), (5376, 21504)]
+    items = bench.dense_sample_from_recipe(model)
+    gemvs = [it for it in items if it[0] == "gemv"]
+    assert len(gemvs) == len(groups) + 1                      # + the lm_head rows
+    assert [it[1].shape[1] * 8 for it in gemvs] == [5376, 5376, 5376, 21504, 5376]
+    assert all(it[1].shape[0] == bench.SAMPLE_ROWS for it in gemvs)
+    assert sum(1 for it in items if it[0] == "gather") == 1    # no per-layer table

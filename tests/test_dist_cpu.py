@@ -42,7 +42,7 @@ def _worker(rank, world, port, out):
 
 def test_max_over_ranks_gloo():
     world = 2
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
     assert dict(out) == {0: 2.5, 1: 2.5}

@@ -63,6 +63,49 @@ def test_gemv_id_matches_oracle(cuda_lib, e, n, k, n_ids, x_rows, pad):
         assert np.array_equal(host_bits(yd)[0], yb[i])
 
 
+# K whose groups do not split evenly over a lane team's chunks: a short last
+# chunk (37 and 13 groups, chunks of 4) and teams padded past the end of a row
+# (101 and 443 groups walked by 32 lanes); broadcast and per-id activations,
+# expert strides with and without padding
+RAGGED_ROUTED = [(4, 70, 1184, 5, 5, 16), (5, 129, 416, 6, 1, 0), (4, 33, 3232, 3, 1, 32),
+                 (3, 20, 14176, 4, 4, 48), (3, 45, 3232, 4, 4, 0)]
+
+
+@pytest.mark.parametrize("e,n,k,n_ids,x_rows,pad", RAGGED_ROUTED)
+def test_gemv_id_ragged_k_matches_oracle(cuda_lib, e, n, k, n_ids, x_rows, pad):
+    p = lib.plan(1, n, k)
+    groups = k // 32
+    assert groups % p["team"] or (-(-groups // p["team"])) % p["chunk_steps"]   # ragged
+    rng = np.random.default_rng(e + 5 * n + k + n_ids + pad)
+    # expert strides: the sizes rounded up to 16 bytes, plus the padding
+    qw_h, st_h, qwb, stb, qs, ss = experts(rng, e, n, k, (-(n * k // 2)) % 16 + pad,
+                                           (-(n * k // 16)) % 16 + pad)
+    ids_h = rng.integers(0, e, size=n_ids).astype(np.int32)
+    ids_h[-1] = ids_h[0]                          # repeated id
+    x_h = synth.np_x(rng, (x_rows, k))
+    y = poison_bf16((n_ids, n))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lib.gemv_id(dev_bytes(qwb), dev_bytes(stb), torch.from_numpy(ids_h).to("cuda"),
+                dev_bf16(x_h), n, k, e, qs, ss, y=y, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    yb = host_bits(y)
+    assert not np.any(yb == POISON)
+    y_ref = oracle.gemv_id_ref(qw_h, st_h, ids_h, x_h)
+    a_ref = np.stack([oracle.gemv_abs_ref(qw_h[d], st_h[d], x_h[0 if x_rows == 1 else i])[0]
+                      for i, d in enumerate(ids_h)])
+    assert oracle.within_bound(yb, y_ref, a_ref)
+    # and row i is bitwise the dense GEMV of expert ids[i]
+    for i, d in enumerate(ids_h):
+        need = lib.workspace_bytes(1, n, k)
+        yd = lib.gemv(dev_words(qw_h[d]), dev_bf16(st_h[d]),
+                      dev_bf16(x_h[0 if x_rows == 1 else i][None]),
+                      workspace=torch.zeros(max(16, need), dtype=torch.uint8, device="cuda")
+                      if need else None)
+        torch.cuda.synchronize()
+        assert np.array_equal(host_bits(yd)[0], yb[i])
+
+
 def test_gemv_id_bad_ids_leave_rows_unwritten(cuda_lib):
     rng = np.random.default_rng(11)
     e, n, k = 4, 64, 2048

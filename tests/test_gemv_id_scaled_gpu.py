@@ -63,6 +63,39 @@ def test_scaled_matches_oracle(cuda_lib, e, n, k, n_ids, x_rows, vec):
     assert oracle.within_bound(yb, y_ref, a_ref)
 
 
+@pytest.mark.parametrize("e,n,k,n_ids,x_rows", [(4, 72, 1184, 5, 5), (5, 136, 416, 6, 1),
+                                                 (4, 40, 3232, 3, 1), (3, 24, 14176, 4, 4)])
+def test_scaled_ragged_k_matches_oracle(cuda_lib, e, n, k, n_ids, x_rows):
+    # K with a short last chunk (37, 13 groups) or a padded lane team (101,
+    # 443 groups), real ids through a slot permutation with the slot table
+    p = lib.plan(1, n, k)
+    groups = k // 32
+    assert groups % p["team"] or (-(-groups // p["team"])) % p["chunk_steps"]   # ragged
+    rng = np.random.default_rng(e * 3 + n + k + n_ids)
+    qw_h, st_h, qw, st = expert_set(rng, e, n, k)
+    sc_h = bf16_bits(rng, (e, n))
+    bi_h = bf16_bits(rng, (e, n), -0.5, 0.5)
+    eids_h = rng.integers(0, e, size=n_ids).astype(np.int32)
+    perm = rng.permutation(e).astype(np.int32)        # slot s holds expert perm[s]
+    slot_of = np.argsort(perm).astype(np.int32)
+    sids_h = slot_of[eids_h]
+    qw_pool = qw[torch.from_numpy(perm).long().cuda()].contiguous()
+    st_pool = st[torch.from_numpy(perm).long().cuda()].contiguous()
+    x_h = synth.np_x(rng, (x_rows, k))
+    y = poison_bf16((n_ids, n))
+    status = status_word()
+    lib.gemv_id_scaled(qw_pool, st_pool, torch.from_numpy(sids_h).cuda(), dev_bf16(x_h), n, k, e,
+                       n * k // 2, n * k // 16, torch.from_numpy(eids_h).cuda(), e,
+                       slot_expert=torch.from_numpy(perm).cuda(), scale=dev_bf16(sc_h),
+                       bias=dev_bf16(bi_h), y=y, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    yb = host_bits(y)
+    assert not np.any(yb == POISON)
+    y_ref, a_ref = oracle.gemv_id_scaled_ref(qw_h, st_h, eids_h, x_h, sc_h, bi_h)
+    assert oracle.within_bound(yb, y_ref, a_ref)
+
+
 def test_no_vectors_is_bitwise_gemv_id(cuda_lib):
     rng = np.random.default_rng(5)
     e, n, k = 6, 704, 2816

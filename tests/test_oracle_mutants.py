@@ -57,8 +57,14 @@ MUTANTS = [
      "ok = err <= rel * np.asarray(abs_ref) + ulp_bf16(y_ref)",
      "ok = err <= rel * np.asarray(abs_ref)"),
     ("bound_accepts_non_finite", ref, "bound_violations",
-     "ok = np.where(ref_finite, ok & np.isfinite(y), ~np.isfinite(y))",
+     "ok = np.where(ref_finite, ok & np.isfinite(y), same_class)",
      "ok = np.where(ref_finite, ok | ~np.isfinite(y), True)"),
+    ("bound_any_non_finite_class", ref, "bound_violations",
+     "ok = np.where(ref_finite, ok & np.isfinite(y), same_class)",
+     "ok = np.where(ref_finite, ok & np.isfinite(y), ~np.isfinite(y))"),
+    ("bound_infinity_sign_ignored", ref, "bound_violations",
+     "(np.isinf(y_ref) & (y == y_ref))",
+     "(np.isinf(y_ref) & np.isinf(y))"),
     ("silu_sign", ref, "silu_mul_ref", "g / (1.0 + np.exp(-g)) * u", "g / (1.0 + np.exp(g)) * u"),
     ("gate_and_up_swapped", ref, "silu_mul_ref", "g, u = x[:, :k], x[:, k:]",
      "u, g = x[:, :k], x[:, k:]"),

@@ -388,6 +388,24 @@ def test_bound_check_logic():
     assert ref.bound_violations(np.array([0x3F80], np.uint16), np.array([np.inf]), np.array([np.inf]))[0]
 
 
+def test_bound_non_finite_classes():
+    # a non-finite reference takes a result of the same class: bf16 bit
+    # patterns +inf 0x7F80, -inf 0xFF80, a quiet NaN 0x7FC0 (and one with the
+    # sign bit set), against references +inf, -inf, NaN
+    bits = np.array([0x7F80, 0xFF80, 0x7FC0, 0xFFC0], np.uint16)
+    refs = np.array([np.inf, -np.inf, np.nan])
+    got = np.array([[ref.bound_violations(np.array([b], np.uint16), np.array([r]),
+                                          np.array([np.inf]))[0] for r in refs] for b in bits])
+    expect = np.array([[False, True, True],     # +inf result
+                       [True, False, True],     # -inf result
+                       [True, True, False],     # NaN result
+                       [True, True, False]])    # negative NaN result
+    assert np.array_equal(got, expect)
+    # and a non-finite result where the reference is finite fails
+    for b in bits:
+        assert ref.bound_violations(np.array([b], np.uint16), np.array([1.0]), np.array([1.0]))[0]
+
+
 # ---------------------------------------------------------------- gather
 def test_gather_matches_exact_products_rounded_by_torch():
     rng = np.random.default_rng(12)
