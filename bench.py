@@ -233,6 +233,34 @@ class DecodePass:
             self.y_flat[o:o + m.vocab].view(1, m.vocab))))
         return out
 
+    def chain_launches(self):
+        """The same pass as the row gather(s) plus ONE w4a16_gemv_chain launch
+        of every GEMV, each task depending on the one before (as in a
+        decoder, where each projection reads what the previous produced)."""
+        lib, m = self.lib, self.model
+        out = [e for e in self.launches() if e[0] == "gather"]
+        tasks, shapes = [], []
+        for li, name, n, k, xk, qw, st in self.mats:
+            x = self.x((li, xk), k).view(-1)
+            gated = self.gated and name == "down"
+            if gated:
+                og = self.y_off[(li, "gate+up")]
+                x = self.y_flat[og:og + 2 * k]
+            o = self.y_off[(li, name)]
+            tasks.append(lib.gemv_task(qw, st, x, self.y_flat[o:o + n], dep=len(tasks) - 1,
+                                       silu_mul=gated))
+            shapes.append((1, n, k))
+        o = self.y_off["logits"]
+        tasks.append(lib.gemv_task(self.emb_qw, self.emb_st, self.x("final", m.hidden).view(-1),
+                                   self.y_flat[o:o + m.vocab], dep=len(tasks) - 1))
+        shapes.append((1, m.vocab, m.hidden))
+        self.chain_ws = torch.zeros(lib.chain_workspace_bytes(tasks), dtype=torch.uint8,
+                                    device=self.dev)
+        call = lib.bind_gemv_chain(tasks, self.chain_ws, self.status)
+        self.chain_plan = lib.chain_plan(tasks)
+        out.append(("chain", shapes, lambda pdl: call(pdl=pdl)))
+        return out
+
     def _gemv(self, qw, st, x, y, gated=False):
         lib = self.lib
         return lambda pdl: lib.gemv(qw, st, x, y=y, workspace=self.ws, status=self.status, pdl=pdl,
@@ -253,6 +281,8 @@ class DecodePass:
 def kernel_key(kind, shape, lib):  # ncu names the instantiation
     if kind == "gather":
         return "gather_kernel"
+    if kind == "chain":
+        return "chain_kernel"
     M, N, K = shape
     p = lib.plan(M, N, K)
     if p["path"] == 2:
@@ -508,6 +538,10 @@ def dense_config(model, args, world, step_bytes):
                           "through silu(gate) * up (fused into its activation staging; "
                           "bytes_per_step counts one activation row)"
                           if args.gated_mlp and not args.separate else None),
+            "launch": ("the row gather(s), then every GEMV of the pass in ONE w4a16_gemv_chain "
+                       "launch, each task waiting for the one before"
+                       if getattr(args, "chain", False) else
+                       "one launch per GEMV, chained with programmatic dependent launch"),
             "global_batch": world, "parallelism": f"replicas x{world}",
             "bytes_per_step": step_bytes,
             "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB of weights per step, "
@@ -539,6 +573,11 @@ def moe_config(cfg, args, world):
                            "overlap": "dense FFN of one expert's shape per layer, the "
                                       "pool fill beside it on a second stream, joined "
                                       "before the routed GEMVs"}[args.shared_ffn],
+            "routed_ffn": ("one w4a16_gemv_chain launch per layer: routed gate/up, then each "
+                           "expert's down product on silu(gate) * up of its own gate/up rows"
+                           if getattr(args, "chain", False) else
+                           "two w4a16_gemv_id launches per layer, down on its own activation "
+                           "rows"),
             "expert_vectors": ("per-expert output scales (gate/up, down) and down "
                                "biases by real id, slot table checked, "
                                "w4a16_gemv_id_scaled; real ids copied to the device "
@@ -593,7 +632,7 @@ def run_gb300(args, world, rank, local):
     torch.cuda.set_device(dev)
     model = DENSE_WORKLOADS[args.workload]()
     dp = DecodePass(model, dev, seed=0, merge=not args.separate, gated=args.gated_mlp)
-    launches = dp.launches()
+    launches = dp.chain_launches() if args.chain else dp.launches()
     stream = torch.cuda.Stream(device=dev)
     # eager warm-up (plans, attributes), then capture the pass as one graph
     with torch.cuda.stream(stream):
@@ -630,7 +669,8 @@ def run_gb300(args, world, rank, local):
     keys = [kernel_key(k, s, lib) for k, s, _ in launches]
     by_key = {}
     for (kind, shape, f), key in zip(launches, keys):
-        b = metrics.gemv_bytes(*shape) if kind == "gemv" else metrics.gather_bytes(*shape)
+        b = (metrics.gemv_bytes(*shape) if kind == "gemv" else metrics.gather_bytes(*shape)
+             if kind == "gather" else sum(metrics.gemv_bytes(*sh) for sh in shape))
         by_key.setdefault(key, []).append((f, b))
     key_time = {}
     for key, items in by_key.items():
@@ -771,6 +811,25 @@ def run_moe(args, world, rank, local):
         for name, (n, k) in shapes.items():
             lay["y"][name] = torch.empty((k_top, n), dtype=torch.bfloat16, device=dev)
             lay["y_full"][name] = torch.empty((k_top, n), dtype=torch.bfloat16, device=dev)
+        if args.chain:
+            # one launch per layer: gate/up, then down on silu(gate) * up of
+            # each expert's own gate/up rows (the fused routed FFN)
+            for full, calls in ((False, lay["calls"]), (True, lay["calls_full"])):
+                ys = lay["y_full" if full else "y"]
+                src_q, src_s = lay["full_q" if full else "pool_q"], lay["full_s" if full else "pool_s"]
+                ids = lay["ids_full" if full else "slot_ids"]
+                ne = E if full else S
+                tasks = [lib.gemv_id_task(src_q[:, qoff["gate_up"] // 4:], src_s[:, soff["gate_up"] // 2:],
+                                          ids, lay["x"]["gate_up"], ys["gate_up"], 2 * I, H, ne,
+                                          qcomb, scomb),
+                         lib.gemv_id_task(src_q[:, qoff["down"] // 4:], src_s[:, soff["down"] // 2:],
+                                          ids, ys["gate_up"], ys["down"], H, I, ne, qcomb, scomb,
+                                          dep=0, silu_mul=True)]
+                ws = torch.zeros(lib.chain_workspace_bytes(tasks), dtype=torch.uint8, device=dev)
+                calls.append(lib.bind_gemv_chain(tasks, ws, status))
+            layers.append(lay)
+            continue
+        for name, (n, k) in shapes.items():
             for full, calls in ((False, lay["calls"]), (True, lay["calls_full"])):
                 q = lay["full_q" if full else "pool_q"][:, qoff[name] // 4:]
                 st = lay["full_s" if full else "pool_s"][:, soff[name] // 2:]
@@ -788,6 +847,8 @@ def run_moe(args, world, rank, local):
         layers.append(lay)
 
     device_pool = args.pool == "device"
+    if args.chain and vectors:
+        raise SystemExit("--chain runs without --expert-vectors")
     if device_pool and shared != "none":
         raise SystemExit("--pool device runs without --shared-ffn")
     # device pool: every step's router ids on the device; a device counter
@@ -953,13 +1014,16 @@ def run_moe(args, world, rank, local):
         "host_seconds_per_step": host_s / steps,
         "kernel": {"ms_per_step": kms, "tok_s": 1000.0 / kms, "bytes_per_step": kernel_bytes,
                    "gbps": gbps, "frac": gbps / peak, "peak": peak, "peak_kind": peak_kind,
-                   "note": "the 60 gemv_id launches of one step replayed as a graph, "
-                           "PDL-chained"},
+                   "note": ("the 30 w4a16_gemv_chain launches (routed gate/up, then down on "
+                            "silu(gate) * up) of one step replayed as a graph, PDL-chained"
+                            if args.chain else "the 60 gemv_id launches of one step replayed "
+                            "as a graph, PDL-chained")},
         "pool": dict(lfu, hit_rate=lfu["hits"] / max(1, lfu["requests"]),
                      copy_bytes_per_step=copied / steps),
         "bitwise_pool_vs_full": {"steps": total, "layers": L, "mismatched_values": int(bad.item())},
         # per layer: pool fill / slot ids, 2 gemv_id (+ 2 dense GEMVs)
-        "gpu_launches": steps * L * (4 if device_pool else 3 if shared == "none" else 5),
+        "gpu_launches": steps * L * ((4 if device_pool else 3 if shared == "none" else 5) -
+                                     (1 if args.chain else 0)),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -1023,6 +1087,9 @@ def build_parser() -> argparse.ArgumentParser:
     ap.add_argument("--expert-vectors", action="store_true",
                     help="routed-expert workload: per-expert output scales (and down biases) "
                          "by real expert id, slot table checked (w4a16_gemv_id_scaled)")
+    ap.add_argument("--chain", action="store_true",
+                    help="decode passes: every GEMV of the pass in one w4a16_gemv_chain launch "
+                         "(each task waiting for the one before) instead of one launch each")
     ap.add_argument("--gated-mlp", action="store_true",
                     help="decode passes: each down projection reads its layer's merged gate/up "
                          "output through silu(gate) * up (W4_FLAG_SILU_MUL) instead of its own "

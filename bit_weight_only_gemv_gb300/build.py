@@ -17,8 +17,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libw4a16.so")
-SOURCES = ["gemv.cu", "gemv_tc.cu", "gemm_tc.cu", "gather.cu", "quant.cu", "slot_pool.cu",
-           "dev_pool.cu"]
+SOURCES = ["gemv.cu", "chain.cu", "gemv_tc.cu", "gemm_tc.cu", "gather.cu", "quant.cu",
+           "slot_pool.cu", "dev_pool.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -46,7 +46,8 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
 def build(verbose_ptxas: bool = False, force: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
     srcs = [os.path.join(CSRC, s) for s in SOURCES]
-    deps = srcs + [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "gemv_tc.h"),
+    deps = srcs + [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "gemv_core.cuh"),
+                   os.path.join(CSRC, "gemv_host.h"), os.path.join(CSRC, "gemv_tc.h"),
                    os.path.join(CSRC, "tc_common.cuh"), os.path.join(CSRC, "pointer_view.h"),
                    os.path.join(os.path.dirname(PKG), "include", "w4a16.h")]
     if not force and os.path.exists(LIB):

@@ -53,6 +53,8 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "gemv_core.cuh"
+#include "gemv_host.h"
 #include "gemv_tc.h"
 
 // Window counters of dense launches that hand out their windows at run time:
@@ -136,56 +138,19 @@ __device__ __noinline__ void stage_x_gated(const GemvParams& p, int nslots, uint
     if (g < p.Kg) {
       const uint4* gs = reinterpret_cast<const uint4*>(p.x + (long long)j * 2 * p.K + (long long)g * 32);
       const uint4* us = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(gs) + p.K);
+      uint4 gv[4], uv[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const uint4 gv = __ldg(gs + i), uv = __ldg(us + i);
-        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-#pragma unroll
-          for (int b = 0; b < 2; ++b) {
-            const float gf = __uint_as_float(b ? (gw[q] & 0xFFFF0000u) : (gw[q] << 16));
-            const float uf = __uint_as_float(b ? (uw[q] & 0xFFFF0000u) : (uw[q] << 16));
-            // every CTA forms the whole row: the fast exponential and
-            // division (relative error near 2^-21, below the staging's
-            // 2^-11; 0 below gate = -87, where the product is under 2^-120)
-            const float v = __fdividef(gf * uf, 1.0f + __expf(-gf));
-            h[8 * i + 2 * q + b] = v;
-            mx = fmaxf(mx, fabsf(v));
-          }
-        }
+        gv[i] = __ldg(gs + i);
+        uv[i] = __ldg(us + i);
       }
+      mx = silu_mul_group(gv, uv, h);
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i) h[i] = 0.0f;
     }
-    int e = 0;
-    float inv = 1.0f;
-    if (mx != 0.0f) {
-      const int ef = (int)((__float_as_uint(mx) >> 23) & 0xFF);
-      const int E = (ef == 0) ? -127 : ef - 127;
-      e = 9 - E;                                     // max * 2^e in [2^9, 2^10)
-      const int ei = E - 9;
-      inv = (ei >= -126) ? __int_as_float((ei + 127) << 23) : __int_as_float(1 << (ei + 149));
-    }
-    const int ea = e >> 1, eb = e - ea;              // split so each factor is normal
-    const float fa = __int_as_float((ea + 127) << 23);
-    const float fb = __int_as_float((eb + 127) << 23);
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      uint4 out;
-      __half2 hp;
-      hp = __floats2half2_rn(h[8 * w] * fa * fb, h[8 * w + 4] * fa * fb);
-      out.x = *reinterpret_cast<uint32_t*>(&hp);
-      hp = __floats2half2_rn(h[8 * w + 1] * fa * fb, h[8 * w + 5] * fa * fb);
-      out.y = *reinterpret_cast<uint32_t*>(&hp);
-      hp = __floats2half2_rn(h[8 * w + 2] * fa * fb, h[8 * w + 6] * fa * fb);
-      out.z = *reinterpret_cast<uint32_t*>(&hp);
-      hp = __floats2half2_rn(h[8 * w + 3] * fa * fb, h[8 * w + 7] * fa * fb);
-      out.w = *reinterpret_cast<uint32_t*>(&hp);
-      *reinterpret_cast<uint4*>(xs + ((long long)(j * 4 + w) * p.Kgp + g) * 16) = out;
-    }
-    xscale[(long long)j * p.Kgp + g] = g < p.Kg ? inv : 0.0f;
+    store_staged_group_f32(h, mx, xs + (long long)j * 4 * p.Kgp * 16 + g * 16, p.Kgp * 16,
+                           xscale + (long long)j * p.Kgp + g, g < p.Kg);
   }
 }
 
@@ -203,101 +168,9 @@ __device__ void stage_x(const GemvParams& p, int item0, int nslots, uint8_t* xs,
 #pragma unroll
       for (int i = 0; i < 4; ++i) v[i] = __ldg(src + i);
     }
-    uint32_t mx = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      mx = __vmaxu2(mx, v[i].x & 0x7FFF7FFFu);
-      mx = __vmaxu2(mx, v[i].y & 0x7FFF7FFFu);
-      mx = __vmaxu2(mx, v[i].z & 0x7FFF7FFFu);
-      mx = __vmaxu2(mx, v[i].w & 0x7FFF7FFFu);
-    }
-    mx = max(mx & 0xFFFFu, mx >> 16);
-    int e = 0;
-    float inv = 1.0f;
-    if (mx != 0) {
-      const int ef = (int)(mx >> 7);                 // biased exponent, 0..255
-      const int E = (ef == 0) ? -127 : ef - 127;     // unbiased (subnormal: -127)
-      e = 9 - E;                                     // max * 2^e in [2^9, 2^10)
-      const int ei = E - 9;                          // inverse scale exponent
-      inv = (ei >= -126) ? __int_as_float((ei + 127) << 23) : __int_as_float(1 << (ei + 149));
-    }
-    const int ea = e >> 1, eb = e - ea;              // split so each factor is normal
-    const float fa = __int_as_float((ea + 127) << 23);
-    const float fb = __int_as_float((eb + 127) << 23);
-    const uint32_t* wv = reinterpret_cast<const uint32_t*>(v);
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      float f[8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t pair = wv[4 * w + i];       // elements 8w+2i, 8w+2i+1
-        f[2 * i] = __uint_as_float(pair << 16) * fa * fb;
-        f[2 * i + 1] = __uint_as_float(pair & 0xFFFF0000u) * fa * fb;
-      }
-      uint4 out;
-      __half2 h;
-      h = __floats2half2_rn(f[0], f[4]);
-      out.x = *reinterpret_cast<uint32_t*>(&h);
-      h = __floats2half2_rn(f[1], f[5]);
-      out.y = *reinterpret_cast<uint32_t*>(&h);
-      h = __floats2half2_rn(f[2], f[6]);
-      out.z = *reinterpret_cast<uint32_t*>(&h);
-      h = __floats2half2_rn(f[3], f[7]);
-      out.w = *reinterpret_cast<uint32_t*>(&h);
-      *reinterpret_cast<uint4*>(xs + ((long long)(j * 4 + w) * p.Kgp + g) * 16) = out;
-    }
-    xscale[(long long)j * p.Kgp + g] = g < p.Kg ? inv : 0.0f;
+    store_staged_group(v, xs + (long long)j * 4 * p.Kgp * 16 + g * 16, p.Kgp * 16,
+                       xscale + (long long)j * p.Kgp + g, g < p.Kg);
   }
-}
-
-// ---------------------------------------------------------------- the dot
-__device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
-
-// Four fp16 pairs (c - 8) of one packed word, in pair order
-// (nibble 0, 4), (1, 5), (2, 6), (3, 7).
-__device__ __forceinline__ void unpack_word(uint32_t wd, __half2 h[4]) {
-  const __half2 k1032 = u2h(0x64086408u);   // 1032
-  const __half2 k16th = u2h(0x2C002C00u);   // 1/16
-  const __half2 km72 = u2h(0xD480D480u);    // -72
-  const uint32_t s8 = wd >> 8;
-  h[0] = __hsub2(u2h(and_or(wd, 0x000F000Fu, 0x64006400u)), k1032);
-  h[1] = __hfma2(u2h(and_or(wd, 0x00F000F0u, 0x64006400u)), k16th, km72);
-  h[2] = __hsub2(u2h(and_or(s8, 0x000F000Fu, 0x64006400u)), k1032);
-  h[3] = __hfma2(u2h(and_or(s8, 0x00F000F0u, 0x64006400u)), k16th, km72);
-}
-
-// c + lo + hi of an fp16 pair, each add in fp32 (exact widening).
-__device__ __forceinline__ float add_pair_f32(float c, __half2 v) {
-  float d;
-  const uint32_t u = *reinterpret_cast<uint32_t*>(&v);
-  asm("{\n\t.reg .f16 lo, hi;\n\t"
-      "mov.b32 {lo, hi}, %1;\n\t"
-      "add.rn.f32.f16 %0, lo, %2;\n\t"
-      "add.rn.f32.f16 %0, hi, %0;\n\t}"
-      : "=f"(d)
-      : "r"(u), "f"(c));
-  return d;
-}
-
-// Dot of one group (4 packed words) with one staged activation row.
-__device__ __forceinline__ float group_sum(const uint4 q, const uint4 xv[4]) {
-  __half2 h[4][4];
-  unpack_word(q.x, h[0]);
-  unpack_word(q.y, h[1]);
-  unpack_word(q.z, h[2]);
-  unpack_word(q.w, h[3]);
-  __half2 a0 = u2h(0u), a1 = u2h(0u), a2 = u2h(0u), a3 = u2h(0u);
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    a0 = __hfma2(h[w][0], u2h(xv[w].x), a0);
-    a1 = __hfma2(h[w][1], u2h(xv[w].y), a1);
-    a2 = __hfma2(h[w][2], u2h(xv[w].z), a2);
-    a3 = __hfma2(h[w][3], u2h(xv[w].w), a3);
-  }
-  float gs = add_pair_f32(0.0f, a0);
-  gs = add_pair_f32(gs, a1);
-  gs = add_pair_f32(gs, a2);
-  return add_pair_f32(gs, a3);
 }
 
 // ---------------------------------------------------------------- work walk
@@ -435,69 +308,6 @@ __device__ void issue_tile(const GemvParams& p, const Walk& wk, const uint8_t* q
 }
 
 // ---------------------------------------------------------------- consumers
-// One chunk of a tile: for each of its `ns` groups per lane, the
-// lane loads the group's staged activations (MR rows) once and applies them
-// to its RW rows.  acc[j][m] = sum over the chunk's groups, in group order.
-// TT, CLT > 0 fix the team size and the (always full) chunk length at compile
-// time, so every shared-memory offset is an immediate.  gleft: groups of the
-// row left from this lane's first one (fewer than the chunk only when the
-// team pads K/32; the generic kernel then drops the padding groups).
-template <int MR, int RW, int TT, int CLT>
-__device__ __forceinline__ void tile_dot(const uint8_t* sm, uint32_t xo, uint32_t xso, int xplane,
-                                         int xmrow, int xsmrow, const uint32_t co[RW],
-                                         const uint32_t so[RW], int ns, int T, int gleft,
-                                         float acc[RW][MR]) {
-#pragma unroll
-  for (int j = 0; j < RW; ++j)
-#pragma unroll
-    for (int m = 0; m < MR; ++m) acc[j][m] = 0.0f;
-  const int gstep = (TT > 0 ? TT : T) * 16;          // bytes between a lane's groups
-  const int sstep = gstep >> 3, xsstep = gstep >> 2;  // the same for steps, scales
-  auto group = [&](int s) {
-    uint4 xv[MR][4];
-    float inv[MR];
-#pragma unroll
-    for (int m = 0; m < MR; ++m) {
-#pragma unroll
-      for (int w = 0; w < 4; ++w)
-        xv[m][w] = *reinterpret_cast<const uint4*>(sm + xo + m * xmrow + w * xplane + s * gstep);
-      inv[m] = *reinterpret_cast<const float*>(sm + xso + m * xsmrow + s * xsstep);
-    }
-#pragma unroll
-    for (int j = 0; j < RW; ++j) {
-      const uint4 q = *reinterpret_cast<const uint4*>(sm + co[j] + s * gstep);
-      float stf = bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(sm + so[j] + s * sstep));
-      // padding groups (generic kernel only): their shared bytes belong to
-      // the next row, so the step is dropped (activations there are zero)
-      if (TT == 0 && s * T >= gleft) stf = 0.0f;
-#pragma unroll
-      for (int m = 0; m < MR; ++m) acc[j][m] = fmaf(group_sum(q, xv[m]) * inv[m], stf, acc[j][m]);
-    }
-  };
-  if constexpr (CLT > 0) {
-#pragma unroll
-    for (int s = 0; s < CLT; ++s) group(s);
-  } else {
-#pragma unroll 4
-    for (int s = 0; s < ns; ++s) group(s);
-  }
-}
-
-// Sum over the T lanes of a team with a fixed xor tree (T a power of two;
-// TT > 0: T = TT known at compile time).
-template <int TT>
-__device__ __forceinline__ float team_sum(float v, int T) {
-  if (TT > 0) {
-#pragma unroll
-    for (int off = TT >> 1; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  } else {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-      if (off < T) v += __shfl_xor_sync(0xffffffffu, v, off);
-  }
-  return v;
-}
-
 // Resident CTAs per SM the register budget allows: two (16 warps, 128
 // registers a thread) for up to four accumulated (row, activation row)
 // pairs, one otherwise.
@@ -981,15 +791,8 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
 }
 
 // ================================================================= host side
-namespace {
-
-struct DeviceInfo {
-  int dev = -1;           // device ordinal, -1 when planning without one
-  int sms = 0;
-  int smem_optin = 0;     // largest dynamic shared memory per CTA
-  int smem_per_sm = 0;
-  int smem_reserved = 0;  // shared memory the system keeps per CTA
-};
+// Host helpers shared with the chain launches (declared in gemv_host.h).
+constexpr long long kRowStepMax = 40 << 10;  // largest step of whole rows
 
 DeviceInfo device_info(int dev) {
   static std::mutex mu;
@@ -1016,28 +819,6 @@ DeviceInfo device_info(int dev) {
   }
   return cache[dev];
 }
-
-struct Plan {
-  bool routed = false;   // routed-expert call (ids), never split
-  bool dyn = false;      // dense whole rows: windows handed out at run time
-  int MR = 1;
-  int Kg = 1;
-  int T = 32, nsw = 1, NI = 1, CL = 1, nch = 1;
-  int RW = 1, RB = 8;
-  int S = 1, cps = 1, upi = 1;
-  long long B = 0, U = 0;
-  int x_slots = 1;
-  int nst = 2, per_sm = 1;
-  int tile_bytes = 0, code_pitch = 0, step_pitch = 0, step_off = 0;
-  int ctas = 0;
-  long long smem = 0;
-  size_t ws_bytes = 0;
-  size_t ws_part_off = 0;
-};
-
-constexpr long long kTileMax = 48 << 10;   // largest stage the planner picks
-constexpr long long kTileGood = 24 << 10;  // stages this large amortise a window's overhead
-constexpr long long kRowStepMax = 40 << 10;  // largest step of whole rows
 
 // The per-row arithmetic comes from K alone.  T: the largest power of two
 // <= 32 dividing K/32 that leaves each lane >= 4 groups of a row (else the
@@ -1070,8 +851,6 @@ void row_shape(int K, int* T, int* NI, int* CL, int* nch) {
   *nch = (ni + cl - 1) / cl;
 }
 
-long long x_bytes(int slots, int MR, int Kgp) { return (long long)slots * MR * Kgp * (64 + 4); }
-
 // Stage geometry of a window of `rb` rows: whole rows (contiguous codes, then
 // the steps' 16-byte superset), or `cps` chunks of each row (split-K: one
 // slot per row for codes and for steps).
@@ -1086,6 +865,53 @@ void tile_geometry(int K, int T, int CL, bool whole, int cps, int rb, int* code_
       whole ? (long long)rb * Kg * 2 + 32 + pad * 2 : (long long)rb * *step_pitch;
   *tile_bytes = (int)((*step_off + steps + 127) & ~127LL);
 }
+
+bool current_device(int* dev, DeviceInfo* di) {
+  if (cudaGetDevice(dev) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  *di = device_info(*dev);
+  return di->sms > 0;
+}
+
+void planning_device(DeviceInfo* di) {
+  int dev = 0;
+  if (!current_device(&dev, di)) {
+    di->sms = 152;              // planning without a device: GB300 figures
+    di->smem_optin = 232448;
+    di->smem_per_sm = 233472;
+    di->smem_reserved = 1024;
+  }
+}
+
+namespace {
+
+
+struct Plan {
+  bool routed = false;   // routed-expert call (ids), never split
+  bool dyn = false;      // dense whole rows: windows handed out at run time
+  int MR = 1;
+  int Kg = 1;
+  int T = 32, nsw = 1, NI = 1, CL = 1, nch = 1;
+  int RW = 1, RB = 8;
+  int S = 1, cps = 1, upi = 1;
+  long long B = 0, U = 0;
+  int x_slots = 1;
+  int nst = 2, per_sm = 1;
+  int tile_bytes = 0, code_pitch = 0, step_pitch = 0, step_off = 0;
+  int ctas = 0;
+  long long smem = 0;
+  size_t ws_bytes = 0;
+  size_t ws_part_off = 0;
+};
+
+constexpr long long kTileMax = 48 << 10;   // largest stage the planner picks
+constexpr long long kTileGood = 24 << 10;  // stages this large amortise a window's overhead
+
+
+long long x_bytes(int slots, int MR, int Kgp) { return (long long)slots * MR * Kgp * (64 + 4); }
+
 
 // Chunk sums of a window of whole rows, one buffer per stage (none for one
 // chunk).
@@ -1443,24 +1269,6 @@ GemvParams base_params(const Plan& pl, int N, int K) {
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-bool current_device(int* dev, DeviceInfo* di) {
-  if (cudaGetDevice(dev) != cudaSuccess) {
-    cudaGetLastError();
-    return false;
-  }
-  *di = device_info(*dev);
-  return di->sms > 0;
-}
-
-void planning_device(DeviceInfo* di) {
-  int dev = 0;
-  if (!current_device(&dev, di)) {
-    di->sms = 152;              // planning without a device: GB300 figures
-    di->smem_optin = 232448;
-    di->smem_per_sm = 233472;
-    di->smem_reserved = 1024;
-  }
-}
 
 // Plans are cached per shape: planning is cheap but not free, and decode
 // loops call the same few shapes over and over.

@@ -31,7 +31,11 @@ EXPORTS = ("w4_status_str", "w4_abi_version", "w4_last_cuda_error", "w4a16_gemv"
            "w4_slot_pool_create", "w4_slot_pool_destroy", "w4_slot_pool_remap",
            "w4_slot_pool_stage", "w4_slot_pool_stats", "w4a16_gemv_plan",
            "w4a16_gemv_static_scratch", "w4_dev_pool_state_bytes", "w4_dev_pool_init",
-           "w4_dev_pool_stage", "w4_dev_pool_stats")
+           "w4_dev_pool_stage", "w4_dev_pool_stats", "w4a16_gemv_chain",
+           "w4a16_gemv_chain_workspace_bytes", "w4a16_gemv_chain_plan",
+           "w4a16_gemv_chain_task_plan")
+W4_TASK_SILU_MUL = 1
+CHAIN_MAX_TASKS = 320
 
 
 class W4Error(RuntimeError):
@@ -47,6 +51,25 @@ class PlanInfo(ctypes.Structure):
                                             "smem_bytes", "rows_per_call", "chunk_steps",
                                             "stages", "ctas_per_sm", "tmpl_team",
                                             "tmpl_chunk", "dynamic_windows")]
+
+
+class GemvTask(ctypes.Structure):
+    """struct w4_gemv_task of include/w4a16.h."""
+    _fields_ = [("y", ctypes.c_void_p), ("qw", ctypes.c_void_p), ("st", ctypes.c_void_p),
+                ("x", ctypes.c_void_p), ("ids", ctypes.c_void_p), ("qw_stride", ctypes.c_size_t),
+                ("st_stride", ctypes.c_size_t), ("num_experts", ctypes.c_int),
+                ("n_ids", ctypes.c_int), ("x_rows", ctypes.c_int), ("N", ctypes.c_int),
+                ("K", ctypes.c_int), ("dep", ctypes.c_int), ("flags", ctypes.c_uint)]
+
+
+class ChainPlanInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("ctas", "threads", "instantiation", "stages",
+                                            "stage_bytes", "smem_bytes", "windows")]
+
+
+class ChainTaskInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("rows_per_window", "rows_per_lane", "team",
+                                            "chunk_steps", "chunks", "windows_per_item", "dot")]
 
 
 _lib = None
@@ -108,6 +131,16 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.w4_dev_pool_stats.argtypes = [vp, i32, i32] + [ctypes.POINTER(ctypes.c_longlong)] * 3
     lib.w4a16_gemv_plan.restype = i32
     lib.w4a16_gemv_plan.argtypes = [i32, i32, i32, ctypes.POINTER(PlanInfo)]
+    lib.w4a16_gemv_chain.restype = i32
+    lib.w4a16_gemv_chain.argtypes = [ctypes.POINTER(GemvTask), i32, vp, sz, vp, u32, vp]
+    lib.w4a16_gemv_chain_workspace_bytes.restype = sz
+    lib.w4a16_gemv_chain_workspace_bytes.argtypes = [ctypes.POINTER(GemvTask), i32]
+    lib.w4a16_gemv_chain_plan.restype = i32
+    lib.w4a16_gemv_chain_plan.argtypes = [ctypes.POINTER(GemvTask), i32,
+                                          ctypes.POINTER(ChainPlanInfo)]
+    lib.w4a16_gemv_chain_task_plan.restype = i32
+    lib.w4a16_gemv_chain_task_plan.argtypes = [ctypes.POINTER(GemvTask), i32, i32,
+                                               ctypes.POINTER(ChainTaskInfo)]
     _lib = lib
     return lib
 
@@ -452,3 +485,99 @@ class SlotPool:
         r, h, m = ctypes.c_longlong(), ctypes.c_longlong(), ctypes.c_longlong()
         self._lib.w4_slot_pool_stats(self._h, ctypes.byref(r), ctypes.byref(h), ctypes.byref(m))
         return {"requests": r.value, "hits": h.value, "misses": m.value}
+
+
+# ------------------------------------------------------------------ chains
+def gemv_task(qw: torch.Tensor, st: torch.Tensor, x: torch.Tensor, y: torch.Tensor, dep: int = -1,
+              silu_mul: bool = False) -> dict:
+    """A dense task of a chain: y[N] = W x (x [K], or [2K] = [gate | up] with silu_mul)."""
+    qw = _as_words(qw)
+    for t, dt, name in ((qw, qw.dtype, "qw"), (st, torch.bfloat16, "st"),
+                        (x, torch.bfloat16, "x"), (y, torch.bfloat16, "y")):
+        _need(t, dt, name)
+    N, K = qw.shape[0], qw.shape[-1] * 8
+    if st.shape[0] != N or st.shape[-1] != K // 32 or y.numel() != N:
+        raise ValueError("qw, st and y disagree on N or K")
+    if x.numel() != K * (2 if silu_mul else 1):
+        raise ValueError("x must hold one activation row")
+    return {"y": y, "qw": qw, "st": st, "x": x, "ids": None, "qw_stride": 0, "st_stride": 0,
+            "num_experts": 0, "n_ids": 1, "x_rows": 1, "N": N, "K": K, "dep": dep,
+            "flags": W4_TASK_SILU_MUL if silu_mul else 0}
+
+
+def gemv_id_task(qw_base: torch.Tensor, st_base: torch.Tensor, ids: torch.Tensor,
+                 x: torch.Tensor, y: torch.Tensor, N: int, K: int, num_experts: int,
+                 qw_stride_bytes: int, st_stride_bytes: int, dep: int = -1,
+                 silu_mul: bool = False) -> dict:
+    """A routed task of a chain: y[i] = W_{ids[i]} x_i (x_i: row i when x has
+    n_ids rows, else row 0; [gate | up] rows of 2K with silu_mul)."""
+    _need(ids, torch.int32, "ids")
+    _need(x, torch.bfloat16, "x")
+    _need(y, torch.bfloat16, "y")
+    n_ids = ids.numel()
+    row = K * (2 if silu_mul else 1)
+    if x.numel() % row or x.numel() // row not in (1, n_ids):
+        raise ValueError("x must hold 1 or n_ids activation rows")
+    if y.numel() != n_ids * N:
+        raise ValueError("y must be [n_ids, N]")
+    return {"y": y, "qw": qw_base, "st": st_base, "x": x, "ids": ids,
+            "qw_stride": qw_stride_bytes, "st_stride": st_stride_bytes,
+            "num_experts": num_experts, "n_ids": n_ids, "x_rows": x.numel() // row, "N": N,
+            "K": K, "dep": dep, "flags": W4_TASK_SILU_MUL if silu_mul else 0}
+
+
+def _task_array(tasks):
+    arr = (GemvTask * len(tasks))()
+    for i, t in enumerate(tasks):
+        g = arr[i]
+        for name in ("y", "qw", "st", "x", "ids"):
+            setattr(g, name, None if t[name] is None else t[name].data_ptr())
+        for name in ("qw_stride", "st_stride", "num_experts", "n_ids", "x_rows", "N", "K", "dep",
+                     "flags"):
+            setattr(g, name, int(t[name]))
+    return arr
+
+
+def chain_workspace_bytes(tasks) -> int:
+    """Bytes of the zero-initialised workspace a chain of these tasks needs."""
+    return int(load().w4a16_gemv_chain_workspace_bytes(_task_array(tasks), len(tasks)))
+
+
+def chain_plan(tasks) -> dict:
+    arr = _task_array(tasks)
+    info = ChainPlanInfo()
+    _check(load().w4a16_gemv_chain_plan(arr, len(tasks), ctypes.byref(info)),
+           "w4a16_gemv_chain_plan")
+    return {n: getattr(info, n) for n, _ in ChainPlanInfo._fields_}
+
+
+def chain_task_plan(tasks, task: int) -> dict:
+    arr = _task_array(tasks)
+    info = ChainTaskInfo()
+    _check(load().w4a16_gemv_chain_task_plan(arr, len(tasks), task, ctypes.byref(info)),
+           "w4a16_gemv_chain_task_plan")
+    return {n: getattr(info, n) for n, _ in ChainTaskInfo._fields_}
+
+
+def bind_gemv_chain(tasks, workspace: torch.Tensor, status: torch.Tensor = None):
+    """w4a16_gemv_chain with the task list marshalled once: returns
+    call(pdl=False, stream=None).  `workspace` (uint8, zeroed once) must hold
+    chain_workspace_bytes(tasks) bytes."""
+    _need(workspace, torch.uint8, "workspace")
+    arr = _task_array(tasks)
+    n = len(tasks)
+    fn = load().w4a16_gemv_chain
+    ws_ptr, ws_bytes = _ptr(workspace), workspace.numel()
+
+    def call(pdl: bool = False, stream=None):
+        _check(fn(arr, n, ws_ptr, ws_bytes, _ptr(status), W4_FLAG_PDL if pdl else 0,
+                  _stream(stream)), "w4a16_gemv_chain")
+
+    call.tensors = (tasks, workspace, status)   # keep the buffers alive with the binding
+    return call
+
+
+def gemv_chain(tasks, workspace: torch.Tensor, status: torch.Tensor = None, pdl: bool = False,
+               stream=None):
+    """Run the tasks (dicts from gemv_task / gemv_id_task) as one launch."""
+    bind_gemv_chain(tasks, workspace, status)(pdl=pdl, stream=stream)

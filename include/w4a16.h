@@ -472,6 +472,109 @@ typedef struct w4_plan_info {
 
 w4_status w4a16_gemv_plan(int M, int N, int K, w4_plan_info *info);
 
+/*
+ * w4a16_gemv_chain — a list of W4A16 GEMVs in one launch.
+ *
+ * Page "Gemma 4 on a 4 GB GPU in Plain PyTorch", section "Step 3 — Multiply
+ * Straight From the Packed Weights": a decoded token is the product of an
+ * activation vector with each weight matrix in turn, and its rate is set by
+ * how fast the packed words stream from memory.  This call runs a whole list
+ * of such products ("tasks": the projections of a decode pass, or a routed
+ * layer's gate/up then down product, page "Running a 26B MoE on an 8 GB
+ * Jetson by streaming experts from SSD", section "Streaming without touching
+ * a single GPU kernel") as one persistent launch, one CTA per SM, whose
+ * weight stream does not pause between tasks (the copy warp keeps fetching
+ * later tasks' weights while the products wait for their inputs).
+ *
+ * Task j computes, with the arithmetic of the same call made alone:
+ *   dense  (ids == NULL): y[N] = W x                     (w4a16_gemv, M = 1)
+ *   routed (ids != NULL): y[i][N] = W_{ids[i]} x_i       (w4a16_gemv_id), for
+ *          i < n_ids, expert e at qw + e * qw_stride, st + e * st_stride,
+ *          x_i = row i of x when x_rows == n_ids > 1, else row 0;
+ * with W4_TASK_SILU_MUL each activation row is [gate K | up K] and the
+ * product takes silu(gate) * up (as W4_FLAG_SILU_MUL).  Every task's outputs
+ * are bitwise those of the single call (tested).
+ *
+ * Order and dependencies: `dep` names an earlier task (index < j) whose
+ * outputs task j reads (its x), or -1.  Task j's products start only after
+ * every output of task `dep` is written; weights of later tasks may already
+ * stream meanwhile.  When both tasks are routed on the same ids, task j's
+ * activation rows are `dep`'s output (x == dep's y, x_rows == n_ids, a row
+ * of K, or 2K gated, values == dep's N), expert i of task j waits only for
+ * expert i of `dep` (a routed layer's down product after its gate/up).  A task with dep = -1 must find its x ready when the
+ * launch starts.  For a strict sequence (each projection reading the one
+ * before, as a decoder does) set dep = j - 1.  Outputs of tasks are written
+ * in an unspecified order; a task must not write what another task of the
+ * launch reads, except through `dep`.
+ *
+ * Arguments, layouts and alignment of each task are those of w4a16_gemv /
+ * w4a16_gemv_id (K multiple of 32 up to W4_MAX_K, qw / st / x 16-byte
+ * aligned, y 2-byte aligned, expert strides multiples of 16 and at least one
+ * expert).  n_tasks <= W4_CHAIN_MAX_TASKS (the task list travels in the
+ * launch's parameters, so a CUDA graph that captures the call keeps it).
+ *
+ * workspace: caller-owned device memory of
+ * w4a16_gemv_chain_workspace_bytes(tasks, n_tasks) bytes (16-byte aligned), zeroed
+ * before the first call; each launch re-arms it when it completes.  After a
+ * call that reported a device-side error, zero it again.  Calls that share a
+ * workspace must not overlap on the GPU.
+ *
+ * Errors: host-detectable ones return before any launch (W4_ERR_ARG for a
+ * null pointer, an unknown flag, N < 1 or a `dep` that is not an earlier
+ * task; W4_ERR_SHAPE / W4_ERR_ALIGN as for the single calls, or when the
+ * tasks' activation rows and the smallest stages do not fit shared memory;
+ * W4_ERR_WORKSPACE).  Device-side: an expert id out of range leaves that
+ * item's rows unwritten and records W4_ERR_INDEX; a wait that exceeds about
+ * a second (a dependency that never completes) records W4_ERR_TIMEOUT.
+ * flags: W4_FLAG_PDL.
+ */
+#define W4_CHAIN_MAX_TASKS 320
+#define W4_TASK_SILU_MUL 1u   /* task: x rows are [gate K | up K] -> silu(gate) * up */
+
+typedef struct w4_gemv_task {
+    void *y;                  /* bf16 [N] (dense) or [n_ids][N] (routed) */
+    const void *qw;           /* packed codes: the matrix, or expert 0 of a routed task */
+    const void *st;           /* bf16 steps, likewise */
+    const void *x;            /* bf16 activation row(s) */
+    const int32_t *ids;       /* routed: n_ids expert (or slot) ids on the device; NULL: dense */
+    size_t qw_stride;         /* routed: bytes between experts' codes */
+    size_t st_stride;         /* routed: bytes between experts' steps */
+    int num_experts;          /* routed: valid ids are 0 .. num_experts - 1 */
+    int n_ids;                /* routed: output rows of y; ignored for dense tasks */
+    int x_rows;               /* routed: 1 (shared row) or n_ids */
+    int N, K;
+    int dep;                  /* earlier task whose outputs this one reads, or -1 */
+    unsigned flags;           /* W4_TASK_SILU_MUL */
+} w4_gemv_task;
+
+/* Workspace of a chain: two ints plus one per task (one per id of a routed
+ * task), rounded up to 256 bytes; 0 for an invalid task list. */
+size_t w4a16_gemv_chain_workspace_bytes(const w4_gemv_task *tasks, int n_tasks);
+
+w4_status w4a16_gemv_chain(const w4_gemv_task *tasks, int n_tasks, void *workspace,
+                           size_t workspace_bytes, int32_t *status_dev, unsigned flags,
+                           w4_stream_t stream);
+
+/* Launch shape of a chain (planned for the current device, or for GB300
+ * figures without one): CTAs and threads, the dot instantiation (0: hidden
+ * 5376 / intermediate 21504, 1: 2048 / 8192, 2: routed 2816 / 704,
+ * 3: generic), stages and their size, shared memory, windows in all. */
+typedef struct w4_chain_plan_info {
+    int ctas, threads, instantiation, stages, stage_bytes, smem_bytes, windows;
+} w4_chain_plan_info;
+
+w4_status w4a16_gemv_chain_plan(const w4_gemv_task *tasks, int n_tasks, w4_chain_plan_info *info);
+
+/* Window shape of one task of a chain: rows per window, rows per lane, lane
+ * team, groups per lane per chunk, chunks per row, windows per item, and
+ * which of the instantiation's two dot loops (0, 1) runs it. */
+typedef struct w4_chain_task_info {
+    int rows_per_window, rows_per_lane, team, chunk_steps, chunks, windows_per_item, dot;
+} w4_chain_task_info;
+
+w4_status w4a16_gemv_chain_task_plan(const w4_gemv_task *tasks, int n_tasks, int task,
+                                     w4_chain_task_info *info);
+
 #ifdef __cplusplus
 }
 #endif
