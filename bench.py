@@ -1066,6 +1066,44 @@ def run_shape(args):
     return 0
 
 
+def run_shape_id(args):
+    """One routed call (w4a16_gemv_id), timed alone: n_ids distinct experts of
+    an N x K expert tensor, one activation row (broadcast) or one per id,
+    rotating expert tensors larger than L2, graph replay, CUDA events."""
+    from bit_weight_only_gemv_gb300 import lib
+    lib.load()
+    parts = [int(v) for v in args.shape_id.split(",")]
+    N, K, n_ids = parts[:3]
+    x_rows = parts[3] if len(parts) > 3 else 1
+    dev = torch.device("cuda", 0)
+    per = metrics.gemv_id_bytes(n_ids, x_rows, N, K)
+    copies = max(2, -(-600_000_000 // per))
+    E = n_ids
+    qws = [synth.torch_words((E, N * K // 8), synth.seed_of(17, i), dev) for i in range(copies)]
+    sts = [synth.torch_steps((E, N * K // 32), synth.seed_of(18, i), dev) for i in range(copies)]
+    ids = torch.randperm(E, generator=torch.Generator().manual_seed(0)).to(torch.int32).to(dev)
+    x = synth.torch_x((x_rows, K), synth.seed_of(19), dev)
+    y = torch.empty((n_ids, N), dtype=torch.bfloat16, device=dev)
+    fns = [lib.bind_gemv_id(q, s_, ids, x, N, K, E, N * K // 2, N * K // 16, y, None)
+           for q, s_ in zip(qws, sts)]
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for i, f in enumerate(fns):
+            f(pdl=i > 0, stream=stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i, f in enumerate(fns):
+            f(pdl=i > 0, stream=stream)
+    for _ in range(args.warmup):
+        g.replay()
+    ms = time_replays(g, stream, args.steps) / copies
+    print(json.dumps({"mode": "shape_id", "N": N, "K": K, "n_ids": n_ids, "x_rows": x_rows,
+                      "us_per_launch": ms * 1e3, "gbps": metrics.gbps(per, ms * 1e-3),
+                      "bytes_per_launch": per, "copies": copies}), flush=True)
+    return 0
+
+
 def build_parser() -> argparse.ArgumentParser:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -1076,6 +1114,9 @@ def build_parser() -> argparse.ArgumentParser:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--shape", default=None,
                     help="M,N,K: time one GEMV shape alone instead of the decode pass")
+    ap.add_argument("--shape-id", default=None,
+                    help="N,K,n_ids[,x_rows]: time one routed call (w4a16_gemv_id) over n_ids "
+                         "experts of N x K alone")
     ap.add_argument("--no-pdl", action="store_true", help="with --shape: plain launches")
     ap.add_argument("--path", choices=("auto", "cuda", "tensor"), default="auto",
                     help="with --shape: the library's choice, CUDA cores or tensor cores")
@@ -1127,6 +1168,8 @@ def main():
             return run_reference(args, world, rank)
         if args.shape:
             return run_shape(args)
+        if args.shape_id:
+            return run_shape_id(args)
         if args.workload.startswith("moe"):
             return run_moe(args, world, rank, local)
         return run_gb300(args, world, rank, local)

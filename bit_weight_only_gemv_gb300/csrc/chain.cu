@@ -201,9 +201,33 @@ __device__ void stage_row(const Task& tk, int item, uint8_t* xs, float* xsc) {
   const int K = tk.K, Kg = K / 32, Kgp = (int)tk.NI * tk.T;
   const int row = (tk.flags & kTaskXPerItem) ? item : 0;
   const bool gated = (tk.flags & kTaskGated) != 0;
+  if (!gated) {
+    // all of a thread's loads (two groups at most up to K = 28672) before
+    // any conversion: one trip to L2
+    for (int base = threadIdx.x; base < Kgp; base += 2 * kCons) {
+      uint4 v[2][4];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int g = base + u * kCons;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[u][i] = make_uint4(0u, 0u, 0u, 0u);
+        if (g < Kg) {
+          const uint4* src = reinterpret_cast<const uint4*>(tk.x + (long long)row * K + g * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) v[u][i] = __ldcg(src + i);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int g = base + u * kCons;
+        if (g < Kgp) store_staged_group(v[u], xs + g * 16, Kgp * 16, xsc + g, g < Kg);
+      }
+    }
+    return;
+  }
   for (int g = threadIdx.x; g < Kgp; g += kCons) {
     const bool valid = g < Kg;
-    if (gated) {
+    {   // gated: silu(gate) * up, one group at a time
       float h[32];
       float mx = 0.0f;
       if (valid) {
@@ -221,14 +245,6 @@ __device__ void stage_row(const Task& tk, int item, uint8_t* xs, float* xsc) {
         for (int i = 0; i < 32; ++i) h[i] = 0.0f;
       }
       store_staged_group_f32(h, mx, xs + g * 16, Kgp * 16, xsc + g, valid);
-    } else {
-      uint4 v[4] = {};
-      if (valid) {
-        const uint4* src = reinterpret_cast<const uint4*>(tk.x + (long long)row * K + g * 32);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = __ldcg(src + i);
-      }
-      store_staged_group(v, xs + g * 16, Kgp * 16, xsc + g, valid);
     }
   }
 }
