@@ -74,6 +74,7 @@ constexpr int kMaxMR = 4;                   // activation rows per launch
 constexpr int kMaxStages = 8;
 constexpr int kBarBytes = 256;              // full[8], empty[8], flags, windows[8]
 constexpr int kWinOff = 160;                // (row0, rows) of each stage's window (dense calls)
+constexpr int kItemOff = 224;               // item of each stage's window (routed run-time windows)
 constexpr long long kWaitCycles = 1LL << 31;
 
 struct GemvParams {
@@ -437,7 +438,64 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
         }
       }
     }
-    while (!DS && wk.next(p)) {
+    if (!DS && p.dyn) {
+      // Routed calls of whole rows: windows of RB rows within one item,
+      // numbered item-major, window blockIdx.x first, then whichever the
+      // launch's counter hands out next.  Each stage carries its window's
+      // (row0, rows, item); rows 0 ends the work, negative rows mark an
+      // item whose id is out of range (nothing copied, rows left unwritten).
+      const int wpi = (p.N + p.RB - 1) / p.RB;
+      const long long nwin = (long long)p.n_items * wpi;
+      long long w = blockIdx.x;
+      int grabbed = 0;
+      bool pending = false;
+      volatile int* witem = reinterpret_cast<volatile int*>(smem + kItemOff);
+      while (true) {
+        if (issued >= nst && !wait_phase(empty0 + 8 * slot, phase ^ 1u, abort_flag)) {
+          if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        if (pending) w = (long long)__shfl_sync(0xffffffffu, grabbed, 0) + gridDim.x;
+        if (w >= nwin) {
+          if (lane == 0) {
+            win[2 * slot + 1] = 0;
+            mbar_arrive(full0 + 8 * slot);
+          }
+          ended = true;
+          break;
+        }
+        if (lane == 0) grabbed = atomicAdd(p.work, 1);
+        pending = true;
+        Walk cur = wk;
+        cur.item = (int)(w / wpi);
+        cur.row0 = (int)(w - (long long)cur.item * wpi) * p.RB;
+        cur.nrows = min(p.RB, p.N - cur.row0);
+        cur.c0 = 0;
+        cur.c1 = p.nch;
+        cur.rb = 0;
+        const uint8_t *qwi, *sti;
+        const bool ok = item_arrays(p, cur.item, &qwi, &sti);
+        if (lane == 0) {
+          win[2 * slot] = cur.row0;
+          win[2 * slot + 1] = ok ? cur.nrows : -cur.nrows;
+          witem[slot] = cur.item;
+        }
+        const uint32_t st_off = kBarBytes + slot * p.tile_bytes;
+        if (ok) {
+          issue_tile(p, cur, qwi, sti, sbase + st_off, smem + st_off, full0 + 8 * slot, lane, pol);
+        } else {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full0 + 8 * slot);
+        }
+        ++issued;
+        if (++slot == nst) {
+          slot = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    while (!DS && !p.dyn && wk.next(p)) {
       const uint8_t *qwi, *sti;
       if (!item_arrays(p, wk.item, &qwi, &sti)) continue;
       // reuse of a slot waits for the consumers to release its last tile
@@ -469,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
     }
     // dyn: the last CTA to finish re-arms the launch's counters (every CTA
     // has taken its last window before it counts itself done)
-    if (DS && p.dyn && lane == 0) {
+    if (p.dyn && lane == 0) {
       __threadfence();
       if (atomicAdd(p.work + 1, 1) == (int)gridDim.x - 1) {
         __threadfence();
@@ -488,7 +546,9 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
 
   // items whose activation rows this CTA needs
   int item0 = 0, nslots = 1;
-  if (p.x_per_item) {
+  if (p.x_per_item && p.dyn) {
+    nslots = p.n_items;   // run-time windows may come from any item
+  } else if (p.x_per_item) {
     Walk r;
     r.init(p);
     if (p.S == 1) {
@@ -611,13 +671,45 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
     return;
   } else {
     bool reported = false;
-    while (wk.next(p)) {
+    volatile int* witem = reinterpret_cast<volatile int*>(smem + kItemOff);
+    while (true) {
       const uint8_t *qwi, *sti;
+      bool bad = false;
+      if (p.dyn) {
+        // routed run-time windows: the stage says which (rows 0: no more)
+        if (!wait_phase(full0 + 8 * slot, phase, abort_flag)) {
+          if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
+          *abort_flag = 1;
+          return;
+        }
+        const int nr = win[2 * slot + 1];
+        if (nr == 0) break;
+        wk.item = witem[slot];
+        wk.row0 = win[2 * slot];
+        wk.nrows = nr < 0 ? -nr : nr;
+        wk.c0 = 0;
+        wk.c1 = p.nch;
+        wk.rb = 0;
+        bad = nr < 0;
+      } else if (!wk.next(p)) {
+        break;
+      }
       int rid = 0;   // real expert id (RID), loaded together with the routed id
       if constexpr (RID) rid = __ldg(p.eids + wk.item);
-      if (!dense && !item_arrays(p, wk.item, &qwi, &sti)) {
+      if (bad || (!p.dyn && !dense && !item_arrays(p, wk.item, &qwi, &sti))) {
         if (!reported && lane == 0) report(p.status, W4_ERR_INDEX);
         reported = true;
+        if (bad) {   // its stage carried nothing: hand it back
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+          if (++slot == nst) {
+            slot = 0;
+            phase ^= 1u;
+            tile = kBarBytes;
+          } else {
+            tile += p.tile_bytes;
+          }
+        }
         continue;
       }
       // Real expert ids: a real id out of range (W4_ERR_INDEX) or a slot that
@@ -651,7 +743,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
       const uint32_t xo0 = xs_off + (uint32_t)(xslot * MR * 4 * p.Kgp * 16);
       const uint32_t xso0 = xsc_off + (uint32_t)(xslot * MR * p.Kgp * 4);
 
-      if (!wait_phase(full0 + 8 * slot, phase, abort_flag)) {
+      if (!p.dyn && !wait_phase(full0 + 8 * slot, phase, abort_flag)) {
         if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
         *abort_flag = 1;
         return;
@@ -908,6 +1000,7 @@ struct Plan {
 
 constexpr long long kTileMax = 48 << 10;   // largest stage the planner picks
 constexpr long long kTileGood = 24 << 10;  // stages this large amortise a window's overhead
+constexpr long long kRoutedXMax = 64 << 10;  // staged activation rows of a routed call
 
 
 long long x_bytes(int slots, int MR, int Kgp) { return (long long)slots * MR * Kgp * (64 + 4); }
@@ -994,9 +1087,16 @@ bool make_plan(int MR, int N, int K, int n_items, int allow_split, int x_per_ite
     pl.U = rows_total;
     pl.ctas = (int)std::max<long long>(1, g1);
   }
-  // activation rows a CTA stages: one, or the items its range touches
+  // activation rows a CTA stages: one, or the items its range touches; a
+  // routed call whose windows are handed out at run time stages every
+  // item's row (when they fit kRoutedXMax)
   pl.x_slots = 1;
-  if (x_per_item) {
+  const bool routed_dyn_ok =
+      routed && pl.S == 1 &&
+      (!x_per_item || x_bytes(n_items, MR, pl.NI * pl.T) <= kRoutedXMax);
+  if (x_per_item && routed_dyn_ok) {
+    pl.x_slots = n_items;
+  } else if (x_per_item) {
     for (int c = 0; c < pl.ctas; ++c) {
       const long long ub = (long long)c * pl.U / pl.ctas, ue = (long long)(c + 1) * pl.U / pl.ctas;
       if (ue <= ub) continue;
@@ -1070,6 +1170,10 @@ bool make_plan(int MR, int N, int K, int n_items, int allow_split, int x_per_ite
   // counter at run time: SMs stream at different speeds, and a fixed share of
   // rows per CTA would make the launch wait for the slowest.
   if (!routed && pl.S == 1) pl.dyn = (pl.U + pl.RB - 1) / pl.RB >= 4LL * pl.ctas;
+  // Routed calls take windows of RB rows within one item; at run time too
+  // once there are enough of them.
+  if (routed_dyn_ok)
+    pl.dyn = (long long)n_items * ((N + pl.RB - 1) / pl.RB) >= 2LL * pl.ctas;
   if (pl.S > 1) {
     // counters first, partials after them
     const size_t part = (size_t)pl.B * pl.nch * pl.RB * MR * sizeof(float);
