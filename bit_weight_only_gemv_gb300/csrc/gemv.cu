@@ -338,13 +338,17 @@ __device__ __forceinline__ void finish_window(const GemvParams& p, const float* 
 // the launch; the other calls take the general walk (kWalkGeneral), which
 // kWalkRealIds extends with the real-id checks and per-expert output vectors
 // of w4a16_gemv_id_scaled, and kWalkGated with the gated activation staging
-// (W4_FLAG_SILU_MUL).
-constexpr int kWalkGeneral = 0, kWalkDense = 1, kWalkRealIds = 2, kWalkGated = 3;
+// (W4_FLAG_SILU_MUL).  kWalkRouted is the dense walk for routed calls whose
+// windows (within one item) are handed out at run time: each stage also
+// names its item, whose output rows (and activation row) the window uses.
+constexpr int kWalkGeneral = 0, kWalkDense = 1, kWalkRealIds = 2, kWalkGated = 3,
+              kWalkRouted = 4;
 
 template <int MR, int RW, int TT, int CLT, int WALK>
 __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
     gemv_kernel(const __grid_constant__ GemvParams p) {
-  constexpr bool DS = WALK == kWalkDense;
+  constexpr bool DS = WALK == kWalkDense || WALK == kWalkRouted;
+  constexpr bool RDS = WALK == kWalkRouted;
   constexpr bool RID = MR == 1 && WALK == kWalkRealIds;
   constexpr bool GATED = WALK == kWalkGated;   // general walk, gated activations
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -381,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
     int slot = 0;
     uint32_t phase = 0;   // use count of the slot, mod 2
     bool ended = false;   // the end of the windows went out in stage `slot`
-    if constexpr (DS) {
+    if constexpr (WALK == kWalkDense) {
       // Windows of RB rows: the CTA's range in order, or (dyn) window
       // blockIdx.x first, then whichever the launch's counter hands out next.
       // Each stage carries its window's (row0, rows) to the consumers; rows 0
@@ -438,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
         }
       }
     }
-    if (!DS && p.dyn) {
+    if (WALK != kWalkDense && p.dyn) {
       // Routed calls of whole rows: windows of RB rows within one item,
       // numbered item-major, window blockIdx.x first, then whichever the
       // launch's counter hands out next.  Each stage carries its window's
@@ -605,6 +609,10 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
     const int items = ncw * nrs_full;
     const int ci_first = warp / nrs_full, rs_first = warp - ci_first * nrs_full;
     const int dci = kConsumerWarps / nrs_full, drs = kConsumerWarps - dci * nrs_full;
+    // routed calls (run-time windows within one item): the item's output
+    // rows and, with one activation row per item, its staged row
+    volatile int* witem = reinterpret_cast<volatile int*>(smem + kItemOff);
+    bool reported = false;
     while (true) {
       if (!wait_phase(full0 + 8 * slot, phase, abort_flag)) {
         if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
@@ -614,6 +622,25 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
       const int row0 = win[2 * slot];
       const int nrows = win[2 * slot + 1];
       if (nrows == 0) break;
+      const int item = RDS ? witem[slot] : 0;
+      if (RDS && nrows < 0) {   // an id out of range: rows left unwritten, stage handed back
+        if (!reported && lane == 0) report(p.status, W4_ERR_INDEX);
+        reported = true;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+        if (++slot == nst) {
+          slot = 0;
+          phase ^= 1u;
+          tile = kBarBytes;
+        } else {
+          tile += p.tile_bytes;
+        }
+        continue;
+      }
+      __nv_bfloat16* yrow = p.y + (long long)item * MR * p.N + row0;
+      const int xslot = RDS && p.x_per_item ? item : 0;
+      const uint32_t xo0 = xs_off + (uint32_t)(xslot * MR * 4 * p.Kgp * 16);
+      const uint32_t xso0 = xsc_off + (uint32_t)(xslot * MR * p.Kgp * 4);
       const uint32_t soff0 = steps_aligned ? 0u : (uint32_t)(((row0 & 7) * (kg2 & 15)) & 15);
       float* redw = red + slot * red_slot;
       int ci = ci_first, rs = rs_first;
@@ -629,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
         const int g0 = ci * gpc + t;
         const int ns = CLT > 0 ? CLT : min(p.CL, p.NI - ci * p.CL);
         float acc[RW][MR];
-        tile_dot<MR, RW, TT, CLT>(smem, xs_off + (uint32_t)(g0 * 16), xsc_off + (uint32_t)(g0 * 4),
+        tile_dot<MR, RW, TT, CLT>(smem, xo0 + (uint32_t)(g0 * 16), xso0 + (uint32_t)(g0 * 4),
                                   xplane, xmrow, xsmrow, co, so, ns, T, kg_valid - g0, acc);
 #pragma unroll
         for (int j = 0; j < RW; ++j)
@@ -643,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
             if (ncw == 1) {   // one chunk: the row is done (0 + chunk sum)
 #pragma unroll
               for (int m = 0; m < MR; ++m)
-                p.y[(long long)m * p.N + row0 + rl] = __float2bfloat16_rn(0.0f + acc[j][m]);
+                yrow[(long long)m * p.N + rl] = __float2bfloat16_rn(0.0f + acc[j][m]);
             } else {
 #pragma unroll
               for (int m = 0; m < MR; ++m) redw[(rl * p.nch + ci) * MR + m] = acc[j][m];
@@ -666,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
       } else {
         tile += p.tile_bytes;
       }
-      if (ncw > 1) finish_window<MR>(p, redw, nrows, ncw, p.y + row0, OutVec{nullptr, nullptr});
+      if (ncw > 1) finish_window<MR>(p, redw, nrows, ncw, yrow, OutVec{nullptr, nullptr});
     }
     return;
   } else {
@@ -1209,7 +1236,10 @@ KernelFn kernel_for(const Plan& pl, bool real_ids = false, int* tt = nullptr, in
       default: return nullptr;
     }
   }
+  // the dense walk: dense calls of whole rows, and (its routed form) routed
+  // calls whose windows within one item are handed out at run time
   const bool ds = !pl.routed && pl.S == 1;
+  const bool rds = pl.routed && pl.dyn && pl.S == 1;
   const bool full = pl.NI % pl.CL == 0 && pl.NI * pl.T == pl.Kg;
   const int key = pl.T * 16 + pl.CL;
   if (real_ids) {
@@ -1231,11 +1261,15 @@ KernelFn kernel_for(const Plan& pl, bool real_ids = false, int* tt = nullptr, in
       default: return nullptr;
     }
   }
-  if (pl.MR == 1 && full && (pl.RW <= 2 || (ds && pl.RW == 4))) {
+  if (pl.MR == 1 && full && (pl.RW <= 2 || ((ds || rds) && pl.RW == 4))) {
 #define W4_SPEC(t, cl)                                                                  \
   if (key == (t) * 16 + (cl)) {                                                         \
     if (tt != nullptr) *tt = t;                                                         \
     if (clt != nullptr) *clt = cl;                                                      \
+    if (rds)                                                                            \
+      return pl.RW == 1 ? gemv_kernel<1, 1, t, cl, kWalkRouted>                         \
+             : pl.RW == 2 ? gemv_kernel<1, 2, t, cl, kWalkRouted>                       \
+                          : gemv_kernel<1, 4, t, cl, kWalkRouted>;                      \
     if (ds && pl.RW == 4) return gemv_kernel<1, 4, t, cl, kWalkDense>;                  \
     if (ds)                                                                             \
       return pl.RW == 1 ? gemv_kernel<1, 1, t, cl, kWalkDense>                          \
@@ -1253,6 +1287,14 @@ KernelFn kernel_for(const Plan& pl, bool real_ids = false, int* tt = nullptr, in
   }
 #define W4_GEN(mr, rw) \
   (ds ? gemv_kernel<mr, rw, 0, 0, kWalkDense> : gemv_kernel<mr, rw, 0, 0, kWalkGeneral>)
+  if (rds) {
+    switch (pl.RW) {
+      case 1: return gemv_kernel<1, 1, 0, 0, kWalkRouted>;
+      case 2: return gemv_kernel<1, 2, 0, 0, kWalkRouted>;
+      case 4: return gemv_kernel<1, 4, 0, 0, kWalkRouted>;
+      default: return nullptr;
+    }
+  }
   switch (pl.MR * 8 + pl.RW) {
     case 8 + 1: return W4_GEN(1, 1);
     case 8 + 2: return W4_GEN(1, 2);
@@ -1562,6 +1604,34 @@ extern "C" w4_status w4a16_gemv_plan(int M, int N, int K, w4_plan_info* info) {
   info->ctas_per_sm = pl.per_sm;
   info->dynamic_windows = pl.dyn ? 1 : 0;
   // compile-time team size / chunk length of the instantiation (0: generic)
+  kernel_for(pl, false, &info->tmpl_team, &info->tmpl_chunk);
+  return W4_OK;
+}
+
+extern "C" w4_status w4a16_gemv_id_plan(int n_ids, int x_rows, int N, int K, w4_plan_info* info) {
+  if (info == nullptr || n_ids < 1 || N < 1) return W4_ERR_ARG;
+  if (K < 32 || K % 32 != 0 || K > W4_MAX_K) return W4_ERR_SHAPE;
+  if (x_rows != 1 && x_rows != n_ids) return W4_ERR_SHAPE;
+  DeviceInfo di;
+  planning_device(&di);
+  const int xpi = (x_rows == n_ids && n_ids > 1) ? 1 : 0;
+  Plan pl;
+  if (!cached_plan(1, N, K, n_ids, 0, xpi, true, di, &pl)) return W4_ERR_SHAPE;
+  *info = w4_plan_info{};
+  info->path = 1;
+  info->ctas = pl.ctas;
+  info->slices = pl.S;
+  info->threads = kThreads;
+  info->team = pl.T;
+  info->unit_rows = pl.RB;
+  info->chunk_groups = pl.CL * pl.T;
+  info->rows_per_lane = pl.RW;
+  info->smem_bytes = (int)pl.smem;
+  info->rows_per_call = 1;
+  info->chunk_steps = pl.CL;
+  info->stages = pl.nst;
+  info->ctas_per_sm = pl.per_sm;
+  info->dynamic_windows = pl.dyn ? 1 : 0;
   kernel_for(pl, false, &info->tmpl_team, &info->tmpl_chunk);
   return W4_OK;
 }

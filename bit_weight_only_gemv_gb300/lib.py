@@ -33,7 +33,7 @@ EXPORTS = ("w4_status_str", "w4_abi_version", "w4_last_cuda_error", "w4a16_gemv"
            "w4a16_gemv_static_scratch", "w4_dev_pool_state_bytes", "w4_dev_pool_init",
            "w4_dev_pool_stage", "w4_dev_pool_stats", "w4a16_gemv_chain",
            "w4a16_gemv_chain_workspace_bytes", "w4a16_gemv_chain_plan",
-           "w4a16_gemv_chain_task_plan")
+           "w4a16_gemv_chain_task_plan", "w4a16_gemv_id_plan")
 W4_TASK_SILU_MUL = 1
 CHAIN_MAX_TASKS = 320
 
@@ -131,6 +131,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.w4_dev_pool_stats.argtypes = [vp, i32, i32] + [ctypes.POINTER(ctypes.c_longlong)] * 3
     lib.w4a16_gemv_plan.restype = i32
     lib.w4a16_gemv_plan.argtypes = [i32, i32, i32, ctypes.POINTER(PlanInfo)]
+    lib.w4a16_gemv_id_plan.restype = i32
+    lib.w4a16_gemv_id_plan.argtypes = [i32, i32, i32, i32, ctypes.POINTER(PlanInfo)]
     lib.w4a16_gemv_chain.restype = i32
     lib.w4a16_gemv_chain.argtypes = [ctypes.POINTER(GemvTask), i32, vp, sz, vp, u32, vp]
     lib.w4a16_gemv_chain_workspace_bytes.restype = sz
@@ -188,6 +190,14 @@ def workspace_bytes(M: int, N: int, K: int, path: str = None) -> int:
 def plan(M: int, N: int, K: int) -> dict:
     info = PlanInfo()
     _check(load().w4a16_gemv_plan(M, N, K, ctypes.byref(info)), "w4a16_gemv_plan")
+    return {n: getattr(info, n) for n, _ in PlanInfo._fields_}
+
+
+def id_plan(n_ids: int, x_rows: int, N: int, K: int) -> dict:
+    """Launch plan of a w4a16_gemv_id call."""
+    info = PlanInfo()
+    _check(load().w4a16_gemv_id_plan(n_ids, x_rows, N, K, ctypes.byref(info)),
+           "w4a16_gemv_id_plan")
     return {n: getattr(info, n) for n, _ in PlanInfo._fields_}
 
 
@@ -555,7 +565,7 @@ def chain_task_plan(tasks, task: int) -> dict:
     arr = _task_array(tasks)
     info = ChainTaskInfo()
     _check(load().w4a16_gemv_chain_task_plan(arr, len(tasks), task, ctypes.byref(info)),
-           "w4a16_gemv_chain_task_plan")
+           "w4a16_gemv_chain_task_plan", "w4a16_gemv_id_plan")
     return {n: getattr(info, n) for n, _ in ChainTaskInfo._fields_}
 
 

@@ -467,10 +467,15 @@ typedef struct w4_plan_info {
     int tmpl_team;      /* team size compiled into the kernel (0: generic) */
     int tmpl_chunk;     /* chunk steps compiled into the kernel (0: generic) */
     int dynamic_windows; /* 1: CTAs take windows of unit_rows rows from a counter at
-                            run time (dense calls with many windows per CTA) */
+                            run time (dense calls with many windows per CTA, and
+                            routed calls with many windows, within one id each) */
 } w4_plan_info;
 
 w4_status w4a16_gemv_plan(int M, int N, int K, w4_plan_info *info);
+
+/* The same for a w4a16_gemv_id call with n_ids ids and x_rows activation
+ * rows (path is always 1). */
+w4_status w4a16_gemv_id_plan(int n_ids, int x_rows, int N, int K, w4_plan_info *info);
 
 /*
  * w4a16_gemv_chain — a list of W4A16 GEMVs in one launch.

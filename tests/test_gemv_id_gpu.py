@@ -106,6 +106,74 @@ def test_gemv_id_ragged_k_matches_oracle(cuda_lib, e, n, k, n_ids, x_rows, pad):
         assert np.array_equal(host_bits(yd)[0], yb[i])
 
 
+# calls with enough windows take them at run time, within one id each, on
+# the dense walk's loop (compiled team shapes with 4, 2 and 1 rows per lane,
+# and the generic loop); shared and per-id activation rows
+RUN_TIME = [(10, 5376, 5376, 8, 1), (8, 4096, 2048, 6, 6), (34, 2816, 704, 32, 32),
+            (10, 9000, 1184, 8, 1), (12, 3000, 1184, 10, 10), (14, 4000, 2816, 12, 1),
+            (9, 3000, 3232, 8, 1)]
+
+
+@pytest.mark.parametrize("e,n,k,n_ids,x_rows", RUN_TIME)
+def test_gemv_id_run_time_windows(cuda_lib, e, n, k, n_ids, x_rows):
+    plan = lib.id_plan(n_ids, x_rows, n, k)
+    assert plan["dynamic_windows"] == 1
+    rng = np.random.default_rng(e * 3 + n + k)
+    qw = synth.torch_words((e, n * k // 8), synth.seed_of(71, n, k), "cuda")
+    st = synth.torch_steps((e, n * k // 32), synth.seed_of(72, n, k), "cuda")
+    ids_h = rng.integers(0, e, size=n_ids).astype(np.int32)
+    ids_h[-1] = ids_h[0]                                   # a repeated id
+    x_h = synth.np_x(rng, (x_rows, k))
+    y = poison_bf16((n_ids, n))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lib.gemv_id(qw, st, torch.from_numpy(ids_h).to("cuda"), dev_bf16(x_h), n, k, e, n * k // 2,
+                n * k // 16, y=y, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    yb = host_bits(y)
+    assert not np.any(yb == POISON)
+    # sampled rows of every id (the item's last rows: a short window) against
+    # the oracle, and every row bitwise the dense GEMV of its expert
+    rows = np.unique(np.concatenate([rng.choice(n, 40, replace=False), np.arange(n - 5, n)]))
+    for i, d in enumerate(ids_h):
+        xi = x_h[0 if x_rows == 1 else i][None]
+        qe = qw[int(d)].view(n, k // 8)
+        se = st[int(d)].view(n, k // 32)
+        need = lib.workspace_bytes(1, n, k)
+        yd = lib.gemv(qe, se, dev_bf16(xi), workspace=torch.zeros(
+            max(16, need), dtype=torch.uint8, device="cuda") if need else None)
+        torch.cuda.synchronize()
+        assert np.array_equal(host_bits(yd)[0], yb[i])
+        idx = torch.from_numpy(rows).to("cuda")
+        q_h = qe[idx].cpu().numpy().view(np.uint32)
+        s_h = se[idx].view(torch.int16).cpu().numpy().view(np.uint16)
+        assert oracle.within_bound(yb[i][rows][None], oracle.gemv_ref(q_h, s_h, xi),
+                                   oracle.gemv_abs_ref(q_h, s_h, xi))
+
+
+def test_gemv_id_run_time_windows_bad_ids(cuda_lib):
+    e, n, k = 6, 4096, 2048
+    assert lib.id_plan(6, 1, n, k)["dynamic_windows"] == 1
+    qw = synth.torch_words((e, n * k // 8), synth.seed_of(73), "cuda")
+    st = synth.torch_steps((e, n * k // 32), synth.seed_of(74), "cuda")
+    ids_h = np.array([1, 6, 3, -2, 5, 1], np.int32)
+    x = dev_bf16(synth.np_x(np.random.default_rng(3), (1, k)))
+    y = poison_bf16((6, n))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lib.gemv_id(qw, st, torch.from_numpy(ids_h).to("cuda"), x, n, k, e, n * k // 2, n * k // 16,
+                y=y, status=status)
+    torch.cuda.synchronize()
+    assert lib.STATUS[int(status.item())] == "W4_ERR_INDEX"
+    yb = host_bits(y)
+    for i, d in enumerate(ids_h):
+        if 0 <= d < e:
+            ref = lib.gemv(qw[int(d)].view(n, k // 8), st[int(d)].view(n, k // 32), x)
+            torch.cuda.synchronize()
+            assert np.array_equal(yb[i], host_bits(ref)[0])
+        else:
+            assert np.all(yb[i] == POISON)
+
+
 def test_gemv_id_bad_ids_leave_rows_unwritten(cuda_lib):
     rng = np.random.default_rng(11)
     e, n, k = 4, 64, 2048
