@@ -43,7 +43,10 @@
 namespace w4 {
 namespace chain {
 
-constexpr int kWarps = 14;                  // consumer warps
+constexpr int kGroups = 2;                  // consumer groups, alternate windows each
+constexpr int kGroupWarps = 7;
+constexpr int kGroupThreads = 32 * kGroupWarps;
+constexpr int kWarps = kGroups * kGroupWarps;   // consumer warps
 constexpr int kCons = 32 * kWarps;
 constexpr int kCopyWarp = kWarps;          // warp 14
 constexpr int kSignalWarp = kWarps + 1;     // warp 15
@@ -51,6 +54,9 @@ constexpr int kThreads = kCons + 64;        // + the copy warp and the signal wa
 constexpr int kMaxStages = 8;
 constexpr int kHdrBytes = 1024;             // barriers, flags, window records
 constexpr int kEndOff = 132;                // windows of this CTA, once known (else -1)
+constexpr int kXsOff = 136;                 // (task, item) whose activation row is staged
+constexpr int kGdoneOff = 144;              // last window each group finished [2]
+constexpr int kGflagOff = 152;              // a group's decision to restage [2]
 constexpr int kInfoOff = 256;               // (task, item, row0, rows) per stage
 constexpr int kSeqOff = 384;                // warps done with each of the last 16 windows
 constexpr int kPendOff = 512;               // finished windows for the signal warp [32]
@@ -106,10 +112,6 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
   }
 }
 
-__device__ __forceinline__ void cons_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kCons) : "memory");
-}
-
 __device__ __forceinline__ int load_acquire_gpu(const int* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -129,6 +131,16 @@ __device__ __forceinline__ int atom_add_acq_rel_cta(int* p, int v) {
   return old;
 }
 
+__device__ __forceinline__ void st_release_cta_s32(int* p, int v) {
+  asm volatile("st.release.cta.shared::cta.s32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_cta_s32(const int* p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared::cta.s32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void st_release_cta_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.release.cta.shared::cta.u64 [%0], %1;" ::"r"(smem_addr(p)), "l"(v) : "memory");
 }
@@ -139,21 +151,25 @@ __device__ __forceinline__ unsigned long long ld_acquire_cta_u64(const unsigned 
   return v;
 }
 
-// Consumer warp, after its stores of the CTA's window number `seq`: the last
-// of the 14 warps to get here hands the window (its done-counter `ctr`) to
-// the signal warp through pend[seq % 32] = (seq + 1) << 32 | ctr.  The
-// per-window warp count is reset by that warp; it is used again 16 windows
-// later, which no warp can reach before every warp has passed this point
-// (the ring holds at most 8 windows).  A pend entry is reused 32 windows
+// Consumer warp of group g, after its stores of the CTA's window number
+// `seq`: the last of the group's 7 warps to get here records that the group
+// is done with the window (gdone[g] = seq: its staged activation row is no
+// longer read for it) and hands the window (its done-counter `ctr`) to the
+// signal warp through pend[seq % 32] = (seq + 1) << 32 | ctr.  The per-window
+// warp count is reset by that warp; it is used again 16 windows later, which
+// no warp can reach before every warp of the group has passed this point
+// (the ring holds at most 8 windows, and the ring only turns once every warp
+// of a window has released its stage).  A pend entry is reused 32 windows
 // later, once the signal warp has cleared it (bounded wait).
-__device__ __forceinline__ bool window_done(uint8_t* smem, int seq, int ctr, int lane,
+__device__ __forceinline__ bool window_done(uint8_t* smem, int seq, int ctr, int g, int lane,
                                             volatile int* abort_flag) {
   __syncwarp();
   bool ok = true;
   if (lane == 0) {
     int* c = reinterpret_cast<int*>(smem + kSeqOff) + (seq & 15);
-    if (atom_add_acq_rel_cta(c, 1) == kWarps - 1) {
+    if (atom_add_acq_rel_cta(c, 1) == kGroupWarps - 1) {
       *c = 0;
+      st_release_cta_s32(reinterpret_cast<int*>(smem + kGdoneOff) + g, seq);
       unsigned long long* pe = reinterpret_cast<unsigned long long*>(smem + kPendOff) + (seq % kPend);
       const long long t0 = clock64();
       while (ld_acquire_cta_u64(pe) != 0ull) {
@@ -197,18 +213,19 @@ __device__ void issue_rows(const Task& tk, const uint8_t* qwi, const uint8_t* st
 
 // Consumers: stage the activation row of (task, item) with loads that see
 // the outputs of earlier tasks of this launch (L2, not the read-only path).
-__device__ void stage_row(const Task& tk, int item, uint8_t* xs, float* xsc) {
+__device__ void stage_row(const Task& tk, int item, uint8_t* xs, float* xsc, int tid,
+                          int nthreads) {
   const int K = tk.K, Kg = K / 32, Kgp = (int)tk.NI * tk.T;
   const int row = (tk.flags & kTaskXPerItem) ? item : 0;
   const bool gated = (tk.flags & kTaskGated) != 0;
   if (!gated) {
-    // all of a thread's loads (two groups at most up to K = 28672) before
-    // any conversion: one trip to L2
-    for (int base = threadIdx.x; base < Kgp; base += 2 * kCons) {
+    // a thread issues the loads of two 32-value groups before converting
+    // either: one trip to L2 per round
+    for (int base = tid; base < Kgp; base += 2 * nthreads) {
       uint4 v[2][4];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const int g = base + u * kCons;
+        const int g = base + u * nthreads;
 #pragma unroll
         for (int i = 0; i < 4; ++i) v[u][i] = make_uint4(0u, 0u, 0u, 0u);
         if (g < Kg) {
@@ -219,13 +236,13 @@ __device__ void stage_row(const Task& tk, int item, uint8_t* xs, float* xsc) {
       }
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const int g = base + u * kCons;
+        const int g = base + u * nthreads;
         if (g < Kgp) store_staged_group(v[u], xs + g * 16, Kgp * 16, xsc + g, g < Kg);
       }
     }
     return;
   }
-  for (int g = threadIdx.x; g < Kgp; g += kCons) {
+  for (int g = tid; g < Kgp; g += nthreads) {
     const bool valid = g < Kg;
     {   // gated: silu(gate) * up, one group at a time
       float h[32];
@@ -249,8 +266,8 @@ __device__ void stage_row(const Task& tk, int item, uint8_t* xs, float* xsc) {
   }
 }
 
-// Consumer warp `warp`: its share of a window's (chunk, row step) items,
-// dealt round robin over the 14 warps.  Rows finished by one chunk are
+// Consumer warp `warp` of its group: its share of a window's (chunk, row
+// step) items, dealt round robin over the group's 7 warps.  Rows finished by one chunk are
 // stored (0 + chunk sum, rounded once); otherwise each chunk sum goes to the
 // window's buffer `redw` [rows][nch].  Rows of a short window past its end
 // read stale stage bytes (in bounds) and are dropped.
@@ -272,7 +289,7 @@ __device__ __forceinline__ void window_dot(const Task& tk, const uint8_t* sm, ui
   const int code_pitch = K / 2;
   const uint32_t step_base = (uint32_t)(tk.RB * code_pitch + (T - 1) * 16);
   const uint32_t soff0 = (kg2 & 15) == 0 ? 0u : (uint32_t)(((row0 & 7) * (kg2 & 15)) & 15);
-  for (int it = warp; it < items; it += kWarps) {
+  for (int it = warp; it < items; it += kGroupWarps) {
     const int ci = it / nrs, rs = it - ci * nrs;
     uint32_t co[RW], so[RW];
 #pragma unroll
@@ -319,10 +336,13 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
   if (threadIdx.x == 0) {
     for (int s = 0; s < nst; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, kWarps);
+      mbar_init(empty0 + 8 * s, kGroupWarps);   // the group that takes the window
     }
     *abort_flag = 0;
     *reinterpret_cast<volatile int*>(smem + kEndOff) = -1;
+    *reinterpret_cast<volatile unsigned long long*>(smem + kXsOff) = ~0ull;   // no row staged
+    reinterpret_cast<volatile int*>(smem + kGdoneOff)[0] = -1;
+    reinterpret_cast<volatile int*>(smem + kGdoneOff)[1] = -1;
     for (int i = 0; i < 16; ++i) seq_cnt[i] = 0;
     for (int i = 0; i < kPend; ++i) reinterpret_cast<unsigned long long*>(smem + kPendOff)[i] = 0ull;
     mbar_init_fence();
@@ -389,6 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     int slot = 0;
     uint32_t phase = 0;
     bool ended = false;
+    int ends = 0;   // end records issued
     int ti = 0;   // task of the current window (windows come in increasing order)
     int w = 0, grabbed = 0;
     if (lane == 0) w = atomicAdd(work, 1);
@@ -401,12 +422,24 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       }
       volatile int* rec = info + 4 * slot;
       if (w >= p.total) {
+        // one end record for each consumer group (the second in the next
+        // stage, once it is free); the signal warp learns the window count
         if (lane == 0) {
+          *reinterpret_cast<volatile int*>(smem + kEndOff) = (int)(issued - ends);
           rec[3] = 0;
           mbar_arrive(full0 + 8 * slot);
         }
-        ended = true;
-        break;
+        __syncwarp();
+        ++issued;
+        if (++slot == nst) {
+          slot = 0;
+          phase ^= 1u;
+        }
+        if (++ends == kGroups) {
+          ended = true;
+          break;
+        }
+        continue;
       }
       // the next window's number travels while this one is requested
       if (lane == 0) grabbed = atomicAdd(work, 1);
@@ -446,10 +479,9 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       }
       w = __shfl_sync(0xffffffffu, grabbed, 0);
     }
-    // let the last copies land before the CTA may leave (the stage that
-    // carried the end had been released by the consumers)
-    const int inflight = ended ? nst - 1 : nst;
-    const int last = issued < inflight ? (int)issued : inflight;
+    // let the last copies land before the CTA may leave (the end records
+    // complete at once)
+    const int last = issued < nst ? (int)issued : nst;
     for (int i = 1; i <= last; ++i) {
       const int sl = slot - i < 0 ? slot - i + nst : slot - i;
       const uint32_t ph = slot - i < 0 ? phase ^ 1u : phase;
@@ -462,16 +494,31 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
   }
 
   // -------------------------------------------------------------- consumers
+  // Two groups of 7 warps take alternate windows (group g: the CTA's windows
+  // g, g + 2, ...), each like one CTA of the per-launch kernel, and share one
+  // staged activation row.  A group whose window needs another row than the
+  // staged one waits until either the other group has staged it or the other
+  // group is done with every earlier window, and in the latter case stages
+  // it itself (after waiting for the task it depends on).  So a row is never
+  // replaced while a window that needs it is still being computed.
+  const int g = warp / kGroupWarps;               // consumer group
+  const int gw = warp - g * kGroupWarps;          // warp within the group
+  const int gtid = threadIdx.x - g * kGroupThreads;
+  const int bar_id = 1 + g;
   uint8_t* xs = smem + p.xs_off;
   float* xsc = reinterpret_cast<float*>(smem + p.xsc_off);
   float* red = reinterpret_cast<float*>(smem + p.red_off);
-  int slot = 0;
-  uint32_t phase = 0;
-  uint32_t tile = kHdrBytes;
-  int cur_task = -1, cur_item = -1;
-  int seq = 0;                   // windows of this CTA so far
+  unsigned long long* xs_key = reinterpret_cast<unsigned long long*>(smem + kXsOff);
+  int* gdone = reinterpret_cast<int*>(smem + kGdoneOff);
+  volatile int* gflag = reinterpret_cast<volatile int*>(smem + kGflagOff);
+  auto group_sync = [&]() {
+    asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "n"(kGroupThreads) : "memory");
+  };
+  int cur_task = -1, cur_item = -1;   // the row this group's windows last used
   bool reported = false;
-  while (true) {
+  for (int seq = g;; seq += kGroups) {
+    const int slot = seq % nst;
+    const uint32_t phase = (uint32_t)((seq / nst) & 1);
     if (!wait_phase(full0 + 8 * slot, phase, abort_flag)) {
       if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
       *abort_flag = 1;
@@ -479,82 +526,93 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     }
     const volatile int* rec = info + 4 * slot;
     const int t = rec[0], item = rec[1], row0 = rec[2], nr = rec[3];
-    const bool end = nr == 0;
-    const bool xpi = !end && (p.tasks[t].flags & kTaskXPerItem) != 0;
-    if (end || t != cur_task || (xpi && item != cur_item)) {
-      // every consumer is done with the previous windows (the staged row and
-      // the chunk-sum buffers)
-      cons_sync();
-      if (end) {
-        if (threadIdx.x == 0) *reinterpret_cast<volatile int*>(smem + kEndOff) = seq;
-        break;
-      }
-      const Task& tk = p.tasks[t];
-      const bool per_item = (tk.flags & kTaskDepPerItem) != 0;
-      if (tk.dep >= 0 && (t != cur_task || per_item) && threadIdx.x == 0) {
-        // the earlier task's windows (all its items, or item `item`) are done
-        const Task& dk = p.tasks[tk.dep];
-        const long long t0 = clock64();
-        for (int i = per_item ? item : 0; i < (per_item ? item + 1 : dk.n_items); ++i) {
-          while (load_acquire_gpu(done + dk.cbase + i) < dk.wpi) {
-            if (*abort_flag != 0 || clock64() - t0 > kWaitCycles) {
-              if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
-              *abort_flag = 1;
-              break;
-            }
-            __nanosleep(32);
-          }
-          if (*abort_flag != 0) break;
-        }
-      }
-      cons_sync();
-      if (*abort_flag != 0) return;
-      stage_row(tk, item, xs, xsc);
-      cons_sync();
-      cur_task = t;
-      cur_item = item;
+    if (nr == 0) {   // no more windows: never make the other group wait for us
+      if (gtid == 0) st_release_cta_s32(gdone + g, 0x7fffffff);
+      return;
     }
     const Task& tk = p.tasks[t];
+    const bool xpi = (tk.flags & kTaskXPerItem) != 0;
+    const int want_item = xpi ? item : 0;
+    const unsigned long long key = ((unsigned long long)(unsigned)t << 32) | (unsigned)want_item;
+    if (t != cur_task || want_item != cur_item) {
+      // the row this window needs: staged already, or stage it here
+      if (gtid == 0) {
+        const long long t0 = clock64();
+        int restage = 0;
+        while (true) {
+          if (ld_acquire_cta_u64(xs_key) == key) break;           // staged by the other group
+          if (ld_acquire_cta_s32(gdone + (1 - g)) >= seq - 1) {  // other group done before us
+            restage = ld_acquire_cta_u64(xs_key) == key ? 0 : 1;
+            break;
+          }
+          if (*abort_flag != 0 || clock64() - t0 > kWaitCycles) {
+            if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+        }
+        if (restage && tk.dep >= 0 && *abort_flag == 0) {
+          // the earlier task's windows (all its items, or item `item`) are done
+          const bool per_item = (tk.flags & kTaskDepPerItem) != 0;
+          const Task& dk = p.tasks[tk.dep];
+          const long long t1 = clock64();
+          for (int i = per_item ? item : 0; i < (per_item ? item + 1 : dk.n_items); ++i) {
+            while (load_acquire_gpu(done + dk.cbase + i) < dk.wpi) {
+              if (*abort_flag != 0 || clock64() - t1 > kWaitCycles) {
+                if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
+                *abort_flag = 1;
+                break;
+              }
+              __nanosleep(32);
+            }
+            if (*abort_flag != 0) break;
+          }
+        }
+        gflag[g] = restage;
+      }
+      group_sync();
+      if (*abort_flag != 0) return;
+      if (gflag[g]) {
+        stage_row(tk, item, xs, xsc, gtid, kGroupThreads);
+        group_sync();
+        if (gtid == 0) st_release_cta_u64(xs_key, key);
+      }
+      cur_task = t;
+      cur_item = want_item;
+    }
     float* redw = red + slot * p.red_slot;
     const int nrows = nr < 0 ? -nr : nr;
+    const uint32_t tile = kHdrBytes + (uint32_t)slot * p.stage_bytes;
     if (nr > 0) {
       __nv_bfloat16* yrow = tk.y + (long long)item * tk.N + row0;
       const uint32_t xs_off = (uint32_t)p.xs_off, xsc_off = (uint32_t)p.xsc_off;
       if (tk.spec == 0 || (RWA == RWB && TTA == TTB && CLA == CLB))
-        window_dot<RWA, TTA, CLA>(tk, smem, tile, xs_off, xsc_off, row0, nrows, yrow, redw, warp,
+        window_dot<RWA, TTA, CLA>(tk, smem, tile, xs_off, xsc_off, row0, nrows, yrow, redw, gw,
                                   lane);
       else
-        window_dot<RWB, TTB, CLB>(tk, smem, tile, xs_off, xsc_off, row0, nrows, yrow, redw, warp,
+        window_dot<RWB, TTB, CLB>(tk, smem, tile, xs_off, xsc_off, row0, nrows, yrow, redw, gw,
                                   lane);
-    } else if (!reported && threadIdx.x == 0) {
+    } else if (!reported && gtid == 0) {
       report(p.status, W4_ERR_INDEX);   // the item's rows stay unwritten
       reported = true;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * slot);   // this warp is done with the stage
-    if (++slot == nst) {
-      slot = 0;
-      phase ^= 1u;
-      tile = kHdrBytes;
-    } else {
-      tile += p.stage_bytes;
-    }
     if (tk.nch > 1 && nr > 0) {
       // rows whose chunks were summed by different warps: added in chunk order
-      cons_sync();
+      group_sync();
       __nv_bfloat16* yrow = tk.y + (long long)item * tk.N + row0;
-      for (int i = threadIdx.x; i < nrows; i += kCons) {
+      for (int i = gtid; i < nrows; i += kGroupThreads) {
         float v = 0.0f;
         for (int c = 0; c < tk.nch; ++c) v += redw[i * tk.nch + c];
         yrow[i] = __float2bfloat16_rn(v);
       }
     }
-    if (!window_done(smem, seq, tk.cbase + item, lane, abort_flag)) {
+    if (!window_done(smem, seq, tk.cbase + item, g, lane, abort_flag)) {
       if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
       *abort_flag = 1;
       return;
     }
-    ++seq;
   }
 }
 
@@ -571,7 +629,7 @@ struct Inst {
 };
 constexpr int kInsts = 4;
 constexpr Inst kInst[kInsts] = {
-    {{2, 8, 3}, {2, 32, 3}, 5376, 21504},   // hidden 5376, intermediate 21504
+    {{4, 8, 3}, {2, 32, 3}, 5376, 21504},   // hidden 5376, intermediate 21504
     {{2, 16, 4}, {1, 32, 4}, 2048, 8192},   // hidden 2048, intermediate 8192
     {{1, 8, 11}, {1, 2, 11}, 2816, 704},    // routed experts: hidden 2816, expert width 704
     {{1, 0, 0}, {1, 0, 0}, 0, 0},           // generic
@@ -581,7 +639,7 @@ using KernelFn = void (*)(Params);
 
 KernelFn kernel_of(int inst) {
   switch (inst) {
-    case 0: return chain_kernel<2, 8, 3, 2, 32, 3>;
+    case 0: return chain_kernel<4, 8, 3, 2, 32, 3>;
     case 1: return chain_kernel<2, 16, 4, 1, 32, 4>;
     case 2: return chain_kernel<1, 8, 11, 1, 2, 11>;
     case 3: return chain_kernel<1, 0, 0, 1, 0, 0>;
@@ -614,20 +672,27 @@ struct ChainPlan {
 };
 
 // Window (rows a multiple of the row step) of a task for stages of at most
-// `cap` bytes.  Each consumer warp takes at most ceil(items / 14) of a
-// window's (chunk, row step) items, so a window lasts about as long as its
-// copy or as its slowest warp's items, whichever is longer, and a task takes
-// about ceil(windows / SMs) such rounds.  The window with the shortest
-// estimate is taken (ties: the taller one): full 14-item windows for large
+// `cap` bytes.  Each warp of a consumer group takes at most ceil(items / 7)
+// of a window's (chunk, row step) items, so a window lasts about as long as
+// its copy (at half the SM's stream rate: two groups) or as its slowest
+// warp's items, whichever is longer, and a task takes about
+// ceil(windows / (2 SMs)) such rounds.  The SM's stream rate is its share of
+// HBM, or less when the stages not held by the two groups cannot keep that
+// share in flight over a copy's latency.  The window with the shortest
+// estimate is taken (ties: the taller one): full 7-item windows for large
 // tasks, more and smaller windows for tasks too small to reach every SM.
 // `est` returns the estimate (microseconds).
 constexpr double kSmBytesPerUs = 44.7e3;    // an SM's share of the HBM stream
-constexpr double kWarpBytesPerUs = 3.7e3;   // weight bytes a consumer warp dequantises
-bool pick_window(int K, int N, int n_items, const TaskPlan& tp, long long cap, int sms,
+constexpr double kCopyLatencyUs = 2.0;      // a stage's copy under load
+// weight bytes a consumer warp dequantises per microsecond, by rows per lane
+constexpr double warp_bytes_per_us(int rw) { return rw >= 4 ? 3.9e3 : rw == 2 ? 3.55e3 : 3.1e3; }
+bool pick_window(int K, int N, int n_items, const TaskPlan& tp, long long cap, int nst, int sms,
                  int* rb_out, int* tile_out, double* est_out) {
   const int nsw = 32 / tp.T;
   const int rstep = nsw * tp.RW;
   const double row_bytes = K / 2 + K / 16;
+  const double sm_rate =
+      std::min(kSmBytesPerUs, std::max(0.5, (double)(nst - kGroups)) * cap / kCopyLatencyUs);
   double best = -1.0;
   for (int rs = 1; rs <= 64; ++rs) {
     const int rb = rs * rstep;
@@ -637,10 +702,12 @@ bool pick_window(int K, int N, int n_items, const TaskPlan& tp, long long cap, i
     if (rs > 1 && rb >= N + rstep) break;   // no taller than the rows there are
     const int items = tp.nch * rs;
     const double item_bytes = rstep * row_bytes / tp.nch;
-    const double t_win = std::max(rb * row_bytes / kSmBytesPerUs,
-                                  ((items + kWarps - 1) / kWarps) * item_bytes / kWarpBytesPerUs);
+    const double t_win =
+        std::max(rb * row_bytes / (sm_rate / kGroups),
+                 ((items + kGroupWarps - 1) / kGroupWarps) * item_bytes / warp_bytes_per_us(tp.RW));
     const long long wins = (long long)n_items * ((N + rb - 1) / rb);
-    const double est = (double)((wins + sms - 1) / sms) * t_win;
+    const long long slots = (long long)kGroups * sms;
+    const double est = (double)((wins + slots - 1) / slots) * t_win;
     if (best < 0.0 || est <= best * (1.0 + 1e-9)) {
       best = est;
       *rb_out = rb;
@@ -651,25 +718,13 @@ bool pick_window(int K, int N, int n_items, const TaskPlan& tp, long long cap, i
   return best >= 0.0;
 }
 
-w4_status make_plan(const w4_gemv_task* tasks, int n, const DeviceInfo& di, ChainPlan* out) {
+// The plan of one instantiation: stages and windows with the shortest
+// estimated chain (more stages unless fewer are clearly faster).
+double plan_inst(const w4_gemv_task* tasks, int n, const DeviceInfo& di, int inst, ChainPlan* out) {
   ChainPlan& pl = *out;
-  // the instantiation: the first whose specs serve every task's K
-  pl.inst = kInsts - 1;
-  for (int i = 0; i < kInsts - 1; ++i) {
-    bool ok = true;
-    for (int j = 0; j < n && ok; ++j) {
-      const int K = tasks[j].K;
-      ok = (K == kInst[i].Ka && spec_fits(kInst[i].a, K)) ||
-           (K == kInst[i].Kb && spec_fits(kInst[i].b, K));
-    }
-    if (ok) {
-      pl.inst = i;
-      break;
-    }
-  }
-  const Inst& in = kInst[pl.inst];
+  pl.inst = inst;
+  const Inst& in = kInst[inst];
   int kgp_max = 0;
-  long long weight_total = 0;
   for (int j = 0; j < n; ++j) {
     TaskPlan& tp = pl.t[j];
     const int K = tasks[j].K;
@@ -678,14 +733,11 @@ w4_status make_plan(const w4_gemv_task* tasks, int n, const DeviceInfo& di, Chai
     tp.RW = sp.RW;
     row_shape(K, &tp.T, &tp.NI, &tp.CL, &tp.nch);
     kgp_max = std::max(kgp_max, tp.NI * tp.T);
-    weight_total += (long long)tasks[j].N * (tasks[j].ids ? tasks[j].n_ids : 1) * (K / 2 + K / 16);
   }
-  (void)weight_total;
   const long long optin = di.smem_optin > 0 ? di.smem_optin : 232448;
   const long long xbytes = (long long)kgp_max * (64 + 4);
-  // stages: the count whose windows give the shortest estimated chain; more
-  // stages unless fewer are clearly faster
   double best_est = -1.0;
+  static thread_local TaskPlan trial[W4_CHAIN_MAX_TASKS];
   for (int nst = kMaxStages; nst >= 2; --nst) {
     const long long room = optin - kHdrBytes - xbytes;
     long long cap = std::min(kStageMax, room / nst);
@@ -694,12 +746,11 @@ w4_status make_plan(const w4_gemv_task* tasks, int n, const DeviceInfo& di, Chai
     double est_sum = 0.0;
     int red_slot = 0, stage = 0;
     bool ok = true;
-    TaskPlan trial[W4_CHAIN_MAX_TASKS];
     for (int j = 0; j < n && ok; ++j) {
       trial[j] = pl.t[j];
       double est = 0.0;
       ok = pick_window(tasks[j].K, tasks[j].N, tasks[j].ids ? tasks[j].n_ids : 1, trial[j], cap,
-                       std::max(1, di.sms), &trial[j].RB, &trial[j].tile, &est);
+                       nst, std::max(1, di.sms), &trial[j].RB, &trial[j].tile, &est);
       est_sum += est;
       if (trial[j].nch > 1) red_slot = std::max(red_slot, trial[j].RB * trial[j].nch);
       stage = std::max(stage, trial[j].tile);
@@ -720,7 +771,32 @@ w4_status make_plan(const w4_gemv_task* tasks, int n, const DeviceInfo& di, Chai
       for (int j = 0; j < n; ++j) pl.t[j] = trial[j];
     }
   }
-  if (best_est < 0.0) return W4_ERR_SHAPE;
+  return best_est;
+}
+
+w4_status make_plan(const w4_gemv_task* tasks, int n, const DeviceInfo& di, ChainPlan* out) {
+  // the compiled instantiations whose specs serve every task's K, the one
+  // with the shortest estimate (the generic loop when none does)
+  static thread_local ChainPlan trial;
+  double best = -1.0;
+  for (int i = 0; i < kInsts; ++i) {
+    bool ok = true;
+    for (int j = 0; j < n && ok; ++j) {
+      const int K = tasks[j].K;
+      ok = kInst[i].a.TT == 0 || (K == kInst[i].Ka && spec_fits(kInst[i].a, K)) ||
+           (K == kInst[i].Kb && spec_fits(kInst[i].b, K));
+    }
+    if (!ok) continue;
+    // the generic loop only when no compiled pair serves the tasks
+    if (kInst[i].a.TT == 0 && best >= 0.0) continue;
+    const double est = plan_inst(tasks, n, di, i, &trial);
+    if (est >= 0.0 && (best < 0.0 || est < 0.99 * best)) {
+      best = est;
+      *out = trial;
+    }
+  }
+  if (best < 0.0) return W4_ERR_SHAPE;
+  ChainPlan& pl = *out;
   long long total = 0;
   for (int j = 0; j < n; ++j) {
     TaskPlan& tp = pl.t[j];

@@ -12,7 +12,7 @@ from bit_weight_only_gemv_gb300 import lib, synth
 
 MAX_SMEM = 232448          # largest dynamic shared memory of a GB300 CTA
 HDR = 1024                 # barriers, flags, window records, finished windows
-WARPS = 14                 # consumer warps
+WARPS = 7                  # warps of a consumer group
 
 
 @pytest.fixture(scope="module")
@@ -146,7 +146,7 @@ def test_decode_pass_chain_plan_and_bounds(L, name):
     plan, per = plans(L, ts)
     assert plan["instantiation"] == (0 if model.hidden == 5376 else 1)
     assert plan["threads"] == 512 and plan["stages"] >= 2
-    # tasks with rows for many rounds of windows keep all 14 consumer warps busy
+    # tasks with rows for many rounds of windows keep all 7 warps of a group busy
     for t, p in zip(ts, per):
         items = p["chunks"] * p["rows_per_window"] // ((32 // p["team"]) * p["rows_per_lane"])
         if p["windows_per_item"] >= 4 * plan["ctas"]:
