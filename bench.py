@@ -1043,12 +1043,22 @@ def run_shape(args):
     sts = [synth.torch_steps((N, K // 32), synth.seed_of(8, i), dev) for i in range(copies)]
     x = synth.torch_x((M, K), synth.seed_of(9), dev)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    path = None if args.path == "auto" else args.path
-    need = lib.workspace_bytes(M, N, K, path)
-    ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev) if need else None
-    fns = [(lambda q, s_: (lambda pdl: lib.gemv(q, s_, x, y=y, workspace=ws, pdl=pdl,
-                                                path=path)))(q, s_)
-           for q, s_ in zip(qws, sts)]
+    if args.path == "chain":
+        # each launch a one-task w4a16_gemv_chain (batch 1), own workspace
+        if M != 1:
+            raise SystemExit("--path chain times batch-1 shapes")
+        fns = []
+        for q, s_ in zip(qws, sts):
+            tasks = [lib.gemv_task(q, s_, x.view(-1), y.view(-1))]
+            wsc = torch.zeros(lib.chain_workspace_bytes(tasks), dtype=torch.uint8, device=dev)
+            fns.append((lambda c: (lambda pdl: c(pdl=pdl)))(lib.bind_gemv_chain(tasks, wsc)))
+    else:
+        path = None if args.path == "auto" else args.path
+        need = lib.workspace_bytes(M, N, K, path)
+        ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev) if need else None
+        fns = [(lambda q, s_: (lambda pdl: lib.gemv(q, s_, x, y=y, workspace=ws, pdl=pdl,
+                                                    path=path)))(q, s_)
+               for q, s_ in zip(qws, sts)]
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         for i, f in enumerate(fns):
@@ -1118,8 +1128,9 @@ def build_parser() -> argparse.ArgumentParser:
                     help="N,K,n_ids[,x_rows]: time one routed call (w4a16_gemv_id) over n_ids "
                          "experts of N x K alone")
     ap.add_argument("--no-pdl", action="store_true", help="with --shape: plain launches")
-    ap.add_argument("--path", choices=("auto", "cuda", "tensor"), default="auto",
-                    help="with --shape: the library's choice, CUDA cores or tensor cores")
+    ap.add_argument("--path", choices=("auto", "cuda", "tensor", "chain"), default="auto",
+                    help="with --shape: the library's choice, CUDA cores, tensor cores, or "
+                         "(batch 1) a one-task w4a16_gemv_chain launch")
     ap.add_argument("--separate", action="store_true",
                     help="one GEMV per projection instead of merged q/k/v and gate/up")
     ap.add_argument("--expert-home", choices=("device", "host"), default="device",

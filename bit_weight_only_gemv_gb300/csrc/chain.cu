@@ -389,6 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         ok = false;
         break;
       }
+      __nanosleep(128);   // idle: leave the issue slots to the consumer warps
     }
     if (ok) {
       __threadfence();
