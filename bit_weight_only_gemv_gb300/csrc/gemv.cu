@@ -1581,7 +1581,7 @@ extern "C" w4_status w4a16_gemv_plan(int M, int N, int K, w4_plan_info* info) {
     info->rows_per_call = std::min(M, tc::kTcMaxM);
     info->chunk_steps = 8;
     info->stages = tp.nst;
-    info->ctas_per_sm = 2;
+    info->ctas_per_sm = tp.per_sm;
     info->tmpl_team = tp.np;
     info->tmpl_chunk = 0;
     return W4_OK;

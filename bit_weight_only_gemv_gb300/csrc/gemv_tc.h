@@ -16,6 +16,7 @@ struct TcPlan {
   int slices = 0, tiles = 0;  // 256-code K slices, 128-row tiles
   int S = 1, sps = 1, units = 0, ctas = 0;
   int nst = 2, stage_bytes = 0, off_b = 0, smem = 0;
+  int bufs = 2, per_sm = 2;   // rounds held in tensor memory; CTAs per SM
   size_t ws_bytes = 0, ws_part_off = 0;
 };
 

@@ -162,9 +162,11 @@ def test_tensor_core_plan_is_valid(M, N, K):
     assert p["path"] == 2 and p["threads"] == 320 and p["unit_rows"] == 128
     assert p["tmpl_team"] == (16 if M <= 16 else 32)      # MMA N: activation columns
     assert p["rows_per_call"] == min(M, 32)
-    assert p["ctas_per_sm"] == 2
-    assert 2 <= p["stages"] <= 4 and p["smem_bytes"] <= 233472 // 2 - 1024
+    assert p["ctas_per_sm"] in (1, 2)
+    assert 2 <= p["stages"] <= 8 and p["smem_bytes"] <= 233472 // p["ctas_per_sm"] - 1024
     assert 1 <= p["ctas"] <= p["ctas_per_sm"] * 152
+    if p["ctas_per_sm"] == 1:      # all of tensor memory: no second CTA fits the SM
+        assert p["smem_bytes"] > 233472 // 2
     tiles, slices = -(-N // 128), K // 256
     assert 1 <= p["slices"] <= slices
     assert (lib.workspace_bytes(M, N, K) > 0) == (p["slices"] > 1)
