@@ -137,9 +137,12 @@ class DecodePass:
     """Device-resident weights, inputs and outputs of one decode pass."""
 
     def __init__(self, model: synth.DenseDecoder, device, seed: int = 0, merge: bool = True,
-                 gated: bool = False):
+                 gated: bool = False, l2_next_bytes: int = 0):
         from bit_weight_only_gemv_gb300 import lib
         self.lib = lib
+        # each GEMV brings up to this many bytes of the next GEMV's weights
+        # (its leading rows) into L2 once its own tiles are requested
+        self.l2_next_bytes = l2_next_bytes
         # gated MLP: each layer's down projection reads the merged gate/up
         # output through silu(gate) * up instead of its own activation row
         self.gated = gated and merge
@@ -218,6 +221,7 @@ class DecodePass:
         if m.per_layer_width:
             out.append(("gather", (1, m.per_layer_width), lambda pdl: lib.embed_gather(
                 self.ple_qw, self.ple_st, self.ids, out=self.ple_row, status=self.status, pdl=pdl)))
+        specs = []   # (n, k, qw, st, x, y, gated) of every GEMV in order
         for li, name, n, k, xk, qw, st in self.mats:
             x = self.x((li, xk), k)
             gated = self.gated and name == "down"
@@ -225,13 +229,25 @@ class DecodePass:
                 og = self.y_off[(li, "gate+up")]
                 x = self.y_flat[og:og + 2 * k].view(1, 2 * k)
             o = self.y_off[(li, name)]
-            y = self.y_flat[o:o + n].view(1, n)
-            out.append(("gemv", (1, n, k), self._gemv(qw, st, x, y, gated)))
+            specs.append((n, k, qw, st, x, self.y_flat[o:o + n].view(1, n), gated))
         o = self.y_off["logits"]
-        out.append(("gemv", (1, m.vocab, m.hidden), self._gemv(
-            self.emb_qw, self.emb_st, self.x("final", m.hidden),
-            self.y_flat[o:o + m.vocab].view(1, m.vocab))))
+        specs.append((m.vocab, m.hidden, self.emb_qw, self.emb_st, self.x("final", m.hidden),
+                      self.y_flat[o:o + m.vocab].view(1, m.vocab), False))
+        for i, (n, k, qw, st, x, y, gated) in enumerate(specs):
+            nxt = specs[i + 1] if i + 1 < len(specs) else None
+            l2 = self.next_ranges(nxt[0], nxt[1], nxt[2], nxt[3]) if nxt else None
+            out.append(("gemv", (1, n, k), self._gemv(qw, st, x, y, gated, l2)))
         return out
+
+    def next_ranges(self, n, k, qw, st):
+        """The leading rows of an (n, k) matrix's codes and steps that fit
+        l2_next_bytes, as w4_l2_range entries (None when disabled)."""
+        if self.l2_next_bytes <= 0:
+            return None
+        rows = min(n, self.l2_next_bytes // (k // 2 + k // 16))
+        if rows < 1:
+            return None
+        return self.lib.l2_ranges([(qw, rows * (k // 2)), (st, rows * (k // 16))])
 
     def chain_launches(self):
         """The same pass as the row gather(s) plus ONE w4a16_gemv_chain launch
@@ -261,10 +277,10 @@ class DecodePass:
         out.append(("chain", shapes, lambda pdl: call(pdl=pdl)))
         return out
 
-    def _gemv(self, qw, st, x, y, gated=False):
+    def _gemv(self, qw, st, x, y, gated=False, l2_next=None):
         lib = self.lib
         return lambda pdl: lib.gemv(qw, st, x, y=y, workspace=self.ws, status=self.status, pdl=pdl,
-                                    silu_mul=gated)
+                                    silu_mul=gated, l2_next=l2_next)
 
     def step_bytes(self):
         return step_bytes_of(self.model)
@@ -542,6 +558,11 @@ def dense_config(model, args, world, step_bytes):
                        "launch, each task waiting for the one before"
                        if getattr(args, "chain", False) else
                        "one launch per GEMV, chained with programmatic dependent launch"),
+            "l2_next": (f"each GEMV brings up to {args.l2_next_mb:g} MiB of the next GEMV's "
+                        "weights into L2 once its own tiles are requested "
+                        "(w4a16_gemv_prefetch_l2)"
+                        if getattr(args, "l2_next_mb", 0) > 0 and not getattr(args, "chain", False)
+                        else None),
             "global_batch": world, "parallelism": f"replicas x{world}",
             "bytes_per_step": step_bytes,
             "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB of weights per step, "
@@ -631,7 +652,8 @@ def run_gb300(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     model = DENSE_WORKLOADS[args.workload]()
-    dp = DecodePass(model, dev, seed=0, merge=not args.separate, gated=args.gated_mlp)
+    dp = DecodePass(model, dev, seed=0, merge=not args.separate, gated=args.gated_mlp,
+                    l2_next_bytes=int(args.l2_next_mb * (1 << 20)))
     launches = dp.chain_launches() if args.chain else dp.launches()
     stream = torch.cuda.Stream(device=dev)
     # eager warm-up (plans, attributes), then capture the pass as one graph
@@ -1056,9 +1078,14 @@ def run_shape(args):
         path = None if args.path == "auto" else args.path
         need = lib.workspace_bytes(M, N, K, path)
         ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev) if need else None
-        fns = [(lambda q, s_: (lambda pdl: lib.gemv(q, s_, x, y=y, workspace=ws, pdl=pdl,
-                                                    path=path)))(q, s_)
-               for q, s_ in zip(qws, sts)]
+        # --l2-next-mb: each launch brings the next copy's leading rows into L2
+        pf_rows = min(N, int(args.l2_next_mb * (1 << 20)) // (K // 2 + K // 16))
+        nxt = [lib.l2_ranges([(qws[(i + 1) % copies], pf_rows * (K // 2)),
+                              (sts[(i + 1) % copies], pf_rows * (K // 16))])
+               if pf_rows > 0 else None for i in range(copies)]
+        fns = [(lambda q, s_, l2: (lambda pdl: lib.gemv(q, s_, x, y=y, workspace=ws, pdl=pdl,
+                                                        path=path, l2_next=l2)))(q, s_, l2)
+               for q, s_, l2 in zip(qws, sts, nxt)]
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         for i, f in enumerate(fns):
@@ -1069,7 +1096,7 @@ def run_shape(args):
         g.replay()
     ms = time_replays(g, stream, args.steps) / copies
     print(json.dumps({"mode": "shape", "M": M, "N": N, "K": K, "pdl": not args.no_pdl,
-                      "path": args.path,
+                      "path": args.path, "l2_next_mb": args.l2_next_mb,
                       "us_per_launch": ms * 1e3, "gbps": metrics.gbps(per, ms * 1e-3),
                       "bytes_per_launch": per, "copies": copies, "plan": lib.plan(M, N, K)}),
           flush=True)
@@ -1142,6 +1169,10 @@ def build_parser() -> argparse.ArgumentParser:
     ap.add_argument("--chain", action="store_true",
                     help="decode passes: every GEMV of the pass in one w4a16_gemv_chain launch "
                          "(each task waiting for the one before) instead of one launch each")
+    ap.add_argument("--l2-next-mb", type=float, default=0.0,
+                    help="decode passes: each GEMV brings up to this many MiB of the next GEMV's "
+                         "weights (its leading rows) into L2 once its own tiles are requested "
+                         "(w4a16_gemv_prefetch_l2); 0 turns it off")
     ap.add_argument("--gated-mlp", action="store_true",
                     help="decode passes: each down projection reads its layer's merged gate/up "
                          "output through silu(gate) * up (W4_FLAG_SILU_MUL) instead of its own "

@@ -25,6 +25,49 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- L2 prefetch
+// Byte ranges to bring into L2 once a launch has requested its own tiles
+// (w4a16_gemv_prefetch_l2): normally the next call's weights, so that HBM
+// keeps streaming while this launch finishes and the next one starts.
+// Addresses are 16-byte aligned; a range's last bytes past a multiple of 16
+// are left out (the bulk prefetch moves whole 16-byte units).
+constexpr int kMaxL2Ranges = W4_MAX_L2_RANGES;
+struct L2Ranges {
+  const uint8_t* ptr[kMaxL2Ranges];
+  unsigned long long bytes[kMaxL2Ranges];
+  int n;
+};
+
+// This CTA's share of the ranges, in order: the ranges' bytes are cut into
+// `ctas` consecutive shares (16-byte multiples); lane l of the calling warp
+// issues the share's chunks l, l + 32, ... of at most kL2Chunk bytes each.
+// Fire and forget: nothing waits for the data, and nothing is written.
+constexpr unsigned long long kL2Chunk = 16384;
+__device__ __forceinline__ void l2_prefetch_share(const L2Ranges& r, int cta, int ctas, int lane) {
+  unsigned long long total = 0;
+  for (int i = 0; i < r.n; ++i) total += r.bytes[i] & ~15ull;
+  if (total == 0) return;
+  const unsigned long long share = ((total + ctas - 1) / ctas + 15) & ~15ull;
+  unsigned long long lo = share * (unsigned long long)cta;
+  const unsigned long long hi = min(total, lo + share);
+  unsigned long long base = 0;   // offset of range i within the concatenation
+  for (int i = 0; i < r.n && lo < hi; ++i) {
+    const unsigned long long len = r.bytes[i] & ~15ull;
+    if (lo < base + len) {
+      const unsigned long long a = lo - base, b = min(len, hi - base);
+      const unsigned long long nchunks = (b - a + kL2Chunk - 1) / kL2Chunk;
+      for (unsigned long long c = lane; c < nchunks; c += 32) {
+        const unsigned long long o = a + c * kL2Chunk;
+        const uint32_t n = (uint32_t)min(kL2Chunk, b - o);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(r.ptr[i] + o), "r"(n)
+                     : "memory");
+      }
+      lo = base + b;
+    }
+    base += len;
+  }
+}
+
 // ---------------------------------------------------------------- smem
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -112,6 +112,7 @@ struct GemvParams {
   const int32_t* slot_expert;          // [num_experts] expert each slot holds, or nullptr
   const __nv_bfloat16* escale;         // [num_real][N] output scale, or nullptr
   const __nv_bfloat16* ebias;          // [num_real][N] output bias, or nullptr
+  L2Ranges l2;                         // brought into L2 after the launch's own tiles
 };
 
 // ---------------------------------------------------------------- activations
@@ -516,6 +517,9 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
         phase ^= 1u;
       }
     }
+    // Every tile of this CTA is requested: its share of the caller's L2
+    // ranges (the next call's weights) goes out now, behind them.
+    if (p.l2.n > 0 && *abort_flag == 0) l2_prefetch_share(p.l2, blockIdx.x, gridDim.x, lane);
     // Let the last copies land before the CTA may leave.  When the end went
     // out in stage `slot`, that stage's previous tile had been released by
     // the consumers (its barrier has moved on since): it is not waited for.
@@ -1497,7 +1501,7 @@ size_t tc_workspace(int M, int N, int K, int sms) {
 // Enqueue the tensor-core launches of a call (up to 32 activation rows each).
 w4_status tc_enqueue(void* y, const void* qw, const void* st, const void* x, int M, int N, int K,
                      void* workspace, size_t workspace_bytes, int32_t* status_dev, bool pdl,
-                     cudaStream_t s, int dev, int sms) {
+                     cudaStream_t s, int dev, int sms, const L2Ranges* l2 = nullptr) {
   // more rows than a small-batch launch takes: one launch of the prompt GEMM
   tc::TpPlan pp;
   if (M > tc::kTcMaxM && tc::tp_plan(M, N, K, sms, &pp)) {
@@ -1524,7 +1528,7 @@ w4_status tc_enqueue(void* y, const void* qw, const void* st, const void* x, int
     const cudaError_t e =
         tc::tc_launch(tp, static_cast<__nv_bfloat16*>(y) + (long long)m0 * N, qw, st,
                       static_cast<const __nv_bfloat16*>(x) + (long long)m0 * K, mr, N, K, workspace,
-                      status_dev, pdl, s, dev);
+                      status_dev, pdl, s, dev, m0 + mr >= M ? l2 : nullptr);
     if (e != cudaSuccess) {
       note_cuda_error(e);
       cudaGetLastError();
@@ -1658,9 +1662,11 @@ extern "C" size_t w4a16_gemv_workspace_bytes(int M, int N, int K) {
   return w4a16_gemv_workspace_bytes_flags(M, N, K, 0);
 }
 
-extern "C" w4_status w4a16_gemv(void* y, const void* qw, const void* st, const void* x, int M,
-                                int N, int K, void* workspace, size_t workspace_bytes,
-                                int32_t* status_dev, unsigned flags, w4_stream_t stream) {
+// w4a16_gemv, and (l2 != nullptr) the caller's L2 ranges fetched by the
+// call's last launch once its CTAs have requested their own tiles.
+static w4_status gemv_call(void* y, const void* qw, const void* st, const void* x, int M, int N,
+                           int K, void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                           unsigned flags, w4_stream_t stream, const L2Ranges* l2) {
   if (y == nullptr || qw == nullptr || st == nullptr || x == nullptr) return W4_ERR_ARG;
   if (M < 1 || N < 1 || (flags & ~(W4_FLAG_PDL | kPathFlags | W4_FLAG_SILU_MUL)) != 0)
     return W4_ERR_ARG;
@@ -1677,7 +1683,7 @@ extern "C" w4_status w4a16_gemv(void* y, const void* qw, const void* st, const v
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (path == 1)
     return tc_enqueue(y, qw, st, x, M, N, K, workspace, workspace_bytes, status_dev,
-                      (flags & W4_FLAG_PDL) != 0, s, dev, di.sms);
+                      (flags & W4_FLAG_PDL) != 0, s, dev, di.sms, l2);
   const int mr_cap = max_rows_per_launch(K, di);
   if (mr_cap < 1) return W4_ERR_SHAPE;
   // every launch of the call is checked before the first one is enqueued
@@ -1706,6 +1712,7 @@ extern "C" w4_status w4a16_gemv(void* y, const void* qw, const void* st, const v
       p.ws_count = static_cast<int*>(workspace);
       p.ws_partial = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pm.ws_part_off);
     }
+    if (l2 != nullptr && m0 + mr >= M) p.l2 = *l2;   // the call's last launch
     const cudaError_t e = launch(p, pm, (flags & W4_FLAG_PDL) != 0, s, dev);
     if (e != cudaSuccess) {
       note_cuda_error(e);
@@ -1714,6 +1721,33 @@ extern "C" w4_status w4a16_gemv(void* y, const void* qw, const void* st, const v
     }
   }
   return W4_OK;
+}
+
+extern "C" w4_status w4a16_gemv(void* y, const void* qw, const void* st, const void* x, int M,
+                                int N, int K, void* workspace, size_t workspace_bytes,
+                                int32_t* status_dev, unsigned flags, w4_stream_t stream) {
+  return gemv_call(y, qw, st, x, M, N, K, workspace, workspace_bytes, status_dev, flags, stream,
+                   nullptr);
+}
+
+extern "C" w4_status w4a16_gemv_prefetch_l2(void* y, const void* qw, const void* st,
+                                            const void* x, int M, int N, int K, void* workspace,
+                                            size_t workspace_bytes, int32_t* status_dev,
+                                            unsigned flags, const w4_l2_range* ranges,
+                                            int n_ranges, w4_stream_t stream) {
+  if (n_ranges < 0 || n_ranges > W4_MAX_L2_RANGES || (n_ranges > 0 && ranges == nullptr))
+    return W4_ERR_ARG;
+  L2Ranges l2{};
+  for (int i = 0; i < n_ranges; ++i) {
+    if (ranges[i].bytes > 0 && ranges[i].ptr == nullptr) return W4_ERR_ARG;
+    if (ranges[i].bytes > 0 && !aligned(ranges[i].ptr, 16)) return W4_ERR_ALIGN;
+    if (ranges[i].bytes < 16) continue;   // less than one 16-byte unit: nothing to fetch
+    l2.ptr[l2.n] = static_cast<const uint8_t*>(ranges[i].ptr);
+    l2.bytes[l2.n] = ranges[i].bytes;
+    ++l2.n;
+  }
+  return gemv_call(y, qw, st, x, M, N, K, workspace, workspace_bytes, status_dev, flags, stream,
+                   l2.n > 0 ? &l2 : nullptr);
 }
 
 namespace w4 {

@@ -81,6 +81,7 @@ struct TcParams {
   float* ws_partial;      // [slices][M][N] under split-K
   int* ws_count;          // [tiles]
   int32_t* status;
+  L2Ranges l2;            // brought into L2 after the launch's own tiles
 };
 
 // MMA width (activation columns, 16 or 32) and groups per round for MC
@@ -202,6 +203,9 @@ __global__ void __launch_bounds__(kThreads, kBufs >= 4 ? 1 : 2)
         }
       }
     }
+    // every tile of this CTA is requested: its share of the caller's L2
+    // ranges (the next call's weights) goes out now, behind them
+    if (p.l2.n > 0 && *abort_flag == 0) l2_prefetch_share(p.l2, blockIdx.x, gridDim.x, lane);
     // let the last copies land before the CTA may leave
     const int last = issued < nst ? issued : nst;
     for (int i = 1; i <= last; ++i) {
@@ -625,7 +629,7 @@ bool tc_plan(int M, int N, int K, int sms, TcPlan* out) {
 
 cudaError_t tc_launch(const TcPlan& pl, void* y, const void* qw, const void* st, const void* x, int M,
                       int N, int K, void* workspace, int32_t* status, bool pdl, cudaStream_t stream,
-                      int dev) {
+                      int dev, const L2Ranges* l2) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
   TcParams p = {};
@@ -676,6 +680,7 @@ cudaError_t tc_launch(const TcPlan& pl, void* y, const void* qw, const void* st,
   p.off_b = pl.off_b;
   p.xrows = M;
   p.status = status;
+  if (l2 != nullptr) p.l2 = *l2;
   if (pl.S > 1) {
     p.ws_count = static_cast<int*>(workspace);
     p.ws_partial = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.ws_part_off);

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "common.cuh"
+
 namespace w4 {
 namespace tc {
 
@@ -26,9 +28,11 @@ bool tc_supported(int M, int K);
 
 bool tc_plan(int M, int N, int K, int sms, TcPlan* out);
 
+// l2: byte ranges the copy warps bring into L2 once their own tiles are
+// requested (w4a16_gemv_prefetch_l2), or nullptr.
 cudaError_t tc_launch(const TcPlan& pl, void* y, const void* qw, const void* st, const void* x,
                       int M, int N, int K, void* workspace, int32_t* status, bool pdl,
-                      cudaStream_t stream, int dev);
+                      cudaStream_t stream, int dev, const L2Ranges* l2 = nullptr);
 
 int tc_sms(int dev);
 

@@ -33,8 +33,9 @@ EXPORTS = ("w4_status_str", "w4_abi_version", "w4_last_cuda_error", "w4a16_gemv"
            "w4a16_gemv_static_scratch", "w4_dev_pool_state_bytes", "w4_dev_pool_init",
            "w4_dev_pool_stage", "w4_dev_pool_stats", "w4a16_gemv_chain",
            "w4a16_gemv_chain_workspace_bytes", "w4a16_gemv_chain_plan",
-           "w4a16_gemv_chain_task_plan", "w4a16_gemv_id_plan")
+           "w4a16_gemv_chain_task_plan", "w4a16_gemv_id_plan", "w4a16_gemv_prefetch_l2")
 W4_TASK_SILU_MUL = 1
+W4_MAX_L2_RANGES = 4
 CHAIN_MAX_TASKS = 320
 
 
@@ -60,6 +61,11 @@ class GemvTask(ctypes.Structure):
                 ("st_stride", ctypes.c_size_t), ("num_experts", ctypes.c_int),
                 ("n_ids", ctypes.c_int), ("x_rows", ctypes.c_int), ("N", ctypes.c_int),
                 ("K", ctypes.c_int), ("dep", ctypes.c_int), ("flags", ctypes.c_uint)]
+
+
+class L2Range(ctypes.Structure):
+    """struct w4_l2_range of include/w4a16.h."""
+    _fields_ = [("ptr", ctypes.c_void_p), ("bytes", ctypes.c_size_t)]
 
 
 class ChainPlanInfo(ctypes.Structure):
@@ -92,6 +98,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.w4_last_cuda_error.argtypes = []
     lib.w4a16_gemv.restype = i32
     lib.w4a16_gemv.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, sz, vp, u32, vp]
+    lib.w4a16_gemv_prefetch_l2.restype = i32
+    lib.w4a16_gemv_prefetch_l2.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, sz, vp, u32,
+                                           ctypes.POINTER(L2Range), i32, vp]
     lib.w4a16_gemv_static_scratch.restype = i32
     lib.w4a16_gemv_static_scratch.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, u32, vp]
     lib.w4a16_gemv_workspace_bytes.restype = sz
@@ -201,15 +210,33 @@ def id_plan(n_ids: int, x_rows: int, N: int, K: int) -> dict:
     return {n: getattr(info, n) for n, _ in PlanInfo._fields_}
 
 
+def l2_ranges(ranges):
+    """A ctypes array of w4_l2_range from (tensor, bytes) or (address, bytes)
+    pairs (bytes None: the whole tensor)."""
+    arr = (L2Range * max(1, len(ranges)))()
+    for i, (t, nbytes) in enumerate(ranges):
+        if isinstance(t, torch.Tensor):
+            _need(t, t.dtype, "prefetch range")
+            full = t.numel() * t.element_size()
+            nbytes = full if nbytes is None else min(int(nbytes), full)
+            arr[i] = L2Range(t.data_ptr(), nbytes)
+        else:
+            arr[i] = L2Range(int(t), int(nbytes))
+    return arr
+
+
 def gemv(qw: torch.Tensor, st: torch.Tensor, x: torch.Tensor, y: torch.Tensor = None,
          workspace: torch.Tensor = None, status: torch.Tensor = None, pdl: bool = False,
-         stream=None, path: str = None, silu_mul: bool = False) -> torch.Tensor:
+         stream=None, path: str = None, silu_mul: bool = False, l2_next=None) -> torch.Tensor:
     """y[M, N] = x[M, K] @ W^T with W from (qw [N, K/8], st [N, K/32]).
 
     path: None (the library's choice), "cuda" (CUDA cores) or "tensor"
     (tcgen05 tensor cores; K a multiple of 256).
     silu_mul: x is [M, 2K] (gate then up) and the product takes
-    silu(gate) * up, formed while the activations are staged."""
+    silu(gate) * up, formed while the activations are staged.
+    l2_next: up to 4 (tensor or address, bytes) ranges, normally the next
+    call's codes and steps, brought into L2 once this call has requested its
+    own weights (w4a16_gemv_prefetch_l2)."""
     qw = _as_words(qw)
     _need(qw, qw.dtype, "qw")
     _need(st, torch.bfloat16, "st")
@@ -231,6 +258,15 @@ def gemv(qw: torch.Tensor, st: torch.Tensor, x: torch.Tensor, y: torch.Tensor = 
         raise ValueError(f"this shape needs a zero-filled workspace of {need} bytes")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     flags = (W4_FLAG_PDL if pdl else 0) | _PATH_FLAGS[path] | (W4_FLAG_SILU_MUL if silu_mul else 0)
+    if l2_next:
+        if len(l2_next) > W4_MAX_L2_RANGES:
+            raise ValueError(f"at most {W4_MAX_L2_RANGES} prefetch ranges")
+        rs = l2_next if isinstance(l2_next, ctypes.Array) else l2_ranges(l2_next)
+        _check(load().w4a16_gemv_prefetch_l2(_ptr(y), _ptr(qw), _ptr(st), _ptr(x2), M, N, K,
+                                             _ptr(workspace), ws_bytes, _ptr(status), flags, rs,
+                                             len(rs), _stream(stream)),
+               "w4a16_gemv_prefetch_l2")
+        return y
     _check(load().w4a16_gemv(_ptr(y), _ptr(qw), _ptr(st), _ptr(x2), M, N, K, _ptr(workspace),
                              ws_bytes, _ptr(status), flags, _stream(stream)),
            "w4a16_gemv")

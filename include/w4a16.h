@@ -174,6 +174,50 @@ size_t w4a16_gemv_workspace_bytes(int M, int N, int K);
 size_t w4a16_gemv_workspace_bytes_flags(int M, int N, int K, unsigned flags);
 
 /*
+ * w4a16_gemv_prefetch_l2 — w4a16_gemv that also brings the next call's
+ * weights into L2 while it finishes.
+ *
+ * Page "Running a 26B MoE on an 8 GB Jetson by streaming experts from SSD",
+ * section on hiding the expert reads: the reads for the next piece of work
+ * are started while the GPU computes work it had to do anyway, and are
+ * joined only where that data is needed.  On GB300 the same overlap applies
+ * between HBM and L2.  A decode pass is a chain of GEMV launches, each
+ * reading the previous one's output.  Each launch's CTAs stay on their SMs
+ * until their last rows are summed, and the next launch's copies cannot
+ * start until those SMs free up, so HBM idles at every launch boundary.
+ * Weights do not depend on earlier results.  So once every CTA of this
+ * call's last launch has requested its own weight tiles, it asks L2 to fetch
+ * its share of the given byte ranges (normally the leading rows of the next
+ * call's codes and steps).  The next call then finds them in L2.
+ *
+ * Arguments, layouts, results and errors are those of w4a16_gemv (the same
+ * bits for the same inputs); the ranges change timing only.
+ *
+ * ranges    host array of n_ranges {ptr, bytes} (read during the call, not
+ *           kept).  ptr is a device address, 16-byte aligned (W4_ERR_ALIGN);
+ *           a range of 0 bytes may have a NULL ptr.  Bytes past the last
+ *           multiple of 16 of a range are not fetched.  The ranges are only
+ *           read by L2 prefetches, never written, and must stay allocated
+ *           until the call's kernels have finished.
+ * n_ranges  0 .. W4_MAX_L2_RANGES (0: exactly w4a16_gemv).
+ *
+ * Size the ranges so that they still fit L2 together with what the next
+ * call reads first.  Prefetched lines that are evicted before use are read
+ * from HBM again.  Prompt chunks (M > 32, one launch of the prompt GEMM)
+ * take no prefetch.
+ */
+#define W4_MAX_L2_RANGES 4
+typedef struct w4_l2_range {
+    const void *ptr;
+    size_t bytes;
+} w4_l2_range;
+
+w4_status w4a16_gemv_prefetch_l2(void *y, const void *qw, const void *st, const void *x,
+                                 int M, int N, int K, void *workspace, size_t workspace_bytes,
+                                 int32_t *status_dev, unsigned flags,
+                                 const w4_l2_range *ranges, int n_ranges, w4_stream_t stream);
+
+/*
  * w4a16_gemv_static_scratch — w4a16_gemv without a caller-provided workspace.
  *
  * No passage of the source pages corresponds to this call; it exists for

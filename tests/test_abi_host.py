@@ -92,6 +92,21 @@ def test_host_validation_rejects_before_any_launch(L):
     assert sgemv(good, good, good, good, 1, 16, 256, None, 8 | 4, None) == 3
     assert sgemv(good, good, good, good, 1, 16, 48, None, 8, None) == 3
     assert sgemv(None, good, good, good, 1, 16, 64, None, 8, None) == 1
+    # the L2-prefetching GEMV: range count, null and misaligned ranges, then
+    # w4a16_gemv's own checks
+    pf = L.w4a16_gemv_prefetch_l2
+    R = lib.l2_ranges
+    ok2 = R([(1 << 22, 4096), (1 << 23, 100)])
+    assert pf(good, good, good, good, 1, 16, 64, None, 0, None, 0, ok2, -1, None) == 1
+    assert pf(good, good, good, good, 1, 16, 64, None, 0, None, 0, ok2, 5, None) == 1
+    assert pf(good, good, good, good, 1, 16, 64, None, 0, None, 0, None, 1, None) == 1
+    assert pf(good, good, good, good, 1, 16, 64, None, 0, None, 0,
+              R([(0, 64)]), 1, None) == 1                                     # null with bytes
+    assert pf(good, good, good, good, 1, 16, 64, None, 0, None, 0,
+              R([((1 << 22) + 8, 64)]), 1, None) == 2                         # misaligned
+    assert pf(good, good, good, good, 1, 16, 48, None, 0, None, 0, ok2, 2, None) == 3
+    assert pf(None, good, good, good, 1, 16, 64, None, 0, None, 0, ok2, 2, None) == 1
+    assert pf(good, good, good, good, 1, 16, 64, None, 0, None, 16, ok2, 2, None) == 1
     assert L.w4_embed_gather(good, good, good, good, 0, 10, 64, None, 0, None) == 1
     assert L.w4_pack(good, good, 4, 40, None, None) == 3
     assert L.w4_quantize(good, good, vp((1 << 20) + 4), 4, 64, None) == 2

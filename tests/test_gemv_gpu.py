@@ -169,6 +169,32 @@ def test_gemv_pdl_flag_same_bits(cuda_lib):
         assert torch.equal(y.view(torch.int16), y0.view(torch.int16))
 
 
+@pytest.mark.parametrize("m,n,k", [(1, 1500, 2048), (5, 300, 2048), (16, 2048, 2048),
+                                   (1, 700, 21504)])
+def test_prefetch_l2_same_bits(cuda_lib, m, n, k):
+    # w4a16_gemv_prefetch_l2 changes timing only: the same bits as
+    # w4a16_gemv on every path (CUDA cores with one and two launches, the
+    # tensor-core small batch, split-K), whole and ragged ranges, and the
+    # prefetched tensors are left as they were
+    rng = np.random.default_rng(m * 7 + n + k)
+    qw_h, st_h, x_h = make(rng, n, k, m)
+    qw, st, x = dev_words(qw_h), dev_bf16(st_h), dev_bf16(x_h)
+    nq, ns = dev_words(synth.np_words(rng, (900, 1024 // 8))), dev_bf16(
+        synth.np_steps(rng, (900, 1024 // 32)))
+    nq0, ns0 = nq.clone(), ns.clone()
+    need = lib.workspace_bytes(m, n, k)
+    ws = torch.zeros(max(need, 16), dtype=torch.uint8, device="cuda") if need else None
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y0 = lib.gemv(qw, st, x, workspace=ws, status=status)
+    for ranges in ([(nq, None), (ns, None)], [(nq, 1000), (ns, 37)], [(ns, 8)],
+                   [(nq, None), (ns, None), (qw, None), (st, None)]):
+        y = lib.gemv(qw, st, x, workspace=ws, status=status, pdl=True, l2_next=ranges)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert torch.equal(y.view(torch.int16), y0.view(torch.int16))
+    assert torch.equal(nq, nq0) and torch.equal(ns.view(torch.int16), ns0.view(torch.int16))
+
+
 def test_gemv_unaligned_output_view_and_guard_band(cuda_lib):
     rng = np.random.default_rng(9)
     n, k = 100, 2048
