@@ -1486,16 +1486,29 @@ int path_of(int M, int K, unsigned flags) {
   return (M >= kTcMinM && tc_shape(K)) ? 1 : 0;
 }
 
-// Largest workspace of the tensor-core launches of an (M, N, K) call.
-size_t tc_workspace(int M, int N, int K, int sms) {
+// Largest workspace of the tensor-core launches of an (M, N, K) call: with
+// allow_sk the size that lets every launch take balanced runs, without it
+// the size the call cannot run without (split-K).
+size_t tc_workspace(int M, int N, int K, int sms, bool allow_sk = true) {
   tc::TpPlan pp;
   if (M > tc::kTcMaxM && tc::tp_plan(M, N, K, sms, &pp)) return 0;   // one prompt launch
   size_t ws = 0;
   for (int m0 = 0; m0 < M; m0 += tc::kTcMaxM) {
     tc::TcPlan tp;
-    if (tc::tc_plan(std::min(tc::kTcMaxM, M - m0), N, K, sms, &tp)) ws = std::max(ws, tp.ws_bytes);
+    if (tc::tc_plan(std::min(tc::kTcMaxM, M - m0), N, K, sms, &tp, allow_sk))
+      ws = std::max(ws, tp.ws_bytes);
   }
   return ws;
+}
+
+// The plan of one small-batch launch: balanced runs when the workspace
+// holds their hand-over slots, else the plain plan (the same bits).
+bool tc_launch_plan(int M, int N, int K, int sms, const void* workspace, size_t workspace_bytes,
+                    tc::TcPlan* tp) {
+  if (!tc::tc_plan(M, N, K, sms, tp)) return false;
+  if (tp->sk && (workspace == nullptr || workspace_bytes < tp->ws_bytes || !aligned(workspace, 16)))
+    return tc::tc_plan(M, N, K, sms, tp, false);
+  return true;
 }
 
 // Enqueue the tensor-core launches of a call (up to 32 activation rows each).
@@ -1516,7 +1529,8 @@ w4_status tc_enqueue(void* y, const void* qw, const void* st, const void* x, int
   // every launch of the call is checked before the first one is enqueued
   for (int m0 = 0; m0 < M; m0 += tc::kTcMaxM) {
     tc::TcPlan tp;
-    if (!tc::tc_plan(std::min(tc::kTcMaxM, M - m0), N, K, sms, &tp)) return W4_ERR_SHAPE;
+    if (!tc_launch_plan(std::min(tc::kTcMaxM, M - m0), N, K, sms, workspace, workspace_bytes, &tp))
+      return W4_ERR_SHAPE;
     if (tp.ws_bytes > 0 && (workspace == nullptr || workspace_bytes < tp.ws_bytes))
       return W4_ERR_WORKSPACE;
     if (tp.ws_bytes > 0 && !aligned(workspace, 16)) return W4_ERR_ALIGN;
@@ -1524,7 +1538,7 @@ w4_status tc_enqueue(void* y, const void* qw, const void* st, const void* x, int
   for (int m0 = 0; m0 < M; m0 += tc::kTcMaxM) {
     const int mr = std::min(tc::kTcMaxM, M - m0);
     tc::TcPlan tp;
-    tc::tc_plan(mr, N, K, sms, &tp);
+    tc_launch_plan(mr, N, K, sms, workspace, workspace_bytes, &tp);
     const cudaError_t e =
         tc::tc_launch(tp, static_cast<__nv_bfloat16*>(y) + (long long)m0 * N, qw, st,
                       static_cast<const __nv_bfloat16*>(x) + (long long)m0 * K, mr, N, K, workspace,
@@ -1588,6 +1602,7 @@ extern "C" w4_status w4a16_gemv_plan(int M, int N, int K, w4_plan_info* info) {
     info->ctas_per_sm = tp.per_sm;
     info->tmpl_team = tp.np;
     info->tmpl_chunk = 0;
+    info->dynamic_windows = tp.sk;   // balanced runs (needs the full workspace)
     return W4_OK;
   }
   Plan pl;
@@ -1893,7 +1908,8 @@ extern "C" w4_status w4a16_gemv_static_scratch(void* y, const void* qw, const vo
   if (!current_device(&dev, &di)) return W4_ERR_DEVICE;
   if (path == 1) {
     // every launch of this call must fit the fixed array: check before any work
-    const size_t need = tc_workspace(M, N, K, di.sms);
+    // (the plain plans: balanced runs are not taken here)
+    const size_t need = tc_workspace(M, N, K, di.sms, false);
     if (need > (size_t)W4_STATIC_SCRATCH_BYTES) return W4_ERR_WORKSPACE;
     void* base = nullptr;
     if (need > 0) {

@@ -82,7 +82,108 @@ struct TcParams {
   int* ws_count;          // [tiles]
   int32_t* status;
   L2Ranges l2;            // brought into L2 after the launch's own tiles
+  // Balanced runs (S == 1): the tiles x slices work items cut into equal
+  // runs per CTA; a tile cut between CTAs c and c + 1 hands its rows' sum
+  // over its first slices (exactly the prefix of the unsplit sum) from c to
+  // c + 1 through prefix slot c.
+  int sk;
+  int* sk_flag;           // [ctas] 1 while prefix slot c holds a prefix
+  float* sk_prefix;       // [ctas][M][128]
 };
+
+// The work of one CTA as a list of segments: (tile, slices [b, e), kind).
+constexpr int kSegWhole = 0;   // a whole tile (or all of it a split covers, S == 1): write y
+constexpr int kSegSplit = 1;   // a K split of a tile (S > 1): slice partials, last CTA adds
+constexpr int kSegHead = 2;    // a tile's first slices: publish the prefix for the next CTA
+constexpr int kSegTail = 3;    // a tile's last slices: continue from the published prefix
+struct Seg {
+  int t, b, e, kind;
+};
+struct Segs {
+  int n;                  // segments of this CTA
+  int u0;                 // first unit (K-split plans)
+  int head_t, head_e;     // balanced runs: head tile (-1: none) and its end slice
+  int wb;                 // first whole tile
+  int nw;                 // whole tiles
+  int tail_t, tail_b;     // tail tile (-1: none) and its first slice
+};
+// Balanced runs: the CTA's items [w0, w1) of tile-major (tile, slice) items.
+// Its last tile, if cut, is processed FIRST (its prefix is published early,
+// so that the next CTA never waits long), then the whole tiles, then its
+// first tile's last slices (behind the previous CTA's prefix).  Each run
+// holds at least one tile's worth of items, so a tile is cut at most once.
+__device__ __forceinline__ Segs segs_of(const TcParams& p) {
+  Segs g{};
+  g.head_t = g.tail_t = -1;
+  if (p.sk) {
+    const long long W = (long long)p.tiles * p.slices;
+    const int w0 = (int)((long long)blockIdx.x * W / gridDim.x);
+    const int w1 = (int)((long long)(blockIdx.x + 1) * W / gridDim.x);
+    const int tf = w0 / p.slices, k0 = w0 - tf * p.slices;
+    const int tl = (w1 - 1) / p.slices, j1 = w1 - tl * p.slices;   // slices [0, j1) of tl
+    if (j1 < p.slices) {
+      g.head_t = tl;
+      g.head_e = j1;
+    }
+    if (k0 > 0) {
+      g.tail_t = tf;
+      g.tail_b = k0;
+    }
+    g.wb = k0 > 0 ? tf + 1 : tf;
+    g.nw = max(0, (j1 < p.slices ? tl : tl + 1) - g.wb);
+    g.n = (g.head_t >= 0) + g.nw + (g.tail_t >= 0);
+  } else {
+    g.u0 = (int)((long long)blockIdx.x * p.units / gridDim.x);
+    g.n = (int)((long long)(blockIdx.x + 1) * p.units / gridDim.x) - g.u0;
+  }
+  return g;
+}
+__device__ __forceinline__ Seg seg_at(const TcParams& p, const Segs& g, int i) {
+  if (p.sk) {
+    if (g.head_t >= 0) {
+      if (i == 0) return Seg{g.head_t, 0, g.head_e, kSegHead};
+      --i;
+    }
+    if (i < g.nw) return Seg{g.wb + i, 0, p.slices, kSegWhole};
+    return Seg{g.tail_t, g.tail_b, p.slices, kSegTail};
+  }
+  const int u = g.u0 + i;
+  const int s = u / p.tiles, t = u - s * p.tiles;
+  const int b = s * p.sps;
+  return Seg{t, b, min(b + p.sps, p.slices), p.S == 1 ? kSegWhole : kSegSplit};
+}
+
+// Balanced runs' hand-over flag: a release store, and a bounded acquire
+// wait (false after about a second, or once the CTA has aborted).
+__device__ __forceinline__ void store_release_gpu(int* f, int v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+__device__ __forceinline__ bool wait_flag_gpu(const int* f, volatile int* abort_flag) {
+  const long long t0 = clock64();
+  while (true) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    if (v != 0) return true;
+    if (*abort_flag != 0) return false;
+    if (clock64() - t0 > kWaitCycles) return false;
+    __nanosleep(64);
+  }
+}
+
+// Row `tid`'s prefix from slot blockIdx.x - 1 (the previous CTA's part of
+// this tile), its M values read once and cleared: the workspace is left
+// zero-filled, as every completed call leaves it.
+template <int MC>
+__device__ __forceinline__ void take_prefix(const TcParams& p, int tid, float* v) {
+  float* slot = p.sk_prefix + (long long)(blockIdx.x - 1) * p.M * kRows + tid;
+#pragma unroll
+  for (int m = 0; m < MC; ++m) {
+    if (m < p.M) {
+      v[m] = __ldcg(slot + (long long)m * kRows);
+      slot[(long long)m * kRows] = 0.0f;
+    }
+  }
+}
 
 // MMA width (activation columns, 16 or 32) and groups per round for MC
 // columns of results.
@@ -167,8 +268,7 @@ __global__ void __launch_bounds__(kThreads, kBufs >= 4 ? 1 : 2)
   pdl_launch_dependents();
   pdl_wait();   // activations and outputs follow earlier kernels
 
-  const int u0 = (int)((long long)blockIdx.x * p.units / gridDim.x);
-  const int u1 = (int)((long long)(blockIdx.x + 1) * p.units / gridDim.x);
+  const Segs segs = segs_of(p);
 
   if (warp == kCopyWarp) {
     // ------------------------------------------------------------ producer
@@ -176,9 +276,9 @@ __global__ void __launch_bounds__(kThreads, kBufs >= 4 ? 1 : 2)
     int slot = 0, issued = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int u = u0; u < u1 && ok; ++u) {
-      const int s = u / p.tiles, t = u - s * p.tiles;
-      const int sl0 = s * p.sps, sl1 = min(sl0 + p.sps, p.slices);
+    for (int i = 0; i < segs.n && ok; ++i) {
+      const Seg sg = seg_at(p, segs, i);
+      const int t = sg.t, sl0 = sg.b, sl1 = sg.e;
       for (int sl = sl0; sl < sl1; ++sl) {
         if (issued >= nst && !wait_bar(empty0 + 8 * slot, phase ^ 1u, abort_flag)) {
           if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
@@ -223,9 +323,9 @@ __global__ void __launch_bounds__(kThreads, kBufs >= 4 ? 1 : 2)
     int slot = 0;
     long long r = 0;
     bool ok = true;
-    for (int u = u0; u < u1 && ok; ++u) {
-      const int s = u / p.tiles;
-      const int sl0 = s * p.sps, sl1 = min(sl0 + p.sps, p.slices);
+    for (int i = 0; i < segs.n && ok; ++i) {
+      const Seg sg = seg_at(p, segs, i);
+      const int sl0 = sg.b, sl1 = sg.e;
       for (int sl = sl0; sl < sl1 && ok; ++sl) {
         const uint32_t stg = st0 + slot * p.stage_bytes;
         for (int q = 0; q < kRounds; ++q, ++r) {
@@ -276,9 +376,9 @@ __global__ void __launch_bounds__(kThreads, kBufs >= 4 ? 1 : 2)
     uint32_t phase = 0;
     long long r = 0;
     bool ok = true;
-    for (int u = u0; u < u1 && ok; ++u) {
-      const int s = u / p.tiles;
-      const int sl0 = s * p.sps, sl1 = min(sl0 + p.sps, p.slices);
+    for (int i = 0; i < segs.n && ok; ++i) {
+      const Seg sg = seg_at(p, segs, i);
+      const int sl0 = sg.b, sl1 = sg.e;
       for (int sl = sl0; sl < sl1 && ok; ++sl) {
         if (!wait_bar(full0 + 8 * slot, phase, abort_flag)) {
           ok = false;
@@ -329,9 +429,10 @@ __global__ void __launch_bounds__(kThreads, kBufs >= 4 ? 1 : 2)
     long long r = 0;
     float acc[MC], rowsum[kTmemSum ? 1 : MC];
     bool ok = true;
-    for (int u = u0; u < u1 && ok; ++u) {
-      const int s = u / p.tiles, t = u - s * p.tiles;
-      const int sl0 = s * p.sps, sl1 = min(sl0 + p.sps, p.slices);
+    for (int i = 0; i < segs.n && ok; ++i) {
+      const Seg sg = seg_at(p, segs, i);
+      const int t = sg.t, sl0 = sg.b, sl1 = sg.e;
+      const bool direct = sg.kind != kSegSplit;   // the row sum stays in this CTA
       const int row = t * kRows + tid;
       if constexpr (!kTmemSum) {
 #pragma unroll
@@ -384,13 +485,26 @@ __global__ void __launch_bounds__(kThreads, kBufs >= 4 ? 1 : 2)
         // the slice is done: its sum goes on, its stage back to the copy warp
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * slot);
-        if (p.S == 1) {
+        // a tile's last slices continue from the previous CTA's prefix (the
+        // same sum, in the same order, as if this CTA had run every slice)
+        const bool from_prefix = sg.kind == kSegTail && sl == sl0;
+        if (from_prefix) {
+          if (tid == 0) *last_flag = wait_flag_gpu(p.sk_flag + blockIdx.x - 1, abort_flag) ? 1 : 0;
+          asm volatile("bar.sync 1, %0;" ::"n"(kRows) : "memory");
+          if (*last_flag == 0) {
+            ok = false;
+            break;
+          }
+        }
+        if (direct) {
           if constexpr (kTmemSum) {
-            // sum (from 0) of the slices so far, kept in tensor memory
+            // sum (from 0, or from the prefix) of the slices so far, kept
+            // in tensor memory
             float sum[MC];
             if (sl == sl0) {
 #pragma unroll
               for (int m = 0; m < MC; ++m) sum[m] = 0.0f;
+              if (from_prefix) take_prefix<MC>(p, tid, sum);
             } else {
               tmem_ld<MC>(tmem + lane_base + kSumCol, sum);
               tmem_wait_ld<MC>(sum);
@@ -402,6 +516,7 @@ __global__ void __launch_bounds__(kThreads, kBufs >= 4 ? 1 : 2)
             for (int c = 0; c < MC; c += 16) tmem_st16(tmem + lane_base + kSumCol + c, v + c);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
           } else {
+            if (from_prefix) take_prefix<MC>(p, tid, rowsum);
 #pragma unroll
             for (int m = 0; m < MC; ++m) rowsum[m] += acc[m];
           }
@@ -416,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, kBufs >= 4 ? 1 : 2)
         }
       }
       if (!ok) break;
-      if (p.S == 1) {
+      if (direct) {
         float* sum = rowsum;
         float tsum[kTmemSum ? MC : 1];
         if constexpr (kTmemSum) {
@@ -424,10 +539,29 @@ __global__ void __launch_bounds__(kThreads, kBufs >= 4 ? 1 : 2)
           tmem_wait_ld<MC>(tsum);
           sum = tsum;
         }
+        if (sg.kind == kSegHead) {
+          // the tile's first slices: their sum (every row of the tile) goes
+          // to prefix slot blockIdx.x for the next CTA.  The barrier orders
+          // all rows' stores before thread 0's release of the flag.
+          float* out = p.sk_prefix + (long long)blockIdx.x * p.M * kRows + tid;
+#pragma unroll
+          for (int m = 0; m < MC; ++m)
+            if (m < p.M) out[(long long)m * kRows] = sum[m];
+          __threadfence();
+          asm volatile("bar.sync 1, %0;" ::"n"(kRows) : "memory");
+          if (tid == 0) store_release_gpu(p.sk_flag + blockIdx.x, 1);
+          continue;
+        }
         if (row < p.N) {
 #pragma unroll
           for (int m = 0; m < MC; ++m)
             if (m < p.M) p.y[(long long)m * p.N + row] = __float2bfloat16_rn(sum[m]);
+        }
+        if (sg.kind == kSegTail) {
+          // every row has read the prefix (at the first slice): the slot is
+          // re-armed for the next call
+          asm volatile("bar.sync 1, %0;" ::"n"(kRows) : "memory");
+          if (tid == 0) p.sk_flag[blockIdx.x - 1] = 0;
         }
         continue;
       }
@@ -583,7 +717,7 @@ bool tc_supported(int M, int K) {
   return M >= 1 && M <= kTcMaxM && K >= kSliceK && K % kSliceK == 0 && encoder() != nullptr;
 }
 
-bool tc_plan(int M, int N, int K, int sms, TcPlan* out) {
+bool tc_plan(int M, int N, int K, int sms, TcPlan* out, bool allow_sk) {
   if (M < 1 || M > kTcMaxM || K % kSliceK != 0 || N < 1) return false;
   TcPlan pl;
   pl.np = M <= 16 ? 16 : 32;
@@ -622,6 +756,20 @@ bool tc_plan(int M, int N, int K, int sms, TcPlan* out) {
   if (pl.S > 1) {
     pl.ws_part_off = ((size_t)pl.tiles * sizeof(int) + 255) & ~size_t(255);
     pl.ws_bytes = pl.ws_part_off + (size_t)pl.slices * M * N * sizeof(float);
+  }
+  // Balanced runs when whole tiles divide badly over the CTAs: the busiest
+  // CTA's tiles at least 1.25x the mean (measured at 43008 x 5376, M = 16:
+  // 336 tiles on 304 CTAs took 78.6 us, 304 tiles 48.3 us, 608 tiles
+  // 82.2 us; balanced runs 56-57 us; near 1.19x the two plans are within
+  // +-8% either way).  Every run covers at least one tile's slices, so a
+  // tile is cut at most once; needs the hand-over slots.
+  const long long busiest = (pl.tiles + pl.ctas - 1) / pl.ctas;
+  if (allow_sk && pl.S == 1 && pl.slices >= 2 && pl.tiles > pl.ctas &&
+      4LL * busiest * pl.ctas >= 5LL * pl.tiles &&
+      (long long)pl.tiles * pl.slices / pl.ctas >= pl.slices) {
+    pl.sk = 1;
+    pl.ws_part_off = ((size_t)pl.ctas * sizeof(int) + 255) & ~size_t(255);
+    pl.ws_bytes = pl.ws_part_off + (size_t)pl.ctas * M * kRows * sizeof(float);
   }
   *out = pl;
   return true;
@@ -681,6 +829,11 @@ cudaError_t tc_launch(const TcPlan& pl, void* y, const void* qw, const void* st,
   p.xrows = M;
   p.status = status;
   if (l2 != nullptr) p.l2 = *l2;
+  if (pl.sk) {
+    p.sk = 1;
+    p.sk_flag = static_cast<int*>(workspace);
+    p.sk_prefix = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.ws_part_off);
+  }
   if (pl.S > 1) {
     p.ws_count = static_cast<int*>(workspace);
     p.ws_partial = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.ws_part_off);

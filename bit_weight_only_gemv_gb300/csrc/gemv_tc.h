@@ -19,6 +19,8 @@ struct TcPlan {
   int S = 1, sps = 1, units = 0, ctas = 0;
   int nst = 2, stage_bytes = 0, off_b = 0, smem = 0;
   int bufs = 2, per_sm = 2;   // rounds held in tensor memory; CTAs per SM
+  int sk = 0;                 // balanced runs per CTA (tiles cut between CTAs hand
+                              // their row sums over through the workspace)
   size_t ws_bytes = 0, ws_part_off = 0;
 };
 
@@ -26,7 +28,9 @@ struct TcPlan {
 // (K a multiple of 256, M <= kTcMaxM, tensor-map encoder available).
 bool tc_supported(int M, int K);
 
-bool tc_plan(int M, int N, int K, int sms, TcPlan* out);
+// allow_sk: plan balanced runs where they apply (they need ws_bytes of
+// workspace; the plain plan computes the same bits without it).
+bool tc_plan(int M, int N, int K, int sms, TcPlan* out, bool allow_sk = true);
 
 // l2: byte ranges the copy warps bring into L2 once their own tiles are
 // requested (w4a16_gemv_prefetch_l2), or nullptr.

@@ -138,7 +138,12 @@ const char *w4_last_cuda_error(void);
  *            bytes (16-byte aligned), or NULL when that is 0.  It must be
  *            zero-filled before its first use; every call that completes
  *            without a device-side error leaves it zero-filled again.  Calls
- *            that may run concurrently need separate workspaces.
+ *            that may run concurrently need separate workspaces.  On the
+ *            tensor-core small-batch path a call whose row tiles do not
+ *            divide evenly over the CTAs uses the workspace for balanced runs
+ *            (w4_plan_info.dynamic_windows); given less (or NULL) it runs the
+ *            plain plan instead, with the same bits, and returns an error only
+ *            when a K split needs the workspace.
  * status_dev device int32 for device-side errors (W4_ERR_TIMEOUT), or NULL.
  * flags      W4_FLAG_PDL, and at most one of W4_FLAG_CUDA_CORES /
  *            W4_FLAG_TENSOR_CORES (default: tensor cores from M = 8 when K is
@@ -510,9 +515,14 @@ typedef struct w4_plan_info {
     int ctas_per_sm;    /* resident CTAs per SM the plan is sized for */
     int tmpl_team;      /* team size compiled into the kernel (0: generic) */
     int tmpl_chunk;     /* chunk steps compiled into the kernel (0: generic) */
-    int dynamic_windows; /* 1: CTAs take windows of unit_rows rows from a counter at
-                            run time (dense calls with many windows per CTA, and
-                            routed calls with many windows, within one id each) */
+    int dynamic_windows; /* path 1: CTAs take windows of unit_rows rows from a
+                            counter at run time (dense calls with many windows per
+                            CTA, and routed calls with many windows, within one id
+                            each).  path 2: balanced runs, each CTA an equal share
+                            of the (128-row tile, 256-code slice) work; a tile cut
+                            between two CTAs hands its rows' running sums over
+                            through the workspace (taken only when the call's
+                            workspace is w4a16_gemv_workspace_bytes large) */
 } w4_plan_info;
 
 w4_status w4a16_gemv_plan(int M, int N, int K, w4_plan_info *info);

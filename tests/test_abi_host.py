@@ -184,7 +184,7 @@ def test_tensor_core_plan_is_valid(M, N, K):
         assert p["smem_bytes"] > 233472 // 2
     tiles, slices = -(-N // 128), K // 256
     assert 1 <= p["slices"] <= slices
-    assert (lib.workspace_bytes(M, N, K) > 0) == (p["slices"] > 1)
+    assert (lib.workspace_bytes(M, N, K) > 0) == (p["slices"] > 1 or p["dynamic_windows"] == 1)
     assert lib.workspace_bytes(M, N, K, "tensor") == lib.workspace_bytes(M, N, K)
 
 
@@ -326,9 +326,71 @@ def test_planner_sweep_of_random_shapes():
         if want == 1:
             assert ws > 0 or p["slices"] == 1, (M, N, K, p, ws)
         else:
-            assert (ws > 0) == (p["slices"] > 1), (M, N, K, p, ws)
+            # (or the hand-over slots of balanced runs)
+            assert (ws > 0) == (p["slices"] > 1 or p["dynamic_windows"] == 1), (M, N, K, p, ws)
         # a call pinned to either path is planned too (tensor cores: K % 256 == 0)
         assert lib.workspace_bytes(M, N, K, "cuda") >= 0
         if K % 256 == 0:
             assert lib.workspace_bytes(M, N, K, "tensor") == (ws if want != 1 else
                                                              lib.workspace_bytes(M, N, K, "tensor"))
+
+
+def tc_segments(c, G, tiles, slices):
+    """The tensor-core kernel's balanced runs for CTA c of G (its segment
+    arithmetic, replayed): [(tile, first slice, end slice, kind)]."""
+    W = tiles * slices
+    w0, w1 = c * W // G, (c + 1) * W // G
+    tf, k0 = divmod(w0, slices)
+    tl = (w1 - 1) // slices
+    j1 = w1 - tl * slices
+    segs = []
+    if j1 < slices:
+        segs.append((tl, 0, j1, "head"))
+    wb = tf + 1 if k0 > 0 else tf
+    we = tl if j1 < slices else tl + 1
+    segs += [(t, 0, slices, "whole") for t in range(wb, max(wb, we))]
+    if k0 > 0:
+        segs.append((tf, k0, slices, "tail"))
+    return segs
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 43008, 5376), (32, 65536, 2048), (8, 40900, 1024),
+                                   (16, 39680, 1024), (32, 131072, 2048), (9, 77824 - 64, 512),
+                                   (32, 38990, 2048), (1, 43008, 5376)])
+def test_tensor_core_balanced_runs_cover_every_item_once(M, N, K):
+    p = lib.plan(M, N, K)
+    if p["path"] != 2:   # batch 1 stays on the CUDA cores
+        return
+    tiles, slices, G = -(-N // 128), K // 256, p["ctas"]
+    if not p["dynamic_windows"]:
+        assert tiles <= G or 4 * -(-tiles // G) * G < 5 * tiles or slices < 2
+        return
+    assert p["ctas_per_sm"] == 2 and tiles > G and tiles * slices // G >= slices
+    # workspace: one flag per CTA (256-byte aligned), then a prefix slot of
+    # M x 128 fp32 per CTA
+    assert lib.workspace_bytes(M, N, K) == (-(-G * 4 // 256)) * 256 + G * M * 128 * 4
+    seen = {}
+    heads, tails = {}, {}
+    for c in range(G):
+        segs = tc_segments(c, G, tiles, slices)
+        kinds = [k for *_, k in segs]
+        # the head (if any) first, the tail (if any) last, whole tiles between
+        assert kinds.count("head") <= 1 and kinds.count("tail") <= 1
+        if "head" in kinds:
+            assert kinds[0] == "head"
+        if "tail" in kinds:
+            assert kinds[-1] == "tail" and c > 0
+        for t, b, e, k in segs:
+            assert 0 <= t < tiles and 0 <= b < e <= slices
+            for sl in range(b, e):
+                assert (t, sl) not in seen
+                seen[(t, sl)] = c
+            if k == "head":
+                heads[c] = (t, e)
+            if k == "tail":
+                tails[c] = (t, b)
+    assert len(seen) == tiles * slices
+    # every cut tile: its head in CTA c (prefix slot c), its tail in CTA c + 1
+    assert len(heads) == len(tails)
+    for c, (t, b) in tails.items():
+        assert heads[c - 1] == (t, b)

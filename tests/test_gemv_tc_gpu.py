@@ -68,6 +68,36 @@ def test_cuda_core_path_pinned_at_large_m(cuda_lib):
     assert_gemv_parity(y, qw_h, st_h, x_h)
 
 
+@pytest.mark.parametrize("n,k,m", [(40900, 1024, 8), (39680, 1024, 16), (38990, 2048, 32),
+                                   (43008, 5376, 16)])
+def test_balanced_runs_equal_the_plain_plan(cuda_lib, n, k, m):
+    # Row tiles that do not divide evenly over the CTAs: each CTA takes an
+    # equal run of (tile, slice) work and a tile cut between two CTAs hands
+    # its rows' running sums over.  With the full workspace the call runs
+    # that plan, without it the plain one: the same bits, within the bound,
+    # every output written (ragged last tile included), the workspace left
+    # zero-filled, and again on a second call (the hand-over flags re-armed).
+    p = lib.plan(m, n, k)
+    assert p["path"] == 2 and p["dynamic_windows"] == 1
+    rng = np.random.default_rng(n + k + m)
+    qw_h, st_h, x_h = make(rng, n, k, m)
+    qw, st, x = dev_words(qw_h), dev_bf16(st_h), dev_bf16(x_h)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y0 = poison_bf16((m, n))
+    lib.gemv(qw, st, x, y=y0, status=status)                 # no workspace: plain plan
+    ws = torch.zeros(lib.workspace_bytes(m, n, k), dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        y = poison_bf16((m, n))
+        lib.gemv(qw, st, x, y=y, workspace=ws, status=status, pdl=True)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert torch.equal(y.view(torch.int16), y0.view(torch.int16))
+        assert int(ws.count_nonzero().item()) == 0          # flags and prefix slots cleared
+    rows = np.unique(np.concatenate([np.arange(0, n, max(1, n // 700)), np.arange(n - 200, n)]))
+    assert_gemv_parity(y, qw_h, st_h, x_h, rows=rows)
+    assert not np.any(host_bits(y) == POISON)
+
+
 def test_tensor_core_rows_do_not_depend_on_n_or_split(cuda_lib):
     # The same 128 rows alone (16 K splits), among 8192 rows (4 splits) and
     # among 40960 rows (no split): the per-row association (groups in order
