@@ -112,10 +112,11 @@ struct Segs {
 // so that the next CTA never waits long), then the whole tiles, then its
 // first tile's last slices (behind the previous CTA's prefix).  Each run
 // holds at least one tile's worth of items, so a tile is cut at most once.
+template <bool SK>
 __device__ __forceinline__ Segs segs_of(const TcParams& p) {
   Segs g{};
   g.head_t = g.tail_t = -1;
-  if (p.sk) {
+  if constexpr (SK) {
     const long long W = (long long)p.tiles * p.slices;
     const int w0 = (int)((long long)blockIdx.x * W / gridDim.x);
     const int w1 = (int)((long long)(blockIdx.x + 1) * W / gridDim.x);
@@ -138,19 +139,21 @@ __device__ __forceinline__ Segs segs_of(const TcParams& p) {
   }
   return g;
 }
+template <bool SK>
 __device__ __forceinline__ Seg seg_at(const TcParams& p, const Segs& g, int i) {
-  if (p.sk) {
+  if constexpr (SK) {
     if (g.head_t >= 0) {
       if (i == 0) return Seg{g.head_t, 0, g.head_e, kSegHead};
       --i;
     }
     if (i < g.nw) return Seg{g.wb + i, 0, p.slices, kSegWhole};
     return Seg{g.tail_t, g.tail_b, p.slices, kSegTail};
-  }
+  } else {
   const int u = g.u0 + i;
   const int s = u / p.tiles, t = u - s * p.tiles;
   const int b = s * p.sps;
   return Seg{t, b, min(b + p.sps, p.slices), p.S == 1 ? kSegWhole : kSegSplit};
+  }
 }
 
 // Balanced runs' hand-over flag: a release store, and a bounded acquire
@@ -202,7 +205,9 @@ __host__ __device__ constexpr int tmem_cols(int np, int g, int bufs) {
 // warp 8 copies, warp 9 issues MMAs.  Per round (G groups) the four roles
 // hand off through mbarriers: aready (A stored), dready / afree (MMAs done:
 // D ready, A free again), dfree (D read back).
-template <int MC, int kBufs>
+// SK: balanced runs (p.sk); compiled only where the planner takes them
+// (two CTAs per SM), so the other kernels carry none of their code.
+template <int MC, int kBufs, bool SK>
 __global__ void __launch_bounds__(kThreads, kBufs >= 4 ? 1 : 2)
     tc_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -266,9 +271,11 @@ __global__ void __launch_bounds__(kThreads, kBufs >= 4 ? 1 : 2)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_launch_dependents();
-  pdl_wait();   // activations and outputs follow earlier kernels
+  // activations, outputs and the workspace follow earlier kernels; the
+  // copy warp waits later, after requesting its first stages' weights
+  if (warp != kCopyWarp) pdl_wait();
 
-  const Segs segs = segs_of(p);
+  const Segs segs = segs_of<SK>(p);
 
   if (warp == kCopyWarp) {
     // ------------------------------------------------------------ producer
@@ -276,10 +283,25 @@ __global__ void __launch_bounds__(kThreads, kBufs >= 4 ? 1 : 2)
     int slot = 0, issued = 0;
     uint32_t phase = 0;
     bool ok = true;
+    // Weights do not depend on earlier kernels (W4_FLAG_PDL's contract): the
+    // first nst stages' codes and steps are requested before the wait, their
+    // activation boxes (slice dsl[s] of stage s) after it.
+    bool waited = false;
+    int dsl[kMaxStages];
+    auto wait_then_activations = [&]() {
+      pdl_wait();
+      waited = true;
+      if (lane == 0)
+        for (int s = 0; s < min(issued, nst); ++s)
+          tma_load_3d(st0 + s * p.stage_bytes + p.off_b, &p.tm_x, 0, 0, dsl[s] * (kSliceK / 8),
+                      full0 + 8 * s, pol);
+      __syncwarp();
+    };
     for (int i = 0; i < segs.n && ok; ++i) {
-      const Seg sg = seg_at(p, segs, i);
+      const Seg sg = seg_at<SK>(p, segs, i);
       const int t = sg.t, sl0 = sg.b, sl1 = sg.e;
       for (int sl = sl0; sl < sl1; ++sl) {
+        if (issued >= nst && !waited) wait_then_activations();
         if (issued >= nst && !wait_bar(empty0 + 8 * slot, phase ^ 1u, abort_flag)) {
           if (*abort_flag == 0) report(p.status, W4_ERR_TIMEOUT);
           *abort_flag = 1;
@@ -293,7 +315,10 @@ __global__ void __launch_bounds__(kThreads, kBufs >= 4 ? 1 : 2)
           tma_load_2d(stg, &p.tm_codes, sl * (kSliceK / 2), t * kRows, full0 + 8 * slot, pol);
           tma_load_2d(stg + kCodesBytes, &p.tm_steps, sl * kSliceGroups, t * kRows,
                       full0 + 8 * slot, pol);
-          tma_load_3d(stg + p.off_b, &p.tm_x, 0, 0, sl * (kSliceK / 8), full0 + 8 * slot, pol);
+          if (waited)
+            tma_load_3d(stg + p.off_b, &p.tm_x, 0, 0, sl * (kSliceK / 8), full0 + 8 * slot, pol);
+          else
+            dsl[slot] = sl;
         }
         __syncwarp();
         ++issued;
@@ -303,6 +328,9 @@ __global__ void __launch_bounds__(kThreads, kBufs >= 4 ? 1 : 2)
         }
       }
     }
+    // fewer stages than the ring holds (or a timed-out wait): the
+    // activation boxes of the stages requested so far still go out
+    if (!waited) wait_then_activations();
     // every tile of this CTA is requested: its share of the caller's L2
     // ranges (the next call's weights) goes out now, behind them
     if (p.l2.n > 0 && *abort_flag == 0) l2_prefetch_share(p.l2, blockIdx.x, gridDim.x, lane);
@@ -324,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, kBufs >= 4 ? 1 : 2)
     long long r = 0;
     bool ok = true;
     for (int i = 0; i < segs.n && ok; ++i) {
-      const Seg sg = seg_at(p, segs, i);
+      const Seg sg = seg_at<SK>(p, segs, i);
       const int sl0 = sg.b, sl1 = sg.e;
       for (int sl = sl0; sl < sl1 && ok; ++sl) {
         const uint32_t stg = st0 + slot * p.stage_bytes;
@@ -377,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, kBufs >= 4 ? 1 : 2)
     long long r = 0;
     bool ok = true;
     for (int i = 0; i < segs.n && ok; ++i) {
-      const Seg sg = seg_at(p, segs, i);
+      const Seg sg = seg_at<SK>(p, segs, i);
       const int sl0 = sg.b, sl1 = sg.e;
       for (int sl = sl0; sl < sl1 && ok; ++sl) {
         if (!wait_bar(full0 + 8 * slot, phase, abort_flag)) {
@@ -430,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, kBufs >= 4 ? 1 : 2)
     float acc[MC], rowsum[kTmemSum ? 1 : MC];
     bool ok = true;
     for (int i = 0; i < segs.n && ok; ++i) {
-      const Seg sg = seg_at(p, segs, i);
+      const Seg sg = seg_at<SK>(p, segs, i);
       const int t = sg.t, sl0 = sg.b, sl1 = sg.e;
       const bool direct = sg.kind != kSegSplit;   // the row sum stays in this CTA
       const int row = t * kRows + tid;
@@ -487,8 +515,8 @@ __global__ void __launch_bounds__(kThreads, kBufs >= 4 ? 1 : 2)
         if (lane == 0) mbar_arrive(empty0 + 8 * slot);
         // a tile's last slices continue from the previous CTA's prefix (the
         // same sum, in the same order, as if this CTA had run every slice)
-        const bool from_prefix = sg.kind == kSegTail && sl == sl0;
-        if (from_prefix) {
+        const bool from_prefix = SK && sg.kind == kSegTail && sl == sl0;
+        if (SK && from_prefix) {
           if (tid == 0) *last_flag = wait_flag_gpu(p.sk_flag + blockIdx.x - 1, abort_flag) ? 1 : 0;
           asm volatile("bar.sync 1, %0;" ::"n"(kRows) : "memory");
           if (*last_flag == 0) {
@@ -539,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, kBufs >= 4 ? 1 : 2)
           tmem_wait_ld<MC>(tsum);
           sum = tsum;
         }
-        if (sg.kind == kSegHead) {
+        if (SK && sg.kind == kSegHead) {
           // the tile's first slices: their sum (every row of the tile) goes
           // to prefix slot blockIdx.x for the next CTA.  The barrier orders
           // all rows' stores before thread 0's release of the flag.
@@ -557,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, kBufs >= 4 ? 1 : 2)
           for (int m = 0; m < MC; ++m)
             if (m < p.M) p.y[(long long)m * p.N + row] = __float2bfloat16_rn(sum[m]);
         }
-        if (sg.kind == kSegTail) {
+        if (SK && sg.kind == kSegTail) {
           // every row has read the prefix (at the first slice): the slot is
           // re-armed for the next call
           asm volatile("bar.sync 1, %0;" ::"n"(kRows) : "memory");
@@ -677,33 +705,49 @@ using TcFn = void (*)(TcParams);
 
 int mc_of(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : M <= 16 ? 16 : 32; }
 
-TcFn kernel_of(int mc, int bufs) {
+// Instantiations: (MC, 4 rounds), (MC, 2 rounds), (MC, 2 rounds, balanced
+// runs); key = log2(MC) + 6 * variant.
+TcFn kernel_of(int mc, int bufs, bool sk) {
   if (bufs >= 4) {
     switch (mc) {
-      case 1: return tc_kernel<1, 4>;
-      case 2: return tc_kernel<2, 4>;
-      case 4: return tc_kernel<4, 4>;
-      case 8: return tc_kernel<8, 4>;
-      case 16: return tc_kernel<16, 4>;
-      default: return tc_kernel<32, 4>;
+      case 1: return tc_kernel<1, 4, false>;
+      case 2: return tc_kernel<2, 4, false>;
+      case 4: return tc_kernel<4, 4, false>;
+      case 8: return tc_kernel<8, 4, false>;
+      case 16: return tc_kernel<16, 4, false>;
+      default: return tc_kernel<32, 4, false>;
+    }
+  }
+  if (sk) {
+    switch (mc) {
+      case 1: return tc_kernel<1, 2, true>;
+      case 2: return tc_kernel<2, 2, true>;
+      case 4: return tc_kernel<4, 2, true>;
+      case 8: return tc_kernel<8, 2, true>;
+      case 16: return tc_kernel<16, 2, true>;
+      default: return tc_kernel<32, 2, true>;
     }
   }
   switch (mc) {
-    case 1: return tc_kernel<1, 2>;
-    case 2: return tc_kernel<2, 2>;
-    case 4: return tc_kernel<4, 2>;
-    case 8: return tc_kernel<8, 2>;
-    case 16: return tc_kernel<16, 2>;
-    default: return tc_kernel<32, 2>;
+    case 1: return tc_kernel<1, 2, false>;
+    case 2: return tc_kernel<2, 2, false>;
+    case 4: return tc_kernel<4, 2, false>;
+    case 8: return tc_kernel<8, 2, false>;
+    case 16: return tc_kernel<16, 2, false>;
+    default: return tc_kernel<32, 2, false>;
   }
 }
+int kernel_key(int mc, int bufs, bool sk) {
+  int l = 0;
+  while ((1 << l) < mc && l < 5) ++l;
+  return l + 6 * (bufs >= 4 ? 1 : (sk ? 2 : 0));
+}
 
-cudaError_t allow_smem(TcFn fn, int smem, int dev) {
+cudaError_t allow_smem(TcFn fn, int key, int smem, int dev) {
   static std::mutex mu;
-  static int done[64][12] = {};
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  int k = 0;
-  while (k < 11 && fn != kernel_of(1 << (k % 6), k < 6 ? 2 : 4)) ++k;
+  static int done[64][18] = {};
+  if (dev < 0 || dev >= 64 || key < 0 || key >= 18) return cudaErrorInvalidDevice;
+  const int k = key;
   std::lock_guard<std::mutex> lock(mu);
   if (done[dev][k] >= smem) return cudaSuccess;
   const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -838,8 +882,8 @@ cudaError_t tc_launch(const TcPlan& pl, void* y, const void* qw, const void* st,
     p.ws_count = static_cast<int*>(workspace);
     p.ws_partial = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.ws_part_off);
   }
-  const TcFn fn = kernel_of(mc_of(M), pl.bufs);
-  const cudaError_t ea = allow_smem(fn, pl.smem, dev);
+  const TcFn fn = kernel_of(mc_of(M), pl.bufs, pl.sk != 0);
+  const cudaError_t ea = allow_smem(fn, kernel_key(mc_of(M), pl.bufs, pl.sk != 0), pl.smem, dev);
   if (ea != cudaSuccess) return ea;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)pl.ctas);
