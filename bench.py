@@ -755,12 +755,18 @@ def run_gb300(args, world, rank, local):
         "gpu_launches": n_launch * args.steps,
         "clocks": clocks,
     }
+    if world == 1 and not args.no_side and not args.chain:
+        # after the main measurement (its clocks, e2e and oracle are taken);
+        # the decode pass's buffers are freed first
+        del g, dp, launches
+        torch.cuda.empty_cache()
+        line["side_workloads"] = side_workloads(args, world, rank, local)
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
 
 
-def run_moe(args, world, rank, local):
+def run_moe(args, world, rank, local, emit=True):
     """Routed-expert decode (30 layers, 128 experts, top-8, 32-slot LFU pool per
     layer): per step and layer, remap the step's experts to pool slots (host),
     copy the missed experts into the pool and write the slot ids (device),
@@ -1047,9 +1053,71 @@ def run_moe(args, world, rank, local):
         "gpu_launches": steps * L * ((4 if device_pool else 3 if shared == "none" else 5) -
                                      (1 if args.chain else 0)),
     }
+    if not emit:
+        return line
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+def shape_us(M, N, K, dev, copies=None, steps=20, warmup=3):
+    """µs per launch of one (M, N, K) GEMV: `copies` weight copies (default:
+    enough to exceed 600 MB, so every launch reads HBM) replayed in turn as
+    one PDL-chained graph; copies=1 keeps the weights in L2."""
+    from bit_weight_only_gemv_gb300 import lib
+    per = metrics.gemv_bytes(M, N, K)
+    n = copies or max(2, -(-600_000_000 // per))
+    qws = [synth.torch_words((N, K // 8), synth.seed_of(7, i), dev) for i in range(n)]
+    sts = [synth.torch_steps((N, K // 32), synth.seed_of(8, i), dev) for i in range(n)]
+    x = synth.torch_x((M, K), synth.seed_of(9), dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    need = lib.workspace_bytes(M, N, K)
+    ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev) if need else None
+    fns = [(lambda q, s_: (lambda pdl: lib.gemv(q, s_, x, y=y, workspace=ws, pdl=pdl)))(q, s_)
+           for q, s_ in zip(qws, sts)]
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for i, f in enumerate(fns):
+            f(i > 0)
+    torch.cuda.synchronize()
+    g = capture(fns * max(1, 16 // n), stream)
+    for _ in range(warmup):
+        g.replay()
+    ms = time_replays(g, stream, steps) / (n * max(1, 16 // n))
+    return ms * 1e3, per
+
+
+def side_workloads(args, world, rank, local):
+    """Two smaller workloads measured after the main one, in the same run:
+    the 2048 x 2048 batch-1 GEMV (HBM-cold over rotating copies, and
+    L2-hot), and the routed decode (30 layers, 128 experts, top-8, 32-slot
+    pools; 128 steps, every step and layer checked bitwise against the call
+    on the full expert tensor)."""
+    dev = torch.device("cuda", local)
+    out = {}
+    us_cold, per = shape_us(1, 2048, 2048, dev)
+    us_hot, _ = shape_us(1, 2048, 2048, dev, copies=1)
+    peak, peak_kind = load_peaks()
+    out["gemv_2048x2048_batch1"] = {
+        "us_hbm_cold": us_cold, "gbps_hbm_cold": metrics.gbps(per, us_cold * 1e-6),
+        "frac_hbm_cold": metrics.gbps(per, us_cold * 1e-6) / peak, "us_l2_hot": us_hot,
+        "gbps_l2_hot": metrics.gbps(per, us_hot * 1e-6), "bytes": per, "peak": peak,
+        "peak_kind": peak_kind,
+        "note": "rotating weight copies over 600 MB (HBM-cold) or one copy (L2-hot), "
+                "PDL-chained graph, CUDA events"}
+    margs = argparse.Namespace(**vars(args))
+    margs.workload, margs.steps, margs.warmup = "moe-30L-h2816", 128, 3
+    margs.pool, margs.expert_home, margs.expert_vectors = "host", "device", False
+    margs.shared_ffn, margs.chain = "none", False
+    m = run_moe(margs, world, rank, local, emit=False)
+    out["routed_decode_moe_30L_h2816"] = {
+        "tok_s": m["value"], "ms_per_step": m["ms_per_step"], "steps": m["steps"],
+        "kernel_gbps": m["kernel"]["gbps"], "kernel_frac": m["kernel"]["frac"],
+        "lfu_hit_rate": m["pool"]["hit_rate"],
+        "bitwise_pool_vs_full": m["bitwise_pool_vs_full"],
+        "note": "eager steps (host LFU remap, pool copies, slot ids, 2 w4a16_gemv_id per "
+                "layer); kernel GB/s from the step's 60 routed launches replayed as a graph"}
+    return out
 
 
 def run_shape(args):
@@ -1149,6 +1217,10 @@ def build_parser() -> argparse.ArgumentParser:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-side", action="store_true",
+                    help="decode passes: skip the two side workloads measured after the main "
+                         "one (the 2048 x 2048 batch-1 GEMV HBM-cold and L2-hot; the routed "
+                         "decode's 128 steps with the bitwise pool-vs-full check)")
     ap.add_argument("--shape", default=None,
                     help="M,N,K: time one GEMV shape alone instead of the decode pass")
     ap.add_argument("--shape-id", default=None,
