@@ -1469,21 +1469,28 @@ int max_rows_per_launch(int K, const DeviceInfo& di) {
   return mr;
 }
 
-// Batches of at least this many activation rows use the tensor-core path
-// (when K is a multiple of 256): below it the CUDA-core kernel is faster.
-constexpr int kTcMinM = 8;
+// Batches that use the tensor-core path (K a multiple of 256): from 5
+// activation rows always (the CUDA cores take a second launch there), at 4
+// rows for weights of 2^24 codes or more and at 3 rows from 2^27 (measured
+// crossovers: at 4 rows 16384 x 2048 takes 13.3 us on the tensor cores
+// against 14.6 on the CUDA cores, 3072 x 2048 7.2 against 5.7; at 3 rows
+// 43008 x 5376 44.5 against 67.0, 9472 x 5376 20.4 against 18.9).
+bool tc_rows(int M, int N, int K) {
+  const long long codes = (long long)N * K;
+  return M >= 5 || (M == 4 && codes >= (1LL << 24)) || (M == 3 && codes >= (1LL << 27));
+}
 constexpr unsigned kPathFlags = W4_FLAG_CUDA_CORES | W4_FLAG_TENSOR_CORES;
 
 bool tc_shape(int K) { return K >= 256 && K % 256 == 0; }
 
 // 1: tensor-core path, 0: CUDA-core path, -1: the flags ask for a path that
 // cannot run this shape (or for both paths).
-int path_of(int M, int K, unsigned flags) {
+int path_of(int M, int N, int K, unsigned flags) {
   if ((flags & kPathFlags) == kPathFlags) return -1;
   if (flags & W4_FLAG_SILU_MUL) return (flags & W4_FLAG_TENSOR_CORES) ? -1 : 0;   // CUDA cores
   if (flags & W4_FLAG_CUDA_CORES) return 0;
   if (flags & W4_FLAG_TENSOR_CORES) return tc_shape(K) ? 1 : -1;
-  return (M >= kTcMinM && tc_shape(K)) ? 1 : 0;
+  return (tc_rows(M, N, K) && tc_shape(K)) ? 1 : 0;
 }
 
 // Largest workspace of the tensor-core launches of an (M, N, K) call: with
@@ -1559,12 +1566,20 @@ w4_status tc_enqueue(void* y, const void* qw, const void* st, const void* x, int
 using namespace w4;
 
 extern "C" w4_status w4a16_gemv_plan(int M, int N, int K, w4_plan_info* info) {
+  return w4a16_gemv_plan_flags(M, N, K, 0, info);
+}
+
+extern "C" w4_status w4a16_gemv_plan_flags(int M, int N, int K, unsigned flags,
+                                           w4_plan_info* info) {
   if (info == nullptr || M < 1 || N < 1) return W4_ERR_ARG;
+  if ((flags & ~(W4_FLAG_PDL | kPathFlags | W4_FLAG_SILU_MUL)) != 0) return W4_ERR_ARG;
+  const int fpath = path_of(M, N, K, flags);
+  if (fpath < 0) return W4_ERR_SHAPE;
   if (M > W4_MAX_M || K < 32 || K % 32 != 0 || K > W4_MAX_K) return W4_ERR_SHAPE;
   DeviceInfo di;
   planning_device(&di);
   tc::TpPlan pp;
-  if (path_of(M, K, 0) == 1 && M > tc::kTcMaxM && tc::tp_plan(M, N, K, di.sms, &pp)) {
+  if (fpath == 1 && M > tc::kTcMaxM && tc::tp_plan(M, N, K, di.sms, &pp)) {
     *info = w4_plan_info{};
     info->path = 3;
     info->ctas = pp.ctas;
@@ -1583,7 +1598,7 @@ extern "C" w4_status w4a16_gemv_plan(int M, int N, int K, w4_plan_info* info) {
     info->tmpl_chunk = 0;
     return W4_OK;
   }
-  if (path_of(M, K, 0) == 1) {
+  if (fpath == 1) {
     tc::TcPlan tp;
     if (!tc::tc_plan(std::min(M, tc::kTcMaxM), N, K, di.sms, &tp)) return W4_ERR_SHAPE;
     *info = w4_plan_info{};
@@ -1657,7 +1672,7 @@ extern "C" w4_status w4a16_gemv_id_plan(int n_ids, int x_rows, int N, int K, w4_
 
 extern "C" size_t w4a16_gemv_workspace_bytes_flags(int M, int N, int K, unsigned flags) {
   if (M < 1 || N < 1 || M > W4_MAX_M || K < 32 || K % 32 != 0 || K > W4_MAX_K) return 0;
-  const int path = path_of(M, K, flags);
+  const int path = path_of(M, N, K, flags);
   if (path < 0) return 0;
   DeviceInfo di;
   planning_device(&di);
@@ -1689,7 +1704,7 @@ static w4_status gemv_call(void* y, const void* qw, const void* st, const void* 
   if (M > W4_MAX_M || K < 32 || K % 32 != 0 || K > W4_MAX_K) return W4_ERR_SHAPE;
   if (!aligned(qw, 16) || !aligned(st, 16) || !aligned(x, 16) || !aligned(y, 2))
     return W4_ERR_ALIGN;
-  const int path = path_of(M, K, flags);
+  const int path = path_of(M, N, K, flags);
   if (path < 0) return W4_ERR_SHAPE;
   const bool gated = (flags & W4_FLAG_SILU_MUL) != 0;   // x rows [gate K | up K]
   int dev = 0;
@@ -1900,7 +1915,7 @@ extern "C" w4_status w4a16_gemv_static_scratch(void* y, const void* qw, const vo
   if (M > W4_MAX_M || K < 32 || K % 32 != 0 || K > W4_MAX_K) return W4_ERR_SHAPE;
   if (!aligned(qw, 16) || !aligned(st, 16) || !aligned(x, 16) || !aligned(y, 2))
     return W4_ERR_ALIGN;
-  const int path = path_of(M, K, flags);
+  const int path = path_of(M, N, K, flags);
   if (path < 0) return W4_ERR_SHAPE;
   const bool gated = (flags & W4_FLAG_SILU_MUL) != 0;   // x rows [gate K | up K]
   int dev = 0;

@@ -33,7 +33,8 @@ EXPORTS = ("w4_status_str", "w4_abi_version", "w4_last_cuda_error", "w4a16_gemv"
            "w4a16_gemv_static_scratch", "w4_dev_pool_state_bytes", "w4_dev_pool_init",
            "w4_dev_pool_stage", "w4_dev_pool_stats", "w4a16_gemv_chain",
            "w4a16_gemv_chain_workspace_bytes", "w4a16_gemv_chain_plan",
-           "w4a16_gemv_chain_task_plan", "w4a16_gemv_id_plan", "w4a16_gemv_prefetch_l2")
+           "w4a16_gemv_chain_task_plan", "w4a16_gemv_id_plan", "w4a16_gemv_prefetch_l2",
+           "w4a16_gemv_plan_flags")
 W4_TASK_SILU_MUL = 1
 W4_MAX_L2_RANGES = 4
 CHAIN_MAX_TASKS = 320
@@ -140,6 +141,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.w4_dev_pool_stats.argtypes = [vp, i32, i32] + [ctypes.POINTER(ctypes.c_longlong)] * 3
     lib.w4a16_gemv_plan.restype = i32
     lib.w4a16_gemv_plan.argtypes = [i32, i32, i32, ctypes.POINTER(PlanInfo)]
+    lib.w4a16_gemv_plan_flags.restype = i32
+    lib.w4a16_gemv_plan_flags.argtypes = [i32, i32, i32, u32, ctypes.POINTER(PlanInfo)]
     lib.w4a16_gemv_id_plan.restype = i32
     lib.w4a16_gemv_id_plan.argtypes = [i32, i32, i32, i32, ctypes.POINTER(PlanInfo)]
     lib.w4a16_gemv_chain.restype = i32
@@ -196,9 +199,11 @@ def workspace_bytes(M: int, N: int, K: int, path: str = None) -> int:
     return int(load().w4a16_gemv_workspace_bytes_flags(M, N, K, _PATH_FLAGS[path]))
 
 
-def plan(M: int, N: int, K: int) -> dict:
+def plan(M: int, N: int, K: int, path: str = None) -> dict:
+    """Launch plan of a w4a16_gemv call (path: None, "cuda" or "tensor")."""
     info = PlanInfo()
-    _check(load().w4a16_gemv_plan(M, N, K, ctypes.byref(info)), "w4a16_gemv_plan")
+    _check(load().w4a16_gemv_plan_flags(M, N, K, _PATH_FLAGS[path], ctypes.byref(info)),
+           "w4a16_gemv_plan_flags")
     return {n: getattr(info, n) for n, _ in PlanInfo._fields_}
 
 

@@ -43,10 +43,11 @@
  *     addresses), so w4a16_gemv_id row i is bitwise equal to w4a16_gemv on
  *     expert ids[i] with the same activation row.
  *   - Two paths compute w4a16_gemv.  The CUDA-core path (every w4a16_gemv_id
- *     call, and w4a16_gemv with fewer than 8 activation rows) dequantises in
- *     packed fp16 with fp16 partial sums of 4 products; its rows do not
- *     depend on M.  The tensor-core path (w4a16_gemv with 8 or more rows and
- *     K a multiple of 256) lets tcgen05 MMAs take exact bf16 products with
+ *     call, and w4a16_gemv with 1 or 2 activation rows, or 3 to 4 rows of
+ *     small weights) dequantises in packed fp16 with fp16 partial sums of 4
+ *     products; its rows do not depend on M.  The tensor-core path
+ *     (w4a16_gemv with 5 or more rows, 4 rows when N * K >= 2^24, 3 rows
+ *     when N * K >= 2^27, K a multiple of 256) lets tcgen05 MMAs take exact bf16 products with
  *     fp32 sums: up to 32 rows it folds each group's step into the sum after
  *     the MMA, from 33 rows (prompt chunks) it splits each weight exactly
  *     into two bf16 parts and accumulates over the whole of K.  Within
@@ -125,9 +126,12 @@ const char *w4_last_cuda_error(void);
  * qw         uint32 [N][K/8], 16-byte aligned.
  * st         bf16 [N][K/32], 16-byte aligned.
  * x          bf16 [M][K], 16-byte aligned.
- * M          1 .. W4_MAX_M activation rows.  By default: below 8 rows the
- *            CUDA-core path, one launch per 4 rows; 8 to 32 rows one launch
- *            of the tensor-core small-batch kernel; 33 to W4_MAX_M rows (a
+ * M          1 .. W4_MAX_M activation rows.  By default (K a multiple of
+ *            256): 1-2 rows, and 3-4 rows of small weights (N * K below 2^27
+ *            at 3 rows, below 2^24 at 4), the CUDA-core path; other batches up
+ *            to 32 rows one launch of the tensor-core small-batch kernel (the
+ *            CUDA-core path for every M up to 32 when K is not a multiple of
+ *            256, one launch per 4 rows); 33 to W4_MAX_M rows (a
  *            prompt chunk) one launch of the tensor-core GEMM.  A call pinned
  *            to the CUDA cores enqueues one launch per 4 rows at any M (each
  *            reading the weights), all checked before the first is
@@ -146,8 +150,8 @@ const char *w4_last_cuda_error(void);
  *            when a K split needs the workspace.
  * status_dev device int32 for device-side errors (W4_ERR_TIMEOUT), or NULL.
  * flags      W4_FLAG_PDL, and at most one of W4_FLAG_CUDA_CORES /
- *            W4_FLAG_TENSOR_CORES (default: tensor cores from M = 8 when K is
- *            a multiple of 256; W4_ERR_SHAPE if the pinned path cannot run K).
+ *            W4_FLAG_TENSOR_CORES (default: the rule under M above;
+ *            W4_ERR_SHAPE if the pinned path cannot run K).
  *            W4_FLAG_SILU_MUL: the gated MLP's down projection fused with its
  *            activation (page "Gemma 4 on a 4 GB GPU in Plain PyTorch", tip
  *            "Merge the Small Projections": gate and up are one merged GEMV,
@@ -526,6 +530,10 @@ typedef struct w4_plan_info {
 } w4_plan_info;
 
 w4_status w4a16_gemv_plan(int M, int N, int K, w4_plan_info *info);
+
+/* The plan of a w4a16_gemv call with the given flags (a pinned path plans
+ * that path's launch).  W4_ERR_SHAPE when the pinned path cannot run K. */
+w4_status w4a16_gemv_plan_flags(int M, int N, int K, unsigned flags, w4_plan_info *info);
 
 /* The same for a w4a16_gemv_id call with n_ids ids and x_rows activation
  * rows (path is always 1). */

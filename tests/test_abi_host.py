@@ -145,8 +145,8 @@ def test_device_pool_host_checks(L):
                                    (4, 8192, 2048), (1, 262144, 2048), (1, 7, 32),
                                    (3, 100, 65536)])
 def test_plan_is_valid(M, N, K):
-    p = lib.plan(M, N, K)
-    assert p["path"] == 1
+    p = lib.plan(M, N, K, path="cuda")          # the CUDA-core plan (4 x 8192 x 2048 defaults
+    assert p["path"] == 1                       # to the tensor cores)
     assert p["threads"] == 256                   # 7 consumer warps + 1 copy warp
     assert p["team"] in (1, 2, 4, 8, 16, 32) and (K // 32) % p["team"] == 0
     assert p["rows_per_lane"] in (1, 2, 4)
@@ -166,7 +166,7 @@ def test_plan_is_valid(M, N, K):
     assert 1 <= p["rows_per_call"] <= min(M, 4)
     if K <= 21504:
         assert p["rows_per_call"] == min(M, 4)
-    ws = lib.workspace_bytes(M, N, K)
+    ws = lib.workspace_bytes(M, N, K, "cuda")
     assert (ws > 0) == (p["slices"] > 1)
 
 
@@ -288,7 +288,8 @@ def test_planner_sweep_of_random_shapes():
         if rng.random() < 0.3:
             K = 256 * max(1, K // 256)
         p = lib.plan(M, N, K)
-        want = 1 if (M < 8 or K % 256) else (2 if M <= 32 else 3)
+        tc_rows = M >= 5 or (M == 4 and N * K >= 1 << 24) or (M == 3 and N * K >= 1 << 27)
+        want = 1 if (not tc_rows or K % 256) else (2 if M <= 32 else 3)
         assert p["path"] == want, (M, N, K, p)
         assert 1 <= p["ctas"] <= p["ctas_per_sm"] * 152, (M, N, K, p)
         assert p["smem_bytes"] <= 232448, (M, N, K, p)

@@ -89,7 +89,7 @@ def test_batched_rows_with_run_time_windows(cuda_lib, m, n, k):
     """Several activation rows (CUDA-core path) with windows handed out at run
     time: sampled rows against the oracle, and each activation row bitwise
     equal to the single-row call (the row arithmetic depends on K alone)."""
-    assert lib.plan(m, n, k)["dynamic_windows"] == 1
+    assert lib.plan(m, n, k, path="cuda")["dynamic_windows"] == 1
     qw, st, _ = weights(n, k, 7 * m + k)
     x = synth.torch_x((m, k), synth.seed_of(m, k), "cuda")
     y = poison_bf16((m, n))
