@@ -598,7 +598,10 @@ def moe_config(cfg, args, world):
                            "expert's down product on silu(gate) * up of its own gate/up rows"
                            if getattr(args, "chain", False) else
                            "two w4a16_gemv_id launches per layer, down on its own activation "
-                           "rows"),
+                           "rows" + ("" if getattr(args, "no_ids_final", False) else
+                                     "; the down call's weight copies start before its "
+                                     "dependency wait (W4_FLAG_IDS_FINAL: its ids are the "
+                                     "gate/up call's)")),
             "expert_vectors": ("per-expert output scales (gate/up, down) and down "
                                "biases by real id, slot table checked, "
                                "w4a16_gemv_id_scaled; real ids copied to the device "
@@ -907,11 +910,18 @@ def run_moe(args, world, rank, local, emit=True):
                 lay["table"].fill_(-1)
         torch.cuda.synchronize()
 
+    ids_final = not getattr(args, "no_ids_final", False) and not args.chain
+
     def gemvs(lay, full=False, pdl=False):
         # programmatic dependent launch after the first kernel: the routed
-        # kernel reads its ids and activations only after the previous one
+        # kernel reads its ids and activations only after the previous one;
+        # the down call's ids are the gate/up call's, written before it ran,
+        # so its weight copies may start before that wait (W4_FLAG_IDS_FINAL)
         for i, call in enumerate(lay["calls_full" if full else "calls"]):
-            call(pdl=pdl or i > 0, stream=stream)
+            if ids_final:
+                call(pdl=pdl or i > 0, stream=stream, ids_final=i > 0)
+            else:
+                call(pdl=pdl or i > 0, stream=stream)
 
     def layer_step(lay, t):
         """One layer of one step: pool fill and slot ids, the dense FFN if any,
@@ -1217,6 +1227,9 @@ def build_parser() -> argparse.ArgumentParser:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-ids-final", action="store_true",
+                    help="routed-expert workload: the down call waits for the gate/up call "
+                         "before reading its ids (without W4_FLAG_IDS_FINAL)")
     ap.add_argument("--no-side", action="store_true",
                     help="decode passes: skip the two side workloads measured after the main "
                          "one (the 2048 x 2048 batch-1 GEMV HBM-cold and L2-hot; the routed "

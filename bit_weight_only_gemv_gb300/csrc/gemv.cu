@@ -113,6 +113,7 @@ struct GemvParams {
   const __nv_bfloat16* escale;         // [num_real][N] output scale, or nullptr
   const __nv_bfloat16* ebias;          // [num_real][N] output bias, or nullptr
   L2Ranges l2;                         // brought into L2 after the launch's own tiles
+  int ids_final;                       // routed ids written before the previous kernel began
 };
 
 // ---------------------------------------------------------------- activations
@@ -377,8 +378,9 @@ __global__ void __launch_bounds__(kThreads, min_ctas(MR, RW))
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
     // Dense weights do not depend on earlier kernels: their tiles are
-    // requested at once.  Routed ids may come from the previous kernel.
-    if (!dense) pdl_wait();
+    // requested at once.  Routed ids may come from the previous kernel,
+    // unless the caller says they were final before it (W4_FLAG_IDS_FINAL).
+    if (!dense && !p.ids_final) pdl_wait();
     const uint64_t pol = policy_evict_first();
     Walk wk;
     wk.init(p);
@@ -1799,7 +1801,8 @@ w4_status routed(void* y, const void* qw_base, size_t qw_stride_bytes, const voi
                  int32_t* status_dev, unsigned flags, w4_stream_t stream) {
   if (y == nullptr || qw_base == nullptr || st_base == nullptr || ids == nullptr || x == nullptr)
     return W4_ERR_ARG;
-  if (n_ids < 1 || N < 1 || num_experts < 1 || (flags & ~W4_FLAG_PDL) != 0) return W4_ERR_ARG;
+  if (n_ids < 1 || N < 1 || num_experts < 1 || (flags & ~(W4_FLAG_PDL | W4_FLAG_IDS_FINAL)) != 0)
+    return W4_ERR_ARG;
   if (K < 32 || K % 32 != 0 || K > W4_MAX_K) return W4_ERR_SHAPE;
   if (x_rows != 1 && x_rows != n_ids) return W4_ERR_SHAPE;
   if (qw_stride_bytes < (size_t)N * K / 2 || st_stride_bytes < (size_t)N * (K / 32) * 2)
@@ -1822,6 +1825,7 @@ w4_status routed(void* y, const void* qw_base, size_t qw_stride_bytes, const voi
   p.qw_item_stride = qw_stride_bytes;
   p.st_item_stride = st_stride_bytes;
   p.ids = ids;
+  p.ids_final = (flags & W4_FLAG_IDS_FINAL) != 0 ? 1 : 0;
   p.num_experts = num_experts;
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.x_per_item = xpi;

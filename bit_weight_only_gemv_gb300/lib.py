@@ -20,6 +20,13 @@ W4_FLAG_PDL = 1
 W4_FLAG_CUDA_CORES = 2
 W4_FLAG_TENSOR_CORES = 4
 W4_FLAG_SILU_MUL = 8
+W4_FLAG_IDS_FINAL = 16
+
+
+def _id_flags(pdl: bool, ids_final: bool) -> int:
+    """ids_final: the ids were written before the previous kernel began
+    (W4_FLAG_IDS_FINAL; only meaningful with pdl)."""
+    return (W4_FLAG_PDL if pdl else 0) | (W4_FLAG_IDS_FINAL if ids_final else 0)
 _PATH_FLAGS = {None: 0, "cuda": W4_FLAG_CUDA_CORES, "tensor": W4_FLAG_TENSOR_CORES}
 STATUS = {0: "W4_OK", 1: "W4_ERR_ARG", 2: "W4_ERR_ALIGN", 3: "W4_ERR_SHAPE",
           4: "W4_ERR_WORKSPACE", 5: "W4_ERR_LAUNCH", 6: "W4_ERR_INDEX", 7: "W4_ERR_VALUE",
@@ -281,7 +288,7 @@ def gemv(qw: torch.Tensor, st: torch.Tensor, x: torch.Tensor, y: torch.Tensor = 
 def gemv_id(qw_base: torch.Tensor, st_base: torch.Tensor, ids: torch.Tensor, x: torch.Tensor,
             N: int, K: int, num_experts: int, qw_stride_bytes: int, st_stride_bytes: int,
             y: torch.Tensor = None, status: torch.Tensor = None, pdl: bool = False,
-            stream=None) -> torch.Tensor:
+            stream=None, ids_final: bool = False) -> torch.Tensor:
     """y[i] = W_{ids[i]} @ x[i or 0]; experts at base + id * stride (bytes)."""
     _need(ids, torch.int32, "ids")
     _need(x, torch.bfloat16, "x")
@@ -294,7 +301,7 @@ def gemv_id(qw_base: torch.Tensor, st_base: torch.Tensor, ids: torch.Tensor, x: 
     _need(y, torch.bfloat16, "y")
     _check(load().w4a16_gemv_id(_ptr(y), _ptr(qw_base), qw_stride_bytes, _ptr(st_base),
                                 st_stride_bytes, num_experts, _ptr(ids), n_ids, _ptr(x2),
-                                x2.shape[0], N, K, _ptr(status), W4_FLAG_PDL if pdl else 0,
+                                x2.shape[0], N, K, _ptr(status), _id_flags(pdl, ids_final),
                                 _stream(stream)), "w4a16_gemv_id")
     return y
 
@@ -318,8 +325,8 @@ def bind_gemv_id(qw_base: torch.Tensor, st_base: torch.Tensor, ids: torch.Tensor
     args = (_ptr(y), _ptr(qw_base), qw_stride_bytes, _ptr(st_base), st_stride_bytes, num_experts,
             _ptr(ids), ids.numel(), _ptr(x2), x2.shape[0], N, K, _ptr(status))
 
-    def call(pdl: bool = False, stream=None):
-        _check(fn(*args, W4_FLAG_PDL if pdl else 0, _stream(stream)), "w4a16_gemv_id")
+    def call(pdl: bool = False, stream=None, ids_final: bool = False):
+        _check(fn(*args, _id_flags(pdl, ids_final), _stream(stream)), "w4a16_gemv_id")
 
     call.tensors = (qw_base, st_base, ids, x2, y, status)   # keep them alive
     return call
@@ -353,14 +360,15 @@ def gemv_id_scaled(qw_base: torch.Tensor, st_base: torch.Tensor, ids: torch.Tens
                    st_stride_bytes: int, expert_ids: torch.Tensor, num_experts: int,
                    slot_expert: torch.Tensor = None, scale: torch.Tensor = None,
                    bias: torch.Tensor = None, y: torch.Tensor = None,
-                   status: torch.Tensor = None, pdl: bool = False, stream=None) -> torch.Tensor:
+                   status: torch.Tensor = None, pdl: bool = False, stream=None,
+                   ids_final: bool = False) -> torch.Tensor:
     """y[i] = bf16(fma(W_{ids[i]} @ x[i or 0], scale[e], bias[e])), e = expert_ids[i]:
     weights through slot (or expert) ids, per-expert vectors through real ids."""
     if y is None:
         y = torch.empty((ids.numel(), N), dtype=torch.bfloat16, device=x.device)
     _, args = _scaled_args(y, qw_base, qw_stride_bytes, st_base, st_stride_bytes, num_slots, ids,
                            x, N, K, expert_ids, num_experts, slot_expert, scale, bias, status)
-    _check(load().w4a16_gemv_id_scaled(*args, W4_FLAG_PDL if pdl else 0, _stream(stream)),
+    _check(load().w4a16_gemv_id_scaled(*args, _id_flags(pdl, ids_final), _stream(stream)),
            "w4a16_gemv_id_scaled")
     return y
 
@@ -375,8 +383,8 @@ def bind_gemv_id_scaled(qw_base, st_base, ids, x, N, K, num_slots, qw_stride_byt
                             status)
     fn = load().w4a16_gemv_id_scaled
 
-    def call(pdl: bool = False, stream=None):
-        _check(fn(*args, W4_FLAG_PDL if pdl else 0, _stream(stream)), "w4a16_gemv_id_scaled")
+    def call(pdl: bool = False, stream=None, ids_final: bool = False):
+        _check(fn(*args, _id_flags(pdl, ids_final), _stream(stream)), "w4a16_gemv_id_scaled")
 
     call.tensors = (qw_base, st_base, ids, x2, y, expert_ids, slot_expert, scale, bias, status)
     return call

@@ -93,6 +93,13 @@ typedef enum w4_status {
 #define W4_FLAG_TENSOR_CORES 4u   /* w4a16_gemv: tensor-core path at any M (K % 256 == 0) */
 #define W4_FLAG_SILU_MUL 8u       /* w4a16_gemv: x rows are [gate K | up K]; the product
                                      takes h = silu(gate) * up (CUDA-core path) */
+#define W4_FLAG_IDS_FINAL 16u     /* w4a16_gemv_id(_scaled) with W4_FLAG_PDL: ids were
+                                     written before the previous kernel in the stream
+                                     began (e.g. the slot ids of the layer's previous
+                                     routed call); the copy warps then read them and start
+                                     the weight copies before the dependency wait
+                                     (activations, real ids and the slot table are still
+                                     read after it) */
 
 #define W4_GROUP 32        /* codes per group along K */
 #define W4_MAX_K 65536     /* largest supported K */

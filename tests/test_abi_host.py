@@ -74,6 +74,11 @@ def test_host_validation_rejects_before_any_launch(L):
                            None) == 2
     assert L.w4a16_gemv_id(good, good, 512, good, 128, 4, good, 3, good, 1, 32, 64, None, 0,
                            None) == 1
+    # routed flags: W4_FLAG_PDL and W4_FLAG_IDS_FINAL only
+    assert L.w4a16_gemv_id(good, good, 1024, good, 128, 4, good, 3, good, 1, 32, 64, None, 32,
+                           None) == 1
+    assert L.w4a16_gemv_id(good, good, 1024, good, 128, 4, good, 3, good, 1, 32, 64, None, 8,
+                           None) == 1
     # gemv_id_scaled: real ids required, vectors 2-byte aligned, table 4-byte aligned
     def scaled(eids=good, n_real=8, table=None, scale=None, bias=None, x_rows=1):
         return L.w4a16_gemv_id_scaled(good, good, 1024, good, 128, 4, good, 3, good, x_rows, 32,

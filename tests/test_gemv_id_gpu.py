@@ -268,3 +268,36 @@ def test_bound_calls_and_side_by_side_slots(cuda_lib):
             y_ref = lib.gemv_id(q, st, ids, xs[name], n, k, E, n * k // 2, n * k // 16)
             assert torch.equal(ys[name].view(torch.int16), y_ref.view(torch.int16)), (name, t)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("e,n,k,n_ids,x_rows", [(8, 2816, 704, 8, 8), (8, 1408, 2816, 8, 1),
+                                                (6, 5376, 5376, 8, 1)])
+def test_ids_final_same_bits_in_a_pdl_chain(cuda_lib, e, n, k, n_ids, x_rows):
+    # A routed call launched as a programmatic dependent of another kernel
+    # with W4_FLAG_IDS_FINAL (its ids written before that kernel) starts its
+    # weight copies early: the same bits as without the flag, and as the
+    # oracle bound, on fixed-share and run-time-window plans alike.
+    rng = np.random.default_rng(e + n + k)
+    qw_h, st_h, qwb, stb, qs, ss = experts(rng, e, n, k)
+    ids_h = rng.permutation(e)[:n_ids].astype(np.int32) if n_ids <= e else \
+        rng.integers(0, e, size=n_ids).astype(np.int32)
+    x_h = synth.np_x(rng, (x_rows, k))
+    qw, st, ids, x = dev_bytes(qwb), dev_bytes(stb), torch.from_numpy(ids_h).to("cuda"), dev_bf16(x_h)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y0 = lib.gemv_id(qw, st, ids, x, n, k, e, qs, ss, status=status)
+    # a kernel before it in the stream: another routed call on the same ids
+    other = poison_bf16((n_ids, n))
+    ys = []
+    for _ in range(3):
+        lib.gemv_id(qw, st, ids, x, n, k, e, qs, ss, y=other, status=status, pdl=True)
+        y = poison_bf16((n_ids, n))
+        lib.gemv_id(qw, st, ids, x, n, k, e, qs, ss, y=y, status=status, pdl=True, ids_final=True)
+        ys.append(y)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for y in ys:
+        assert torch.equal(y.view(torch.int16), y0.view(torch.int16))
+    y_ref = oracle.gemv_id_ref(qw_h, st_h, ids_h, x_h)
+    a_ref = np.stack([oracle.gemv_abs_ref(qw_h[d], st_h[d], x_h[0 if x_rows == 1 else i])[0]
+                      for i, d in enumerate(ids_h)])
+    assert oracle.within_bound(host_bits(ys[-1]), y_ref, a_ref)
