@@ -28,7 +28,7 @@ import torch
 
 import oracle
 from bit_weight_only_gemv_gb300 import lib, synth
-from _helpers import POISON, dev_bf16, dev_words, host_bits, poison_bf16
+from _helpers import POISON, assert_gemv_parity, dev_bf16, dev_words, host_bits, poison_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -114,6 +114,36 @@ def test_static_scratch_gated_activation(cuda_lib, m, n, k):
     assert int(status.item()) == 0
     y_ref, a_ref = oracle.gemv_values_ref(qw_h, st_h, oracle.silu_mul_ref(x_h))
     _check(ys, y_ws, y_ref, a_ref)
+
+
+def test_static_scratch_runs_the_plain_plan_of_balanced_shapes(cuda_lib):
+    # A tensor-core shape whose full-speed plan cuts tiles between CTAs
+    # (balanced runs, their hand-over slots well beyond the fixed array)
+    # runs the plain plan here: the same bits as w4a16_gemv with the full
+    # workspace, within the oracle bound on sampled rows, no device memory
+    # taken.
+    L = cuda_lib
+    m, n, k = 16, 39680, 1024
+    assert lib.plan(m, n, k)["dynamic_windows"] == 1
+    assert lib.workspace_bytes(m, n, k) > STATIC_SCRATCH_BYTES
+    rng = np.random.default_rng(321)
+    qw_h = synth.np_words(rng, (n, k // 8))
+    st_h = synth.np_steps(rng, (n, k // 32))
+    x_h = synth.np_x(rng, (m, k))
+    qw, st, x = dev_words(qw_h), dev_bf16(st_h), dev_bf16(x_h)
+    ws = torch.zeros(lib.workspace_bytes(m, n, k), dtype=torch.uint8, device="cuda")
+    y_ws = lib.gemv(qw, st, x, workspace=ws)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = poison_bf16((m, n))
+    torch.cuda.synchronize()
+    before = torch.cuda.memory_allocated()
+    assert lib.STATUS[_static_call(L, y, qw, st, x, m, n, k, status)] == "W4_OK"
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated() == before
+    assert int(status.item()) == 0
+    assert torch.equal(y.view(torch.int16), y_ws.view(torch.int16))
+    rows = np.unique(np.concatenate([np.arange(0, n, 97), np.arange(n - 130, n)]))
+    assert_gemv_parity(y, qw_h, st_h, x_h, rows=rows)
 
 
 def test_static_scratch_refuses_shapes_beyond_the_array(cuda_lib):
