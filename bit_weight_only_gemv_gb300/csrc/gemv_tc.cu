@@ -3,7 +3,7 @@
 //
 // Page "Gemma 4 on a 4 GB GPU in Plain PyTorch", section "Step 3 — Multiply
 // Straight From the Packed Weights": the weights are multiplied straight from
-// the packed 4-bit words.  With several activation rows (M of 8 to 32) the
+// the packed 4-bit words.  With several activation rows (M up to 32) the
 // product is a real dense contraction, and the tensor cores take the dot
 // products while the CUDA cores only unpack codes:
 //

@@ -1,7 +1,8 @@
 """GPU parity of the tensor-core (tcgen05) path of w4a16_gemv against the fp64
 oracle, through the C ABI.
 
-The path is the default for 8 to 32 activation rows (K a multiple of 256) and
+The path is the default for 5 to 32 activation rows, and 3 to 4 rows of large
+weights (K a multiple of 256), and
 can be pinned at any M with the path flag.  Bar: every output within
 |y - y_ref| <= 2e-3 * sum_k |w x| + one bf16 ulp of y_ref.
 """
