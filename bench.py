@@ -512,17 +512,79 @@ def sample_note(items, pass_bytes):
             "pass by algorithmic bytes; NumPy may use BLAS threads on the listed cores")
 
 
-def cpu_baseline_of(items, pass_bytes, seconds=CPU_BASELINE_SECONDS):
+_ONE_CORE_CHILD = r"""
+import os, sys, time
+import numpy as np
+sys.path.insert(0, sys.argv[1])
+try:
+    os.sched_setaffinity(0, {sorted(os.sched_getaffinity(0))[0]})
+except Exception:
+    pass
+import oracle
+z = np.load(sys.argv[2])
+items = []
+for i in range(int(z["n"])):
+    items.append((str(z["k%d" % i]), z["q%d" % i], z["s%d" % i],
+                  z["x%d" % i] if ("x%d" % i) in z.files else None))
+reps, spent, seconds = 0, 0.0, float(sys.argv[3])
+while reps == 0 or spent < seconds:
+    t0 = time.perf_counter()
+    for kind, qw, st, x in items:
+        if kind == "gemv":
+            oracle.gemv_ref(qw, st, x)
+        else:
+            oracle.gather_ref(qw, st, np.array([0]))
+    spent += time.perf_counter() - t0
+    reps += 1
+print(spent / reps * 1e3, reps)
+"""
+
+
+def one_core_sample_ms(items, seconds=5.0):
+    """ms per run of the same sample in a child process held to one core
+    (its BLAS and OpenMP pools one thread each), or None if it failed."""
+    with tempfile.TemporaryDirectory() as d:
+        path = os.path.join(d, "sample.npz")
+        arrays = {"n": np.array(len(items))}
+        for i, (kind, qw, st, x) in enumerate(items):
+            arrays[f"k{i}"], arrays[f"q{i}"], arrays[f"s{i}"] = np.array(kind), qw, st
+            if x is not None:
+                arrays[f"x{i}"] = x
+        np.savez(path, **arrays)
+        env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1",
+                   MKL_NUM_THREADS="1", BLIS_NUM_THREADS="1")
+        try:
+            out = subprocess.run([sys.executable, "-c", _ONE_CORE_CHILD, ROOT, path,
+                                  str(seconds)], env=env, capture_output=True, text=True,
+                                 timeout=60 + 4 * seconds)
+            ms, reps = out.stdout.split()[:2]
+            return float(ms), int(reps)
+        except Exception:
+            return None
+
+
+def cpu_baseline_of(items, pass_bytes, seconds=CPU_BASELINE_SECONDS, one_core=True):
     """The oracle on the sample, repeated for about `seconds`; tok/s scaled
-    to whole passes."""
+    to whole passes.  one_core: also the same sample on one core."""
     reps, spent = 0, 0.0
     while reps == 0 or spent < seconds:
         spent += run_oracle_sample(items)
         reps += 1
     per_token = spent / reps * pass_bytes / sample_bytes(items)
-    return {"value": 1.0 / per_token, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-            "sample": sample_note(items, pass_bytes) + f"; {reps} repetitions, {spent:.1f} s",
-            "sample_ms": spent / reps * 1e3, "extrapolated_ms_per_token": per_token * 1e3}
+    out = {"value": 1.0 / per_token, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+           "sample": sample_note(items, pass_bytes) + f"; {reps} repetitions, {spent:.1f} s",
+           "sample_ms": spent / reps * 1e3, "extrapolated_ms_per_token": per_token * 1e3,
+           "cpu_count": os.cpu_count(), "affinity_cores": cpu_cores()}
+    if one_core:
+        r = one_core_sample_ms(items)
+        if r is not None:
+            ms1, reps1 = r
+            per1 = ms1 * 1e-3 * pass_bytes / sample_bytes(items)
+            out["one_core"] = {"value": 1.0 / per1, "unit": UNIT, "sample_ms": ms1,
+                               "extrapolated_ms_per_token": per1 * 1e3, "repetitions": reps1,
+                               "note": "the same sample in a child process held to one core, "
+                                       "BLAS and OpenMP pools of one thread"}
+    return out
 
 
 # ------------------------------------------------------------------ arms
