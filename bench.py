@@ -563,9 +563,11 @@ def one_core_sample_ms(items, seconds=5.0):
             return None
 
 
-def cpu_baseline_of(items, pass_bytes, seconds=CPU_BASELINE_SECONDS, one_core=True):
+def cpu_baseline_of(items, pass_bytes, seconds=CPU_BASELINE_SECONDS, one_core=True,
+                    one_core_seconds=5.0):
     """The oracle on the sample, repeated for about `seconds`; tok/s scaled
-    to whole passes.  one_core: also the same sample on one core."""
+    to whole passes.  one_core: also the same sample on one core (for about
+    one_core_seconds)."""
     reps, spent = 0, 0.0
     while reps == 0 or spent < seconds:
         spent += run_oracle_sample(items)
@@ -576,7 +578,7 @@ def cpu_baseline_of(items, pass_bytes, seconds=CPU_BASELINE_SECONDS, one_core=Tr
            "sample_ms": spent / reps * 1e3, "extrapolated_ms_per_token": per_token * 1e3,
            "cpu_count": os.cpu_count(), "affinity_cores": cpu_cores()}
     if one_core:
-        r = one_core_sample_ms(items)
+        r = one_core_sample_ms(items, one_core_seconds)
         if r is not None:
             ms1, reps1 = r
             per1 = ms1 * 1e-3 * pass_bytes / sample_bytes(items)

@@ -87,3 +87,20 @@ def test_dense_sample_covers_each_launched_matrix():
     assert [it[1].shape[1] * 8 for it in gemvs] == [5376, 5376, 5376, 21504, 5376]
     assert all(it[1].shape[0] == bench.SAMPLE_ROWS for it in gemvs)
     assert sum(1 for it in items if it[0] == "gather") == 1    # no per-layer table
+
+
+def test_cpu_baseline_times_the_sample_on_all_cores_and_on_one():
+    import numpy as np
+    from bit_weight_only_gemv_gb300 import synth
+    rng = np.random.default_rng(0)
+    items = [("gemv", synth.np_words(rng, (32, 256)), synth.np_steps(rng, (32, 64)),
+              synth.np_x(rng, (1, 2048))),
+             ("gather", synth.np_words(rng, (1, 256)), synth.np_steps(rng, (1, 64)), None)]
+    out = bench.cpu_baseline_of(items, 10 ** 9, seconds=0.2, one_core_seconds=0.2)
+    assert out["kind"] == "oracle" and out["value"] > 0 and out["cores"] >= 1
+    assert out["cpu_count"] >= out["affinity_cores"] >= 1
+    one = out["one_core"]                        # the child process held to one core
+    assert one["value"] > 0 and one["repetitions"] >= 1
+    # both rates scale the same sample to the same pass
+    assert abs(one["extrapolated_ms_per_token"] * one["value"] - 1000.0) < 1e-6
+    assert abs(out["extrapolated_ms_per_token"] * out["value"] - 1000.0) < 1e-6
