@@ -178,7 +178,9 @@ __global__ void __launch_bounds__(kThreads, 1) tp_kernel(const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_launch_dependents();
-  pdl_wait();   // activations and outputs follow earlier kernels
+  // activations and outputs follow earlier kernels; the copy warp waits
+  // later, after requesting its first code stages
+  if (warp != kCopyWarp) pdl_wait();
 
   const int u0 = (int)((long long)blockIdx.x * p.units / gridDim.x);
   const int u1 = (int)((long long)(blockIdx.x + 1) * p.units / gridDim.x);
@@ -190,25 +192,39 @@ __global__ void __launch_bounds__(kThreads, 1) tp_kernel(const __grid_constant__
     int cslot = 0, xslot = 0;
     uint32_t cph = 0, xph = 0;
     long long cissued = 0, xissued = 0;
+    auto issue_codes = [&](int t, int sl) {
+      const uint32_t cst = cst0 + cslot * kCodeStageBytes;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(cfull0 + 8 * cslot, (uint32_t)kCodeStageBytes);
+        tma_load_2d(cst, &p.tm_codes, sl * (kSliceK / 2), t * kRows, cfull0 + 8 * cslot, pol);
+        tma_load_2d(cst + kCodesBytes, &p.tm_steps, sl * kSliceGroups, t * kRows,
+                    cfull0 + 8 * cslot, pol);
+      }
+      __syncwarp();
+      ++cissued;
+      if (++cslot == kCodeStages) {
+        cslot = 0;
+        cph ^= 1u;
+      }
+    };
+    // Weights do not depend on earlier kernels (W4_FLAG_PDL's contract):
+    // the first code stages are requested before the wait.
+    long long pre = 0;
+    for (int u = u0; u < u1 && pre < kCodeStages; ++u) {
+      const int t = u - (u / p.tiles) * p.tiles;
+      for (int sl = 0; sl < slices && pre < kCodeStages; ++sl, ++pre) issue_codes(t, sl);
+    }
+    pdl_wait();
+    long long idx = 0;   // (unit, slice) pairs walked so far
     for (int u = u0; u < u1 && ok; ++u) {
       const int mt = u / p.tiles, t = u - mt * p.tiles;
       for (int sl = 0; sl < slices && ok; ++sl) {
-        if (cissued >= kCodeStages && !wait_bar(cempty0 + 8 * cslot, cph ^ 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        const uint32_t cst = cst0 + cslot * kCodeStageBytes;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(cfull0 + 8 * cslot, (uint32_t)kCodeStageBytes);
-          tma_load_2d(cst, &p.tm_codes, sl * (kSliceK / 2), t * kRows, cfull0 + 8 * cslot, pol);
-          tma_load_2d(cst + kCodesBytes, &p.tm_steps, sl * kSliceGroups, t * kRows,
-                      cfull0 + 8 * cslot, pol);
-        }
-        __syncwarp();
-        ++cissued;
-        if (++cslot == kCodeStages) {
-          cslot = 0;
-          cph ^= 1u;
+        if (idx++ >= pre) {
+          if (cissued >= kCodeStages && !wait_bar(cempty0 + 8 * cslot, cph ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          issue_codes(t, sl);
         }
         for (int g = 0; g < kSliceGroups; g += 2) {
           if (xissued >= xs && !wait_bar(xempty0 + 8 * xslot, xph ^ 1u, abort_flag)) {
